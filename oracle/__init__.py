@@ -1,0 +1,396 @@
+"""fp64 CPU oracle for head-chunked causal self-attention with packed segments.
+
+TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the benchmark's CPU-baseline leg
+may import this package.  The product path (the CUDA library and its binding) never calls it and
+shares no code with it; the only thing both sides share is the seeded input generator
+(``upipe_inputs``), which holds none of the arithmetic below.
+
+What is computed, and where it is stated:
+
+* Attention is computed per head over the whole sequence ("Road to 5 Million Tokens" podcast
+  summary, chapter on DeepSpeed Ulysses; neuro-slop.ru transcript, quiz answer on Ulysses:
+  each head is computed whole, which is why flash attention applies).  The pages never write
+  the formula; this oracle takes the textbook scaled dot product softmax(Q K^T * scale + M) V
+  with scale = 1/sqrt(Dh), the plainest reading.
+* Compute is quadratic because every element interacts with every other (podcast summary,
+  概要 "兩個瓶頸"; transcript quiz, first answer).
+* Head chunking changes only which heads run together, not the result (podcast summary,
+  章節 "分批算 heads"; transcript, quiz answer on U-Pipe).  So the oracle has no chunks: it
+  computes every head at once, which is the result the chunked method must reproduce.
+* The mask: causal, and packed sequences attend only inside their own segment; blocks with no
+  visible pair are skippable (MaxText long-context article on techmoon.xyz, paragraph on Splash
+  attention: fully masked blocks are skipped and packing needs no padding).  GQA is in the
+  supported set (same paragraph); query head h reads KV head h // (Hq / Hkv).
+* The layer: Q/K/V projections from the hidden states, attention, output projection
+  (podcast summary, Q&A chapter: UPipe concerns the layer's query, key and value matrices).
+
+All inputs are bf16 bit patterns widened exactly to float64; nothing is rounded in between.
+Matrix products use numpy's float64 matmul as a library step.  Gradients follow the chain rule
+of the same definition.
+
+parity: every function here is pinned by tests/test_oracle.py (brute-force per-row softmax,
+torch float64 autograd, central finite differences, closed forms, invariants, brute-force
+tile classification).  No function is "parity unpinned".
+"""
+from __future__ import annotations
+
+import numpy as np
+
+NEG_INF = -np.inf
+TILE = 128  # tile edge of the skip table (rows and columns)
+
+
+# ----------------------------------------------------------------------------------------------
+# helpers
+# ----------------------------------------------------------------------------------------------
+
+def bf16_bits_to_f64(u16) -> np.ndarray:
+    """Exact widening of bf16 bit patterns (uint16) to float64."""
+    u16 = np.asarray(u16, dtype=np.uint16)
+    return (u16.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def default_scale(Dh: int) -> float:
+    return 1.0 / np.sqrt(Dh)
+
+
+def visibility(seg, rows, cols, causal: bool) -> np.ndarray:
+    """vis[r, c] = (seg[rows[r]] == seg[cols[c]]) and (not causal or cols[c] <= rows[r]).
+
+    `seg` None means a single segment.  This is the mask definition; everything else uses it.
+    """
+    rows = np.asarray(rows, dtype=np.int64)
+    cols = np.asarray(cols, dtype=np.int64)
+    if seg is None:
+        vis = np.ones((rows.size, cols.size), dtype=bool)
+    else:
+        seg = np.asarray(seg)
+        vis = seg[rows][:, None] == seg[cols][None, :]
+    if causal:
+        vis &= cols[None, :] <= rows[:, None]
+    return vis
+
+
+def split_wqkv(Wqkv: np.ndarray, Hq: int, Hkv: int, Dh: int):
+    """Rows of Wqkv are [Q heads | K heads | V heads], Dh rows per head (nn.Linear layout)."""
+    Wq = Wqkv[: Hq * Dh]
+    Wk = Wqkv[Hq * Dh: (Hq + Hkv) * Dh]
+    Wv = Wqkv[(Hq + Hkv) * Dh: (Hq + 2 * Hkv) * Dh]
+    return Wq, Wk, Wv
+
+
+def heads(M: np.ndarray, H: int, Dh: int) -> np.ndarray:
+    """[S, H*Dh] -> [H, S, Dh]."""
+    S = M.shape[0]
+    return M.reshape(S, H, Dh).transpose(1, 0, 2)
+
+
+def unheads(M: np.ndarray) -> np.ndarray:
+    """[H, S, Dh] -> [S, H*Dh]."""
+    H, S, Dh = M.shape
+    return M.transpose(1, 0, 2).reshape(S, H * Dh)
+
+
+# ----------------------------------------------------------------------------------------------
+# attention, per head, over the whole sequence
+# ----------------------------------------------------------------------------------------------
+
+def attention_forward(Q, K, V, seg, causal: bool, scale: float, rows=None, row_block: int = 1024):
+    """O_h[i] = sum_j P_ij V_kv[j],  P_ij = exp(s_ij - m_i) / l_i over visible j,
+    s_ij = scale * Q_h[i] . K_kv[j],  m_i = max_j s_ij,  l_i = sum_j exp(s_ij - m_i),
+    LSE_h[i] = m_i + ln l_i  (natural log).  kv = h // (Hq / Hkv).
+
+    Q: [Hq, S, Dh]; K, V: [Hkv, S, Dh] (float64).  `rows` selects query rows (default: all);
+    rows are independent, so they are taken `row_block` at a time to bound memory.
+    A row that sees no key gets O = 0 and LSE = -inf.
+    Returns O [Hq, R, Dh], LSE [Hq, R].
+    """
+    Hq, S, Dh = Q.shape
+    Hkv = K.shape[0]
+    g = Hq // Hkv
+    rows = np.arange(S) if rows is None else np.asarray(rows, dtype=np.int64)
+    cols = np.arange(K.shape[1])
+    O = np.zeros((Hq, rows.size, Dh))
+    LSE = np.full((Hq, rows.size), NEG_INF)
+    for r0 in range(0, rows.size, row_block):
+        rr = rows[r0: r0 + row_block]
+        vis = visibility(seg, rr, cols, causal)
+        any_vis = vis.any(axis=1)
+        for h in range(Hq):
+            kv = h // g
+            s = scale * (Q[h, rr] @ K[kv].T)
+            s = np.where(vis, s, NEG_INF)
+            m = np.where(any_vis, s.max(axis=1), 0.0)
+            e = np.where(vis, np.exp(s - m[:, None]), 0.0)
+            l = e.sum(axis=1)
+            P = np.divide(e, l[:, None], out=np.zeros_like(e), where=l[:, None] > 0)
+            O[h, r0: r0 + rr.size] = P @ V[kv]
+            with np.errstate(divide="ignore"):
+                LSE[h, r0: r0 + rr.size] = np.where(any_vis, m + np.log(l), NEG_INF)
+    return O, LSE
+
+
+def attention_backward(Q, K, V, dO, seg, causal: bool, scale: float, row_block: int = 1024):
+    """Gradients of sum(dO * O) for the attention above (chain rule):
+    D_i = dO_h[i] . O_h[i];  dP_ij = dO_h[i] . V_kv[j];  dS_ij = P_ij (dP_ij - D_i);
+    dQ_h[i] = scale sum_j dS_ij K_kv[j];
+    dK_kv[j] = scale sum_{h in group(kv)} sum_i dS_ij Q_h[i];
+    dV_kv[j] = sum_{h in group(kv)} sum_i P_ij dO_h[i].
+    Returns dQ [Hq,S,Dh], dK, dV [Hkv,S,Dh].
+    """
+    Hq, S, Dh = Q.shape
+    Hkv = K.shape[0]
+    g = Hq // Hkv
+    cols = np.arange(S)
+    dQ = np.zeros_like(Q)
+    dK = np.zeros_like(K)
+    dV = np.zeros_like(V)
+    for r0 in range(0, S, row_block):
+        rr = np.arange(r0, min(S, r0 + row_block))
+        vis = visibility(seg, rr, cols, causal)
+        any_vis = vis.any(axis=1)
+        for h in range(Hq):
+            kv = h // g
+            s = scale * (Q[h, rr] @ K[kv].T)
+            s = np.where(vis, s, NEG_INF)
+            m = np.where(any_vis, s.max(axis=1), 0.0)
+            e = np.where(vis, np.exp(s - m[:, None]), 0.0)
+            l = e.sum(axis=1)
+            P = np.divide(e, l[:, None], out=np.zeros_like(e), where=l[:, None] > 0)
+            O = P @ V[kv]
+            D = (dO[h, rr] * O).sum(axis=1)
+            dP = dO[h, rr] @ V[kv].T
+            dS = P * (dP - D[:, None])
+            dQ[h, rr] = scale * (dS @ K[kv])
+            dK[kv] += scale * (dS.T @ Q[h, rr])
+            dV[kv] += P.T @ dO[h, rr]
+    return dQ, dK, dV
+
+
+# ----------------------------------------------------------------------------------------------
+# the layer: projections -> attention -> output projection
+# ----------------------------------------------------------------------------------------------
+
+def _widen(a):
+    a = np.asarray(a)
+    return bf16_bits_to_f64(a) if a.dtype == np.uint16 else a.astype(np.float64)
+
+
+def layer_forward(X, Wqkv, Wo, seg, Hq, Hkv, Dh, causal=True, scale=None, return_all=False):
+    """Y = [O_0 ... O_{Hq-1}] Wo^T with Q_h = X Wq_h^T, K_kv = X Wk_kv^T, V_kv = X Wv_kv^T.
+
+    X [S,d], Wqkv [(Hq+2Hkv)Dh, d], Wo [d, Hq Dh]: bf16 bit patterns (uint16) or floats.
+    Returns Y [S,d] and LSE [Hq,S] in float64 (and the intermediates if asked).
+    """
+    X, Wqkv, Wo = _widen(X), _widen(Wqkv), _widen(Wo)
+    scale = default_scale(Dh) if scale is None else scale
+    Wq, Wk, Wv = split_wqkv(Wqkv, Hq, Hkv, Dh)
+    Q = heads(X @ Wq.T, Hq, Dh)
+    K = heads(X @ Wk.T, Hkv, Dh)
+    V = heads(X @ Wv.T, Hkv, Dh)
+    O, LSE = attention_forward(Q, K, V, seg, causal, scale)
+    Y = unheads(O) @ Wo.T
+    if return_all:
+        return Y, LSE, dict(Q=Q, K=K, V=V, O=O)
+    return Y, LSE
+
+
+def layer_forward_rows(X_rows, X_keys, key_index, rows, Wqkv, Wo, seg, Hq, Hkv, Dh, causal=True,
+                       scale=None):
+    """Output rows `rows` of the layer, for long sequences.
+
+    X_rows [R, d] are the hidden states of the query rows; X_keys [n, d] those of the key
+    positions `key_index` (sorted), which must include every key any of the rows can see.
+    Returns Y [R, d] and LSE [Hq, R].
+    """
+    X_rows, X_keys, Wqkv, Wo = _widen(X_rows), _widen(X_keys), _widen(Wqkv), _widen(Wo)
+    scale = default_scale(Dh) if scale is None else scale
+    rows = np.asarray(rows, dtype=np.int64)
+    key_index = np.asarray(key_index, dtype=np.int64)
+    Wq, Wk, Wv = split_wqkv(Wqkv, Hq, Hkv, Dh)
+    Q = heads(X_rows @ Wq.T, Hq, Dh)
+    K = heads(X_keys @ Wk.T, Hkv, Dh)
+    V = heads(X_keys @ Wv.T, Hkv, Dh)
+    g = Hq // Hkv
+    O = np.zeros((Hq, rows.size, Dh))
+    LSE = np.full((Hq, rows.size), NEG_INF)
+    vis = visibility(seg, rows, key_index, causal) if seg is not None else (
+        (key_index[None, :] <= rows[:, None]) if causal else np.ones((rows.size, key_index.size), bool))
+    any_vis = vis.any(axis=1)
+    for h in range(Hq):
+        kv = h // g
+        s = np.where(vis, scale * (Q[h] @ K[kv].T), NEG_INF)
+        m = np.where(any_vis, s.max(axis=1), 0.0)
+        e = np.where(vis, np.exp(s - m[:, None]), 0.0)
+        l = e.sum(axis=1)
+        P = np.divide(e, l[:, None], out=np.zeros_like(e), where=l[:, None] > 0)
+        O[h] = P @ V[kv]
+        with np.errstate(divide="ignore"):
+            LSE[h] = np.where(any_vis, m + np.log(l), NEG_INF)
+    return unheads(O) @ Wo.T, LSE
+
+
+def layer_backward(X, Wqkv, Wo, seg, dY, Hq, Hkv, Dh, causal=True, scale=None, return_all=False):
+    """Gradients of sum(dY * Y) for the layer above:
+    dO = dY Wo (split per head); dWo = dY^T [O_0 ... O_{Hq-1}];
+    (dQ, dK, dV) from attention_backward; dQKV = [dQ | dK | dV] (row order of Wqkv);
+    dX = dQKV Wqkv; dWqkv = dQKV^T X.
+    Returns dX [S,d], dWqkv, dWo (float64).
+    """
+    X, Wqkv, Wo, dY = _widen(X), _widen(Wqkv), _widen(Wo), _widen(dY)
+    scale = default_scale(Dh) if scale is None else scale
+    Wq, Wk, Wv = split_wqkv(Wqkv, Hq, Hkv, Dh)
+    Q = heads(X @ Wq.T, Hq, Dh)
+    K = heads(X @ Wk.T, Hkv, Dh)
+    V = heads(X @ Wv.T, Hkv, Dh)
+    O, _ = attention_forward(Q, K, V, seg, causal, scale)
+    dOcat = dY @ Wo
+    dWo = dY.T @ unheads(O)
+    dO = heads(dOcat, Hq, Dh)
+    dQ, dK, dV = attention_backward(Q, K, V, dO, seg, causal, scale)
+    dQKV = np.concatenate([unheads(dQ), unheads(dK), unheads(dV)], axis=1)
+    dX = dQKV @ Wqkv
+    dWqkv = dQKV.T @ X
+    if return_all:
+        return dX, dWqkv, dWo, dict(dQ=dQ, dK=dK, dV=dV, dO=dO, O=O)
+    return dX, dWqkv, dWo
+
+
+# ----------------------------------------------------------------------------------------------
+# tile-skip table (Splash-style block skipping, MaxText article)
+# ----------------------------------------------------------------------------------------------
+
+EMPTY, PARTIAL, FULL = 0, 1, 2
+
+
+def tile_classes_bruteforce(S: int, seg, causal: bool, B: int = TILE) -> np.ndarray:
+    """cls[i, j] for B x B tiles by counting visible pairs element by element: EMPTY when no
+    pair is visible, FULL when every in-range pair is, PARTIAL otherwise.  Small S only."""
+    n = -(-S // B)
+    vis = visibility(seg, np.arange(S), np.arange(S), causal)
+    cls = np.zeros((n, n), dtype=np.int8)
+    for i in range(n):
+        for j in range(n):
+            blk = vis[i * B: (i + 1) * B, j * B: (j + 1) * B]
+            c = int(blk.sum())
+            cls[i, j] = EMPTY if c == 0 else (FULL if c == blk.size else PARTIAL)
+    return cls
+
+
+def _row_intervals(S: int, seg, causal: bool):
+    """For contiguous (non-decreasing) segment ids, row r sees exactly the columns
+    [lo_r, hi_r]: lo_r = first position of r's segment, hi_r = r (causal) or the segment's last
+    position.  Returns (lo, hi) as int64 arrays."""
+    r = np.arange(S, dtype=np.int64)
+    if seg is None:
+        start = np.zeros(S, dtype=np.int64)
+        end = np.full(S, S - 1, dtype=np.int64)
+    else:
+        seg = np.asarray(seg)
+        if np.any(seg[1:] < seg[:-1]):
+            raise ValueError("segment ids are not contiguous (must be non-decreasing)")
+        new = np.ones(S, dtype=bool)
+        new[1:] = seg[1:] != seg[:-1]
+        start = np.maximum.accumulate(np.where(new, r, 0))
+        last = np.ones(S, dtype=bool)
+        last[:-1] = seg[:-1] != seg[1:]
+        end = np.minimum.accumulate(np.where(last, r, S - 1)[::-1])[::-1]
+    return start, (r if causal else end)
+
+
+def tile_counts(S: int, seg, causal: bool, q_tiles=None, B: int = TILE) -> np.ndarray:
+    """count[i, j] = number of visible (row, column) pairs in tile (i, j), summed row by row
+    from the row intervals above.  `q_tiles` selects the tile rows (default: all)."""
+    lo, hi = _row_intervals(S, seg, causal)
+    n = -(-S // B)
+    q_tiles = np.arange(n) if q_tiles is None else np.asarray(q_tiles, dtype=np.int64)
+    c0 = np.arange(n, dtype=np.int64) * B
+    c1 = np.minimum(c0 + B, S)  # exclusive
+    out = np.zeros((q_tiles.size, n), dtype=np.int64)
+    for a, i in enumerate(q_tiles):
+        rr = np.arange(i * B, min(S, (i + 1) * B))
+        width = np.minimum(hi[rr, None] + 1, c1[None, :]) - np.maximum(lo[rr, None], c0[None, :])
+        out[a] = np.maximum(width, 0).sum(axis=0)
+    return out
+
+
+def tile_counts_cols(S: int, seg, causal: bool, kv_tiles, B: int = TILE) -> np.ndarray:
+    """count[i, j] for the selected kv tiles j and every q tile i (the transpose view of
+    tile_counts), from the same row intervals."""
+    lo, hi = _row_intervals(S, seg, causal)
+    n = -(-S // B)
+    kv_tiles = np.asarray(kv_tiles, dtype=np.int64)
+    starts = np.arange(n, dtype=np.int64) * B
+    out = np.zeros((kv_tiles.size, n), dtype=np.int64)
+    for a, j in enumerate(kv_tiles):
+        c0, c1 = j * B, min(S, (j + 1) * B)
+        width = np.maximum(np.minimum(hi + 1, c1) - np.maximum(lo, c0), 0)
+        out[a] = np.add.reduceat(width, starts)
+    return out
+
+
+def classes_from_counts(S: int, counts: np.ndarray, q_tiles, kv_tiles=None, B: int = TILE) -> np.ndarray:
+    """Classes of tiles (q_tiles[a], kv_tiles[b]) from their visible-pair counts[a, b]:
+    EMPTY if 0, FULL if every in-range pair is visible, PARTIAL otherwise."""
+    n = -(-S // B)
+    q_tiles = np.asarray(q_tiles, dtype=np.int64)
+    kv_tiles = np.arange(n) if kv_tiles is None else np.asarray(kv_tiles, dtype=np.int64)
+    rows_in = np.minimum((q_tiles + 1) * B, S) - q_tiles * B
+    cols_in = np.minimum((kv_tiles + 1) * B, S) - kv_tiles * B
+    full = counts == rows_in[:, None] * cols_in[None, :]
+    return np.where(counts == 0, EMPTY, np.where(full, FULL, PARTIAL)).astype(np.int8)
+
+
+def ranges_from_classes(cls_rows: np.ndarray) -> np.ndarray:
+    """Per tile row: {begin, full_begin, full_end, end} with non-empty tiles [begin, end),
+    full tiles [full_begin, full_end) and partial tiles elsewhere in [begin, end); when a row
+    has no full tile, full_begin = full_end = end.  Raises if the row is not of that shape."""
+    out = np.zeros((cls_rows.shape[0], 4), dtype=np.int32)
+    for a, c in enumerate(cls_rows):
+        ne = np.nonzero(c != EMPTY)[0]
+        fu = np.nonzero(c == FULL)[0]
+        b, e = (int(ne[0]), int(ne[-1]) + 1) if ne.size else (0, 0)
+        fb, fe = (int(fu[0]), int(fu[-1]) + 1) if fu.size else (e, e)
+        if ne.size and (ne.size != e - b or (fu.size and fu.size != fe - fb)):
+            raise ValueError("tile row is not a contiguous range")
+        out[a] = (b, fb, fe, e)
+    return out
+
+
+def tile_table(S: int, seg, causal: bool, q_tiles=None, kv_tiles=None, B: int = TILE):
+    """The skip table: q-major rows {kv_begin, kv_full_begin, kv_full_end, kv_end} for the
+    selected q tiles, kv-major rows {q_begin, q_full_begin, q_full_end, q_end} for the selected
+    kv tiles, and the totals {partial, full} when all q tiles are selected (else None)."""
+    n = -(-S // B)
+    all_q = q_tiles is None
+    q_tiles = np.arange(n) if q_tiles is None else np.asarray(q_tiles, dtype=np.int64)
+    cq = classes_from_counts(S, tile_counts(S, seg, causal, q_tiles, B), q_tiles, None, B)
+    q_rows = ranges_from_classes(cq)
+    totals = None
+    if all_q:
+        totals = np.array([(cq == PARTIAL).sum(), (cq == FULL).sum()], dtype=np.int64)
+    kv_rows = None
+    if all_q and kv_tiles is None:
+        kv_rows = ranges_from_classes(cq.T)
+    elif kv_tiles is not None:
+        kv_tiles = np.asarray(kv_tiles, dtype=np.int64)
+        counts = tile_counts_cols(S, seg, causal, kv_tiles, B)
+        ck = classes_from_counts(S, counts.T, np.arange(n), kv_tiles, B).T
+        kv_rows = ranges_from_classes(ck)
+    return q_rows, kv_rows, totals
+
+
+# ----------------------------------------------------------------------------------------------
+# brute-force row softmax (a pin for the vectorised code above)
+# ----------------------------------------------------------------------------------------------
+
+def rowsoftmax_bruteforce(scores_row, visible_row):
+    """Softmax of one row over its visible entries, one element at a time, in Python floats."""
+    import math
+    vals = [float(s) for s, v in zip(scores_row, visible_row) if v]
+    if not vals:
+        return [0.0] * len(scores_row), float("-inf")
+    m = max(vals)
+    tot = sum(math.exp(v - m) for v in vals)
+    p = [math.exp(float(s) - m) / tot if v else 0.0 for s, v in zip(scores_row, visible_row)]
+    return p, m + math.log(tot)
