@@ -1,0 +1,419 @@
+"""Benchmark of the head-chunked attention layer (forward + backward) on GB300.
+
+One step = upipe_attn_fwd + upipe_attn_bwd of the whole layer (tile table, per-chunk QKV
+projection, attention forward, output-projection accumulation; recompute, attention backward,
+input and weight gradients) on one batch of synthetic seeded inputs already resident in HBM.
+The default workload is the Llama-3.1-8B-shaped attention layer at 32,768 tokens (hidden 4096,
+32 query / 8 KV heads, head_dim 128, causal, one segment) with 8 query heads per chunk.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Multi-GPU runs are independent replicas (weak scaling): the
+layer's single-GPU share has no exchange step.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attn fwd+bwd TFLOP/s (% bf16 peak) and peak HBM GB vs heads_per_chunk"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="llama8b_32k")
+    ap.add_argument("--hpc", type=int, default=8)
+    ap.add_argument("--accum-mode", type=int, default=0)
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--sample-tokens", type=int, default=1024, help="oracle sample length (CPU legs)")
+    return ap.parse_args()
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# ----------------------------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.5)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.3)
+        self.proc.terminate()
+        self.proc.wait()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------------------------
+# CPU legs: the fp64 oracle on a bounded sample of the workload
+# ----------------------------------------------------------------------------------------------
+
+def oracle_sample(w, sample_tokens, repeats=1):
+    """Time the oracle's full forward + backward on the first `sample_tokens` tokens of the
+    workload (same hidden size, heads and mask); returns (seconds per sample, FLOPs per sample,
+    threads)."""
+    import numpy as np
+
+    import oracle as orc
+    import upipe_inputs as ui
+
+    S = min(sample_tokens, w.S)
+    X = ui.normal_bf16(S * w.d, ui.TID_X).reshape(S, w.d)
+    W = ui.normal_bf16((w.Hq + 2 * w.Hkv) * w.Dh * w.d, ui.TID_WQKV, ui.W_STD).reshape(-1, w.d)
+    Wo = ui.normal_bf16(w.d * w.Hq * w.Dh, ui.TID_WO, ui.W_STD).reshape(w.d, -1)
+    dY = ui.normal_bf16(S * w.d, ui.TID_DY).reshape(S, w.d)
+    seg = None
+    if w.seg_lengths is not None:
+        seg = w.segments()[:S]
+    sub = ui.Workload("sample", S, w.d, w.Hq, w.Hkv, w.Dh, (w.Hq,), w.causal,
+                      None if seg is None else tuple(np.bincount(seg - seg[0]).tolist()))
+    t0 = time.perf_counter()
+    for _ in range(repeats):
+        orc.layer_forward(X, W, Wo, seg, w.Hq, w.Hkv, w.Dh, w.causal)
+        orc.layer_backward(X, W, Wo, seg, dY, w.Hq, w.Hkv, w.Dh, w.causal)
+    dt = (time.perf_counter() - t0) / repeats
+    threads = None
+    try:
+        from threadpoolctl import threadpool_info
+        threads = max((i.get("num_threads", 1) for i in threadpool_info()), default=None)
+    except Exception:
+        pass
+    if threads is None:
+        threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return dt, sub.flops_fwd_bwd(), threads, S
+
+
+def run_reference(args):
+    """The reference arm: the oracle as it stands, timed on the host cores (rank 0 only)."""
+    import upipe_inputs as ui
+
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = ui.workload(args.workload)
+    for _ in range(args.warmup):
+        oracle_sample(w, args.sample_tokens)
+    times = []
+    flops = threads = S = None
+    for _ in range(args.steps):
+        dt, flops, threads, S = oracle_sample(w, args.sample_tokens)
+        times.append(dt)
+    ms = 1e3 * sum(times) / len(times)
+    value = flops / (ms * 1e-3) / 1e12
+    sample = f"oracle fp64 forward+backward on the first {S} tokens of {w.name} (same hidden size, heads, mask)"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "seq_len": w.S, "heads_per_chunk": args.hpc, "sample_tokens": S},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------------------------
+
+def attn_kernel_flops(w, nh, kernel):
+    """MMA FLOPs one launch of an attention kernel does over the visible pairs of nh heads:
+    fwd / recompute: Q K^T and P V (4 Dh per pair); dq: Q K^T, dO V^T, dS K (6 Dh);
+    dkdv: Q K^T, dO V^T, P^T dO, dS^T Q (8 Dh)."""
+    per_pair = {"fwd": 4, "recompute": 4, "dq": 6, "dkdv": 8}[kernel] * w.Dh
+    return per_pair * w.visible_pairs() * nh
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    __graft_entry__.build()
+    import long_context_attention_upipe_gb300 as up
+    import upipe_inputs as ui
+
+    w = ui.workload(args.workload)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    S, d, Hq, Hkv, Dh = w.S, w.d, w.Hq, w.Hkv, w.Dh
+
+    def fill(shape, tid, std):
+        t = torch.empty(shape, dtype=torch.bfloat16, device=dev)
+        ui.fill_device_bf16(t.data_ptr(), t.numel(), tid, std, stream=stream.cuda_stream)
+        return t
+
+    X = fill((S, d), ui.TID_X, 1.0)
+    W = fill(((Hq + 2 * Hkv) * Dh, d), ui.TID_WQKV, ui.W_STD)
+    Wo = fill((d, Hq * Dh), ui.TID_WO, ui.W_STD)
+    dY = fill((S, d), ui.TID_DY, 1.0)
+    seg = w.segments()
+    seg_t = torch.from_numpy(seg).to(dev) if seg is not None else None
+
+    def make_layer(hpc):
+        desc = up.make_desc(S, d, Hq, Hkv, Dh, hpc, w.causal, args.accum_mode)
+        layer = up.Layer(desc, device=dev)
+        Y = torch.empty_like(X)
+        lse = torch.empty(Hq, S, dtype=torch.float32, device=dev)
+        dX = torch.empty_like(X)
+        dW = torch.empty(W.shape, dtype=torch.float32, device=dev)
+        dWo = torch.empty(Wo.shape, dtype=torch.float32, device=dev)
+
+        def step():
+            up.fwd(desc, X, W, Wo, seg_t, Y, lse, layer.ws_fwd, stream)
+            up.bwd(desc, X, W, Wo, seg_t, dY, lse, dX, dW, dWo, layer.ws_bwd, stream)
+
+        return desc, layer, step, (Y, lse, dX, dW, dWo)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    def time_steps(step, n):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        e0.record(stream)
+        for _ in range(n):
+            step()
+        e1.record(stream)
+        barrier()
+        return e0.elapsed_time(e1) / n
+
+    flops = w.flops_fwd_bwd()
+    peaks, peak_kind = measured_peaks()
+
+    # ---------------- main timed run
+    torch.cuda.reset_peak_memory_stats(dev)
+    base_alloc = torch.cuda.memory_allocated(dev)
+    desc, layer, step, outs = make_layer(args.hpc)
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    ms = time_steps(step, args.steps)
+    clocks = sampler.stop()
+    peak_gb = torch.cuda.max_memory_allocated(dev) / 1e9
+    ms_all = ms
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_all = float(t.item())
+    value = flops * world / (ms_all * 1e-3) / 1e12
+
+    result = {}
+    if rank == 0:
+        # ---------------- launches of our kernels in one step
+        launches = None
+        try:
+            from torch.profiler import ProfilerActivity, profile
+            with profile(activities=[ProfilerActivity.CUDA]) as prof:
+                step()
+                torch.cuda.synchronize()
+            names = [e.name for e in prof.events() if e.device_type.name == "CUDA"]
+            ours = [n for n in names if "upipe" in n]
+            launches = len(ours) * args.steps if ours else None
+        except Exception:
+            launches = None
+
+        # ---------------- per-kernel timing of the attention kernels (same launch configuration)
+        hpc = args.hpc
+        g = Hq // Hkv
+        kvc = max(1, hpc // g)
+        n_chunks = Hq // hpc
+        cdesc = up.make_desc(S, d, hpc, kvc, Dh, hpc, w.causal)
+        q = fill((hpc, S, Dh), 10, 1.0)
+        k = fill((kvc, S, Dh), 11, 1.0)
+        v = fill((kvc, S, Dh), 12, 1.0)
+        do = fill((hpc, S, Dh), 13, 1.0)
+        o = torch.empty_like(q)
+        lse_c = torch.empty(hpc, S, dtype=torch.float32, device=dev)
+        Dt = torch.empty(hpc, S, dtype=torch.float32, device=dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        table = torch.empty(up.tile_table_bytes(cdesc), dtype=torch.uint8, device=dev)
+        up.build_tile_table(cdesc, seg_t, table, stream)
+        kernels = {
+            "fwd": lambda: up.core_fwd(cdesc, q, k, v, seg_t, table, o, lse_c, stream),
+            "recompute": lambda: up.core_recompute(cdesc, q, k, v, do, lse_c, seg_t, table, o, Dt, stream),
+            "dq": lambda: up.core_bwd_dq(cdesc, q, k, v, do, lse_c, Dt, seg_t, table, dq, stream),
+            "dkdv": lambda: up.core_bwd_dkdv(cdesc, q, k, v, do, lse_c, Dt, seg_t, table, dk, dv, stream),
+        }
+        ktimes = {}
+        for name in ("fwd", "recompute", "dq", "dkdv"):
+            f = kernels[name]
+            for _ in range(2):
+                f()
+            ktimes[name] = time_steps(f, 5)
+        shares = {n: ktimes[n] * n_chunks / ms for n in ktimes}
+        dom = max(ktimes, key=lambda n: ktimes[n] * n_chunks)
+        achieved = attn_kernel_flops(w, hpc, dom) / (ktimes[dom] * 1e-3) / 1e12
+        peak = peaks["bf16_tflops"]
+        traffic = None
+        roofline = {"bound": "tensor", "kernel": f"attention {dom}", "achieved": achieved, "peak": peak,
+                    "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
+                    "peak_kind": f"{peak_kind} bf16 burst (kernel timed alone)"}
+        kernel_ms = {n: round(t, 4) for n, t in ktimes.items()}
+
+        # ---------------- hpc sweep: speed and peak memory vs chunk size
+        sweep = []
+        if not args.no_sweep:
+            del layer
+            for h in w.hpc_sweep:
+                torch.cuda.synchronize()
+                torch.cuda.empty_cache()
+                torch.cuda.reset_peak_memory_stats(dev)
+                before = torch.cuda.memory_allocated(dev)
+                dsc, lay, stp, _ = make_layer(h)
+                stp()
+                t = time_steps(stp, 3)
+                pk = torch.cuda.max_memory_allocated(dev) / 1e9
+                sweep.append({"heads_per_chunk": h, "ms_per_step": round(t, 3),
+                              "tflops": round(flops / (t * 1e-3) / 1e12, 2), "peak_hbm_gb": round(pk, 3),
+                              "workspace_gb": round((up.workspace_bytes(dsc, 0) + up.workspace_bytes(dsc, 1)) / 1e9, 3),
+                              "inputs_outputs_gb": round(before / 1e9, 3)})
+                del lay, stp
+            desc, layer, step, outs = make_layer(args.hpc)
+
+        # ---------------- end to end through the C-ABI with host buffers
+        e2e = None
+        if not args.no_e2e:
+            hX = torch.empty(X.shape, dtype=X.dtype, pin_memory=True)
+            hW = torch.empty(W.shape, dtype=W.dtype, pin_memory=True)
+            hWo = torch.empty(Wo.shape, dtype=Wo.dtype, pin_memory=True)
+            hdY = torch.empty(dY.shape, dtype=dY.dtype, pin_memory=True)
+            for h, t in ((hX, X), (hW, W), (hWo, Wo), (hdY, dY)):
+                h.copy_(t)
+            Y, lse, dX, dW, dWo = outs
+            hdX = torch.empty(dX.shape, dtype=dX.dtype, pin_memory=True)
+            hdW = torch.empty(dW.shape, dtype=dW.dtype, pin_memory=True)
+            hdWo = torch.empty(dWo.shape, dtype=dWo.dtype, pin_memory=True)
+            dX_, dW_, dWo_ = dX, dW, dWo
+
+            def e2e_step():
+                X.copy_(hX, non_blocking=True)
+                W.copy_(hW, non_blocking=True)
+                Wo.copy_(hWo, non_blocking=True)
+                dY.copy_(hdY, non_blocking=True)
+                step()
+                hdX.copy_(dX_, non_blocking=True)
+                hdW.copy_(dW_, non_blocking=True)
+                hdWo.copy_(dWo_, non_blocking=True)
+
+            for _ in range(2):
+                e2e_step()
+            t = time_steps(e2e_step, max(3, args.steps // 2))
+            h2d = sum(x.numel() * x.element_size() for x in (hX, hW, hWo, hdY))
+            d2h = sum(x.numel() * x.element_size() for x in (hdX, hdW, hdWo))
+            e2e = {"value": flops / (t * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                   "d2h_bytes_per_step": d2h, "ms_per_step": t}
+
+        # ---------------- CPU baseline: the oracle on a bounded sample
+        cpu = None
+        if not args.no_cpu and world == 1:
+            dt, fl, threads, Ssamp = oracle_sample(w, args.sample_tokens)
+            cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                   "sample": f"oracle fp64 forward+backward on the first {Ssamp} tokens of {w.name}; "
+                             f"{dt:.2f} s for {fl / 1e12:.4f} TFLOP"}
+
+        result = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": ms_all, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "seq_len": S, "hidden": d, "n_q_heads": Hq, "n_kv_heads": Hkv,
+                       "head_dim": Dh, "heads_per_chunk": args.hpc, "causal": bool(w.causal),
+                       "accum_mode": args.accum_mode,
+                       "l2": "inputs larger than L2 (X and dY are 268 MB each); no flush",
+                       "flops_per_step": flops, "parallelism": f"replicas{world}"},
+            "tokens_per_s": S * world / (ms_all * 1e-3),
+            "pct_bf16_peak": 100.0 * (value / world) / peaks["bf16_tflops_sustained"],
+            "peak_hbm_gb": round(peak_gb, 3),
+            "roofline": roofline,
+            "kernel_ms": kernel_ms,
+            "kernel_share": {n: round(s, 3) for n, s in shares.items()},
+            "hpc_sweep": sweep,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "gpu_launches": launches,
+            "clocks": clocks,
+        }
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

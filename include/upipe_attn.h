@@ -1,0 +1,166 @@
+/*
+ * upipe_attn: head-chunked causal self-attention (forward and backward) on one GB300.
+ *
+ * The layer is  Y = concat_h softmax(Q_h K_{h/g}^T * scale + M) V_{h/g} * Wo^T  with
+ * [Q | K | V] = X * Wqkv^T, for a sequence of S tokens of hidden size d.  Its query heads are
+ * processed in chunks of `heads_per_chunk`, one chunk after another, and every chunk's Q/K/V
+ * projection, attention and output-projection accumulation run inside one caller-provided
+ * workspace that is reused from chunk to chunk, so activation memory grows with the chunk
+ * size and not with the number of heads.
+ *
+ * Sources: "Road to 5 Million Tokens" (podcast summary, chapters "主要貢獻 UPipe" and
+ * "分批算 heads": heads on one GPU run in groups, one group after another; partial results
+ * are kept and the next group reuses the buffer the previous one allocated; Q&A chapter: it
+ * concerns the layer's query, key and value matrices).  neuro-slop.ru transcript ("Как
+ * уместить 5 млн токенов...", quiz answer on U-Pipe and insight 02: one set of heads already
+ * saturates the GPU, so heads are chunked in time with one small reused buffer).  Packed
+ * sequences and skipping of fully masked tiles: MaxText long-context article (techmoon.xyz),
+ * paragraph on Splash attention.  GQA: same paragraph.
+ *
+ * Conventions for every entry point
+ *  - All tensors are row-major.  bf16 tensors are passed as uint16_t bit patterns.
+ *  - Weights follow the nn.Linear layout [out, in].  Wqkv rows are [Q heads | K heads | V heads],
+ *    head_dim rows per head; query head h uses KV head h / (n_q_heads / n_kv_heads).
+ *  - Pointers marked "device" are CUDA device addresses; every device pointer must be 16-byte
+ *    aligned.  `stream` is a cudaStream_t (NULL = the legacy default stream).
+ *  - The caller owns every buffer, including the workspace.  The library allocates no device
+ *    memory and keeps no state between calls.  Calls are stream-ordered and asynchronous;
+ *    two calls may run concurrently only with different workspaces.
+ *  - Every check that depends only on the arguments is made on the host before any launch; a
+ *    failing check returns a status and launches nothing.  Conditions only the device can see
+ *    (segment ids that are not non-decreasing) set an error word in the workspace or table,
+ *    read with upipe_attn_device_status().  No call aborts, traps or throws.
+ */
+#ifndef UPIPE_ATTN_H
+#define UPIPE_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  UPIPE_OK = 0,
+  UPIPE_ERR_INVALID_ARG = 1,             /* NULL pointer, bad size or shape                    */
+  UPIPE_ERR_UNSUPPORTED = 2,             /* valid but not supported (e.g. head_dim 96)         */
+  UPIPE_ERR_ALIGNMENT = 3,               /* a device pointer is not 16-byte aligned            */
+  UPIPE_ERR_WORKSPACE_TOO_SMALL = 4,     /* ws_bytes / table_bytes below the required size     */
+  UPIPE_ERR_SEGMENTS_NOT_CONTIGUOUS = 5, /* device-detected: segment ids decrease somewhere    */
+  UPIPE_ERR_CUDA = 6,                    /* a CUDA runtime call failed (launch error)          */
+  UPIPE_ERR_DEVICE_TIMEOUT = 7           /* a bounded device-side wait ran out                 */
+} upipe_status_t;
+
+typedef struct {
+  int64_t seq_len;         /* S: 1 .. 2^31 - 1 tokens                                          */
+  int32_t hidden;          /* d: multiple of 64                                                */
+  int32_t n_q_heads;       /* Hq                                                               */
+  int32_t n_kv_heads;      /* Hkv; Hq % Hkv == 0 (g = Hq / Hkv query heads share a KV head)     */
+  int32_t head_dim;        /* Dh: 64 or 128                                                    */
+  int32_t heads_per_chunk; /* query heads per chunk; Hq % hpc == 0 and (hpc % g == 0 or
+                              g % hpc == 0), so a chunk holds whole KV groups or part of one */
+  int32_t causal;          /* 1: key j visible to query i only if j <= i                       */
+  int32_t accum_mode;      /* 0: fp32 accumulators for Y / dX in the workspace (default);
+                              1: accumulate in place in the bf16 output (fp32 math per chunk,
+                              one bf16 rounding per chunk; smaller workspace)                  */
+  float softmax_scale;     /* 0 selects 1/sqrt(head_dim)                                       */
+} upipe_attn_desc_t;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* upipe_attn_status_string(upipe_status_t status);
+
+/* Workspace bytes needed by upipe_attn_fwd (pass = 0) or upipe_attn_bwd (pass = 1) for this
+ * descriptor.  Host-only; writes *bytes.  The size grows with heads_per_chunk (per-chunk
+ * Q/O/dO/dQ buffers and the resident K/V of one KV group), not with n_q_heads. */
+upipe_status_t upipe_attn_workspace_size(const upipe_attn_desc_t* desc, int pass, size_t* bytes);
+
+/* Bytes of the tile-skip table for seq_len S: 32-byte header + 2 * ceil(S/128) * 16. */
+upipe_status_t upipe_attn_tile_table_size(const upipe_attn_desc_t* desc, size_t* bytes);
+
+/* Tile-skip table (Splash-style skipping of fully masked blocks, MaxText article).
+ * For 128x128 tiles (query tile i, key tile j) a tile is EMPTY when no (query, key) pair in it
+ * is visible, FULL when every in-range pair is, PARTIAL otherwise; visible means
+ * seg[q] == seg[k] and (not causal or k <= q).  With non-decreasing segment ids the non-empty
+ * tiles of a row form one range with the full ones in the middle, so the table stores
+ *   header  : int64 n_partial, int64 n_full (tile pairs per head), int32 error (0 or
+ *             UPIPE_ERR_SEGMENTS_NOT_CONTIGUOUS), int32 n_tiles, int64 reserved
+ *   q-major : int32[n_tiles][4] {kv_begin, kv_full_begin, kv_full_end, kv_end}
+ *   kv-major: int32[n_tiles][4] {q_begin, q_full_begin, q_full_end, q_end}
+ * (half-open ranges of tile indices; a row with no full tile has full_begin = full_end = end).
+ * seg: device int32[S] or NULL (one segment).  table: device, table_bytes from
+ * upipe_attn_tile_table_size.  Only desc->seq_len and desc->causal are read. */
+upipe_status_t upipe_attn_build_tile_table(const upipe_attn_desc_t* desc, const int32_t* seg, void* table,
+                                           size_t table_bytes, void* stream);
+
+/* Forward pass of the layer.
+ *   X    device bf16 [S, d]                      hidden states
+ *   Wqkv device bf16 [(Hq + 2 Hkv) * Dh, d]
+ *   Wo   device bf16 [d, Hq * Dh]
+ *   seg  device int32 [S] non-decreasing segment ids, or NULL (one segment)
+ *   Y    device bf16 [S, d]                      output (written)
+ *   lse  device fp32 [Hq, S]                     natural-log softmax normaliser per query row,
+ *                                                the only state the backward pass needs
+ *   ws   device workspace of ws_bytes >= upipe_attn_workspace_size(desc, 0)
+ * Chunks run in ascending head order; the K/V of a KV group stay resident in the workspace
+ * while the chunks of that group run. */
+upipe_status_t upipe_attn_fwd(const upipe_attn_desc_t* desc, const uint16_t* X, const uint16_t* Wqkv,
+                              const uint16_t* Wo, const int32_t* seg, uint16_t* Y, float* lse, void* ws,
+                              size_t ws_bytes, void* stream);
+
+/* Backward pass: gradients of sum(dY * Y).  Activations are recomputed chunk by chunk from X
+ * and the saved lse (activation checkpointing inside the layer: podcast summary, chapter
+ * "Activation checkpointing").
+ *   dY    device bf16 [S, d]
+ *   lse   device fp32 [Hq, S] as written by upipe_attn_fwd for the same inputs
+ *   dX    device bf16 [S, d]                    (written)
+ *   dWqkv device fp32 [(Hq + 2 Hkv) * Dh, d]     (written, not accumulated)
+ *   dWo   device fp32 [d, Hq * Dh]               (written, not accumulated)
+ *   ws    device workspace of ws_bytes >= upipe_attn_workspace_size(desc, 1) */
+upipe_status_t upipe_attn_bwd(const upipe_attn_desc_t* desc, const uint16_t* X, const uint16_t* Wqkv,
+                              const uint16_t* Wo, const int32_t* seg, const uint16_t* dY, const float* lse,
+                              uint16_t* dX, float* dWqkv, float* dWo, void* ws, size_t ws_bytes,
+                              void* stream);
+
+/* Attention core alone, Q/K/V given directly (head-major), for testing the kernels in isolation.
+ *   q [Hq, S, Dh], k, v [Hkv, S, Dh] device bf16; table from upipe_attn_build_tile_table;
+ *   o [Hq, S, Dh] device bf16 (written); lse [Hq, S] device fp32 (written).
+ * heads_per_chunk and hidden are ignored. */
+upipe_status_t upipe_attn_core_fwd(const upipe_attn_desc_t* desc, const uint16_t* q, const uint16_t* k,
+                                   const uint16_t* v, const int32_t* seg, const void* table, uint16_t* o,
+                                   float* lse, void* stream);
+
+/* The three kernels of the attention backward, one launch each, in the order the layer runs
+ * them.  Arguments as in upipe_attn_core_fwd; dO [Hq, S, Dh] device bf16; lse [Hq, S] from the
+ * forward pass.
+ *   recompute: o [Hq, S, Dh] bf16 and D [Hq, S] fp32 = rowsum(dO * O), from q, k, v and lse
+ *              without online rescaling (activation recompute).
+ *   bwd_dq   : dq [Hq, S, Dh] bf16 = scale * sum_j P_ij (dP_ij - D_i) k_j,  dP = dO v^T.
+ *   bwd_dkdv : dk, dv [Hkv, S, Dh] bf16, summed over the query heads of each KV head:
+ *              dv_j = sum P_ij dO_i,  dk_j = scale * sum P_ij (dP_ij - D_i) q_i. */
+upipe_status_t upipe_attn_core_recompute(const upipe_attn_desc_t* desc, const uint16_t* q, const uint16_t* k,
+                                         const uint16_t* v, const uint16_t* dO, const float* lse, const int32_t* seg,
+                                         const void* table, uint16_t* o, float* D, void* stream);
+upipe_status_t upipe_attn_core_bwd_dq(const upipe_attn_desc_t* desc, const uint16_t* q, const uint16_t* k,
+                                      const uint16_t* v, const uint16_t* dO, const float* lse, const float* D,
+                                      const int32_t* seg, const void* table, uint16_t* dq, void* stream);
+upipe_status_t upipe_attn_core_bwd_dkdv(const upipe_attn_desc_t* desc, const uint16_t* q, const uint16_t* k,
+                                        const uint16_t* v, const uint16_t* dO, const float* lse, const float* D,
+                                        const int32_t* seg, const void* table, uint16_t* dk, uint16_t* dv,
+                                        void* stream);
+
+/* Projection GEMM alone, for testing: C[M, N] (fp32, row-major, ldc) = A[M, K] * B[N, K]^T with
+ * A, B device bf16 row-major (lda, ldb in elements). */
+upipe_status_t upipe_attn_gemm_nt(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda,
+                                  const uint16_t* B, int64_t ldb, float* C, int64_t ldc, void* stream);
+
+/* Reads the device error word of a workspace (after fwd/bwd) or of a table (after
+ * build_tile_table) into *code (a upipe_status_t value; UPIPE_OK when none).  Synchronises
+ * `stream`.  `buf` is the workspace or the table. */
+upipe_status_t upipe_attn_device_status(const void* buf, int32_t* code, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* UPIPE_ATTN_H */

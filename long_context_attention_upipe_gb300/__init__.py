@@ -1,0 +1,193 @@
+"""Python binding of the head-chunked attention library (libupipe_attn.so).
+
+Argument marshalling only: every step of the layer runs in the library's CUDA kernels.  torch
+is used for device memory and streams.  There is no fallback: if the library is missing, the
+import raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libupipe_attn.so")
+
+STATUS = {0: "UPIPE_OK", 1: "UPIPE_ERR_INVALID_ARG", 2: "UPIPE_ERR_UNSUPPORTED", 3: "UPIPE_ERR_ALIGNMENT",
+          4: "UPIPE_ERR_WORKSPACE_TOO_SMALL", 5: "UPIPE_ERR_SEGMENTS_NOT_CONTIGUOUS", 6: "UPIPE_ERR_CUDA",
+          7: "UPIPE_ERR_DEVICE_TIMEOUT"}
+UPIPE_OK = 0
+
+EXPORTS = ["upipe_attn_status_string", "upipe_attn_workspace_size", "upipe_attn_tile_table_size",
+           "upipe_attn_build_tile_table", "upipe_attn_fwd", "upipe_attn_bwd", "upipe_attn_core_fwd",
+           "upipe_attn_core_recompute", "upipe_attn_core_bwd_dq", "upipe_attn_core_bwd_dkdv", "upipe_attn_gemm_nt",
+           "upipe_attn_device_status"]
+
+
+class Desc(ctypes.Structure):
+    _fields_ = [("seq_len", ctypes.c_int64), ("hidden", ctypes.c_int32), ("n_q_heads", ctypes.c_int32),
+                ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("heads_per_chunk", ctypes.c_int32),
+                ("causal", ctypes.c_int32), ("accum_mode", ctypes.c_int32), ("softmax_scale", ctypes.c_float)]
+
+
+def make_desc(S, d, Hq, Hkv, Dh, hpc=None, causal=True, accum_mode=0, scale=0.0) -> Desc:
+    return Desc(int(S), int(d), int(Hq), int(Hkv), int(Dh), int(hpc if hpc is not None else Hq), int(bool(causal)),
+                int(accum_mode), float(scale))
+
+
+class UpipeError(RuntimeError):
+    def __init__(self, code, where):
+        super().__init__(f"{where}: {STATUS.get(code, code)}")
+        self.code = code
+
+
+_lib = None
+
+
+def lib():
+    """The loaded library.  Raises if it was not built (no fallback path exists)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"libupipe_attn.so not found at {LIB_PATH}; run __graft_entry__.build() first")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I64, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
+        D = ctypes.POINTER(Desc)
+        sig = {
+            "upipe_attn_status_string": ([ctypes.c_int], ctypes.c_char_p),
+            "upipe_attn_workspace_size": ([D, ctypes.c_int, ctypes.POINTER(SZ)], ctypes.c_int),
+            "upipe_attn_tile_table_size": ([D, ctypes.POINTER(SZ)], ctypes.c_int),
+            "upipe_attn_build_tile_table": ([D, P, P, SZ, P], ctypes.c_int),
+            "upipe_attn_fwd": ([D, P, P, P, P, P, P, P, SZ, P], ctypes.c_int),
+            "upipe_attn_bwd": ([D, P, P, P, P, P, P, P, P, P, P, SZ, P], ctypes.c_int),
+            "upipe_attn_core_fwd": ([D, P, P, P, P, P, P, P, P], ctypes.c_int),
+            "upipe_attn_core_recompute": ([D, P, P, P, P, P, P, P, P, P, P], ctypes.c_int),
+            "upipe_attn_core_bwd_dq": ([D, P, P, P, P, P, P, P, P, P, P], ctypes.c_int),
+            "upipe_attn_core_bwd_dkdv": ([D, P, P, P, P, P, P, P, P, P, P, P], ctypes.c_int),
+            "upipe_attn_gemm_nt": ([I64, I64, I64, P, I64, P, I64, P, I64, P], ctypes.c_int),
+            "upipe_attn_device_status": ([P, ctypes.POINTER(ctypes.c_int32), P], ctypes.c_int),
+        }
+        for name, (args, res) in sig.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = res
+        _lib = L
+    return _lib
+
+
+def _check(code, where):
+    if code != UPIPE_OK:
+        raise UpipeError(code, where)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _bf16(t):
+    assert t.dtype == torch.bfloat16 and t.is_contiguous(), "bf16 contiguous tensor expected"
+    return _ptr(t)
+
+
+def workspace_bytes(desc: Desc, pass_: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().upipe_attn_workspace_size(ctypes.byref(desc), pass_, ctypes.byref(n)), "workspace_size")
+    return n.value
+
+
+def tile_table_bytes(desc: Desc) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().upipe_attn_tile_table_size(ctypes.byref(desc), ctypes.byref(n)), "tile_table_size")
+    return n.value
+
+
+def build_tile_table(desc: Desc, seg, table, stream=None):
+    _check(lib().upipe_attn_build_tile_table(ctypes.byref(desc), _ptr(seg), _ptr(table), table.numel() * table.element_size(),
+                                             _stream(stream)), "build_tile_table")
+
+
+def device_status(buf, stream=None) -> int:
+    code = ctypes.c_int32(0)
+    _check(lib().upipe_attn_device_status(_ptr(buf), ctypes.byref(code), _stream(stream)), "device_status")
+    return code.value
+
+
+def fwd(desc: Desc, X, Wqkv, Wo, seg, Y, lse, ws, stream=None):
+    _check(lib().upipe_attn_fwd(ctypes.byref(desc), _bf16(X), _bf16(Wqkv), _bf16(Wo), _ptr(seg), _bf16(Y), _ptr(lse),
+                                _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)), "fwd")
+
+
+def bwd(desc: Desc, X, Wqkv, Wo, seg, dY, lse, dX, dWqkv, dWo, ws, stream=None):
+    _check(lib().upipe_attn_bwd(ctypes.byref(desc), _bf16(X), _bf16(Wqkv), _bf16(Wo), _ptr(seg), _bf16(dY), _ptr(lse),
+                                _bf16(dX), _ptr(dWqkv), _ptr(dWo), _ptr(ws), ws.numel() * ws.element_size(),
+                                _stream(stream)), "bwd")
+
+
+def core_fwd(desc: Desc, q, k, v, seg, table, o, lse, stream=None):
+    _check(lib().upipe_attn_core_fwd(ctypes.byref(desc), _bf16(q), _bf16(k), _bf16(v), _ptr(seg), _ptr(table), _bf16(o),
+                                     _ptr(lse), _stream(stream)), "core_fwd")
+
+
+def core_recompute(desc: Desc, q, k, v, dO, lse, seg, table, o, D, stream=None):
+    _check(lib().upipe_attn_core_recompute(ctypes.byref(desc), _bf16(q), _bf16(k), _bf16(v), _bf16(dO), _ptr(lse),
+                                           _ptr(seg), _ptr(table), _bf16(o), _ptr(D), _stream(stream)), "core_recompute")
+
+
+def core_bwd_dq(desc: Desc, q, k, v, dO, lse, D, seg, table, dq, stream=None):
+    _check(lib().upipe_attn_core_bwd_dq(ctypes.byref(desc), _bf16(q), _bf16(k), _bf16(v), _bf16(dO), _ptr(lse), _ptr(D),
+                                        _ptr(seg), _ptr(table), _bf16(dq), _stream(stream)), "core_bwd_dq")
+
+
+def core_bwd_dkdv(desc: Desc, q, k, v, dO, lse, D, seg, table, dk, dv, stream=None):
+    _check(lib().upipe_attn_core_bwd_dkdv(ctypes.byref(desc), _bf16(q), _bf16(k), _bf16(v), _bf16(dO), _ptr(lse),
+                                          _ptr(D), _ptr(seg), _ptr(table), _bf16(dk), _bf16(dv), _stream(stream)),
+           "core_bwd_dkdv")
+
+
+def core_bwd(desc: Desc, q, k, v, dO, lse, seg, table, dq, dk, dv, stream=None):
+    """recompute -> dq -> dkdv, with O and D in temporary torch buffers."""
+    H, S = lse.shape
+    o = torch.empty_like(q)
+    D = torch.empty(H, S, dtype=torch.float32, device=q.device)
+    core_recompute(desc, q, k, v, dO, lse, seg, table, o, D, stream)
+    core_bwd_dq(desc, q, k, v, dO, lse, D, seg, table, dq, stream)
+    core_bwd_dkdv(desc, q, k, v, dO, lse, D, seg, table, dk, dv, stream)
+    return o, D
+
+
+def gemm_nt(A, B, C, stream=None):
+    M, K = A.shape
+    N = B.shape[0]
+    _check(lib().upipe_attn_gemm_nt(M, N, K, _bf16(A), A.stride(0), _bf16(B), B.stride(0), _ptr(C), C.stride(0),
+                                    _stream(stream)), "gemm_nt")
+
+
+class Layer:
+    """Convenience wrapper: owns the workspaces for one descriptor (allocated with torch)."""
+
+    def __init__(self, desc: Desc, device="cuda"):
+        self.desc = desc
+        self.ws_fwd = torch.empty(workspace_bytes(desc, 0), dtype=torch.uint8, device=device)
+        self.ws_bwd = torch.empty(workspace_bytes(desc, 1), dtype=torch.uint8, device=device)
+
+    def forward(self, X, Wqkv, Wo, seg=None):
+        S, d = X.shape
+        Y = torch.empty_like(X)
+        lse = torch.empty(self.desc.n_q_heads, S, dtype=torch.float32, device=X.device)
+        fwd(self.desc, X, Wqkv, Wo, seg, Y, lse, self.ws_fwd)
+        return Y, lse
+
+    def backward(self, X, Wqkv, Wo, seg, dY, lse):
+        dX = torch.empty_like(X)
+        dWqkv = torch.empty(Wqkv.shape, dtype=torch.float32, device=X.device)
+        dWo = torch.empty(Wo.shape, dtype=torch.float32, device=X.device)
+        bwd(self.desc, X, Wqkv, Wo, seg, dY, lse, dX, dWqkv, dWo, self.ws_bwd)
+        return dX, dWqkv, dWo

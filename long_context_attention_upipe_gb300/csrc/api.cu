@@ -1,0 +1,533 @@
+// C-ABI entry points and the head-chunk scheduler.
+//
+// UPipe: the query heads one GPU owns are processed a chunk at a time; every chunk's Q/K/V
+// projection, attention and output-projection accumulation run in one workspace that the next
+// chunk reuses, and only the partial output sum is carried from chunk to chunk ("Road to 5
+// Million Tokens" podcast summary, chapters "主要貢獻 UPipe" and "分批算 heads"; neuro-slop.ru
+// transcript, insight 02).  The backward pass recomputes each chunk's activations from X and
+// the saved log-sum-exp (activation checkpointing, same summary, chapter "Activation
+// checkpointing"), so no per-head activation survives a chunk.
+//
+// Workspace carve-up (every region 256-byte aligned, offsets from the workspace base):
+//   table   skip table (its header holds the device error word)              both passes
+//   K, V    bf16 [kvc, S, Dh]: the KV heads of the current group, resident     both
+//           while the chunks of that group run
+//   Q, O    bf16 [hpc, S, Dh]                                                   both
+//   Yacc    f32 [S, d] partial output projection (fwd, several chunks, accum_mode 0)
+//   dO      bf16 [hpc, S, Dh]; D f32 [hpc, S]; dQ bf16 [hpc, S, Dh]             bwd
+//   dK, dV  bf16 [kvc, S, Dh]; dKacc, dVacc f32 [S, Dh] when a chunk holds only part of a
+//           KV group (hpc < g)                                                  bwd
+//   dXacc   f32 [S, d] partial input gradient (several chunks, accum_mode 0)   bwd
+//   split   f32 split-K partials of the weight-gradient GEMMs                  bwd
+#include <cmath>
+#include <cstring>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace upipe {
+
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+struct Plan {
+  int64_t S;
+  int d, Hq, Hkv, Dh, hpc, g, kvc, n_chunks, causal, accum;
+  float scale;
+  // workspace offsets
+  size_t table, k, v, q, o, yacc, dO, D, dq, dk, dv, dkacc, dvacc, dxacc, split, total;
+  int split_wo, split_wqkv_q, split_wqkv_full;
+};
+
+int num_sms() {
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+      sms = 152;
+  }
+  return sms;
+}
+
+upipe_status_t check_desc(const upipe_attn_desc_t* d) {
+  if (!d) return UPIPE_ERR_INVALID_ARG;
+  if (d->seq_len < 1 || d->seq_len > INT32_MAX) return UPIPE_ERR_INVALID_ARG;
+  if (d->hidden <= 0 || d->n_q_heads <= 0 || d->n_kv_heads <= 0 || d->heads_per_chunk <= 0) return UPIPE_ERR_INVALID_ARG;
+  if (d->n_q_heads % d->n_kv_heads != 0 || d->n_q_heads % d->heads_per_chunk != 0) return UPIPE_ERR_INVALID_ARG;
+  const int g = d->n_q_heads / d->n_kv_heads;
+  if (d->heads_per_chunk % g != 0 && g % d->heads_per_chunk != 0) return UPIPE_ERR_INVALID_ARG;
+  if (d->causal != 0 && d->causal != 1) return UPIPE_ERR_INVALID_ARG;
+  if (d->accum_mode != 0 && d->accum_mode != 1) return UPIPE_ERR_INVALID_ARG;
+  if (!(d->softmax_scale >= 0.f) || !std::isfinite(d->softmax_scale)) return UPIPE_ERR_INVALID_ARG;
+  if (d->head_dim != 64 && d->head_dim != 128) return UPIPE_ERR_UNSUPPORTED;
+  if (d->hidden % 64 != 0) return UPIPE_ERR_UNSUPPORTED;
+  const int kvc = d->heads_per_chunk >= g ? d->heads_per_chunk / g : 1;
+  if (d->heads_per_chunk + 2 * kvc > kMaxBlocks) return UPIPE_ERR_UNSUPPORTED;
+  return UPIPE_OK;
+}
+
+Plan make_plan(const upipe_attn_desc_t* desc, int pass) {
+  Plan p;
+  p.S = desc->seq_len;
+  p.d = desc->hidden;
+  p.Hq = desc->n_q_heads;
+  p.Hkv = desc->n_kv_heads;
+  p.Dh = desc->head_dim;
+  p.hpc = desc->heads_per_chunk;
+  p.g = p.Hq / p.Hkv;
+  p.kvc = p.hpc >= p.g ? p.hpc / p.g : 1;
+  p.n_chunks = p.Hq / p.hpc;
+  p.causal = desc->causal;
+  p.accum = desc->accum_mode;
+  p.scale = desc->softmax_scale > 0.f ? desc->softmax_scale : 1.0f / std::sqrt((float)p.Dh);
+  const size_t head = (size_t)p.S * p.Dh * sizeof(bf16);
+  size_t off = 0;
+  auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes); return o; };
+  p.table = take(tile_table_bytes(p.S));
+  p.k = take(p.kvc * head);
+  p.v = take(p.kvc * head);
+  p.q = take(p.hpc * head);
+  p.o = take(p.hpc * head);
+  p.yacc = p.dO = p.D = p.dq = p.dk = p.dv = p.dkacc = p.dvacc = p.dxacc = p.split = 0;
+  p.split_wo = p.split_wqkv_q = p.split_wqkv_full = 1;
+  const bool multi = p.n_chunks > 1;
+  if (pass == 0) {
+    if (multi && p.accum == 0) p.yacc = take((size_t)p.S * p.d * sizeof(float));
+  } else {
+    p.dO = take(p.hpc * head);
+    p.D = take((size_t)p.hpc * p.S * sizeof(float));
+    p.dq = take(p.hpc * head);
+    p.dk = take(p.kvc * head);
+    p.dv = take(p.kvc * head);
+    if (p.hpc < p.g) {
+      p.dkacc = take((size_t)p.S * p.Dh * sizeof(float));
+      p.dvacc = take((size_t)p.S * p.Dh * sizeof(float));
+    }
+    if (multi && p.accum == 0) p.dxacc = take((size_t)p.S * p.d * sizeof(float));
+    const int sms = num_sms();
+    p.split_wo = gemm_pick_split(p.d, (int64_t)p.hpc * p.Dh, p.S, sms);
+    p.split_wqkv_q = gemm_pick_split((int64_t)p.hpc * p.Dh, p.d, p.S, sms);
+    const int64_t full_rows = (int64_t)(p.hpc + 2 * p.kvc) * p.Dh;
+    p.split_wqkv_full = gemm_pick_split(full_rows, p.d, p.S, sms);
+    size_t sb = gemm_split_scratch_bytes(p.d, (int64_t)p.hpc * p.Dh, p.split_wo);
+    sb = std::max(sb, gemm_split_scratch_bytes((int64_t)p.hpc * p.Dh, p.d, p.split_wqkv_q));
+    sb = std::max(sb, gemm_split_scratch_bytes(full_rows, p.d, p.split_wqkv_full));
+    if (sb) p.split = take(sb);
+  }
+  p.total = off;
+  return p;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(reinterpret_cast<char*>(ws) + off);
+}
+
+#define UPIPE_CUDA(x)                          \
+  do {                                         \
+    if ((x) != cudaSuccess) return UPIPE_ERR_CUDA; \
+  } while (0)
+
+// Wqkv row of the first weight row of a head: Q heads, then K heads, then V heads.
+inline int64_t wrow_q(const Plan& p, int h) { return (int64_t)h * p.Dh; }
+inline int64_t wrow_k(const Plan& p, int kv) { return (int64_t)(p.Hq + kv) * p.Dh; }
+inline int64_t wrow_v(const Plan& p, int kv) { return (int64_t)(p.Hq + p.Hkv + kv) * p.Dh; }
+
+int log2i(int x) {
+  int s = 0;
+  while ((1 << s) < x) ++s;
+  return s;
+}
+
+// Q (and, at the start of a KV group, K and V) of chunk c:  [Q|K|V]_c = X * Wqkv_c^T
+cudaError_t project_qkv(const Plan& p, int c, bool with_kv, const bf16* X, const bf16* Wqkv, void* ws, cudaStream_t st) {
+  GemmArgs g{};
+  const int sh = log2i(p.Dh);
+  int nb = 0;
+  g.a.blk[0] = X; g.a.ld = p.d; g.a.blk_shift = -1; g.a.blk_dim = 0; g.a.k_major = 1;
+  g.b.ld = p.d; g.b.blk_shift = sh; g.b.blk_dim = 0; g.b.k_major = 1;
+  g.c.ld = p.Dh; g.c.blk_shift = sh; g.c.blk_dim = 1;
+  for (int hl = 0; hl < p.hpc; ++hl, ++nb) {
+    g.b.blk[nb] = Wqkv + wrow_q(p, c * p.hpc + hl) * p.d;
+    g.c.blk[nb] = at<bf16>(ws, p.q) + (int64_t)hl * p.S * p.Dh;
+  }
+  if (with_kv) {
+    const int kv0 = (c * p.hpc) / p.g;
+    for (int j = 0; j < p.kvc; ++j, ++nb) {
+      g.b.blk[nb] = Wqkv + wrow_k(p, kv0 + j) * p.d;
+      g.c.blk[nb] = at<bf16>(ws, p.k) + (int64_t)j * p.S * p.Dh;
+    }
+    for (int j = 0; j < p.kvc; ++j, ++nb) {
+      g.b.blk[nb] = Wqkv + wrow_v(p, kv0 + j) * p.d;
+      g.c.blk[nb] = at<bf16>(ws, p.v) + (int64_t)j * p.S * p.Dh;
+    }
+  }
+  g.M = p.S; g.N = (int64_t)nb * p.Dh; g.K = p.d;
+  g.epi = EPI_STORE_BF16;
+  return launch_gemm(g, 1, nullptr, st);
+}
+
+// Epilogue schedule of a quantity accumulated over the n_chunks chunks (Y, dX).
+int accum_epi(const Plan& p, int c, bool bf16_direct) {
+  if (p.n_chunks == 1) return EPI_STORE_BF16;
+  if (p.accum == 1) return c == 0 ? EPI_STORE_BF16 : EPI_ACC_BF16;
+  (void)bf16_direct;
+  if (c == 0) return EPI_STORE_F32;
+  return c == p.n_chunks - 1 ? EPI_ACC_F32_TO_BF16 : EPI_ACC_F32;
+}
+
+void set_accum_out(GemmOutput& o, const Plan& p, int epi, void* bf16_out, float* acc) {
+  o.blk_shift = -1; o.blk_dim = 0; o.ld = p.d;
+  o.aux = acc; o.aux_ld = p.d;
+  if (epi == EPI_STORE_F32 || epi == EPI_ACC_F32) o.blk[0] = acc;
+  else o.blk[0] = bf16_out;
+}
+
+AttnArgs attn_args(const Plan& p, int c, void* ws, const int32_t* seg, float* lse) {
+  AttnArgs a{};
+  a.q = at<bf16>(ws, p.q);
+  a.k = at<bf16>(ws, p.k);
+  a.v = at<bf16>(ws, p.v);
+  a.o = at<bf16>(ws, p.o);
+  a.lse = lse + (int64_t)c * p.hpc * p.S;
+  a.seg = seg;
+  a.q_rows = table_q_rows(at<char>(ws, p.table));
+  a.kv_rows = table_kv_rows(at<char>(ws, p.table), p.S);
+  a.S = p.S;
+  a.nh = p.hpc;
+  a.g = p.g;
+  a.causal = p.causal;
+  a.scale = p.scale;
+  return a;
+}
+
+upipe_status_t run_fwd(const Plan& p, const bf16* X, const bf16* Wqkv, const bf16* Wo, const int32_t* seg, bf16* Y,
+                       float* lse, void* ws, cudaStream_t st) {
+  UPIPE_CUDA(launch_tile_table(p.S, p.causal, seg, at<char>(ws, p.table), st));
+  const int sh = log2i(p.Dh);
+  for (int c = 0; c < p.n_chunks; ++c) {
+    const bool new_group = p.hpc >= p.g || (c * p.hpc) % p.g == 0;
+    UPIPE_CUDA(project_qkv(p, c, new_group, X, Wqkv, ws, st));
+    AttnArgs a = attn_args(p, c, ws, seg, lse);
+    UPIPE_CUDA(launch_attn_fwd(a, p.Dh, st));
+    // Y (+)= O_c * Wo_c^T
+    GemmArgs g{};
+    g.M = p.S; g.N = p.d; g.K = (int64_t)p.hpc * p.Dh;
+    for (int hl = 0; hl < p.hpc; ++hl) g.a.blk[hl] = at<bf16>(ws, p.o) + (int64_t)hl * p.S * p.Dh;
+    g.a.ld = p.Dh; g.a.blk_shift = sh; g.a.blk_dim = 1; g.a.k_major = 1;
+    g.b.blk[0] = Wo + (int64_t)c * p.hpc * p.Dh; g.b.ld = (int64_t)p.Hq * p.Dh; g.b.blk_shift = -1; g.b.k_major = 1;
+    g.epi = accum_epi(p, c, true);
+    set_accum_out(g.c, p, g.epi, Y, p.yacc ? at<float>(ws, p.yacc) : nullptr);
+    UPIPE_CUDA(launch_gemm(g, 1, nullptr, st));
+  }
+  return UPIPE_OK;
+}
+
+upipe_status_t run_bwd(const Plan& p, const bf16* X, const bf16* Wqkv, const bf16* Wo, const int32_t* seg,
+                       const bf16* dY, const float* lse, bf16* dX, float* dWqkv, float* dWo, void* ws, cudaStream_t st) {
+  UPIPE_CUDA(launch_tile_table(p.S, p.causal, seg, at<char>(ws, p.table), st));
+  const int sh = log2i(p.Dh);
+  const int64_t HD = (int64_t)p.Hq * p.Dh;
+  float* split = p.split ? at<float>(ws, p.split) : nullptr;
+  for (int c = 0; c < p.n_chunks; ++c) {
+    const bool new_group = p.hpc >= p.g || (c * p.hpc) % p.g == 0;
+    const bool end_group = p.hpc >= p.g || ((c + 1) * p.hpc) % p.g == 0;
+    const int kv0 = (c * p.hpc) / p.g;
+    UPIPE_CUDA(project_qkv(p, c, new_group, X, Wqkv, ws, st));
+    if (new_group && p.hpc < p.g) {
+      UPIPE_CUDA(launch_zero(at<char>(ws, p.dkacc), (int64_t)p.S * p.Dh * 4, st));
+      UPIPE_CUDA(launch_zero(at<char>(ws, p.dvacc), (int64_t)p.S * p.Dh * 4, st));
+    }
+    {  // dO_c = dY * Wo_c   (Wo_c: columns of Wo, read as [K = d][N = hpc Dh])
+      GemmArgs g{};
+      g.M = p.S; g.N = (int64_t)p.hpc * p.Dh; g.K = p.d;
+      g.a.blk[0] = dY; g.a.ld = p.d; g.a.blk_shift = -1; g.a.k_major = 1;
+      g.b.blk[0] = Wo + (int64_t)c * p.hpc * p.Dh; g.b.ld = HD; g.b.blk_shift = -1; g.b.k_major = 0;
+      for (int hl = 0; hl < p.hpc; ++hl) g.c.blk[hl] = at<bf16>(ws, p.dO) + (int64_t)hl * p.S * p.Dh;
+      g.c.ld = p.Dh; g.c.blk_shift = sh; g.c.blk_dim = 1;
+      g.epi = EPI_STORE_BF16;
+      UPIPE_CUDA(launch_gemm(g, 1, nullptr, st));
+    }
+    AttnArgs a = attn_args(p, c, ws, seg, const_cast<float*>(lse));
+    a.dO = at<bf16>(ws, p.dO);
+    a.D = at<float>(ws, p.D);
+    UPIPE_CUDA(launch_attn_recompute(a, p.Dh, st));
+    {  // dWo_c = dY^T * O_c   (split-K over S)
+      GemmArgs g{};
+      g.M = p.d; g.N = (int64_t)p.hpc * p.Dh; g.K = p.S;
+      g.a.blk[0] = dY; g.a.ld = p.d; g.a.blk_shift = -1; g.a.k_major = 0;
+      for (int hl = 0; hl < p.hpc; ++hl) g.b.blk[hl] = at<bf16>(ws, p.o) + (int64_t)hl * p.S * p.Dh;
+      g.b.ld = p.Dh; g.b.blk_shift = sh; g.b.blk_dim = 0; g.b.k_major = 0;
+      g.c.blk[0] = dWo + (int64_t)c * p.hpc * p.Dh; g.c.ld = HD; g.c.blk_shift = -1;
+      g.epi = EPI_STORE_F32;
+      UPIPE_CUDA(launch_gemm(g, p.split_wo, split, st));
+    }
+    AttnBwdArgs b{};
+    b.f = a;
+    b.dq = at<bf16>(ws, p.dq);
+    b.dk = at<bf16>(ws, p.dk);
+    b.dv = at<bf16>(ws, p.dv);
+    b.acc_kv = p.hpc < p.g;
+    b.dk_acc = p.dkacc ? at<float>(ws, p.dkacc) : nullptr;
+    b.dv_acc = p.dvacc ? at<float>(ws, p.dvacc) : nullptr;
+    b.nkv = p.kvc;
+    UPIPE_CUDA(launch_attn_bwd_dq(b, p.Dh, st));
+    UPIPE_CUDA(launch_attn_bwd_dkdv(b, p.Dh, st));
+    if (end_group && p.hpc < p.g) {
+      UPIPE_CUDA(launch_f32_to_bf16(at<float>(ws, p.dkacc), at<bf16>(ws, p.dk), p.S * p.Dh, 1.f, st));
+      UPIPE_CUDA(launch_f32_to_bf16(at<float>(ws, p.dvacc), at<bf16>(ws, p.dv), p.S * p.Dh, 1.f, st));
+    }
+    // blocks of dQKV_c that are final now: the chunk's dQ heads, plus dK/dV at a group end
+    const bf16* blk_act[kMaxBlocks];
+    int64_t blk_row[kMaxBlocks];
+    int nb = 0;
+    for (int hl = 0; hl < p.hpc; ++hl, ++nb) {
+      blk_act[nb] = at<bf16>(ws, p.dq) + (int64_t)hl * p.S * p.Dh;
+      blk_row[nb] = wrow_q(p, c * p.hpc + hl);
+    }
+    if (end_group) {
+      for (int j = 0; j < p.kvc; ++j, ++nb) {
+        blk_act[nb] = at<bf16>(ws, p.dk) + (int64_t)j * p.S * p.Dh;
+        blk_row[nb] = wrow_k(p, kv0 + j);
+      }
+      for (int j = 0; j < p.kvc; ++j, ++nb) {
+        blk_act[nb] = at<bf16>(ws, p.dv) + (int64_t)j * p.S * p.Dh;
+        blk_row[nb] = wrow_v(p, kv0 + j);
+      }
+    }
+    {  // dX (+)= dQKV_c * Wqkv_c
+      GemmArgs g{};
+      g.M = p.S; g.N = p.d; g.K = (int64_t)nb * p.Dh;
+      for (int i = 0; i < nb; ++i) {
+        g.a.blk[i] = blk_act[i];
+        g.b.blk[i] = Wqkv + blk_row[i] * p.d;
+      }
+      g.a.ld = p.Dh; g.a.blk_shift = sh; g.a.blk_dim = 1; g.a.k_major = 1;
+      g.b.ld = p.d; g.b.blk_shift = sh; g.b.blk_dim = 1; g.b.k_major = 0;
+      g.epi = accum_epi(p, c, true);
+      set_accum_out(g.c, p, g.epi, dX, p.dxacc ? at<float>(ws, p.dxacc) : nullptr);
+      UPIPE_CUDA(launch_gemm(g, 1, nullptr, st));
+    }
+    {  // dWqkv rows of these blocks = dQKV_block^T * X   (split-K over S)
+      GemmArgs g{};
+      g.M = (int64_t)nb * p.Dh; g.N = p.d; g.K = p.S;
+      for (int i = 0; i < nb; ++i) {
+        g.a.blk[i] = blk_act[i];
+        g.c.blk[i] = dWqkv + blk_row[i] * p.d;
+      }
+      g.a.ld = p.Dh; g.a.blk_shift = sh; g.a.blk_dim = 0; g.a.k_major = 0;
+      g.b.blk[0] = X; g.b.ld = p.d; g.b.blk_shift = -1; g.b.k_major = 0;
+      g.c.ld = p.d; g.c.blk_shift = sh; g.c.blk_dim = 0;
+      g.epi = EPI_STORE_F32;
+      const int split_k = nb == p.hpc ? p.split_wqkv_q : p.split_wqkv_full;
+      UPIPE_CUDA(launch_gemm(g, split_k, split, st));
+    }
+  }
+  return UPIPE_OK;
+}
+
+}  // namespace
+}  // namespace upipe
+
+using namespace upipe;
+
+extern "C" {
+
+const char* upipe_attn_status_string(upipe_status_t s) {
+  switch (s) {
+    case UPIPE_OK: return "ok";
+    case UPIPE_ERR_INVALID_ARG: return "invalid argument";
+    case UPIPE_ERR_UNSUPPORTED: return "unsupported configuration";
+    case UPIPE_ERR_ALIGNMENT: return "device pointer not 16-byte aligned";
+    case UPIPE_ERR_WORKSPACE_TOO_SMALL: return "workspace or table buffer too small";
+    case UPIPE_ERR_SEGMENTS_NOT_CONTIGUOUS: return "segment ids are not non-decreasing";
+    case UPIPE_ERR_CUDA: return "CUDA runtime error";
+    case UPIPE_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+  }
+  return "unknown status";
+}
+
+upipe_status_t upipe_attn_workspace_size(const upipe_attn_desc_t* desc, int pass, size_t* bytes) {
+  upipe_status_t s = check_desc(desc);
+  if (s != UPIPE_OK) return s;
+  if (!bytes || (pass != 0 && pass != 1)) return UPIPE_ERR_INVALID_ARG;
+  *bytes = make_plan(desc, pass).total;
+  return UPIPE_OK;
+}
+
+upipe_status_t upipe_attn_tile_table_size(const upipe_attn_desc_t* desc, size_t* bytes) {
+  if (!desc || !bytes || desc->seq_len < 1 || desc->seq_len > INT32_MAX) return UPIPE_ERR_INVALID_ARG;
+  *bytes = tile_table_bytes(desc->seq_len);
+  return UPIPE_OK;
+}
+
+upipe_status_t upipe_attn_build_tile_table(const upipe_attn_desc_t* desc, const int32_t* seg, void* table,
+                                           size_t table_bytes, void* stream) {
+  if (!desc || !table || desc->seq_len < 1 || desc->seq_len > INT32_MAX) return UPIPE_ERR_INVALID_ARG;
+  if (desc->causal != 0 && desc->causal != 1) return UPIPE_ERR_INVALID_ARG;
+  if (!aligned16(table) || (seg && !aligned16(seg))) return UPIPE_ERR_ALIGNMENT;
+  if (table_bytes < tile_table_bytes(desc->seq_len)) return UPIPE_ERR_WORKSPACE_TOO_SMALL;
+  if (launch_tile_table(desc->seq_len, desc->causal, seg, table, (cudaStream_t)stream) != cudaSuccess) return UPIPE_ERR_CUDA;
+  return UPIPE_OK;
+}
+
+upipe_status_t upipe_attn_fwd(const upipe_attn_desc_t* desc, const uint16_t* X, const uint16_t* Wqkv, const uint16_t* Wo,
+                              const int32_t* seg, uint16_t* Y, float* lse, void* ws, size_t ws_bytes, void* stream) {
+  upipe_status_t s = check_desc(desc);
+  if (s != UPIPE_OK) return s;
+  if (!X || !Wqkv || !Wo || !Y || !lse || !ws) return UPIPE_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(Wqkv) || !aligned16(Wo) || !aligned16(Y) || !aligned16(lse) || !aligned16(ws) ||
+      (seg && !aligned16(seg)))
+    return UPIPE_ERR_ALIGNMENT;
+  const Plan p = make_plan(desc, 0);
+  if (ws_bytes < p.total) return UPIPE_ERR_WORKSPACE_TOO_SMALL;
+  return run_fwd(p, reinterpret_cast<const bf16*>(X), reinterpret_cast<const bf16*>(Wqkv),
+                 reinterpret_cast<const bf16*>(Wo), seg, reinterpret_cast<bf16*>(Y), lse, ws, (cudaStream_t)stream);
+}
+
+upipe_status_t upipe_attn_bwd(const upipe_attn_desc_t* desc, const uint16_t* X, const uint16_t* Wqkv, const uint16_t* Wo,
+                              const int32_t* seg, const uint16_t* dY, const float* lse, uint16_t* dX, float* dWqkv,
+                              float* dWo, void* ws, size_t ws_bytes, void* stream) {
+  upipe_status_t s = check_desc(desc);
+  if (s != UPIPE_OK) return s;
+  if (!X || !Wqkv || !Wo || !dY || !lse || !dX || !dWqkv || !dWo || !ws) return UPIPE_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(Wqkv) || !aligned16(Wo) || !aligned16(dY) || !aligned16(lse) || !aligned16(dX) ||
+      !aligned16(dWqkv) || !aligned16(dWo) || !aligned16(ws) || (seg && !aligned16(seg)))
+    return UPIPE_ERR_ALIGNMENT;
+  const Plan p = make_plan(desc, 1);
+  if (ws_bytes < p.total) return UPIPE_ERR_WORKSPACE_TOO_SMALL;
+  return run_bwd(p, reinterpret_cast<const bf16*>(X), reinterpret_cast<const bf16*>(Wqkv),
+                 reinterpret_cast<const bf16*>(Wo), seg, reinterpret_cast<const bf16*>(dY), lse,
+                 reinterpret_cast<bf16*>(dX), dWqkv, dWo, ws, (cudaStream_t)stream);
+}
+
+static upipe_status_t check_core(const upipe_attn_desc_t* desc) {
+  if (!desc || desc->seq_len < 1 || desc->seq_len > INT32_MAX || desc->n_q_heads <= 0 || desc->n_kv_heads <= 0 ||
+      desc->n_q_heads % desc->n_kv_heads != 0 || (desc->causal != 0 && desc->causal != 1))
+    return UPIPE_ERR_INVALID_ARG;
+  if (desc->head_dim != 64 && desc->head_dim != 128) return UPIPE_ERR_UNSUPPORTED;
+  return UPIPE_OK;
+}
+
+static AttnArgs core_args(const upipe_attn_desc_t* desc, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                          const int32_t* seg, const void* table) {
+  AttnArgs a{};
+  a.q = reinterpret_cast<const bf16*>(q);
+  a.k = reinterpret_cast<const bf16*>(k);
+  a.v = reinterpret_cast<const bf16*>(v);
+  a.seg = seg;
+  a.q_rows = table_q_rows(table);
+  a.kv_rows = table_kv_rows(table, desc->seq_len);
+  a.S = desc->seq_len;
+  a.nh = desc->n_q_heads;
+  a.g = desc->n_q_heads / desc->n_kv_heads;
+  a.causal = desc->causal;
+  a.scale = desc->softmax_scale > 0.f ? desc->softmax_scale : 1.0f / std::sqrt((float)desc->head_dim);
+  return a;
+}
+
+upipe_status_t upipe_attn_core_fwd(const upipe_attn_desc_t* desc, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                                   const int32_t* seg, const void* table, uint16_t* o, float* lse, void* stream) {
+  upipe_status_t s = check_core(desc);
+  if (s != UPIPE_OK) return s;
+  if (!q || !k || !v || !table || !o || !lse) return UPIPE_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(table) || !aligned16(o) || !aligned16(lse))
+    return UPIPE_ERR_ALIGNMENT;
+  AttnArgs a = core_args(desc, q, k, v, seg, table);
+  a.o = reinterpret_cast<bf16*>(o);
+  a.lse = lse;
+  return launch_attn_fwd(a, desc->head_dim, (cudaStream_t)stream) == cudaSuccess ? UPIPE_OK : UPIPE_ERR_CUDA;
+}
+
+upipe_status_t upipe_attn_core_recompute(const upipe_attn_desc_t* desc, const uint16_t* q, const uint16_t* k,
+                                         const uint16_t* v, const uint16_t* dO, const float* lse, const int32_t* seg,
+                                         const void* table, uint16_t* o, float* D, void* stream) {
+  upipe_status_t s = check_core(desc);
+  if (s != UPIPE_OK) return s;
+  if (!q || !k || !v || !dO || !lse || !table || !o || !D) return UPIPE_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(lse) || !aligned16(table) ||
+      !aligned16(o) || !aligned16(D))
+    return UPIPE_ERR_ALIGNMENT;
+  AttnArgs a = core_args(desc, q, k, v, seg, table);
+  a.lse = const_cast<float*>(lse);
+  a.dO = reinterpret_cast<const bf16*>(dO);
+  a.D = D;
+  a.o = reinterpret_cast<bf16*>(o);
+  return launch_attn_recompute(a, desc->head_dim, (cudaStream_t)stream) == cudaSuccess ? UPIPE_OK : UPIPE_ERR_CUDA;
+}
+
+static upipe_status_t core_bwd_common(const upipe_attn_desc_t* desc, const uint16_t* q, const uint16_t* k,
+                                      const uint16_t* v, const uint16_t* dO, const float* lse, const float* D,
+                                      const int32_t* seg, const void* table, AttnBwdArgs* b) {
+  upipe_status_t s = check_core(desc);
+  if (s != UPIPE_OK) return s;
+  if (!q || !k || !v || !dO || !lse || !D || !table) return UPIPE_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(lse) || !aligned16(D) ||
+      !aligned16(table))
+    return UPIPE_ERR_ALIGNMENT;
+  *b = AttnBwdArgs{};
+  b->f = core_args(desc, q, k, v, seg, table);
+  b->f.lse = const_cast<float*>(lse);
+  b->f.dO = reinterpret_cast<const bf16*>(dO);
+  b->f.D = const_cast<float*>(D);
+  b->nkv = desc->n_kv_heads;
+  return UPIPE_OK;
+}
+
+upipe_status_t upipe_attn_core_bwd_dq(const upipe_attn_desc_t* desc, const uint16_t* q, const uint16_t* k,
+                                      const uint16_t* v, const uint16_t* dO, const float* lse, const float* D,
+                                      const int32_t* seg, const void* table, uint16_t* dq, void* stream) {
+  AttnBwdArgs b;
+  upipe_status_t s = core_bwd_common(desc, q, k, v, dO, lse, D, seg, table, &b);
+  if (s != UPIPE_OK) return s;
+  if (!dq) return UPIPE_ERR_INVALID_ARG;
+  if (!aligned16(dq)) return UPIPE_ERR_ALIGNMENT;
+  b.dq = reinterpret_cast<bf16*>(dq);
+  return launch_attn_bwd_dq(b, desc->head_dim, (cudaStream_t)stream) == cudaSuccess ? UPIPE_OK : UPIPE_ERR_CUDA;
+}
+
+upipe_status_t upipe_attn_core_bwd_dkdv(const upipe_attn_desc_t* desc, const uint16_t* q, const uint16_t* k,
+                                        const uint16_t* v, const uint16_t* dO, const float* lse, const float* D,
+                                        const int32_t* seg, const void* table, uint16_t* dk, uint16_t* dv,
+                                        void* stream) {
+  AttnBwdArgs b;
+  upipe_status_t s = core_bwd_common(desc, q, k, v, dO, lse, D, seg, table, &b);
+  if (s != UPIPE_OK) return s;
+  if (!dk || !dv) return UPIPE_ERR_INVALID_ARG;
+  if (!aligned16(dk) || !aligned16(dv)) return UPIPE_ERR_ALIGNMENT;
+  b.dk = reinterpret_cast<bf16*>(dk);
+  b.dv = reinterpret_cast<bf16*>(dv);
+  return launch_attn_bwd_dkdv(b, desc->head_dim, (cudaStream_t)stream) == cudaSuccess ? UPIPE_OK : UPIPE_ERR_CUDA;
+}
+
+upipe_status_t upipe_attn_gemm_nt(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda, const uint16_t* B,
+                                  int64_t ldb, float* C, int64_t ldc, void* stream) {
+  if (M <= 0 || N <= 0 || K <= 0 || !A || !B || !C || lda < K || ldb < K || ldc < N) return UPIPE_ERR_INVALID_ARG;
+  if (K % 8 || N % 8 || lda % 8 || ldb % 8 || ldc % 4) return UPIPE_ERR_UNSUPPORTED;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(C)) return UPIPE_ERR_ALIGNMENT;
+  GemmArgs g{};
+  g.M = M; g.N = N; g.K = K;
+  g.a.blk[0] = A; g.a.ld = lda; g.a.blk_shift = -1; g.a.k_major = 1;
+  g.b.blk[0] = B; g.b.ld = ldb; g.b.blk_shift = -1; g.b.k_major = 1;
+  g.c.blk[0] = C; g.c.ld = ldc; g.c.blk_shift = -1;
+  g.epi = EPI_STORE_F32;
+  return launch_gemm(g, 1, nullptr, (cudaStream_t)stream) == cudaSuccess ? UPIPE_OK : UPIPE_ERR_CUDA;
+}
+
+upipe_status_t upipe_attn_device_status(const void* buf, int32_t* code, void* stream) {
+  if (!buf || !code) return UPIPE_ERR_INVALID_ARG;
+  int32_t v = 0;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemcpyAsync(&v, reinterpret_cast<const char*>(buf) + offsetof(TableHeader, error), sizeof(v),
+                      cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return UPIPE_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return UPIPE_ERR_CUDA;
+  *code = v;
+  return UPIPE_OK;
+}
+
+}  // extern "C"

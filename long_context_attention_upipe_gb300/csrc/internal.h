@@ -1,0 +1,107 @@
+// Internal launch interfaces of the head-chunked attention library.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace upipe {
+
+// ---------------------------------------------------------------- tile-skip table
+size_t tile_table_bytes(int64_t S);
+cudaError_t launch_tile_table(int64_t S, int causal, const int32_t* seg, void* table, cudaStream_t st);
+
+inline const int4* table_q_rows(const void* table) {
+  return reinterpret_cast<const int4*>(reinterpret_cast<const char*>(table) + sizeof(TableHeader));
+}
+inline const int4* table_kv_rows(const void* table, int64_t S) {
+  return table_q_rows(table) + ceil_div(S, kTile);
+}
+
+// ---------------------------------------------------------------- projection GEMMs
+// Logical operands: A is [M, K], B is [N, K]; C[M, N] = A * B^T.  Each operand is a set of
+// row-major blocks: along one logical dimension the index is split into blocks of blk_len
+// (a power of two) with one base pointer per block (head-major activations, column slices of a
+// weight).  k_major: the K index is the contiguous one inside a block; otherwise the M/N index.
+constexpr int kMaxBlocks = 64;
+
+struct GemmOperand {
+  const void* blk[kMaxBlocks];
+  int64_t ld;      // elements between consecutive rows of a block
+  int blk_shift;   // log2(block length) along the blocked dimension; -1: unblocked
+  int blk_dim;     // 0: blocked along M (or N), 1: blocked along K
+  int k_major;
+};
+
+enum GemmEpilogue : int {
+  EPI_STORE_BF16 = 0,      // out(bf16) = acc
+  EPI_STORE_F32 = 1,       // out(f32) = acc
+  EPI_ACC_F32 = 2,         // out(f32) += acc
+  EPI_ACC_F32_TO_BF16 = 3, // out(bf16) = aux(f32) + acc
+  EPI_ACC_BF16 = 4,        // out(bf16) = out(bf16) + acc (fp32 math)
+};
+
+struct GemmOutput {
+  void* blk[kMaxBlocks];  // row-major [M][N] blocks; blocked along blk_dim (0: M, 1: N)
+  int64_t ld;
+  int blk_shift;          // -1: unblocked
+  int blk_dim;
+  const float* aux;       // EPI_ACC_F32_TO_BF16: plain row-major f32 [M][N] with ld aux_ld
+  int64_t aux_ld;
+};
+
+struct GemmArgs {
+  int64_t M, N, K;
+  GemmOperand a, b;
+  GemmOutput c;
+  int epi;
+};
+
+// C = A * B^T with the given epilogue.  split_k > 1 requires epi == EPI_STORE_F32 and a
+// scratch of split_k * M * N floats; the splits are reduced in a fixed order (deterministic).
+cudaError_t launch_gemm(const GemmArgs& args, int split_k, float* split_scratch, cudaStream_t st);
+size_t gemm_split_scratch_bytes(int64_t M, int64_t N, int split_k);
+int gemm_pick_split(int64_t M, int64_t N, int64_t K, int num_sms);
+
+// ---------------------------------------------------------------- attention core
+struct AttnArgs {
+  const bf16* q;    // [nh, S, Dh]   query heads of this launch
+  const bf16* k;    // [nkv, S, Dh]  KV heads; local query head h reads KV head h / g
+  const bf16* v;
+  bf16* o;          // [nh, S, Dh]
+  float* lse;       // [nh] rows of stride S: natural-log normaliser (written in fwd, read in bwd)
+  const bf16* dO;   // [nh, S, Dh]   (recompute mode and backward)
+  float* D;         // [nh, S]       rowsum(dO * O) (recompute mode writes, backward reads)
+  const int32_t* seg;
+  const int4* q_rows;   // q-major skip table
+  const int4* kv_rows;  // kv-major skip table
+  int64_t S;
+  int nh;           // query heads of the launch
+  int g;            // query heads per KV head (local head h -> KV head h / g)
+  int causal;
+  float scale;      // softmax scale
+};
+
+cudaError_t launch_attn_fwd(const AttnArgs& a, int head_dim, cudaStream_t st);
+// O and D from the saved lse (no online rescaling): activation recompute for the backward pass.
+cudaError_t launch_attn_recompute(const AttnArgs& a, int head_dim, cudaStream_t st);
+
+struct AttnBwdArgs {
+  AttnArgs f;       // q, k, v, dO, lse, D, seg, tables
+  bf16* dq;         // [nh, S, Dh]
+  bf16* dk;         // [nkv, S, Dh]  written when acc_kv == 0
+  bf16* dv;
+  float* dk_acc;    // [nkv, S, Dh]  f32 accumulators when acc_kv == 1 (partial KV group)
+  float* dv_acc;
+  int acc_kv;
+  int nkv;
+};
+cudaError_t launch_attn_bwd_dq(const AttnBwdArgs& a, int head_dim, cudaStream_t st);
+cudaError_t launch_attn_bwd_dkdv(const AttnBwdArgs& a, int head_dim, cudaStream_t st);
+
+// ---------------------------------------------------------------- small kernels
+cudaError_t launch_f32_to_bf16(const float* in, bf16* out, int64_t n, float mul, cudaStream_t st);
+cudaError_t launch_zero(void* p, int64_t bytes, cudaStream_t st);
+
+}  // namespace upipe

@@ -1,0 +1,48 @@
+"""Shared test helpers: seeded inputs as numpy (for the oracle) and torch (for the library)."""
+import numpy as np
+import torch
+
+import upipe_inputs as ui
+
+# Tolerances of the parity bar: outputs max-abs <= 1e-2 and relative Frobenius <= 5e-3,
+# gradients relative Frobenius <= 1e-2.
+OUT_MAX_ABS = 1e-2
+OUT_REL_FRO = 5e-3
+GRAD_REL_FRO = 1e-2
+
+
+def rel_fro(got, want):
+    got = np.asarray(got, dtype=np.float64)
+    want = np.asarray(want, dtype=np.float64)
+    den = np.linalg.norm(want)
+    return float(np.linalg.norm(got - want) / (den if den > 0 else 1.0))
+
+
+def max_abs(got, want):
+    return float(np.max(np.abs(np.asarray(got, np.float64) - np.asarray(want, np.float64)))) if np.size(want) else 0.0
+
+
+def to_f64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().double().numpy() if t.dtype == torch.bfloat16 else t.detach().cpu().double().numpy()
+
+
+def bf16_tensor(u16: np.ndarray, device="cuda") -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(u16).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+def layer_inputs(S, d, Hq, Hkv, Dh, seed=ui.SEED, dy=True):
+    """Seeded X, Wqkv, Wo (and dY) as uint16 bf16 bit patterns."""
+    X = ui.normal_bf16(S * d, ui.TID_X, 1.0, seed).reshape(S, d)
+    W = ui.normal_bf16((Hq + 2 * Hkv) * Dh * d, ui.TID_WQKV, ui.W_STD, seed).reshape((Hq + 2 * Hkv) * Dh, d)
+    Wo = ui.normal_bf16(d * Hq * Dh, ui.TID_WO, ui.W_STD, seed).reshape(d, Hq * Dh)
+    dY = ui.normal_bf16(S * d, ui.TID_DY, 1.0, seed).reshape(S, d) if dy else None
+    return X, W, Wo, dY
+
+
+def qkv_inputs(S, Hq, Hkv, Dh, seed=ui.SEED, std=1.0):
+    """Seeded head-major Q [Hq,S,Dh], K, V [Hkv,S,Dh], dO [Hq,S,Dh] as uint16 bf16 bit patterns."""
+    q = ui.normal_bf16(Hq * S * Dh, 10, std, seed).reshape(Hq, S, Dh)
+    k = ui.normal_bf16(Hkv * S * Dh, 11, std, seed).reshape(Hkv, S, Dh)
+    v = ui.normal_bf16(Hkv * S * Dh, 12, 1.0, seed).reshape(Hkv, S, Dh)
+    do = ui.normal_bf16(Hq * S * Dh, 13, 1.0, seed).reshape(Hq, S, Dh)
+    return q, k, v, do

@@ -1,0 +1,76 @@
+"""C-ABI library: loads, exports every declared symbol, and rejects bad arguments on the host
+before any launch (these calls touch no GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import long_context_attention_upipe_gb300 as up
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "upipe_attn.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(upipe_attn_\w+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from long_context_attention_upipe_gb300 import _build
+    _build.build()
+
+
+def test_every_declared_symbol_is_exported():
+    names = declared_functions()
+    assert len(names) >= 10
+    L = ctypes.CDLL(up.LIB_PATH)
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(up.EXPORTS)
+
+
+def test_status_strings():
+    for code in range(8):
+        assert up.lib().upipe_attn_status_string(code)
+
+
+def test_workspace_grows_with_chunk_not_heads():
+    sizes = [up.workspace_bytes(up.make_desc(32768, 4096, 32, 8, 128, h), 1) for h in (4, 8, 32)]
+    assert sizes[0] < sizes[1] < sizes[2]
+    # doubling the head count at a fixed chunk size leaves the workspace unchanged
+    a = up.workspace_bytes(up.make_desc(32768, 4096, 32, 8, 128, 8), 0)
+    b = up.workspace_bytes(up.make_desc(32768, 4096, 64, 16, 128, 8), 0)
+    assert a == b
+
+
+@pytest.mark.parametrize("bad", [
+    dict(S=0), dict(Hq=6, Hkv=4), dict(hpc=3), dict(Dh=96), dict(d=100), dict(causal=2), dict(accum=3),
+    dict(Hq=32, Hkv=8, hpc=6), dict(scale=-1.0)])
+def test_bad_descriptors_rejected(bad):
+    kw = dict(S=512, d=256, Hq=4, Hkv=2, Dh=64, hpc=2, causal=1, accum=0, scale=0.0)
+    kw.update(bad)
+    d = up.make_desc(kw["S"], kw["d"], kw["Hq"], kw["Hkv"], kw["Dh"], kw["hpc"], True, kw["accum"], kw["scale"])
+    d.causal = kw["causal"]
+    n = ctypes.c_size_t(0)
+    rc = up.lib().upipe_attn_workspace_size(ctypes.byref(d), 0, ctypes.byref(n))
+    assert rc in (1, 2)
+
+
+def test_fwd_host_checks_run_before_any_launch():
+    d = up.make_desc(512, 256, 4, 2, 64, 2)
+    L = up.lib()
+    fake = ctypes.c_void_p(0x10000)       # never dereferenced: the checks fail first
+    odd = ctypes.c_void_p(0x10008)
+    args = [fake] * 6
+    assert L.upipe_attn_fwd(ctypes.byref(d), None, *args[1:], fake, 1 << 40, None) == 1       # NULL X
+    assert L.upipe_attn_fwd(ctypes.byref(d), odd, fake, fake, None, fake, fake, fake, 1 << 40, None) == 3
+    assert L.upipe_attn_fwd(ctypes.byref(d), fake, fake, fake, None, fake, fake, fake, 16, None) == 4
+    assert L.upipe_attn_bwd(ctypes.byref(d), fake, fake, fake, None, fake, fake, fake, fake, fake, fake, 16, None) == 4
+    bad = up.make_desc(512, 256, 4, 2, 96, 2)
+    assert L.upipe_attn_fwd(ctypes.byref(bad), fake, fake, fake, None, fake, fake, fake, 1 << 40, None) == 2
+    t = up.make_desc(512, 256, 4, 2, 64, 2)
+    assert L.upipe_attn_build_tile_table(ctypes.byref(t), None, fake, 16, None) == 4
+    assert L.upipe_attn_build_tile_table(ctypes.byref(t), odd, fake, 1 << 20, None) == 3

@@ -1,0 +1,226 @@
+"""GPU parity: the CUDA path through the C-ABI against the fp64 oracle on the same seeded inputs.
+
+Bar: tile tables and visited counts bit-exact; outputs max-abs <= 1e-2 and relative Frobenius
+<= 5e-3; gradients relative Frobenius <= 1e-2."""
+import numpy as np
+import pytest
+import torch
+
+import long_context_attention_upipe_gb300 as up
+import oracle as orc
+import upipe_inputs as ui
+from helpers import (GRAD_REL_FRO, OUT_MAX_ABS, OUT_REL_FRO, bf16_tensor, layer_inputs, max_abs, qkv_inputs, rel_fro,
+                     to_f64)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from long_context_attention_upipe_gb300 import _build
+    _build.build()
+    ui.build(device=True)
+
+
+def gpu_table(S, seg_np, causal):
+    desc = up.make_desc(S, 64, 1, 1, 64, 1, causal)
+    table = torch.empty(up.tile_table_bytes(desc), dtype=torch.uint8, device="cuda")
+    seg = torch.from_numpy(seg_np).cuda() if seg_np is not None else None
+    up.build_tile_table(desc, seg, table)
+    torch.cuda.synchronize()
+    t = table.cpu().numpy()
+    nt = -(-S // 128)
+    head = t[:32]
+    counts = head[:16].view(np.int64)
+    err = int(head[16:20].view(np.int32)[0])
+    q_rows = t[32:32 + 16 * nt].view(np.int32).reshape(nt, 4)
+    kv_rows = t[32 + 16 * nt:32 + 32 * nt].view(np.int32).reshape(nt, 4)
+    return q_rows, kv_rows, counts, err, table
+
+
+def random_segments(S, rng, max_segs=8):
+    k = int(rng.integers(1, max_segs + 1))
+    if S < 2 or k == 1:
+        return ui.segments_from_lengths([S])
+    cuts = np.sort(rng.choice(np.arange(1, S), size=min(k - 1, S - 1), replace=False))
+    return ui.segments_from_lengths(np.diff(np.concatenate([[0], cuts, [S]])))
+
+
+# ----------------------------------------------------------------------------------------------
+# tile-skip table: bit-exact
+# ----------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("S", [1, 7, 128, 129, 300, 512, 1000, 5000, 70000])
+@pytest.mark.parametrize("causal", [True, False])
+def test_tile_table_bit_exact(S, causal):
+    rng = np.random.default_rng(S * 3 + causal)
+    for trial in range(3):
+        seg = None if trial == 0 else random_segments(S, rng, 8 if trial == 1 else 40)
+        want_q, want_kv, want_tot = orc.tile_table(S, seg, causal)
+        q, kv, counts, err, _ = gpu_table(S, seg, causal)
+        assert err == 0
+        np.testing.assert_array_equal(q, want_q)
+        np.testing.assert_array_equal(kv, want_kv)
+        np.testing.assert_array_equal(counts, want_tot)
+
+
+def test_tile_table_packed_131k():
+    w = ui.workload("packed_131k")
+    seg = w.segments()
+    want_q, want_kv, want_tot = orc.tile_table(w.S, seg, True)
+    q, kv, counts, err, _ = gpu_table(w.S, seg, True)
+    assert err == 0
+    np.testing.assert_array_equal(q, want_q)
+    np.testing.assert_array_equal(kv, want_kv)
+    np.testing.assert_array_equal(counts, want_tot)
+
+
+def test_tile_table_5m_sampled_and_closed_form():
+    S = 5_000_000
+    n = -(-S // 128)
+    q, kv, counts, err, _ = gpu_table(S, None, True)
+    assert err == 0
+    assert counts.tolist() == [n, n * (n - 1) // 2]  # diagonal partial, the rest of the triangle full
+    sel = np.array([0, 1, 2, 777, n // 2, n - 2, n - 1])
+    want_q, want_kv, _ = orc.tile_table(S, None, True, q_tiles=sel, kv_tiles=sel)
+    np.testing.assert_array_equal(q[sel], want_q)
+    np.testing.assert_array_equal(kv[sel], want_kv)
+
+
+def test_tile_table_rejects_unsorted_segments():
+    seg = np.array([0] * 100 + [1] * 100 + [0] * 56, dtype=np.int32)
+    *_, err, table = gpu_table(256, seg, True)
+    assert err == 5
+    assert up.device_status(table) == 5
+
+
+# ----------------------------------------------------------------------------------------------
+# GEMM alone
+# ----------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("M,N,K", [(1, 8, 8), (300, 128, 64), (1000, 384, 256), (4096, 1024, 4096)])
+def test_gemm_nt_matches_fp64(M, N, K):
+    A = ui.normal_bf16(M * K, 20).reshape(M, K)
+    B = ui.normal_bf16(N * K, 21, 0.05).reshape(N, K)
+    C = torch.empty(M, N, dtype=torch.float32, device="cuda")
+    up.gemm_nt(bf16_tensor(A), bf16_tensor(B), C)
+    torch.cuda.synchronize()
+    want = ui.bf16_to_f64(A) @ ui.bf16_to_f64(B).T
+    got = C.cpu().double().numpy()
+    assert rel_fro(got, want) < 1e-5
+    assert max_abs(got, want) < 1e-3 * max(1.0, np.abs(want).max())
+
+
+# ----------------------------------------------------------------------------------------------
+# attention core alone (Q, K, V given directly)
+# ----------------------------------------------------------------------------------------------
+
+CORE_CASES = [
+    # S, Hq, Hkv, Dh, segment lengths, causal
+    (1, 1, 1, 64, None, True),
+    (300, 4, 2, 64, [100, 200], True),
+    (700, 2, 1, 128, [300, 1, 399], True),
+    (512, 4, 4, 128, None, False),
+    (1000, 4, 1, 128, [129, 500, 371], False),
+    (2048, 2, 1, 128, None, True),
+]
+
+
+def run_core(S, Hq, Hkv, Dh, segs, causal):
+    q, k, v, do = qkv_inputs(S, Hq, Hkv, Dh)
+    seg = ui.segments_from_lengths(segs) if segs else None
+    desc = up.make_desc(S, 64, Hq, Hkv, Dh, Hq, causal)
+    table = torch.empty(up.tile_table_bytes(desc), dtype=torch.uint8, device="cuda")
+    seg_t = torch.from_numpy(seg).cuda() if seg is not None else None
+    up.build_tile_table(desc, seg_t, table)
+    qt, kt, vt, dot = (bf16_tensor(x) for x in (q, k, v, do))
+    o = torch.empty_like(qt)
+    lse = torch.empty(Hq, S, dtype=torch.float32, device="cuda")
+    up.core_fwd(desc, qt, kt, vt, seg_t, table, o, lse)
+    dq, dk, dv = torch.empty_like(qt), torch.empty_like(kt), torch.empty_like(vt)
+    up.core_bwd(desc, qt, kt, vt, dot, lse, seg_t, table, dq, dk, dv)
+    torch.cuda.synchronize()
+    return (q, k, v, do, seg), (to_f64(o), to_f64(lse), to_f64(dq), to_f64(dk), to_f64(dv))
+
+
+@pytest.mark.parametrize("case", CORE_CASES)
+def test_core_fwd_bwd_match_oracle(case):
+    S, Hq, Hkv, Dh, segs, causal = case
+    (q, k, v, do, seg), (o, lse, dq, dk, dv) = run_core(*case)
+    Q, K, V, dO = (ui.bf16_to_f64(x) for x in (q, k, v, do))
+    scale = orc.default_scale(Dh)
+    O_ref, L_ref = orc.attention_forward(Q, K, V, seg, causal, scale)
+    assert max_abs(o, O_ref) <= OUT_MAX_ABS
+    assert rel_fro(o, O_ref) <= OUT_REL_FRO
+    assert max_abs(lse, L_ref) <= 1e-3
+    dQ, dK, dV = orc.attention_backward(Q, K, V, dO, seg, causal, scale)
+    assert rel_fro(dq, dQ) <= GRAD_REL_FRO, rel_fro(dq, dQ)
+    assert rel_fro(dk, dK) <= GRAD_REL_FRO, rel_fro(dk, dK)
+    assert rel_fro(dv, dV) <= GRAD_REL_FRO, rel_fro(dv, dV)
+
+
+# ----------------------------------------------------------------------------------------------
+# the whole layer, chunked
+# ----------------------------------------------------------------------------------------------
+
+LAYER_CASES = [
+    # S, d, Hq, Hkv, Dh, segment lengths, causal, hpc, accum_mode
+    (512, 256, 4, 2, 64, [300, 212], True, 2, 0),   # the tiny workload
+    (512, 256, 4, 2, 64, [300, 212], True, 1, 0),
+    (512, 256, 4, 2, 64, [300, 212], True, 4, 0),
+    (512, 256, 4, 2, 64, [300, 212], True, 1, 1),
+    (300, 128, 4, 1, 128, None, True, 1, 0),        # partial KV groups, ragged S
+    (300, 128, 4, 1, 128, None, False, 2, 0),
+    (1000, 256, 8, 2, 128, [250, 1, 600, 149], True, 4, 0),
+    (1000, 256, 8, 2, 128, [250, 1, 600, 149], True, 8, 1),
+]
+
+
+@pytest.mark.parametrize("case", LAYER_CASES)
+def test_layer_fwd_bwd_match_oracle(case):
+    S, d, Hq, Hkv, Dh, segs, causal, hpc, accum = case
+    X, W, Wo, dY = layer_inputs(S, d, Hq, Hkv, Dh)
+    seg = ui.segments_from_lengths(segs) if segs else None
+    desc = up.make_desc(S, d, Hq, Hkv, Dh, hpc, causal, accum)
+    layer = up.Layer(desc)
+    Xt, Wt, Wot, dYt = (bf16_tensor(x) for x in (X, W, Wo, dY))
+    seg_t = torch.from_numpy(seg).cuda() if seg is not None else None
+    Y, lse = layer.forward(Xt, Wt, Wot, seg_t)
+    dX, dW, dWo = layer.backward(Xt, Wt, Wot, seg_t, dYt, lse)
+    torch.cuda.synchronize()
+    assert up.device_status(layer.ws_fwd) == 0 and up.device_status(layer.ws_bwd) == 0
+    Y_ref, L_ref = orc.layer_forward(X, W, Wo, seg, Hq, Hkv, Dh, causal)
+    dX_ref, dW_ref, dWo_ref = orc.layer_backward(X, W, Wo, seg, dY, Hq, Hkv, Dh, causal)
+    y = to_f64(Y)
+    assert max_abs(y, Y_ref) <= OUT_MAX_ABS
+    assert rel_fro(y, Y_ref) <= OUT_REL_FRO, rel_fro(y, Y_ref)
+    assert max_abs(to_f64(lse), L_ref) <= 1e-3
+    assert rel_fro(to_f64(dX), dX_ref) <= GRAD_REL_FRO, rel_fro(to_f64(dX), dX_ref)
+    assert rel_fro(to_f64(dW), dW_ref) <= GRAD_REL_FRO, rel_fro(to_f64(dW), dW_ref)
+    assert rel_fro(to_f64(dWo), dWo_ref) <= GRAD_REL_FRO, rel_fro(to_f64(dWo), dWo_ref)
+
+
+def test_layer_output_independent_of_chunking():
+    S, d, Hq, Hkv, Dh = 640, 256, 8, 2, 64
+    X, W, Wo, dY = layer_inputs(S, d, Hq, Hkv, Dh)
+    Xt, Wt, Wot, dYt = (bf16_tensor(x) for x in (X, W, Wo, dY))
+    outs = []
+    for hpc in (1, 2, 4, 8):
+        layer = up.Layer(up.make_desc(S, d, Hq, Hkv, Dh, hpc, True))
+        Y, lse = layer.forward(Xt, Wt, Wot)
+        dX, dW, dWo = layer.backward(Xt, Wt, Wot, None, dYt, lse)
+        outs.append([to_f64(t) for t in (Y, lse, dX, dW, dWo)])
+    for o in outs[1:]:
+        assert rel_fro(o[0], outs[0][0]) <= OUT_REL_FRO
+        assert max_abs(o[1], outs[0][1]) <= 1e-4
+        for i in (2, 3, 4):
+            assert rel_fro(o[i], outs[0][i]) <= GRAD_REL_FRO
+
+
+def test_layer_flags_unsorted_segments():
+    S, d, Hq, Hkv, Dh = 256, 128, 2, 1, 64
+    X, W, Wo, _ = layer_inputs(S, d, Hq, Hkv, Dh, dy=False)
+    seg = np.array([0] * 100 + [2] * 100 + [1] * 56, dtype=np.int32)
+    layer = up.Layer(up.make_desc(S, d, Hq, Hkv, Dh, 1, True))
+    layer.forward(bf16_tensor(X), bf16_tensor(W), bf16_tensor(Wo), torch.from_numpy(seg).cuda())
+    assert up.device_status(layer.ws_fwd) == 5
