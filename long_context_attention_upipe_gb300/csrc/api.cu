@@ -199,9 +199,11 @@ AttnArgs attn_args(const Plan& p, int c, void* ws, const int32_t* seg, float* ls
   a.kv_rows = table_kv_rows(at<char>(ws, p.table), p.S);
   a.S = p.S;
   a.nh = p.hpc;
+  a.nkv = p.kvc;
   a.g = p.g;
   a.causal = p.causal;
   a.scale = p.scale;
+  a.err = &at<TableHeader>(ws, p.table)->error;
   return a;
 }
 
@@ -424,9 +426,11 @@ static AttnArgs core_args(const upipe_attn_desc_t* desc, const uint16_t* q, cons
   a.kv_rows = table_kv_rows(table, desc->seq_len);
   a.S = desc->seq_len;
   a.nh = desc->n_q_heads;
+  a.nkv = desc->n_kv_heads;
   a.g = desc->n_q_heads / desc->n_kv_heads;
   a.causal = desc->causal;
   a.scale = desc->softmax_scale > 0.f ? desc->softmax_scale : 1.0f / std::sqrt((float)desc->head_dim);
+  a.err = reinterpret_cast<int*>(reinterpret_cast<char*>(const_cast<void*>(table)) + offsetof(TableHeader, error));
   return a;
 }
 

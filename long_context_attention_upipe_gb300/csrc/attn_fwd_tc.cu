@@ -1,0 +1,356 @@
+// Flash-style attention forward on the 5th-generation tensor cores (tcgen05, TMEM, TMA).
+//
+// Per head, softmax(Q K^T * scale + M) V over the whole sequence with online softmax (podcast
+// summary "Road to 5 Million Tokens", chapter on DeepSpeed Ulysses: each GPU computes whole
+// heads, so flash attention applies).  Key tiles come from the skip table (MaxText article,
+// Splash attention paragraph): tiles outside a query tile's range are never loaded, full tiles
+// run unmasked, partial tiles and the ragged last tile apply the causal / segment mask.
+//
+// One CTA = one head x two 128-row query tiles (a, b), 12 warps:
+//   warp 0     TMA producer: Q_a, Q_b once, then K/V tiles through a 2-stage ring
+//   warp 1     MMA issuer (one thread) and TMEM owner: S_t = Q_t K^T (both operands in shared
+//              memory), O_t += P_t V (P_t read from TMEM, V from shared memory)
+//   warps 4-7  softmax of tile a, warps 8-11 softmax of tile b: each thread owns one query row
+//              (one TMEM lane): row max, exp2, row sum, P written back over S as bf16
+// TMEM columns: S/P_a [0,128) S/P_b [128,256) O_a [256,256+Dh) O_b [256+Dh, 256+2Dh).
+// While one softmax group works, the tensor core runs the other tile's P V and next Q K^T.
+// The running max is rescaled lazily: O is corrected only when the row max grows by more than
+// 2^8 (in exp2 units), which keeps every P <= 256 and the final O / l exact in fp32.
+//
+// MODE 1 (activation recompute for the backward pass): P = exp2(S*scale*log2e - lse*log2e)
+// from the saved log-sum-exp, no rescaling; the epilogue also writes D = rowsum(dO * O).
+#include "internal.h"
+#include "tc_common.cuh"
+
+namespace upipe {
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr int kFwdThreads = 384;
+constexpr uint32_t kBoxBytes = 128 * 128;  // one TMA box: 128 rows x 64 bf16 (128 B, swizzled)
+
+template <int DH>
+struct FwdLayout {
+  static constexpr uint32_t TB = 128 * DH * 2;  // one 128-row tile of Q, K or V
+  static constexpr uint32_t Q = 0, K = 2 * TB, V = 4 * TB, BAR = 6 * TB;
+  static constexpr uint32_t SEG = BAR + 256;             // int32 [2][128]
+  static constexpr uint32_t BYTES = SEG + 2 * 128 * 4;   // + 1024 alignment slack at launch
+  __device__ static constexpr uint32_t s_col(int t) { return t * 128; }
+  __device__ static constexpr uint32_t o_col(int t) { return 256 + t * DH; }
+  static constexpr uint32_t TMEM_COLS = 512;
+};
+
+__device__ __forceinline__ bool in_range(const int4& r, int j) { return j >= r.x && j < r.w; }
+
+template <int DH, int MODE>
+__global__ void __launch_bounds__(kFwdThreads, 1)
+    k_attn_fwd_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                  const __grid_constant__ CUtensorMap tv, AttnArgs a) {
+  using L = FwdLayout<DH>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR);
+  uint64_t* q_full = bars + 0;
+  uint64_t* kv_full = bars + 1;   // [2]
+  uint64_t* kv_empty = bars + 3;  // [2]
+  uint64_t* s_full = bars + 5;    // [2] per query tile
+  uint64_t* p_full = bars + 7;    // [2]
+  uint64_t* o_full = bars + 9;    // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 11);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 12);
+  int32_t* seg_buf = reinterpret_cast<int32_t*>(smem + L::SEG);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t S = a.S;
+  const int nt = (int)ceil_div(S, kTile);
+  const int pair = gridDim.x - 1 - blockIdx.x;  // longest query tiles first
+  const int h = blockIdx.y;
+  const int kvh = h / a.g;
+  int qt[2] = {2 * pair, 2 * pair + 1};
+  bool valid[2] = {qt[0] < nt, qt[1] < nt};
+  int4 rng[2];
+  rng[0] = valid[0] ? a.q_rows[qt[0]] : make_int4(0, 0, 0, 0);
+  rng[1] = valid[1] ? a.q_rows[qt[1]] : make_int4(0, 0, 0, 0);
+  const int j0 = valid[1] ? min(rng[0].x, rng[1].x) : rng[0].x;
+  const int j1 = valid[1] ? max(rng[0].w, rng[1].w) : rng[0].w;
+
+  if (threadIdx.x == 0) {
+    tc::mbar_init(q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&kv_full[i], 1);
+      tc::mbar_init(&kv_empty[i], 1);
+      tc::mbar_init(&s_full[i], 1);
+      tc::mbar_init(&p_full[i], 128);
+      tc::mbar_init(&o_full[i], 1);
+    }
+    *abort_flag = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tmem_slot, L::TMEM_COLS);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tc::prefetch_tmap(&tq);
+      tc::prefetch_tmap(&tk);
+      tc::prefetch_tmap(&tv);
+      uint32_t qbytes = 0;
+      for (int t = 0; t < 2; ++t) qbytes += valid[t] ? L::TB : 0;
+      tc::mbar_arrive_expect_tx(q_full, qbytes);
+      for (int t = 0; t < 2; ++t)
+        if (valid[t])
+          for (int at = 0; at < DH / 64; ++at)
+            tc::tma_load_3d(smem + L::Q + t * L::TB + at * kBoxBytes, &tq, q_full, at * 64, qt[t] * kTile, h);
+      for (int j = j0, n = 0; j < j1; ++j, ++n) {
+        const int s = n & 1;
+        if (n >= 2 && !tc::mbar_wait(&kv_empty[s], ((n >> 1) - 1) & 1, abort_flag, a.err)) break;
+        tc::mbar_arrive_expect_tx(&kv_full[s], 2 * L::TB);
+        for (int at = 0; at < DH / 64; ++at) {
+          tc::tma_load_3d(smem + L::K + s * L::TB + at * kBoxBytes, &tk, &kv_full[s], at * 64, j * kTile, kvh);
+          tc::tma_load_3d(smem + L::V + s * L::TB + at * kBoxBytes, &tv, &kv_full[s], at * 64, j * kTile, kvh);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdS = tc::idesc_bf16(128, 128, false, false);
+      constexpr uint32_t kIdO = tc::idesc_bf16(128, DH, false, true);
+      const uint32_t sQ = smem_u32(smem + L::Q), sK = smem_u32(smem + L::K), sV = smem_u32(smem + L::V);
+      bool ok = tc::mbar_wait(q_full, 0, abort_flag, a.err);
+      int waited = -1;
+      auto wait_kv = [&](int n) {
+        while (ok && waited < n) {
+          ++waited;
+          ok = tc::mbar_wait(&kv_full[waited & 1], (waited >> 1) & 1, abort_flag, a.err);
+        }
+        tc::fence_after_sync();
+      };
+      auto issue_s = [&](int t, int n) {
+        const uint32_t kb = sK + (n & 1) * L::TB;
+        const uint32_t qb = sQ + t * L::TB;
+#pragma unroll
+        for (int k = 0; k < DH / 16; ++k) {
+          const uint32_t off = (k >> 2) * kBoxBytes + (k & 3) * 32;
+          tc::mma_ss(tmem + L::s_col(t), tc::sdesc_sw128(qb + off, 16, 1024), tc::sdesc_sw128(kb + off, 16, 1024),
+                     kIdS, k > 0);
+        }
+        tc::mma_commit(&s_full[t]);
+      };
+      auto issue_pv = [&](int t, int n, bool first) {
+        const uint32_t vb = sV + (n & 1) * L::TB;
+#pragma unroll
+        for (int k = 0; k < 128 / 16; ++k)
+          tc::mma_ts(tmem + L::o_col(t), tmem + L::s_col(t) + k * 8, tc::sdesc_sw128(vb + k * 2048, kBoxBytes, 1024),
+                     kIdO, (!first) || k > 0);
+      };
+      int cnt_p[2] = {0, 0};
+      bool first_pv[2] = {true, true};
+      if (ok) {
+        wait_kv(0);
+        for (int t = 0; t < 2; ++t)
+          if (ok && in_range(rng[t], j0)) issue_s(t, 0);
+      }
+      for (int j = j0, n = 0; ok && j < j1; ++j, ++n) {
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (in_range(rng[t], j)) {
+            ok = tc::mbar_wait(&p_full[t], cnt_p[t] & 1, abort_flag, a.err);
+            if (!ok) break;
+            ++cnt_p[t];
+            tc::fence_after_sync();
+            issue_pv(t, n, first_pv[t]);
+            first_pv[t] = false;
+            if (j == rng[t].w - 1) tc::mma_commit(&o_full[t]);
+          }
+          if (in_range(rng[t], j + 1)) {
+            wait_kv(n + 1);
+            if (ok) issue_s(t, n + 1);
+          }
+        }
+        if (ok) tc::mma_commit(&kv_empty[n & 1]);
+      }
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------------ softmax groups
+    const int t = (warp - 4) >> 2;
+    const int r = threadIdx.x - 128 * (1 + t);  // row within the tile == TMEM lane
+    if (valid[t]) {
+      const int64_t row = (int64_t)qt[t] * kTile + r;
+      const bool row_ok = row < S;
+      const int32_t seg_row = (a.seg && row_ok) ? a.seg[row] : 0;
+      const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+      const float c = a.scale * kLog2e;
+      const bool ragged = (S % kTile) != 0;
+      float m_used = -INFINITY, l = 0.f;
+      if (MODE == 1) m_used = row_ok ? a.lse[(int64_t)h * S + row] * kLog2e : 0.f;
+      int32_t* sb = seg_buf + t * 128;
+      bool ok = true;
+      int cnt = 0;
+      for (int j = rng[t].x; j < rng[t].w; ++j, ++cnt) {
+        const bool partial = j < rng[t].y || j >= rng[t].z || (ragged && j == nt - 1);
+        if (partial && a.seg) {
+          const int64_t col = (int64_t)j * kTile + r;
+          tc::named_bar_sync(1 + t, 128);
+          sb[r] = col < S ? a.seg[col] : 0;
+          tc::named_bar_sync(1 + t, 128);
+        }
+        ok = tc::mbar_wait(&s_full[t], cnt & 1, abort_flag, a.err);
+        if (!ok) break;
+        tc::fence_after_sync();
+        const int64_t col0 = (int64_t)j * kTile;
+        // scaled score of column k (log2 units), -inf where masked
+        auto score = [&](uint32_t bits, int k) {
+          float v = __uint_as_float(bits) * c;
+          if (partial) {
+            const int64_t col = col0 + k;
+            const bool vis = row_ok && col < S && (!a.causal || col <= row) && (!a.seg || sb[k] == seg_row);
+            if (!vis) v = -INFINITY;
+          }
+          return v;
+        };
+        float mu;
+        if (MODE == 0) {
+          // pass 1 over the row of S: its maximum
+          float mx = m_used;
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            uint32_t v[32];
+            tc::tmem_ld32(lane_addr + L::s_col(t) + ch * 32, v);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) mx = fmaxf(mx, score(v[i], ch * 32 + i));
+          }
+          const bool need = mx > m_used + 8.f;
+          const bool rescale_o = need && cnt > 0 && m_used != -INFINITY;
+          if (__any_sync(0xffffffffu, rescale_o)) {
+            const float f = rescale_o ? fast_exp2(m_used - mx) : 1.f;
+#pragma unroll
+            for (int ch = 0; ch < DH / 32; ++ch) {
+              uint32_t v[32];
+              tc::tmem_ld32(lane_addr + L::o_col(t) + ch * 32, v);
+              tc::tmem_ld_wait();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * f);
+              tc::tmem_st32(lane_addr + L::o_col(t) + ch * 32, v);
+            }
+            tc::tmem_st_wait();
+            l *= f;
+          }
+          if (need) m_used = mx;
+          mu = m_used == -INFINITY ? 0.f : m_used;
+        } else {
+          mu = m_used;
+        }
+        // pass 2: P = exp2(score - mu) as bf16 pairs over the first 64 columns of S.  Half h
+        // reads S columns [64h, 64h + 64) and writes P columns [32h, 32h + 32), which this
+        // thread has already read.
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int sub = 0; sub < 2; ++sub) {
+            const int ch = hf * 2 + sub;
+            uint32_t v[32];
+            tc::tmem_ld32(lane_addr + L::s_col(t) + ch * 32, v);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float p0 = fast_exp2(score(v[2 * i], ch * 32 + 2 * i) - mu);
+              const float p1 = fast_exp2(score(v[2 * i + 1], ch * 32 + 2 * i + 1) - mu);
+              l += p0 + p1;
+              pk[sub * 16 + i] = tc::pack_bf16x2(p0, p1);
+            }
+          }
+          tc::tmem_st32(lane_addr + L::s_col(t) + hf * 32, pk);
+        }
+        tc::tmem_st_wait();
+        tc::fence_before_sync();
+        tc::mbar_arrive(&p_full[t]);
+      }
+      if (ok && rng[t].w > rng[t].x) ok = tc::mbar_wait(&o_full[t], 0, abort_flag, a.err);
+      tc::fence_after_sync();
+      // epilogue: O / l -> bf16 row; lse or D
+      const float inv = (MODE == 0) ? (l > 0.f ? 1.f / l : 0.f) : 1.f;
+      bf16* orow = a.o + ((int64_t)h * S + (row_ok ? row : 0)) * DH;
+      const bf16* dorow = (MODE == 1) ? a.dO + ((int64_t)h * S + (row_ok ? row : 0)) * DH : nullptr;
+      float dsum = 0.f;
+#pragma unroll
+      for (int ch = 0; ch < DH / 32; ++ch) {
+        uint32_t v[32];
+        tc::tmem_ld32(lane_addr + L::o_col(t) + ch * 32, v);
+        tc::tmem_ld_wait();
+        if (ok && row_ok) {
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint4 pkt;
+            uint32_t* pw = reinterpret_cast<uint32_t*>(&pkt);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float o0 = __uint_as_float(v[q4 * 8 + 2 * i]) * inv;
+              const float o1 = __uint_as_float(v[q4 * 8 + 2 * i + 1]) * inv;
+              pw[i] = tc::pack_bf16x2(o0, o1);
+              if (MODE == 1) {
+                const uint4 dv4 = *reinterpret_cast<const uint4*>(dorow + ch * 32 + q4 * 8);
+                const __nv_bfloat162 d2 = reinterpret_cast<const __nv_bfloat162*>(&dv4)[i];
+                dsum += o0 * __low2float(d2) + o1 * __high2float(d2);
+              }
+            }
+            *reinterpret_cast<uint4*>(orow + ch * 32 + q4 * 8) = pkt;
+          }
+        }
+      }
+      if (ok && row_ok) {
+        if (MODE == 0)
+          a.lse[(int64_t)h * S + row] = l > 0.f ? (m_used + log2f(l)) * kLn2 : -INFINITY;
+        else
+          a.D[(int64_t)h * S + row] = dsum;
+      }
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, L::TMEM_COLS);
+  }
+}
+
+template <int DH, int MODE>
+cudaError_t run(const AttnArgs& a, cudaStream_t st) {
+  using L = FwdLayout<DH>;
+  CUtensorMap tq, tk, tv;
+  if (!make_tmap_3d_bf16(&tq, a.q, DH, a.S, a.nh, 64, 128) || !make_tmap_3d_bf16(&tk, a.k, DH, a.S, a.nkv, 64, 128) ||
+      !make_tmap_3d_bf16(&tv, a.v, DH, a.S, a.nkv, 64, 128))
+    return cudaErrorInvalidValue;
+  // at least 120 KB so that two CTAs never share an SM (each takes all 512 TMEM columns)
+  const size_t smem = L::BYTES + 1024 > 120 * 1024 ? L::BYTES + 1024 : 120 * 1024;
+  auto kfn = k_attn_fwd_tc<DH, MODE>;
+  cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int nt = (int)ceil_div(a.S, kTile);
+  dim3 grid((unsigned)ceil_div(nt, 2), (unsigned)a.nh);
+  kfn<<<grid, kFwdThreads, smem, st>>>(tq, tk, tv, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_fwd(const AttnArgs& a, int head_dim, cudaStream_t st) {
+  return head_dim == 64 ? run<64, 0>(a, st) : run<128, 0>(a, st);
+}
+cudaError_t launch_attn_recompute(const AttnArgs& a, int head_dim, cudaStream_t st) {
+  return head_dim == 64 ? run<64, 1>(a, st) : run<128, 1>(a, st);
+}
+
+}  // namespace upipe

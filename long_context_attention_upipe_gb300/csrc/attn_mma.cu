@@ -6,8 +6,6 @@
 // query tile's range are never touched, full tiles run without a mask, partial ones (and the
 // ragged last tile) apply  seg[q] == seg[k] && (!causal || k <= q) && k < S  per element.
 //
-//   fwd        : O = softmax(Q K^T * scale + M) V, lse = m + ln(l)        (grid: q tile x head)
-//   recompute  : O and D = rowsum(dO * O) from the saved lse             (grid: q tile x head)
 //   bwd dq     : dQ = scale * dS K, dS = P * (dP - D), dP = dO V^T       (grid: q tile x head)
 //   bwd dkdv   : dV = sum_h P^T dO, dK = scale * sum_h dS^T Q  over the query heads of a
 //                KV head (GQA reduction in registers)                    (grid: kv tile x kv head)
@@ -88,192 +86,6 @@ __device__ __forceinline__ void pv_tile(float (&acc)[DH / 8][4], const float (&p
       ldmatrix_x4_trans(b, sV + (kk * 16 + (q & 1) * 8 + r) * LD + nj * 16 + (q >> 1) * 8);
       mma_bf16_16816(acc[2 * nj], a, b);
       mma_bf16_16816(acc[2 * nj + 1], a, b + 2);
-    }
-  }
-}
-
-// ---------------------------------------------------------------------------------------------
-// forward (MODE 0) and recompute (MODE 1)
-// ---------------------------------------------------------------------------------------------
-template <int DH, int MODE>
-__global__ void __launch_bounds__(kThreads, 2) k_attn_fwd(AttnArgs a) {
-  constexpr int LD = Smem<DH>::LD;
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  bf16* sQ = reinterpret_cast<bf16*>(smem_raw);
-  bf16* sK = sQ + kTile * LD;          // [2][kSub][LD]
-  bf16* sV = sK + 2 * kSub * LD;       // [2][kSub][LD]
-  int32_t* sSeg = reinterpret_cast<int32_t*>(sV + 2 * kSub * LD);  // [2][kSub]
-
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t S = a.S;
-  const int64_t nt = ceil_div(S, kTile);
-  const int64_t qt = nt - 1 - blockIdx.x;  // longest rows first
-  const int h = blockIdx.y;
-  const int kvh = h / a.g;
-  const bf16* Qh = a.q + (int64_t)h * S * DH;
-  const bf16* Kh = a.k + (int64_t)kvh * S * DH;
-  const bf16* Vh = a.v + (int64_t)kvh * S * DH;
-  const int64_t row0 = qt * kTile;
-  const int4 tr = a.q_rows[qt];  // {kv_begin, kv_full_begin, kv_full_end, kv_end}
-  const bool ragged = (S % kTile) != 0;
-
-  load_rows<DH>(sQ, Qh, row0, kTile, S, tid);
-  cp_async_commit();
-
-  // key sub-tiles: two per 128-tile, the last half dropped when it starts past S
-  const int n_sub_all = 2 * (tr.w - tr.x);
-  auto sub_row = [&](int s) { return (int64_t)tr.x * kTile + (int64_t)s * kSub; };
-  int n_sub = n_sub_all;
-  while (n_sub > 0 && sub_row(n_sub - 1) >= S) --n_sub;
-
-  auto prefetch = [&](int s, int buf) {
-    const int64_t kr0 = sub_row(s);
-    load_rows<DH>(sK + buf * kSub * LD, Kh, kr0, kSub, S, tid);
-    load_rows<DH>(sV + buf * kSub * LD, Vh, kr0, kSub, S, tid);
-    if (a.seg && tid < kSub) sSeg[buf * kSub + tid] = (kr0 + tid < S) ? a.seg[kr0 + tid] : 0;
-  };
-  if (n_sub > 0) prefetch(0, 0);
-  cp_async_commit();
-
-  const int g = lane >> 2, t = lane & 3;
-  const int64_t rA = row0 + warp * 16 + g, rB = rA + 8;  // this thread's two rows
-  const int32_t segA = (a.seg && rA < S) ? a.seg[rA] : 0;
-  const int32_t segB = (a.seg && rB < S) ? a.seg[rB] : 0;
-  const float c = a.scale * kLog2e;
-
-  float m2[2], l[2];  // running max (log2 units) and partial sum per row
-  if (MODE == 0) {
-    m2[0] = m2[1] = -INFINITY;
-  } else {
-    m2[0] = rA < S ? a.lse[(int64_t)h * S + rA] * kLog2e : 0.f;
-    m2[1] = rB < S ? a.lse[(int64_t)h * S + rB] * kLog2e : 0.f;
-  }
-  l[0] = l[1] = 0.f;
-  float acc[DH / 8][4];
-#pragma unroll
-  for (int i = 0; i < DH / 8; ++i)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) acc[i][e] = 0.f;
-
-  for (int s = 0; s < n_sub; ++s) {
-    const int buf = s & 1;
-    if (s + 1 < n_sub) prefetch(s + 1, buf ^ 1);
-    cp_async_commit();
-    cp_async_wait<1>();
-    __syncthreads();
-
-    float sc[8][4];
-    qk_tile<DH>(sc, sQ + warp * 16 * LD, sK + buf * kSub * LD, lane);
-
-    const int64_t kr0 = sub_row(s);
-    const int64_t jt = kr0 / kTile;
-    const bool partial = jt < tr.y || jt >= tr.z || (ragged && jt == nt - 1);
-#pragma unroll
-    for (int nb = 0; nb < 8; ++nb)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float v = sc[nb][e] * c;
-        if (partial) {
-          const int col = nb * 8 + 2 * t + (e & 1);
-          const int64_t kk = kr0 + col;
-          const bool up = e < 2;
-          const int32_t sk = a.seg ? sSeg[buf * kSub + col] : 0;
-          if (!visible(a.seg, up ? segA : segB, sk, up ? rA : rB, kk, S, a.causal)) v = -INFINITY;
-        }
-        sc[nb][e] = v;
-      }
-
-    if (MODE == 0) {
-      float mx[2] = {m2[0], m2[1]};
-#pragma unroll
-      for (int nb = 0; nb < 8; ++nb) {
-        mx[0] = fmaxf(mx[0], fmaxf(sc[nb][0], sc[nb][1]));
-        mx[1] = fmaxf(mx[1], fmaxf(sc[nb][2], sc[nb][3]));
-      }
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-      }
-      float corr[2];
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const float mu = mx[r] == -INFINITY ? 0.f : mx[r];
-        corr[r] = fast_exp2(m2[r] - mu);
-        m2[r] = mx[r];
-        l[r] *= corr[r];
-      }
-#pragma unroll
-      for (int i = 0; i < DH / 8; ++i) {
-        acc[i][0] *= corr[0]; acc[i][1] *= corr[0];
-        acc[i][2] *= corr[1]; acc[i][3] *= corr[1];
-      }
-      const float mu0 = m2[0] == -INFINITY ? 0.f : m2[0];
-      const float mu1 = m2[1] == -INFINITY ? 0.f : m2[1];
-#pragma unroll
-      for (int nb = 0; nb < 8; ++nb) {
-        sc[nb][0] = fast_exp2(sc[nb][0] - mu0);
-        sc[nb][1] = fast_exp2(sc[nb][1] - mu0);
-        sc[nb][2] = fast_exp2(sc[nb][2] - mu1);
-        sc[nb][3] = fast_exp2(sc[nb][3] - mu1);
-        l[0] += sc[nb][0] + sc[nb][1];
-        l[1] += sc[nb][2] + sc[nb][3];
-      }
-    } else {
-#pragma unroll
-      for (int nb = 0; nb < 8; ++nb) {
-        sc[nb][0] = fast_exp2(sc[nb][0] - m2[0]);
-        sc[nb][1] = fast_exp2(sc[nb][1] - m2[0]);
-        sc[nb][2] = fast_exp2(sc[nb][2] - m2[1]);
-        sc[nb][3] = fast_exp2(sc[nb][3] - m2[1]);
-      }
-    }
-    pv_tile<DH>(acc, sc, sV + buf * kSub * LD, lane);
-    __syncthreads();
-  }
-  cp_async_wait<0>();
-
-  bf16* Oh = a.o + (int64_t)h * S * DH;
-  float inv[2] = {1.f, 1.f};
-  if (MODE == 0) {
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      l[r] += __shfl_xor_sync(0xffffffffu, l[r], 1);
-      l[r] += __shfl_xor_sync(0xffffffffu, l[r], 2);
-      inv[r] = l[r] > 0.f ? 1.f / l[r] : 0.f;
-    }
-  }
-  float dsum[2] = {0.f, 0.f};
-#pragma unroll
-  for (int i = 0; i < DH / 8; ++i) {
-    const int col = i * 8 + 2 * t;
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int64_t row = r ? rB : rA;
-      const float o0 = acc[i][2 * r] * inv[r], o1 = acc[i][2 * r + 1] * inv[r];
-      if (row < S) {
-        *reinterpret_cast<uint32_t*>(Oh + row * DH + col) = pack_bf16(o0, o1);
-        if (MODE == 1) {
-          const __nv_bfloat162 d2 = *reinterpret_cast<const __nv_bfloat162*>(a.dO + ((int64_t)h * S + row) * DH + col);
-          dsum[r] += o0 * __low2float(d2) + o1 * __high2float(d2);
-        }
-      }
-    }
-  }
-  if (MODE == 0) {
-    if (t == 0) {
-      if (rA < S) a.lse[(int64_t)h * S + rA] = l[0] > 0.f ? (m2[0] + log2f(l[0])) * kLn2 : -INFINITY;
-      if (rB < S) a.lse[(int64_t)h * S + rB] = l[1] > 0.f ? (m2[1] + log2f(l[1])) * kLn2 : -INFINITY;
-    }
-  } else {
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      dsum[r] += __shfl_xor_sync(0xffffffffu, dsum[r], 1);
-      dsum[r] += __shfl_xor_sync(0xffffffffu, dsum[r], 2);
-    }
-    if (t == 0) {
-      if (rA < S) a.D[(int64_t)h * S + rA] = dsum[0];
-      if (rB < S) a.D[(int64_t)h * S + rB] = dsum[1];
     }
   }
 }
@@ -546,26 +358,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv(AttnBwdArgs b) {
 }
 
 template <int DH>
-size_t fwd_smem() {
-  return (size_t)(kTile + 4 * kSub) * Smem<DH>::LD * sizeof(bf16) + 2 * kSub * sizeof(int32_t);
-}
-template <int DH>
 size_t dq_smem() {
   return (size_t)(2 * kTile + 4 * kSub) * Smem<DH>::LD * sizeof(bf16) + 2 * kSub * sizeof(int32_t);
 }
 template <int DH>
 size_t dkdv_smem() {
   return (size_t)(2 * kTile + 4 * kQSub) * Smem<DH>::LD * sizeof(bf16) + 6 * kQSub * sizeof(float);
-}
-
-template <int DH, int MODE>
-cudaError_t run_fwd(const AttnArgs& a, cudaStream_t st) {
-  const size_t smem = fwd_smem<DH>();
-  cudaError_t e = cudaFuncSetAttribute(k_attn_fwd<DH, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  dim3 grid((unsigned)ceil_div(a.S, kTile), (unsigned)a.nh);
-  k_attn_fwd<DH, MODE><<<grid, kThreads, smem, st>>>(a);
-  return cudaGetLastError();
 }
 
 template <int DH>
@@ -590,12 +388,6 @@ cudaError_t run_bwd_dkdv(const AttnBwdArgs& b, cudaStream_t st) {
 
 }  // namespace
 
-cudaError_t launch_attn_fwd(const AttnArgs& a, int head_dim, cudaStream_t st) {
-  return head_dim == 64 ? run_fwd<64, 0>(a, st) : run_fwd<128, 0>(a, st);
-}
-cudaError_t launch_attn_recompute(const AttnArgs& a, int head_dim, cudaStream_t st) {
-  return head_dim == 64 ? run_fwd<64, 1>(a, st) : run_fwd<128, 1>(a, st);
-}
 cudaError_t launch_attn_bwd_dq(const AttnBwdArgs& b, int head_dim, cudaStream_t st) {
   return head_dim == 64 ? run_bwd_dq<64>(b, st) : run_bwd_dq<128>(b, st);
 }

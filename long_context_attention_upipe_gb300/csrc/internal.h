@@ -78,9 +78,11 @@ struct AttnArgs {
   const int4* kv_rows;  // kv-major skip table
   int64_t S;
   int nh;           // query heads of the launch
+  int nkv;          // KV heads of the launch
   int g;            // query heads per KV head (local head h -> KV head h / g)
   int causal;
   float scale;      // softmax scale
+  int* err;         // device error word (table header), set by bounded waits that time out
 };
 
 cudaError_t launch_attn_fwd(const AttnArgs& a, int head_dim, cudaStream_t st);

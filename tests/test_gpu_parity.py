@@ -143,7 +143,7 @@ def run_core(S, Hq, Hkv, Dh, segs, causal):
     return (q, k, v, do, seg), (to_f64(o), to_f64(lse), to_f64(dq), to_f64(dk), to_f64(dv))
 
 
-@pytest.mark.parametrize("case", CORE_CASES)
+@pytest.mark.parametrize("case", CORE_CASES, ids=lambda c: f"S{c[0]}_hq{c[1]}_hkv{c[2]}_dh{c[3]}_c{int(c[5])}")
 def test_core_fwd_bwd_match_oracle(case):
     S, Hq, Hkv, Dh, segs, causal = case
     (q, k, v, do, seg), (o, lse, dq, dk, dv) = run_core(*case)
@@ -176,7 +176,8 @@ LAYER_CASES = [
 ]
 
 
-@pytest.mark.parametrize("case", LAYER_CASES)
+@pytest.mark.parametrize("case", LAYER_CASES,
+                         ids=lambda c: f"S{c[0]}_d{c[1]}_hq{c[2]}_hkv{c[3]}_dh{c[4]}_c{int(c[6])}_hpc{c[7]}_acc{c[8]}")
 def test_layer_fwd_bwd_match_oracle(case):
     S, d, Hq, Hkv, Dh, segs, causal, hpc, accum = case
     X, W, Wo, dY = layer_inputs(S, d, Hq, Hkv, Dh)
