@@ -43,6 +43,9 @@ def parse():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-profile", action="store_true", help="skip the torch-profiler launch count")
     ap.add_argument("--sample-tokens", type=int, default=1024, help="oracle sample length (CPU legs)")
+    ap.add_argument("--kernel", default=None, choices=["fwd", "recompute", "dq", "dkdv"],
+                    help="time one attention kernel alone at the workload's chunk shapes (for profilers)")
+    ap.add_argument("--reps", type=int, default=3)
     return ap.parse_args()
 
 
@@ -256,6 +259,38 @@ def main():
     flops = w.flops_fwd_bwd()
     peaks, peak_kind = measured_peaks()
 
+    def chunk_kernels(hpc):
+        """The four attention kernels of one chunk (hpc query heads) on seeded Q/K/V/dO."""
+        g = Hq // Hkv
+        kvc = max(1, hpc // g)
+        cdesc = up.make_desc(S, d, hpc, kvc, Dh, hpc, w.causal)
+        q = fill((hpc, S, Dh), 10, 1.0)
+        k = fill((kvc, S, Dh), 11, 1.0)
+        v = fill((kvc, S, Dh), 12, 1.0)
+        do = fill((hpc, S, Dh), 13, 1.0)
+        o = torch.empty_like(q)
+        lse_c = torch.empty(hpc, S, dtype=torch.float32, device=dev)
+        Dt = torch.empty(hpc, S, dtype=torch.float32, device=dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        table = torch.empty(up.tile_table_bytes(cdesc), dtype=torch.uint8, device=dev)
+        up.build_tile_table(cdesc, seg_t, table, stream)
+        up.core_fwd(cdesc, q, k, v, seg_t, table, o, lse_c, stream)
+        up.core_recompute(cdesc, q, k, v, do, lse_c, seg_t, table, o, Dt, stream)
+        return {
+            "fwd": lambda: up.core_fwd(cdesc, q, k, v, seg_t, table, o, lse_c, stream),
+            "recompute": lambda: up.core_recompute(cdesc, q, k, v, do, lse_c, seg_t, table, o, Dt, stream),
+            "dq": lambda: up.core_bwd_dq(cdesc, q, k, v, do, lse_c, Dt, seg_t, table, dq, stream),
+            "dkdv": lambda: up.core_bwd_dkdv(cdesc, q, k, v, do, lse_c, Dt, seg_t, table, dk, dv, stream),
+        }
+
+    if args.kernel:
+        f = chunk_kernels(args.hpc)[args.kernel]
+        f()
+        ms_k = time_steps(f, args.reps)
+        tf = attn_kernel_flops(w, args.hpc, args.kernel) / (ms_k * 1e-3) / 1e12
+        print(json.dumps({"kernel": args.kernel, "workload": w.name, "heads": args.hpc, "ms": ms_k, "tflops": tf}))
+        return
+
     # ---------------- main timed run
     torch.cuda.reset_peak_memory_stats(dev)
     base_alloc = torch.cuda.memory_allocated(dev)
@@ -296,26 +331,8 @@ def main():
 
         # ---------------- per-kernel timing of the attention kernels (same launch configuration)
         hpc = args.hpc
-        g = Hq // Hkv
-        kvc = max(1, hpc // g)
         n_chunks = Hq // hpc
-        cdesc = up.make_desc(S, d, hpc, kvc, Dh, hpc, w.causal)
-        q = fill((hpc, S, Dh), 10, 1.0)
-        k = fill((kvc, S, Dh), 11, 1.0)
-        v = fill((kvc, S, Dh), 12, 1.0)
-        do = fill((hpc, S, Dh), 13, 1.0)
-        o = torch.empty_like(q)
-        lse_c = torch.empty(hpc, S, dtype=torch.float32, device=dev)
-        Dt = torch.empty(hpc, S, dtype=torch.float32, device=dev)
-        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-        table = torch.empty(up.tile_table_bytes(cdesc), dtype=torch.uint8, device=dev)
-        up.build_tile_table(cdesc, seg_t, table, stream)
-        kernels = {
-            "fwd": lambda: up.core_fwd(cdesc, q, k, v, seg_t, table, o, lse_c, stream),
-            "recompute": lambda: up.core_recompute(cdesc, q, k, v, do, lse_c, seg_t, table, o, Dt, stream),
-            "dq": lambda: up.core_bwd_dq(cdesc, q, k, v, do, lse_c, Dt, seg_t, table, dq, stream),
-            "dkdv": lambda: up.core_bwd_dkdv(cdesc, q, k, v, do, lse_c, Dt, seg_t, table, dk, dv, stream),
-        }
+        kernels = chunk_kernels(hpc)
         ktimes = {}
         for name in ("fwd", "recompute", "dq", "dkdv"):
             f = kernels[name]

@@ -7,7 +7,8 @@
 // run unmasked, partial tiles and the ragged last tile apply the causal / segment mask.
 //
 // One CTA = one head x two 128-row query tiles (a, b), 12 warps:
-//   warp 0     TMA producer: Q_a, Q_b once, then K/V tiles through a 2-stage ring
+//   warp 0     TMA producer: Q_a, Q_b once, then K_j, V_j, K_j+1, ... through a ring of
+//              tile-sized slots; a K slot is freed as soon as both Q K^T products are done
 //   warp 1     MMA issuer (one thread) and TMEM owner: S_t = Q_t K^T (both operands in shared
 //              memory), O_t += P_t V (P_t read from TMEM, V from shared memory)
 //   warps 4-7  softmax of tile a, warps 8-11 softmax of tile b: each thread owns one query row
@@ -33,13 +34,14 @@ constexpr uint32_t kBoxBytes = 128 * 128;  // one TMA box: 128 rows x 64 bf16 (1
 
 template <int DH>
 struct FwdLayout {
-  static constexpr uint32_t TB = 128 * DH * 2;  // one 128-row tile of Q, K or V
-  static constexpr uint32_t Q = 0, K = 2 * TB, V = 4 * TB, BAR = 6 * TB;
-  static constexpr uint32_t SEG = BAR + 256;             // int32 [2][128]
-  static constexpr uint32_t BYTES = SEG + 2 * 128 * 4;   // + 1024 alignment slack at launch
+  static constexpr uint32_t TB = 128 * DH * 2;          // one 128-row tile of Q, K or V
+  static constexpr int NSLOT = DH == 128 ? 5 : 8;       // K/V ring slots
+  static constexpr uint32_t Q = 0, RING = 2 * TB, BAR = RING + NSLOT * TB;
+  static constexpr uint32_t SEG = BAR + 512;            // int32 [2][128]
+  static constexpr uint32_t BYTES = SEG + 2 * 128 * 4;  // + 1024 alignment slack at launch
+  static constexpr uint32_t TMEM_COLS = 512;
   __device__ static constexpr uint32_t s_col(int t) { return t * 128; }
   __device__ static constexpr uint32_t o_col(int t) { return 256 + t * DH; }
-  static constexpr uint32_t TMEM_COLS = 512;
 };
 
 __device__ __forceinline__ bool in_range(const int4& r, int j) { return j >= r.x && j < r.w; }
@@ -49,17 +51,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     k_attn_fwd_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, AttnArgs a) {
   using L = FwdLayout<DH>;
+  constexpr int NS = L::NSLOT;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR);
   uint64_t* q_full = bars + 0;
-  uint64_t* kv_full = bars + 1;   // [2]
-  uint64_t* kv_empty = bars + 3;  // [2]
-  uint64_t* s_full = bars + 5;    // [2] per query tile
-  uint64_t* p_full = bars + 7;    // [2]
-  uint64_t* o_full = bars + 9;    // [2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 11);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 12);
+  uint64_t* s_full = bars + 1;          // [2] per query tile
+  uint64_t* p_full = bars + 3;          // [2]
+  uint64_t* o_full = bars + 5;          // [2]
+  uint64_t* slot_full = bars + 7;       // [NS]
+  uint64_t* slot_empty = bars + 7 + NS; // [NS]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 7 + 2 * NS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 8 + 2 * NS);
   int32_t* seg_buf = reinterpret_cast<int32_t*>(smem + L::SEG);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -68,22 +71,23 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const int pair = gridDim.x - 1 - blockIdx.x;  // longest query tiles first
   const int h = blockIdx.y;
   const int kvh = h / a.g;
-  int qt[2] = {2 * pair, 2 * pair + 1};
-  bool valid[2] = {qt[0] < nt, qt[1] < nt};
-  int4 rng[2];
-  rng[0] = valid[0] ? a.q_rows[qt[0]] : make_int4(0, 0, 0, 0);
-  rng[1] = valid[1] ? a.q_rows[qt[1]] : make_int4(0, 0, 0, 0);
-  const int j0 = valid[1] ? min(rng[0].x, rng[1].x) : rng[0].x;
-  const int j1 = valid[1] ? max(rng[0].w, rng[1].w) : rng[0].w;
+  const int qt0 = 2 * pair, qt1 = 2 * pair + 1;
+  const bool valid1 = qt1 < nt;
+  const int4 rng0 = a.q_rows[qt0];
+  const int4 rng1 = valid1 ? a.q_rows[qt1] : make_int4(0, 0, 0, 0);
+  const int j0 = valid1 ? min(rng0.x, rng1.x) : rng0.x;
+  const int j1 = valid1 ? max(rng0.w, rng1.w) : rng0.w;
 
   if (threadIdx.x == 0) {
     tc::mbar_init(q_full, 1);
     for (int i = 0; i < 2; ++i) {
-      tc::mbar_init(&kv_full[i], 1);
-      tc::mbar_init(&kv_empty[i], 1);
       tc::mbar_init(&s_full[i], 1);
       tc::mbar_init(&p_full[i], 128);
       tc::mbar_init(&o_full[i], 1);
+    }
+    for (int i = 0; i < NS; ++i) {
+      tc::mbar_init(&slot_full[i], 1);
+      tc::mbar_init(&slot_empty[i], 1);
     }
     *abort_flag = 0;
     tc::fence_mbar_init();
@@ -103,21 +107,21 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tc::prefetch_tmap(&tq);
       tc::prefetch_tmap(&tk);
       tc::prefetch_tmap(&tv);
-      uint32_t qbytes = 0;
-      for (int t = 0; t < 2; ++t) qbytes += valid[t] ? L::TB : 0;
-      tc::mbar_arrive_expect_tx(q_full, qbytes);
-      for (int t = 0; t < 2; ++t)
-        if (valid[t])
-          for (int at = 0; at < DH / 64; ++at)
-            tc::tma_load_3d(smem + L::Q + t * L::TB + at * kBoxBytes, &tq, q_full, at * 64, qt[t] * kTile, h);
-      for (int j = j0, n = 0; j < j1; ++j, ++n) {
-        const int s = n & 1;
-        if (n >= 2 && !tc::mbar_wait(&kv_empty[s], ((n >> 1) - 1) & 1, abort_flag, a.err)) break;
-        tc::mbar_arrive_expect_tx(&kv_full[s], 2 * L::TB);
-        for (int at = 0; at < DH / 64; ++at) {
-          tc::tma_load_3d(smem + L::K + s * L::TB + at * kBoxBytes, &tk, &kv_full[s], at * 64, j * kTile, kvh);
-          tc::tma_load_3d(smem + L::V + s * L::TB + at * kBoxBytes, &tv, &kv_full[s], at * 64, j * kTile, kvh);
-        }
+      tc::mbar_arrive_expect_tx(q_full, (valid1 ? 2 : 1) * L::TB);
+      for (int at = 0; at < DH / 64; ++at) {
+        tc::tma_load_3d(smem + L::Q + at * kBoxBytes, &tq, q_full, at * 64, qt0 * kTile, h);
+        if (valid1) tc::tma_load_3d(smem + L::Q + L::TB + at * kBoxBytes, &tq, q_full, at * 64, qt1 * kTile, h);
+      }
+      // item 2n = K of the n-th key tile, item 2n+1 = its V
+      const int n_items = 2 * (j1 - j0);
+      for (int it = 0; it < n_items; ++it) {
+        const int sl = it % NS;
+        if (it >= NS && !tc::mbar_wait(&slot_empty[sl], ((it / NS) - 1) & 1, abort_flag, a.err)) break;
+        tc::mbar_arrive_expect_tx(&slot_full[sl], L::TB);
+        const CUtensorMap* map = (it & 1) ? &tv : &tk;
+        const int row = (j0 + (it >> 1)) * kTile;
+        for (int at = 0; at < DH / 64; ++at)
+          tc::tma_load_3d(smem + L::RING + sl * L::TB + at * kBoxBytes, map, &slot_full[sl], at * 64, row, kvh);
       }
     }
     __syncwarp();
@@ -126,18 +130,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     if (lane == 0) {
       constexpr uint32_t kIdS = tc::idesc_bf16(128, 128, false, false);
       constexpr uint32_t kIdO = tc::idesc_bf16(128, DH, false, true);
-      const uint32_t sQ = smem_u32(smem + L::Q), sK = smem_u32(smem + L::K), sV = smem_u32(smem + L::V);
+      const uint32_t sQ = smem_u32(smem + L::Q), sR = smem_u32(smem + L::RING);
       bool ok = tc::mbar_wait(q_full, 0, abort_flag, a.err);
-      int waited = -1;
-      auto wait_kv = [&](int n) {
-        while (ok && waited < n) {
-          ++waited;
-          ok = tc::mbar_wait(&kv_full[waited & 1], (waited >> 1) & 1, abort_flag, a.err);
-        }
+      auto wait_item = [&](int it) {
+        if (ok) ok = tc::mbar_wait(&slot_full[it % NS], (it / NS) & 1, abort_flag, a.err);
         tc::fence_after_sync();
       };
       auto issue_s = [&](int t, int n) {
-        const uint32_t kb = sK + (n & 1) * L::TB;
+        const uint32_t kb = sR + ((2 * n) % NS) * L::TB;
         const uint32_t qb = sQ + t * L::TB;
 #pragma unroll
         for (int k = 0; k < DH / 16; ++k) {
@@ -148,20 +148,24 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tc::mma_commit(&s_full[t]);
       };
       auto issue_pv = [&](int t, int n, bool first) {
-        const uint32_t vb = sV + (n & 1) * L::TB;
+        const uint32_t vb = sR + ((2 * n + 1) % NS) * L::TB;
 #pragma unroll
         for (int k = 0; k < 128 / 16; ++k)
           tc::mma_ts(tmem + L::o_col(t), tmem + L::s_col(t) + k * 8, tc::sdesc_sw128(vb + k * 2048, kBoxBytes, 1024),
                      kIdO, (!first) || k > 0);
       };
+      const int4 rng[2] = {rng0, rng1};
       int cnt_p[2] = {0, 0};
       bool first_pv[2] = {true, true};
       if (ok) {
-        wait_kv(0);
+        wait_item(0);
         for (int t = 0; t < 2; ++t)
           if (ok && in_range(rng[t], j0)) issue_s(t, 0);
+        if (ok) tc::mma_commit(&slot_empty[0]);
       }
       for (int j = j0, n = 0; ok && j < j1; ++j, ++n) {
+        wait_item(2 * n + 1);                   // V_j
+        if (j + 1 < j1) wait_item(2 * n + 2);   // K_j+1
         for (int t = 0; t < 2 && ok; ++t) {
           if (in_range(rng[t], j)) {
             ok = tc::mbar_wait(&p_full[t], cnt_p[t] & 1, abort_flag, a.err);
@@ -172,12 +176,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             first_pv[t] = false;
             if (j == rng[t].w - 1) tc::mma_commit(&o_full[t]);
           }
-          if (in_range(rng[t], j + 1)) {
-            wait_kv(n + 1);
-            if (ok) issue_s(t, n + 1);
-          }
+          if (in_range(rng[t], j + 1)) issue_s(t, n + 1);
         }
-        if (ok) tc::mma_commit(&kv_empty[n & 1]);
+        if (ok) {
+          tc::mma_commit(&slot_empty[(2 * n + 1) % NS]);                  // V_j free
+          if (j + 1 < j1) tc::mma_commit(&slot_empty[(2 * n + 2) % NS]);  // K_j+1 free
+        }
       }
     }
     __syncwarp();
@@ -185,11 +189,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     // ------------------------------------------------------------------ softmax groups
     const int t = (warp - 4) >> 2;
     const int r = threadIdx.x - 128 * (1 + t);  // row within the tile == TMEM lane
-    if (valid[t]) {
-      const int64_t row = (int64_t)qt[t] * kTile + r;
+    const int4 rg = t ? rng1 : rng0;
+    if (t == 0 || valid1) {
+      const int64_t row = (int64_t)(t ? qt1 : qt0) * kTile + r;
       const bool row_ok = row < S;
       const int32_t seg_row = (a.seg && row_ok) ? a.seg[row] : 0;
       const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+      const uint32_t s_addr = lane_addr + L::s_col(t), o_addr = lane_addr + L::o_col(t);
       const float c = a.scale * kLog2e;
       const bool ragged = (S % kTile) != 0;
       float m_used = -INFINITY, l = 0.f;
@@ -197,8 +203,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       int32_t* sb = seg_buf + t * 128;
       bool ok = true;
       int cnt = 0;
-      for (int j = rng[t].x; j < rng[t].w; ++j, ++cnt) {
-        const bool partial = j < rng[t].y || j >= rng[t].z || (ragged && j == nt - 1);
+      for (int j = rg.x; j < rg.w; ++j, ++cnt) {
+        const bool partial = j < rg.y || j >= rg.z || (ragged && j == nt - 1);
         if (partial && a.seg) {
           const int64_t col = (int64_t)j * kTile + r;
           tc::named_bar_sync(1 + t, 128);
@@ -221,15 +227,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         };
         float mu;
         if (MODE == 0) {
-          // pass 1 over the row of S: its maximum
+          // pass 1 over the row of S: its maximum (two 32-column loads in flight per wait)
           float mx = m_used;
 #pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
-            uint32_t v[32];
-            tc::tmem_ld32(lane_addr + L::s_col(t) + ch * 32, v);
+          for (int hf = 0; hf < 2; ++hf) {
+            uint32_t v0[32], v1[32];
+            tc::tmem_ld32(s_addr + hf * 64, v0);
+            tc::tmem_ld32(s_addr + hf * 64 + 32, v1);
             tc::tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) mx = fmaxf(mx, score(v[i], ch * 32 + i));
+            for (int i = 0; i < 32; ++i) {
+              mx = fmaxf(mx, score(v0[i], hf * 64 + i));
+              mx = fmaxf(mx, score(v1[i], hf * 64 + 32 + i));
+            }
           }
           const bool need = mx > m_used + 8.f;
           const bool rescale_o = need && cnt > 0 && m_used != -INFINITY;
@@ -238,11 +248,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
             for (int ch = 0; ch < DH / 32; ++ch) {
               uint32_t v[32];
-              tc::tmem_ld32(lane_addr + L::o_col(t) + ch * 32, v);
+              tc::tmem_ld32(o_addr + ch * 32, v);
               tc::tmem_ld_wait();
 #pragma unroll
               for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * f);
-              tc::tmem_st32(lane_addr + L::o_col(t) + ch * 32, v);
+              tc::tmem_st32(o_addr + ch * 32, v);
             }
             tc::tmem_st_wait();
             l *= f;
@@ -255,30 +265,32 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         // pass 2: P = exp2(score - mu) as bf16 pairs over the first 64 columns of S.  Half h
         // reads S columns [64h, 64h + 64) and writes P columns [32h, 32h + 32), which this
         // thread has already read.
+        float l0 = 0.f, l1 = 0.f;
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
-          uint32_t pk[32];
+          uint32_t v0[32], v1[32];
+          tc::tmem_ld32(s_addr + hf * 64, v0);
+          tc::tmem_ld32(s_addr + hf * 64 + 32, v1);
+          tc::tmem_ld_wait();
 #pragma unroll
-          for (int sub = 0; sub < 2; ++sub) {
-            const int ch = hf * 2 + sub;
-            uint32_t v[32];
-            tc::tmem_ld32(lane_addr + L::s_col(t) + ch * 32, v);
-            tc::tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float p0 = fast_exp2(score(v[2 * i], ch * 32 + 2 * i) - mu);
-              const float p1 = fast_exp2(score(v[2 * i + 1], ch * 32 + 2 * i + 1) - mu);
-              l += p0 + p1;
-              pk[sub * 16 + i] = tc::pack_bf16x2(p0, p1);
-            }
+          for (int i = 0; i < 16; ++i) {
+            const float p0 = fast_exp2(score(v0[2 * i], hf * 64 + 2 * i) - mu);
+            const float p1 = fast_exp2(score(v0[2 * i + 1], hf * 64 + 2 * i + 1) - mu);
+            const float p2 = fast_exp2(score(v1[2 * i], hf * 64 + 32 + 2 * i) - mu);
+            const float p3 = fast_exp2(score(v1[2 * i + 1], hf * 64 + 32 + 2 * i + 1) - mu);
+            l0 += p0 + p1;
+            l1 += p2 + p3;
+            v0[i] = tc::pack_bf16x2(p0, p1);
+            v0[16 + i] = tc::pack_bf16x2(p2, p3);
           }
-          tc::tmem_st32(lane_addr + L::s_col(t) + hf * 32, pk);
+          tc::tmem_st32(s_addr + hf * 32, v0);
         }
+        l += l0 + l1;
         tc::tmem_st_wait();
         tc::fence_before_sync();
         tc::mbar_arrive(&p_full[t]);
       }
-      if (ok && rng[t].w > rng[t].x) ok = tc::mbar_wait(&o_full[t], 0, abort_flag, a.err);
+      if (ok) ok = tc::mbar_wait(&o_full[t], 0, abort_flag, a.err);
       tc::fence_after_sync();
       // epilogue: O / l -> bf16 row; lse or D
       const float inv = (MODE == 0) ? (l > 0.f ? 1.f / l : 0.f) : 1.f;
@@ -288,20 +300,21 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
 #pragma unroll
       for (int ch = 0; ch < DH / 32; ++ch) {
         uint32_t v[32];
-        tc::tmem_ld32(lane_addr + L::o_col(t) + ch * 32, v);
+        tc::tmem_ld32(o_addr + ch * 32, v);
         tc::tmem_ld_wait();
         if (ok && row_ok) {
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
             uint4 pkt;
             uint32_t* pw = reinterpret_cast<uint32_t*>(&pkt);
+            uint4 dv4;
+            if (MODE == 1) dv4 = *reinterpret_cast<const uint4*>(dorow + ch * 32 + q4 * 8);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               const float o0 = __uint_as_float(v[q4 * 8 + 2 * i]) * inv;
               const float o1 = __uint_as_float(v[q4 * 8 + 2 * i + 1]) * inv;
               pw[i] = tc::pack_bf16x2(o0, o1);
               if (MODE == 1) {
-                const uint4 dv4 = *reinterpret_cast<const uint4*>(dorow + ch * 32 + q4 * 8);
                 const __nv_bfloat162 d2 = reinterpret_cast<const __nv_bfloat162*>(&dv4)[i];
                 dsum += o0 * __low2float(d2) + o1 * __high2float(d2);
               }
