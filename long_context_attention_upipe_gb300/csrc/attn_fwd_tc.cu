@@ -268,7 +268,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         float l0 = 0.f, l1 = 0.f;
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
-          uint32_t v0[32], v1[32];
+          uint32_t v0[32], v1[32], pk[32];
           tc::tmem_ld32(s_addr + hf * 64, v0);
           tc::tmem_ld32(s_addr + hf * 64 + 32, v1);
           tc::tmem_ld_wait();
@@ -280,10 +280,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             const float p3 = fast_exp2(score(v1[2 * i + 1], hf * 64 + 32 + 2 * i + 1) - mu);
             l0 += p0 + p1;
             l1 += p2 + p3;
-            v0[i] = tc::pack_bf16x2(p0, p1);
-            v0[16 + i] = tc::pack_bf16x2(p2, p3);
+            pk[i] = tc::pack_bf16x2(p0, p1);
+            pk[16 + i] = tc::pack_bf16x2(p2, p3);
           }
-          tc::tmem_st32(s_addr + hf * 32, v0);
+          tc::tmem_st32(s_addr + hf * 32, pk);
         }
         l += l0 + l1;
         tc::tmem_st_wait();
