@@ -4,15 +4,18 @@
 // summary "Road to 5 Million Tokens", chapter on DeepSpeed Ulysses: each GPU computes whole
 // heads, so flash attention applies).  Key tiles come from the skip table (MaxText article,
 // Splash attention paragraph): tiles outside a query tile's range are never loaded, full tiles
-// run unmasked, partial tiles and the ragged last tile apply the causal / segment mask.
+// run unmasked, partial tiles and the ragged last tile apply the causal / segment mask.  With
+// contiguous segments a query row sees one interval of keys, so the mask of a partial tile is
+// two integer compares per element.
 //
-// One CTA = one head x two 128-row query tiles (a, b), 12 warps:
+// One CTA = one head x two 128-row query tiles (a, b), 10 warps:
 //   warp 0     TMA producer: Q_a, Q_b once, then K_j, V_j, K_j+1, ... through a ring of
 //              tile-sized slots; a K slot is freed as soon as both Q K^T products are done
 //   warp 1     MMA issuer (one thread) and TMEM owner: S_t = Q_t K^T (both operands in shared
 //              memory), O_t += P_t V (P_t read from TMEM, V from shared memory)
-//   warps 4-7  softmax of tile a, warps 8-11 softmax of tile b: each thread owns one query row
-//              (one TMEM lane): row max, exp2, row sum, P written back over S as bf16
+//   warps 2-5  softmax of tile a, warps 6-9 softmax of tile b: each thread owns one query row
+//              (TMEM lane 32 * (warp % 4) + lane): row max, exp2, row sum, P written back over
+//              S as bf16, all from one TMEM read of the row
 // TMEM columns: S/P_a [0,128) S/P_b [128,256) O_a [256,256+Dh) O_b [256+Dh, 256+2Dh).
 // While one softmax group works, the tensor core runs the other tile's P V and next Q K^T.
 // The running max is rescaled lazily: O is corrected only when the row max grows by more than
@@ -29,16 +32,15 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr int kFwdThreads = 384;
+constexpr int kFwdThreads = 320;
 constexpr uint32_t kBoxBytes = 128 * 128;  // one TMA box: 128 rows x 64 bf16 (128 B, swizzled)
 
 template <int DH>
 struct FwdLayout {
-  static constexpr uint32_t TB = 128 * DH * 2;          // one 128-row tile of Q, K or V
-  static constexpr int NSLOT = DH == 128 ? 5 : 8;       // K/V ring slots
+  static constexpr uint32_t TB = 128 * DH * 2;     // one 128-row tile of Q, K or V
+  static constexpr int NSLOT = DH == 128 ? 5 : 8;  // K/V ring slots
   static constexpr uint32_t Q = 0, RING = 2 * TB, BAR = RING + NSLOT * TB;
-  static constexpr uint32_t SEG = BAR + 512;            // int32 [2][128]
-  static constexpr uint32_t BYTES = SEG + 2 * 128 * 4;  // + 1024 alignment slack at launch
+  static constexpr uint32_t BYTES = BAR + 512;     // + 1024 alignment slack at launch
   static constexpr uint32_t TMEM_COLS = 512;
   __device__ static constexpr uint32_t s_col(int t) { return t * 128; }
   __device__ static constexpr uint32_t o_col(int t) { return 256 + t * DH; }
@@ -46,8 +48,10 @@ struct FwdLayout {
 
 __device__ __forceinline__ bool in_range(const int4& r, int j) { return j >= r.x && j < r.w; }
 
+// 320 threads x 200 registers = 64,000 of the SM's 65,536: one CTA per SM (it also holds all of
+// TMEM and most of shared memory)
 template <int DH, int MODE>
-__global__ void __launch_bounds__(kFwdThreads, 1)
+__global__ void __maxnreg__(200)
     k_attn_fwd_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, AttnArgs a) {
   using L = FwdLayout<DH>;
@@ -56,14 +60,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR);
   uint64_t* q_full = bars + 0;
-  uint64_t* s_full = bars + 1;          // [2] per query tile
-  uint64_t* p_full = bars + 3;          // [2]
-  uint64_t* o_full = bars + 5;          // [2]
-  uint64_t* slot_full = bars + 7;       // [NS]
-  uint64_t* slot_empty = bars + 7 + NS; // [NS]
+  uint64_t* s_full = bars + 1;           // [2] per query tile
+  uint64_t* p_full = bars + 3;           // [2]
+  uint64_t* o_full = bars + 5;           // [2]
+  uint64_t* slot_full = bars + 7;        // [NS]
+  uint64_t* slot_empty = bars + 7 + NS;  // [NS]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 7 + 2 * NS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 8 + 2 * NS);
-  int32_t* seg_buf = reinterpret_cast<int32_t*>(smem + L::SEG);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t S = a.S;
@@ -185,108 +188,93 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp >= 4) {
+  } else {
     // ------------------------------------------------------------------ softmax groups
-    const int t = (warp - 4) >> 2;
-    const int r = threadIdx.x - 128 * (1 + t);  // row within the tile == TMEM lane
+    const int t = (warp - 2) >> 2;
+    const int r = 32 * (warp & 3) + lane;  // row within the tile == TMEM lane this warp may access
     const int4 rg = t ? rng1 : rng0;
     if (t == 0 || valid1) {
       const int64_t row = (int64_t)(t ? qt1 : qt0) * kTile + r;
       const bool row_ok = row < S;
-      const int32_t seg_row = (a.seg && row_ok) ? a.seg[row] : 0;
+      // the keys this row sees: [vis_lo, vis_hi] (empty for rows past the end)
+      int64_t vis_lo = 0, vis_hi = -1;
+      if (row_ok) {
+        vis_lo = seg_first(a.seg, row);
+        vis_hi = a.causal ? row : seg_last(a.seg, S, row);
+      }
       const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
       const uint32_t s_addr = lane_addr + L::s_col(t), o_addr = lane_addr + L::o_col(t);
       const float c = a.scale * kLog2e;
       const bool ragged = (S % kTile) != 0;
       float m_used = -INFINITY, l = 0.f;
       if (MODE == 1) m_used = row_ok ? a.lse[(int64_t)h * S + row] * kLog2e : 0.f;
-      int32_t* sb = seg_buf + t * 128;
       bool ok = true;
       int cnt = 0;
       for (int j = rg.x; j < rg.w; ++j, ++cnt) {
         const bool partial = j < rg.y || j >= rg.z || (ragged && j == nt - 1);
-        if (partial && a.seg) {
-          const int64_t col = (int64_t)j * kTile + r;
-          tc::named_bar_sync(1 + t, 128);
-          sb[r] = col < S ? a.seg[col] : 0;
-          tc::named_bar_sync(1 + t, 128);
-        }
         ok = tc::mbar_wait(&s_full[t], cnt & 1, abort_flag, a.err);
         if (!ok) break;
         tc::fence_after_sync();
-        const int64_t col0 = (int64_t)j * kTile;
-        // scaled score of column k (log2 units), -inf where masked
-        auto score = [&](uint32_t bits, int k) {
-          float v = __uint_as_float(bits) * c;
-          if (partial) {
-            const int64_t col = col0 + k;
-            const bool vis = row_ok && col < S && (!a.causal || col <= row) && (!a.seg || sb[k] == seg_row);
-            if (!vis) v = -INFINITY;
-          }
-          return v;
-        };
+        uint32_t sv[128];
+        tc::tmem_ld32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+        tc::tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+        tc::tmem_ld32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[64]));
+        tc::tmem_ld32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&sv[96]));
+        tc::tmem_ld_wait();
+        if (partial) {
+          const int64_t col0 = (int64_t)j * kTile;
+          const int lo = (int)max((int64_t)-1, min(vis_lo - col0, (int64_t)128));
+          const int hi = (int)max((int64_t)-1, min(vis_hi - col0, (int64_t)128));
+#pragma unroll
+          for (int k = 0; k < 128; ++k)
+            if (k < lo || k > hi) sv[k] = 0xff800000u;  // -inf
+        }
         float mu;
+        float f = 1.f;
+        bool rescale_o = false;
         if (MODE == 0) {
-          // pass 1 over the row of S: its maximum (two 32-column loads in flight per wait)
-          float mx = m_used;
+          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            uint32_t v0[32], v1[32];
-            tc::tmem_ld32(s_addr + hf * 64, v0);
-            tc::tmem_ld32(s_addr + hf * 64 + 32, v1);
-            tc::tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              mx = fmaxf(mx, score(v0[i], hf * 64 + i));
-              mx = fmaxf(mx, score(v1[i], hf * 64 + 32 + i));
-            }
-          }
+          for (int k = 0; k < 128; ++k) m4[k & 3] = fmaxf(m4[k & 3], __uint_as_float(sv[k]));
+          const float mx = fmaxf(m_used, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * c);
           const bool need = mx > m_used + 8.f;
-          const bool rescale_o = need && cnt > 0 && m_used != -INFINITY;
-          if (__any_sync(0xffffffffu, rescale_o)) {
-            const float f = rescale_o ? fast_exp2(m_used - mx) : 1.f;
-#pragma unroll
-            for (int ch = 0; ch < DH / 32; ++ch) {
-              uint32_t v[32];
-              tc::tmem_ld32(o_addr + ch * 32, v);
-              tc::tmem_ld_wait();
-#pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * f);
-              tc::tmem_st32(o_addr + ch * 32, v);
-            }
-            tc::tmem_st_wait();
-            l *= f;
-          }
+          rescale_o = need && cnt > 0 && m_used != -INFINITY;
+          if (rescale_o) f = fast_exp2(m_used - mx);
           if (need) m_used = mx;
           mu = m_used == -INFINITY ? 0.f : m_used;
         } else {
           mu = m_used;
         }
-        // pass 2: P = exp2(score - mu) as bf16 pairs over the first 64 columns of S.  Half h
-        // reads S columns [64h, 64h + 64) and writes P columns [32h, 32h + 32), which this
-        // thread has already read.
-        float l0 = 0.f, l1 = 0.f;
+        // P = exp2(s * c - mu) as bf16 pairs into the first 64 columns of S (already read)
+        float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
-          uint32_t v0[32], v1[32], pk[32];
-          tc::tmem_ld32(s_addr + hf * 64, v0);
-          tc::tmem_ld32(s_addr + hf * 64 + 32, v1);
-          tc::tmem_ld_wait();
+          uint32_t pk[32];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float p0 = fast_exp2(score(v0[2 * i], hf * 64 + 2 * i) - mu);
-            const float p1 = fast_exp2(score(v0[2 * i + 1], hf * 64 + 2 * i + 1) - mu);
-            const float p2 = fast_exp2(score(v1[2 * i], hf * 64 + 32 + 2 * i) - mu);
-            const float p3 = fast_exp2(score(v1[2 * i + 1], hf * 64 + 32 + 2 * i + 1) - mu);
-            l0 += p0 + p1;
-            l1 += p2 + p3;
+          for (int i = 0; i < 32; ++i) {
+            const float p0 = fast_exp2(fmaf(__uint_as_float(sv[hf * 64 + 2 * i]), c, -mu));
+            const float p1 = fast_exp2(fmaf(__uint_as_float(sv[hf * 64 + 2 * i + 1]), c, -mu));
+            l4[i & 3] += p0 + p1;
             pk[i] = tc::pack_bf16x2(p0, p1);
-            pk[16 + i] = tc::pack_bf16x2(p2, p3);
           }
           tc::tmem_st32(s_addr + hf * 32, pk);
         }
-        l += l0 + l1;
         tc::tmem_st_wait();
+        if (MODE == 0 && __any_sync(0xffffffffu, rescale_o)) {
+          // O_t is idle here: P V of the previous tile completed before this S was ready, and
+          // this tile's P V waits for the arrival below
+#pragma unroll
+          for (int ch = 0; ch < DH / 32; ++ch) {
+            uint32_t v[32];
+            tc::tmem_ld32(o_addr + ch * 32, v);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * f);
+            tc::tmem_st32(o_addr + ch * 32, v);
+          }
+          tc::tmem_st_wait();
+        }
+        l = l * f + ((l4[0] + l4[1]) + (l4[2] + l4[3]));
         tc::fence_before_sync();
         tc::mbar_arrive(&p_full[t]);
       }

@@ -26,6 +26,29 @@ static_assert(sizeof(TableHeader) == 32, "table header is 32 bytes");
 
 inline __host__ __device__ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Segment bounds of position r for non-decreasing segment ids (NULL: one segment [0, S)).
+// With contiguous segments, query r sees exactly the keys [seg_first(r), causal ? r : seg_last(r)].
+__device__ __forceinline__ int64_t seg_first(const int32_t* seg, int64_t r) {
+  if (!seg) return 0;
+  const int32_t v = seg[r];
+  int64_t lo = 0, hi = r;  // first p in [0, r] with seg[p] >= v
+  while (lo < hi) {
+    const int64_t mid = (lo + hi) >> 1;
+    if (seg[mid] >= v) hi = mid; else lo = mid + 1;
+  }
+  return lo;
+}
+__device__ __forceinline__ int64_t seg_last(const int32_t* seg, int64_t S, int64_t r) {
+  if (!seg) return S - 1;
+  const int32_t v = seg[r];
+  int64_t lo = r, hi = S - 1;  // last p in [r, S) with seg[p] <= v
+  while (lo < hi) {
+    const int64_t mid = (lo + hi + 1) >> 1;
+    if (seg[mid] <= v) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
 // First error wins; the word lives in the table header.
 __device__ __forceinline__ void set_error(int* word, int code) { atomicCAS(word, 0, code); }
 
