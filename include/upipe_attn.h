@@ -70,6 +70,10 @@ typedef struct {
 /* Human-readable name of a status code (static string, never NULL). */
 const char* upipe_attn_status_string(upipe_status_t status);
 
+/* Name of the CUDA runtime error (e.g. "cudaErrorInvalidValue") behind the most recent
+ * UPIPE_ERR_CUDA returned on the calling host thread; "cudaSuccess" if none.  Static string. */
+const char* upipe_attn_last_error_string(void);
+
 /* Workspace bytes needed by upipe_attn_fwd (pass = 0) or upipe_attn_bwd (pass = 1) for this
  * descriptor.  Host-only; writes *bytes.  The size grows with heads_per_chunk (per-chunk
  * Q/O/dO/dQ buffers and the resident K/V of one KV group), not with n_q_heads. */

@@ -19,7 +19,7 @@ STATUS = {0: "UPIPE_OK", 1: "UPIPE_ERR_INVALID_ARG", 2: "UPIPE_ERR_UNSUPPORTED",
           7: "UPIPE_ERR_DEVICE_TIMEOUT"}
 UPIPE_OK = 0
 
-EXPORTS = ["upipe_attn_status_string", "upipe_attn_workspace_size", "upipe_attn_tile_table_size",
+EXPORTS = ["upipe_attn_status_string", "upipe_attn_last_error_string", "upipe_attn_workspace_size", "upipe_attn_tile_table_size",
            "upipe_attn_build_tile_table", "upipe_attn_fwd", "upipe_attn_bwd", "upipe_attn_core_fwd",
            "upipe_attn_core_recompute", "upipe_attn_core_bwd_dq", "upipe_attn_core_bwd_dkdv", "upipe_attn_gemm_nt",
            "upipe_attn_device_status"]
@@ -56,6 +56,7 @@ def lib():
         D = ctypes.POINTER(Desc)
         sig = {
             "upipe_attn_status_string": ([ctypes.c_int], ctypes.c_char_p),
+            "upipe_attn_last_error_string": ([], ctypes.c_char_p),
             "upipe_attn_workspace_size": ([D, ctypes.c_int, ctypes.POINTER(SZ)], ctypes.c_int),
             "upipe_attn_tile_table_size": ([D, ctypes.POINTER(SZ)], ctypes.c_int),
             "upipe_attn_build_tile_table": ([D, P, P, SZ, P], ctypes.c_int),
@@ -78,6 +79,8 @@ def lib():
 
 def _check(code, where):
     if code != UPIPE_OK:
+        if code == 6:  # UPIPE_ERR_CUDA: name the CUDA error behind it
+            where = f"{where} ({lib().upipe_attn_last_error_string().decode()})"
         raise UpipeError(code, where)
 
 

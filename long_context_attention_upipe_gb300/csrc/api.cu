@@ -27,6 +27,15 @@
 
 namespace upipe {
 
+// Name of the CUDA error behind the last UPIPE_ERR_CUDA returned on this host thread.
+thread_local const char* g_last_cuda_error = "cudaSuccess";
+
+upipe_status_t cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return UPIPE_OK;
+  g_last_cuda_error = cudaGetErrorName(e);
+  return UPIPE_ERR_CUDA;
+}
+
 namespace {
 
 constexpr size_t kAlign = 256;
@@ -127,9 +136,10 @@ T* at(void* ws, size_t off) {
   return reinterpret_cast<T*>(reinterpret_cast<char*>(ws) + off);
 }
 
-#define UPIPE_CUDA(x)                          \
-  do {                                         \
-    if ((x) != cudaSuccess) return UPIPE_ERR_CUDA; \
+#define UPIPE_CUDA(x)                                 \
+  do {                                                \
+    const cudaError_t e_ = (x);                       \
+    if (e_ != cudaSuccess) return cuda_status(e_);    \
   } while (0)
 
 // Wqkv row of the first weight row of a head: Q heads, then K heads, then V heads.
@@ -339,6 +349,8 @@ using namespace upipe;
 
 extern "C" {
 
+const char* upipe_attn_last_error_string(void) { return upipe::g_last_cuda_error; }
+
 const char* upipe_attn_status_string(upipe_status_t s) {
   switch (s) {
     case UPIPE_OK: return "ok";
@@ -373,8 +385,7 @@ upipe_status_t upipe_attn_build_tile_table(const upipe_attn_desc_t* desc, const 
   if (desc->causal != 0 && desc->causal != 1) return UPIPE_ERR_INVALID_ARG;
   if (!aligned16(table) || (seg && !aligned16(seg))) return UPIPE_ERR_ALIGNMENT;
   if (table_bytes < tile_table_bytes(desc->seq_len)) return UPIPE_ERR_WORKSPACE_TOO_SMALL;
-  if (launch_tile_table(desc->seq_len, desc->causal, seg, table, (cudaStream_t)stream) != cudaSuccess) return UPIPE_ERR_CUDA;
-  return UPIPE_OK;
+  return cuda_status(launch_tile_table(desc->seq_len, desc->causal, seg, table, (cudaStream_t)stream));
 }
 
 upipe_status_t upipe_attn_fwd(const upipe_attn_desc_t* desc, const uint16_t* X, const uint16_t* Wqkv, const uint16_t* Wo,
@@ -444,7 +455,7 @@ upipe_status_t upipe_attn_core_fwd(const upipe_attn_desc_t* desc, const uint16_t
   AttnArgs a = core_args(desc, q, k, v, seg, table);
   a.o = reinterpret_cast<bf16*>(o);
   a.lse = lse;
-  return launch_attn_fwd(a, desc->head_dim, (cudaStream_t)stream) == cudaSuccess ? UPIPE_OK : UPIPE_ERR_CUDA;
+  return cuda_status(launch_attn_fwd(a, desc->head_dim, (cudaStream_t)stream));
 }
 
 upipe_status_t upipe_attn_core_recompute(const upipe_attn_desc_t* desc, const uint16_t* q, const uint16_t* k,
@@ -461,7 +472,7 @@ upipe_status_t upipe_attn_core_recompute(const upipe_attn_desc_t* desc, const ui
   a.dO = reinterpret_cast<const bf16*>(dO);
   a.D = D;
   a.o = reinterpret_cast<bf16*>(o);
-  return launch_attn_recompute(a, desc->head_dim, (cudaStream_t)stream) == cudaSuccess ? UPIPE_OK : UPIPE_ERR_CUDA;
+  return cuda_status(launch_attn_recompute(a, desc->head_dim, (cudaStream_t)stream));
 }
 
 static upipe_status_t core_bwd_common(const upipe_attn_desc_t* desc, const uint16_t* q, const uint16_t* k,
@@ -491,7 +502,7 @@ upipe_status_t upipe_attn_core_bwd_dq(const upipe_attn_desc_t* desc, const uint1
   if (!dq) return UPIPE_ERR_INVALID_ARG;
   if (!aligned16(dq)) return UPIPE_ERR_ALIGNMENT;
   b.dq = reinterpret_cast<bf16*>(dq);
-  return launch_attn_bwd_dq(b, desc->head_dim, (cudaStream_t)stream) == cudaSuccess ? UPIPE_OK : UPIPE_ERR_CUDA;
+  return cuda_status(launch_attn_bwd_dq(b, desc->head_dim, (cudaStream_t)stream));
 }
 
 upipe_status_t upipe_attn_core_bwd_dkdv(const upipe_attn_desc_t* desc, const uint16_t* q, const uint16_t* k,
@@ -505,7 +516,7 @@ upipe_status_t upipe_attn_core_bwd_dkdv(const upipe_attn_desc_t* desc, const uin
   if (!aligned16(dk) || !aligned16(dv)) return UPIPE_ERR_ALIGNMENT;
   b.dk = reinterpret_cast<bf16*>(dk);
   b.dv = reinterpret_cast<bf16*>(dv);
-  return launch_attn_bwd_dkdv(b, desc->head_dim, (cudaStream_t)stream) == cudaSuccess ? UPIPE_OK : UPIPE_ERR_CUDA;
+  return cuda_status(launch_attn_bwd_dkdv(b, desc->head_dim, (cudaStream_t)stream));
 }
 
 upipe_status_t upipe_attn_gemm_nt(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda, const uint16_t* B,
@@ -519,17 +530,17 @@ upipe_status_t upipe_attn_gemm_nt(int64_t M, int64_t N, int64_t K, const uint16_
   g.b.blk[0] = B; g.b.ld = ldb; g.b.blk_shift = -1; g.b.k_major = 1;
   g.c.blk[0] = C; g.c.ld = ldc; g.c.blk_shift = -1;
   g.epi = EPI_STORE_F32;
-  return launch_gemm(g, 1, nullptr, (cudaStream_t)stream) == cudaSuccess ? UPIPE_OK : UPIPE_ERR_CUDA;
+  return cuda_status(launch_gemm(g, 1, nullptr, (cudaStream_t)stream));
 }
 
 upipe_status_t upipe_attn_device_status(const void* buf, int32_t* code, void* stream) {
   if (!buf || !code) return UPIPE_ERR_INVALID_ARG;
   int32_t v = 0;
   cudaStream_t st = (cudaStream_t)stream;
-  if (cudaMemcpyAsync(&v, reinterpret_cast<const char*>(buf) + offsetof(TableHeader, error), sizeof(v),
-                      cudaMemcpyDeviceToHost, st) != cudaSuccess)
-    return UPIPE_ERR_CUDA;
-  if (cudaStreamSynchronize(st) != cudaSuccess) return UPIPE_ERR_CUDA;
+  cudaError_t e = cudaMemcpyAsync(&v, reinterpret_cast<const char*>(buf) + offsetof(TableHeader, error), sizeof(v),
+                                  cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_status(e);
   *code = v;
   return UPIPE_OK;
 }

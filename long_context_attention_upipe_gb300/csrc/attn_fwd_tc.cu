@@ -8,12 +8,12 @@
 // contiguous segments a query row sees one interval of keys, so the mask of a partial tile is
 // two integer compares per element.
 //
-// One CTA = one head x two 128-row query tiles (a, b), 10 warps:
+// One CTA = one head x two 128-row query tiles (a, b), 12 warps (warps 2-3 idle):
 //   warp 0     TMA producer: Q_a, Q_b once, then K_j, V_j, K_j+1, ... through a ring of
 //              tile-sized slots; a K slot is freed as soon as both Q K^T products are done
 //   warp 1     MMA issuer (one thread) and TMEM owner: S_t = Q_t K^T (both operands in shared
 //              memory), O_t += P_t V (P_t read from TMEM, V from shared memory)
-//   warps 2-5  softmax of tile a, warps 6-9 softmax of tile b: each thread owns one query row
+//   warps 4-7  softmax of tile a, warps 8-11 softmax of tile b: each thread owns one query row
 //              (TMEM lane 32 * (warp % 4) + lane): row max, exp2, row sum, P written back over
 //              S as bf16, all from one TMEM read of the row
 // TMEM columns: S/P_a [0,128) S/P_b [128,256) O_a [256,256+Dh) O_b [256+Dh, 256+2Dh).
@@ -32,7 +32,7 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr int kFwdThreads = 320;
+constexpr int kFwdThreads = 384;
 constexpr uint32_t kBoxBytes = 128 * 128;  // one TMA box: 128 rows x 64 bf16 (128 B, swizzled)
 
 template <int DH>
@@ -48,10 +48,11 @@ struct FwdLayout {
 
 __device__ __forceinline__ bool in_range(const int4& r, int j) { return j >= r.x && j < r.w; }
 
-// 320 threads x 200 registers = 64,000 of the SM's 65,536: one CTA per SM (it also holds all of
-// TMEM and most of shared memory)
+// Launched with 168 registers per thread (12 warps, 3 per SM sub-partition of 16K registers).
+// The control warpgroup then drops to 56 and the two softmax warpgroups rise to 216: per
+// sub-partition 56 + 216 + 216 = 488 <= 512 per lane, per CTA 62,464 <= 64,512.
 template <int DH, int MODE>
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(kFwdThreads, 1)
     k_attn_fwd_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, AttnArgs a) {
   using L = FwdLayout<DH>;
@@ -104,6 +105,8 @@ __global__ void __maxnreg__(200)
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
+  if (warp < 4) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 56;\n" ::: "memory");
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -188,9 +191,11 @@ __global__ void __maxnreg__(200)
       }
     }
     __syncwarp();
+  }
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 216;\n" ::: "memory");
     // ------------------------------------------------------------------ softmax groups
-    const int t = (warp - 2) >> 2;
+    const int t = (warp - 4) >> 2;
     const int r = 32 * (warp & 3) + lane;  // row within the tile == TMEM lane this warp may access
     const int4 rg = t ? rng1 : rng0;
     if (t == 0 || valid1) {
