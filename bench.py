@@ -270,7 +270,7 @@ def main():
         do = fill((hpc, S, Dh), 13, 1.0)
         o = torch.empty_like(q)
         lse_c = torch.empty(hpc, S, dtype=torch.float32, device=dev)
-        Dt = torch.empty(hpc, S, dtype=torch.float32, device=dev)
+        Dt = torch.empty(2, hpc, -(-S // 128) * 128, dtype=torch.float32, device=dev)
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
         table = torch.empty(up.tile_table_bytes(cdesc), dtype=torch.uint8, device=dev)
         up.build_tile_table(cdesc, seg_t, table, stream)

@@ -137,8 +137,10 @@ upipe_status_t upipe_attn_core_fwd(const upipe_attn_desc_t* desc, const uint16_t
 /* The three kernels of the attention backward, one launch each, in the order the layer runs
  * them.  Arguments as in upipe_attn_core_fwd; dO [Hq, S, Dh] device bf16; lse [Hq, S] from the
  * forward pass.
- *   recompute: o [Hq, S, Dh] bf16 and D [Hq, S] fp32 = rowsum(dO * O), from q, k, v and lse
- *              without online rescaling (activation recompute).
+ *   recompute: o [Hq, S, Dh] bf16 and D, device fp32 [2][Hq][Sp] with Sp = ceil(S/128)*128:
+ *              D[0][h][i] = rowsum(dO * O) of query row i, D[1][h][i] = lse * log2(e), zeros
+ *              for i >= S; from q, k, v and lse without online rescaling (activation
+ *              recompute).  bwd_dq and bwd_dkdv read D in this layout.
  *   bwd_dq   : dq [Hq, S, Dh] bf16 = scale * sum_j P_ij (dP_ij - D_i) k_j,  dP = dO v^T.
  *   bwd_dkdv : dk, dv [Hkv, S, Dh] bf16, summed over the query heads of each KV head:
  *              dv_j = sum P_ij dO_i,  dk_j = scale * sum P_ij (dP_ij - D_i) q_i. */

@@ -159,7 +159,7 @@ def core_bwd(desc: Desc, q, k, v, dO, lse, seg, table, dq, dk, dv, stream=None):
     """recompute -> dq -> dkdv, with O and D in temporary torch buffers."""
     H, S = lse.shape
     o = torch.empty_like(q)
-    D = torch.empty(H, S, dtype=torch.float32, device=q.device)
+    D = torch.empty(2, H, -(-S // 128) * 128, dtype=torch.float32, device=q.device)
     core_recompute(desc, q, k, v, dO, lse, seg, table, o, D, stream)
     core_bwd_dq(desc, q, k, v, dO, lse, D, seg, table, dq, stream)
     core_bwd_dkdv(desc, q, k, v, dO, lse, D, seg, table, dk, dv, stream)

@@ -106,7 +106,7 @@ Plan make_plan(const upipe_attn_desc_t* desc, int pass) {
     if (multi && p.accum == 0) p.yacc = take((size_t)p.S * p.d * sizeof(float));
   } else {
     p.dO = take(p.hpc * head);
-    p.D = take((size_t)p.hpc * p.S * sizeof(float));
+    p.D = take(2 * (size_t)p.hpc * ceil_div(p.S, kTile) * kTile * sizeof(float));
     p.dq = take(p.hpc * head);
     p.dk = take(p.kvc * head);
     p.dv = take(p.kvc * head);

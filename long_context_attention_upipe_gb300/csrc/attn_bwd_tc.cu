@@ -1,0 +1,644 @@
+// Attention backward on the 5th-generation tensor cores (tcgen05, TMEM, TMA).
+//
+// Chain rule of softmax(Q K^T * scale + M) V per head, with P rebuilt from the saved
+// log-sum-exp (activation recompute: podcast summary "Road to 5 Million Tokens", chapter
+// "Activation checkpointing").  The recompute kernel leaves, per query row, D = rowsum(dO * O)
+// and lse*log2e in a padded buffer Dbuf [2][nh][ceil(S/128)*128] (zeros past the end).
+//   dP = dO V^T,  dS = P * (dP - D),  dQ = scale * dS K,  dK = scale * dS^T Q,  dV = P^T dO.
+// Two kernels, both over the skip table's tiles:
+//
+// k_attn_bwd_dq_tc  (one head x two 128-row query tiles per CTA, 12 warps)
+//   warp 0 TMA: Q_t, dO_t once, then K_j through a 2-slot ring and V_j through one slot (V_j is
+//   only read by dP, so its slot is refilled early); warp 1 MMA + TMEM owner; warps 4-7 / 8-11
+//   element-wise for tile a / b, one query row per thread (TMEM lane).
+//   TMEM per tile: a 128-column region that holds S, then dP, then dS (bf16, columns 0-63),
+//   and the dQ accumulator.  Per key tile:  S = Q K^T -> P = exp2(S c - lse2) kept in
+//   registers as bf16 -> region free -> dP = dO V^T -> dS = P (dP - D) written to TMEM ->
+//   dQ += dS K (A operand from TMEM, K in shared memory read MN-major).
+//
+// k_attn_bwd_dkdv_tc  (one KV head x one 128-row key tile per CTA, 12 warps)
+//   warp 0 TMA: K_j, V_j once, then per work item (query head of the group x query tile) Q_i
+//   into a 3-slot ring and dO_i into a 2-slot ring; warp 1 MMA; warps 4-7 and 8-11 take
+//   alternate items, one key row per thread.  TMEM: dK and dV accumulators and two 128-column
+//   regions, one per element-wise group.  Per item:  S^T = K Q^T -> P^T written to TMEM (kept
+//   in registers) -> dV += P^T dO and dP^T = V dO^T into the same region -> dS^T = P^T (dP^T - D)
+//   written to TMEM -> dK += dS^T Q.  Query heads sharing the KV head accumulate in TMEM (GQA
+//   reduction inside the CTA).
+//
+// Every wait is bounded (see tc::mbar_wait); registers are split per role with setmaxnreg
+// (launch 168 x 384; control warpgroup 56, element-wise warpgroups 216).
+#include "internal.h"
+#include "tc_common.cuh"
+
+namespace upipe {
+
+namespace {
+
+constexpr int kThreads = 384;
+constexpr uint32_t kBoxBytes = 128 * 128;  // one TMA box: 128 rows x 64 bf16 (128 B, swizzled)
+
+__device__ __forceinline__ bool in_range(const int4& r, int j) { return j >= r.x && j < r.w; }
+
+// 128 fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld128(uint32_t addr, uint32_t (&v)[128]) {
+  tc::tmem_ld32(addr + 0, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+  tc::tmem_ld32(addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+  tc::tmem_ld32(addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&v[64]));
+  tc::tmem_ld32(addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&v[96]));
+  tc::tmem_ld_wait();
+}
+
+template <int DH>
+__device__ __forceinline__ void mma_nt(uint32_t d, uint32_t abase, uint32_t bbase) {  // D = A B^T, K-major
+  constexpr uint32_t kId = tc::idesc_bf16(128, 128, false, false);
+#pragma unroll
+  for (int k = 0; k < DH / 16; ++k) {
+    const uint32_t off = (k >> 2) * kBoxBytes + (k & 3) * 32;
+    tc::mma_ss(d, tc::sdesc_sw128(abase + off, 16, 1024), tc::sdesc_sw128(bbase + off, 16, 1024), kId, k > 0);
+  }
+}
+
+template <int DH>
+__device__ __forceinline__ void mma_acc(uint32_t d, uint32_t a_tmem, uint32_t bbase, bool acc) {  // D (+)= A[tmem] B
+  constexpr uint32_t kId = tc::idesc_bf16(128, DH, false, true);  // B [128 rows x Dh] read MN-major
+#pragma unroll
+  for (int k = 0; k < 128 / 16; ++k)
+    tc::mma_ts(d, a_tmem + k * 8, tc::sdesc_sw128(bbase + k * 2048, kBoxBytes, 1024), kId, acc || k > 0);
+}
+
+// dS = P (dP - D) for 64 packed P pairs, dP in the region, result written over columns [0, 64):
+// half h reads dP columns [64h, 64h + 64) and writes [32h, 32h + 32), already read.
+template <typename DFn>
+__device__ __forceinline__ void ds_pass(uint32_t r_addr, const uint32_t (&pk)[64], DFn dval) {
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf) {
+    uint32_t v0[32], v1[32], o[32];
+    tc::tmem_ld32(r_addr + hf * 64, v0);
+    tc::tmem_ld32(r_addr + hf * 64 + 32, v1);
+    tc::tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int k0 = hf * 64 + 2 * i, k1 = hf * 64 + 32 + 2 * i;
+      const float2 d0 = dval(k0), d1 = dval(k1);
+      const __nv_bfloat162 pa = *reinterpret_cast<const __nv_bfloat162*>(&pk[hf * 32 + i]);
+      const __nv_bfloat162 pb = *reinterpret_cast<const __nv_bfloat162*>(&pk[hf * 32 + 16 + i]);
+      o[i] = tc::pack_bf16x2(__low2float(pa) * (__uint_as_float(v0[2 * i]) - d0.x),
+                             __high2float(pa) * (__uint_as_float(v0[2 * i + 1]) - d0.y));
+      o[16 + i] = tc::pack_bf16x2(__low2float(pb) * (__uint_as_float(v1[2 * i]) - d1.x),
+                                  __high2float(pb) * (__uint_as_float(v1[2 * i + 1]) - d1.y));
+    }
+    tc::tmem_st32(r_addr + hf * 32, o);
+  }
+  tc::tmem_st_wait();
+}
+
+// ================================================================================================
+// dQ
+// ================================================================================================
+template <int DH>
+struct DqLayout {
+  static constexpr uint32_t TB = 128 * DH * 2;
+  static constexpr uint32_t Q = 0, DO = 2 * TB, KR = 4 * TB, VR = 6 * TB, BAR = 7 * TB;  // K ring 2, V 1
+  static constexpr uint32_t BYTES = BAR + 256;
+  static constexpr uint32_t TMEM_COLS = 512;
+  __device__ static constexpr uint32_t r_col(int t) { return t * 128; }        // S / dP / dS
+  __device__ static constexpr uint32_t q_col(int t) { return 256 + t * 128; }  // dQ accumulator
+};
+
+template <int DH>
+__global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dq_tc(const __grid_constant__ CUtensorMap tq,
+                                                                const __grid_constant__ CUtensorMap tdo,
+                                                                const __grid_constant__ CUtensorMap tk,
+                                                                const __grid_constant__ CUtensorMap tv,
+                                                                AttnBwdArgs b) {
+  using L = DqLayout<DH>;
+  const AttnArgs& a = b.f;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR);
+  uint64_t* q_full = bars + 0;
+  uint64_t* s_full = bars + 1;    // [2] S ready in the region
+  uint64_t* s_free = bars + 3;    // [2] S consumed (P in registers)
+  uint64_t* dp_full = bars + 5;   // [2]
+  uint64_t* ds_full = bars + 7;   // [2]
+  uint64_t* dq_full = bars + 9;   // [2]
+  uint64_t* k_full = bars + 11;   // [2]
+  uint64_t* k_empty = bars + 13;  // [2]
+  uint64_t* v_full = bars + 15;
+  uint64_t* v_empty = bars + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 17);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 18);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t S = a.S;
+  const int nt = (int)ceil_div(S, kTile);
+  const int64_t sp = (int64_t)nt * kTile;
+  const int pair = gridDim.x - 1 - blockIdx.x;
+  const int h = blockIdx.y;
+  const int kvh = h / a.g;
+  const int qt0 = 2 * pair, qt1 = 2 * pair + 1;
+  const bool valid1 = qt1 < nt;
+  const int4 rng0 = a.q_rows[qt0];
+  const int4 rng1 = valid1 ? a.q_rows[qt1] : make_int4(0, 0, 0, 0);
+  const int j0 = valid1 ? min(rng0.x, rng1.x) : rng0.x;
+  const int j1 = valid1 ? max(rng0.w, rng1.w) : rng0.w;
+
+  if (threadIdx.x == 0) {
+    tc::mbar_init(q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&s_full[i], 1);
+      tc::mbar_init(&s_free[i], 128);
+      tc::mbar_init(&dp_full[i], 1);
+      tc::mbar_init(&ds_full[i], 128);
+      tc::mbar_init(&dq_full[i], 1);
+      tc::mbar_init(&k_full[i], 1);
+      tc::mbar_init(&k_empty[i], 1);
+    }
+    tc::mbar_init(v_full, 1);
+    tc::mbar_init(v_empty, 1);
+    *abort_flag = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tmem_slot, L::TMEM_COLS);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;\n" ::: "memory");
+    if (warp == 0) {
+      if (lane == 0) {
+        tc::prefetch_tmap(&tq);
+        tc::prefetch_tmap(&tdo);
+        tc::prefetch_tmap(&tk);
+        tc::prefetch_tmap(&tv);
+        tc::mbar_arrive_expect_tx(q_full, (valid1 ? 4 : 2) * L::TB);
+        for (int at = 0; at < DH / 64; ++at) {
+          tc::tma_load_3d(smem + L::Q + at * kBoxBytes, &tq, q_full, at * 64, qt0 * kTile, h);
+          tc::tma_load_3d(smem + L::DO + at * kBoxBytes, &tdo, q_full, at * 64, qt0 * kTile, h);
+          if (valid1) {
+            tc::tma_load_3d(smem + L::Q + L::TB + at * kBoxBytes, &tq, q_full, at * 64, qt1 * kTile, h);
+            tc::tma_load_3d(smem + L::DO + L::TB + at * kBoxBytes, &tdo, q_full, at * 64, qt1 * kTile, h);
+          }
+        }
+        for (int j = j0, n = 0; j < j1; ++j, ++n) {
+          // K_j into K slot n % 2 once K_{j-2} is released; V_j into the V slot once dP of V_{j-1} is done
+          if (n >= 2 && !tc::mbar_wait(&k_empty[n & 1], ((n >> 1) - 1) & 1, abort_flag, a.err)) break;
+          tc::mbar_arrive_expect_tx(&k_full[n & 1], L::TB);
+          for (int at = 0; at < DH / 64; ++at)
+            tc::tma_load_3d(smem + L::KR + (n & 1) * L::TB + at * kBoxBytes, &tk, &k_full[n & 1], at * 64, j * kTile, kvh);
+          if (n >= 1 && !tc::mbar_wait(v_empty, (n - 1) & 1, abort_flag, a.err)) break;
+          tc::mbar_arrive_expect_tx(v_full, L::TB);
+          for (int at = 0; at < DH / 64; ++at)
+            tc::tma_load_3d(smem + L::VR + at * kBoxBytes, &tv, v_full, at * 64, j * kTile, kvh);
+        }
+      }
+      __syncwarp();
+    } else if (warp == 1) {
+      if (lane == 0) {
+        const uint32_t sQ = smem_u32(smem + L::Q), sDO = smem_u32(smem + L::DO);
+        const uint32_t sK = smem_u32(smem + L::KR), sV = smem_u32(smem + L::VR);
+        bool ok = tc::mbar_wait(q_full, 0, abort_flag, a.err);
+        const int4 rng[2] = {rng0, rng1};
+        int cnt[2] = {0, 0};
+        bool first[2] = {true, true};
+        if (ok) {
+          ok = tc::mbar_wait(&k_full[0], 0, abort_flag, a.err);
+          tc::fence_after_sync();
+          for (int t = 0; t < 2 && ok; ++t)
+            if (in_range(rng[t], j0)) {
+              mma_nt<DH>(tmem + L::r_col(t), sQ + t * L::TB, sK);
+              tc::mma_commit(&s_full[t]);
+            }
+        }
+        for (int j = j0, n = 0; ok && j < j1; ++j, ++n) {
+          const uint32_t kb = sK + (n & 1) * L::TB;
+          ok = tc::mbar_wait(v_full, n & 1, abort_flag, a.err);  // V_j
+          if (!ok) break;
+          tc::fence_after_sync();
+          for (int t = 0; t < 2 && ok; ++t)
+            if (in_range(rng[t], j)) {
+              ok = tc::mbar_wait(&s_free[t], cnt[t] & 1, abort_flag, a.err);
+              if (!ok) break;
+              tc::fence_after_sync();
+              mma_nt<DH>(tmem + L::r_col(t), sDO + t * L::TB, sV);  // dP = dO V^T
+              tc::mma_commit(&dp_full[t]);
+            }
+          if (!ok) break;
+          tc::mma_commit(v_empty);
+          if (j + 1 < j1) {
+            ok = tc::mbar_wait(&k_full[(n + 1) & 1], ((n + 1) >> 1) & 1, abort_flag, a.err);  // K_j+1
+            tc::fence_after_sync();
+          }
+          for (int t = 0; t < 2 && ok; ++t) {
+            if (in_range(rng[t], j)) {
+              ok = tc::mbar_wait(&ds_full[t], cnt[t] & 1, abort_flag, a.err);
+              if (!ok) break;
+              ++cnt[t];
+              tc::fence_after_sync();
+              mma_acc<DH>(tmem + L::q_col(t), tmem + L::r_col(t), kb, !first[t]);  // dQ += dS K_j
+              first[t] = false;
+              if (j == rng[t].w - 1) tc::mma_commit(&dq_full[t]);
+            }
+            if (in_range(rng[t], j + 1)) {
+              mma_nt<DH>(tmem + L::r_col(t), sQ + t * L::TB, sK + ((n + 1) & 1) * L::TB);
+              tc::mma_commit(&s_full[t]);
+            }
+          }
+          if (ok) tc::mma_commit(&k_empty[n & 1]);
+        }
+      }
+      __syncwarp();
+    }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 216;\n" ::: "memory");
+    const int t = (warp - 4) >> 2;
+    const int r = 32 * (warp & 3) + lane;
+    const int4 rg = t ? rng1 : rng0;
+    if (t == 0 || valid1) {
+      const int64_t row = (int64_t)(t ? qt1 : qt0) * kTile + r;
+      const bool row_ok = row < S;
+      int64_t vis_lo = 0, vis_hi = -1;
+      if (row_ok) {
+        vis_lo = seg_first(a.seg, row);
+        vis_hi = a.causal ? row : seg_last(a.seg, S, row);
+      }
+      const float Dr = a.D[(int64_t)h * sp + row];
+      const float lse2 = a.D[((int64_t)a.nh + h) * sp + row];
+      const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+      const uint32_t r_addr = lane_addr + L::r_col(t), q_addr = lane_addr + L::q_col(t);
+      const float c = a.scale * 1.4426950408889634f;
+      const bool ragged = (S % kTile) != 0;
+      bool ok = true;
+      int cnt = 0;
+      for (int j = rg.x; j < rg.w; ++j, ++cnt) {
+        const bool partial = j < rg.y || j >= rg.z || (ragged && j == nt - 1);
+        ok = tc::mbar_wait(&s_full[t], cnt & 1, abort_flag, a.err);
+        if (!ok) break;
+        tc::fence_after_sync();
+        uint32_t pk[64];  // P as bf16 pairs
+        {
+          uint32_t sv[128];
+          tmem_ld128(r_addr, sv);
+          int lo = 0, hi = 127;
+          if (partial) {
+            const int64_t col0 = (int64_t)j * kTile;
+            lo = (int)max((int64_t)-1, min(vis_lo - col0, (int64_t)128));
+            hi = (int)max((int64_t)-1, min(vis_hi - col0, (int64_t)128));
+          }
+#pragma unroll
+          for (int i = 0; i < 64; ++i) {
+            float p0 = fast_exp2(fmaf(__uint_as_float(sv[2 * i]), c, -lse2));
+            float p1 = fast_exp2(fmaf(__uint_as_float(sv[2 * i + 1]), c, -lse2));
+            if (partial) {
+              if (2 * i < lo || 2 * i > hi) p0 = 0.f;
+              if (2 * i + 1 < lo || 2 * i + 1 > hi) p1 = 0.f;
+            }
+            pk[i] = tc::pack_bf16x2(p0, p1);
+          }
+        }
+        tc::fence_before_sync();
+        tc::mbar_arrive(&s_free[t]);
+        ok = tc::mbar_wait(&dp_full[t], cnt & 1, abort_flag, a.err);
+        if (!ok) break;
+        tc::fence_after_sync();
+        ds_pass(r_addr, pk, [&](int) { return make_float2(Dr, Dr); });
+        tc::fence_before_sync();
+        tc::mbar_arrive(&ds_full[t]);
+      }
+      if (ok) ok = tc::mbar_wait(&dq_full[t], 0, abort_flag, a.err);
+      tc::fence_after_sync();
+      bf16* dqrow = b.dq + ((int64_t)h * S + (row_ok ? row : 0)) * DH;
+#pragma unroll
+      for (int ch = 0; ch < DH / 32; ++ch) {
+        uint32_t v[32];
+        tc::tmem_ld32(q_addr + ch * 32, v);
+        tc::tmem_ld_wait();
+        if (ok && row_ok) {
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint4 pkt;
+            uint32_t* pw = reinterpret_cast<uint32_t*>(&pkt);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              pw[i] = tc::pack_bf16x2(__uint_as_float(v[q4 * 8 + 2 * i]) * a.scale,
+                                      __uint_as_float(v[q4 * 8 + 2 * i + 1]) * a.scale);
+            *reinterpret_cast<uint4*>(dqrow + ch * 32 + q4 * 8) = pkt;
+          }
+        }
+      }
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, L::TMEM_COLS);
+  }
+}
+
+// ================================================================================================
+// dK, dV
+// ================================================================================================
+template <int DH>
+struct DkvLayout {
+  static constexpr uint32_t TB = 128 * DH * 2;
+  static constexpr int NQ = 3, NO = 2;  // Q ring, dO ring
+  static constexpr uint32_t K = 0, V = TB, QR = 2 * TB, OR = QR + NQ * TB, BAR = OR + NO * TB;
+  static constexpr uint32_t BYTES = BAR + 256;
+  static constexpr uint32_t TMEM_COLS = 512;
+  __device__ static constexpr uint32_t r_col(int t) { return t * 128; }  // S^T / P^T / dP^T / dS^T
+  static constexpr uint32_t DK_COL = 256, DV_COL = 384;
+};
+
+template <int DH>
+__global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tq,
+                                                                  const __grid_constant__ CUtensorMap tdo,
+                                                                  const __grid_constant__ CUtensorMap tk,
+                                                                  const __grid_constant__ CUtensorMap tv,
+                                                                  AttnBwdArgs b) {
+  using L = DkvLayout<DH>;
+  constexpr int NQ = L::NQ, NO = L::NO;
+  const AttnArgs& a = b.f;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR);
+  uint64_t* kv_full = bars + 0;
+  uint64_t* s_full = bars + 1;    // [2] per region
+  uint64_t* p_full = bars + 3;    // [2]
+  uint64_t* dp_full = bars + 5;   // [2]
+  uint64_t* ds_full = bars + 7;   // [2]
+  uint64_t* acc_full = bars + 9;
+  uint64_t* q_full = bars + 10;   // [NQ]
+  uint64_t* q_empty = bars + 13;  // [NQ]
+  uint64_t* o_full = bars + 16;   // [NO]
+  uint64_t* o_empty = bars + 18;  // [NO]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 21);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t S = a.S;
+  const int nt = (int)ceil_div(S, kTile);
+  const int64_t sp = (int64_t)nt * kTile;
+  const int jt = blockIdx.x;  // key tile (small j has the most query tiles under causality)
+  const int kvh = blockIdx.y;
+  const int4 tr = a.kv_rows[jt];  // query tiles {begin, full_begin, full_end, end}
+  const int h_first = kvh * a.g;
+  const int n_heads = max(0, min(a.nh, h_first + a.g) - h_first);
+  const int nq = tr.w - tr.x;
+  const int n_items = n_heads * nq;
+
+  if (threadIdx.x == 0) {
+    tc::mbar_init(kv_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&s_full[i], 1);
+      tc::mbar_init(&p_full[i], 128);
+      tc::mbar_init(&dp_full[i], 1);
+      tc::mbar_init(&ds_full[i], 128);
+    }
+    tc::mbar_init(acc_full, 1);
+    for (int i = 0; i < NQ; ++i) {
+      tc::mbar_init(&q_full[i], 1);
+      tc::mbar_init(&q_empty[i], 1);
+    }
+    for (int i = 0; i < NO; ++i) {
+      tc::mbar_init(&o_full[i], 1);
+      tc::mbar_init(&o_empty[i], 1);
+    }
+    *abort_flag = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tmem_slot, L::TMEM_COLS);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;\n" ::: "memory");
+    if (warp == 0) {
+      if (lane == 0) {
+        tc::prefetch_tmap(&tq);
+        tc::prefetch_tmap(&tdo);
+        tc::mbar_arrive_expect_tx(kv_full, 2 * L::TB);
+        for (int at = 0; at < DH / 64; ++at) {
+          tc::tma_load_3d(smem + L::K + at * kBoxBytes, &tk, kv_full, at * 64, jt * kTile, kvh);
+          tc::tma_load_3d(smem + L::V + at * kBoxBytes, &tv, kv_full, at * 64, jt * kTile, kvh);
+        }
+        for (int n = 0; n < n_items; ++n) {
+          const int hh = h_first + n / nq;
+          const int qi = tr.x + n % nq;
+          const int sq = n % NQ, so = n % NO;
+          if (n >= NQ && !tc::mbar_wait(&q_empty[sq], ((n / NQ) - 1) & 1, abort_flag, a.err)) break;
+          tc::mbar_arrive_expect_tx(&q_full[sq], L::TB);
+          for (int at = 0; at < DH / 64; ++at)
+            tc::tma_load_3d(smem + L::QR + sq * L::TB + at * kBoxBytes, &tq, &q_full[sq], at * 64, qi * kTile, hh);
+          if (n >= NO && !tc::mbar_wait(&o_empty[so], ((n / NO) - 1) & 1, abort_flag, a.err)) break;
+          tc::mbar_arrive_expect_tx(&o_full[so], L::TB);
+          for (int at = 0; at < DH / 64; ++at)
+            tc::tma_load_3d(smem + L::OR + so * L::TB + at * kBoxBytes, &tdo, &o_full[so], at * 64, qi * kTile, hh);
+        }
+      }
+      __syncwarp();
+    } else if (warp == 1) {
+      if (lane == 0) {
+        const uint32_t sK = smem_u32(smem + L::K), sV = smem_u32(smem + L::V);
+        const uint32_t sQ = smem_u32(smem + L::QR), sO = smem_u32(smem + L::OR);
+        bool ok = tc::mbar_wait(kv_full, 0, abort_flag, a.err);
+        auto issue_st = [&](int n) {  // S^T of item n into region n % 2
+          if (ok) ok = tc::mbar_wait(&q_full[n % NQ], (n / NQ) & 1, abort_flag, a.err);
+          if (!ok) return;
+          tc::fence_after_sync();
+          mma_nt<DH>(tmem + L::r_col(n & 1), sK, sQ + (n % NQ) * L::TB);
+          tc::mma_commit(&s_full[n & 1]);
+        };
+        for (int n = 0; n < 2 && n < n_items; ++n) issue_st(n);
+        for (int n = 0; ok && n < n_items; ++n) {
+          const int rr = n & 1;
+          const uint32_t qb = sQ + (n % NQ) * L::TB, ob = sO + (n % NO) * L::TB;
+          ok = tc::mbar_wait(&p_full[rr], (n >> 1) & 1, abort_flag, a.err);
+          if (ok) ok = tc::mbar_wait(&o_full[n % NO], (n / NO) & 1, abort_flag, a.err);
+          if (!ok) break;
+          tc::fence_after_sync();
+          mma_acc<DH>(tmem + L::DV_COL, tmem + L::r_col(rr), ob, n > 0);  // dV += P^T dO
+          mma_nt<DH>(tmem + L::r_col(rr), sV, ob);                         // dP^T = V dO^T
+          tc::mma_commit(&dp_full[rr]);
+          tc::mma_commit(&o_empty[n % NO]);
+          ok = tc::mbar_wait(&ds_full[rr], (n >> 1) & 1, abort_flag, a.err);
+          if (!ok) break;
+          tc::fence_after_sync();
+          mma_acc<DH>(tmem + L::DK_COL, tmem + L::r_col(rr), qb, n > 0);   // dK += dS^T Q
+          tc::mma_commit(&q_empty[n % NQ]);
+          if (n == n_items - 1) tc::mma_commit(acc_full);
+          if (n + 2 < n_items) issue_st(n + 2);
+        }
+      }
+      __syncwarp();
+    }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 216;\n" ::: "memory");
+    const int grp = (warp - 4) >> 2;       // element-wise group: items n with n % 2 == grp
+    const int r = 32 * (warp & 3) + lane;  // key row within the tile == TMEM lane
+    const int64_t krow = (int64_t)jt * kTile + r;
+    const bool k_ok = krow < S;
+    // the queries that see this key: [vis_lo, vis_hi]
+    int64_t vis_lo = 0, vis_hi = -1;
+    if (k_ok) {
+      vis_lo = a.causal ? krow : seg_first(a.seg, krow);
+      vis_hi = seg_last(a.seg, S, krow);
+    }
+    const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    const uint32_t r_addr = lane_addr + L::r_col(grp);
+    const float c = a.scale * 1.4426950408889634f;
+    const bool ragged = (S % kTile) != 0;
+    bool ok = true;
+    for (int n = grp; n < n_items; n += 2) {
+      const int hh = h_first + n / nq;
+      const int qi = tr.x + n % nq;
+      const bool partial = qi < tr.y || qi >= tr.z || (ragged && (qi == nt - 1 || jt == nt - 1));
+      const float* dq_d = a.D + (int64_t)hh * sp + (int64_t)qi * kTile;              // D of the 128 queries
+      const float* dq_l = a.D + ((int64_t)a.nh + hh) * sp + (int64_t)qi * kTile;     // lse*log2e
+      const int cyc = (n >> 1) & 1;
+      int lo = 0, hi = 127;
+      if (partial) {
+        const int64_t col0 = (int64_t)qi * kTile;
+        lo = (int)max((int64_t)-1, min(vis_lo - col0, (int64_t)128));
+        hi = (int)max((int64_t)-1, min(vis_hi - col0, (int64_t)128));
+      }
+      ok = tc::mbar_wait(&s_full[grp], cyc, abort_flag, a.err);
+      if (!ok) break;
+      tc::fence_after_sync();
+      uint32_t pk[64];  // P^T as bf16 pairs
+      {
+        uint32_t sv[128];
+        tmem_ld128(r_addr, sv);
+#pragma unroll
+        for (int i = 0; i < 64; i += 2) {
+          const float4 l4 = __ldg(reinterpret_cast<const float4*>(dq_l + 2 * i));
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int k = 2 * (i + u);
+            float p0 = fast_exp2(fmaf(__uint_as_float(sv[k]), c, -(u ? l4.z : l4.x)));
+            float p1 = fast_exp2(fmaf(__uint_as_float(sv[k + 1]), c, -(u ? l4.w : l4.y)));
+            if (partial) {
+              if (k < lo || k > hi) p0 = 0.f;
+              if (k + 1 < lo || k + 1 > hi) p1 = 0.f;
+            }
+            pk[i + u] = tc::pack_bf16x2(p0, p1);
+          }
+        }
+      }
+      tc::tmem_st32(r_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+      tc::tmem_st32(r_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+      tc::tmem_st_wait();
+      tc::fence_before_sync();
+      tc::mbar_arrive(&p_full[grp]);
+      ok = tc::mbar_wait(&dp_full[grp], cyc, abort_flag, a.err);
+      if (!ok) break;
+      tc::fence_after_sync();
+      ds_pass(r_addr, pk, [&](int k) { return __ldg(reinterpret_cast<const float2*>(dq_d + k)); });
+      tc::fence_before_sync();
+      tc::mbar_arrive(&ds_full[grp]);
+    }
+    // epilogue: group 0 writes dK rows (scaled), group 1 writes dV rows
+    if (ok && n_items > 0) ok = tc::mbar_wait(acc_full, 0, abort_flag, a.err);
+    tc::fence_after_sync();
+    const uint32_t acc_addr = lane_addr + (grp == 0 ? L::DK_COL : L::DV_COL);
+    const float mul = grp == 0 ? a.scale : 1.f;
+    const int64_t off = ((int64_t)kvh * S + (k_ok ? krow : 0)) * DH;
+#pragma unroll
+    for (int ch = 0; ch < DH / 32; ++ch) {
+      uint32_t v[32];
+      tc::tmem_ld32(acc_addr + ch * 32, v);
+      tc::tmem_ld_wait();
+      if (n_items == 0) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = 0u;
+      }
+      if (ok && k_ok) {
+        if (b.acc_kv) {
+          float* dst = (grp == 0 ? b.dk_acc : b.dv_acc) + off + ch * 32;
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4) {
+            float4 o4 = *reinterpret_cast<float4*>(dst + q4 * 4);
+            o4.x += __uint_as_float(v[q4 * 4 + 0]) * mul;
+            o4.y += __uint_as_float(v[q4 * 4 + 1]) * mul;
+            o4.z += __uint_as_float(v[q4 * 4 + 2]) * mul;
+            o4.w += __uint_as_float(v[q4 * 4 + 3]) * mul;
+            *reinterpret_cast<float4*>(dst + q4 * 4) = o4;
+          }
+        } else {
+          bf16* dst = (grp == 0 ? b.dk : b.dv) + off + ch * 32;
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint4 pkt;
+            uint32_t* pw = reinterpret_cast<uint32_t*>(&pkt);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              pw[i] = tc::pack_bf16x2(__uint_as_float(v[q4 * 8 + 2 * i]) * mul, __uint_as_float(v[q4 * 8 + 2 * i + 1]) * mul);
+            *reinterpret_cast<uint4*>(dst + q4 * 8) = pkt;
+          }
+        }
+      }
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, L::TMEM_COLS);
+  }
+}
+
+template <int DH>
+bool make_maps(const AttnArgs& a, CUtensorMap* tq, CUtensorMap* tdo, CUtensorMap* tk, CUtensorMap* tv) {
+  return make_tmap_3d_bf16(tq, a.q, DH, a.S, a.nh, 64, 128) && make_tmap_3d_bf16(tdo, a.dO, DH, a.S, a.nh, 64, 128) &&
+         make_tmap_3d_bf16(tk, a.k, DH, a.S, a.nkv, 64, 128) && make_tmap_3d_bf16(tv, a.v, DH, a.S, a.nkv, 64, 128);
+}
+
+template <typename KFN>
+cudaError_t launch(KFN kfn, size_t bytes, dim3 grid, const CUtensorMap& tq, const CUtensorMap& tdo,
+                   const CUtensorMap& tk, const CUtensorMap& tv, const AttnBwdArgs& b, cudaStream_t st) {
+  // at least 120 KB so that two CTAs never share an SM (each takes all 512 TMEM columns)
+  const size_t smem = bytes + 1024 > 120 * 1024 ? bytes + 1024 : 120 * 1024;
+  cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kfn<<<grid, kThreads, smem, st>>>(tq, tdo, tk, tv, b);
+  return cudaGetLastError();
+}
+
+template <int DH>
+cudaError_t run_dq(const AttnBwdArgs& b, cudaStream_t st) {
+  CUtensorMap tq, tdo, tk, tv;
+  if (!make_maps<DH>(b.f, &tq, &tdo, &tk, &tv)) return cudaErrorInvalidValue;
+  const int nt = (int)ceil_div(b.f.S, kTile);
+  return launch(k_attn_bwd_dq_tc<DH>, DqLayout<DH>::BYTES, dim3((unsigned)ceil_div(nt, 2), (unsigned)b.f.nh), tq,
+                tdo, tk, tv, b, st);
+}
+
+template <int DH>
+cudaError_t run_dkdv(const AttnBwdArgs& b, cudaStream_t st) {
+  CUtensorMap tq, tdo, tk, tv;
+  if (!make_maps<DH>(b.f, &tq, &tdo, &tk, &tv)) return cudaErrorInvalidValue;
+  const int nt = (int)ceil_div(b.f.S, kTile);
+  return launch(k_attn_bwd_dkdv_tc<DH>, DkvLayout<DH>::BYTES, dim3((unsigned)nt, (unsigned)b.nkv), tq, tdo, tk, tv,
+                b, st);
+}
+
+}  // namespace
+
+cudaError_t launch_attn_bwd_dq(const AttnBwdArgs& b, int head_dim, cudaStream_t st) {
+  return head_dim == 64 ? run_dq<64>(b, st) : run_dq<128>(b, st);
+}
+cudaError_t launch_attn_bwd_dkdv(const AttnBwdArgs& b, int head_dim, cudaStream_t st) {
+  return head_dim == 64 ? run_dkdv<64>(b, st) : run_dkdv<128>(b, st);
+}
+
+}  // namespace upipe

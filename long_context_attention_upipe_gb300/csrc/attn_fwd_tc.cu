@@ -316,11 +316,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           }
         }
       }
-      if (ok && row_ok) {
-        if (MODE == 0)
-          a.lse[(int64_t)h * S + row] = l > 0.f ? (m_used + log2f(l)) * kLn2 : -INFINITY;
-        else
-          a.D[(int64_t)h * S + row] = dsum;
+      if (MODE == 0) {
+        if (ok && row_ok) a.lse[(int64_t)h * S + row] = l > 0.f ? (m_used + log2f(l)) * kLn2 : -INFINITY;
+      } else if (ok) {
+        // padded [2][nh][nt*128]: D, then lse*log2e; zeros past the end of the sequence
+        const int64_t sp = (int64_t)nt * kTile;
+        a.D[(int64_t)h * sp + row] = row_ok ? dsum : 0.f;
+        a.D[((int64_t)a.nh + h) * sp + row] = row_ok ? m_used : 0.f;
       }
     }
   }

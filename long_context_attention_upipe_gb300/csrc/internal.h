@@ -72,7 +72,8 @@ struct AttnArgs {
   bf16* o;          // [nh, S, Dh]
   float* lse;       // [nh] rows of stride S: natural-log normaliser (written in fwd, read in bwd)
   const bf16* dO;   // [nh, S, Dh]   (recompute mode and backward)
-  float* D;         // [nh, S]       rowsum(dO * O) (recompute mode writes, backward reads)
+  float* D;         // [2][nh][ceil(S/128)*128]: rowsum(dO * O), then lse*log2e; zero past S
+                    // (recompute mode writes, backward reads)
   const int32_t* seg;
   const int4* q_rows;   // q-major skip table
   const int4* kv_rows;  // kv-major skip table
