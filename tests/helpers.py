@@ -22,6 +22,21 @@ def max_abs(got, want):
     return float(np.max(np.abs(np.asarray(got, np.float64) - np.asarray(want, np.float64)))) if np.size(want) else 0.0
 
 
+def bf16_half_ulp(x):
+    """Half a bf16 ulp at |x|: the rounding error any bf16 output of value x may carry."""
+    ax = np.abs(np.asarray(x, np.float64))
+    e = np.floor(np.log2(np.maximum(ax, 2.0 ** -126)))
+    return np.exp2(e - 8)
+
+
+def max_abs_bf16_out(got, want):
+    """Max error of a bf16 output beyond its own final rounding: max(|got - want| - ulp/2)."""
+    if not np.size(want):
+        return 0.0
+    err = np.abs(np.asarray(got, np.float64) - np.asarray(want, np.float64)) - bf16_half_ulp(want)
+    return float(max(0.0, err.max()))
+
+
 def to_f64(t: torch.Tensor) -> np.ndarray:
     return t.detach().float().cpu().double().numpy() if t.dtype == torch.bfloat16 else t.detach().cpu().double().numpy()
 

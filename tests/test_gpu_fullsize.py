@@ -1,0 +1,96 @@
+"""Parity at the full workload sizes, in the launch configuration the benchmark times.
+
+Forward: sampled query rows (first, tile-boundary and last rows) checked against the oracle,
+which projects only the rows it needs.  Backward: dY is zero outside the first P rows; by
+causality every gradient then equals the oracle's on the first P tokens (same mask, segments
+truncated) and dX rows >= P are exactly zero.  Inputs are generated on the device with the same
+counter-based generator the host uses for the oracle (checked bit for bit below)."""
+import numpy as np
+import pytest
+import torch
+
+import long_context_attention_upipe_gb300 as up
+import oracle as orc
+import upipe_inputs as ui
+from helpers import GRAD_REL_FRO, OUT_MAX_ABS, OUT_REL_FRO, bf16_tensor, max_abs, max_abs_bf16_out, rel_fro, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from long_context_attention_upipe_gb300 import _build
+    _build.build()
+    ui.build(device=True)
+
+
+def dev_fill(shape, tid, std):
+    t = torch.empty(shape, dtype=torch.bfloat16, device="cuda")
+    ui.fill_device_bf16(t.data_ptr(), t.numel(), tid, std, stream=torch.cuda.current_stream().cuda_stream)
+    return t
+
+
+def test_device_generator_matches_host_bit_for_bit():
+    n = 1 << 20
+    for tid, std, first in ((ui.TID_X, 1.0, 0), (ui.TID_WQKV, ui.W_STD, 12345), (ui.TID_DY, 1.0, 7 << 30)):
+        t = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+        ui.fill_device_bf16(t.data_ptr(), n, tid, std, first=first)
+        torch.cuda.synchronize()
+        got = t.cpu().view(torch.int16).numpy().view(np.uint16)
+        np.testing.assert_array_equal(got, ui.normal_bf16(n, tid, std, first=first))
+
+
+def run_layer(w, hpc, prefix):
+    S, d, Hq, Hkv, Dh = w.S, w.d, w.Hq, w.Hkv, w.Dh
+    X = dev_fill((S, d), ui.TID_X, 1.0)
+    W = dev_fill(((Hq + 2 * Hkv) * Dh, d), ui.TID_WQKV, ui.W_STD)
+    Wo = dev_fill((d, Hq * Dh), ui.TID_WO, ui.W_STD)
+    dY = torch.zeros((S, d), dtype=torch.bfloat16, device="cuda")
+    ui.fill_device_bf16(dY.data_ptr(), prefix * d, ui.TID_DY, 1.0)   # rows [0, prefix) only
+    seg = w.segments()
+    seg_t = torch.from_numpy(seg).cuda() if seg is not None else None
+    layer = up.Layer(up.make_desc(S, d, Hq, Hkv, Dh, hpc, w.causal))
+    Y, lse = layer.forward(X, W, Wo, seg_t)
+    dX, dW, dWo = layer.backward(X, W, Wo, seg_t, dY, lse)
+    torch.cuda.synchronize()
+    assert up.device_status(layer.ws_fwd) == 0 and up.device_status(layer.ws_bwd) == 0
+    return seg, Y, lse, dX, dW, dWo
+
+
+def host_inputs(w, rows_needed, prefix):
+    d, Hq, Hkv, Dh = w.d, w.Hq, w.Hkv, w.Dh
+    Xr = ui.normal_bf16_rows(rows_needed, d, ui.TID_X)
+    W = ui.normal_bf16((Hq + 2 * Hkv) * Dh * d, ui.TID_WQKV, ui.W_STD).reshape(-1, d)
+    Wo = ui.normal_bf16(d * Hq * Dh, ui.TID_WO, ui.W_STD).reshape(d, -1)
+    dYp = ui.normal_bf16(prefix * d, ui.TID_DY).reshape(prefix, d)
+    return Xr, W, Wo, dYp
+
+
+@pytest.mark.parametrize("key,hpc,prefix", [("llama8b_32k", 8, 1024), ("packed_131k", 8, 2048)])
+def test_full_size_layer(key, hpc, prefix):
+    w = ui.workload(key)
+    S = w.S
+    seg, Y, lse, dX, dW, dWo = run_layer(w, hpc, prefix)
+    rows = np.array(sorted({0, 1, 127, 128, 129, 1000, S // 2 - 1, S // 2, S - 129, S - 128, S - 2, S - 1}))
+    # keys any sampled row can see: from the start of its segment to itself
+    if seg is None:
+        key_index = np.arange(0, rows.max() + 1)
+    else:
+        key_index = np.unique(np.concatenate(
+            [np.arange(int(np.searchsorted(seg, seg[r], side="left")), r + 1) for r in rows]))
+    Xk, W, Wo, dYp = host_inputs(w, key_index, prefix)
+    Xr = Xk[np.searchsorted(key_index, rows)]
+    Y_ref, L_ref = orc.layer_forward_rows(Xr, Xk, key_index, rows, W, Wo, seg, w.Hq, w.Hkv, w.Dh, w.causal)
+    y = to_f64(Y)[rows]
+    assert max_abs_bf16_out(y, Y_ref) <= OUT_MAX_ABS, max_abs_bf16_out(y, Y_ref)
+    assert rel_fro(y, Y_ref) <= OUT_REL_FRO, rel_fro(y, Y_ref)
+    assert max_abs(to_f64(lse)[:, rows], L_ref) <= 1e-3
+    # backward on the prefix
+    Xp = ui.normal_bf16_rows(np.arange(prefix), w.d, ui.TID_X)
+    segp = None if seg is None else seg[:prefix]
+    dX_ref, dW_ref, dWo_ref = orc.layer_backward(Xp, W, Wo, segp, dYp, w.Hq, w.Hkv, w.Dh, w.causal)
+    dXg = to_f64(dX)
+    assert rel_fro(dXg[:prefix], dX_ref) <= GRAD_REL_FRO, rel_fro(dXg[:prefix], dX_ref)
+    assert not np.any(dXg[prefix:])
+    assert rel_fro(to_f64(dW), dW_ref) <= GRAD_REL_FRO, rel_fro(to_f64(dW), dW_ref)
+    assert rel_fro(to_f64(dWo), dWo_ref) <= GRAD_REL_FRO, rel_fro(to_f64(dWo), dWo_ref)
