@@ -126,6 +126,23 @@ upipe_status_t upipe_attn_bwd(const upipe_attn_desc_t* desc, const uint16_t* X, 
                               uint16_t* dX, float* dWqkv, float* dWo, void* ws, size_t ws_bytes,
                               void* stream);
 
+/* Forward pass for callers that cannot allocate device memory (for example code recorded into
+ * someone else's CUDA graph, or a plugin that only receives input and output pointers).  The
+ * pages describe nothing like it; it is a convenience of this library.  Same arguments and
+ * results as upipe_attn_fwd, without ws/ws_bytes: the workspace is a 32 MiB device array
+ * inside the library, which every GPU that loads the library holds until the process exits.
+ *  - Descriptors whose forward workspace (upipe_attn_workspace_size, pass 0) exceeds 32 MiB
+ *    are rejected with UPIPE_ERR_WORKSPACE_TOO_SMALL before any launch.
+ *  - No cudaMalloc, cudaFree or other allocating call is made.
+ *  - The first call on a device looks up the array's device address on that (current)
+ *    device; make that first call before any stream capture.
+ *  - Every call uses the same array and leaves its contents behind; the forward pass
+ *    initialises everything it reads.  Calls whose executions overlap on the GPU (different
+ *    streams, or concurrent host threads) race on the array: serialise them. */
+upipe_status_t upipe_attn_fwd_no_alloc(const upipe_attn_desc_t* desc, const uint16_t* X, const uint16_t* Wqkv,
+                                       const uint16_t* Wo, const int32_t* seg, uint16_t* Y, float* lse,
+                                       void* stream);
+
 /* Attention core alone, Q/K/V given directly (head-major), for testing the kernels in isolation.
  *   q [Hq, S, Dh], k, v [Hkv, S, Dh] device bf16; table from upipe_attn_build_tile_table;
  *   o [Hq, S, Dh] device bf16 (written); lse [Hq, S] device fp32 (written).
