@@ -14,9 +14,10 @@
 //           while the chunks of that group run
 //   Q, O    bf16 [hpc, S, Dh]                                                   both
 //   Yacc    f32 [S, d] partial output projection (fwd, several chunks, accum_mode 0)
-//   dO      bf16 [hpc, S, Dh]; D f32 [hpc, S]; dQ bf16 [hpc, S, Dh]             bwd
-//   dK, dV  bf16 [kvc, S, Dh]; dKacc, dVacc f32 [S, Dh] when a chunk holds only part of a
-//           KV group (hpc < g)                                                  bwd
+//   dO      bf16 [hpc, S, Dh]; D f32 [2][hpc][Sp] (D and lse*log2e, Sp = S rounded to 128)
+//   dQKV    bf16 [hpc + 2 kvc, S, Dh]: dQ heads, then dK, dV heads (one tensor, so the dX and
+//           dWqkv GEMMs read it through one 3-D tensor map)                     bwd
+//   dKacc, dVacc f32 [S, Dh] when a chunk holds only part of a KV group (hpc < g)  bwd
 //   dXacc   f32 [S, d] partial input gradient (several chunks, accum_mode 0)   bwd
 //   split   f32 split-K partials of the weight-gradient GEMMs                  bwd
 #include <cmath>
@@ -107,9 +108,9 @@ Plan make_plan(const upipe_attn_desc_t* desc, int pass) {
   } else {
     p.dO = take(p.hpc * head);
     p.D = take(2 * (size_t)p.hpc * ceil_div(p.S, kTile) * kTile * sizeof(float));
-    p.dq = take(p.hpc * head);
-    p.dk = take(p.kvc * head);
-    p.dv = take(p.kvc * head);
+    p.dq = take((p.hpc + 2 * p.kvc) * head);  // [dQ heads | dK heads | dV heads], one 3-D tensor
+    p.dk = p.dq + p.hpc * head;
+    p.dv = p.dk + p.kvc * head;
     if (p.hpc < p.g) {
       p.dkacc = take((size_t)p.S * p.Dh * sizeof(float));
       p.dvacc = take((size_t)p.S * p.Dh * sizeof(float));
@@ -153,32 +154,50 @@ int log2i(int x) {
   return s;
 }
 
+TcOperand op2d(const void* base, uint64_t inner, uint64_t outer, uint64_t row_stride, int k_major) {
+  TcOperand o{};
+  o.base = base; o.rank = 2; o.inner = inner; o.outer = outer; o.planes = 1; o.row_stride = row_stride;
+  o.k_major = k_major; o.blk_shift = -1; o.blk_dim = 0;
+  return o;
+}
+
+TcOperand op3d(const void* base, uint64_t inner, uint64_t outer, uint64_t planes, int k_major, int blk_shift,
+               int blk_dim) {
+  TcOperand o{};
+  o.base = base; o.rank = 3; o.inner = inner; o.outer = outer; o.planes = planes; o.row_stride = inner;
+  o.k_major = k_major; o.blk_shift = blk_shift; o.blk_dim = blk_dim;
+  return o;
+}
+
 // Q (and, at the start of a KV group, K and V) of chunk c:  [Q|K|V]_c = X * Wqkv_c^T
+// B = the chunk's rows of Wqkv (a 2-D map with one starting row per head), output head-major.
 cudaError_t project_qkv(const Plan& p, int c, bool with_kv, const bf16* X, const bf16* Wqkv, void* ws, cudaStream_t st) {
-  GemmArgs g{};
+  TcGemmArgs g{};
   const int sh = log2i(p.Dh);
-  int nb = 0;
-  g.a.blk[0] = X; g.a.ld = p.d; g.a.blk_shift = -1; g.a.blk_dim = 0; g.a.k_major = 1;
-  g.b.ld = p.d; g.b.blk_shift = sh; g.b.blk_dim = 0; g.b.k_major = 1;
+  const uint64_t wrows = (uint64_t)(p.Hq + 2 * p.Hkv) * p.Dh;
+  g.a = op2d(X, p.d, p.S, p.d, 1);
+  g.b = op2d(Wqkv, p.d, wrows, p.d, 1);
+  g.b.blk_shift = sh; g.b.blk_dim = 0;
   g.c.ld = p.Dh; g.c.blk_shift = sh; g.c.blk_dim = 1;
+  int nb = 0;
   for (int hl = 0; hl < p.hpc; ++hl, ++nb) {
-    g.b.blk[nb] = Wqkv + wrow_q(p, c * p.hpc + hl) * p.d;
+    g.b.row_base[nb] = (int32_t)wrow_q(p, c * p.hpc + hl);
     g.c.blk[nb] = at<bf16>(ws, p.q) + (int64_t)hl * p.S * p.Dh;
   }
   if (with_kv) {
     const int kv0 = (c * p.hpc) / p.g;
     for (int j = 0; j < p.kvc; ++j, ++nb) {
-      g.b.blk[nb] = Wqkv + wrow_k(p, kv0 + j) * p.d;
+      g.b.row_base[nb] = (int32_t)wrow_k(p, kv0 + j);
       g.c.blk[nb] = at<bf16>(ws, p.k) + (int64_t)j * p.S * p.Dh;
     }
     for (int j = 0; j < p.kvc; ++j, ++nb) {
-      g.b.blk[nb] = Wqkv + wrow_v(p, kv0 + j) * p.d;
+      g.b.row_base[nb] = (int32_t)wrow_v(p, kv0 + j);
       g.c.blk[nb] = at<bf16>(ws, p.v) + (int64_t)j * p.S * p.Dh;
     }
   }
   g.M = p.S; g.N = (int64_t)nb * p.Dh; g.K = p.d;
   g.epi = EPI_STORE_BF16;
-  return launch_gemm(g, 1, nullptr, st);
+  return launch_gemm_tc(g, 1, nullptr, st);
 }
 
 // Epilogue schedule of a quantity accumulated over the n_chunks chunks (Y, dX).
@@ -227,14 +246,13 @@ upipe_status_t run_fwd(const Plan& p, const bf16* X, const bf16* Wqkv, const bf1
     AttnArgs a = attn_args(p, c, ws, seg, lse);
     UPIPE_CUDA(launch_attn_fwd(a, p.Dh, st));
     // Y (+)= O_c * Wo_c^T
-    GemmArgs g{};
+    TcGemmArgs g{};
     g.M = p.S; g.N = p.d; g.K = (int64_t)p.hpc * p.Dh;
-    for (int hl = 0; hl < p.hpc; ++hl) g.a.blk[hl] = at<bf16>(ws, p.o) + (int64_t)hl * p.S * p.Dh;
-    g.a.ld = p.Dh; g.a.blk_shift = sh; g.a.blk_dim = 1; g.a.k_major = 1;
-    g.b.blk[0] = Wo + (int64_t)c * p.hpc * p.Dh; g.b.ld = (int64_t)p.Hq * p.Dh; g.b.blk_shift = -1; g.b.k_major = 1;
+    g.a = op3d(at<bf16>(ws, p.o), p.Dh, p.S, p.hpc, 1, sh, 1);                        // O_c, K blocked by head
+    g.b = op2d(Wo + (int64_t)c * p.hpc * p.Dh, (uint64_t)p.hpc * p.Dh, p.d, (uint64_t)p.Hq * p.Dh, 1);  // Wo_c
     g.epi = accum_epi(p, c, true);
     set_accum_out(g.c, p, g.epi, Y, p.yacc ? at<float>(ws, p.yacc) : nullptr);
-    UPIPE_CUDA(launch_gemm(g, 1, nullptr, st));
+    UPIPE_CUDA(launch_gemm_tc(g, 1, nullptr, st));
   }
   return UPIPE_OK;
 }
@@ -255,28 +273,27 @@ upipe_status_t run_bwd(const Plan& p, const bf16* X, const bf16* Wqkv, const bf1
       UPIPE_CUDA(launch_zero(at<char>(ws, p.dvacc), (int64_t)p.S * p.Dh * 4, st));
     }
     {  // dO_c = dY * Wo_c   (Wo_c: columns of Wo, read as [K = d][N = hpc Dh])
-      GemmArgs g{};
+      TcGemmArgs g{};
       g.M = p.S; g.N = (int64_t)p.hpc * p.Dh; g.K = p.d;
-      g.a.blk[0] = dY; g.a.ld = p.d; g.a.blk_shift = -1; g.a.k_major = 1;
-      g.b.blk[0] = Wo + (int64_t)c * p.hpc * p.Dh; g.b.ld = HD; g.b.blk_shift = -1; g.b.k_major = 0;
+      g.a = op2d(dY, p.d, p.S, p.d, 1);
+      g.b = op2d(Wo + (int64_t)c * p.hpc * p.Dh, (uint64_t)p.hpc * p.Dh, p.d, HD, 0);
       for (int hl = 0; hl < p.hpc; ++hl) g.c.blk[hl] = at<bf16>(ws, p.dO) + (int64_t)hl * p.S * p.Dh;
       g.c.ld = p.Dh; g.c.blk_shift = sh; g.c.blk_dim = 1;
       g.epi = EPI_STORE_BF16;
-      UPIPE_CUDA(launch_gemm(g, 1, nullptr, st));
+      UPIPE_CUDA(launch_gemm_tc(g, 1, nullptr, st));
     }
     AttnArgs a = attn_args(p, c, ws, seg, const_cast<float*>(lse));
     a.dO = at<bf16>(ws, p.dO);
     a.D = at<float>(ws, p.D);
     UPIPE_CUDA(launch_attn_recompute(a, p.Dh, st));
     {  // dWo_c = dY^T * O_c   (split-K over S)
-      GemmArgs g{};
+      TcGemmArgs g{};
       g.M = p.d; g.N = (int64_t)p.hpc * p.Dh; g.K = p.S;
-      g.a.blk[0] = dY; g.a.ld = p.d; g.a.blk_shift = -1; g.a.k_major = 0;
-      for (int hl = 0; hl < p.hpc; ++hl) g.b.blk[hl] = at<bf16>(ws, p.o) + (int64_t)hl * p.S * p.Dh;
-      g.b.ld = p.Dh; g.b.blk_shift = sh; g.b.blk_dim = 0; g.b.k_major = 0;
+      g.a = op2d(dY, p.d, p.S, p.d, 0);                              // dY^T: M runs along d
+      g.b = op3d(at<bf16>(ws, p.o), p.Dh, p.S, p.hpc, 0, sh, 0);    // O_c: N blocked by head
       g.c.blk[0] = dWo + (int64_t)c * p.hpc * p.Dh; g.c.ld = HD; g.c.blk_shift = -1;
       g.epi = EPI_STORE_F32;
-      UPIPE_CUDA(launch_gemm(g, p.split_wo, split, st));
+      UPIPE_CUDA(launch_gemm_tc(g, p.split_wo, split, st));
     }
     AttnBwdArgs b{};
     b.f = a;
@@ -293,50 +310,38 @@ upipe_status_t run_bwd(const Plan& p, const bf16* X, const bf16* Wqkv, const bf1
       UPIPE_CUDA(launch_f32_to_bf16(at<float>(ws, p.dkacc), at<bf16>(ws, p.dk), p.S * p.Dh, 1.f, st));
       UPIPE_CUDA(launch_f32_to_bf16(at<float>(ws, p.dvacc), at<bf16>(ws, p.dv), p.S * p.Dh, 1.f, st));
     }
-    // blocks of dQKV_c that are final now: the chunk's dQ heads, plus dK/dV at a group end
-    const bf16* blk_act[kMaxBlocks];
-    int64_t blk_row[kMaxBlocks];
+    // blocks of dQKV_c that are final now: the chunk's dQ heads, plus dK/dV at a group end.
+    // They are planes [0, nb) of the [dQ | dK | dV] tensor of the workspace.
+    int32_t blk_row[kMaxBlocks];
     int nb = 0;
-    for (int hl = 0; hl < p.hpc; ++hl, ++nb) {
-      blk_act[nb] = at<bf16>(ws, p.dq) + (int64_t)hl * p.S * p.Dh;
-      blk_row[nb] = wrow_q(p, c * p.hpc + hl);
-    }
+    for (int hl = 0; hl < p.hpc; ++hl, ++nb) blk_row[nb] = (int32_t)wrow_q(p, c * p.hpc + hl);
     if (end_group) {
-      for (int j = 0; j < p.kvc; ++j, ++nb) {
-        blk_act[nb] = at<bf16>(ws, p.dk) + (int64_t)j * p.S * p.Dh;
-        blk_row[nb] = wrow_k(p, kv0 + j);
-      }
-      for (int j = 0; j < p.kvc; ++j, ++nb) {
-        blk_act[nb] = at<bf16>(ws, p.dv) + (int64_t)j * p.S * p.Dh;
-        blk_row[nb] = wrow_v(p, kv0 + j);
-      }
+      for (int j = 0; j < p.kvc; ++j, ++nb) blk_row[nb] = (int32_t)wrow_k(p, kv0 + j);
+      for (int j = 0; j < p.kvc; ++j, ++nb) blk_row[nb] = (int32_t)wrow_v(p, kv0 + j);
     }
+    const uint64_t planes = (uint64_t)(p.hpc + 2 * p.kvc);
+    const uint64_t wrows = (uint64_t)(p.Hq + 2 * p.Hkv) * p.Dh;
     {  // dX (+)= dQKV_c * Wqkv_c
-      GemmArgs g{};
+      TcGemmArgs g{};
       g.M = p.S; g.N = p.d; g.K = (int64_t)nb * p.Dh;
-      for (int i = 0; i < nb; ++i) {
-        g.a.blk[i] = blk_act[i];
-        g.b.blk[i] = Wqkv + blk_row[i] * p.d;
-      }
-      g.a.ld = p.Dh; g.a.blk_shift = sh; g.a.blk_dim = 1; g.a.k_major = 1;
-      g.b.ld = p.d; g.b.blk_shift = sh; g.b.blk_dim = 1; g.b.k_major = 0;
+      g.a = op3d(at<bf16>(ws, p.dq), p.Dh, p.S, planes, 1, sh, 1);   // K blocked by head
+      g.b = op2d(Wqkv, p.d, wrows, p.d, 0);                           // rows of the blocks, N along d
+      g.b.blk_shift = sh; g.b.blk_dim = 1;
+      for (int i = 0; i < nb; ++i) g.b.row_base[i] = blk_row[i];
       g.epi = accum_epi(p, c, true);
       set_accum_out(g.c, p, g.epi, dX, p.dxacc ? at<float>(ws, p.dxacc) : nullptr);
-      UPIPE_CUDA(launch_gemm(g, 1, nullptr, st));
+      UPIPE_CUDA(launch_gemm_tc(g, 1, nullptr, st));
     }
     {  // dWqkv rows of these blocks = dQKV_block^T * X   (split-K over S)
-      GemmArgs g{};
+      TcGemmArgs g{};
       g.M = (int64_t)nb * p.Dh; g.N = p.d; g.K = p.S;
-      for (int i = 0; i < nb; ++i) {
-        g.a.blk[i] = blk_act[i];
-        g.c.blk[i] = dWqkv + blk_row[i] * p.d;
-      }
-      g.a.ld = p.Dh; g.a.blk_shift = sh; g.a.blk_dim = 0; g.a.k_major = 0;
-      g.b.blk[0] = X; g.b.ld = p.d; g.b.blk_shift = -1; g.b.k_major = 0;
+      g.a = op3d(at<bf16>(ws, p.dq), p.Dh, p.S, planes, 0, sh, 0);   // M blocked by head
+      g.b = op2d(X, p.d, p.S, p.d, 0);
+      for (int i = 0; i < nb; ++i) g.c.blk[i] = dWqkv + (int64_t)blk_row[i] * p.d;
       g.c.ld = p.d; g.c.blk_shift = sh; g.c.blk_dim = 0;
       g.epi = EPI_STORE_F32;
       const int split_k = nb == p.hpc ? p.split_wqkv_q : p.split_wqkv_full;
-      UPIPE_CUDA(launch_gemm(g, split_k, split, st));
+      UPIPE_CUDA(launch_gemm_tc(g, split_k, split, st));
     }
   }
   return UPIPE_OK;
@@ -524,13 +529,13 @@ upipe_status_t upipe_attn_gemm_nt(int64_t M, int64_t N, int64_t K, const uint16_
   if (M <= 0 || N <= 0 || K <= 0 || !A || !B || !C || lda < K || ldb < K || ldc < N) return UPIPE_ERR_INVALID_ARG;
   if (K % 8 || N % 8 || lda % 8 || ldb % 8 || ldc % 4) return UPIPE_ERR_UNSUPPORTED;
   if (!aligned16(A) || !aligned16(B) || !aligned16(C)) return UPIPE_ERR_ALIGNMENT;
-  GemmArgs g{};
+  TcGemmArgs g{};
   g.M = M; g.N = N; g.K = K;
-  g.a.blk[0] = A; g.a.ld = lda; g.a.blk_shift = -1; g.a.k_major = 1;
-  g.b.blk[0] = B; g.b.ld = ldb; g.b.blk_shift = -1; g.b.k_major = 1;
+  g.a = op2d(A, K, M, lda, 1);
+  g.b = op2d(B, K, N, ldb, 1);
   g.c.blk[0] = C; g.c.ld = ldc; g.c.blk_shift = -1;
   g.epi = EPI_STORE_F32;
-  return cuda_status(launch_gemm(g, 1, nullptr, (cudaStream_t)stream));
+  return cuda_status(launch_gemm_tc(g, 1, nullptr, (cudaStream_t)stream));
 }
 
 upipe_status_t upipe_attn_device_status(const void* buf, int32_t* code, void* stream) {

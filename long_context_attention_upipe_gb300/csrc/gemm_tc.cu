@@ -1,0 +1,384 @@
+// Projection GEMMs of the layer on the 5th-generation tensor cores (tcgen05, TMEM, TMA).
+//
+// C[M, N] = A[M, K] * B[N, K]^T, bf16 operands, fp32 accumulation in TMEM, one of the epilogues
+// of GemmEpilogue.  Every operand is read by TMA in 64 x 64 boxes (128-byte swizzle) from a 2-D
+// or 3-D tensor map, K-major or MN-major, so each projection of the chunk loop reads its
+// operands in place: head-major activations ([heads][S][Dh], a 3-D map whose third coordinate
+// is the head), column slices of Wo (a 2-D map with the row stride of Wo) and the row blocks of
+// Wqkv that belong to a chunk (a 2-D map plus the first row of each block).
+//
+// Persistent kernel, one CTA per SM, 6 warps:
+//   warp 0     TMA producer over a 6-stage ring of (A 128x64, B 128x64) tiles
+//   warp 1     MMA issuer (one thread), TMEM owner: 4 tcgen05.mma (M128 N128 K16) per stage into
+//              one of two TMEM accumulators, so the epilogue of a tile overlaps the next tile
+//   warps 2-5  epilogue: one output row per thread (TMEM lane), 32 columns at a time
+// Split-K (weight gradients, K = S) writes fp32 partials that k_split_reduce sums in order.
+#include "internal.h"
+#include "tc_common.cuh"
+
+namespace upipe {
+
+namespace {
+
+constexpr int BM = 128, BN = 128, BK = 64, STAGES = 6, THREADS = 192;
+constexpr uint32_t BOX = 64 * 64 * 2;          // one 64 x 64 bf16 box, 8 KB
+constexpr uint32_t TILE = 2 * BOX;             // one 128 x 64 operand tile
+constexpr uint32_t STAGE = 2 * TILE;           // A + B
+constexpr uint32_t BAR_OFF = STAGES * STAGE;
+constexpr uint32_t SMEM_BYTES = BAR_OFF + 256 + 1024;
+
+struct TcOpDev {
+  int k_major, rank, blk_shift, blk_dim;
+  int32_t row_base[kMaxBlocks];
+};
+
+struct TcGemmParams {
+  int64_t M, N, K;
+  TcOpDev a, b;
+  GemmOutput c;
+  int epi;
+  int split_k;
+  int64_t k_per_split;  // multiple of BK
+  int tiles_m, tiles_n;
+  float* split_out;
+};
+
+// TMA coordinates of the 64 x 64 box that starts at logical (mn, k).
+__device__ __forceinline__ void box_coords(const TcOpDev& o, int64_t mn, int64_t k, int& c0, int& c1, int& c2) {
+  int b = 0;
+  if (o.blk_shift >= 0) {
+    const int64_t mask = (int64_t(1) << o.blk_shift) - 1;
+    if (o.blk_dim == 0) { b = (int)(mn >> o.blk_shift); mn &= mask; }
+    else { b = (int)(k >> o.blk_shift); k &= mask; }
+  }
+  const int64_t inner = o.k_major ? k : mn, outer = o.k_major ? mn : k;
+  if (o.rank == 3) {
+    c0 = (int)inner; c1 = (int)outer; c2 = b;
+  } else {
+    c0 = (int)inner; c1 = (int)(outer + (o.blk_shift >= 0 ? o.row_base[b] : 0)); c2 = 0;
+  }
+}
+
+__device__ __forceinline__ void load_box(uint8_t* dst, const CUtensorMap* map, const TcOpDev& o, uint64_t* bar,
+                                         int64_t mn, int64_t k) {
+  int c0, c1, c2;
+  box_coords(o, mn, k, c0, c1, c2);
+  if (o.rank == 3) tc::tma_load_3d(dst, map, bar, c0, c1, c2);
+  else tc::tma_load_2d(dst, map, bar, c0, c1);
+}
+
+// smem descriptor of one operand tile at MMA K-step k16 (16 elements)
+__device__ __forceinline__ uint64_t tile_desc(uint32_t base, int k_major, int k16) {
+  return k_major ? tc::sdesc_sw128(base + k16 * 32, 16, 1024)        // 128 rows x 128 B, 8-row groups
+                 : tc::sdesc_sw128(base + k16 * 2048, BOX, 1024);    // two 64-wide MN atoms, BOX apart
+}
+
+template <typename T>
+__device__ __forceinline__ T* out_ptr(const GemmOutput& o, int64_t m, int64_t n) {
+  int b = 0;
+  if (o.blk_shift >= 0) {
+    const int64_t idx = o.blk_dim == 0 ? m : n;
+    b = (int)(idx >> o.blk_shift);
+    const int64_t local = idx & ((int64_t(1) << o.blk_shift) - 1);
+    if (o.blk_dim == 0) m = local; else n = local;
+  }
+  return reinterpret_cast<T*>(o.blk[b]) + m * o.ld + n;
+}
+
+__global__ void __launch_bounds__(THREADS, 1) k_gemm_tc(const __grid_constant__ CUtensorMap ta,
+                                                        const __grid_constant__ CUtensorMap tb, TcGemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
+  uint64_t* full = bars;                // [STAGES]
+  uint64_t* empty = bars + STAGES;      // [STAGES]
+  uint64_t* acc_full = bars + 2 * STAGES;       // [2]
+  uint64_t* acc_empty = bars + 2 * STAGES + 2;  // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 4);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * STAGES + 5);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t tiles_mn = (int64_t)p.tiles_m * p.tiles_n;
+  const int64_t n_tiles = tiles_mn * p.split_k;
+  const int nk_full = (int)ceil_div(p.k_per_split, BK);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      tc::mbar_init(&full[i], 1);
+      tc::mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&acc_full[i], 1);
+      tc::mbar_init(&acc_empty[i], 128);
+    }
+    *abort_flag = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tmem_slot, 256);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  // tile t -> (m tile, n tile, split); n fastest so that CTAs running together share A rows in L2
+  auto decode = [&](int64_t t, int& tm, int& tn, int& ks) {
+    ks = (int)(t / tiles_mn);
+    const int64_t r = t % tiles_mn;
+    tm = (int)(r / p.tiles_n);
+    tn = (int)(r % p.tiles_n);
+  };
+  auto k_tiles = [&](int ks) {
+    const int64_t kb = (int64_t)ks * p.k_per_split;
+    const int64_t ke = min(p.K, kb + p.k_per_split);
+    return ke > kb ? (int)ceil_div(ke - kb, BK) : 0;
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tc::prefetch_tmap(&ta);
+      tc::prefetch_tmap(&tb);
+      int it = 0;
+      bool ok = true;
+      for (int64_t t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
+        int tm, tn, ks;
+        decode(t, tm, tn, ks);
+        const int nk = k_tiles(ks);
+        for (int kt = 0; kt < nk; ++kt, ++it) {
+          const int s = it % STAGES;
+          if (it >= STAGES && !(ok = tc::mbar_wait(&empty[s], ((it / STAGES) - 1) & 1, abort_flag, nullptr))) break;
+          tc::mbar_arrive_expect_tx(&full[s], STAGE);
+          uint8_t* sa = smem + s * STAGE;
+          const int64_t k = (int64_t)ks * p.k_per_split + (int64_t)kt * BK;
+          for (int i = 0; i < 2; ++i) {
+            load_box(sa + i * BOX, &ta, p.a, &full[s], (int64_t)tm * BM + 64 * i, k);
+            load_box(sa + TILE + i * BOX, &tb, p.b, &full[s], (int64_t)tn * BN + 64 * i, k);
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = tc::idesc_bf16(BM, BN, !p.a.k_major, !p.b.k_major);
+      int it = 0, tcount = 0;
+      bool ok = true;
+      for (int64_t t = blockIdx.x; ok && t < n_tiles; t += gridDim.x, ++tcount) {
+        int tm, tn, ks;
+        decode(t, tm, tn, ks);
+        const int nk = k_tiles(ks);
+        const int buf = tcount & 1;
+        if (tcount >= 2 && !(ok = tc::mbar_wait(&acc_empty[buf], ((tcount >> 1) - 1) & 1, abort_flag, nullptr))) break;
+        tc::fence_after_sync();
+        const uint32_t d = tmem + buf * 128;
+        for (int kt = 0; kt < nk; ++kt, ++it) {
+          const int s = it % STAGES;
+          if (!(ok = tc::mbar_wait(&full[s], (it / STAGES) & 1, abort_flag, nullptr))) break;
+          tc::fence_after_sync();
+          const uint32_t sa = smem_u32(smem + s * STAGE), sb = sa + TILE;
+#pragma unroll
+          for (int k16 = 0; k16 < BK / 16; ++k16)
+            tc::mma_ss(d, tile_desc(sa, p.a.k_major, k16), tile_desc(sb, p.b.k_major, k16), idesc, kt > 0 || k16 > 0);
+          tc::mma_commit(&empty[s]);
+        }
+        tc::mma_commit(&acc_full[buf]);
+      }
+    }
+    __syncwarp();
+  } else {
+    // epilogue warps 2..5: TMEM lanes 32 * (warp % 4) + lane
+    const int row_in_tile = 32 * (warp & 3) + lane;
+    const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    int tcount = 0;
+    bool ok = true;
+    for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x, ++tcount) {
+      int tm, tn, ks;
+      decode(t, tm, tn, ks);
+      const int nk = k_tiles(ks);
+      const int buf = tcount & 1;
+      if (ok) ok = tc::mbar_wait(&acc_full[buf], (tcount >> 1) & 1, abort_flag, nullptr);
+      tc::fence_after_sync();
+      const int64_t m = (int64_t)tm * BM + row_in_tile;
+      const bool m_ok = m < p.M;
+#pragma unroll 1
+      for (int ch = 0; ch < BN / 32; ++ch) {
+        uint32_t v[32];
+        tc::tmem_ld32(lane_addr + buf * 128 + ch * 32, v);
+        tc::tmem_ld_wait();
+        if (nk == 0) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0u;
+        }
+        const int64_t n0 = (int64_t)tn * BN + ch * 32;
+        if (!ok || !m_ok || n0 >= p.N) continue;
+        const int ncols = (int)min((int64_t)32, p.N - n0);  // multiple of 8
+        if (p.split_out) {
+          float* dst = p.split_out + ((int64_t)ks * p.M + m) * p.N + n0;
+          _Pragma("unroll") for (int i = 0; i < 32; i += 4) if (i < ncols)
+            *reinterpret_cast<float4*>(dst + i) = make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
+                                                              __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+          continue;
+        }
+        switch (p.epi) {
+          case EPI_STORE_BF16: {
+            bf16* dst = out_ptr<bf16>(p.c, m, n0);
+            _Pragma("unroll") for (int i = 0; i < 32; i += 8) if (i < ncols) {
+              uint4 q;
+              q.x = tc::pack_bf16x2(__uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+              q.y = tc::pack_bf16x2(__uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+              q.z = tc::pack_bf16x2(__uint_as_float(v[i + 4]), __uint_as_float(v[i + 5]));
+              q.w = tc::pack_bf16x2(__uint_as_float(v[i + 6]), __uint_as_float(v[i + 7]));
+              *reinterpret_cast<uint4*>(dst + i) = q;
+            }
+            break;
+          }
+          case EPI_STORE_F32: {
+            float* dst = out_ptr<float>(p.c, m, n0);
+            _Pragma("unroll") for (int i = 0; i < 32; i += 4) if (i < ncols)
+              *reinterpret_cast<float4*>(dst + i) = make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
+                                                                __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+            break;
+          }
+          case EPI_ACC_F32: {
+            float* dst = out_ptr<float>(p.c, m, n0);
+            _Pragma("unroll") for (int i = 0; i < 32; i += 4) if (i < ncols) {
+              float4 o = *reinterpret_cast<float4*>(dst + i);
+              o.x += __uint_as_float(v[i]); o.y += __uint_as_float(v[i + 1]);
+              o.z += __uint_as_float(v[i + 2]); o.w += __uint_as_float(v[i + 3]);
+              *reinterpret_cast<float4*>(dst + i) = o;
+            }
+            break;
+          }
+          case EPI_ACC_F32_TO_BF16: {
+            const float* aux = p.c.aux + m * p.c.aux_ld + n0;
+            bf16* dst = out_ptr<bf16>(p.c, m, n0);
+            _Pragma("unroll") for (int i = 0; i < 32; i += 8) if (i < ncols) {
+              const float4 a0 = *reinterpret_cast<const float4*>(aux + i);
+              const float4 a1 = *reinterpret_cast<const float4*>(aux + i + 4);
+              uint4 q;
+              q.x = tc::pack_bf16x2(a0.x + __uint_as_float(v[i]), a0.y + __uint_as_float(v[i + 1]));
+              q.y = tc::pack_bf16x2(a0.z + __uint_as_float(v[i + 2]), a0.w + __uint_as_float(v[i + 3]));
+              q.z = tc::pack_bf16x2(a1.x + __uint_as_float(v[i + 4]), a1.y + __uint_as_float(v[i + 5]));
+              q.w = tc::pack_bf16x2(a1.z + __uint_as_float(v[i + 6]), a1.w + __uint_as_float(v[i + 7]));
+              *reinterpret_cast<uint4*>(dst + i) = q;
+            }
+            break;
+          }
+          case EPI_ACC_BF16: {
+            bf16* dst = out_ptr<bf16>(p.c, m, n0);
+            _Pragma("unroll") for (int i = 0; i < 32; i += 8) if (i < ncols) {
+              uint4 q = *reinterpret_cast<uint4*>(dst + i);
+              __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&q);
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const float2 f = __bfloat1622float2(h2[u]);
+                h2[u] = __floats2bfloat162_rn(f.x + __uint_as_float(v[i + 2 * u]), f.y + __uint_as_float(v[i + 2 * u + 1]));
+              }
+              *reinterpret_cast<uint4*>(dst + i) = q;
+            }
+            break;
+          }
+        }
+      }
+      tc::fence_before_sync();
+      tc::mbar_arrive(&acc_empty[buf]);
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, 256);
+  }
+}
+
+// Fixed-order reduction of split-K partials into the (blocked) fp32 output.
+__global__ void k_split_reduce(const float* __restrict__ part, int splits, int64_t M, int64_t N, GemmOutput out) {
+  const int64_t total = M * N / 4;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+    const int64_t e = i * 4;
+    const int64_t m = e / N, n = e % N;
+    float4 s = reinterpret_cast<const float4*>(part)[i];
+    for (int z = 1; z < splits; ++z) {
+      const float4 v = reinterpret_cast<const float4*>(part + (int64_t)z * M * N)[i];
+      s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+    }
+    *reinterpret_cast<float4*>(out_ptr<float>(out, m, n)) = s;
+  }
+}
+
+bool make_map(CUtensorMap* map, const TcOperand& o) {
+  if (o.rank == 3) return make_tmap_3d_bf16(map, o.base, o.inner, o.outer, o.planes, 64, 64);
+  return make_tmap_2d_bf16(map, o.base, o.inner, o.outer, o.row_stride, 64, 64);
+}
+
+TcOpDev dev_op(const TcOperand& o) {
+  TcOpDev d{};
+  d.k_major = o.k_major;
+  d.rank = o.rank;
+  d.blk_shift = o.blk_shift;
+  d.blk_dim = o.blk_dim;
+  for (int i = 0; i < kMaxBlocks; ++i) d.row_base[i] = o.row_base[i];
+  return d;
+}
+
+}  // namespace
+
+size_t gemm_split_scratch_bytes(int64_t M, int64_t N, int split_k) {
+  return split_k > 1 ? (size_t)split_k * M * N * sizeof(float) : 0;
+}
+
+// Split K until the tile count covers two waves of the SMs (each split keeps >= 2048 of K).
+int gemm_pick_split(int64_t M, int64_t N, int64_t K, int num_sms) {
+  const int64_t tiles = ceil_div(M, BM) * ceil_div(N, BN);
+  int split = 1;
+  while (tiles * split < 2 * num_sms && K / (split * 2) >= 2048 && split < 32) split *= 2;
+  return split;
+}
+
+cudaError_t launch_split_reduce(const float* part, int splits, int64_t M, int64_t N, const GemmOutput& out,
+                                cudaStream_t st) {
+  const int64_t total4 = M * N / 4;
+  const unsigned blocks = (unsigned)std::max<int64_t>(1, std::min<int64_t>(ceil_div(total4, 256), 152 * 8));
+  k_split_reduce<<<blocks, 256, 0, st>>>(part, splits, M, N, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_tc(const TcGemmArgs& g, int split_k, float* split_scratch, cudaStream_t st) {
+  if (g.M <= 0 || g.N <= 0) return cudaSuccess;
+  CUtensorMap ta, tb;
+  if (!make_map(&ta, g.a) || !make_map(&tb, g.b)) return cudaErrorInvalidValue;
+  TcGemmParams p{};
+  p.M = g.M; p.N = g.N; p.K = g.K;
+  p.a = dev_op(g.a);
+  p.b = dev_op(g.b);
+  p.c = g.c;
+  p.epi = g.epi;
+  const int64_t ktiles = ceil_div(g.K, BK);
+  if (split_k < 1) split_k = 1;
+  if (split_k > ktiles) split_k = (int)std::max<int64_t>(1, ktiles);
+  p.split_k = split_k;
+  p.k_per_split = ceil_div(ktiles, split_k) * BK;
+  p.tiles_m = (int)ceil_div(g.M, BM);
+  p.tiles_n = (int)ceil_div(g.N, BN);
+  p.split_out = split_k > 1 ? split_scratch : nullptr;
+  static int sms = 0;
+  if (!sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      sms = 152;
+  }
+  const int64_t n_tiles = (int64_t)p.tiles_m * p.tiles_n * split_k;
+  const int grid = (int)std::min<int64_t>(n_tiles, sms);
+  cudaError_t e = cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  k_gemm_tc<<<grid, THREADS, SMEM_BYTES, st>>>(ta, tb, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || split_k <= 1) return e;
+  return launch_split_reduce(split_scratch, split_k, g.M, g.N, g.c, st);
+}
+
+}  // namespace upipe

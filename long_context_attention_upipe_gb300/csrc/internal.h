@@ -20,19 +20,8 @@ inline const int4* table_kv_rows(const void* table, int64_t S) {
 }
 
 // ---------------------------------------------------------------- projection GEMMs
-// Logical operands: A is [M, K], B is [N, K]; C[M, N] = A * B^T.  Each operand is a set of
-// row-major blocks: along one logical dimension the index is split into blocks of blk_len
-// (a power of two) with one base pointer per block (head-major activations, column slices of a
-// weight).  k_major: the K index is the contiguous one inside a block; otherwise the M/N index.
+// Logical operands: A is [M, K], B is [N, K]; C[M, N] = A * B^T.
 constexpr int kMaxBlocks = 64;
-
-struct GemmOperand {
-  const void* blk[kMaxBlocks];
-  int64_t ld;      // elements between consecutive rows of a block
-  int blk_shift;   // log2(block length) along the blocked dimension; -1: unblocked
-  int blk_dim;     // 0: blocked along M (or N), 1: blocked along K
-  int k_major;
-};
 
 enum GemmEpilogue : int {
   EPI_STORE_BF16 = 0,      // out(bf16) = acc
@@ -51,18 +40,37 @@ struct GemmOutput {
   int64_t aux_ld;
 };
 
-struct GemmArgs {
+size_t gemm_split_scratch_bytes(int64_t M, int64_t N, int split_k);
+int gemm_pick_split(int64_t M, int64_t N, int64_t K, int num_sms);
+
+// Operand of the tensor-core GEMM as a TMA tensor map.  rank 2: rows of `row_stride` elements,
+// [outer][inner]; rank 3: dense [planes][outer][inner].  k_major: the logical K index runs along
+// `inner` (else the M/N index does).  With blk_shift >= 0 the logical index along blk_dim
+// (0: M/N, 1: K) is split into blocks of 2^blk_shift (>= 64): rank 3 takes the block as the
+// plane; rank 2 (blocked dimension outer only) starts block b at outer coordinate row_base[b].
+struct TcOperand {
+  const void* base;
+  int rank;
+  uint64_t inner, outer, planes, row_stride;
+  int k_major;
+  int blk_shift;
+  int blk_dim;
+  int32_t row_base[kMaxBlocks];
+};
+
+struct TcGemmArgs {
   int64_t M, N, K;
-  GemmOperand a, b;
+  TcOperand a, b;
   GemmOutput c;
   int epi;
 };
 
-// C = A * B^T with the given epilogue.  split_k > 1 requires epi == EPI_STORE_F32 and a
-// scratch of split_k * M * N floats; the splits are reduced in a fixed order (deterministic).
-cudaError_t launch_gemm(const GemmArgs& args, int split_k, float* split_scratch, cudaStream_t st);
-size_t gemm_split_scratch_bytes(int64_t M, int64_t N, int split_k);
-int gemm_pick_split(int64_t M, int64_t N, int64_t K, int num_sms);
+// C = A * B^T with the given epilogue on the tcgen05 path.  split_k > 1 requires
+// epi == EPI_STORE_F32 and a scratch of split_k * M * N floats; the splits are reduced in a
+// fixed order (deterministic).
+cudaError_t launch_gemm_tc(const TcGemmArgs& args, int split_k, float* split_scratch, cudaStream_t st);
+cudaError_t launch_split_reduce(const float* part, int splits, int64_t M, int64_t N, const GemmOutput& out,
+                                cudaStream_t st);
 
 // ---------------------------------------------------------------- attention core
 struct AttnArgs {
