@@ -179,6 +179,24 @@ def run_reference(args):
 # GPU arm
 # ----------------------------------------------------------------------------------------------
 
+def measured_traffic(kernel, workload, heads):
+    """DRAM bytes per launch from a committed ncu capture of this kernel, or None when there is
+    none for this launch shape or the kernel's source changed since the capture."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f).get(kernel)
+    if not rec or rec.get("workload") != workload or rec.get("heads") != heads:
+        return None
+    src = os.path.join(ROOT, rec["source"])
+    with open(src, "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest()[:16] != rec["sha256_16"]:
+            return None
+    return rec["bytes_per_launch"]
+
+
 def attn_kernel_flops(w, nh, kernel):
     """MMA FLOPs one launch of an attention kernel does over the visible pairs of nh heads:
     fwd / recompute: Q K^T and P V (4 Dh per pair); dq: Q K^T, dO V^T, dS K (6 Dh);
@@ -343,7 +361,7 @@ def main():
         dom = max(ktimes, key=lambda n: ktimes[n] * n_chunks)
         achieved = attn_kernel_flops(w, hpc, dom) / (ktimes[dom] * 1e-3) / 1e12
         peak = peaks["bf16_tflops"]
-        traffic = None
+        traffic = measured_traffic(dom, args.workload, hpc)
         roofline = {"bound": "tensor", "kernel": f"attention {dom}", "achieved": achieved, "peak": peak,
                     "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
                     "peak_kind": f"{peak_kind} bf16 burst (kernel timed alone)"}
