@@ -68,8 +68,9 @@ __device__ __forceinline__ void mma_acc(uint32_t d, uint32_t a_tmem, uint32_t bb
 
 // dS = P (dP - D) for 64 packed P pairs, dP in the region, result written over columns [0, 64):
 // half h reads dP columns [64h, 64h + 64) and writes [32h, 32h + 32), already read.
+// ndval(k) returns (-D[k], -D[k+1]); the arithmetic runs on fp32 pairs.
 template <typename DFn>
-__device__ __forceinline__ void ds_pass(uint32_t r_addr, const uint32_t (&pk)[64], DFn dval) {
+__device__ __forceinline__ void ds_pass(uint32_t r_addr, const uint32_t (&pk)[64], DFn ndval) {
 #pragma unroll
   for (int hf = 0; hf < 2; ++hf) {
     uint32_t v0[32], v1[32], o[32];
@@ -79,13 +80,13 @@ __device__ __forceinline__ void ds_pass(uint32_t r_addr, const uint32_t (&pk)[64
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int k0 = hf * 64 + 2 * i, k1 = hf * 64 + 32 + 2 * i;
-      const float2 d0 = dval(k0), d1 = dval(k1);
-      const __nv_bfloat162 pa = *reinterpret_cast<const __nv_bfloat162*>(&pk[hf * 32 + i]);
-      const __nv_bfloat162 pb = *reinterpret_cast<const __nv_bfloat162*>(&pk[hf * 32 + 16 + i]);
-      o[i] = tc::pack_bf16x2(__low2float(pa) * (__uint_as_float(v0[2 * i]) - d0.x),
-                             __high2float(pa) * (__uint_as_float(v0[2 * i + 1]) - d0.y));
-      o[16 + i] = tc::pack_bf16x2(__low2float(pb) * (__uint_as_float(v1[2 * i]) - d1.x),
-                                  __high2float(pb) * (__uint_as_float(v1[2 * i + 1]) - d1.y));
+      const float2 pa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[hf * 32 + i]));
+      const float2 pb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[hf * 32 + 16 + i]));
+      const float2 da = __fadd2_rn(make_float2(__uint_as_float(v0[2 * i]), __uint_as_float(v0[2 * i + 1])), ndval(k0));
+      const float2 db = __fadd2_rn(make_float2(__uint_as_float(v1[2 * i]), __uint_as_float(v1[2 * i + 1])), ndval(k1));
+      const float2 ra = __fmul2_rn(pa, da), rb = __fmul2_rn(pb, db);
+      o[i] = tc::pack_bf16x2(ra.x, ra.y);
+      o[16 + i] = tc::pack_bf16x2(rb.x, rb.y);
     }
     tc::tmem_st32(r_addr + hf * 32, o);
   }
@@ -290,10 +291,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dq_tc(const __grid_con
             lo = (int)max((int64_t)-1, min(vis_lo - col0, (int64_t)128));
             hi = (int)max((int64_t)-1, min(vis_hi - col0, (int64_t)128));
           }
+          const float2 cc = make_float2(c, c), nl = make_float2(-lse2, -lse2);
 #pragma unroll
           for (int i = 0; i < 64; ++i) {
-            float p0 = fast_exp2(fmaf(__uint_as_float(sv[2 * i]), c, -lse2));
-            float p1 = fast_exp2(fmaf(__uint_as_float(sv[2 * i + 1]), c, -lse2));
+            const float2 arg = __ffma2_rn(make_float2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])), cc, nl);
+            float p0 = fast_exp2(arg.x);
+            float p1 = fast_exp2(arg.y);
             if (partial) {
               if (2 * i < lo || 2 * i > hi) p0 = 0.f;
               if (2 * i + 1 < lo || 2 * i + 1 > hi) p1 = 0.f;
@@ -306,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dq_tc(const __grid_con
         ok = tc::mbar_wait(&dp_full[t], cnt & 1, abort_flag, a.err);
         if (!ok) break;
         tc::fence_after_sync();
-        ds_pass(r_addr, pk, [&](int) { return make_float2(Dr, Dr); });
+        ds_pass(r_addr, pk, [&](int) { return make_float2(-Dr, -Dr); });
         tc::fence_before_sync();
         tc::mbar_arrive(&ds_full[t]);
       }
@@ -348,7 +351,8 @@ template <int DH>
 struct DkvLayout {
   static constexpr uint32_t TB = 128 * DH * 2;
   static constexpr int NQ = 3, NO = 2;  // Q ring, dO ring
-  static constexpr uint32_t K = 0, V = TB, QR = 2 * TB, OR = QR + NQ * TB, BAR = OR + NO * TB;
+  static constexpr uint32_t K = 0, V = TB, QR = 2 * TB, OR = QR + NQ * TB, VEC = OR + NO * TB;
+  static constexpr uint32_t BAR = VEC + 2 * 256 * 4;  // per element-wise group: -lse*log2e [128], -D [128]
   static constexpr uint32_t BYTES = BAR + 256;
   static constexpr uint32_t TMEM_COLS = 512;
   __device__ static constexpr uint32_t r_col(int t) { return t * 128; }  // S^T / P^T / dP^T / dS^T
@@ -365,7 +369,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
   constexpr int NQ = L::NQ, NO = L::NO;
   const AttnArgs& a = b.f;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // this kernel uses all but ~0.7 KB of the 227 KB: no room to round the base up, so it relies on
+  // the dynamic shared memory window starting 1024-byte aligned and reports otherwise
+  uint8_t* smem = smem_raw;
+  if (smem_u32(smem_raw) & 1023) {
+    if (threadIdx.x == 0 && b.f.err) atomicCAS(b.f.err, 0, (int)UPIPE_ERR_UNSUPPORTED);
+    return;
+  }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::BAR);
   uint64_t* kv_full = bars + 0;
   uint64_t* s_full = bars + 1;    // [2] per region
@@ -459,22 +469,30 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
           mma_nt<DH>(tmem + L::r_col(n & 1), sK, sQ + (n % NQ) * L::TB);
           tc::mma_commit(&s_full[n & 1]);
         };
-        for (int n = 0; n < 2 && n < n_items; ++n) issue_st(n);
-        for (int n = 0; ok && n < n_items; ++n) {
+        // software pipeline: dV/dP^T of item n+1 are issued before dK of item n, so the tensor
+        // core works while the element-wise group of item n computes dS^T
+        auto issue_dv_dp = [&](int n) {
           const int rr = n & 1;
-          const uint32_t qb = sQ + (n % NQ) * L::TB, ob = sO + (n % NO) * L::TB;
+          const uint32_t ob = sO + (n % NO) * L::TB;
           ok = tc::mbar_wait(&p_full[rr], (n >> 1) & 1, abort_flag, a.err);
           if (ok) ok = tc::mbar_wait(&o_full[n % NO], (n / NO) & 1, abort_flag, a.err);
-          if (!ok) break;
+          if (!ok) return;
           tc::fence_after_sync();
           mma_acc<DH>(tmem + L::DV_COL, tmem + L::r_col(rr), ob, n > 0);  // dV += P^T dO
           mma_nt<DH>(tmem + L::r_col(rr), sV, ob);                         // dP^T = V dO^T
           tc::mma_commit(&dp_full[rr]);
           tc::mma_commit(&o_empty[n % NO]);
+        };
+        for (int n = 0; n < 2 && n < n_items; ++n) issue_st(n);
+        if (ok && n_items > 0) issue_dv_dp(0);
+        for (int n = 0; ok && n < n_items; ++n) {
+          const int rr = n & 1;
+          if (n + 1 < n_items) issue_dv_dp(n + 1);
+          if (!ok) break;
           ok = tc::mbar_wait(&ds_full[rr], (n >> 1) & 1, abort_flag, a.err);
           if (!ok) break;
           tc::fence_after_sync();
-          mma_acc<DH>(tmem + L::DK_COL, tmem + L::r_col(rr), qb, n > 0);   // dK += dS^T Q
+          mma_acc<DH>(tmem + L::DK_COL, tmem + L::r_col(rr), sQ + (n % NQ) * L::TB, n > 0);  // dK += dS^T Q
           tc::mma_commit(&q_empty[n % NQ]);
           if (n == n_items - 1) tc::mma_commit(acc_full);
           if (n + 2 < n_items) issue_st(n + 2);
@@ -496,6 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
     }
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
     const uint32_t r_addr = lane_addr + L::r_col(grp);
+    float* nvec = reinterpret_cast<float*>(smem + L::VEC) + grp * 256;  // this group's -lse2 | -D
     const float c = a.scale * 1.4426950408889634f;
     const bool ragged = (S % kTile) != 0;
     bool ok = true;
@@ -503,8 +522,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
       const int hh = h_first + n / nq;
       const int qi = tr.x + n % nq;
       const bool partial = qi < tr.y || qi >= tr.z || (ragged && (qi == nt - 1 || jt == nt - 1));
-      const float* dq_d = a.D + (int64_t)hh * sp + (int64_t)qi * kTile;              // D of the 128 queries
-      const float* dq_l = a.D + ((int64_t)a.nh + hh) * sp + (int64_t)qi * kTile;     // lse*log2e
       const int cyc = (n >> 1) & 1;
       int lo = 0, hi = 127;
       if (partial) {
@@ -512,6 +529,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
         lo = (int)max((int64_t)-1, min(vis_lo - col0, (int64_t)128));
         hi = (int)max((int64_t)-1, min(vis_hi - col0, (int64_t)128));
       }
+      // stage -lse*log2e and -D of the item's 128 queries in shared memory (one per thread)
+      tc::named_bar_sync(1 + grp, 128);  // the previous item's readers are done
+      {
+        const int64_t qoff = (int64_t)qi * kTile + r;
+        nvec[r] = -a.D[((int64_t)a.nh + hh) * sp + qoff];
+        nvec[128 + r] = -a.D[(int64_t)hh * sp + qoff];
+      }
+      tc::named_bar_sync(1 + grp, 128);
       ok = tc::mbar_wait(&s_full[grp], cyc, abort_flag, a.err);
       if (!ok) break;
       tc::fence_after_sync();
@@ -519,14 +544,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
       {
         uint32_t sv[128];
         tmem_ld128(r_addr, sv);
+        const float2 cc = make_float2(c, c);
 #pragma unroll
         for (int i = 0; i < 64; i += 2) {
-          const float4 l4 = __ldg(reinterpret_cast<const float4*>(dq_l + 2 * i));
+          const float4 l4 = *reinterpret_cast<const float4*>(nvec + 2 * i);
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
             const int k = 2 * (i + u);
-            float p0 = fast_exp2(fmaf(__uint_as_float(sv[k]), c, -(u ? l4.z : l4.x)));
-            float p1 = fast_exp2(fmaf(__uint_as_float(sv[k + 1]), c, -(u ? l4.w : l4.y)));
+            const float2 arg = __ffma2_rn(make_float2(__uint_as_float(sv[k]), __uint_as_float(sv[k + 1])), cc,
+                                          u ? make_float2(l4.z, l4.w) : make_float2(l4.x, l4.y));
+            float p0 = fast_exp2(arg.x);
+            float p1 = fast_exp2(arg.y);
             if (partial) {
               if (k < lo || k > hi) p0 = 0.f;
               if (k + 1 < lo || k + 1 > hi) p1 = 0.f;
@@ -543,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
       ok = tc::mbar_wait(&dp_full[grp], cyc, abort_flag, a.err);
       if (!ok) break;
       tc::fence_after_sync();
-      ds_pass(r_addr, pk, [&](int k) { return __ldg(reinterpret_cast<const float2*>(dq_d + k)); });
+      ds_pass(r_addr, pk, [&](int k) { return *reinterpret_cast<const float2*>(nvec + 128 + k); });
       tc::fence_before_sync();
       tc::mbar_arrive(&ds_full[grp]);
     }
@@ -607,7 +635,7 @@ template <typename KFN>
 cudaError_t launch(KFN kfn, size_t bytes, dim3 grid, const CUtensorMap& tq, const CUtensorMap& tdo,
                    const CUtensorMap& tk, const CUtensorMap& tv, const AttnBwdArgs& b, cudaStream_t st) {
   // at least 120 KB so that two CTAs never share an SM (each takes all 512 TMEM columns)
-  const size_t smem = bytes + 1024 > 120 * 1024 ? bytes + 1024 : 120 * 1024;
+  const size_t smem = bytes > 120 * 1024 ? bytes : 120 * 1024;
   cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   kfn<<<grid, kThreads, smem, st>>>(tq, tdo, tk, tv, b);
@@ -619,7 +647,7 @@ cudaError_t run_dq(const AttnBwdArgs& b, cudaStream_t st) {
   CUtensorMap tq, tdo, tk, tv;
   if (!make_maps<DH>(b.f, &tq, &tdo, &tk, &tv)) return cudaErrorInvalidValue;
   const int nt = (int)ceil_div(b.f.S, kTile);
-  return launch(k_attn_bwd_dq_tc<DH>, DqLayout<DH>::BYTES, dim3((unsigned)ceil_div(nt, 2), (unsigned)b.f.nh), tq,
+  return launch(k_attn_bwd_dq_tc<DH>, DqLayout<DH>::BYTES + 1024, dim3((unsigned)ceil_div(nt, 2), (unsigned)b.f.nh), tq,
                 tdo, tk, tv, b, st);
 }
 

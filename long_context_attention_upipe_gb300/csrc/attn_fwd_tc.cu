@@ -251,19 +251,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           mu = m_used;
         }
         // P = exp2(s * c - mu) as bf16 pairs into the first 64 columns of S (already read)
-        float l4[4] = {0.f, 0.f, 0.f, 0.f};
+        float2 l2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        const float2 cc = make_float2(c, c), nmu = make_float2(-mu, -mu);
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           uint32_t pk[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            const float p0 = fast_exp2(fmaf(__uint_as_float(sv[hf * 64 + 2 * i]), c, -mu));
-            const float p1 = fast_exp2(fmaf(__uint_as_float(sv[hf * 64 + 2 * i + 1]), c, -mu));
-            l4[i & 3] += p0 + p1;
-            pk[i] = tc::pack_bf16x2(p0, p1);
+            const float2 arg = __ffma2_rn(
+                make_float2(__uint_as_float(sv[hf * 64 + 2 * i]), __uint_as_float(sv[hf * 64 + 2 * i + 1])), cc, nmu);
+            const float2 p = make_float2(fast_exp2(arg.x), fast_exp2(arg.y));
+            l2[i & 1] = __fadd2_rn(l2[i & 1], p);
+            pk[i] = tc::pack_bf16x2(p.x, p.y);
           }
           tc::tmem_st32(s_addr + hf * 32, pk);
         }
+        const float l4[4] = {l2[0].x, l2[0].y, l2[1].x, l2[1].y};
         tc::tmem_st_wait();
         if (MODE == 0 && __any_sync(0xffffffffu, rescale_o)) {
           // O_t is idle here: P V of the previous tile completed before this S was ready, and

@@ -8,8 +8,8 @@
 // Wqkv that belong to a chunk (a 2-D map plus the first row of each block).
 //
 // Persistent kernel, one CTA per SM, 6 warps:
-//   warp 0     TMA producer over a 6-stage ring of (A 128x64, B 128x64) tiles
-//   warp 1     MMA issuer (one thread), TMEM owner: 4 tcgen05.mma (M128 N128 K16) per stage into
+//   warp 0     TMA producer over a 4-stage ring of (A 128x64, B 256x64) tiles
+//   warp 1     MMA issuer (one thread), TMEM owner: 4 tcgen05.mma (M128 N256 K16) per stage into
 //              one of two TMEM accumulators, so the epilogue of a tile overlaps the next tile
 //   warps 2-5  epilogue: one output row per thread (TMEM lane), 32 columns at a time
 // Split-K (weight gradients, K = S) writes fp32 partials that k_split_reduce sums in order.
@@ -20,10 +20,11 @@ namespace upipe {
 
 namespace {
 
-constexpr int BM = 128, BN = 128, BK = 64, STAGES = 6, THREADS = 192;
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4, THREADS = 192;
 constexpr uint32_t BOX = 64 * 64 * 2;          // one 64 x 64 bf16 box, 8 KB
-constexpr uint32_t TILE = 2 * BOX;             // one 128 x 64 operand tile
-constexpr uint32_t STAGE = 2 * TILE;           // A + B
+constexpr uint32_t TILE_A = 2 * BOX;           // 128 x 64 A tile
+constexpr uint32_t TILE_B = 4 * BOX;           // 256 x 64 B tile
+constexpr uint32_t STAGE = TILE_A + TILE_B;
 constexpr uint32_t BAR_OFF = STAGES * STAGE;
 constexpr uint32_t SMEM_BYTES = BAR_OFF + 256 + 1024;
 
@@ -115,7 +116,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_gemm_tc(const __grid_constant__ 
     tc::fence_mbar_init();
   }
   if (warp == 1) {
-    tc::tmem_alloc(tmem_slot, 256);
+    tc::tmem_alloc(tmem_slot, 2 * BN);
     tc::tmem_relinquish();
   }
   tc::fence_before_sync();
@@ -152,10 +153,9 @@ __global__ void __launch_bounds__(THREADS, 1) k_gemm_tc(const __grid_constant__ 
           tc::mbar_arrive_expect_tx(&full[s], STAGE);
           uint8_t* sa = smem + s * STAGE;
           const int64_t k = (int64_t)ks * p.k_per_split + (int64_t)kt * BK;
-          for (int i = 0; i < 2; ++i) {
-            load_box(sa + i * BOX, &ta, p.a, &full[s], (int64_t)tm * BM + 64 * i, k);
-            load_box(sa + TILE + i * BOX, &tb, p.b, &full[s], (int64_t)tn * BN + 64 * i, k);
-          }
+          for (int i = 0; i < BM / 64; ++i) load_box(sa + i * BOX, &ta, p.a, &full[s], (int64_t)tm * BM + 64 * i, k);
+          for (int i = 0; i < BN / 64; ++i)
+            load_box(sa + TILE_A + i * BOX, &tb, p.b, &full[s], (int64_t)tn * BN + 64 * i, k);
         }
       }
     }
@@ -172,12 +172,12 @@ __global__ void __launch_bounds__(THREADS, 1) k_gemm_tc(const __grid_constant__ 
         const int buf = tcount & 1;
         if (tcount >= 2 && !(ok = tc::mbar_wait(&acc_empty[buf], ((tcount >> 1) - 1) & 1, abort_flag, nullptr))) break;
         tc::fence_after_sync();
-        const uint32_t d = tmem + buf * 128;
+        const uint32_t d = tmem + buf * BN;
         for (int kt = 0; kt < nk; ++kt, ++it) {
           const int s = it % STAGES;
           if (!(ok = tc::mbar_wait(&full[s], (it / STAGES) & 1, abort_flag, nullptr))) break;
           tc::fence_after_sync();
-          const uint32_t sa = smem_u32(smem + s * STAGE), sb = sa + TILE;
+          const uint32_t sa = smem_u32(smem + s * STAGE), sb = sa + TILE_A;
 #pragma unroll
           for (int k16 = 0; k16 < BK / 16; ++k16)
             tc::mma_ss(d, tile_desc(sa, p.a.k_major, k16), tile_desc(sb, p.b.k_major, k16), idesc, kt > 0 || k16 > 0);
@@ -205,7 +205,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_gemm_tc(const __grid_constant__ 
 #pragma unroll 1
       for (int ch = 0; ch < BN / 32; ++ch) {
         uint32_t v[32];
-        tc::tmem_ld32(lane_addr + buf * 128 + ch * 32, v);
+        tc::tmem_ld32(lane_addr + buf * BN + ch * 32, v);
         tc::tmem_ld_wait();
         if (nk == 0) {
 #pragma unroll
@@ -290,7 +290,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_gemm_tc(const __grid_constant__ 
   __syncthreads();
   if (warp == 1) {
     tc::fence_after_sync();
-    tc::tmem_dealloc(tmem, 256);
+    tc::tmem_dealloc(tmem, 2 * BN);
   }
 }
 
