@@ -295,8 +295,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dq_tc(const __grid_con
 #pragma unroll
           for (int i = 0; i < 64; ++i) {
             const float2 arg = __ffma2_rn(make_float2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])), cc, nl);
-            float p0 = fast_exp2(arg.x);
-            float p1 = fast_exp2(arg.y);
+            const float2 pe = (i & 1) ? tc::exp2_fma2(arg) : make_float2(fast_exp2(arg.x), fast_exp2(arg.y));
+            float p0 = pe.x;
+            float p1 = pe.y;
             if (partial) {
               if (2 * i < lo || 2 * i > hi) p0 = 0.f;
               if (2 * i + 1 < lo || 2 * i + 1 > hi) p1 = 0.f;
@@ -432,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
   const uint32_t tmem = *tmem_slot;
 
   if (warp < 4) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;\n" ::: "memory");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 72;\n" ::: "memory");
     if (warp == 0) {
       if (lane == 0) {
         tc::prefetch_tmap(&tq);
@@ -483,19 +484,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
           tc::mma_commit(&dp_full[rr]);
           tc::mma_commit(&o_empty[n % NO]);
         };
-        for (int n = 0; n < 2 && n < n_items; ++n) issue_st(n);
-        if (ok && n_items > 0) issue_dv_dp(0);
-        for (int n = 0; ok && n < n_items; ++n) {
+        auto issue_dk = [&](int n) {
           const int rr = n & 1;
-          if (n + 1 < n_items) issue_dv_dp(n + 1);
-          if (!ok) break;
           ok = tc::mbar_wait(&ds_full[rr], (n >> 1) & 1, abort_flag, a.err);
-          if (!ok) break;
+          if (!ok) return;
           tc::fence_after_sync();
           mma_acc<DH>(tmem + L::DK_COL, tmem + L::r_col(rr), sQ + (n % NQ) * L::TB, n > 0);  // dK += dS^T Q
           tc::mma_commit(&q_empty[n % NQ]);
           if (n == n_items - 1) tc::mma_commit(acc_full);
           if (n + 2 < n_items) issue_st(n + 2);
+        };
+        // items in pairs (one per element-wise group): dV/dP^T of both, then dK and the next S^T
+        // of each, so no wait blocks work that is already possible
+        for (int n = 0; n < 2 && n < n_items; ++n) issue_st(n);
+        for (int n = 0; ok && n < n_items; n += 2) {
+#pragma unroll 1
+          for (int step = 0; step < 4 && ok; ++step) {  // dV/dP^T(n), dV/dP^T(n+1), dK(n), dK(n+1)
+            const int m = n + (step & 1);
+            if (m >= n_items) continue;
+            if (step < 2) issue_dv_dp(m); else issue_dk(m);
+          }
         }
       }
       __syncwarp();

@@ -163,6 +163,27 @@ __device__ __forceinline__ void named_bar_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// 2^x for a pair of arguments on the FMA/ALU pipes, to take part of the softmax exponentials off
+// the MUFU unit.  Cody-Waite range reduction: n = round(x) from the 1.5 * 2^23 shifter and
+// f = x - n in [-1/2, 1/2]; 2^f from a degree-3 polynomial fitted here to 2^f on [-1/2, 1/2]
+// (relative minimax by Lawson-reweighted least squares on Chebyshev points; max relative error
+// 7.5e-5 in fp32 evaluation, below the bf16 rounding P gets next); 2^n is added to the exponent
+// field.  Arguments below -125 (masked scores are -inf) give exactly 0.
+__device__ __forceinline__ float2 exp2_fma2(float2 x) {
+  const float2 shift = make_float2(12582912.f, 12582912.f);  // 1.5 * 2^23
+  const float2 t = __fadd2_rn(make_float2(fmaxf(x.x, -125.f), fmaxf(x.y, -125.f)), shift);
+  const float2 f = __fadd2_rn(make_float2(fmaxf(x.x, -125.f), fmaxf(x.y, -125.f)),
+                              __fadd2_rn(t, make_float2(-12582912.f, -12582912.f)));
+  float2 p = __ffma2_rn(make_float2(0.055171655627233016f, 0.055171655627233016f), f,
+                        make_float2(0.24261114021856436f, 0.24261114021856436f));
+  p = __ffma2_rn(p, f, make_float2(0.6932609895940305f, 0.6932609895940305f));
+  p = __ffma2_rn(p, f, make_float2(0.9999280725445912f, 0.9999280725445912f));
+  float2 r;
+  r.x = x.x > -125.f ? __int_as_float(__float_as_int(p.x) + (__float_as_int(t.x) << 23)) : 0.f;
+  r.y = x.y > -125.f ? __int_as_float(__float_as_int(p.y) + (__float_as_int(t.y) << 23)) : 0.f;
+  return r;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
