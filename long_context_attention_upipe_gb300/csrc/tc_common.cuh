@@ -178,9 +178,11 @@ __device__ __forceinline__ float2 exp2_fma2(float2 x) {
                         make_float2(0.24261114021856436f, 0.24261114021856436f));
   p = __ffma2_rn(p, f, make_float2(0.6932609895940305f, 0.6932609895940305f));
   p = __ffma2_rn(p, f, make_float2(0.9999280725445912f, 0.9999280725445912f));
+  // n << 23 taken from the shifter's bits in unsigned arithmetic (the low 9 bits of t hold n mod
+  // 2^9; the shifter's own bits shift out), added to the exponent field of 2^f
   float2 r;
-  r.x = x.x > -125.f ? __int_as_float(__float_as_int(p.x) + (__float_as_int(t.x) << 23)) : 0.f;
-  r.y = x.y > -125.f ? __int_as_float(__float_as_int(p.y) + (__float_as_int(t.y) << 23)) : 0.f;
+  r.x = x.x > -125.f ? __uint_as_float(__float_as_uint(p.x) + (__float_as_uint(t.x) << 23)) : 0.f;
+  r.y = x.y > -125.f ? __uint_as_float(__float_as_uint(p.y) + (__float_as_uint(t.y) << 23)) : 0.f;
   return r;
 }
 
