@@ -169,22 +169,21 @@ __device__ __forceinline__ void named_bar_sync(int id, int threads) {
 // (relative minimax by Lawson-reweighted least squares on Chebyshev points; max relative error
 // 7.5e-5 in fp32 evaluation, below the bf16 rounding P gets next); 2^n is added to the exponent
 // field.  Arguments below -125 (masked scores are -inf) give exactly 0.
-__device__ __forceinline__ float2 exp2_fma2(float2 x) {
-  const float2 shift = make_float2(12582912.f, 12582912.f);  // 1.5 * 2^23
-  const float2 t = __fadd2_rn(make_float2(fmaxf(x.x, -125.f), fmaxf(x.y, -125.f)), shift);
-  const float2 f = __fadd2_rn(make_float2(fmaxf(x.x, -125.f), fmaxf(x.y, -125.f)),
-                              __fadd2_rn(t, make_float2(-12582912.f, -12582912.f)));
-  float2 p = __ffma2_rn(make_float2(0.055171655627233016f, 0.055171655627233016f), f,
-                        make_float2(0.24261114021856436f, 0.24261114021856436f));
-  p = __ffma2_rn(p, f, make_float2(0.6932609895940305f, 0.6932609895940305f));
-  p = __ffma2_rn(p, f, make_float2(0.9999280725445912f, 0.9999280725445912f));
-  // n << 23 taken from the shifter's bits in unsigned arithmetic (the low 9 bits of t hold n mod
-  // 2^9; the shifter's own bits shift out), added to the exponent field of 2^f
-  float2 r;
-  r.x = x.x > -125.f ? __uint_as_float(__float_as_uint(p.x) + (__float_as_uint(t.x) << 23)) : 0.f;
-  r.y = x.y > -125.f ? __uint_as_float(__float_as_uint(p.y) + (__float_as_uint(t.y) << 23)) : 0.f;
-  return r;
+__device__ __forceinline__ float exp2_fma(float x) {
+  const float xc = fmaxf(x, -125.f);
+  const float t = __fadd_rn(xc, 12582912.f);         // 1.5 * 2^23 + round(xc)
+  const float n = __fadd_rn(t, -12582912.f);         // round(xc), exact
+  const float f = __fadd_rn(xc, -n);                 // in [-1/2, 1/2], exact
+  float p = __fmaf_rn(0.055171655627233016f, f, 0.24261114021856436f);
+  p = __fmaf_rn(p, f, 0.6932609895940305f);
+  p = __fmaf_rn(p, f, 0.9999280725445912f);
+  // n * 2^23 from the shifter's bits in unsigned arithmetic (its low 9 bits hold n mod 2^9, the
+  // shifter's own bits shift out), added to the exponent field of 2^f
+  const uint32_t bits = __float_as_uint(p) + (__float_as_uint(t) << 23);
+  return x > -125.f ? __uint_as_float(bits) : 0.f;
 }
+
+__device__ __forceinline__ float2 exp2_fma2(float2 x) { return make_float2(exp2_fma(x.x), exp2_fma(x.y)); }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
