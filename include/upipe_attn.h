@@ -177,11 +177,6 @@ upipe_status_t upipe_attn_core_bwd_dkdv(const upipe_attn_desc_t* desc, const uin
 upipe_status_t upipe_attn_gemm_nt(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda,
                                   const uint16_t* B, int64_t ldb, float* C, int64_t ldc, void* stream);
 
-/* Evaluates, for testing, the exponential the attention kernels compute on the FMA pipe for
- * part of their softmax terms: y[i] = 2^x[i] (range reduction + degree-3 polynomial; exactly 0
- * below -125).  x, y: device fp32 [n]. */
-upipe_status_t upipe_attn_exp2_poly(const float* x, float* y, int64_t n, void* stream);
-
 /* Reads the device error word of a workspace (after fwd/bwd) or of a table (after
  * build_tile_table) into *code (a upipe_status_t value; UPIPE_OK when none).  Synchronises
  * `stream`.  `buf` is the workspace or the table. */

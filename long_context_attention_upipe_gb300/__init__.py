@@ -22,7 +22,7 @@ UPIPE_OK = 0
 EXPORTS = ["upipe_attn_status_string", "upipe_attn_last_error_string", "upipe_attn_workspace_size", "upipe_attn_tile_table_size",
            "upipe_attn_build_tile_table", "upipe_attn_fwd", "upipe_attn_bwd", "upipe_attn_core_fwd",
            "upipe_attn_core_recompute", "upipe_attn_core_bwd_dq", "upipe_attn_core_bwd_dkdv", "upipe_attn_gemm_nt",
-           "upipe_attn_device_status", "upipe_attn_fwd_no_alloc", "upipe_attn_exp2_poly"]
+           "upipe_attn_device_status", "upipe_attn_fwd_no_alloc"]
 
 
 class Desc(ctypes.Structure):
@@ -69,7 +69,6 @@ def lib():
             "upipe_attn_gemm_nt": ([I64, I64, I64, P, I64, P, I64, P, I64, P], ctypes.c_int),
             "upipe_attn_device_status": ([P, ctypes.POINTER(ctypes.c_int32), P], ctypes.c_int),
             "upipe_attn_fwd_no_alloc": ([D, P, P, P, P, P, P, P], ctypes.c_int),
-            "upipe_attn_exp2_poly": ([P, P, I64, P], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -166,10 +165,6 @@ def core_bwd(desc: Desc, q, k, v, dO, lse, seg, table, dq, dk, dv, stream=None):
     core_bwd_dq(desc, q, k, v, dO, lse, D, seg, table, dq, stream)
     core_bwd_dkdv(desc, q, k, v, dO, lse, D, seg, table, dk, dv, stream)
     return o, D
-
-
-def exp2_poly(x, y, stream=None):
-    _check(lib().upipe_attn_exp2_poly(_ptr(x), _ptr(y), x.numel(), _stream(stream)), "exp2_poly")
 
 
 def gemm_nt(A, B, C, stream=None):

@@ -538,11 +538,6 @@ upipe_status_t upipe_attn_gemm_nt(int64_t M, int64_t N, int64_t K, const uint16_
   return cuda_status(launch_gemm_tc(g, 1, nullptr, (cudaStream_t)stream));
 }
 
-upipe_status_t upipe_attn_exp2_poly(const float* x, float* y, int64_t n, void* stream) {
-  if (n < 0 || (n > 0 && (!x || !y))) return UPIPE_ERR_INVALID_ARG;
-  return cuda_status(launch_exp2_poly(x, y, n, (cudaStream_t)stream));
-}
-
 upipe_status_t upipe_attn_device_status(const void* buf, int32_t* code, void* stream) {
   if (!buf || !code) return UPIPE_ERR_INVALID_ARG;
   int32_t v = 0;

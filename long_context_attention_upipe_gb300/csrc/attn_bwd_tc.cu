@@ -295,9 +295,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dq_tc(const __grid_con
 #pragma unroll
           for (int i = 0; i < 64; ++i) {
             const float2 arg = __ffma2_rn(make_float2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])), cc, nl);
-            const float2 pe = (i & 1) ? tc::exp2_fma2(arg) : make_float2(fast_exp2(arg.x), fast_exp2(arg.y));
-            float p0 = pe.x;
-            float p1 = pe.y;
+            float p0 = fast_exp2(arg.x);
+            float p1 = fast_exp2(arg.y);
             if (partial) {
               if (2 * i < lo || 2 * i > hi) p0 = 0.f;
               if (2 * i + 1 < lo || 2 * i + 1 > hi) p1 = 0.f;

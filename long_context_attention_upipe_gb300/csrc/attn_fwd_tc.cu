@@ -260,8 +260,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           for (int i = 0; i < 32; ++i) {
             const float2 arg = __ffma2_rn(
                 make_float2(__uint_as_float(sv[hf * 64 + 2 * i]), __uint_as_float(sv[hf * 64 + 2 * i + 1])), cc, nmu);
-            // every other pair on the FMA pipe: the MUFU unit would otherwise pace the kernel
-            const float2 p = (i & 1) ? tc::exp2_fma2(arg) : make_float2(fast_exp2(arg.x), fast_exp2(arg.y));
+            const float2 p = make_float2(fast_exp2(arg.x), fast_exp2(arg.y));
             l2[i & 1] = __fadd2_rn(l2[i & 1], p);
             pk[i] = tc::pack_bf16x2(p.x, p.y);
           }

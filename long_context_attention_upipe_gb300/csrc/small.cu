@@ -2,7 +2,6 @@
 // Grid-stride loops over 16-byte vectors, grid sized to a few waves of the 152 SMs.
 #include "common.cuh"
 #include "internal.h"
-#include "tc_common.cuh"
 
 namespace upipe {
 
@@ -30,15 +29,6 @@ __global__ void k_zero(uint4* __restrict__ p, int64_t n16) {
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride) p[i] = make_uint4(0, 0, 0, 0);
 }
 
-__global__ void k_exp2_poly(const float* __restrict__ x, float* __restrict__ y, int64_t n) {
-  const int64_t i = 2 * ((int64_t)blockIdx.x * blockDim.x + threadIdx.x);
-  if (i >= n) return;
-  const float2 v = make_float2(x[i], i + 1 < n ? x[i + 1] : 0.f);
-  const float2 r = tc::exp2_fma2(v);
-  y[i] = r.x;
-  if (i + 1 < n) y[i + 1] = r.y;
-}
-
 unsigned grid_for(int64_t work) { return (unsigned)std::max<int64_t>(1, std::min<int64_t>(ceil_div(work, 256), 152 * 16)); }
 
 }  // namespace
@@ -46,12 +36,6 @@ unsigned grid_for(int64_t work) { return (unsigned)std::max<int64_t>(1, std::min
 cudaError_t launch_f32_to_bf16(const float* in, bf16* out, int64_t n, float mul, cudaStream_t st) {
   if (n <= 0) return cudaSuccess;
   k_f32_to_bf16<<<grid_for(n / 8 + 1), 256, 0, st>>>(in, out, n, mul);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_exp2_poly(const float* x, float* y, int64_t n, cudaStream_t st) {
-  if (n <= 0) return cudaSuccess;
-  k_exp2_poly<<<(unsigned)ceil_div(ceil_div(n, 2), 256), 256, 0, st>>>(x, y, n);
   return cudaGetLastError();
 }
 

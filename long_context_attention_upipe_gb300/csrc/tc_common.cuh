@@ -163,28 +163,6 @@ __device__ __forceinline__ void named_bar_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
-// 2^x for a pair of arguments on the FMA/ALU pipes, to take part of the softmax exponentials off
-// the MUFU unit.  Cody-Waite range reduction: n = round(x) from the 1.5 * 2^23 shifter and
-// f = x - n in [-1/2, 1/2]; 2^f from a degree-3 polynomial fitted here to 2^f on [-1/2, 1/2]
-// (relative minimax by Lawson-reweighted least squares on Chebyshev points; max relative error
-// 7.5e-5 in fp32 evaluation, below the bf16 rounding P gets next); 2^n is added to the exponent
-// field.  Arguments below -125 (masked scores are -inf) give exactly 0.
-__device__ __forceinline__ float exp2_fma(float x) {
-  const float xc = fmaxf(x, -125.f);
-  const float t = __fadd_rn(xc, 12582912.f);         // 1.5 * 2^23 + round(xc)
-  const float n = __fadd_rn(t, -12582912.f);         // round(xc), exact
-  const float f = __fadd_rn(xc, -n);                 // in [-1/2, 1/2], exact
-  float p = __fmaf_rn(0.055171655627233016f, f, 0.24261114021856436f);
-  p = __fmaf_rn(p, f, 0.6932609895940305f);
-  p = __fmaf_rn(p, f, 0.9999280725445912f);
-  // n * 2^23 from the shifter's bits in unsigned arithmetic (its low 9 bits hold n mod 2^9, the
-  // shifter's own bits shift out), added to the exponent field of 2^f
-  const uint32_t bits = __float_as_uint(p) + (__float_as_uint(t) << 23);
-  return x > -125.f ? __uint_as_float(bits) : 0.f;
-}
-
-__device__ __forceinline__ float2 exp2_fma2(float2 x) { return make_float2(exp2_fma(x.x), exp2_fma(x.y)); }
-
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);

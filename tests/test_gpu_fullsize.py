@@ -90,10 +90,10 @@ def test_full_size_layer(key, hpc, prefix):
     # bf16-in/fp32-accumulate contraction becomes 2e-2 here.  Relative Frobenius keeps 5e-3.
     assert max_abs_bf16_out(y, Y_ref) <= FULL_OUT_MAX_ABS, max_abs_bf16_out(y, Y_ref)
     assert rel_fro(y, Y_ref) <= OUT_REL_FRO, rel_fro(y, Y_ref)
-    # the log-sum-exp inherits the bf16 rounding of Q and K, an error proportional to the scores:
-    # checked relative to max(1, |lse|)
+    # the log-sum-exp inherits the bf16 rounding of Q and K: |d lse| <= max_j |d s_ij|, about
+    # 2^-8 of the score magnitudes; checked relative to max(1, |lse|) at 2^-7 (about 1e-2)
     lse_err = np.abs(to_f64(lse)[:, rows] - L_ref) / np.maximum(1.0, np.abs(L_ref))
-    assert lse_err.max() <= 1e-3, lse_err.max()
+    assert lse_err.max() <= 1e-2, lse_err.max()
     # backward on the prefix
     Xp = ui.normal_bf16_rows(np.arange(prefix), w.d, ui.TID_X)
     segp = None if seg is None else seg[:prefix]
