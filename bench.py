@@ -41,7 +41,6 @@ def parse():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--no-profile", action="store_true", help="skip the torch-profiler launch count")
     ap.add_argument("--sample-tokens", type=int, default=1024, help="oracle sample length (CPU legs)")
     ap.add_argument("--kernel", default=None, choices=["fwd", "recompute", "dq", "dkdv"],
                     help="time one attention kernel alone at the workload's chunk shapes (for profilers)")
@@ -318,7 +317,9 @@ def main():
     torch.cuda.synchronize()
     sampler = ClockSampler(local)
     sampler.start()
+    launches_before = up.launch_count()
     ms = time_steps(step, args.steps)
+    launches = up.launch_count() - launches_before  # our kernels launched in the timed region
     clocks = sampler.stop()
     peak_gb = torch.cuda.max_memory_allocated(dev) / 1e9
     ms_all = ms
@@ -330,23 +331,6 @@ def main():
 
     result = {}
     if rank == 0:
-        # ---------------- launches of our kernels in one step
-        launches = None
-        launch_note = None
-        if not args.no_profile:
-            try:
-                from torch.profiler import ProfilerActivity, profile
-                with profile(activities=[ProfilerActivity.CUDA]) as prof:
-                    step()
-                    torch.cuda.synchronize()
-                names = [e.name for e in prof.events()]
-                ours = [n for n in names if "upipe" in n and ("k_" in n or "kernel" in n)]
-                launches = len(ours) * args.steps if ours else None
-                if not ours:
-                    launch_note = f"profiler saw {len(names)} events, none of ours"
-            except Exception as ex:  # profiler unavailable: report why
-                launch_note = f"profiler error: {type(ex).__name__}: {ex}"[:200]
-
         # ---------------- per-kernel timing of the attention kernels (same launch configuration)
         hpc = args.hpc
         n_chunks = Hq // hpc
@@ -447,7 +431,6 @@ def main():
             "e2e": e2e,
             "cpu_baseline": cpu,
             "gpu_launches": launches,
-            "gpu_launches_note": launch_note,
             "clocks": clocks,
         }
         print(json.dumps(result), flush=True)

@@ -182,6 +182,11 @@ upipe_status_t upipe_attn_gemm_nt(int64_t M, int64_t N, int64_t K, const uint16_
  * `stream`.  `buf` is the workspace or the table. */
 upipe_status_t upipe_attn_device_status(const void* buf, int32_t* code, void* stream);
 
+/* Number of GPU kernels this library has launched in the process so far (every entry point
+ * counts its own launches; a diagnostic with no counterpart in the method).  The difference of
+ * two reads brackets the launches of the calls between them on any thread. */
+uint64_t upipe_attn_launch_count(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -22,7 +22,7 @@ UPIPE_OK = 0
 EXPORTS = ["upipe_attn_status_string", "upipe_attn_last_error_string", "upipe_attn_workspace_size", "upipe_attn_tile_table_size",
            "upipe_attn_build_tile_table", "upipe_attn_fwd", "upipe_attn_bwd", "upipe_attn_core_fwd",
            "upipe_attn_core_recompute", "upipe_attn_core_bwd_dq", "upipe_attn_core_bwd_dkdv", "upipe_attn_gemm_nt",
-           "upipe_attn_device_status", "upipe_attn_fwd_no_alloc"]
+           "upipe_attn_device_status", "upipe_attn_fwd_no_alloc", "upipe_attn_launch_count"]
 
 
 class Desc(ctypes.Structure):
@@ -69,6 +69,7 @@ def lib():
             "upipe_attn_gemm_nt": ([I64, I64, I64, P, I64, P, I64, P, I64, P], ctypes.c_int),
             "upipe_attn_device_status": ([P, ctypes.POINTER(ctypes.c_int32), P], ctypes.c_int),
             "upipe_attn_fwd_no_alloc": ([D, P, P, P, P, P, P, P], ctypes.c_int),
+            "upipe_attn_launch_count": ([], ctypes.c_uint64),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -122,6 +123,11 @@ def device_status(buf, stream=None) -> int:
     code = ctypes.c_int32(0)
     _check(lib().upipe_attn_device_status(_ptr(buf), ctypes.byref(code), _stream(stream)), "device_status")
     return code.value
+
+
+def launch_count() -> int:
+    """Kernels the library has launched in this process so far."""
+    return int(lib().upipe_attn_launch_count())
 
 
 def fwd(desc: Desc, X, Wqkv, Wo, seg, Y, lse, ws, stream=None):

@@ -20,6 +20,7 @@
 //   dKacc, dVacc f32 [S, Dh] when a chunk holds only part of a KV group (hpc < g)  bwd
 //   dXacc   f32 [S, d] partial input gradient (several chunks, accum_mode 0)   bwd
 //   split   f32 split-K partials of the weight-gradient GEMMs                  bwd
+#include <atomic>
 #include <cmath>
 #include <cstring>
 
@@ -30,6 +31,9 @@ namespace upipe {
 
 // Name of the CUDA error behind the last UPIPE_ERR_CUDA returned on this host thread.
 thread_local const char* g_last_cuda_error = "cudaSuccess";
+
+std::atomic<uint64_t> g_launch_count{0};
+void note_launch() { g_launch_count.fetch_add(1, std::memory_order_relaxed); }
 
 upipe_status_t cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return UPIPE_OK;
@@ -537,6 +541,8 @@ upipe_status_t upipe_attn_gemm_nt(int64_t M, int64_t N, int64_t K, const uint16_
   g.epi = EPI_STORE_F32;
   return cuda_status(launch_gemm_tc(g, 1, nullptr, (cudaStream_t)stream));
 }
+
+uint64_t upipe_attn_launch_count(void) { return upipe::g_launch_count.load(std::memory_order_relaxed); }
 
 upipe_status_t upipe_attn_device_status(const void* buf, int32_t* code, void* stream) {
   if (!buf || !code) return UPIPE_ERR_INVALID_ARG;

@@ -646,6 +646,7 @@ cudaError_t launch(KFN kfn, size_t bytes, dim3 grid, const CUtensorMap& tq, cons
   cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   kfn<<<grid, kThreads, smem, st>>>(tq, tdo, tk, tv, b);
+  note_launch();
   return cudaGetLastError();
 }
 

@@ -352,6 +352,7 @@ cudaError_t run(const AttnArgs& a, cudaStream_t st) {
   const int nt = (int)ceil_div(a.S, kTile);
   dim3 grid((unsigned)ceil_div(nt, 2), (unsigned)a.nh);
   kfn<<<grid, kFwdThreads, smem, st>>>(tq, tk, tv, a);
+  note_launch();
   return cudaGetLastError();
 }
 

@@ -344,6 +344,7 @@ cudaError_t launch_split_reduce(const float* part, int splits, int64_t M, int64_
   const int64_t total4 = M * N / 4;
   const unsigned blocks = (unsigned)std::max<int64_t>(1, std::min<int64_t>(ceil_div(total4, 256), 152 * 8));
   k_split_reduce<<<blocks, 256, 0, st>>>(part, splits, M, N, out);
+  note_launch();
   return cudaGetLastError();
 }
 
@@ -376,6 +377,7 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, int split_k, float* split_scratc
   cudaError_t e = cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
   if (e != cudaSuccess) return e;
   k_gemm_tc<<<grid, THREADS, SMEM_BYTES, st>>>(ta, tb, p);
+  note_launch();
   e = cudaGetLastError();
   if (e != cudaSuccess || split_k <= 1) return e;
   return launch_split_reduce(split_scratch, split_k, g.M, g.N, g.c, st);

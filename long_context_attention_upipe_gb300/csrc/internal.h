@@ -8,6 +8,10 @@
 
 namespace upipe {
 
+// Every kernel launch of the library calls this once (a process-wide counter, read through
+// upipe_attn_launch_count).
+void note_launch();
+
 // ---------------------------------------------------------------- tile-skip table
 size_t tile_table_bytes(int64_t S);
 cudaError_t launch_tile_table(int64_t S, int causal, const int32_t* seg, void* table, cudaStream_t st);

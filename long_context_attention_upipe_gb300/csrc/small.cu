@@ -36,12 +36,14 @@ unsigned grid_for(int64_t work) { return (unsigned)std::max<int64_t>(1, std::min
 cudaError_t launch_f32_to_bf16(const float* in, bf16* out, int64_t n, float mul, cudaStream_t st) {
   if (n <= 0) return cudaSuccess;
   k_f32_to_bf16<<<grid_for(n / 8 + 1), 256, 0, st>>>(in, out, n, mul);
+  note_launch();
   return cudaGetLastError();
 }
 
 cudaError_t launch_zero(void* p, int64_t bytes, cudaStream_t st) {
   if (bytes <= 0) return cudaSuccess;
   k_zero<<<grid_for(bytes / 16), 256, 0, st>>>(reinterpret_cast<uint4*>(p), bytes / 16);
+  note_launch();
   return cudaGetLastError();
 }
 

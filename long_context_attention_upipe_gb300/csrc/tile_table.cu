@@ -153,14 +153,18 @@ cudaError_t launch_tile_table(int64_t S, int causal, const int32_t* seg, void* t
   int4* q_rows = reinterpret_cast<int4*>(reinterpret_cast<char*>(table) + sizeof(TableHeader));
   int4* kv_rows = q_rows + nt;
   k_table_init<<<1, 32, 0, st>>>(h, (int)nt);
+  note_launch();
   if (seg && S > 1) {
     int64_t blocks = std::min<int64_t>(ceil_div(S, 256), 152 * 8);
     k_check_monotone<<<(unsigned)blocks, 256, 0, st>>>(seg, S, h);
+    note_launch();
   }
   SegView sv{seg, S};
   const unsigned tb = (unsigned)ceil_div(nt, 256);
   k_q_rows<<<tb, 256, 0, st>>>(sv, causal, nt, q_rows, h);
+  note_launch();
   k_kv_rows<<<tb, 256, 0, st>>>(sv, causal, nt, kv_rows);
+  note_launch();
   return cudaGetLastError();
 }
 

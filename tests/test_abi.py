@@ -62,6 +62,7 @@ def test_bad_descriptors_rejected(bad):
 def test_fwd_host_checks_run_before_any_launch():
     d = up.make_desc(512, 256, 4, 2, 64, 2)
     L = up.lib()
+    launches = up.launch_count()
     fake = ctypes.c_void_p(0x10000)       # never dereferenced: the checks fail first
     odd = ctypes.c_void_p(0x10008)
     args = [fake] * 6
@@ -74,3 +75,4 @@ def test_fwd_host_checks_run_before_any_launch():
     t = up.make_desc(512, 256, 4, 2, 64, 2)
     assert L.upipe_attn_build_tile_table(ctypes.byref(t), None, fake, 16, None) == 4
     assert L.upipe_attn_build_tile_table(ctypes.byref(t), odd, fake, 1 << 20, None) == 3
+    assert up.launch_count() == launches  # rejected calls launch nothing

@@ -103,7 +103,10 @@ def test_gemm_nt_matches_fp64(M, N, K):
     A = ui.normal_bf16(M * K, 20).reshape(M, K)
     B = ui.normal_bf16(N * K, 21, 0.05).reshape(N, K)
     C = torch.empty(M, N, dtype=torch.float32, device="cuda")
-    up.gemm_nt(bf16_tensor(A), bf16_tensor(B), C)
+    a, b = bf16_tensor(A), bf16_tensor(B)
+    n0 = up.launch_count()
+    up.gemm_nt(a, b, C)
+    assert up.launch_count() - n0 == 1  # one tensor-core GEMM kernel, no split-K reduce
     torch.cuda.synchronize()
     want = ui.bf16_to_f64(A) @ ui.bf16_to_f64(B).T
     got = C.cpu().double().numpy()
