@@ -204,18 +204,23 @@ cudaError_t project_qkv(const Plan& p, int c, bool with_kv, const bf16* X, const
   return launch_gemm_tc(g, 1, nullptr, st);
 }
 
-// Epilogue schedule of a quantity accumulated over the n_chunks chunks (Y, dX).
-int accum_epi(const Plan& p, int c, bool bf16_direct) {
+// Epilogue schedule of a quantity accumulated over the n_chunks chunks (Y, dX): the first chunk
+// stores, later chunks add (accum_mode 0: into the fp32 workspace sum, reduced in L2 by TMA;
+// accum_mode 1: into the bf16 output in place).  With accum_mode 0 the fp32 sum is rounded to
+// bf16 once, after the last chunk (accum_finish).
+int accum_epi(const Plan& p, int c) {
   if (p.n_chunks == 1) return EPI_STORE_BF16;
   if (p.accum == 1) return c == 0 ? EPI_STORE_BF16 : EPI_ACC_BF16;
-  (void)bf16_direct;
-  if (c == 0) return EPI_STORE_F32;
-  return c == p.n_chunks - 1 ? EPI_ACC_F32_TO_BF16 : EPI_ACC_F32;
+  return c == 0 ? EPI_STORE_F32 : EPI_ACC_F32;
+}
+
+cudaError_t accum_finish(const Plan& p, int c, const float* acc, bf16* out, cudaStream_t st) {
+  if (p.n_chunks == 1 || p.accum == 1 || c != p.n_chunks - 1) return cudaSuccess;
+  return launch_f32_to_bf16(acc, out, p.S * p.d, 1.f, st);
 }
 
 void set_accum_out(GemmOutput& o, const Plan& p, int epi, void* bf16_out, float* acc) {
   o.blk_shift = -1; o.blk_dim = 0; o.ld = p.d;
-  o.aux = acc; o.aux_ld = p.d;
   if (epi == EPI_STORE_F32 || epi == EPI_ACC_F32) o.blk[0] = acc;
   else o.blk[0] = bf16_out;
 }
@@ -254,9 +259,10 @@ upipe_status_t run_fwd(const Plan& p, const bf16* X, const bf16* Wqkv, const bf1
     g.M = p.S; g.N = p.d; g.K = (int64_t)p.hpc * p.Dh;
     g.a = op3d(at<bf16>(ws, p.o), p.Dh, p.S, p.hpc, 1, sh, 1);                        // O_c, K blocked by head
     g.b = op2d(Wo + (int64_t)c * p.hpc * p.Dh, (uint64_t)p.hpc * p.Dh, p.d, (uint64_t)p.Hq * p.Dh, 1);  // Wo_c
-    g.epi = accum_epi(p, c, true);
+    g.epi = accum_epi(p, c);
     set_accum_out(g.c, p, g.epi, Y, p.yacc ? at<float>(ws, p.yacc) : nullptr);
     UPIPE_CUDA(launch_gemm_tc(g, 1, nullptr, st));
+    UPIPE_CUDA(accum_finish(p, c, p.yacc ? at<float>(ws, p.yacc) : nullptr, Y, st));
   }
   return UPIPE_OK;
 }
@@ -332,9 +338,10 @@ upipe_status_t run_bwd(const Plan& p, const bf16* X, const bf16* Wqkv, const bf1
       g.b = op2d(Wqkv, p.d, wrows, p.d, 0);                           // rows of the blocks, N along d
       g.b.blk_shift = sh; g.b.blk_dim = 1;
       for (int i = 0; i < nb; ++i) g.b.row_base[i] = blk_row[i];
-      g.epi = accum_epi(p, c, true);
+      g.epi = accum_epi(p, c);
       set_accum_out(g.c, p, g.epi, dX, p.dxacc ? at<float>(ws, p.dxacc) : nullptr);
       UPIPE_CUDA(launch_gemm_tc(g, 1, nullptr, st));
+      UPIPE_CUDA(accum_finish(p, c, p.dxacc ? at<float>(ws, p.dxacc) : nullptr, dX, st));
     }
     {  // dWqkv rows of these blocks = dQKV_block^T * X   (split-K over S)
       TcGemmArgs g{};

@@ -39,31 +39,44 @@ constexpr uint32_t kBoxBytes = 128 * 128;  // one TMA box: 128 rows x 64 bf16 (1
 
 __device__ __forceinline__ bool in_range(const int4& r, int j) { return j >= r.x && j < r.w; }
 
-// 128 fp32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld128(uint32_t addr, uint32_t (&v)[128]) {
+// Start loading 64 fp32 columns of this thread's TMEM lane (complete after tmem_ld_wait_for).
+__device__ __forceinline__ void tmem_ld64(uint32_t addr, uint32_t (&v)[64]) {
   tc::tmem_ld32(addr + 0, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
   tc::tmem_ld32(addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-  tc::tmem_ld32(addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&v[64]));
-  tc::tmem_ld32(addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&v[96]));
-  tc::tmem_ld_wait();
 }
 
+// Wait for outstanding TMEM loads, then tie the registers of `v` to the wait so the compiler
+// cannot move their uses above it (the load writes them asynchronously).
+__device__ __forceinline__ void tmem_ld_wait_for(uint32_t (&v)[64]) {
+  tc::tmem_ld_wait();
+#pragma unroll
+  for (int i = 0; i < 64; ++i) asm volatile("" : "+r"(v[i]));
+}
+
+// The MMA-issuing thread shares its SM sub-partition with two busy element-wise warps, so its
+// issue path is kept short: operand descriptors are built once per buffer (kdesc / mndesc) and
+// stepped by constant offsets (tc::sdesc_add).
+__device__ __forceinline__ uint64_t kdesc(uint32_t saddr) { return tc::sdesc_sw128(saddr, 16, 1024); }          // K-major tile
+__device__ __forceinline__ uint64_t mndesc(uint32_t saddr) { return tc::sdesc_sw128(saddr, kBoxBytes, 1024); }  // MN-major tile
+
 template <int DH>
-__device__ __forceinline__ void mma_nt(uint32_t d, uint32_t abase, uint32_t bbase) {  // D = A B^T, K-major
+__device__ __forceinline__ void mma_nt(uint32_t d, uint64_t adesc, uint64_t bdesc) {  // D = A B^T, both K-major
   constexpr uint32_t kId = tc::idesc_bf16(128, 128, false, false);
+  adesc = tc::opaque(adesc);
+  bdesc = tc::opaque(bdesc);
 #pragma unroll
   for (int k = 0; k < DH / 16; ++k) {
     const uint32_t off = (k >> 2) * kBoxBytes + (k & 3) * 32;
-    tc::mma_ss(d, tc::sdesc_sw128(abase + off, 16, 1024), tc::sdesc_sw128(bbase + off, 16, 1024), kId, k > 0);
+    tc::mma_ss(d, tc::sdesc_add(adesc, off), tc::sdesc_add(bdesc, off), kId, k > 0);
   }
 }
 
 template <int DH>
-__device__ __forceinline__ void mma_acc(uint32_t d, uint32_t a_tmem, uint32_t bbase, bool acc) {  // D (+)= A[tmem] B
+__device__ __forceinline__ void mma_acc(uint32_t d, uint32_t a_tmem, uint64_t bdesc, bool acc) {  // D (+)= A[tmem] B
   constexpr uint32_t kId = tc::idesc_bf16(128, DH, false, true);  // B [128 rows x Dh] read MN-major
+  bdesc = tc::opaque(bdesc);
 #pragma unroll
-  for (int k = 0; k < 128 / 16; ++k)
-    tc::mma_ts(d, a_tmem + k * 8, tc::sdesc_sw128(bbase + k * 2048, kBoxBytes, 1024), kId, acc || k > 0);
+  for (int k = 0; k < 128 / 16; ++k) tc::mma_ts(d, a_tmem + k * 8, tc::sdesc_add(bdesc, k * 2048), kId, acc || k > 0);
 }
 
 // dS = P (dP - D) for 64 packed P pairs, dP in the region, result written over columns [0, 64):
@@ -170,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dq_tc(const __grid_con
   const uint32_t tmem = *tmem_slot;
 
   if (warp < 4) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;\n" ::: "memory");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 72;\n" ::: "memory");
     if (warp == 0) {
       if (lane == 0) {
         tc::prefetch_tmap(&tq);
@@ -201,8 +214,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dq_tc(const __grid_con
       __syncwarp();
     } else if (warp == 1) {
       if (lane == 0) {
-        const uint32_t sQ = smem_u32(smem + L::Q), sDO = smem_u32(smem + L::DO);
-        const uint32_t sK = smem_u32(smem + L::KR), sV = smem_u32(smem + L::VR);
+        const uint64_t dQ = kdesc(smem_u32(smem + L::Q)), dDO = kdesc(smem_u32(smem + L::DO));
+        const uint64_t dK = kdesc(smem_u32(smem + L::KR)), dKmn = mndesc(smem_u32(smem + L::KR));
+        const uint64_t dV = kdesc(smem_u32(smem + L::VR));
         bool ok = tc::mbar_wait(q_full, 0, abort_flag, a.err);
         const int4 rng[2] = {rng0, rng1};
         int cnt[2] = {0, 0};
@@ -212,12 +226,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dq_tc(const __grid_con
           tc::fence_after_sync();
           for (int t = 0; t < 2 && ok; ++t)
             if (in_range(rng[t], j0)) {
-              mma_nt<DH>(tmem + L::r_col(t), sQ + t * L::TB, sK);
+              mma_nt<DH>(tmem + L::r_col(t), tc::sdesc_add(dQ, t * L::TB), dK);
               tc::mma_commit(&s_full[t]);
             }
         }
         for (int j = j0, n = 0; ok && j < j1; ++j, ++n) {
-          const uint32_t kb = sK + (n & 1) * L::TB;
+          const uint64_t kb = tc::sdesc_add(dKmn, (n & 1) * L::TB);
           ok = tc::mbar_wait(v_full, n & 1, abort_flag, a.err);  // V_j
           if (!ok) break;
           tc::fence_after_sync();
@@ -226,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dq_tc(const __grid_con
               ok = tc::mbar_wait(&s_free[t], cnt[t] & 1, abort_flag, a.err);
               if (!ok) break;
               tc::fence_after_sync();
-              mma_nt<DH>(tmem + L::r_col(t), sDO + t * L::TB, sV);  // dP = dO V^T
+              mma_nt<DH>(tmem + L::r_col(t), tc::sdesc_add(dDO, t * L::TB), dV);  // dP = dO V^T
               tc::mma_commit(&dp_full[t]);
             }
           if (!ok) break;
@@ -246,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dq_tc(const __grid_con
               if (j == rng[t].w - 1) tc::mma_commit(&dq_full[t]);
             }
             if (in_range(rng[t], j + 1)) {
-              mma_nt<DH>(tmem + L::r_col(t), sQ + t * L::TB, sK + ((n + 1) & 1) * L::TB);
+              mma_nt<DH>(tmem + L::r_col(t), tc::sdesc_add(dQ, t * L::TB), tc::sdesc_add(dK, ((n + 1) & 1) * L::TB));
               tc::mma_commit(&s_full[t]);
             }
           }
@@ -283,8 +297,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dq_tc(const __grid_con
         tc::fence_after_sync();
         uint32_t pk[64];  // P as bf16 pairs
         {
-          uint32_t sv[128];
-          tmem_ld128(r_addr, sv);
           int lo = 0, hi = 127;
           if (partial) {
             const int64_t col0 = (int64_t)j * kTile;
@@ -292,17 +304,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dq_tc(const __grid_con
             hi = (int)max((int64_t)-1, min(vis_hi - col0, (int64_t)128));
           }
           const float2 cc = make_float2(c, c), nl = make_float2(-lse2, -lse2);
+          // two halves of 64 columns: the second half's TMEM load overlaps the first half's math,
+          // and at most 128 score registers are live next to P
+          auto half = [&](const uint32_t (&sv)[64], int hf) {
 #pragma unroll
-          for (int i = 0; i < 64; ++i) {
-            const float2 arg = __ffma2_rn(make_float2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])), cc, nl);
-            float p0 = fast_exp2(arg.x);
-            float p1 = fast_exp2(arg.y);
-            if (partial) {
-              if (2 * i < lo || 2 * i > hi) p0 = 0.f;
-              if (2 * i + 1 < lo || 2 * i + 1 > hi) p1 = 0.f;
+            for (int i = 0; i < 32; ++i) {
+              const int k = hf * 64 + 2 * i;
+              const float2 arg = __ffma2_rn(make_float2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])), cc, nl);
+              float p0 = fast_exp2(arg.x);
+              float p1 = fast_exp2(arg.y);
+              if (partial) {
+                if (k < lo || k > hi) p0 = 0.f;
+                if (k + 1 < lo || k + 1 > hi) p1 = 0.f;
+              }
+              pk[hf * 32 + i] = tc::pack_bf16x2(p0, p1);
             }
-            pk[i] = tc::pack_bf16x2(p0, p1);
-          }
+          };
+          uint32_t sa[64], sb[64];
+          tmem_ld64(r_addr, sa);
+          tmem_ld_wait_for(sa);
+          tmem_ld64(r_addr + 64, sb);
+          half(sa, 0);
+          tmem_ld_wait_for(sb);
+          half(sb, 1);
         }
         tc::fence_before_sync();
         tc::mbar_arrive(&s_free[t]);
@@ -459,27 +483,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
       __syncwarp();
     } else if (warp == 1) {
       if (lane == 0) {
-        const uint32_t sK = smem_u32(smem + L::K), sV = smem_u32(smem + L::V);
-        const uint32_t sQ = smem_u32(smem + L::QR), sO = smem_u32(smem + L::OR);
+        const uint64_t dK = kdesc(smem_u32(smem + L::K)), dV = kdesc(smem_u32(smem + L::V));
+        const uint64_t dQ = kdesc(smem_u32(smem + L::QR)), dQmn = mndesc(smem_u32(smem + L::QR));
+        const uint64_t dO = kdesc(smem_u32(smem + L::OR)), dOmn = mndesc(smem_u32(smem + L::OR));
         bool ok = tc::mbar_wait(kv_full, 0, abort_flag, a.err);
         auto issue_st = [&](int n) {  // S^T of item n into region n % 2
           if (ok) ok = tc::mbar_wait(&q_full[n % NQ], (n / NQ) & 1, abort_flag, a.err);
           if (!ok) return;
           tc::fence_after_sync();
-          mma_nt<DH>(tmem + L::r_col(n & 1), sK, sQ + (n % NQ) * L::TB);
+          mma_nt<DH>(tmem + L::r_col(n & 1), dK, tc::sdesc_add(dQ, (n % NQ) * L::TB));
           tc::mma_commit(&s_full[n & 1]);
         };
         // software pipeline: dV/dP^T of item n+1 are issued before dK of item n, so the tensor
         // core works while the element-wise group of item n computes dS^T
         auto issue_dv_dp = [&](int n) {
           const int rr = n & 1;
-          const uint32_t ob = sO + (n % NO) * L::TB;
+          const uint32_t oo = (n % NO) * L::TB;
           ok = tc::mbar_wait(&p_full[rr], (n >> 1) & 1, abort_flag, a.err);
           if (ok) ok = tc::mbar_wait(&o_full[n % NO], (n / NO) & 1, abort_flag, a.err);
           if (!ok) return;
           tc::fence_after_sync();
-          mma_acc<DH>(tmem + L::DV_COL, tmem + L::r_col(rr), ob, n > 0);  // dV += P^T dO
-          mma_nt<DH>(tmem + L::r_col(rr), sV, ob);                         // dP^T = V dO^T
+          mma_acc<DH>(tmem + L::DV_COL, tmem + L::r_col(rr), tc::sdesc_add(dOmn, oo), n > 0);  // dV += P^T dO
+          mma_nt<DH>(tmem + L::r_col(rr), dV, tc::sdesc_add(dO, oo));                           // dP^T = V dO^T
           tc::mma_commit(&dp_full[rr]);
           tc::mma_commit(&o_empty[n % NO]);
         };
@@ -488,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
           ok = tc::mbar_wait(&ds_full[rr], (n >> 1) & 1, abort_flag, a.err);
           if (!ok) return;
           tc::fence_after_sync();
-          mma_acc<DH>(tmem + L::DK_COL, tmem + L::r_col(rr), sQ + (n % NQ) * L::TB, n > 0);  // dK += dS^T Q
+          mma_acc<DH>(tmem + L::DK_COL, tmem + L::r_col(rr), tc::sdesc_add(dQmn, (n % NQ) * L::TB), n > 0);  // dK += dS^T Q
           tc::mma_commit(&q_empty[n % NQ]);
           if (n == n_items - 1) tc::mma_commit(acc_full);
           if (n + 2 < n_items) issue_st(n + 2);
@@ -525,8 +550,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
     const float c = a.scale * 1.4426950408889634f;
     const bool ragged = (S % kTile) != 0;
     bool ok = true;
-    for (int n = grp; n < n_items; n += 2) {
+    // -lse*log2e and -D of query r of item n (one value pair per thread), loaded one item ahead
+    auto load_vec = [&](int n) {
+      const int64_t qoff = (int64_t)(tr.x + n % nq) * kTile + r;
       const int hh = h_first + n / nq;
+      return make_float2(-a.D[((int64_t)a.nh + hh) * sp + qoff], -a.D[(int64_t)hh * sp + qoff]);
+    };
+    float2 vec_next = grp < n_items ? load_vec(grp) : make_float2(0.f, 0.f);
+    for (int n = grp; n < n_items; n += 2) {
       const int qi = tr.x + n % nq;
       const bool partial = qi < tr.y || qi >= tr.z || (ragged && (qi == nt - 1 || jt == nt - 1));
       const int cyc = (n >> 1) & 1;
@@ -536,39 +567,45 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
         lo = (int)max((int64_t)-1, min(vis_lo - col0, (int64_t)128));
         hi = (int)max((int64_t)-1, min(vis_hi - col0, (int64_t)128));
       }
-      // stage -lse*log2e and -D of the item's 128 queries in shared memory (one per thread)
+      // stage the item's 128 (-lse2, -D) pairs in shared memory, then start the next item's loads
       tc::named_bar_sync(1 + grp, 128);  // the previous item's readers are done
-      {
-        const int64_t qoff = (int64_t)qi * kTile + r;
-        nvec[r] = -a.D[((int64_t)a.nh + hh) * sp + qoff];
-        nvec[128 + r] = -a.D[(int64_t)hh * sp + qoff];
-      }
+      nvec[r] = vec_next.x;
+      nvec[128 + r] = vec_next.y;
       tc::named_bar_sync(1 + grp, 128);
+      if (n + 2 < n_items) vec_next = load_vec(n + 2);
       ok = tc::mbar_wait(&s_full[grp], cyc, abort_flag, a.err);
       if (!ok) break;
       tc::fence_after_sync();
       uint32_t pk[64];  // P^T as bf16 pairs
       {
-        uint32_t sv[128];
-        tmem_ld128(r_addr, sv);
         const float2 cc = make_float2(c, c);
+        // two halves of 64 columns, the second loading while the first is computed (as in dQ)
+        auto half = [&](const uint32_t (&sv)[64], int hf) {
 #pragma unroll
-        for (int i = 0; i < 64; i += 2) {
-          const float4 l4 = *reinterpret_cast<const float4*>(nvec + 2 * i);
+          for (int i = 0; i < 32; i += 2) {
+            const float4 l4 = *reinterpret_cast<const float4*>(nvec + hf * 64 + 2 * i);
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int k = 2 * (i + u);
-            const float2 arg = __ffma2_rn(make_float2(__uint_as_float(sv[k]), __uint_as_float(sv[k + 1])), cc,
-                                          u ? make_float2(l4.z, l4.w) : make_float2(l4.x, l4.y));
-            float p0 = fast_exp2(arg.x);
-            float p1 = fast_exp2(arg.y);
-            if (partial) {
-              if (k < lo || k > hi) p0 = 0.f;
-              if (k + 1 < lo || k + 1 > hi) p1 = 0.f;
+            for (int u = 0; u < 2; ++u) {
+              const int kk = 2 * (i + u), k = hf * 64 + kk;
+              const float2 arg = __ffma2_rn(make_float2(__uint_as_float(sv[kk]), __uint_as_float(sv[kk + 1])), cc,
+                                            u ? make_float2(l4.z, l4.w) : make_float2(l4.x, l4.y));
+              float p0 = fast_exp2(arg.x);
+              float p1 = fast_exp2(arg.y);
+              if (partial) {
+                if (k < lo || k > hi) p0 = 0.f;
+                if (k + 1 < lo || k + 1 > hi) p1 = 0.f;
+              }
+              pk[hf * 32 + i + u] = tc::pack_bf16x2(p0, p1);
             }
-            pk[i + u] = tc::pack_bf16x2(p0, p1);
           }
-        }
+        };
+        uint32_t sa[64], sb[64];
+        tmem_ld64(r_addr, sa);
+        tmem_ld_wait_for(sa);
+        tmem_ld64(r_addr + 64, sb);
+        half(sa, 0);
+        tmem_ld_wait_for(sb);
+        half(sb, 1);
       }
       tc::tmem_st32(r_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
       tc::tmem_st32(r_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));

@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp < 4) {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 56;\n" ::: "memory");
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 72;\n" ::: "memory");
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -133,61 +133,69 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
+    // Lean issue path: descriptors are built once and stepped by constant offsets, ring slots and
+    // phases are tracked incrementally, so the thread keeps the tensor pipe fed although it
+    // shares its SM sub-partition with two busy softmax warps.
     if (lane == 0) {
       constexpr uint32_t kIdS = tc::idesc_bf16(128, 128, false, false);
       constexpr uint32_t kIdO = tc::idesc_bf16(128, DH, false, true);
       const uint32_t sQ = smem_u32(smem + L::Q), sR = smem_u32(smem + L::RING);
+      const uint64_t dQ = tc::sdesc_sw128(sQ, 16, 1024);           // Q_t, K-major
+      const uint64_t dK = tc::sdesc_sw128(sR, 16, 1024);           // ring slot 0 read as K (K-major)
+      const uint64_t dV = tc::sdesc_sw128(sR, kBoxBytes, 1024);    // ring slot 0 read as V (MN-major)
       bool ok = tc::mbar_wait(q_full, 0, abort_flag, a.err);
-      auto wait_item = [&](int it) {
-        if (ok) ok = tc::mbar_wait(&slot_full[it % NS], (it / NS) & 1, abort_flag, a.err);
+      struct Pos { int slot; uint32_t phase; };
+      auto next = [](Pos p) { return p.slot + 1 == NS ? Pos{0, p.phase ^ 1u} : Pos{p.slot + 1, p.phase}; };
+      auto wait_item = [&](Pos p) {
+        if (ok) ok = tc::mbar_wait(&slot_full[p.slot], p.phase, abort_flag, a.err);
         tc::fence_after_sync();
       };
-      auto issue_s = [&](int t, int n) {
-        const uint32_t kb = sR + ((2 * n) % NS) * L::TB;
-        const uint32_t qb = sQ + t * L::TB;
+      auto issue_s = [&](int t, int slot) {
+        const uint64_t qd = tc::opaque(tc::sdesc_add(dQ, t * L::TB)), kd = tc::opaque(tc::sdesc_add(dK, slot * L::TB));
 #pragma unroll
         for (int k = 0; k < DH / 16; ++k) {
           const uint32_t off = (k >> 2) * kBoxBytes + (k & 3) * 32;
-          tc::mma_ss(tmem + L::s_col(t), tc::sdesc_sw128(qb + off, 16, 1024), tc::sdesc_sw128(kb + off, 16, 1024),
-                     kIdS, k > 0);
+          tc::mma_ss(tmem + L::s_col(t), tc::sdesc_add(qd, off), tc::sdesc_add(kd, off), kIdS, k > 0);
         }
         tc::mma_commit(&s_full[t]);
       };
-      auto issue_pv = [&](int t, int n, bool first) {
-        const uint32_t vb = sR + ((2 * n + 1) % NS) * L::TB;
+      auto issue_pv = [&](int t, int slot, bool first) {
+        const uint64_t vd = tc::opaque(tc::sdesc_add(dV, slot * L::TB));
 #pragma unroll
         for (int k = 0; k < 128 / 16; ++k)
-          tc::mma_ts(tmem + L::o_col(t), tmem + L::s_col(t) + k * 8, tc::sdesc_sw128(vb + k * 2048, kBoxBytes, 1024),
-                     kIdO, (!first) || k > 0);
+          tc::mma_ts(tmem + L::o_col(t), tmem + L::s_col(t) + k * 8, tc::sdesc_add(vd, k * 2048), kIdO, (!first) || k > 0);
       };
       const int4 rng[2] = {rng0, rng1};
       int cnt_p[2] = {0, 0};
       bool first_pv[2] = {true, true};
+      Pos kpos{0, 0u};  // ring position of K_j (item 2n); V_j follows it, then K_j+1
       if (ok) {
-        wait_item(0);
+        wait_item(kpos);
         for (int t = 0; t < 2; ++t)
-          if (ok && in_range(rng[t], j0)) issue_s(t, 0);
-        if (ok) tc::mma_commit(&slot_empty[0]);
+          if (ok && in_range(rng[t], j0)) issue_s(t, kpos.slot);
+        if (ok) tc::mma_commit(&slot_empty[kpos.slot]);
       }
-      for (int j = j0, n = 0; ok && j < j1; ++j, ++n) {
-        wait_item(2 * n + 1);                   // V_j
-        if (j + 1 < j1) wait_item(2 * n + 2);   // K_j+1
+      for (int j = j0; ok && j < j1; ++j) {
+        const Pos vpos = next(kpos), knext = next(vpos);
+        wait_item(vpos);                       // V_j
+        if (j + 1 < j1) wait_item(knext);      // K_j+1
         for (int t = 0; t < 2 && ok; ++t) {
           if (in_range(rng[t], j)) {
             ok = tc::mbar_wait(&p_full[t], cnt_p[t] & 1, abort_flag, a.err);
             if (!ok) break;
             ++cnt_p[t];
             tc::fence_after_sync();
-            issue_pv(t, n, first_pv[t]);
+            issue_pv(t, vpos.slot, first_pv[t]);
             first_pv[t] = false;
             if (j == rng[t].w - 1) tc::mma_commit(&o_full[t]);
           }
-          if (in_range(rng[t], j + 1)) issue_s(t, n + 1);
+          if (in_range(rng[t], j + 1)) issue_s(t, knext.slot);
         }
         if (ok) {
-          tc::mma_commit(&slot_empty[(2 * n + 1) % NS]);                  // V_j free
-          if (j + 1 < j1) tc::mma_commit(&slot_empty[(2 * n + 2) % NS]);  // K_j+1 free
+          tc::mma_commit(&slot_empty[vpos.slot]);                  // V_j free
+          if (j + 1 < j1) tc::mma_commit(&slot_empty[knext.slot]);  // K_j+1 free
         }
+        kpos = knext;
       }
     }
     __syncwarp();

@@ -12,7 +12,13 @@
 //   warp 1     MMA issuer (one thread), TMEM owner: 4 tcgen05.mma (M128 N256 K16) per stage into
 //              one of two TMEM accumulators, so the epilogue of a tile overlaps the next tile
 //   warps 2-5  epilogue: one output row per thread (TMEM lane), 32 columns at a time
-// Split-K (weight gradients, K = S) writes fp32 partials that k_split_reduce sums in order.
+// Plain row-major fp32 outputs (and split-K partials) leave through shared memory: each epilogue
+// warp stages a 32 x 32 fp32 box (128-byte swizzle, double-buffered) and one lane hands it to a
+// TMA bulk store, or to a TMA bulk reduce-add for C += A B^T, so the read-modify-write of an
+// accumulator runs in L2 without the SM waiting on its loads.  Other outputs are stored per
+// thread.  Split-K (weight gradients, K = S) writes fp32 partials that k_split_reduce sums in order.
+#include <cstring>
+
 #include "internal.h"
 #include "tc_common.cuh"
 
@@ -25,7 +31,9 @@ constexpr uint32_t BOX = 64 * 64 * 2;          // one 64 x 64 bf16 box, 8 KB
 constexpr uint32_t TILE_A = 2 * BOX;           // 128 x 64 A tile
 constexpr uint32_t TILE_B = 4 * BOX;           // 256 x 64 B tile
 constexpr uint32_t STAGE = TILE_A + TILE_B;
-constexpr uint32_t BAR_OFF = STAGES * STAGE;
+constexpr uint32_t STG_OFF = STAGES * STAGE;         // epilogue staging: 4 warps x 2 boxes of 32 x 32 fp32
+constexpr uint32_t STG_BOX = 32 * 32 * 4;
+constexpr uint32_t BAR_OFF = STG_OFF + 8 * STG_BOX;
 constexpr uint32_t SMEM_BYTES = BAR_OFF + 256 + 1024;
 
 struct TcOpDev {
@@ -42,7 +50,10 @@ struct TcGemmParams {
   int64_t k_per_split;  // multiple of BK
   int tiles_m, tiles_n;
   float* split_out;
+  int tma_out;  // 0: per-thread stores; 1: TMA store (2-D map); 2: TMA reduce-add (2-D); 3: TMA store of split partials (3-D)
 };
+
+enum : int { TMA_OUT_NONE = 0, TMA_OUT_STORE = 1, TMA_OUT_ADD = 2, TMA_OUT_SPLIT = 3 };
 
 // TMA coordinates of the 64 x 64 box that starts at logical (mn, k).
 __device__ __forceinline__ void box_coords(const TcOpDev& o, int64_t mn, int64_t k, int& c0, int& c1, int& c2) {
@@ -87,7 +98,8 @@ __device__ __forceinline__ T* out_ptr(const GemmOutput& o, int64_t m, int64_t n)
 }
 
 __global__ void __launch_bounds__(THREADS, 1) k_gemm_tc(const __grid_constant__ CUtensorMap ta,
-                                                        const __grid_constant__ CUtensorMap tb, TcGemmParams p) {
+                                                        const __grid_constant__ CUtensorMap tb,
+                                                        const __grid_constant__ CUtensorMap tout, TcGemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
@@ -163,6 +175,10 @@ __global__ void __launch_bounds__(THREADS, 1) k_gemm_tc(const __grid_constant__ 
   } else if (warp == 1) {
     if (lane == 0) {
       const uint32_t idesc = tc::idesc_bf16(BM, BN, !p.a.k_major, !p.b.k_major);
+      // descriptors of stage 0, stepped by constant offsets (stage, K step) in the loop
+      const uint32_t s0 = smem_u32(smem);
+      const uint64_t a0 = tile_desc(s0, p.a.k_major, 0), b0 = tile_desc(s0 + TILE_A, p.b.k_major, 0);
+      const uint32_t a_step = p.a.k_major ? 32 : 2048, b_step = p.b.k_major ? 32 : 2048;  // bytes per K16 step
       int it = 0, tcount = 0;
       bool ok = true;
       for (int64_t t = blockIdx.x; ok && t < n_tiles; t += gridDim.x, ++tcount) {
@@ -177,10 +193,10 @@ __global__ void __launch_bounds__(THREADS, 1) k_gemm_tc(const __grid_constant__ 
           const int s = it % STAGES;
           if (!(ok = tc::mbar_wait(&full[s], (it / STAGES) & 1, abort_flag, nullptr))) break;
           tc::fence_after_sync();
-          const uint32_t sa = smem_u32(smem + s * STAGE), sb = sa + TILE_A;
+          const uint64_t ad = tc::opaque(tc::sdesc_add(a0, s * STAGE)), bd = tc::opaque(tc::sdesc_add(b0, s * STAGE));
 #pragma unroll
           for (int k16 = 0; k16 < BK / 16; ++k16)
-            tc::mma_ss(d, tile_desc(sa, p.a.k_major, k16), tile_desc(sb, p.b.k_major, k16), idesc, kt > 0 || k16 > 0);
+            tc::mma_ss(d, tc::sdesc_add(ad, k16 * a_step), tc::sdesc_add(bd, k16 * b_step), idesc, kt > 0 || k16 > 0);
           tc::mma_commit(&empty[s]);
         }
         tc::mma_commit(&acc_full[buf]);
@@ -191,7 +207,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_gemm_tc(const __grid_constant__ 
     // epilogue warps 2..5: TMEM lanes 32 * (warp % 4) + lane
     const int row_in_tile = 32 * (warp & 3) + lane;
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-    int tcount = 0;
+    int tcount = 0, nstage = 0;
     bool ok = true;
     for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x, ++tcount) {
       int tm, tn, ks;
@@ -212,6 +228,32 @@ __global__ void __launch_bounds__(THREADS, 1) k_gemm_tc(const __grid_constant__ 
           for (int i = 0; i < 32; ++i) v[i] = 0u;
         }
         const int64_t n0 = (int64_t)tn * BN + ch * 32;
+        if (p.tma_out != TMA_OUT_NONE) {
+          // stage this warp's 32 rows x 32 columns, row `lane` with 128-byte swizzle (16-byte
+          // chunk j of row r at chunk j ^ (r % 8)), then one lane issues the bulk copy.  Only
+          // boxes that are issued are staged, so the two buffers alternate with the committed
+          // groups and "at most one group still reading" frees the buffer about to be written.
+          const int64_t y = (int64_t)tm * BM + 32 * (warp & 3);
+          if (!__all_sync(0xffffffffu, ok) || n0 >= p.N || y >= p.M) continue;
+          uint8_t* box = smem + STG_OFF + ((warp & 3) * 2 + (nstage & 1)) * STG_BOX;
+          ++nstage;
+          if (lane == 0) tc::bulk_wait_read<1>();  // the copy that last read this buffer is done
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<float4*>(box + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]), __uint_as_float(v[4 * j + 2]),
+                            __uint_as_float(v[4 * j + 3]));
+          tc::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            if (p.tma_out == TMA_OUT_STORE) tc::tma_store_2d(&tout, box, (int)n0, (int)y);
+            else if (p.tma_out == TMA_OUT_ADD) tc::tma_reduce_add_2d(&tout, box, (int)n0, (int)y);
+            else tc::tma_store_3d(&tout, box, (int)n0, (int)y, ks);
+            tc::bulk_commit();
+          }
+          continue;
+        }
         if (!ok || !m_ok || n0 >= p.N) continue;
         const int ncols = (int)min((int64_t)32, p.N - n0);  // multiple of 8
         if (p.split_out) {
@@ -251,21 +293,6 @@ __global__ void __launch_bounds__(THREADS, 1) k_gemm_tc(const __grid_constant__ 
             }
             break;
           }
-          case EPI_ACC_F32_TO_BF16: {
-            const float* aux = p.c.aux + m * p.c.aux_ld + n0;
-            bf16* dst = out_ptr<bf16>(p.c, m, n0);
-            _Pragma("unroll") for (int i = 0; i < 32; i += 8) if (i < ncols) {
-              const float4 a0 = *reinterpret_cast<const float4*>(aux + i);
-              const float4 a1 = *reinterpret_cast<const float4*>(aux + i + 4);
-              uint4 q;
-              q.x = tc::pack_bf16x2(a0.x + __uint_as_float(v[i]), a0.y + __uint_as_float(v[i + 1]));
-              q.y = tc::pack_bf16x2(a0.z + __uint_as_float(v[i + 2]), a0.w + __uint_as_float(v[i + 3]));
-              q.z = tc::pack_bf16x2(a1.x + __uint_as_float(v[i + 4]), a1.y + __uint_as_float(v[i + 5]));
-              q.w = tc::pack_bf16x2(a1.z + __uint_as_float(v[i + 6]), a1.w + __uint_as_float(v[i + 7]));
-              *reinterpret_cast<uint4*>(dst + i) = q;
-            }
-            break;
-          }
           case EPI_ACC_BF16: {
             bf16* dst = out_ptr<bf16>(p.c, m, n0);
             _Pragma("unroll") for (int i = 0; i < 32; i += 8) if (i < ncols) {
@@ -285,6 +312,8 @@ __global__ void __launch_bounds__(THREADS, 1) k_gemm_tc(const __grid_constant__ 
       tc::fence_before_sync();
       tc::mbar_arrive(&acc_empty[buf]);
     }
+    if (lane == 0) tc::bulk_wait_all();  // bulk stores complete before the CTA exits
+    __syncwarp();
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -314,6 +343,8 @@ bool make_map(CUtensorMap* map, const TcOperand& o) {
   if (o.rank == 3) return make_tmap_3d_bf16(map, o.base, o.inner, o.outer, o.planes, 64, 64);
   return make_tmap_2d_bf16(map, o.base, o.inner, o.outer, o.row_stride, 64, 64);
 }
+
+bool aligned16(const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15) == 0; }
 
 TcOpDev dev_op(const TcOperand& o) {
   TcOpDev d{};
@@ -366,6 +397,22 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, int split_k, float* split_scratc
   p.tiles_m = (int)ceil_div(g.M, BM);
   p.tiles_n = (int)ceil_div(g.N, BN);
   p.split_out = split_k > 1 ? split_scratch : nullptr;
+  // fp32 outputs through TMA where the layout allows it (16-byte aligned base and rows)
+  CUtensorMap tout;
+  std::memset(&tout, 0, sizeof(tout));
+  p.tma_out = TMA_OUT_NONE;
+  if (split_k > 1) {
+    const uint64_t dims[3] = {(uint64_t)g.N, (uint64_t)g.M, (uint64_t)split_k};
+    const uint64_t strides[2] = {(uint64_t)g.N * 4, (uint64_t)g.M * g.N * 4};
+    if (g.N % 4 == 0 && aligned16(split_scratch) && make_tmap_f32_out(&tout, split_scratch, 3, dims, strides))
+      p.tma_out = TMA_OUT_SPLIT;
+  } else if ((g.epi == EPI_STORE_F32 || g.epi == EPI_ACC_F32) && g.c.blk_shift < 0) {
+    const uint64_t dims[2] = {(uint64_t)g.N, (uint64_t)g.M};
+    const uint64_t strides[1] = {(uint64_t)g.c.ld * 4};
+    if (g.N % 4 == 0 && g.c.ld % 4 == 0 && aligned16(g.c.blk[0]) &&
+        make_tmap_f32_out(&tout, g.c.blk[0], 2, dims, strides))
+      p.tma_out = g.epi == EPI_ACC_F32 ? TMA_OUT_ADD : TMA_OUT_STORE;
+  }
   static int sms = 0;
   if (!sms) {
     int dev = 0;
@@ -376,7 +423,7 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, int split_k, float* split_scratc
   const int grid = (int)std::min<int64_t>(n_tiles, sms);
   cudaError_t e = cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  k_gemm_tc<<<grid, THREADS, SMEM_BYTES, st>>>(ta, tb, p);
+  k_gemm_tc<<<grid, THREADS, SMEM_BYTES, st>>>(ta, tb, tout, p);
   note_launch();
   e = cudaGetLastError();
   if (e != cudaSuccess || split_k <= 1) return e;

@@ -31,8 +31,7 @@ enum GemmEpilogue : int {
   EPI_STORE_BF16 = 0,      // out(bf16) = acc
   EPI_STORE_F32 = 1,       // out(f32) = acc
   EPI_ACC_F32 = 2,         // out(f32) += acc
-  EPI_ACC_F32_TO_BF16 = 3, // out(bf16) = aux(f32) + acc
-  EPI_ACC_BF16 = 4,        // out(bf16) = out(bf16) + acc (fp32 math)
+  EPI_ACC_BF16 = 3,        // out(bf16) = out(bf16) + acc (fp32 math)
 };
 
 struct GemmOutput {
@@ -40,8 +39,6 @@ struct GemmOutput {
   int64_t ld;
   int blk_shift;          // -1: unblocked
   int blk_dim;
-  const float* aux;       // EPI_ACC_F32_TO_BF16: plain row-major f32 [M][N] with ld aux_ld
-  int64_t aux_ld;
 };
 
 size_t gemm_split_scratch_bytes(int64_t M, int64_t N, int split_k);

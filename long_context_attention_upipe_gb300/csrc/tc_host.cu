@@ -48,4 +48,16 @@ bool make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint6
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_tmap_f32_out(CUtensorMap* map, void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes) {
+  auto fn = encode_fn();
+  if (!fn || rank < 2 || rank > 3) return false;
+  cuuint64_t d[3] = {dims[0], dims[1], rank == 3 ? dims[2] : 1};
+  cuuint64_t st[2] = {strides_bytes[0], rank == 3 ? strides_bytes[1] : 0};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, rank, base, d, st, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace upipe
