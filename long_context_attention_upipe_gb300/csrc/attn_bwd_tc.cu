@@ -306,18 +306,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dq_tc(const __grid_con
           const float2 cc = make_float2(c, c), nl = make_float2(-lse2, -lse2);
           // two halves of 64 columns: the second half's TMEM load overlaps the first half's math,
           // and at most 128 score registers are live next to P
-          auto half = [&](const uint32_t (&sv)[64], int hf) {
+          // masked scores become -inf (exp2 -> 0) in a separate pass that only partial tiles run
+          auto half = [&](uint32_t (&sv)[64], int hf) {
+            if (partial) {
+#pragma unroll
+              for (int i = 0; i < 64; ++i)
+                if (hf * 64 + i < lo || hf * 64 + i > hi) sv[i] = 0xff800000u;
+            }
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-              const int k = hf * 64 + 2 * i;
               const float2 arg = __ffma2_rn(make_float2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])), cc, nl);
-              float p0 = fast_exp2(arg.x);
-              float p1 = fast_exp2(arg.y);
-              if (partial) {
-                if (k < lo || k > hi) p0 = 0.f;
-                if (k + 1 < lo || k + 1 > hi) p1 = 0.f;
-              }
-              pk[hf * 32 + i] = tc::pack_bf16x2(p0, p1);
+              pk[hf * 32 + i] = tc::pack_bf16x2(fast_exp2(arg.x), fast_exp2(arg.y));
             }
           };
           uint32_t sa[64], sb[64];
@@ -580,22 +579,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
       {
         const float2 cc = make_float2(c, c);
         // two halves of 64 columns, the second loading while the first is computed (as in dQ)
-        auto half = [&](const uint32_t (&sv)[64], int hf) {
+        auto half = [&](uint32_t (&sv)[64], int hf) {
+          if (partial) {  // masked scores -> -inf (exp2 -> 0), only on partial tiles
+#pragma unroll
+            for (int i = 0; i < 64; ++i)
+              if (hf * 64 + i < lo || hf * 64 + i > hi) sv[i] = 0xff800000u;
+          }
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {
             const float4 l4 = *reinterpret_cast<const float4*>(nvec + hf * 64 + 2 * i);
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
-              const int kk = 2 * (i + u), k = hf * 64 + kk;
+              const int kk = 2 * (i + u);
               const float2 arg = __ffma2_rn(make_float2(__uint_as_float(sv[kk]), __uint_as_float(sv[kk + 1])), cc,
                                             u ? make_float2(l4.z, l4.w) : make_float2(l4.x, l4.y));
-              float p0 = fast_exp2(arg.x);
-              float p1 = fast_exp2(arg.y);
-              if (partial) {
-                if (k < lo || k > hi) p0 = 0.f;
-                if (k + 1 < lo || k + 1 > hi) p1 = 0.f;
-              }
-              pk[hf * 32 + i + u] = tc::pack_bf16x2(p0, p1);
+              pk[hf * 32 + i + u] = tc::pack_bf16x2(fast_exp2(arg.x), fast_exp2(arg.y));
             }
           }
         };

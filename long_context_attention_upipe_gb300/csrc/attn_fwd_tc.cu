@@ -189,12 +189,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             first_pv[t] = false;
             if (j == rng[t].w - 1) tc::mma_commit(&o_full[t]);
           }
+          if (t == 1 && ok) tc::mma_commit(&slot_empty[vpos.slot]);  // V_j free once both P V are issued
           if (in_range(rng[t], j + 1)) issue_s(t, knext.slot);
         }
-        if (ok) {
-          tc::mma_commit(&slot_empty[vpos.slot]);                  // V_j free
-          if (j + 1 < j1) tc::mma_commit(&slot_empty[knext.slot]);  // K_j+1 free
-        }
+        if (ok && j + 1 < j1) tc::mma_commit(&slot_empty[knext.slot]);  // K_j+1 free
         kpos = knext;
       }
     }
