@@ -7,8 +7,12 @@
 // is the head), column slices of Wo (a 2-D map with the row stride of Wo) and the row blocks of
 // Wqkv that belong to a chunk (a 2-D map plus the first row of each block).
 //
-// Persistent kernel, one CTA per SM, 6 warps:
-//   warp 0     TMA producer over a 4-stage ring of (A 128x64, B 256x64) tiles
+// Persistent kernel, one CTA per SM, launched as clusters of two CTAs that take the two M tiles
+// (m, m+1) of the same N tile: each CTA loads its own A tile and one half of the shared B tile,
+// multicast into both CTAs' shared memory, so every B byte crosses L2 once per pair (a third
+// less L2 traffic per MMA than independent CTAs).  6 warps:
+//   warp 0     TMA producer over a 4-stage ring of (A 128x64, B 256x64) tiles; a stage is
+//              refilled once the MMAs of both CTAs have released it (commits multicast to both)
 //   warp 1     MMA issuer (one thread), TMEM owner: 4 tcgen05.mma (M128 N256 K16) per stage into
 //              one of two TMEM accumulators, so the epilogue of a tile overlaps the next tile
 //   warps 2-5  epilogue: one output row per thread (TMEM lane), 32 columns at a time
@@ -79,6 +83,15 @@ __device__ __forceinline__ void load_box(uint8_t* dst, const CUtensorMap* map, c
   else tc::tma_load_2d(dst, map, bar, c0, c1);
 }
 
+// The same box into both CTAs of the cluster pair.
+__device__ __forceinline__ void load_box_pair(uint8_t* dst, const CUtensorMap* map, const TcOpDev& o, uint64_t* bar,
+                                              int64_t mn, int64_t k) {
+  int c0, c1, c2;
+  box_coords(o, mn, k, c0, c1, c2);
+  if (o.rank == 3) tc::tma_load_3d_mc(dst, map, bar, c0, c1, c2, 0x3);
+  else tc::tma_load_2d_mc(dst, map, bar, c0, c1, 0x3);
+}
+
 // smem descriptor of one operand tile at MMA K-step k16 (16 elements)
 __device__ __forceinline__ uint64_t tile_desc(uint32_t base, int k_major, int k16) {
   return k_major ? tc::sdesc_sw128(base + k16 * 32, 16, 1024)        // 128 rows x 128 B, 8-row groups
@@ -111,14 +124,18 @@ __global__ void __launch_bounds__(THREADS, 1) k_gemm_tc(const __grid_constant__ 
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * STAGES + 5);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t tiles_mn = (int64_t)p.tiles_m * p.tiles_n;
-  const int64_t n_tiles = tiles_mn * p.split_k;
-  const int nk_full = (int)ceil_div(p.k_per_split, BK);
+  // work unit = a pair of M tiles (2 pm, 2 pm + 1) of one N tile and K split; CTA `crank` of the
+  // cluster takes M tile 2 pm + crank (a tile past M is computed on zero-filled rows and dropped)
+  const int crank = (int)tc::cluster_ctarank();
+  const int cid = blockIdx.x >> 1, n_clusters = gridDim.x >> 1;
+  const int tiles_mp = (p.tiles_m + 1) >> 1;
+  const int64_t tiles_pn = (int64_t)tiles_mp * p.tiles_n;
+  const int64_t n_tiles = tiles_pn * p.split_k;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
       tc::mbar_init(&full[i], 1);
-      tc::mbar_init(&empty[i], 1);
+      tc::mbar_init(&empty[i], 2);  // the MMA commits of both CTAs
     }
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&acc_full[i], 1);
@@ -133,14 +150,15 @@ __global__ void __launch_bounds__(THREADS, 1) k_gemm_tc(const __grid_constant__ 
   }
   tc::fence_before_sync();
   __syncthreads();
+  tc::cluster_sync();  // the peer's barriers are initialised before any multicast reaches them
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  // tile t -> (m tile, n tile, split); n fastest so that CTAs running together share A rows in L2
+  // unit t -> (m tile, n tile, split); n fastest so that clusters running together share A rows in L2
   auto decode = [&](int64_t t, int& tm, int& tn, int& ks) {
-    ks = (int)(t / tiles_mn);
-    const int64_t r = t % tiles_mn;
-    tm = (int)(r / p.tiles_n);
+    ks = (int)(t / tiles_pn);
+    const int64_t r = t % tiles_pn;
+    tm = 2 * (int)(r / p.tiles_n) + crank;
     tn = (int)(r % p.tiles_n);
   };
   auto k_tiles = [&](int ks) {
@@ -155,19 +173,19 @@ __global__ void __launch_bounds__(THREADS, 1) k_gemm_tc(const __grid_constant__ 
       tc::prefetch_tmap(&tb);
       int it = 0;
       bool ok = true;
-      for (int64_t t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
+      for (int64_t t = cid; ok && t < n_tiles; t += n_clusters) {
         int tm, tn, ks;
         decode(t, tm, tn, ks);
         const int nk = k_tiles(ks);
         for (int kt = 0; kt < nk; ++kt, ++it) {
           const int s = it % STAGES;
           if (it >= STAGES && !(ok = tc::mbar_wait(&empty[s], ((it / STAGES) - 1) & 1, abort_flag, nullptr))) break;
-          tc::mbar_arrive_expect_tx(&full[s], STAGE);
+          tc::mbar_arrive_expect_tx(&full[s], STAGE);  // own A + both halves of B
           uint8_t* sa = smem + s * STAGE;
           const int64_t k = (int64_t)ks * p.k_per_split + (int64_t)kt * BK;
           for (int i = 0; i < BM / 64; ++i) load_box(sa + i * BOX, &ta, p.a, &full[s], (int64_t)tm * BM + 64 * i, k);
-          for (int i = 0; i < BN / 64; ++i)
-            load_box(sa + TILE_A + i * BOX, &tb, p.b, &full[s], (int64_t)tn * BN + 64 * i, k);
+          for (int i = crank * (BN / 128); i < (crank + 1) * (BN / 128); ++i)  // this CTA's half of B, to both
+            load_box_pair(sa + TILE_A + i * BOX, &tb, p.b, &full[s], (int64_t)tn * BN + 64 * i, k);
         }
       }
     }
@@ -181,7 +199,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_gemm_tc(const __grid_constant__ 
       const uint32_t a_step = p.a.k_major ? 32 : 2048, b_step = p.b.k_major ? 32 : 2048;  // bytes per K16 step
       int it = 0, tcount = 0;
       bool ok = true;
-      for (int64_t t = blockIdx.x; ok && t < n_tiles; t += gridDim.x, ++tcount) {
+      for (int64_t t = cid; ok && t < n_tiles; t += n_clusters, ++tcount) {
         int tm, tn, ks;
         decode(t, tm, tn, ks);
         const int nk = k_tiles(ks);
@@ -197,7 +215,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_gemm_tc(const __grid_constant__ 
 #pragma unroll
           for (int k16 = 0; k16 < BK / 16; ++k16)
             tc::mma_ss(d, tc::sdesc_add(ad, k16 * a_step), tc::sdesc_add(bd, k16 * b_step), idesc, kt > 0 || k16 > 0);
-          tc::mma_commit(&empty[s]);
+          tc::mma_commit_mc(&empty[s], 0x3);  // release the stage in both CTAs (the peer multicasts into it)
         }
         tc::mma_commit(&acc_full[buf]);
       }
@@ -209,7 +227,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_gemm_tc(const __grid_constant__ 
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
     int tcount = 0, nstage = 0;
     bool ok = true;
-    for (int64_t t = blockIdx.x; t < n_tiles; t += gridDim.x, ++tcount) {
+    for (int64_t t = cid; t < n_tiles; t += n_clusters, ++tcount) {
       int tm, tn, ks;
       decode(t, tm, tn, ks);
       const int nk = k_tiles(ks);
@@ -317,6 +335,9 @@ __global__ void __launch_bounds__(THREADS, 1) k_gemm_tc(const __grid_constant__ 
   }
   tc::fence_before_sync();
   __syncthreads();
+  // the peer may still multicast into this CTA's shared memory or arrive on its barriers until
+  // its own last MMAs are done: leave together
+  tc::cluster_sync();
   if (warp == 1) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, 2 * BN);
@@ -419,13 +440,25 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, int split_k, float* split_scratc
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       sms = 152;
   }
-  const int64_t n_tiles = (int64_t)p.tiles_m * p.tiles_n * split_k;
-  const int grid = (int)std::min<int64_t>(n_tiles, sms);
+  const int64_t n_units = (int64_t)((p.tiles_m + 1) / 2) * p.tiles_n * split_k;  // M-tile pairs
+  const int clusters = (int)std::max<int64_t>(1, std::min<int64_t>(n_units, sms / 2));
   cudaError_t e = cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  k_gemm_tc<<<grid, THREADS, SMEM_BYTES, st>>>(ta, tb, tout, p);
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)(2 * clusters));
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, k_gemm_tc, ta, tb, tout, p);
   note_launch();
-  e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess || split_k <= 1) return e;
   return launch_split_reduce(split_scratch, split_k, g.M, g.N, g.c, st);
 }
