@@ -8,14 +8,17 @@
 // contiguous segments a query row sees one interval of keys, so the mask of a partial tile is
 // two integer compares per element.
 //
-// One CTA = one head x two 128-row query tiles (a, b), 12 warps (warps 2-3 idle):
+// One CTA = one head x two 128-row query tiles (a, b), 12 warps (warp 3 idle):
 //   warp 0     TMA producer: Q_a, Q_b once, then K_j, V_j, K_j+1, ... through a ring of
-//              tile-sized slots; a K slot is freed as soon as both Q K^T products are done
-//   warp 1     MMA issuer (one thread) and TMEM owner: S_t = Q_t K^T (both operands in shared
-//              memory), O_t += P_t V (P_t read from TMEM, V from shared memory)
+//              tile-sized slots; a slot is refilled once both MMA issuers have released it
+//   warps 1, 2 MMA issuers (one thread each), one per query tile: S_t = Q_t K^T (both operands
+//              in shared memory), O_t += P_t V (P_t read from TMEM, V from shared memory); two
+//              independent streams keep the tensor pipe fed; warp 1 owns the TMEM allocation
 //   warps 4-7  softmax of tile a, warps 8-11 softmax of tile b: each thread owns one query row
 //              (TMEM lane 32 * (warp % 4) + lane): row max, exp2, row sum, P written back over
-//              S as bf16, all from one TMEM read of the row
+//              S as bf16, all from one TMEM read of the row.  On the key tiles both query tiles
+//              see, the two groups take turns (named-barrier ping-pong), so one group's softmax
+//              overlaps the tensor core's work on the other tile.
 // TMEM columns: S/P_a [0,128) S/P_b [128,256) O_a [256,256+Dh) O_b [256+Dh, 256+2Dh).
 // While one softmax group works, the tensor core runs the other tile's P V and next Q K^T.
 // The running max is rescaled lazily: O is corrected only when the row max grows by more than
@@ -49,8 +52,8 @@ struct FwdLayout {
 __device__ __forceinline__ bool in_range(const int4& r, int j) { return j >= r.x && j < r.w; }
 
 // Launched with 168 registers per thread (12 warps, 3 per SM sub-partition of 16K registers).
-// The control warpgroup then drops to 56 and the two softmax warpgroups rise to 216: per
-// sub-partition 56 + 216 + 216 = 488 <= 512 per lane, per CTA 62,464 <= 64,512.
+// The control warpgroup then drops to 72 and the two softmax warpgroups rise to 216: per
+// sub-partition 72 + 216 + 216 = 504 <= 512 per lane, per CTA 64,512 = the launch's 384 x 168.
 template <int DH, int MODE>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     k_attn_fwd_tc(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
@@ -91,7 +94,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
     for (int i = 0; i < NS; ++i) {
       tc::mbar_init(&slot_full[i], 1);
-      tc::mbar_init(&slot_empty[i], 1);
+      tc::mbar_init(&slot_empty[i], valid1 ? 2 : 1);  // released by each MMA issuer
     }
     *abort_flag = 0;
     tc::fence_mbar_init();
@@ -131,18 +134,23 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issuer
-    // Lean issue path: descriptors are built once and stepped by constant offsets, ring slots and
-    // phases are tracked incrementally, so the thread keeps the tensor pipe fed although it
-    // shares its SM sub-partition with two busy softmax warps.
-    if (lane == 0) {
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------------ MMA issuers
+    // One issuing thread per query tile (warp 1: tile a, warp 2: tile b), so the two tiles' MMA
+    // streams are independent and the tensor pipe takes whichever is ready.  Both walk all key
+    // tiles of the CTA and release every K/V slot (the slot barriers count one arrival per
+    // issuer).  The issue path is lean: descriptors are built once and stepped by constant
+    // offsets, ring slots and phases are tracked incrementally.
+    const int t = warp - 1;
+    if (lane == 0 && (t == 0 || valid1)) {
       constexpr uint32_t kIdS = tc::idesc_bf16(128, 128, false, false);
       constexpr uint32_t kIdO = tc::idesc_bf16(128, DH, false, true);
       const uint32_t sQ = smem_u32(smem + L::Q), sR = smem_u32(smem + L::RING);
-      const uint64_t dQ = tc::sdesc_sw128(sQ, 16, 1024);           // Q_t, K-major
+      const uint64_t dQt = tc::sdesc_add(tc::sdesc_sw128(sQ, 16, 1024), t * L::TB);  // Q_t, K-major
       const uint64_t dK = tc::sdesc_sw128(sR, 16, 1024);           // ring slot 0 read as K (K-major)
       const uint64_t dV = tc::sdesc_sw128(sR, kBoxBytes, 1024);    // ring slot 0 read as V (MN-major)
+      const uint32_t s_tm = tmem + L::s_col(t), o_tm = tmem + L::o_col(t);
+      const int4 rg = t ? rng1 : rng0;
       bool ok = tc::mbar_wait(q_full, 0, abort_flag, a.err);
       struct Pos { int slot; uint32_t phase; };
       auto next = [](Pos p) { return p.slot + 1 == NS ? Pos{0, p.phase ^ 1u} : Pos{p.slot + 1, p.phase}; };
@@ -150,49 +158,46 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (ok) ok = tc::mbar_wait(&slot_full[p.slot], p.phase, abort_flag, a.err);
         tc::fence_after_sync();
       };
-      auto issue_s = [&](int t, int slot) {
-        const uint64_t qd = tc::opaque(tc::sdesc_add(dQ, t * L::TB)), kd = tc::opaque(tc::sdesc_add(dK, slot * L::TB));
+      auto issue_s = [&](int slot) {
+        const uint64_t kd = tc::opaque(tc::sdesc_add(dK, slot * L::TB));
 #pragma unroll
         for (int k = 0; k < DH / 16; ++k) {
           const uint32_t off = (k >> 2) * kBoxBytes + (k & 3) * 32;
-          tc::mma_ss(tmem + L::s_col(t), tc::sdesc_add(qd, off), tc::sdesc_add(kd, off), kIdS, k > 0);
+          tc::mma_ss(s_tm, tc::sdesc_add(dQt, off), tc::sdesc_add(kd, off), kIdS, k > 0);
         }
         tc::mma_commit(&s_full[t]);
       };
-      auto issue_pv = [&](int t, int slot, bool first) {
+      auto issue_pv = [&](int slot, bool first) {
         const uint64_t vd = tc::opaque(tc::sdesc_add(dV, slot * L::TB));
 #pragma unroll
         for (int k = 0; k < 128 / 16; ++k)
-          tc::mma_ts(tmem + L::o_col(t), tmem + L::s_col(t) + k * 8, tc::sdesc_add(vd, k * 2048), kIdO, (!first) || k > 0);
+          tc::mma_ts(o_tm, s_tm + k * 8, tc::sdesc_add(vd, k * 2048), kIdO, (!first) || k > 0);
       };
-      const int4 rng[2] = {rng0, rng1};
-      int cnt_p[2] = {0, 0};
-      bool first_pv[2] = {true, true};
+      int cnt_p = 0;
+      bool first_pv = true;
       Pos kpos{0, 0u};  // ring position of K_j (item 2n); V_j follows it, then K_j+1
       if (ok) {
         wait_item(kpos);
-        for (int t = 0; t < 2; ++t)
-          if (ok && in_range(rng[t], j0)) issue_s(t, kpos.slot);
+        if (ok && in_range(rg, j0)) issue_s(kpos.slot);
         if (ok) tc::mma_commit(&slot_empty[kpos.slot]);
       }
       for (int j = j0; ok && j < j1; ++j) {
         const Pos vpos = next(kpos), knext = next(vpos);
         wait_item(vpos);                       // V_j
         if (j + 1 < j1) wait_item(knext);      // K_j+1
-        for (int t = 0; t < 2 && ok; ++t) {
-          if (in_range(rng[t], j)) {
-            ok = tc::mbar_wait(&p_full[t], cnt_p[t] & 1, abort_flag, a.err);
-            if (!ok) break;
-            ++cnt_p[t];
-            tc::fence_after_sync();
-            issue_pv(t, vpos.slot, first_pv[t]);
-            first_pv[t] = false;
-            if (j == rng[t].w - 1) tc::mma_commit(&o_full[t]);
-          }
-          if (t == 1 && ok) tc::mma_commit(&slot_empty[vpos.slot]);  // V_j free once both P V are issued
-          if (in_range(rng[t], j + 1)) issue_s(t, knext.slot);
+        if (!ok) break;
+        if (in_range(rg, j)) {
+          ok = tc::mbar_wait(&p_full[t], cnt_p & 1, abort_flag, a.err);
+          if (!ok) break;
+          ++cnt_p;
+          tc::fence_after_sync();
+          issue_pv(vpos.slot, first_pv);
+          first_pv = false;
+          if (j == rg.w - 1) tc::mma_commit(&o_full[t]);
         }
-        if (ok && j + 1 < j1) tc::mma_commit(&slot_empty[knext.slot]);  // K_j+1 free
+        tc::mma_commit(&slot_empty[vpos.slot]);                   // V_j released by this issuer
+        if (in_range(rg, j + 1)) issue_s(knext.slot);
+        if (j + 1 < j1) tc::mma_commit(&slot_empty[knext.slot]);  // K_j+1 released by this issuer
         kpos = knext;
       }
     }
@@ -219,10 +224,24 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const bool ragged = (S % kTile) != 0;
       float m_used = -INFINITY, l = 0.f;
       if (MODE == 1) m_used = row_ok ? a.lse[(int64_t)h * S + row] * kLog2e : 0.f;
+      // Ping-pong: on the key tiles that both query tiles see, the two softmax groups take turns
+      // (a then b on each key tile), so one group's softmax overlaps the tensor core's work on
+      // the other tile instead of both competing for the same issue slots.  Named barrier
+      // kPing + t is where group t waits for its turn; the other group's arrival grants it.
+      // Turns pair the same key tile in both groups, so the shared K/V ring never waits on a
+      // group that is waiting for its turn (on other key tiles the groups run free).
+      constexpr int kPing = 3;
+      const int pp_lo = max(rng0.x, rng1.x), pp_hi = valid1 ? min(rng0.w, rng1.w) : pp_lo;
+      const int n_pp = max(0, pp_hi - pp_lo);       // shared key tiles: one turn each per group
+      const int n_give = t == 0 ? n_pp : n_pp - 1;  // turns this group hands over inside the loop
+      if (t == 1 && n_pp > 0) tc::named_bar_arrive(kPing + 0, 256);
+      int turn = 0;
       bool ok = true;
       int cnt = 0;
       for (int j = rg.x; j < rg.w; ++j, ++cnt) {
         const bool partial = j < rg.y || j >= rg.z || (ragged && j == nt - 1);
+        const bool pp = j >= pp_lo && j < pp_hi;
+        if (pp) tc::named_bar_sync(kPing + t, 256);
         ok = tc::mbar_wait(&s_full[t], cnt & 1, abort_flag, a.err);
         if (!ok) break;
         tc::fence_after_sync();
@@ -291,7 +310,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         l = l * f + ((l4[0] + l4[1]) + (l4[2] + l4[3]));
         tc::fence_before_sync();
         tc::mbar_arrive(&p_full[t]);
+        if (pp) {
+          if (turn < n_give) tc::named_bar_arrive(kPing + 1 - t, 256);
+          ++turn;
+        }
       }
+      // after an abort, hand over the turns still owed so the other group never blocks on them
+      for (int k = turn; k < n_give; ++k) tc::named_bar_arrive(kPing + 1 - t, 256);
       if (ok) ok = tc::mbar_wait(&o_full[t], 0, abort_flag, a.err);
       tc::fence_after_sync();
       // epilogue: O / l -> bf16 row; lse or D
