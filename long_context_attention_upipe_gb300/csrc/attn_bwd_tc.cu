@@ -18,15 +18,16 @@
 //
 // k_attn_bwd_dkdv_tc  (one KV head x one 128-row key tile per CTA, 12 warps)
 //   warp 0 TMA: K_j, V_j once, then per work item (query head of the group x query tile) Q_i
-//   into a 3-slot ring and dO_i into a 2-slot ring; warp 1 MMA; warps 4-7 and 8-11 take
-//   alternate items, one key row per thread.  TMEM: dK and dV accumulators and two 128-column
-//   regions, one per element-wise group.  Per item:  S^T = K Q^T -> P^T written to TMEM (kept
-//   in registers) -> dV += P^T dO and dP^T = V dO^T into the same region -> dS^T = P^T (dP^T - D)
-//   written to TMEM -> dK += dS^T Q.  Query heads sharing the KV head accumulate in TMEM (GQA
-//   reduction inside the CTA).
-//
-// Every wait is bounded (see tc::mbar_wait); registers are split per role with setmaxnreg
-// (launch 168 x 384; control warpgroup 56, element-wise warpgroups 216).
+//   into a 3-slot ring and dO_i into a 2-slot ring; warps 1 and 2 issue the MMAs of the even
+//   and the odd items; warps 4-7 and 8-11 take the even and the odd items, one key row per
+//   thread.  TMEM: dK and dV accumulators and two 128-column regions, one per element-wise
+//   group.  Per item:  S^T = K Q^T -> P^T written to TMEM (kept in registers) -> dV += P^T dO
+//   and dP^T = V dO^T into the same region -> dS^T = P^T (dP^T - D) written to TMEM ->
+//   dK += dS^T Q.  Query heads sharing the KV head accumulate in TMEM (GQA reduction inside the
+//   CTA).  The two issuers keep the shared dK / dV accumulations in item order through token
+//   barriers; the two element-wise groups take turns phase by phase (named-barrier ping-pong).
+// Every wait on an mbarrier is bounded (see tc::mbar_wait); registers are split per role with
+// setmaxnreg (launch 168 x 384; control warpgroup 72, element-wise warpgroups 216).
 #include "internal.h"
 #include "tc_common.cuh"
 
@@ -412,6 +413,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
   uint64_t* o_empty = bars + 18;  // [NO]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 20);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 21);
+  uint64_t* dv_tok = bars + 22;   // phase n completes once dV(n) is issued
+  uint64_t* dk_tok = bars + 23;   // phase n completes once dK(n) is issued
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t S = a.S;
@@ -433,7 +436,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
       tc::mbar_init(&dp_full[i], 1);
       tc::mbar_init(&ds_full[i], 128);
     }
-    tc::mbar_init(acc_full, 1);
+    tc::mbar_init(acc_full, n_items >= 2 ? 2 : 1);  // the last MMAs of each issuer
+    tc::mbar_init(dv_tok, 1);
+    tc::mbar_init(dk_tok, 1);
     for (int i = 0; i < NQ; ++i) {
       tc::mbar_init(&q_full[i], 1);
       tc::mbar_init(&q_empty[i], 1);
@@ -480,53 +485,51 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
         }
       }
       __syncwarp();
-    } else if (warp == 1) {
-      if (lane == 0) {
+    } else if (warp == 1 || warp == 2) {
+      // One MMA-issuing thread per element-wise group (warp 1: even items, warp 2: odd items),
+      // so the two groups' waits and handshakes overlap.  The dK and dV accumulators are shared:
+      // the accumulating MMA groups stay in item order across the two threads through token
+      // barriers (tcgen05 fence before the arrival, fence after the wait), exactly as if one
+      // thread had issued them.
+      const int g = warp - 1;
+      if (lane == 0 && g < n_items) {
         const uint64_t dK = kdesc(smem_u32(smem + L::K)), dV = kdesc(smem_u32(smem + L::V));
         const uint64_t dQ = kdesc(smem_u32(smem + L::QR)), dQmn = mndesc(smem_u32(smem + L::QR));
-        const uint64_t dO = kdesc(smem_u32(smem + L::OR)), dOmn = mndesc(smem_u32(smem + L::OR));
+        const uint64_t dO = tc::sdesc_add(kdesc(smem_u32(smem + L::OR)), (g % NO) * L::TB);  // item n uses dO slot n % 2 == g
+        const uint64_t dOmn = tc::sdesc_add(mndesc(smem_u32(smem + L::OR)), (g % NO) * L::TB);
+        const uint32_t r_tm = tmem + L::r_col(g);
         bool ok = tc::mbar_wait(kv_full, 0, abort_flag, a.err);
-        auto issue_st = [&](int n) {  // S^T of item n into region n % 2
+        auto issue_st = [&](int n) {  // S^T of item n into this group's region
           if (ok) ok = tc::mbar_wait(&q_full[n % NQ], (n / NQ) & 1, abort_flag, a.err);
           if (!ok) return;
           tc::fence_after_sync();
-          mma_nt<DH>(tmem + L::r_col(n & 1), dK, tc::sdesc_add(dQ, (n % NQ) * L::TB));
-          tc::mma_commit(&s_full[n & 1]);
+          mma_nt<DH>(r_tm, dK, tc::sdesc_add(dQ, (n % NQ) * L::TB));
+          tc::mma_commit(&s_full[g]);
         };
-        // software pipeline: dV/dP^T of item n+1 are issued before dK of item n, so the tensor
-        // core works while the element-wise group of item n computes dS^T
-        auto issue_dv_dp = [&](int n) {
-          const int rr = n & 1;
-          const uint32_t oo = (n % NO) * L::TB;
-          ok = tc::mbar_wait(&p_full[rr], (n >> 1) & 1, abort_flag, a.err);
-          if (ok) ok = tc::mbar_wait(&o_full[n % NO], (n / NO) & 1, abort_flag, a.err);
-          if (!ok) return;
+        issue_st(g);
+        for (int n = g; ok && n < n_items; n += 2) {
+          const uint32_t ph = (n >> 1) & 1;
+          ok = tc::mbar_wait(&p_full[g], ph, abort_flag, a.err);
+          if (ok) ok = tc::mbar_wait(&o_full[g], (n / NO) & 1, abort_flag, a.err);
+          if (ok && n > 0) ok = tc::mbar_wait(dv_tok, (n - 1) & 1, abort_flag, a.err);  // dV(n-1) issued
+          if (!ok) break;
           tc::fence_after_sync();
-          mma_acc<DH>(tmem + L::DV_COL, tmem + L::r_col(rr), tc::sdesc_add(dOmn, oo), n > 0);  // dV += P^T dO
-          mma_nt<DH>(tmem + L::r_col(rr), dV, tc::sdesc_add(dO, oo));                           // dP^T = V dO^T
-          tc::mma_commit(&dp_full[rr]);
-          tc::mma_commit(&o_empty[n % NO]);
-        };
-        auto issue_dk = [&](int n) {
-          const int rr = n & 1;
-          ok = tc::mbar_wait(&ds_full[rr], (n >> 1) & 1, abort_flag, a.err);
-          if (!ok) return;
+          mma_acc<DH>(tmem + L::DV_COL, r_tm, dOmn, n > 0);  // dV += P^T dO
+          tc::fence_before_sync();
+          tc::mbar_arrive(dv_tok);
+          mma_nt<DH>(r_tm, dV, dO);  // dP^T = V dO^T
+          tc::mma_commit(&dp_full[g]);
+          tc::mma_commit(&o_empty[g]);
+          ok = tc::mbar_wait(&ds_full[g], ph, abort_flag, a.err);
+          if (ok && n > 0) ok = tc::mbar_wait(dk_tok, (n - 1) & 1, abort_flag, a.err);  // dK(n-1) issued
+          if (!ok) break;
           tc::fence_after_sync();
-          mma_acc<DH>(tmem + L::DK_COL, tmem + L::r_col(rr), tc::sdesc_add(dQmn, (n % NQ) * L::TB), n > 0);  // dK += dS^T Q
+          mma_acc<DH>(tmem + L::DK_COL, r_tm, tc::sdesc_add(dQmn, (n % NQ) * L::TB), n > 0);  // dK += dS^T Q
+          tc::fence_before_sync();
+          tc::mbar_arrive(dk_tok);
           tc::mma_commit(&q_empty[n % NQ]);
-          if (n == n_items - 1) tc::mma_commit(acc_full);
+          if (n + 2 >= n_items) tc::mma_commit(acc_full);  // this issuer's last item
           if (n + 2 < n_items) issue_st(n + 2);
-        };
-        // items in pairs (one per element-wise group): dV/dP^T of both, then dK and the next S^T
-        // of each, so no wait blocks work that is already possible
-        for (int n = 0; n < 2 && n < n_items; ++n) issue_st(n);
-        for (int n = 0; ok && n < n_items; n += 2) {
-#pragma unroll 1
-          for (int step = 0; step < 4 && ok; ++step) {  // dV/dP^T(n), dV/dP^T(n+1), dK(n), dK(n+1)
-            const int m = n + (step & 1);
-            if (m >= n_items) continue;
-            if (step < 2) issue_dv_dp(m); else issue_dk(m);
-          }
         }
       }
       __syncwarp();
@@ -556,6 +559,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
       return make_float2(-a.D[((int64_t)a.nh + hh) * sp + qoff], -a.D[(int64_t)hh * sp + qoff]);
     };
     float2 vec_next = grp < n_items ? load_vec(grp) : make_float2(0.f, 0.f);
+    // Ping-pong: the groups take turns phase by phase (P of items n and n+1, then dS of both),
+    // so one group's element-wise work overlaps the tensor core's work on the other's item.
+    // Group grp waits for its turn at named barrier kPing + grp (ids 1 and 2 stage lse/D).
+    constexpr int kPing = 3;
+    const int n_pp = 2 * min((n_items + 1) / 2, n_items / 2);
+    const int n_give = grp == 0 ? n_pp : n_pp - 1;
+    if (grp == 1 && n_pp > 0) tc::named_bar_arrive(kPing + 0, 256);
+    int turn = 0;
+    auto take_turn = [&]() { if (turn < n_pp) tc::named_bar_sync(kPing + grp, 256); };
+    auto give_turn = [&]() {
+      if (turn < n_give) tc::named_bar_arrive(kPing + 1 - grp, 256);
+      ++turn;
+    };
     for (int n = grp; n < n_items; n += 2) {
       const int qi = tr.x + n % nq;
       const bool partial = qi < tr.y || qi >= tr.z || (ragged && (qi == nt - 1 || jt == nt - 1));
@@ -572,6 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
       nvec[128 + r] = vec_next.y;
       tc::named_bar_sync(1 + grp, 128);
       if (n + 2 < n_items) vec_next = load_vec(n + 2);
+      take_turn();
       ok = tc::mbar_wait(&s_full[grp], cyc, abort_flag, a.err);
       if (!ok) break;
       tc::fence_after_sync();
@@ -610,13 +627,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
       tc::tmem_st_wait();
       tc::fence_before_sync();
       tc::mbar_arrive(&p_full[grp]);
+      give_turn();
+      take_turn();
       ok = tc::mbar_wait(&dp_full[grp], cyc, abort_flag, a.err);
       if (!ok) break;
       tc::fence_after_sync();
       ds_pass(r_addr, pk, [&](int k) { return *reinterpret_cast<const float2*>(nvec + 128 + k); });
       tc::fence_before_sync();
       tc::mbar_arrive(&ds_full[grp]);
+      give_turn();
     }
+    // after an abort, hand over the turns still owed so the other group never blocks on them
+    for (int k = turn; k < n_give; ++k) tc::named_bar_arrive(kPing + 1 - grp, 256);
     // epilogue: group 0 writes dK rows (scaled), group 1 writes dV rows
     if (ok && n_items > 0) ok = tc::mbar_wait(acc_full, 0, abort_flag, a.err);
     tc::fence_after_sync();

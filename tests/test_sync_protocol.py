@@ -131,3 +131,76 @@ def test_random_ranges_never_deadlock(kind):
         xa = rng.randint(0, 12); wa = xa + rng.randint(1, 12)
         xb = rng.randint(0, 12); wb = xb + rng.randint(1, 12)
         assert run(kind, (xa, wa), (xb, wb), rng.random() < 0.9), ((xa, wa), (xb, wb))
+
+
+# dK/dV: one MMA issuer per element-wise group; the shared dK / dV accumulations stay in item
+# order through token barriers; the element-wise groups take turns phase by phase.
+def run_dkdv_pp(N, NQ=3, NO=2):
+    ev = set()
+    Na, Nb = (N + 1) // 2, N // 2
+    n_pp = 2 * min(Na, Nb)
+    give = {0: 0, 1: 0}
+    def producer():
+        for n in range(N):
+            if n >= NQ:
+                yield lambda n=n: ("q_empty", n - NQ) in ev
+            ev.add(("Q", n))
+            if n >= NO:
+                yield lambda n=n: ("o_empty", n - NO) in ev
+            ev.add(("O", n))
+    def issuer(g):
+        if g >= N: return
+        yield lambda: ("Q", g) in ev
+        ev.add(("S", g))
+        for n in range(g, N, 2):
+            yield lambda n=n: ("P", n) in ev
+            yield lambda n=n: ("O", n) in ev
+            if n > 0:
+                yield lambda n=n: ("dv_tok", n - 1) in ev
+            ev.add(("dv_tok", n))
+            ev.add(("dP", n)); ev.add(("o_empty", n))
+            yield lambda n=n: ("dS", n) in ev
+            if n > 0:
+                yield lambda n=n: ("dk_tok", n - 1) in ev
+            ev.add(("dk_tok", n)); ev.add(("q_empty", n))
+            if n + 2 < N:
+                yield lambda n=n: ("Q", n + 2) in ev
+                ev.add(("S", n + 2))
+    def ew(g):
+        n_give = n_pp if g == 0 else n_pp - 1
+        st = {"turn": 0, "sync": 0}
+        if g == 1 and n_pp > 0: give[0] += 1
+        def take():
+            if st["turn"] < n_pp:
+                need = st["sync"] + 1
+                yield lambda: give[g] >= need
+                st["sync"] += 1
+        def giv():
+            if st["turn"] < n_pp:
+                if st["turn"] < n_give: give[1 - g] += 1
+            st["turn"] += 1
+        for n in range(g, N, 2):
+            yield from take()
+            yield lambda n=n: ("S", n) in ev
+            ev.add(("P", n)); giv()
+            yield from take()
+            yield lambda n=n: ("dP", n) in ev
+            ev.add(("dS", n)); giv()
+    actors = [producer(), issuer(0), issuer(1), ew(0), ew(1)]
+    waits = [None] * len(actors); done = [False] * len(actors)
+    while not all(done):
+        progress = False
+        for i, a in enumerate(actors):
+            if done[i]: continue
+            while waits[i] is None or waits[i]():
+                try:
+                    waits[i] = next(a); progress = True
+                except StopIteration:
+                    done[i] = True; break
+            if done[i]: progress = True
+        if not progress: return False
+    return True
+
+
+def test_dkdv_two_issuers_never_deadlock():
+    assert all(run_dkdv_pp(n) for n in range(0, 40))
