@@ -80,29 +80,27 @@ __device__ __forceinline__ void mma_acc(uint32_t d, uint32_t a_tmem, uint64_t bd
   for (int k = 0; k < 128 / 16; ++k) tc::mma_ts(d, a_tmem + k * 8, tc::sdesc_add(bdesc, k * 2048), kId, acc || k > 0);
 }
 
-// dS = P (dP - D) for 64 packed P pairs, dP in the region, result written over columns [0, 64):
-// half h reads dP columns [64h, 64h + 64) and writes [32h, 32h + 32), already read.
-// ndval(k) returns (-D[k], -D[k+1]); the arithmetic runs on fp32 pairs.
+// dS = P (dP - D) with P kept in fp32 registers (pa: columns 0-63, pb: 64-127); ndval(k)
+// returns (-D[k], -D[k+1]).  dP is read 32 columns at a time and dS chunk c (bf16 pairs) written
+// to columns [16c, 16c + 16), all of which earlier chunks have already read.
 template <typename DFn>
-__device__ __forceinline__ void ds_pass(uint32_t r_addr, const uint32_t (&pk)[64], DFn ndval) {
+__device__ __forceinline__ void ds_pass_f32(uint32_t r_addr, const uint32_t (&pa)[64], const uint32_t (&pb)[64],
+                                            DFn ndval) {
 #pragma unroll
-  for (int hf = 0; hf < 2; ++hf) {
-    uint32_t v0[32], v1[32], o[32];
-    tc::tmem_ld32(r_addr + hf * 64, v0);
-    tc::tmem_ld32(r_addr + hf * 64 + 32, v1);
+  for (int c = 0; c < 4; ++c) {
+    uint32_t v[32], o[16];
+    tc::tmem_ld32(r_addr + 32 * c, v);
     tc::tmem_ld_wait();
 #pragma unroll
+    for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(v[i]));
+    const uint32_t* pp = c < 2 ? &pa[32 * c] : &pb[32 * (c - 2)];
+#pragma unroll
     for (int i = 0; i < 16; ++i) {
-      const int k0 = hf * 64 + 2 * i, k1 = hf * 64 + 32 + 2 * i;
-      const float2 pa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[hf * 32 + i]));
-      const float2 pb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&pk[hf * 32 + 16 + i]));
-      const float2 da = __fadd2_rn(make_float2(__uint_as_float(v0[2 * i]), __uint_as_float(v0[2 * i + 1])), ndval(k0));
-      const float2 db = __fadd2_rn(make_float2(__uint_as_float(v1[2 * i]), __uint_as_float(v1[2 * i + 1])), ndval(k1));
-      const float2 ra = __fmul2_rn(pa, da), rb = __fmul2_rn(pb, db);
-      o[i] = tc::pack_bf16x2(ra.x, ra.y);
-      o[16 + i] = tc::pack_bf16x2(rb.x, rb.y);
+      const float2 d = __fadd2_rn(make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])), ndval(32 * c + 2 * i));
+      const float2 r = __fmul2_rn(make_float2(__uint_as_float(pp[2 * i]), __uint_as_float(pp[2 * i + 1])), d);
+      o[i] = tc::pack_bf16x2(r.x, r.y);
     }
-    tc::tmem_st32(r_addr + hf * 32, o);
+    tc::tmem_st16(r_addr + 16 * c, o);
   }
   tc::tmem_st_wait();
 }
@@ -296,7 +294,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dq_tc(const __grid_con
         ok = tc::mbar_wait(&s_full[t], cnt & 1, abort_flag, a.err);
         if (!ok) break;
         tc::fence_after_sync();
-        uint32_t pk[64];  // P as bf16 pairs
+        // P = exp2(s c - lse2) in fp32, in place of the scores (P only feeds dS here, so it is
+        // never rounded to bf16); the second half's TMEM load overlaps the first half's math
+        uint32_t sa[64], sb[64];
         {
           int lo = 0, hi = 127;
           if (partial) {
@@ -305,8 +305,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dq_tc(const __grid_con
             hi = (int)max((int64_t)-1, min(vis_hi - col0, (int64_t)128));
           }
           const float2 cc = make_float2(c, c), nl = make_float2(-lse2, -lse2);
-          // two halves of 64 columns: the second half's TMEM load overlaps the first half's math,
-          // and at most 128 score registers are live next to P
           // masked scores become -inf (exp2 -> 0) in a separate pass that only partial tiles run
           auto half = [&](uint32_t (&sv)[64], int hf) {
             if (partial) {
@@ -317,10 +315,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dq_tc(const __grid_con
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               const float2 arg = __ffma2_rn(make_float2(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])), cc, nl);
-              pk[hf * 32 + i] = tc::pack_bf16x2(fast_exp2(arg.x), fast_exp2(arg.y));
+              sv[2 * i] = __float_as_uint(fast_exp2(arg.x));
+              sv[2 * i + 1] = __float_as_uint(fast_exp2(arg.y));
             }
           };
-          uint32_t sa[64], sb[64];
           tmem_ld64(r_addr, sa);
           tmem_ld_wait_for(sa);
           tmem_ld64(r_addr + 64, sb);
@@ -333,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dq_tc(const __grid_con
         ok = tc::mbar_wait(&dp_full[t], cnt & 1, abort_flag, a.err);
         if (!ok) break;
         tc::fence_after_sync();
-        ds_pass(r_addr, pk, [&](int) { return make_float2(-Dr, -Dr); });
+        ds_pass_f32(r_addr, sa, sb, [&](int) { return make_float2(-Dr, -Dr); });
         tc::fence_before_sync();
         tc::mbar_arrive(&ds_full[t]);
       }
@@ -592,7 +590,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
       ok = tc::mbar_wait(&s_full[grp], cyc, abort_flag, a.err);
       if (!ok) break;
       tc::fence_after_sync();
-      uint32_t pk[64];  // P^T as bf16 pairs
+      // P^T = exp2(s c - lse2) kept in fp32 in place of the scores (for dS^T); its bf16 copy goes
+      // to TMEM as the A operand of dV += P^T dO
+      uint32_t sa[64], sb[64];
       {
         const float2 cc = make_float2(c, c);
         // two halves of 64 columns, the second loading while the first is computed (as in dQ)
@@ -610,11 +610,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
               const int kk = 2 * (i + u);
               const float2 arg = __ffma2_rn(make_float2(__uint_as_float(sv[kk]), __uint_as_float(sv[kk + 1])), cc,
                                             u ? make_float2(l4.z, l4.w) : make_float2(l4.x, l4.y));
-              pk[hf * 32 + i + u] = tc::pack_bf16x2(fast_exp2(arg.x), fast_exp2(arg.y));
+              sv[kk] = __float_as_uint(fast_exp2(arg.x));
+              sv[kk + 1] = __float_as_uint(fast_exp2(arg.y));
             }
           }
         };
-        uint32_t sa[64], sb[64];
         tmem_ld64(r_addr, sa);
         tmem_ld_wait_for(sa);
         tmem_ld64(r_addr + 64, sb);
@@ -622,8 +622,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
         tmem_ld_wait_for(sb);
         half(sb, 1);
       }
-      tc::tmem_st32(r_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-      tc::tmem_st32(r_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {  // bf16 pairs of columns [32q, 32q + 32) -> TMEM columns [16q, 16q + 16)
+        const uint32_t* pp = q < 2 ? &sa[32 * q] : &sb[32 * (q - 2)];
+        uint32_t o[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) o[i] = tc::pack_bf16x2(__uint_as_float(pp[2 * i]), __uint_as_float(pp[2 * i + 1]));
+        tc::tmem_st16(r_addr + 16 * q, o);
+      }
       tc::tmem_st_wait();
       tc::fence_before_sync();
       tc::mbar_arrive(&p_full[grp]);
@@ -632,7 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
       ok = tc::mbar_wait(&dp_full[grp], cyc, abort_flag, a.err);
       if (!ok) break;
       tc::fence_after_sync();
-      ds_pass(r_addr, pk, [&](int k) { return *reinterpret_cast<const float2*>(nvec + 128 + k); });
+      ds_pass_f32(r_addr, sa, sb, [&](int k) { return *reinterpret_cast<const float2*>(nvec + 128 + k); });
       tc::fence_before_sync();
       tc::mbar_arrive(&ds_full[grp]);
       give_turn();
