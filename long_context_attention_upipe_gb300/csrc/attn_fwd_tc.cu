@@ -265,7 +265,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (MODE == 0) {
           float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-          for (int k = 0; k < 128; ++k) m4[k & 3] = fmaxf(m4[k & 3], __uint_as_float(sv[k]));
+          for (int k = 0; k < 128; k += 2)
+            m4[(k >> 1) & 3] = fmax3(m4[(k >> 1) & 3], __uint_as_float(sv[k]), __uint_as_float(sv[k + 1]));
           const float mx = fmaxf(m_used, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * c);
           const bool need = mx > m_used + 8.f;
           rescale_o = need && cnt > 0 && m_used != -INFINITY;
