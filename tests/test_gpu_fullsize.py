@@ -103,3 +103,42 @@ def test_full_size_layer(key, hpc, prefix):
     assert not np.any(dXg[prefix:])
     assert rel_fro(to_f64(dW), dW_ref) <= GRAD_REL_FRO, rel_fro(to_f64(dW), dW_ref)
     assert rel_fro(to_f64(dWo), dWo_ref) <= GRAD_REL_FRO, rel_fro(to_f64(dWo), dWo_ref)
+
+
+def test_full_size_1m_share():
+    """The 1M-token share (4 query heads, 1 KV head, one chunk as benchmarked).  The oracle checks
+    rows of the first 4096 tokens (every key they see); every later row is checked through
+    properties that hold at any size: causality makes the first T rows of the 1M-token layer equal
+    to a T-token layer on the same inputs (checked against a separate 4096-token run of the
+    library), all outputs are finite, and with dY zero past the first P rows every gradient equals
+    the oracle's on the first P tokens and dX rows >= P are exactly zero."""
+    w = ui.workload("ulysses_1m")
+    hpc, prefix, T = 4, 1024, 4096
+    seg, Y, lse, dX, dW, dWo = run_layer(w, hpc, prefix)
+    for t in (Y, lse, dX, dW, dWo):
+        assert bool(torch.isfinite(t.float()).all())
+    assert int(torch.count_nonzero(dX[prefix:])) == 0
+    # oracle on sampled rows of the first T tokens
+    rows = np.array([0, 1, 127, 128, 129, 1000, 2047, 2048, T - 129, T - 1])
+    key_index = np.arange(0, T)
+    Xk, W, Wo, dYp = host_inputs(w, key_index, prefix)
+    Y_ref, L_ref = orc.layer_forward_rows(Xk[rows], Xk, key_index, rows, W, Wo, None, w.Hq, w.Hkv, w.Dh, w.causal)
+    y = to_f64(Y[torch.from_numpy(rows).cuda()])
+    assert max_abs_bf16_out(y, Y_ref) <= FULL_OUT_MAX_ABS, max_abs_bf16_out(y, Y_ref)
+    assert rel_fro(y, Y_ref) <= OUT_REL_FRO, rel_fro(y, Y_ref)
+    lse_err = np.abs(to_f64(lse)[:, rows] - L_ref) / np.maximum(1.0, np.abs(L_ref))
+    assert lse_err.max() <= 1e-2, lse_err.max()
+    # causality: the first T rows equal a T-token layer's (same tiles, same order of work)
+    small = up.Layer(up.make_desc(T, w.d, w.Hq, w.Hkv, w.Dh, hpc, w.causal))
+    Wd = dev_fill(((w.Hq + 2 * w.Hkv) * w.Dh, w.d), ui.TID_WQKV, ui.W_STD)
+    Wod = dev_fill((w.d, w.Hq * w.Dh), ui.TID_WO, ui.W_STD)
+    Ys, lses = small.forward(dev_fill((T, w.d), ui.TID_X, 1.0), Wd, Wod, None)
+    torch.cuda.synchronize()
+    assert max_abs(to_f64(Y[:T]), to_f64(Ys)) <= 1e-6 * max(1.0, float(Ys.float().abs().max()))
+    assert max_abs(to_f64(lse[:, :T]), to_f64(lses)) <= 1e-6 * max(1.0, float(lses.abs().max()))
+    # backward on the prefix
+    Xp = ui.normal_bf16_rows(np.arange(prefix), w.d, ui.TID_X)
+    dX_ref, dW_ref, dWo_ref = orc.layer_backward(Xp, W, Wo, None, dYp, w.Hq, w.Hkv, w.Dh, w.causal)
+    assert rel_fro(to_f64(dX[:prefix]), dX_ref) <= GRAD_REL_FRO, rel_fro(to_f64(dX[:prefix]), dX_ref)
+    assert rel_fro(to_f64(dW), dW_ref) <= GRAD_REL_FRO, rel_fro(to_f64(dW), dW_ref)
+    assert rel_fro(to_f64(dWo), dWo_ref) <= GRAD_REL_FRO, rel_fro(to_f64(dWo), dWo_ref)
