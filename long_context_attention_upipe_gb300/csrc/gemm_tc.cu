@@ -7,15 +7,21 @@
 // is the head), column slices of Wo (a 2-D map with the row stride of Wo) and the row blocks of
 // Wqkv that belong to a chunk (a 2-D map plus the first row of each block).
 //
-// Persistent kernel, one CTA per SM, launched as clusters of two CTAs that take the two M tiles
-// (m, m+1) of the same N tile: each CTA loads its own A tile and one half of the shared B tile,
-// multicast into both CTAs' shared memory, so every B byte crosses L2 once per pair (a third
-// less L2 traffic per MMA than independent CTAs).  6 warps:
-//   warp 0     TMA producer over a 4-stage ring of (A 128x64, B 256x64) tiles; a stage is
-//              refilled once the MMAs of both CTAs have released it (commits multicast to both)
-//   warp 1     MMA issuer (one thread), TMEM owner: 4 tcgen05.mma (M128 N256 K16) per stage into
-//              one of two TMEM accumulators, so the epilogue of a tile overlaps the next tile
-//   warps 2-5  epilogue: one output row per thread (TMEM lane), 32 columns at a time
+// Persistent kernel, one CTA per SM, launched as CTA pairs (clusters of two) that compute one
+// 256 x 256 output tile with the pair form of the tensor core (tcgen05 cta_group::2): each CTA
+// holds its own 128 rows of A and one half (128 columns) of B, the even CTA issues M256 N256
+// MMAs that read both CTAs' shared memory, and each CTA's TMEM receives its 128 rows of D.  A
+// stage is 32 KB per CTA (half of a single-CTA 128 x 256 tile's 48 KB), so six stages fit and
+// the tensor core reads half as many shared-memory bytes per FLOP.  6 warps per CTA:
+//   warps 0, 6 TMA producers (A and B respectively; one thread could not issue a stage's loads
+//              within its MMA time) over a 6-stage ring of (A 128x64, B half 128x64) tiles; both
+//              CTAs' loads count on the even CTA's stage barrier; a stage is refilled once the
+//              MMAs that read it have completed (commit multicast to both CTAs)
+//   warp 1     TMEM owner in both CTAs; in the even CTA the MMA issuer (one thread): 4 MMAs
+//              (M256 N256 K16) per stage into one of two TMEM accumulators, so the epilogue of
+//              a tile overlaps the next tile
+//   warps 2-5  epilogue: one output row per thread (TMEM lane), 32 columns at a time; both CTAs'
+//              epilogues release an accumulator on the even CTA's barrier
 // Plain row-major fp32 outputs (and split-K partials) leave through shared memory: each epilogue
 // warp stages a 32 x 32 fp32 box (128-byte swizzle, double-buffered) and one lane hands it to a
 // TMA bulk store, or to a TMA bulk reduce-add for C += A B^T, so the read-modify-write of an
@@ -30,10 +36,10 @@ namespace upipe {
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4, THREADS = 192;
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 6, THREADS = 224;  // BM: rows per CTA of the pair
 constexpr uint32_t BOX = 64 * 64 * 2;          // one 64 x 64 bf16 box, 8 KB
-constexpr uint32_t TILE_A = 2 * BOX;           // 128 x 64 A tile
-constexpr uint32_t TILE_B = 4 * BOX;           // 256 x 64 B tile
+constexpr uint32_t TILE_A = 2 * BOX;           // 128 x 64 A tile (this CTA's rows)
+constexpr uint32_t TILE_B = 2 * BOX;           // 128 x 64: this CTA's half of the 256-wide B tile
 constexpr uint32_t STAGE = TILE_A + TILE_B;
 constexpr uint32_t STG_OFF = STAGES * STAGE;         // epilogue staging: 4 warps x 2 boxes of 32 x 32 fp32
 constexpr uint32_t STG_BOX = 32 * 32 * 4;
@@ -83,13 +89,13 @@ __device__ __forceinline__ void load_box(uint8_t* dst, const CUtensorMap* map, c
   else tc::tma_load_2d(dst, map, bar, c0, c1);
 }
 
-// The same box into both CTAs of the cluster pair.
-__device__ __forceinline__ void load_box_pair(uint8_t* dst, const CUtensorMap* map, const TcOpDev& o, uint64_t* bar,
-                                              int64_t mn, int64_t k) {
+// A box into this CTA's shared memory, counted on the even CTA's barrier (shared::cluster address).
+__device__ __forceinline__ void load_box_pair(uint8_t* dst, const CUtensorMap* map, const TcOpDev& o,
+                                              uint32_t bar_cluster, int64_t mn, int64_t k) {
   int c0, c1, c2;
   box_coords(o, mn, k, c0, c1, c2);
-  if (o.rank == 3) tc::tma_load_3d_mc(dst, map, bar, c0, c1, c2, 0x3);
-  else tc::tma_load_2d_mc(dst, map, bar, c0, c1, 0x3);
+  if (o.rank == 3) tc::tma_load_3d_pair(dst, map, bar_cluster, c0, c1, c2);
+  else tc::tma_load_2d_pair(dst, map, bar_cluster, c0, c1);
 }
 
 // smem descriptor of one operand tile at MMA K-step k16 (16 elements)
@@ -134,19 +140,19 @@ __global__ void __launch_bounds__(THREADS, 1) k_gemm_tc(const __grid_constant__ 
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
-      tc::mbar_init(&full[i], 1);
-      tc::mbar_init(&empty[i], 2);  // the MMA commits of both CTAs
+      tc::mbar_init(&full[i], 1);   // even CTA: its producer's arrival + both CTAs' bytes
+      tc::mbar_init(&empty[i], 1);  // the even CTA's MMA commit (multicast to both)
     }
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&acc_full[i], 1);
-      tc::mbar_init(&acc_empty[i], 128);
+      tc::mbar_init(&acc_empty[i], 2 * 128);  // even CTA: both CTAs' epilogue threads
     }
     *abort_flag = 0;
     tc::fence_mbar_init();
   }
   if (warp == 1) {
-    tc::tmem_alloc(tmem_slot, 2 * BN);
-    tc::tmem_relinquish();
+    tc::tmem_alloc_pair(tmem_slot, 2 * BN);
+    tc::tmem_relinquish_pair();
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -167,10 +173,12 @@ __global__ void __launch_bounds__(THREADS, 1) k_gemm_tc(const __grid_constant__ 
     return ke > kb ? (int)ceil_div(ke - kb, BK) : 0;
   };
 
-  if (warp == 0) {
+  if (warp == 0 || warp == 6) {
+    // warp 0 loads A (and announces the stage's bytes), warp 6 loads this CTA's half of B
+    const bool is_a = warp == 0;
     if (lane == 0) {
-      tc::prefetch_tmap(&ta);
-      tc::prefetch_tmap(&tb);
+      tc::prefetch_tmap(is_a ? &ta : &tb);
+      const uint32_t full0 = tc::mapa_cluster(smem_u32(&full[0]), 0);  // the even CTA's stage barriers
       int it = 0;
       bool ok = true;
       for (int64_t t = cid; ok && t < n_tiles; t += n_clusters) {
@@ -180,19 +188,23 @@ __global__ void __launch_bounds__(THREADS, 1) k_gemm_tc(const __grid_constant__ 
         for (int kt = 0; kt < nk; ++kt, ++it) {
           const int s = it % STAGES;
           if (it >= STAGES && !(ok = tc::mbar_wait(&empty[s], ((it / STAGES) - 1) & 1, abort_flag, nullptr))) break;
-          tc::mbar_arrive_expect_tx(&full[s], STAGE);  // own A + both halves of B
+          if (is_a && crank == 0) tc::mbar_arrive_expect_tx(&full[s], 2 * STAGE);  // both CTAs' A and B halves
+          const uint32_t bar = full0 + s * 8;
           uint8_t* sa = smem + s * STAGE;
           const int64_t k = (int64_t)ks * p.k_per_split + (int64_t)kt * BK;
-          for (int i = 0; i < BM / 64; ++i) load_box(sa + i * BOX, &ta, p.a, &full[s], (int64_t)tm * BM + 64 * i, k);
-          for (int i = crank * (BN / 128); i < (crank + 1) * (BN / 128); ++i)  // this CTA's half of B, to both
-            load_box_pair(sa + TILE_A + i * BOX, &tb, p.b, &full[s], (int64_t)tn * BN + 64 * i, k);
+          if (is_a) {
+            for (int i = 0; i < BM / 64; ++i) load_box_pair(sa + i * BOX, &ta, p.a, bar, (int64_t)tm * BM + 64 * i, k);
+          } else {
+            for (int i = 0; i < 2; ++i)  // B columns [tn*BN + 128*crank, +128): this CTA's half
+              load_box_pair(sa + TILE_A + i * BOX, &tb, p.b, bar, (int64_t)tn * BN + 128 * crank + 64 * i, k);
+          }
         }
       }
     }
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0) {
-      const uint32_t idesc = tc::idesc_bf16(BM, BN, !p.a.k_major, !p.b.k_major);
+    if (lane == 0 && crank == 0) {
+      const uint32_t idesc = tc::idesc_bf16(2 * BM, BN, !p.a.k_major, !p.b.k_major);
       // descriptors of stage 0, stepped by constant offsets (stage, K step) in the loop
       const uint32_t s0 = smem_u32(smem);
       const uint64_t a0 = tile_desc(s0, p.a.k_major, 0), b0 = tile_desc(s0 + TILE_A, p.b.k_major, 0);
@@ -214,10 +226,10 @@ __global__ void __launch_bounds__(THREADS, 1) k_gemm_tc(const __grid_constant__ 
           const uint64_t ad = tc::opaque(tc::sdesc_add(a0, s * STAGE)), bd = tc::opaque(tc::sdesc_add(b0, s * STAGE));
 #pragma unroll
           for (int k16 = 0; k16 < BK / 16; ++k16)
-            tc::mma_ss(d, tc::sdesc_add(ad, k16 * a_step), tc::sdesc_add(bd, k16 * b_step), idesc, kt > 0 || k16 > 0);
-          tc::mma_commit_mc(&empty[s], 0x3);  // release the stage in both CTAs (the peer multicasts into it)
+            tc::mma_ss_pair(d, tc::sdesc_add(ad, k16 * a_step), tc::sdesc_add(bd, k16 * b_step), idesc, kt > 0 || k16 > 0);
+          tc::mma_commit_pair(&empty[s]);  // release the stage in both CTAs
         }
-        tc::mma_commit(&acc_full[buf]);
+        tc::mma_commit_pair(&acc_full[buf]);
       }
     }
     __syncwarp();
@@ -328,7 +340,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_gemm_tc(const __grid_constant__ 
         }
       }
       tc::fence_before_sync();
-      tc::mbar_arrive(&acc_empty[buf]);
+      tc::mbar_arrive_cluster(tc::mapa_cluster(smem_u32(&acc_empty[buf]), 0));  // on the even CTA's barrier
     }
     if (lane == 0) tc::bulk_wait_all();  // bulk stores complete before the CTA exits
     __syncwarp();
@@ -340,7 +352,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_gemm_tc(const __grid_constant__ 
   tc::cluster_sync();
   if (warp == 1) {
     tc::fence_after_sync();
-    tc::tmem_dealloc(tmem, 2 * BN);
+    tc::tmem_dealloc_pair(tmem, 2 * BN);
   }
 }
 
