@@ -13,10 +13,11 @@
 // MMAs that read both CTAs' shared memory, and each CTA's TMEM receives its 128 rows of D.  A
 // stage is 32 KB per CTA (half of a single-CTA 128 x 256 tile's 48 KB), so six stages fit and
 // the tensor core reads half as many shared-memory bytes per FLOP.  6 warps per CTA:
-//   warps 0, 6 TMA producers (A and B respectively; one thread could not issue a stage's loads
-//              within its MMA time) over a 6-stage ring of (A 128x64, B half 128x64) tiles; both
-//              CTAs' loads count on the even CTA's stage barrier; a stage is refilled once the
-//              MMAs that read it have completed (commit multicast to both CTAs)
+//   warps 0, 6, 7, 8  TMA producers, one 64 x 64 box of a stage each (A rows 0-63, A rows 64-127,
+//              B rows 0-63, B rows 64-127; one thread could not issue a stage's four loads within
+//              its MMA time) over a 6-stage ring of (A 128x64, B half 128x64) tiles; both CTAs'
+//              loads count on the even CTA's stage barrier; a stage is refilled once the MMAs
+//              that read it have completed (commit multicast to both CTAs)
 //   warp 1     TMEM owner in both CTAs; in the even CTA the MMA issuer (one thread): 4 MMAs
 //              (M256 N256 K16) per stage into one of two TMEM accumulators, so the epilogue of
 //              a tile overlaps the next tile
@@ -36,7 +37,7 @@ namespace upipe {
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 6, THREADS = 224;  // BM: rows per CTA of the pair
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 6, THREADS = 288;  // BM: rows per CTA of the pair
 constexpr uint32_t BOX = 64 * 64 * 2;          // one 64 x 64 bf16 box, 8 KB
 constexpr uint32_t TILE_A = 2 * BOX;           // 128 x 64 A tile (this CTA's rows)
 constexpr uint32_t TILE_B = 2 * BOX;           // 128 x 64: this CTA's half of the 256-wide B tile
@@ -173,9 +174,11 @@ __global__ void __launch_bounds__(THREADS, 1) k_gemm_tc(const __grid_constant__ 
     return ke > kb ? (int)ceil_div(ke - kb, BK) : 0;
   };
 
-  if (warp == 0 || warp == 6) {
-    // warp 0 loads A (and announces the stage's bytes), warp 6 loads this CTA's half of B
-    const bool is_a = warp == 0;
+  if (warp == 0 || warp >= 6) {
+    // one box per warp and stage: warps 0, 6 load A rows 0-63 / 64-127 (warp 0 also announces the
+    // stage's bytes), warps 7, 8 load this CTA's half of B, rows 0-63 / 64-127
+    const int q = warp == 0 ? 0 : warp - 5;  // 0..3
+    const bool is_a = q < 2;
     if (lane == 0) {
       tc::prefetch_tmap(is_a ? &ta : &tb);
       const uint32_t full0 = tc::mapa_cluster(smem_u32(&full[0]), 0);  // the even CTA's stage barriers
@@ -188,16 +191,14 @@ __global__ void __launch_bounds__(THREADS, 1) k_gemm_tc(const __grid_constant__ 
         for (int kt = 0; kt < nk; ++kt, ++it) {
           const int s = it % STAGES;
           if (it >= STAGES && !(ok = tc::mbar_wait(&empty[s], ((it / STAGES) - 1) & 1, abort_flag, nullptr))) break;
-          if (is_a && crank == 0) tc::mbar_arrive_expect_tx(&full[s], 2 * STAGE);  // both CTAs' A and B halves
+          if (q == 0 && crank == 0) tc::mbar_arrive_expect_tx(&full[s], 2 * STAGE);  // both CTAs' A and B halves
           const uint32_t bar = full0 + s * 8;
           uint8_t* sa = smem + s * STAGE;
           const int64_t k = (int64_t)ks * p.k_per_split + (int64_t)kt * BK;
-          if (is_a) {
-            for (int i = 0; i < BM / 64; ++i) load_box_pair(sa + i * BOX, &ta, p.a, bar, (int64_t)tm * BM + 64 * i, k);
-          } else {
-            for (int i = 0; i < 2; ++i)  // B columns [tn*BN + 128*crank, +128): this CTA's half
-              load_box_pair(sa + TILE_A + i * BOX, &tb, p.b, bar, (int64_t)tn * BN + 128 * crank + 64 * i, k);
-          }
+          const int i = q & 1;
+          if (is_a) load_box_pair(sa + i * BOX, &ta, p.a, bar, (int64_t)tm * BM + 64 * i, k);
+          else  // B columns [tn*BN + 128*crank, +128): this CTA's half
+            load_box_pair(sa + TILE_A + i * BOX, &tb, p.b, bar, (int64_t)tn * BN + 128 * crank + 64 * i, k);
         }
       }
     }
