@@ -39,6 +39,8 @@ def parse():
     ap.add_argument("--hpc", type=int, default=8)
     ap.add_argument("--accum-mode", type=int, default=0)
     ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-graph", action="store_true", help="launch the step's kernels one by one instead of replaying "
+                    "a CUDA graph of them")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--sample-tokens", type=int, default=1024, help="oracle sample length (CPU legs)")
@@ -252,11 +254,29 @@ def main():
         dW = torch.empty(W.shape, dtype=torch.float32, device=dev)
         dWo = torch.empty(Wo.shape, dtype=torch.float32, device=dev)
 
-        def step():
-            up.fwd(desc, X, W, Wo, seg_t, Y, lse, layer.ws_fwd, stream)
-            up.bwd(desc, X, W, Wo, seg_t, dY, lse, dX, dW, dWo, layer.ws_bwd, stream)
+        def step_on(s):
+            up.fwd(desc, X, W, Wo, seg_t, Y, lse, layer.ws_fwd, s)
+            up.bwd(desc, X, W, Wo, seg_t, dY, lse, dX, dW, dWo, layer.ws_bwd, s)
 
-        return desc, layer, step, (Y, lse, dX, dW, dWo)
+        def step():
+            step_on(stream)
+
+        return desc, layer, step, (Y, lse, dX, dW, dWo), step_on
+
+    def graph_of(step_on):
+        """The step's kernel launches captured once in a CUDA graph (same kernels, same arguments,
+        no per-kernel host launch cost); returns (replay, kernels per step) or (None, reason)."""
+        try:
+            g = torch.cuda.CUDAGraph()
+            torch.cuda.synchronize()
+            n0 = up.launch_count()
+            with torch.cuda.graph(g):
+                step_on(torch.cuda.current_stream())
+            n = up.launch_count() - n0
+            torch.cuda.synchronize()
+            return g, n
+        except Exception as ex:  # report and fall back to launching kernel by kernel
+            return None, f"{type(ex).__name__}: {ex}"[:160]
 
     def barrier():
         if world > 1:
@@ -311,15 +331,29 @@ def main():
     # ---------------- main timed run
     torch.cuda.reset_peak_memory_stats(dev)
     base_alloc = torch.cuda.memory_allocated(dev)
-    desc, layer, step, outs = make_layer(args.hpc)
+    desc, layer, step, outs, step_on = make_layer(args.hpc)
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize()
+    launch_mode, graph, per_step = "eager", None, 0
+    if not args.no_graph:
+        graph, per_step = graph_of(step_on)
+        if graph is not None:
+            launch_mode = "cuda_graph"
+            timed = graph.replay
+            for _ in range(max(3, args.warmup)):
+                timed()
+            torch.cuda.synchronize()
+        else:
+            launch_mode = f"eager (graph capture failed: {per_step})"
+    if graph is None:
+        timed = step
     sampler = ClockSampler(local)
     sampler.start()
     launches_before = up.launch_count()
-    ms = time_steps(step, args.steps)
-    launches = up.launch_count() - launches_before  # our kernels launched in the timed region
+    ms = time_steps(timed, args.steps)
+    # our kernels launched in the timed region (graph replays launch the kernels counted at capture)
+    launches = per_step * args.steps if graph is not None else up.launch_count() - launches_before
     clocks = sampler.stop()
     peak_gb = torch.cuda.max_memory_allocated(dev) / 1e9
     ms_all = ms
@@ -360,7 +394,10 @@ def main():
                 torch.cuda.empty_cache()
                 torch.cuda.reset_peak_memory_stats(dev)
                 before = torch.cuda.memory_allocated(dev)
-                dsc, lay, stp, _ = make_layer(h)
+                dsc, lay, stp, _, stp_on = make_layer(h)
+                gr = None if args.no_graph else graph_of(stp_on)[0]
+                if gr is not None:
+                    stp = gr.replay
                 stp()
                 t = time_steps(stp, 3)
                 pk = torch.cuda.max_memory_allocated(dev) / 1e9
@@ -368,8 +405,8 @@ def main():
                               "tflops": round(flops / (t * 1e-3) / 1e12, 2), "peak_hbm_gb": round(pk, 3),
                               "workspace_gb": round((up.workspace_bytes(dsc, 0) + up.workspace_bytes(dsc, 1)) / 1e9, 3),
                               "inputs_outputs_gb": round(before / 1e9, 3)})
-                del lay, stp
-            desc, layer, step, outs = make_layer(args.hpc)
+                del lay, stp, gr
+            desc, layer, step, outs, step_on = make_layer(args.hpc)
 
         # ---------------- end to end through the C-ABI with host buffers
         e2e = None
@@ -431,6 +468,7 @@ def main():
             "e2e": e2e,
             "cpu_baseline": cpu,
             "gpu_launches": launches,
+            "launch": launch_mode,
             "clocks": clocks,
         }
         print(json.dumps(result), flush=True)

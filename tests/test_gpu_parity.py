@@ -229,3 +229,36 @@ def test_layer_flags_unsorted_segments():
     layer.forward(bf16_tensor(X), bf16_tensor(W), bf16_tensor(Wo), torch.from_numpy(seg).cuda())
     assert up.device_status(layer.ws_fwd) == 5
 
+
+
+def test_layer_step_replays_bit_exact_from_a_cuda_graph():
+    """The forward and backward calls make no synchronous host call and allocate nothing, so a
+    step can be captured once in a CUDA graph; its replays give the eager results bit for bit."""
+    S, d, Hq, Hkv, Dh = 640, 256, 8, 2, 64
+    X, W, Wo, dY = layer_inputs(S, d, Hq, Hkv, Dh)
+    Xt, Wt, Wot, dYt = (bf16_tensor(x) for x in (X, W, Wo, dY))
+    desc = up.make_desc(S, d, Hq, Hkv, Dh, 2, True)
+    layer = up.Layer(desc)
+    Y = torch.empty_like(Xt); lse = torch.empty(Hq, S, dtype=torch.float32, device="cuda")
+    dX = torch.empty_like(Xt); dW = torch.empty(Wt.shape, dtype=torch.float32, device="cuda")
+    dWo = torch.empty(Wot.shape, dtype=torch.float32, device="cuda")
+
+    def step(s):
+        up.fwd(desc, Xt, Wt, Wot, None, Y, lse, layer.ws_fwd, s)
+        up.bwd(desc, Xt, Wt, Wot, None, dYt, lse, dX, dW, dWo, layer.ws_bwd, s)
+
+    step(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    eager = [t.clone() for t in (Y, lse, dX, dW, dWo)]
+    for t in (Y, lse, dX, dW, dWo):
+        t.zero_()
+    g = torch.cuda.CUDAGraph()
+    n0 = up.launch_count()
+    with torch.cuda.graph(g):
+        step(torch.cuda.current_stream())
+    assert up.launch_count() > n0
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    for got, want in zip((Y, lse, dX, dW, dWo), eager):
+        assert torch.equal(got, want)
