@@ -146,8 +146,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dq_tc(const __grid_con
   const int64_t S = a.S;
   const int nt = (int)ceil_div(S, kTile);
   const int64_t sp = (int64_t)nt * kTile;
-  const int pair = gridDim.x - 1 - blockIdx.x;
-  const int h = blockIdx.y;
+  const int pair = gridDim.y - 1 - blockIdx.y;  // longest query tiles first, across all heads
+  const int h = blockIdx.x;
   const int kvh = h / a.g;
   const int qt0 = 2 * pair, qt1 = 2 * pair + 1;
   const bool valid1 = qt1 < nt;
@@ -418,8 +418,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
   const int64_t S = a.S;
   const int nt = (int)ceil_div(S, kTile);
   const int64_t sp = (int64_t)nt * kTile;
-  const int jt = blockIdx.x;  // key tile (small j has the most query tiles under causality)
-  const int kvh = blockIdx.y;
+  // grid (KV heads, key tiles) with the head fastest: the longest key tiles (small j has the most
+  // query tiles under causality) of every head are dispatched first
+  const int jt = blockIdx.y;
+  const int kvh = blockIdx.x;
   const int4 tr = a.kv_rows[jt];  // query tiles {begin, full_begin, full_end, end}
   const int h_first = kvh * a.g;
   const int n_heads = max(0, min(a.nh, h_first + a.g) - h_first);
@@ -718,7 +720,7 @@ cudaError_t run_dq(const AttnBwdArgs& b, cudaStream_t st) {
   CUtensorMap tq, tdo, tk, tv;
   if (!make_maps<DH>(b.f, &tq, &tdo, &tk, &tv)) return cudaErrorInvalidValue;
   const int nt = (int)ceil_div(b.f.S, kTile);
-  return launch(k_attn_bwd_dq_tc<DH>, DqLayout<DH>::BYTES + 1024, dim3((unsigned)ceil_div(nt, 2), (unsigned)b.f.nh), tq,
+  return launch(k_attn_bwd_dq_tc<DH>, DqLayout<DH>::BYTES + 1024, dim3((unsigned)b.f.nh, (unsigned)ceil_div(nt, 2)), tq,
                 tdo, tk, tv, b, st);
 }
 
@@ -727,7 +729,7 @@ cudaError_t run_dkdv(const AttnBwdArgs& b, cudaStream_t st) {
   CUtensorMap tq, tdo, tk, tv;
   if (!make_maps<DH>(b.f, &tq, &tdo, &tk, &tv)) return cudaErrorInvalidValue;
   const int nt = (int)ceil_div(b.f.S, kTile);
-  return launch(k_attn_bwd_dkdv_tc<DH>, DkvLayout<DH>::BYTES, dim3((unsigned)nt, (unsigned)b.nkv), tq, tdo, tk, tv,
+  return launch(k_attn_bwd_dkdv_tc<DH>, DkvLayout<DH>::BYTES, dim3((unsigned)b.nkv, (unsigned)nt), tq, tdo, tk, tv,
                 b, st);
 }
 

@@ -75,8 +75,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t S = a.S;
   const int nt = (int)ceil_div(S, kTile);
-  const int pair = gridDim.x - 1 - blockIdx.x;  // longest query tiles first
-  const int h = blockIdx.y;
+  // grid (heads, query-tile pairs) with the head fastest, so the CTAs are dispatched longest
+  // query tiles first across all heads (a late long CTA would leave the others idle at the end)
+  const int pair = gridDim.y - 1 - blockIdx.y;
+  const int h = blockIdx.x;
   const int kvh = h / a.g;
   const int qt0 = 2 * pair, qt1 = 2 * pair + 1;
   const bool valid1 = qt1 < nt;
@@ -382,7 +384,7 @@ cudaError_t run(const AttnArgs& a, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int nt = (int)ceil_div(a.S, kTile);
-  dim3 grid((unsigned)ceil_div(nt, 2), (unsigned)a.nh);
+  dim3 grid((unsigned)a.nh, (unsigned)ceil_div(nt, 2));
   kfn<<<grid, kFwdThreads, smem, st>>>(tq, tk, tv, a);
   note_launch();
   return cudaGetLastError();
