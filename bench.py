@@ -254,9 +254,17 @@ def main():
         dW = torch.empty(W.shape, dtype=torch.float32, device=dev)
         dWo = torch.empty(Wo.shape, dtype=torch.float32, device=dev)
 
-        def step_on(s):
+        def fwd_on(s):
             up.fwd(desc, X, W, Wo, seg_t, Y, lse, layer.ws_fwd, s)
+
+        def bwd_on(s):
             up.bwd(desc, X, W, Wo, seg_t, dY, lse, dX, dW, dWo, layer.ws_bwd, s)
+
+        def step_on(s):
+            fwd_on(s)
+            bwd_on(s)
+
+        step_on.fwd, step_on.bwd = fwd_on, bwd_on
 
         def step():
             step_on(stream)
@@ -388,7 +396,7 @@ def main():
         # ---------------- hpc sweep: speed and peak memory vs chunk size
         sweep = []
         if not args.no_sweep:
-            del layer
+            del layer, graph, timed, step, step_on
             for h in w.hpc_sweep:
                 torch.cuda.synchronize()
                 torch.cuda.empty_cache()
@@ -405,7 +413,7 @@ def main():
                               "tflops": round(flops / (t * 1e-3) / 1e12, 2), "peak_hbm_gb": round(pk, 3),
                               "workspace_gb": round((up.workspace_bytes(dsc, 0) + up.workspace_bytes(dsc, 1)) / 1e9, 3),
                               "inputs_outputs_gb": round(before / 1e9, 3)})
-                del lay, stp, gr
+                del lay, stp, gr, stp_on  # the graph and the step closures hold the layer's workspace
             desc, layer, step, outs, step_on = make_layer(args.hpc)
 
         # ---------------- end to end through the C-ABI with host buffers
@@ -423,12 +431,21 @@ def main():
             hdWo = torch.empty(dWo.shape, dtype=dWo.dtype, pin_memory=True)
             dX_, dW_, dWo_ = dX, dW, dWo
 
+            copy = torch.cuda.Stream()
+            dy_ready = torch.cuda.Event()
+
             def e2e_step():
+                # dY is only needed by the backward: its upload overlaps the forward
+                copy.wait_stream(stream)  # the previous step's backward has finished reading dY
+                with torch.cuda.stream(copy):
+                    dY.copy_(hdY, non_blocking=True)
+                    dy_ready.record(copy)
                 X.copy_(hX, non_blocking=True)
                 W.copy_(hW, non_blocking=True)
                 Wo.copy_(hWo, non_blocking=True)
-                dY.copy_(hdY, non_blocking=True)
-                step()
+                step_on.fwd(stream)
+                stream.wait_event(dy_ready)
+                step_on.bwd(stream)
                 hdX.copy_(dX_, non_blocking=True)
                 hdW.copy_(dW_, non_blocking=True)
                 hdWo.copy_(dWo_, non_blocking=True)
