@@ -195,6 +195,20 @@ def layer_forward(X, Wqkv, Wo, seg, Hq, Hkv, Dh, causal=True, scale=None, return
     return Y, LSE
 
 
+def project_kv(X_keys, Wk, Wv, Hkv, Dh, row_block: int = 65536):
+    """K_kv = X Wk_kv^T and V_kv = X Wv_kv^T for the rows of X_keys ([n, d], bf16 bit patterns or
+    floats), widened and multiplied `row_block` rows at a time so that a million-row X never
+    exists in float64 at once.  Returns K, V [Hkv, n, Dh]."""
+    n = np.asarray(X_keys).shape[0]
+    K = np.empty((Hkv, n, Dh))
+    V = np.empty((Hkv, n, Dh))
+    for a in range(0, n, row_block):
+        Xb = _widen(X_keys[a: a + row_block])
+        K[:, a: a + Xb.shape[0]] = heads(Xb @ Wk.T, Hkv, Dh)
+        V[:, a: a + Xb.shape[0]] = heads(Xb @ Wv.T, Hkv, Dh)
+    return K, V
+
+
 def layer_forward_rows(X_rows, X_keys, key_index, rows, Wqkv, Wo, seg, Hq, Hkv, Dh, causal=True,
                        scale=None):
     """Output rows `rows` of the layer, for long sequences.
@@ -203,14 +217,13 @@ def layer_forward_rows(X_rows, X_keys, key_index, rows, Wqkv, Wo, seg, Hq, Hkv, 
     positions `key_index` (sorted), which must include every key any of the rows can see.
     Returns Y [R, d] and LSE [Hq, R].
     """
-    X_rows, X_keys, Wqkv, Wo = _widen(X_rows), _widen(X_keys), _widen(Wqkv), _widen(Wo)
+    X_rows, Wqkv, Wo = _widen(X_rows), _widen(Wqkv), _widen(Wo)
     scale = default_scale(Dh) if scale is None else scale
     rows = np.asarray(rows, dtype=np.int64)
     key_index = np.asarray(key_index, dtype=np.int64)
     Wq, Wk, Wv = split_wqkv(Wqkv, Hq, Hkv, Dh)
     Q = heads(X_rows @ Wq.T, Hq, Dh)
-    K = heads(X_keys @ Wk.T, Hkv, Dh)
-    V = heads(X_keys @ Wv.T, Hkv, Dh)
+    K, V = project_kv(X_keys, Wk, Wv, Hkv, Dh)
     g = Hq // Hkv
     O = np.zeros((Hq, rows.size, Dh))
     LSE = np.full((Hq, rows.size), NEG_INF)
@@ -254,6 +267,55 @@ def layer_backward(X, Wqkv, Wo, seg, dY, Hq, Hkv, Dh, causal=True, scale=None, r
     if return_all:
         return dX, dWqkv, dWo, dict(dQ=dQ, dK=dK, dV=dV, dO=dO, O=O)
     return dX, dWqkv, dWo
+
+
+def layer_backward_rows(X, Wqkv, Wo, seg, dY_rows, rows, Hq, Hkv, Dh, causal=True, scale=None):
+    """layer_backward for an upstream gradient dY that is zero on every row except `rows`
+    (sorted, distinct), where it equals dY_rows [R, d].  The formulas are those of
+    layer_backward; the rows of zero dY contribute exact zeros to every sum (dO, D, dS and P^T dO
+    vanish there), so they are left out:
+    dO_h[i] = (dY Wo)_h[i] and O_h[i] for i in rows only; dWo = dY_rows^T [O_0 ... O_{Hq-1}](rows);
+    for i in rows: D_i = dO_h[i] . O_h[i], dP_ij = dO_h[i] . V_kv[j], dS_ij = P_ij (dP_ij - D_i),
+    dQ_h[i] = scale sum_j dS_ij K_kv[j]; dK_kv[j] = scale sum_h sum_{i in rows} dS_ij Q_h[i],
+    dV_kv[j] = sum_h sum_{i in rows} P_ij dO_h[i]; dQKV = [dQ | dK | dV] (dQ zero off `rows`);
+    dX = dQKV Wqkv; dWqkv = dQKV^T X.  X [S, d] is needed whole (every key and dWqkv).
+    Returns dX [S, d], dWqkv, dWo (float64)."""
+    X, Wqkv, Wo, dY_rows = _widen(X), _widen(Wqkv), _widen(Wo), _widen(dY_rows)
+    scale = default_scale(Dh) if scale is None else scale
+    rows = np.asarray(rows, dtype=np.int64)
+    S = X.shape[0]
+    g = Hq // Hkv
+    Wq, Wk, Wv = split_wqkv(Wqkv, Hq, Hkv, Dh)
+    Qr = heads(X[rows] @ Wq.T, Hq, Dh)
+    K = heads(X @ Wk.T, Hkv, Dh)
+    V = heads(X @ Wv.T, Hkv, Dh)
+    vis = visibility(seg, rows, np.arange(S), causal)
+    any_vis = vis.any(axis=1)
+    dOr = heads(dY_rows @ Wo, Hq, Dh)
+    Or = np.zeros((Hq, rows.size, Dh))
+    dQr = np.zeros((Hq, rows.size, Dh))
+    dK = np.zeros_like(K)
+    dV = np.zeros_like(V)
+    for h in range(Hq):
+        kv = h // g
+        s = np.where(vis, scale * (Qr[h] @ K[kv].T), NEG_INF)
+        m = np.where(any_vis, s.max(axis=1), 0.0)
+        e = np.where(vis, np.exp(s - m[:, None]), 0.0)
+        l = e.sum(axis=1)
+        P = np.divide(e, l[:, None], out=np.zeros_like(e), where=l[:, None] > 0)
+        Or[h] = P @ V[kv]
+        D = (dOr[h] * Or[h]).sum(axis=1)
+        dP = dOr[h] @ V[kv].T
+        dS = P * (dP - D[:, None])
+        dQr[h] = scale * (dS @ K[kv])
+        dK[kv] += scale * (dS.T @ Qr[h])
+        dV[kv] += P.T @ dOr[h]
+    dWo = dY_rows.T @ unheads(Or)
+    dQKV = np.zeros((S, (Hq + 2 * Hkv) * Dh))
+    dQKV[rows, : Hq * Dh] = unheads(dQr)
+    dQKV[:, Hq * Dh: (Hq + Hkv) * Dh] = unheads(dK)
+    dQKV[:, (Hq + Hkv) * Dh:] = unheads(dV)
+    return dQKV @ Wqkv, dQKV.T @ X, dWo
 
 
 # ----------------------------------------------------------------------------------------------

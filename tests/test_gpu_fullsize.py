@@ -105,24 +105,66 @@ def test_full_size_layer(key, hpc, prefix):
     assert rel_fro(to_f64(dWo), dWo_ref) <= GRAD_REL_FRO, rel_fro(to_f64(dWo), dWo_ref)
 
 
+def test_full_size_tail_window_backward():
+    """dY non-zero on the last 128 rows only: every key of the 32K-token layer then gets a
+    gradient, so dK and dV are checked for all 256 key tiles (each accumulating over the query
+    tiles of all four heads of its group) and dX on every row, against the oracle's backward
+    restricted to those rows (the zero rows of dY contribute exact zeros)."""
+    w = ui.workload("llama8b_32k")
+    S, d, Hq, Hkv, Dh, hpc, n = w.S, w.d, w.Hq, w.Hkv, w.Dh, 8, 128
+    X = dev_fill((S, d), ui.TID_X, 1.0)
+    W = dev_fill(((Hq + 2 * Hkv) * Dh, d), ui.TID_WQKV, ui.W_STD)
+    Wo = dev_fill((d, Hq * Dh), ui.TID_WO, ui.W_STD)
+    dY = torch.zeros((S, d), dtype=torch.bfloat16, device="cuda")
+    ui.fill_device_bf16(dY[S - n:].data_ptr(), n * d, ui.TID_DY, 1.0, first=(S - n) * d)
+    layer = up.Layer(up.make_desc(S, d, Hq, Hkv, Dh, hpc, w.causal))
+    Y, lse = layer.forward(X, W, Wo, None)
+    dX, dW, dWo = layer.backward(X, W, Wo, None, dY, lse)
+    torch.cuda.synchronize()
+    assert up.device_status(layer.ws_fwd) == 0 and up.device_status(layer.ws_bwd) == 0
+    rows = np.arange(S - n, S)
+    Xh = ui.normal_bf16(S * d, ui.TID_X).reshape(S, d)
+    Wh = ui.normal_bf16((Hq + 2 * Hkv) * Dh * d, ui.TID_WQKV, ui.W_STD).reshape(-1, d)
+    Woh = ui.normal_bf16(d * Hq * Dh, ui.TID_WO, ui.W_STD).reshape(d, -1)
+    dYr = ui.normal_bf16(n * d, ui.TID_DY, first=(S - n) * d).reshape(n, d)
+    dX_ref, dW_ref, dWo_ref = orc.layer_backward_rows(Xh, Wh, Woh, None, dYr, rows, Hq, Hkv, Dh, w.causal)
+    dXg = to_f64(dX)
+    assert np.all(np.abs(dX_ref).sum(axis=1) > 0)      # every row receives a gradient
+    assert rel_fro(dXg, dX_ref) <= GRAD_REL_FRO, rel_fro(dXg, dX_ref)
+    # the rows of the first and of the last key tile separately (longest and shortest dK/dV loops)
+    for a in (0, S - 128):
+        assert rel_fro(dXg[a: a + 128], dX_ref[a: a + 128]) <= GRAD_REL_FRO, (a, rel_fro(dXg[a: a + 128], dX_ref[a: a + 128]))
+    assert rel_fro(to_f64(dW), dW_ref) <= GRAD_REL_FRO, rel_fro(to_f64(dW), dW_ref)
+    assert rel_fro(to_f64(dWo), dWo_ref) <= GRAD_REL_FRO, rel_fro(to_f64(dWo), dWo_ref)
+
+
 def test_full_size_1m_share():
     """The 1M-token share (4 query heads, 1 KV head, one chunk as benchmarked).  The oracle checks
-    rows of the first 4096 tokens (every key they see); every later row is checked through
-    properties that hold at any size: causality makes the first T rows of the 1M-token layer equal
-    to a T-token layer on the same inputs (checked against a separate 4096-token run of the
-    library), all outputs are finite, and with dY zero past the first P rows every gradient equals
-    the oracle's on the first P tokens and dX rows >= P are exactly zero."""
+    sampled rows across the whole sequence (first, tile-boundary, middle, random and last rows;
+    K and V of all 2^20 keys projected in float64 block by block); causality makes the first T
+    rows of the 1M-token layer equal to a T-token layer on the same inputs (checked against a
+    separate 4096-token run of the library); all outputs are finite; and with dY zero past the
+    first P rows every gradient equals the oracle's on the first P tokens and dX rows >= P are
+    exactly zero."""
     w = ui.workload("ulysses_1m")
+    S = w.S
     hpc, prefix, T = 4, 1024, 4096
     seg, Y, lse, dX, dW, dWo = run_layer(w, hpc, prefix)
     for t in (Y, lse, dX, dW, dWo):
         assert bool(torch.isfinite(t.float()).all())
-    assert int(torch.count_nonzero(dX[prefix:])) == 0
-    # oracle on sampled rows of the first T tokens
-    rows = np.array([0, 1, 127, 128, 129, 1000, 2047, 2048, T - 129, T - 1])
-    key_index = np.arange(0, T)
-    Xk, W, Wo, dYp = host_inputs(w, key_index, prefix)
+    for a in range(prefix, S, 1 << 18):     # in slices: a whole-tensor count would need ~8 GB
+        assert not bool((dX[a: a + (1 << 18)] != 0).any())
+    # oracle on sampled rows of the whole sequence
+    rng = np.random.default_rng(1234)
+    rows = np.unique(np.concatenate([
+        [0, 1, 127, 128, 129, 1000, 2047, 2048, T - 129, T - 1, S // 2 - 1, S // 2, S // 2 + 1],
+        [S - 257, S - 256, S - 129, S - 128, S - 127, S - 2, S - 1],
+        rng.integers(0, S, size=12)]))
+    key_index = np.arange(0, S)
+    Xk = ui.normal_bf16(S * w.d, ui.TID_X).reshape(S, w.d)
+    _, W, Wo, dYp = host_inputs(w, np.arange(1), prefix)
     Y_ref, L_ref = orc.layer_forward_rows(Xk[rows], Xk, key_index, rows, W, Wo, None, w.Hq, w.Hkv, w.Dh, w.causal)
+    del Xk
     y = to_f64(Y[torch.from_numpy(rows).cuda()])
     assert max_abs_bf16_out(y, Y_ref) <= FULL_OUT_MAX_ABS, max_abs_bf16_out(y, Y_ref)
     assert rel_fro(y, Y_ref) <= OUT_REL_FRO, rel_fro(y, Y_ref)

@@ -253,6 +253,34 @@ def test_rows_helper_matches_full_forward():
     np.testing.assert_allclose(Lr, LSE[:, rows], rtol=1e-12, atol=1e-13)
 
 
+@pytest.mark.parametrize("causal,segs,Hq,Hkv", [(True, None, 4, 2), (True, [20, 1, 27], 4, 1),
+                                               (False, [30, 18], 2, 2)])
+def test_rows_backward_matches_torch_autograd(causal, segs, Hq, Hkv):
+    """dY non-zero on a few rows only (a tail window, a segment start, a single row)."""
+    S, d, Dh = 48, 16, 8
+    X, Wqkv, Wo, dY = rand_layer(S, d, Hq, Hkv, Dh, seed=21)
+    seg = None if segs is None else ui.segments_from_lengths(segs)
+    scale = orc.default_scale(Dh)
+    rows = np.array([0, 20, 21, 33, 40, 41, 42, 43, 44, 45, 46, 47])
+    dYz = np.zeros_like(dY)
+    dYz[rows] = dY[rows]
+    yt, (Xt, Wt, Wot) = torch_layer(X, Wqkv, Wo, seg, Hq, Hkv, Dh, causal, scale)
+    yt.backward(torch.tensor(dYz))
+    dX, dW, dWo = orc.layer_backward_rows(X, Wqkv, Wo, seg, dY[rows], rows, Hq, Hkv, Dh, causal, scale)
+    np.testing.assert_allclose(dX, Xt.grad.numpy(), rtol=1e-10, atol=1e-11)
+    np.testing.assert_allclose(dW, Wt.grad.numpy(), rtol=1e-10, atol=1e-11)
+    np.testing.assert_allclose(dWo, Wot.grad.numpy(), rtol=1e-10, atol=1e-11)
+
+
+def test_project_kv_blocks_match_one_product():
+    S, d, Hq, Hkv, Dh = 300, 16, 4, 2, 8
+    X, Wqkv, _, _ = rand_layer(S, d, Hq, Hkv, Dh, seed=5)
+    _, Wk, Wv = orc.split_wqkv(Wqkv, Hq, Hkv, Dh)
+    K, V = orc.project_kv(X, Wk, Wv, Hkv, Dh, row_block=64)
+    np.testing.assert_allclose(K, (X @ Wk.T).reshape(S, Hkv, Dh).transpose(1, 0, 2), rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(V, (X @ Wv.T).reshape(S, Hkv, Dh).transpose(1, 0, 2), rtol=1e-13, atol=1e-14)
+
+
 # ------------------------------------------------------------------------------------------
 # 6. tile-skip table
 # ------------------------------------------------------------------------------------------
