@@ -79,7 +79,8 @@ const char* upipe_attn_last_error_string(void);
  * Q/O/dO/dQ buffers and the resident K/V of one KV group), not with n_q_heads. */
 upipe_status_t upipe_attn_workspace_size(const upipe_attn_desc_t* desc, int pass, size_t* bytes);
 
-/* Bytes of the tile-skip table for seq_len S: 32-byte header + 2 * ceil(S/128) * 16. */
+/* Bytes of the tile-skip table for seq_len S, with n = ceil(S/128):
+ * 32-byte header + 2 * n * 16 + 4 * (ceil(n/2) + n), rounded up to a multiple of 16. */
 upipe_status_t upipe_attn_tile_table_size(const upipe_attn_desc_t* desc, size_t* bytes);
 
 /* Tile-skip table (Splash-style skipping of fully masked blocks, MaxText article).
@@ -91,7 +92,13 @@ upipe_status_t upipe_attn_tile_table_size(const upipe_attn_desc_t* desc, size_t*
  *             UPIPE_ERR_SEGMENTS_NOT_CONTIGUOUS), int32 n_tiles, int64 reserved
  *   q-major : int32[n_tiles][4] {kv_begin, kv_full_begin, kv_full_end, kv_end}
  *   kv-major: int32[n_tiles][4] {q_begin, q_full_begin, q_full_end, q_end}
+ *   q-order : int32[ceil(n_tiles/2)] query-tile pairs p (tiles 2p, 2p + 1) by non-increasing
+ *             number of non-empty tiles in their rows, ties later pair first
+ *   kv-order: int32[n_tiles] key tiles by non-increasing number of non-empty tiles in their
+ *             rows, ties earlier tile first
  * (half-open ranges of tile indices; a row with no full tile has full_begin = full_end = end).
+ * The two orders are the attention kernels' dispatch orders (most work first); they do not change
+ * any result.
  * seg: device int32[S] or NULL (one segment).  table: device, table_bytes from
  * upipe_attn_tile_table_size.  Only desc->seq_len and desc->causal are read. */
 upipe_status_t upipe_attn_build_tile_table(const upipe_attn_desc_t* desc, const int32_t* seg, void* table,

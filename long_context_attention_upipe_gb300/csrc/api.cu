@@ -235,6 +235,8 @@ AttnArgs attn_args(const Plan& p, int c, void* ws, const int32_t* seg, float* ls
   a.seg = seg;
   a.q_rows = table_q_rows(at<char>(ws, p.table));
   a.kv_rows = table_kv_rows(at<char>(ws, p.table), p.S);
+  a.q_order = table_q_order(at<char>(ws, p.table), p.S);
+  a.kv_order = table_kv_order(at<char>(ws, p.table), p.S);
   a.S = p.S;
   a.nh = p.hpc;
   a.nkv = p.kvc;
@@ -451,6 +453,8 @@ static AttnArgs core_args(const upipe_attn_desc_t* desc, const uint16_t* q, cons
   a.seg = seg;
   a.q_rows = table_q_rows(table);
   a.kv_rows = table_kv_rows(table, desc->seq_len);
+  a.q_order = table_q_order(table, desc->seq_len);
+  a.kv_order = table_kv_order(table, desc->seq_len);
   a.S = desc->seq_len;
   a.nh = desc->n_q_heads;
   a.nkv = desc->n_kv_heads;

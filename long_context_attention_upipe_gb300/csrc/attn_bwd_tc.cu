@@ -146,7 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dq_tc(const __grid_con
   const int64_t S = a.S;
   const int nt = (int)ceil_div(S, kTile);
   const int64_t sp = (int64_t)nt * kTile;
-  const int pair = gridDim.y - 1 - blockIdx.y;  // longest query tiles first, across all heads
+  const int pair = a.q_order[blockIdx.y];  // most work first (table dispatch order), across all heads
   const int h = blockIdx.x;
   const int kvh = h / a.g;
   const int qt0 = 2 * pair, qt1 = 2 * pair + 1;
@@ -418,9 +418,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
   const int64_t S = a.S;
   const int nt = (int)ceil_div(S, kTile);
   const int64_t sp = (int64_t)nt * kTile;
-  // grid (KV heads, key tiles) with the head fastest: the longest key tiles (small j has the most
-  // query tiles under causality) of every head are dispatched first
-  const int jt = blockIdx.y;
+  // grid (KV heads, key tiles) with the head fastest, the key tiles in the table's dispatch order:
+  // the key tiles seen by the most query tiles (under causality the first ones of each segment)
+  // of every head are dispatched first
+  const int jt = a.kv_order[blockIdx.y];
   const int kvh = blockIdx.x;
   const int4 tr = a.kv_rows[jt];  // query tiles {begin, full_begin, full_end, end}
   const int h_first = kvh * a.g;

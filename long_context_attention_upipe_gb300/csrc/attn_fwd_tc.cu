@@ -75,9 +75,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t S = a.S;
   const int nt = (int)ceil_div(S, kTile);
-  // grid (heads, query-tile pairs) with the head fastest, so the CTAs are dispatched longest
-  // query tiles first across all heads (a late long CTA would leave the others idle at the end)
-  const int pair = gridDim.y - 1 - blockIdx.y;
+  // grid (heads, query-tile pairs) with the head fastest, the pairs in the table's dispatch order,
+  // so the CTAs are dispatched most work first across all heads (a late long CTA would leave the
+  // others idle at the end); with packed segments the work depends on the position in the segment
+  const int pair = a.q_order[blockIdx.y];
   const int h = blockIdx.x;
   const int kvh = h / a.g;
   const int qt0 = 2 * pair, qt1 = 2 * pair + 1;

@@ -22,6 +22,15 @@ inline const int4* table_q_rows(const void* table) {
 inline const int4* table_kv_rows(const void* table, int64_t S) {
   return table_q_rows(table) + ceil_div(S, kTile);
 }
+// Dispatch orders: query-tile pairs (2p, 2p + 1) and key tiles, each by non-increasing number of
+// non-empty tiles (the work of the CTA that takes it), ties by the position the kernels used before
+// (later pairs first, earlier key tiles first).
+inline const int32_t* table_q_order(const void* table, int64_t S) {
+  return reinterpret_cast<const int32_t*>(table_kv_rows(table, S) + ceil_div(S, kTile));
+}
+inline const int32_t* table_kv_order(const void* table, int64_t S) {
+  return table_q_order(table, S) + ceil_div(ceil_div(S, kTile), 2);
+}
 
 // ---------------------------------------------------------------- projection GEMMs
 // Logical operands: A is [M, K], B is [N, K]; C[M, N] = A * B^T.
@@ -86,6 +95,8 @@ struct AttnArgs {
   const int32_t* seg;
   const int4* q_rows;   // q-major skip table
   const int4* kv_rows;  // kv-major skip table
+  const int32_t* q_order;   // query-tile pairs, most work first
+  const int32_t* kv_order;  // key tiles, most work first
   int64_t S;
   int nh;           // query heads of the launch
   int nkv;          // KV heads of the launch

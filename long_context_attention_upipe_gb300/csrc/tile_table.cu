@@ -143,9 +143,52 @@ __global__ void k_kv_rows(SegView sv, int causal, int64_t nt, int4* __restrict__
   rows[j] = make_int4(b, fb, fe, e);
 }
 
+// Dispatch orders by rank: entry x goes to position #{y : work(y) > work(x)} + #{y : work(y) ==
+// work(x), y before x in the tie order}, a permutation.  Blocks [0, nbq) rank the query-tile pairs
+// (ties: later pair first), the rest the key tiles (ties: earlier tile first).  Each block stages
+// the works 256 at a time in shared memory.
+__global__ void k_orders(const int4* __restrict__ q_rows, const int4* __restrict__ kv_rows, int64_t nt, int nbq,
+                         int32_t* __restrict__ q_order, int32_t* __restrict__ kv_order) {
+  const bool qside = (int)blockIdx.x < nbq;
+  const int64_t n = qside ? (nt + 1) / 2 : nt;
+  const int64_t x = (int64_t)(qside ? blockIdx.x : blockIdx.x - nbq) * blockDim.x + threadIdx.x;
+  auto work = [&](int64_t y) -> int32_t {
+    if (qside) {
+      const int4 a = q_rows[2 * y];
+      int32_t w = a.w - a.x;
+      if (2 * y + 1 < nt) {
+        const int4 b = q_rows[2 * y + 1];
+        w += b.w - b.x;
+      }
+      return w;
+    }
+    const int4 a = kv_rows[y];
+    return a.w - a.x;
+  };
+  const int32_t wx = x < n ? work(x) : 0;
+  __shared__ int32_t ws[256];
+  int64_t rank = 0;
+  for (int64_t base = 0; base < n; base += 256) {
+    __syncthreads();
+    if (base + threadIdx.x < n) ws[threadIdx.x] = work(base + threadIdx.x);
+    __syncthreads();
+    const int cnt = (int)min((int64_t)256, n - base);
+    for (int t = 0; t < cnt; ++t) {
+      const int64_t y = base + t;
+      const int32_t wy = ws[t];
+      rank += (wy > wx) || (wy == wx && (qside ? y > x : y < x));
+    }
+  }
+  if (x < n) (qside ? q_order : kv_order)[rank] = (int32_t)x;
+}
+
 }  // namespace
 
-size_t tile_table_bytes(int64_t S) { return sizeof(TableHeader) + 2 * (size_t)ceil_div(S, kTile) * 16; }
+size_t tile_table_bytes(int64_t S) {
+  const size_t nt = (size_t)ceil_div(S, kTile);
+  const size_t bytes = sizeof(TableHeader) + 2 * nt * 16 + 4 * ((nt + 1) / 2 + nt);
+  return (bytes + 15) & ~(size_t)15;
+}
 
 cudaError_t launch_tile_table(int64_t S, int causal, const int32_t* seg, void* table, cudaStream_t st) {
   const int64_t nt = ceil_div(S, kTile);
@@ -164,6 +207,10 @@ cudaError_t launch_tile_table(int64_t S, int causal, const int32_t* seg, void* t
   k_q_rows<<<tb, 256, 0, st>>>(sv, causal, nt, q_rows, h);
   note_launch();
   k_kv_rows<<<tb, 256, 0, st>>>(sv, causal, nt, kv_rows);
+  note_launch();
+  const int nbq = (int)ceil_div((nt + 1) / 2, 256), nbk = (int)ceil_div(nt, 256);
+  k_orders<<<nbq + nbk, 256, 0, st>>>(q_rows, kv_rows, nt, nbq, const_cast<int32_t*>(table_q_order(table, S)),
+                                      const_cast<int32_t*>(table_kv_order(table, S)));
   note_launch();
   return cudaGetLastError();
 }

@@ -38,6 +38,29 @@ def gpu_table(S, seg_np, causal):
     return q_rows, kv_rows, counts, err, table
 
 
+def gpu_orders(table, S):
+    """The table's dispatch orders: query-tile pairs, then key tiles (int32, after the ranges)."""
+    t = table.cpu().numpy()
+    nt = -(-S // 128)
+    np_ = (nt + 1) // 2
+    o = 32 + 32 * nt
+    return t[o:o + 4 * np_].view(np.int32), t[o + 4 * np_:o + 4 * np_ + 4 * nt].view(np.int32)
+
+
+def expected_orders(q_rows, kv_rows):
+    """Pairs (2p, 2p + 1) by non-increasing number of non-empty key tiles, ties later pair first;
+    key tiles by non-increasing number of non-empty query tiles, ties earlier tile first."""
+    nt = len(q_rows)
+    wq = (q_rows[:, 3] - q_rows[:, 0]).astype(np.int64)
+    wq = np.append(wq, 0) if nt % 2 else wq
+    wp = wq[0::2] + wq[1::2]
+    pairs = np.arange(len(wp))
+    q_order = np.lexsort((-pairs, -wp))
+    wk = (kv_rows[:, 3] - kv_rows[:, 0]).astype(np.int64)
+    kv_order = np.lexsort((np.arange(nt), -wk))
+    return q_order.astype(np.int32), kv_order.astype(np.int32)
+
+
 def random_segments(S, rng, max_segs=8):
     k = int(rng.integers(1, max_segs + 1))
     if S < 2 or k == 1:
@@ -57,30 +80,40 @@ def test_tile_table_bit_exact(S, causal):
     for trial in range(3):
         seg = None if trial == 0 else random_segments(S, rng, 8 if trial == 1 else 40)
         want_q, want_kv, want_tot = orc.tile_table(S, seg, causal)
-        q, kv, counts, err, _ = gpu_table(S, seg, causal)
+        q, kv, counts, err, table = gpu_table(S, seg, causal)
         assert err == 0
         np.testing.assert_array_equal(q, want_q)
         np.testing.assert_array_equal(kv, want_kv)
         np.testing.assert_array_equal(counts, want_tot)
+        for got, want in zip(gpu_orders(table, S), expected_orders(want_q, want_kv)):
+            np.testing.assert_array_equal(got, want)
 
 
 def test_tile_table_packed_131k():
     w = ui.workload("packed_131k")
     seg = w.segments()
     want_q, want_kv, want_tot = orc.tile_table(w.S, seg, True)
-    q, kv, counts, err, _ = gpu_table(w.S, seg, True)
+    q, kv, counts, err, table = gpu_table(w.S, seg, True)
     assert err == 0
     np.testing.assert_array_equal(q, want_q)
     np.testing.assert_array_equal(kv, want_kv)
     np.testing.assert_array_equal(counts, want_tot)
+    for got, want in zip(gpu_orders(table, w.S), expected_orders(want_q, want_kv)):
+        np.testing.assert_array_equal(got, want)
 
 
 def test_tile_table_5m_sampled_and_closed_form():
     S = 5_000_000
     n = -(-S // 128)
-    q, kv, counts, err, _ = gpu_table(S, None, True)
+    q, kv, counts, err, table = gpu_table(S, None, True)
     assert err == 0
     assert counts.tolist() == [n, n * (n - 1) // 2]  # diagonal partial, the rest of the triangle full
+    # one causal segment: query tile i sees i + 1 key tiles, key tile j is seen by n - j query tiles
+    i = np.arange(n)
+    closed_q = np.stack([0 * i, 0 * i, i, i + 1], 1)
+    closed_kv = np.stack([i, i, 0 * i + n, 0 * i + n], 1)
+    for got, want in zip(gpu_orders(table, S), expected_orders(closed_q, closed_kv)):
+        np.testing.assert_array_equal(got, want)
     sel = np.array([0, 1, 2, 777, n // 2, n - 2, n - 1])
     want_q, want_kv, _ = orc.tile_table(S, None, True, q_tiles=sel, kv_tiles=sel)
     np.testing.assert_array_equal(q[sel], want_q)
