@@ -510,9 +510,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
         issue_st(g);
         for (int n = g; ok && n < n_items; n += 2) {
           const uint32_t ph = (n >> 1) & 1;
-          ok = tc::mbar_wait(&p_full[g], ph, abort_flag, a.err);
-          if (ok) ok = tc::mbar_wait(&o_full[g], (n / NO) & 1, abort_flag, a.err);
+          // the waits that are normally already satisfied come first, so that the issue of dV
+          // follows the element-wise group's P^T arrival as closely as possible
+          ok = tc::mbar_wait(&o_full[g], (n / NO) & 1, abort_flag, a.err);
           if (ok && n > 0) ok = tc::mbar_wait(dv_tok, (n - 1) & 1, abort_flag, a.err);  // dV(n-1) issued
+          if (ok) ok = tc::mbar_wait(&p_full[g], ph, abort_flag, a.err);
           if (!ok) break;
           tc::fence_after_sync();
           mma_acc<DH>(tmem + L::DV_COL, r_tm, dOmn, n > 0);  // dV += P^T dO
@@ -521,8 +523,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
           mma_nt<DH>(r_tm, dV, dO);  // dP^T = V dO^T
           tc::mma_commit(&dp_full[g]);
           tc::mma_commit(&o_empty[g]);
-          ok = tc::mbar_wait(&ds_full[g], ph, abort_flag, a.err);
-          if (ok && n > 0) ok = tc::mbar_wait(dk_tok, (n - 1) & 1, abort_flag, a.err);  // dK(n-1) issued
+          if (n > 0) ok = tc::mbar_wait(dk_tok, (n - 1) & 1, abort_flag, a.err);  // dK(n-1) issued
+          if (ok) ok = tc::mbar_wait(&ds_full[g], ph, abort_flag, a.err);
           if (!ok) break;
           tc::fence_after_sync();
           mma_acc<DH>(tmem + L::DK_COL, r_tm, tc::sdesc_add(dQmn, (n % NQ) * L::TB), n > 0);  // dK += dS^T Q
