@@ -86,21 +86,31 @@ __device__ __forceinline__ void mma_acc(uint32_t d, uint32_t a_tmem, uint64_t bd
 template <typename DFn>
 __device__ __forceinline__ void ds_pass_f32(uint32_t r_addr, const uint32_t (&pa)[64], const uint32_t (&pb)[64],
                                             DFn ndval) {
+  // chunk c + 1 loads while chunk c is computed and stored: its columns [32c + 32, 32c + 64) are
+  // disjoint from the store's [16c, 16c + 16)
+  uint32_t v[2][32];
+  tc::tmem_ld32(r_addr, v[0]);
+  tc::tmem_ld_wait();
+#pragma unroll
+  for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(v[0][i]));
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
-    uint32_t v[32], o[16];
-    tc::tmem_ld32(r_addr + 32 * c, v);
-    tc::tmem_ld_wait();
-#pragma unroll
-    for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(v[i]));
+    uint32_t o[16];
+    if (c + 1 < 4) tc::tmem_ld32(r_addr + 32 * (c + 1), v[(c + 1) & 1]);
     const uint32_t* pp = c < 2 ? &pa[32 * c] : &pb[32 * (c - 2)];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      const float2 d = __fadd2_rn(make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])), ndval(32 * c + 2 * i));
+      const float2 d = __fadd2_rn(make_float2(__uint_as_float(v[c & 1][2 * i]), __uint_as_float(v[c & 1][2 * i + 1])),
+                                  ndval(32 * c + 2 * i));
       const float2 r = __fmul2_rn(make_float2(__uint_as_float(pp[2 * i]), __uint_as_float(pp[2 * i + 1])), d);
       o[i] = tc::pack_bf16x2(r.x, r.y);
     }
     tc::tmem_st16(r_addr + 16 * c, o);
+    if (c + 1 < 4) {
+      tc::tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(v[(c + 1) & 1][i]));
+    }
   }
   tc::tmem_st_wait();
 }
