@@ -42,7 +42,7 @@ def test_device_generator_matches_host_bit_for_bit():
         np.testing.assert_array_equal(got, ui.normal_bf16(n, tid, std, first=first))
 
 
-def run_layer(w, hpc, prefix):
+def run_layer(w, hpc, prefix, accum=0):
     S, d, Hq, Hkv, Dh = w.S, w.d, w.Hq, w.Hkv, w.Dh
     X = dev_fill((S, d), ui.TID_X, 1.0)
     W = dev_fill(((Hq + 2 * Hkv) * Dh, d), ui.TID_WQKV, ui.W_STD)
@@ -51,12 +51,21 @@ def run_layer(w, hpc, prefix):
     ui.fill_device_bf16(dY.data_ptr(), prefix * d, ui.TID_DY, 1.0)   # rows [0, prefix) only
     seg = w.segments()
     seg_t = torch.from_numpy(seg).cuda() if seg is not None else None
-    layer = up.Layer(up.make_desc(S, d, Hq, Hkv, Dh, hpc, w.causal))
+    layer = up.Layer(up.make_desc(S, d, Hq, Hkv, Dh, hpc, w.causal, accum))
     Y, lse = layer.forward(X, W, Wo, seg_t)
     dX, dW, dWo = layer.backward(X, W, Wo, seg_t, dY, lse)
     torch.cuda.synchronize()
     assert up.device_status(layer.ws_fwd) == 0 and up.device_status(layer.ws_bwd) == 0
     return seg, Y, lse, dX, dW, dWo
+
+
+def all_finite(t, rows=1 << 18):
+    """isfinite over row slices (a whole-tensor float copy of a 51 GB output would not fit)."""
+    return all(bool(torch.isfinite(t[a: a + rows].float()).all()) for a in range(0, t.shape[0], rows))
+
+
+def all_zero_from(t, start, rows=1 << 18):
+    return all(not bool((t[a: a + rows] != 0).any()) for a in range(start, t.shape[0], rows))
 
 
 def host_inputs(w, rows_needed, prefix):
@@ -179,6 +188,44 @@ def test_full_size_1m_share():
     assert max_abs(to_f64(Y[:T]), to_f64(Ys)) <= 1e-6 * max(1.0, float(Ys.float().abs().max()))
     assert max_abs(to_f64(lse[:, :T]), to_f64(lses)) <= 1e-6 * max(1.0, float(lses.abs().max()))
     # backward on the prefix
+    Xp = ui.normal_bf16_rows(np.arange(prefix), w.d, ui.TID_X)
+    dX_ref, dW_ref, dWo_ref = orc.layer_backward(Xp, W, Wo, None, dYp, w.Hq, w.Hkv, w.Dh, w.causal)
+    assert rel_fro(to_f64(dX[:prefix]), dX_ref) <= GRAD_REL_FRO, rel_fro(to_f64(dX[:prefix]), dX_ref)
+    assert rel_fro(to_f64(dW), dW_ref) <= GRAD_REL_FRO, rel_fro(to_f64(dW), dW_ref)
+    assert rel_fro(to_f64(dWo), dWo_ref) <= GRAD_REL_FRO, rel_fro(to_f64(dWo), dWo_ref)
+
+
+def test_full_size_5m_share():
+    """The 5M-token 32B-shaped share (8 query heads, 1 KV head, hidden 5120), two heads per chunk
+    with bf16 partial sums (fp32 sums would not fit beside the caller's 205 GB of X, Y, dY and dX).
+    Checked as the 1M share is, except that the oracle rows lie in the first 4096 tokens: a row near
+    the end would need the float64 projection of all five million keys.  Those rows against the
+    oracle; the first T rows against a separate T-token run with the same chunking (causality);
+    finite outputs; dX exactly zero past the first P rows, where dY is zero; every gradient against
+    the oracle on the first P tokens."""
+    w = ui.workload("share32b_5m")
+    hpc, prefix, T = 2, 1024, 4096
+    seg, Y, lse, dX, dW, dWo = run_layer(w, hpc, prefix, accum=1)
+    assert all_finite(Y) and all_finite(dX)
+    for t in (lse, dW, dWo):
+        assert bool(torch.isfinite(t.float()).all())
+    assert all_zero_from(dX, prefix)
+    rows = np.array([0, 1, 127, 128, 129, 1000, 2047, 2048, T - 129, T - 1])
+    key_index = np.arange(0, T)
+    Xk, W, Wo, dYp = host_inputs(w, key_index, prefix)
+    Y_ref, L_ref = orc.layer_forward_rows(Xk[rows], Xk, key_index, rows, W, Wo, None, w.Hq, w.Hkv, w.Dh, w.causal)
+    y = to_f64(Y[torch.from_numpy(rows).cuda()])
+    assert max_abs_bf16_out(y, Y_ref) <= FULL_OUT_MAX_ABS, max_abs_bf16_out(y, Y_ref)
+    assert rel_fro(y, Y_ref) <= OUT_REL_FRO, rel_fro(y, Y_ref)
+    lse_err = np.abs(to_f64(lse)[:, rows] - L_ref) / np.maximum(1.0, np.abs(L_ref))
+    assert lse_err.max() <= 1e-2, lse_err.max()
+    small = up.Layer(up.make_desc(T, w.d, w.Hq, w.Hkv, w.Dh, hpc, w.causal, 1))
+    Wd = dev_fill(((w.Hq + 2 * w.Hkv) * w.Dh, w.d), ui.TID_WQKV, ui.W_STD)
+    Wod = dev_fill((w.d, w.Hq * w.Dh), ui.TID_WO, ui.W_STD)
+    Ys, lses = small.forward(dev_fill((T, w.d), ui.TID_X, 1.0), Wd, Wod, None)
+    torch.cuda.synchronize()
+    assert max_abs(to_f64(Y[:T]), to_f64(Ys)) <= 1e-6 * max(1.0, float(Ys.float().abs().max()))
+    assert max_abs(to_f64(lse[:, :T]), to_f64(lses)) <= 1e-6 * max(1.0, float(lses.abs().max()))
     Xp = ui.normal_bf16_rows(np.arange(prefix), w.d, ui.TID_X)
     dX_ref, dW_ref, dWo_ref = orc.layer_backward(Xp, W, Wo, None, dYp, w.Hq, w.Hkv, w.Dh, w.causal)
     assert rel_fro(to_f64(dX[:prefix]), dX_ref) <= GRAD_REL_FRO, rel_fro(to_f64(dX[:prefix]), dX_ref)
