@@ -149,6 +149,23 @@ def oracle_sample(w, sample_tokens, repeats=1):
     return dt, sub.flops_fwd_bwd(), threads, S
 
 
+def max_over_ranks(ms: float, device) -> float:
+    """The job's time per step is its slowest replica's: MAX over the ranks of the process group
+    (any backend; a single process returns `ms`)."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(flops_per_step: float, world: int, ms_all: float) -> float:
+    """Whole-job TFLOP/s: every replica runs the full step, the job takes the slowest one's time."""
+    return flops_per_step * world / (ms_all * 1e-3) / 1e12
+
+
 def run_reference(args):
     """The reference arm: the oracle as it stands, timed on the host cores (rank 0 only)."""
     import upipe_inputs as ui
@@ -364,12 +381,8 @@ def main():
     launches = per_step * args.steps if graph is not None else up.launch_count() - launches_before
     clocks = sampler.stop()
     peak_gb = torch.cuda.max_memory_allocated(dev) / 1e9
-    ms_all = ms
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_all = float(t.item())
-    value = flops * world / (ms_all * 1e-3) / 1e12
+    ms_all = max_over_ranks(ms, dev)
+    value = job_value(flops, world, ms_all)
 
     result = {}
     if rank == 0:
