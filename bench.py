@@ -44,8 +44,11 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--sample-tokens", type=int, default=1024, help="oracle sample length (CPU legs)")
-    ap.add_argument("--kernel", default=None, choices=["fwd", "recompute", "dq", "dkdv"],
-                    help="time one attention kernel alone at the workload's chunk shapes (for profilers)")
+    ap.add_argument("--kernel", default=None, choices=["fwd", "recompute", "dq", "dkdv", "lse_merge", "ring"],
+                    help="time one attention kernel alone at the workload's chunk shapes (for profilers); "
+                         "lse_merge: the ring merge of one block into fp32 accumulators; ring: the chunk's causal "
+                         "attention as the blocks of a zigzag ring of --ring-p devices, run on this GPU")
+    ap.add_argument("--ring-p", type=int, default=4)
     ap.add_argument("--reps", type=int, default=3)
     return ap.parse_args()
 
@@ -345,6 +348,35 @@ def main():
             "dkdv": lambda: up.core_bwd_dkdv(cdesc, q, k, v, do, lse_c, Dt, seg_t, table, dk, dv, stream),
         }
 
+    if args.kernel in ("lse_merge", "ring"):
+        if seg_t is not None:
+            raise SystemExit("the ring share runs unpacked sequences only")
+        g = Hq // Hkv
+        kvc = max(1, args.hpc // g)
+        q = fill((args.hpc, S, Dh), 10, 1.0)
+        k = fill((kvc, S, Dh), 11, 1.0)
+        v = fill((kvc, S, Dh), 12, 1.0)
+        if args.kernel == "lse_merge":
+            o_b = fill((args.hpc, S, Dh), 13, 1.0)
+            l_b = torch.zeros(args.hpc, S, dtype=torch.float32, device=dev)
+            o_acc = torch.zeros(args.hpc, S, Dh, dtype=torch.float32, device=dev)
+            l_acc = torch.zeros(args.hpc, S, dtype=torch.float32, device=dev)
+            f = lambda: up.lse_merge(o_b, l_b, o_acc, l_acc, None, stream)
+            f()
+            ms_k = time_steps(f, args.reps)
+            rows = args.hpc * S
+            nbytes = rows * Dh * (2 + 4 + 4) + rows * 4 * 3   # O_b, O_acc read + write; lse_b, lse_acc read + write
+            gbs = nbytes / (ms_k * 1e-3) / 1e9
+            print(json.dumps({"kernel": "lse_merge", "workload": w.name, "heads": args.hpc, "ms": ms_k,
+                              "bytes": nbytes, "gbs": gbs, "hbm_frac": gbs / peaks["hbm_gbs"]}))
+            return
+        f = lambda: up.ring_attention_share(q, k, v, args.ring_p, 0.0, stream)
+        f()
+        ms_k = time_steps(f, args.reps)
+        tf = attn_kernel_flops(w, args.hpc, "fwd") / (ms_k * 1e-3) / 1e12
+        print(json.dumps({"kernel": "ring", "ring_p": args.ring_p, "workload": w.name, "heads": args.hpc,
+                          "ms": ms_k, "tflops": tf}))
+        return
     if args.kernel:
         f = chunk_kernels(args.hpc)[args.kernel]
         f()

@@ -184,6 +184,23 @@ upipe_status_t upipe_attn_core_bwd_dkdv(const upipe_attn_desc_t* desc, const uin
 upipe_status_t upipe_attn_gemm_nt(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda,
                                   const uint16_t* B, int64_t ldb, float* C, int64_t ldc, void* stream);
 
+/* Merge of block attention results: the single-GPU share of ring (P2P) context parallelism, where
+ * key/value blocks travel around a ring of devices and each device attends its query block to
+ * the visiting block (MaxText long-context article, table of context-parallel strategies, row
+ * "P2P (Ring)").  For `rows` query rows (e.g. n_heads * block length, head-major as
+ * upipe_attn_core_fwd writes them), with L the natural-log log-sum-exp of a row's scores:
+ *   L_acc <- log(e^{L_acc} + e^{L_b}),   O_acc <- (e^{L_acc,old} O_acc + e^{L_b} O_b) / e^{L_acc,new}
+ * which is attention over the union of the key sets seen so far and the block's.
+ *   O_b      device bf16 [rows][head_dim]: the block's output (upipe_attn_core_fwd `o`)
+ *   lse_b    device fp32 [rows]: the block's log-sum-exp (upipe_attn_core_fwd `lse`)
+ *   O_acc    device fp32 [rows][head_dim], updated in place; start from zeros
+ *   lse_acc  device fp32 [rows], updated in place; start from -inf
+ *   O_out    NULL, or device bf16 [rows][head_dim] that receives the merged O rounded to bf16
+ * A side whose L is -inf contributes nothing; a row with both -inf stays O = 0, L = -inf.
+ * head_dim 64 or 128; all pointers 16-byte aligned.  Stream-ordered, asynchronous. */
+upipe_status_t upipe_attn_lse_merge(int64_t rows, int32_t head_dim, const uint16_t* O_b, const float* lse_b,
+                                    float* O_acc, float* lse_acc, uint16_t* O_out, void* stream);
+
 /* Reads the device error word of a workspace (after fwd/bwd) or of a table (after
  * build_tile_table) into *code (a upipe_status_t value; UPIPE_OK when none).  Synchronises
  * `stream`.  `buf` is the workspace or the table. */

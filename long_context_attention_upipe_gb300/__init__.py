@@ -22,7 +22,7 @@ UPIPE_OK = 0
 EXPORTS = ["upipe_attn_status_string", "upipe_attn_last_error_string", "upipe_attn_workspace_size", "upipe_attn_tile_table_size",
            "upipe_attn_build_tile_table", "upipe_attn_fwd", "upipe_attn_bwd", "upipe_attn_core_fwd",
            "upipe_attn_core_recompute", "upipe_attn_core_bwd_dq", "upipe_attn_core_bwd_dkdv", "upipe_attn_gemm_nt",
-           "upipe_attn_device_status", "upipe_attn_fwd_no_alloc", "upipe_attn_launch_count"]
+           "upipe_attn_device_status", "upipe_attn_fwd_no_alloc", "upipe_attn_launch_count", "upipe_attn_lse_merge"]
 
 
 class Desc(ctypes.Structure):
@@ -70,6 +70,7 @@ def lib():
             "upipe_attn_device_status": ([P, ctypes.POINTER(ctypes.c_int32), P], ctypes.c_int),
             "upipe_attn_fwd_no_alloc": ([D, P, P, P, P, P, P, P], ctypes.c_int),
             "upipe_attn_launch_count": ([], ctypes.c_uint64),
+            "upipe_attn_lse_merge": ([I64, ctypes.c_int32, P, P, P, P, P, P], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -178,6 +179,88 @@ def gemm_nt(A, B, C, stream=None):
     N = B.shape[0]
     _check(lib().upipe_attn_gemm_nt(M, N, K, _bf16(A), A.stride(0), _bf16(B), B.stride(0), _ptr(C), C.stride(0),
                                     _stream(stream)), "gemm_nt")
+
+
+def lse_merge(O_b, lse_b, O_acc, lse_acc, O_out=None, stream=None):
+    """Fold a block's attention result (O_b bf16 [..., Dh], lse_b fp32 [...]) into the fp32
+    accumulator (O_acc, lse_acc) in place; O_out (bf16, optional) receives the merged O."""
+    Dh = O_b.shape[-1]
+    rows = lse_b.numel()
+    _check(lib().upipe_attn_lse_merge(rows, Dh, _bf16(O_b), _ptr(lse_b), _ptr(O_acc), _ptr(lse_acc),
+                                      _bf16(O_out) if O_out is not None else None, _stream(stream)), "lse_merge")
+
+
+# ------------------------------------------------------------------------------------------------
+# Ring (P2P) context parallelism, single-GPU share: the host schedule and a one-GPU run of it
+# ------------------------------------------------------------------------------------------------
+
+def zigzag_chunks(P: int):
+    """Causal load balancing for a ring of P devices: the sequence is cut into 2P equal chunks
+    and device r holds chunks r and 2P - 1 - r, so every device owns one early and one late chunk
+    and does the same number of block computations (the ring strategy needs explicit load
+    balancing because later positions look back over more keys)."""
+    return [(r, 2 * P - 1 - r) for r in range(P)]
+
+
+def ring_block_schedule(P: int):
+    """For each device r and ring step s (the key/value chunks of device (r - s) mod P visit r):
+    the blocks (query chunk, key chunk, "causal" | "full") that r computes; key chunks after the
+    query chunk are skipped."""
+    chunks = zigzag_chunks(P)
+    sched = []
+    for r in range(P):
+        steps = []
+        for s in range(P):
+            src = (r - s) % P
+            blocks = []
+            for qc in chunks[r]:
+                for kc in chunks[src]:
+                    if kc < qc:
+                        blocks.append((qc, kc, "full"))
+                    elif kc == qc:
+                        blocks.append((qc, kc, "causal"))
+            steps.append(blocks)
+        sched.append(steps)
+    return sched
+
+
+def ring_attention_share(q, k, v, P: int, softmax_scale: float = 0.0, stream=None):
+    """Causal attention of q [Hq, S, Dh] over k, v [Hkv, S, Dh] computed block by block as the P
+    devices of a zigzag ring would, each block with upipe_attn_core_fwd on contiguous chunk copies
+    and folded into per-chunk fp32 accumulators with upipe_attn_lse_merge, in ring-step order.
+    One GPU runs every device's blocks in turn (there is no exchange to make).  Returns O bf16
+    [Hq, S, Dh] and lse fp32 [Hq, S].  softmax_scale 0 means 1/sqrt(Dh)."""
+    Hq, S, Dh = q.shape
+    Hkv = k.shape[0]
+    n = 2 * P
+    if S % n:
+        raise ValueError("S must be a multiple of 2P")
+    C = S // n
+    descs = {kind: make_desc(C, 64, Hq, Hkv, Dh, Hq, kind == "causal", 0, softmax_scale) for kind in ("causal", "full")}
+    tables = {}
+    for kind, dsc in descs.items():
+        t = torch.empty(tile_table_bytes(dsc), dtype=torch.uint8, device=q.device)
+        build_tile_table(dsc, None, t, stream)
+        tables[kind] = t
+    # each chunk once as a dense [heads, C, Dh] block: a device holds its own query chunks, and the
+    # ring delivers the key/value chunks of the others in this form
+    qs, ks, vs = ([x[:, c * C:(c + 1) * C].contiguous() for c in range(n)] for x in (q, k, v))
+    o_acc = {c: torch.zeros(Hq, C, Dh, dtype=torch.float32, device=q.device) for c in range(n)}
+    l_acc = {c: torch.full((Hq, C), float("-inf"), dtype=torch.float32, device=q.device) for c in range(n)}
+    o_b = torch.empty(Hq, C, Dh, dtype=torch.bfloat16, device=q.device)
+    l_b = torch.empty(Hq, C, dtype=torch.float32, device=q.device)
+    o_out = {c: torch.empty(Hq, C, Dh, dtype=torch.bfloat16, device=q.device) for c in range(n)}
+    order = [blk for steps in ring_block_schedule(P) for blocks in steps for blk in blocks]
+    last = {qc: i for i, (qc, _, _) in enumerate(order)}   # the merge that also writes the bf16 output
+    for i, (qc, kc, kind) in enumerate(order):
+        core_fwd(descs[kind], qs[qc], ks[kc], vs[kc], None, tables[kind], o_b, l_b, stream)
+        lse_merge(o_b, l_b, o_acc[qc], l_acc[qc], o_out[qc] if last[qc] == i else None, stream)
+    O = torch.empty_like(q)
+    lse = torch.empty(Hq, S, dtype=torch.float32, device=q.device)
+    for c in range(n):  # placement only
+        O[:, c * C:(c + 1) * C] = o_out[c]
+        lse[:, c * C:(c + 1) * C] = l_acc[c]
+    return O, lse
 
 
 class Layer:

@@ -553,6 +553,16 @@ upipe_status_t upipe_attn_gemm_nt(int64_t M, int64_t N, int64_t K, const uint16_
   return cuda_status(launch_gemm_tc(g, 1, nullptr, (cudaStream_t)stream));
 }
 
+upipe_status_t upipe_attn_lse_merge(int64_t rows, int32_t head_dim, const uint16_t* O_b, const float* lse_b,
+                                    float* O_acc, float* lse_acc, uint16_t* O_out, void* stream) {
+  if (rows < 0 || !O_b || !lse_b || !O_acc || !lse_acc) return UPIPE_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return UPIPE_ERR_UNSUPPORTED;
+  if (!aligned16(O_b) || !aligned16(lse_b) || !aligned16(O_acc) || !aligned16(lse_acc) || (O_out && !aligned16(O_out)))
+    return UPIPE_ERR_ALIGNMENT;
+  return cuda_status(launch_lse_merge(rows, head_dim, reinterpret_cast<const bf16*>(O_b), lse_b, O_acc, lse_acc,
+                                      reinterpret_cast<bf16*>(O_out), (cudaStream_t)stream));
+}
+
 uint64_t upipe_attn_launch_count(void) { return upipe::g_launch_count.load(std::memory_order_relaxed); }
 
 upipe_status_t upipe_attn_device_status(const void* buf, int32_t* code, void* stream) {

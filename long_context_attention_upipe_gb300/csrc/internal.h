@@ -126,5 +126,7 @@ cudaError_t launch_attn_bwd_dkdv(const AttnBwdArgs& a, int head_dim, cudaStream_
 // ---------------------------------------------------------------- small kernels
 cudaError_t launch_f32_to_bf16(const float* in, bf16* out, int64_t n, float mul, cudaStream_t st);
 cudaError_t launch_zero(void* p, int64_t bytes, cudaStream_t st);
+cudaError_t launch_lse_merge(int64_t rows, int head_dim, const bf16* ob, const float* lb, float* oacc, float* lacc,
+                             bf16* oout, cudaStream_t st);
 
 }  // namespace upipe

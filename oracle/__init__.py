@@ -318,6 +318,23 @@ def layer_backward_rows(X, Wqkv, Wo, seg, dY_rows, rows, Hq, Hkv, Dh, causal=Tru
     return dQKV @ Wqkv, dQKV.T @ X, dWo
 
 
+def lse_merge(O_a, L_a, O_b, L_b):
+    """Attention over the union of two disjoint key sets from the per-set results, as ring (P2P)
+    context parallelism combines the key/value blocks that visit a device (MaxText long-context
+    article on techmoon.xyz, table of the four context-parallel strategies, row "P2P (Ring)").
+    With L the natural-log log-sum-exp of a row's scores over a key set and O its softmax-weighted
+    values: L = log(e^{L_a} + e^{L_b}), O = (e^{L_a} O_a + e^{L_b} O_b) / e^{L}.  A side with
+    L = -inf (no key) contributes nothing; both -inf gives O = 0, L = -inf.
+    O_*: [..., Dh], L_*: [...] (float64)."""
+    O_a, L_a, O_b, L_b = (np.asarray(x, dtype=np.float64) for x in (O_a, L_a, O_b, L_b))
+    L = np.logaddexp(L_a, L_b)
+    ok = np.isfinite(L)
+    with np.errstate(invalid="ignore", over="ignore"):
+        wa = np.where(ok & np.isfinite(L_a), np.exp(L_a - np.where(ok, L, 0.0)), 0.0)
+        wb = np.where(ok & np.isfinite(L_b), np.exp(L_b - np.where(ok, L, 0.0)), 0.0)
+    return wa[..., None] * O_a + wb[..., None] * O_b, L
+
+
 # ----------------------------------------------------------------------------------------------
 # tile-skip table (Splash-style block skipping, MaxText article)
 # ----------------------------------------------------------------------------------------------

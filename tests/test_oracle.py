@@ -282,6 +282,69 @@ def test_project_kv_blocks_match_one_product():
 
 
 # ------------------------------------------------------------------------------------------
+# 5b. ring (P2P) merge of block results
+# ------------------------------------------------------------------------------------------
+
+def test_merge_of_disjoint_key_sets_equals_attention_over_their_union():
+    S, Dh = 40, 8
+    Q, K, V = rand_qkv(S, 2, 1, Dh, seed=31)
+    scale = orc.default_scale(Dh)
+    O, L = orc.attention_forward(Q, K, V, None, False, scale)
+    rng = np.random.default_rng(3)
+    sel = rng.permutation(S)
+    A, B = np.sort(sel[:13]), np.sort(sel[13:])
+    Oa, La = orc.attention_forward(Q, K[:, A], V[:, A], None, False, scale)
+    Ob, Lb = orc.attention_forward(Q, K[:, B], V[:, B], None, False, scale)
+    Om, Lm = orc.lse_merge(Oa, La, Ob, Lb)
+    np.testing.assert_allclose(Om, O, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(Lm, L, rtol=1e-13, atol=1e-13)
+    Om2, Lm2 = orc.lse_merge(Ob, Lb, Oa, La)  # order of the blocks does not matter
+    np.testing.assert_allclose(Om2, Om, rtol=1e-13, atol=1e-14)
+
+
+def test_merge_with_an_empty_side():
+    rng = np.random.default_rng(4)
+    O = rng.standard_normal((3, 5, 4))
+    L = rng.standard_normal((3, 5))
+    ninf = np.full((3, 5), -np.inf)
+    Om, Lm = orc.lse_merge(O, L, np.full_like(O, 7.0), ninf)
+    np.testing.assert_array_equal(Lm, L)
+    np.testing.assert_allclose(Om, O, rtol=1e-15, atol=0)
+    Oz, Lz = orc.lse_merge(np.zeros_like(O), ninf, np.zeros_like(O), ninf)
+    assert np.all(np.isneginf(Lz)) and not np.any(Oz)
+
+
+def test_zigzag_ring_schedule_reproduces_causal_attention():
+    """Every device's blocks of the zigzag ring (causal on its own chunks, full on earlier ones,
+    skipped on later ones), merged in ring order, give causal attention over the whole sequence;
+    and every device computes the same number of blocks (the load balancing)."""
+    import long_context_attention_upipe_gb300 as up
+    P, C, Dh = 3, 7, 8
+    S = 2 * P * C
+    Q, K, V = rand_qkv(S, 2, 1, Dh, seed=32)
+    scale = orc.default_scale(Dh)
+    O, L = orc.attention_forward(Q, K, V, None, True, scale)
+    sched = up.ring_block_schedule(P)
+    assert len({sum(len(b) for b in steps) for steps in sched}) == 1
+    seen = set()
+    Oacc = {c: np.zeros((2, C, Dh)) for c in range(2 * P)}
+    Lacc = {c: np.full((2, C), -np.inf) for c in range(2 * P)}
+    for steps in sched:
+        for blocks in steps:
+            for qc, kc, kind in blocks:
+                assert kc <= qc and (kind == "causal") == (kc == qc)
+                seen.add((qc, kc))
+                q = Q[:, qc * C:(qc + 1) * C]
+                Ob, Lb = orc.attention_forward(q, K[:, kc * C:(kc + 1) * C], V[:, kc * C:(kc + 1) * C], None,
+                                               kind == "causal", scale)
+                Oacc[qc], Lacc[qc] = orc.lse_merge(Oacc[qc], Lacc[qc], Ob, Lb)
+    assert seen == {(a, b) for a in range(2 * P) for b in range(a + 1)}   # each block exactly once
+    for c in range(2 * P):
+        np.testing.assert_allclose(Oacc[c], O[:, c * C:(c + 1) * C], rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(Lacc[c], L[:, c * C:(c + 1) * C], rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------------------------------------------------
 # 6. tile-skip table
 # ------------------------------------------------------------------------------------------
 
