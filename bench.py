@@ -44,7 +44,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--sample-tokens", type=int, default=1024, help="oracle sample length (CPU legs)")
-    ap.add_argument("--kernel", default=None, choices=["fwd", "recompute", "dq", "dkdv", "lse_merge", "ring"],
+    ap.add_argument("--kernel", default=None, choices=["fwd", "recompute", "dq", "dkdv", "lse_merge", "ring", "ring_bwd"],
                     help="time one attention kernel alone at the workload's chunk shapes (for profilers); "
                          "lse_merge: the ring merge of one block into fp32 accumulators; ring: the chunk's causal "
                          "attention as the blocks of a zigzag ring of --ring-p devices, run on this GPU")
@@ -348,7 +348,7 @@ def main():
             "dkdv": lambda: up.core_bwd_dkdv(cdesc, q, k, v, do, lse_c, Dt, seg_t, table, dk, dv, stream),
         }
 
-    if args.kernel in ("lse_merge", "ring"):
+    if args.kernel in ("lse_merge", "ring", "ring_bwd"):
         if seg_t is not None:
             raise SystemExit("the ring share runs unpacked sequences only")
         g = Hq // Hkv
@@ -370,11 +370,18 @@ def main():
             print(json.dumps({"kernel": "lse_merge", "workload": w.name, "heads": args.hpc, "ms": ms_k,
                               "bytes": nbytes, "gbs": gbs, "hbm_frac": gbs / peaks["hbm_gbs"]}))
             return
-        f = lambda: up.ring_attention_share(q, k, v, args.ring_p, 0.0, stream)
+        if args.kernel == "ring":
+            f = lambda: up.ring_attention_share(q, k, v, args.ring_p, 0.0, stream)
+            fl = attn_kernel_flops(w, args.hpc, "fwd")
+        else:  # dQ, dK, dV of the ring's blocks (recompute-free: the forward's O and lse are given)
+            do = fill((args.hpc, S, Dh), 13, 1.0)
+            o, lse_r = up.ring_attention_share(q, k, v, args.ring_p, 0.0, stream)
+            f = lambda: up.ring_attention_share_backward(q, k, v, o, lse_r, do, args.ring_p, 0.0, stream)
+            fl = attn_kernel_flops(w, args.hpc, "dq") + attn_kernel_flops(w, args.hpc, "dkdv")
         f()
         ms_k = time_steps(f, args.reps)
-        tf = attn_kernel_flops(w, args.hpc, "fwd") / (ms_k * 1e-3) / 1e12
-        print(json.dumps({"kernel": "ring", "ring_p": args.ring_p, "workload": w.name, "heads": args.hpc,
+        tf = fl / (ms_k * 1e-3) / 1e12
+        print(json.dumps({"kernel": args.kernel, "ring_p": args.ring_p, "workload": w.name, "heads": args.hpc,
                           "ms": ms_k, "tflops": tf}))
         return
     if args.kernel:

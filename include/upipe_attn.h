@@ -201,6 +201,22 @@ upipe_status_t upipe_attn_gemm_nt(int64_t M, int64_t N, int64_t K, const uint16_
 upipe_status_t upipe_attn_lse_merge(int64_t rows, int32_t head_dim, const uint16_t* O_b, const float* lse_b,
                                     float* O_acc, float* lse_acc, uint16_t* O_out, void* stream);
 
+/* Backward of the ring share.  Every block (query chunk, key chunk) runs upipe_attn_core_bwd_dq
+ * and upipe_attn_core_bwd_dkdv with the softmax over the whole key set: the query chunk's final
+ * log-sum-exp and D = rowsum(dO * O) of its final (merged) output.  This fills their D buffer
+ * from those: D device fp32 [2][n_heads][Sp], Sp = ceil(seq_len/128)*128, D[0][h][i] = sum over
+ * the head dimension of dO * O, D[1][h][i] = lse * log2(e), zeros for i >= seq_len.
+ *   O, dO  device bf16 [n_heads][seq_len][head_dim]: the chunk's final output and its gradient
+ *   lse    device fp32 [n_heads][seq_len]: the chunk's final log-sum-exp (natural log)
+ * head_dim 64 or 128; pointers 16-byte aligned. */
+upipe_status_t upipe_attn_ring_bwd_prep(int32_t n_heads, int64_t seq_len, int32_t head_dim, const uint16_t* O,
+                                        const uint16_t* dO, const float* lse, float* D, void* stream);
+
+/* acc[i] += src[i] for n elements (src device bf16, acc device fp32, in place); out, if not NULL,
+ * receives bf16(acc[i]) (round to nearest even).  The ring backward sums the blocks' dQ, dK and dV
+ * contributions with it and rounds each gradient once.  Pointers 16-byte aligned. */
+upipe_status_t upipe_attn_accumulate(int64_t n, const uint16_t* src, float* acc, uint16_t* out, void* stream);
+
 /* Reads the device error word of a workspace (after fwd/bwd) or of a table (after
  * build_tile_table) into *code (a upipe_status_t value; UPIPE_OK when none).  Synchronises
  * `stream`.  `buf` is the workspace or the table. */

@@ -22,7 +22,8 @@ UPIPE_OK = 0
 EXPORTS = ["upipe_attn_status_string", "upipe_attn_last_error_string", "upipe_attn_workspace_size", "upipe_attn_tile_table_size",
            "upipe_attn_build_tile_table", "upipe_attn_fwd", "upipe_attn_bwd", "upipe_attn_core_fwd",
            "upipe_attn_core_recompute", "upipe_attn_core_bwd_dq", "upipe_attn_core_bwd_dkdv", "upipe_attn_gemm_nt",
-           "upipe_attn_device_status", "upipe_attn_fwd_no_alloc", "upipe_attn_launch_count", "upipe_attn_lse_merge"]
+           "upipe_attn_device_status", "upipe_attn_fwd_no_alloc", "upipe_attn_launch_count", "upipe_attn_lse_merge",
+           "upipe_attn_ring_bwd_prep", "upipe_attn_accumulate"]
 
 
 class Desc(ctypes.Structure):
@@ -71,6 +72,8 @@ def lib():
             "upipe_attn_fwd_no_alloc": ([D, P, P, P, P, P, P, P], ctypes.c_int),
             "upipe_attn_launch_count": ([], ctypes.c_uint64),
             "upipe_attn_lse_merge": ([I64, ctypes.c_int32, P, P, P, P, P, P], ctypes.c_int),
+            "upipe_attn_ring_bwd_prep": ([ctypes.c_int32, I64, ctypes.c_int32, P, P, P, P, P], ctypes.c_int),
+            "upipe_attn_accumulate": ([I64, P, P, P, P], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -261,6 +264,69 @@ def ring_attention_share(q, k, v, P: int, softmax_scale: float = 0.0, stream=Non
         O[:, c * C:(c + 1) * C] = o_out[c]
         lse[:, c * C:(c + 1) * C] = l_acc[c]
     return O, lse
+
+
+def ring_bwd_prep(O, dO, lse, D, stream=None):
+    """D buffer [2][H][Sp] of the backward kernels from a chunk's final O, dO [H, S, Dh] and lse."""
+    H, S, Dh = O.shape
+    _check(lib().upipe_attn_ring_bwd_prep(H, S, Dh, _bf16(O), _bf16(dO), _ptr(lse), _ptr(D), _stream(stream)),
+           "ring_bwd_prep")
+
+
+def accumulate(src, acc, out=None, stream=None):
+    """acc += src (bf16 into fp32, in place); out (bf16, optional) = the rounded sum."""
+    _check(lib().upipe_attn_accumulate(src.numel(), _bf16(src), _ptr(acc), _bf16(out) if out is not None else None,
+                                       _stream(stream)), "accumulate")
+
+
+def ring_attention_share_backward(q, k, v, O, lse, dO, P: int, softmax_scale: float = 0.0, stream=None):
+    """Gradients of causal attention (dQ [Hq, S, Dh], dK, dV [Hkv, S, Dh], bf16) computed block by
+    block as the zigzag ring's devices would: each block runs upipe_attn_core_bwd_dq and _dkdv with
+    its query chunk's final log-sum-exp and D = rowsum(dO * O) (upipe_attn_ring_bwd_prep), and the
+    blocks' contributions are summed in fp32 per chunk (upipe_attn_accumulate), rounded once.
+    O, lse: the forward's result over the whole sequence (ring_attention_share)."""
+    Hq, S, Dh = q.shape
+    Hkv = k.shape[0]
+    n = 2 * P
+    if S % n:
+        raise ValueError("S must be a multiple of 2P")
+    C = S // n
+    dev = q.device
+    descs = {kind: make_desc(C, 64, Hq, Hkv, Dh, Hq, kind == "causal", 0, softmax_scale) for kind in ("causal", "full")}
+    tables = {}
+    for kind, dsc in descs.items():
+        t = torch.empty(tile_table_bytes(dsc), dtype=torch.uint8, device=dev)
+        build_tile_table(dsc, None, t, stream)
+        tables[kind] = t
+    cut = lambda x: [x[:, c * C:(c + 1) * C].contiguous() for c in range(n)]
+    qs, ks, vs, os_, dos, ls = cut(q), cut(k), cut(v), cut(O), cut(dO), cut(lse)
+    sp = -(-C // 128) * 128
+    Ds = [torch.empty(2, Hq, sp, dtype=torch.float32, device=dev) for _ in range(n)]
+    for c in range(n):
+        ring_bwd_prep(os_[c], dos[c], ls[c], Ds[c], stream)
+    f32 = lambda H: [torch.zeros(H, C, Dh, dtype=torch.float32, device=dev) for _ in range(n)]
+    b16 = lambda H: [torch.empty(H, C, Dh, dtype=torch.bfloat16, device=dev) for _ in range(n)]
+    dq_acc, dk_acc, dv_acc = f32(Hq), f32(Hkv), f32(Hkv)
+    dq_out, dk_out, dv_out = b16(Hq), b16(Hkv), b16(Hkv)
+    dq_b = torch.empty(Hq, C, Dh, dtype=torch.bfloat16, device=dev)
+    dk_b = torch.empty(Hkv, C, Dh, dtype=torch.bfloat16, device=dev)
+    dv_b = torch.empty(Hkv, C, Dh, dtype=torch.bfloat16, device=dev)
+    order = [blk for steps in ring_block_schedule(P) for blocks in steps for blk in blocks]
+    last_q = {qc: i for i, (qc, _, _) in enumerate(order)}
+    last_k = {kc: i for i, (_, kc, _) in enumerate(order)}
+    for i, (qc, kc, kind) in enumerate(order):
+        d, t = descs[kind], tables[kind]
+        core_bwd_dq(d, qs[qc], ks[kc], vs[kc], dos[qc], ls[qc], Ds[qc], None, t, dq_b, stream)
+        accumulate(dq_b, dq_acc[qc], dq_out[qc] if last_q[qc] == i else None, stream)
+        core_bwd_dkdv(d, qs[qc], ks[kc], vs[kc], dos[qc], ls[qc], Ds[qc], None, t, dk_b, dv_b, stream)
+        accumulate(dk_b, dk_acc[kc], dk_out[kc] if last_k[kc] == i else None, stream)
+        accumulate(dv_b, dv_acc[kc], dv_out[kc] if last_k[kc] == i else None, stream)
+    dQ, dK, dV = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    for c in range(n):  # placement only
+        dQ[:, c * C:(c + 1) * C] = dq_out[c]
+        dK[:, c * C:(c + 1) * C] = dk_out[c]
+        dV[:, c * C:(c + 1) * C] = dv_out[c]
+    return dQ, dK, dV
 
 
 class Layer:

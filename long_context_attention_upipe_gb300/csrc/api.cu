@@ -563,6 +563,22 @@ upipe_status_t upipe_attn_lse_merge(int64_t rows, int32_t head_dim, const uint16
                                       reinterpret_cast<bf16*>(O_out), (cudaStream_t)stream));
 }
 
+upipe_status_t upipe_attn_ring_bwd_prep(int32_t n_heads, int64_t seq_len, int32_t head_dim, const uint16_t* O,
+                                        const uint16_t* dO, const float* lse, float* D, void* stream) {
+  if (n_heads <= 0 || seq_len < 1 || seq_len > INT32_MAX || !O || !dO || !lse || !D) return UPIPE_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return UPIPE_ERR_UNSUPPORTED;
+  if (!aligned16(O) || !aligned16(dO) || !aligned16(lse) || !aligned16(D)) return UPIPE_ERR_ALIGNMENT;
+  return cuda_status(launch_ring_bwd_prep(n_heads, seq_len, head_dim, reinterpret_cast<const bf16*>(O),
+                                          reinterpret_cast<const bf16*>(dO), lse, D, (cudaStream_t)stream));
+}
+
+upipe_status_t upipe_attn_accumulate(int64_t n, const uint16_t* src, float* acc, uint16_t* out, void* stream) {
+  if (n < 0 || !src || !acc) return UPIPE_ERR_INVALID_ARG;
+  if (!aligned16(src) || !aligned16(acc) || (out && !aligned16(out))) return UPIPE_ERR_ALIGNMENT;
+  return cuda_status(launch_accumulate(n, reinterpret_cast<const bf16*>(src), acc, reinterpret_cast<bf16*>(out),
+                                       (cudaStream_t)stream));
+}
+
 uint64_t upipe_attn_launch_count(void) { return upipe::g_launch_count.load(std::memory_order_relaxed); }
 
 upipe_status_t upipe_attn_device_status(const void* buf, int32_t* code, void* stream) {

@@ -128,5 +128,8 @@ cudaError_t launch_f32_to_bf16(const float* in, bf16* out, int64_t n, float mul,
 cudaError_t launch_zero(void* p, int64_t bytes, cudaStream_t st);
 cudaError_t launch_lse_merge(int64_t rows, int head_dim, const bf16* ob, const float* lb, float* oacc, float* lacc,
                              bf16* oout, cudaStream_t st);
+cudaError_t launch_ring_bwd_prep(int nh, int64_t S, int head_dim, const bf16* o, const bf16* dout, const float* lse,
+                                 float* D, cudaStream_t st);
+cudaError_t launch_accumulate(int64_t n, const bf16* src, float* acc, bf16* out, cudaStream_t st);
 
 }  // namespace upipe

@@ -335,6 +335,34 @@ def lse_merge(O_a, L_a, O_b, L_b):
     return wa[..., None] * O_a + wb[..., None] * O_b, L
 
 
+def attention_backward_block(Q, K, V, dO, L, D, causal: bool, scale: float):
+    """One key/value block's share of the attention backward when each row's softmax runs over more
+    keys than the block holds (the ring's backward): with the row's final log-sum-exp L_h[i] and
+    D_h[i] = dO_h[i] . O_h[i] of its final output, over the block's visible keys
+    P_ij = exp(s_ij - L_i), dP_ij = dO_h[i] . V[j], dS_ij = P_ij (dP_ij - D_i); the block adds
+    dQ_h[i] += scale sum_j dS_ij K[j], dK[j] += scale sum_{h,i} dS_ij Q_h[i], dV[j] += sum_{h,i} P_ij dO_h[i].
+    Q, dO [Hq, R, Dh]; K, V [Hkv, C, Dh]; L, D [Hq, R]; positions as in attention_forward (row i and
+    column j of the block; causal means j <= i).  Returns the block's dQ [Hq, R, Dh], dK, dV [Hkv, C, Dh]."""
+    Hq, R, Dh = Q.shape
+    Hkv, C = K.shape[0], K.shape[1]
+    g = Hq // Hkv
+    vis = visibility(None, np.arange(R), np.arange(C), causal)
+    dQ = np.zeros_like(Q)
+    dK = np.zeros_like(K)
+    dV = np.zeros_like(V)
+    for h in range(Hq):
+        kv = h // g
+        s = scale * (Q[h] @ K[kv].T)
+        ok = vis & np.isfinite(L[h])[:, None]
+        P = np.where(ok, np.exp(np.where(ok, s, 0.0) - np.where(np.isfinite(L[h]), L[h], 0.0)[:, None]), 0.0)
+        dP = dO[h] @ V[kv].T
+        dS = P * (dP - D[h][:, None])
+        dQ[h] = scale * (dS @ K[kv])
+        dK[kv] += scale * (dS.T @ Q[h])
+        dV[kv] += P.T @ dO[h]
+    return dQ, dK, dV
+
+
 # ----------------------------------------------------------------------------------------------
 # tile-skip table (Splash-style block skipping, MaxText article)
 # ----------------------------------------------------------------------------------------------

@@ -344,6 +344,33 @@ def test_zigzag_ring_schedule_reproduces_causal_attention():
         np.testing.assert_allclose(Lacc[c], L[:, c * C:(c + 1) * C], rtol=1e-12, atol=1e-12)
 
 
+def test_zigzag_ring_blocks_reproduce_the_causal_backward():
+    """The blocks of the zigzag ring, each with its query chunk's final log-sum-exp and
+    D = dO . O, summed per chunk, give the gradients of causal attention over the whole sequence."""
+    import long_context_attention_upipe_gb300 as up
+    P, C, Dh = 2, 9, 8
+    S = 2 * P * C
+    Q, K, V = rand_qkv(S, 4, 2, Dh, seed=33)
+    dO = np.random.default_rng(34).standard_normal(Q.shape)
+    scale = orc.default_scale(Dh)
+    O, L = orc.attention_forward(Q, K, V, None, True, scale)
+    dQ, dK, dV = orc.attention_backward(Q, K, V, dO, None, True, scale)
+    D = (dO * O).sum(axis=2)
+    gq, gk, gv = np.zeros_like(Q), np.zeros_like(K), np.zeros_like(V)
+    for steps in up.ring_block_schedule(P):
+        for blocks in steps:
+            for qc, kc, kind in blocks:
+                qs, ks = slice(qc * C, (qc + 1) * C), slice(kc * C, (kc + 1) * C)
+                bq, bk, bv = orc.attention_backward_block(Q[:, qs], K[:, ks], V[:, ks], dO[:, qs], L[:, qs], D[:, qs],
+                                                          kind == "causal", scale)
+                gq[:, qs] += bq
+                gk[:, ks] += bk
+                gv[:, ks] += bv
+    np.testing.assert_allclose(gq, dQ, rtol=1e-10, atol=1e-11)
+    np.testing.assert_allclose(gk, dK, rtol=1e-10, atol=1e-11)
+    np.testing.assert_allclose(gv, dV, rtol=1e-10, atol=1e-11)
+
+
 # ------------------------------------------------------------------------------------------
 # 6. tile-skip table
 # ------------------------------------------------------------------------------------------
