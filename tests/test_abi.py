@@ -76,3 +76,41 @@ def test_fwd_host_checks_run_before_any_launch():
     assert L.upipe_attn_build_tile_table(ctypes.byref(t), None, fake, 16, None) == 4
     assert L.upipe_attn_build_tile_table(ctypes.byref(t), odd, fake, 1 << 20, None) == 3
     assert up.launch_count() == launches  # rejected calls launch nothing
+
+
+def test_ring_entry_points_check_arguments_before_any_launch():
+    L = up.lib()
+    launches = up.launch_count()
+    fake = ctypes.c_void_p(0x10000)       # never dereferenced: the checks fail first
+    odd = ctypes.c_void_p(0x10008)
+    assert L.upipe_attn_lse_merge(8, 128, None, fake, fake, fake, None, None) == 1          # NULL O_b
+    assert L.upipe_attn_lse_merge(-1, 128, fake, fake, fake, fake, None, None) == 1         # negative rows
+    assert L.upipe_attn_lse_merge(8, 96, fake, fake, fake, fake, None, None) == 2           # head_dim
+    assert L.upipe_attn_lse_merge(8, 128, fake, fake, odd, fake, None, None) == 3           # alignment
+    assert L.upipe_attn_lse_merge(8, 128, fake, fake, fake, fake, odd, None) == 3           # O_out alignment
+    assert L.upipe_attn_ring_bwd_prep(0, 128, 128, fake, fake, fake, fake, None) == 1       # no heads
+    assert L.upipe_attn_ring_bwd_prep(2, 0, 128, fake, fake, fake, fake, None) == 1         # empty chunk
+    assert L.upipe_attn_ring_bwd_prep(2, 128, 80, fake, fake, fake, fake, None) == 2        # head_dim
+    assert L.upipe_attn_ring_bwd_prep(2, 128, 64, fake, odd, fake, fake, None) == 3         # alignment
+    assert L.upipe_attn_accumulate(16, None, fake, None, None) == 1                         # NULL source
+    assert L.upipe_attn_accumulate(16, fake, odd, None, None) == 3                          # alignment
+    assert up.launch_count() == launches  # rejected calls launch nothing
+    # zero rows / elements are valid and launch nothing
+    assert L.upipe_attn_lse_merge(0, 64, fake, fake, fake, fake, None, None) == 0
+    assert L.upipe_attn_accumulate(0, fake, fake, None, None) == 0
+    assert up.launch_count() == launches
+
+
+@pytest.mark.parametrize("P", [1, 2, 3, 4, 5, 8])
+def test_zigzag_ring_schedule_is_balanced_and_complete(P):
+    """Each device computes 2P + 1 blocks (the zigzag balance); over all devices every block with
+    key chunk <= query chunk is computed exactly once, causal exactly on the diagonal; a contiguous
+    split (device r holding chunks 2r and 2r + 1) would not be balanced."""
+    sched = up.ring_block_schedule(P)
+    assert [sum(len(b) for b in steps) for steps in sched] == [2 * P + 1] * P
+    blocks = [blk for steps in sched for b in steps for blk in b]
+    assert sorted((q, k) for q, k, _ in blocks) == sorted((q, k) for q in range(2 * P) for k in range(q + 1))
+    assert all((kind == "causal") == (q == k) for q, k, kind in blocks)
+    if P > 1:
+        contiguous = [sum(1 for q in (2 * r, 2 * r + 1) for k in range(q + 1)) for r in range(P)]
+        assert len(set(contiguous)) > 1
