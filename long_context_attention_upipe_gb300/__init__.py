@@ -227,17 +227,33 @@ def ring_block_schedule(P: int):
     return sched
 
 
+def _check_ring_inputs(q, k, v, P):
+    if P < 1:
+        raise ValueError("P must be at least 1")
+    if q.dim() != 3 or k.dim() != 3 or v.shape != k.shape:
+        raise ValueError("q must be [Hq, S, Dh] and k, v [Hkv, S, Dh]")
+    if q.dtype != torch.bfloat16 or k.dtype != torch.bfloat16 or v.dtype != torch.bfloat16:
+        raise ValueError("q, k, v must be bf16")
+    Hq, S, Dh = q.shape
+    Hkv = k.shape[0]
+    if k.shape[1] != S or k.shape[2] != Dh or Hq % Hkv:
+        raise ValueError("k, v must cover the same positions and head_dim as q, with Hq a multiple of Hkv")
+    if Dh not in (64, 128):
+        raise ValueError("head_dim must be 64 or 128")
+    if S % (2 * P):
+        raise ValueError("S must be a multiple of 2P")
+
+
 def ring_attention_share(q, k, v, P: int, softmax_scale: float = 0.0, stream=None):
     """Causal attention of q [Hq, S, Dh] over k, v [Hkv, S, Dh] computed block by block as the P
     devices of a zigzag ring would, each block with upipe_attn_core_fwd on contiguous chunk copies
     and folded into per-chunk fp32 accumulators with upipe_attn_lse_merge, in ring-step order.
     One GPU runs every device's blocks in turn (there is no exchange to make).  Returns O bf16
     [Hq, S, Dh] and lse fp32 [Hq, S].  softmax_scale 0 means 1/sqrt(Dh)."""
+    _check_ring_inputs(q, k, v, P)
     Hq, S, Dh = q.shape
     Hkv = k.shape[0]
     n = 2 * P
-    if S % n:
-        raise ValueError("S must be a multiple of 2P")
     C = S // n
     descs = {kind: make_desc(C, 64, Hq, Hkv, Dh, Hq, kind == "causal", 0, softmax_scale) for kind in ("causal", "full")}
     tables = {}
@@ -285,11 +301,12 @@ def ring_attention_share_backward(q, k, v, O, lse, dO, P: int, softmax_scale: fl
     its query chunk's final log-sum-exp and D = rowsum(dO * O) (upipe_attn_ring_bwd_prep), and the
     blocks' contributions are summed in fp32 per chunk (upipe_attn_accumulate), rounded once.
     O, lse: the forward's result over the whole sequence (ring_attention_share)."""
+    _check_ring_inputs(q, k, v, P)
+    if O.shape != q.shape or dO.shape != q.shape or tuple(lse.shape) != tuple(q.shape[:2]):
+        raise ValueError("O and dO must be shaped like q, lse [Hq, S]")
     Hq, S, Dh = q.shape
     Hkv = k.shape[0]
     n = 2 * P
-    if S % n:
-        raise ValueError("S must be a multiple of 2P")
     C = S // n
     dev = q.device
     descs = {kind: make_desc(C, 64, Hq, Hkv, Dh, Hq, kind == "causal", 0, softmax_scale) for kind in ("causal", "full")}

@@ -114,3 +114,22 @@ def test_zigzag_ring_schedule_is_balanced_and_complete(P):
     if P > 1:
         contiguous = [sum(1 for q in (2 * r, 2 * r + 1) for k in range(q + 1)) for r in range(P)]
         assert len(set(contiguous)) > 1
+
+
+def test_ring_runs_check_their_inputs_before_touching_the_gpu():
+    import torch
+    q = torch.zeros(4, 64, 128, dtype=torch.bfloat16)
+    k = torch.zeros(2, 64, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        up.ring_attention_share(q, k, k, 3)                    # 64 not a multiple of 2P = 6
+    with pytest.raises(ValueError):
+        up.ring_attention_share(q, k[:, :32], k[:, :32], 2)    # key positions differ
+    with pytest.raises(ValueError):
+        up.ring_attention_share(q.float(), k, k, 2)            # not bf16
+    with pytest.raises(ValueError):
+        up.ring_attention_share(q[:3], k, k, 2)                # Hq not a multiple of Hkv
+    with pytest.raises(ValueError):
+        up.ring_attention_share(q, k, k, 0)
+    lse = torch.zeros(4, 64)
+    with pytest.raises(ValueError):
+        up.ring_attention_share_backward(q, k, k, q, lse[:, :32], q, 2)
