@@ -79,3 +79,22 @@ def test_segment_recipe():
     assert L == ui.loguniform_lengths(131072)
     seg = ui.segments_from_lengths(L)
     assert seg.dtype == np.int32 and np.all(np.diff(seg) >= 0) and seg[-1] == len(L) - 1
+
+
+def test_metric_flops_of_the_workloads():
+    """The metric counts algorithmic FLOPs: attention 4 Dh per visible (query, key) pair and head
+    forward, 3.5x that forward+backward, and the projections 2 M N K forward, 3x forward+backward.
+    The visible pairs of the packed 131K workload are recounted here from the oracle's per-tile
+    counts (a row-by-row count of the mask, independent of the closed form used by the metric)."""
+    import oracle as orc
+    w = ui.workload("packed_131k")
+    pairs = int(orc.tile_counts(w.S, w.segments(), True).sum())
+    assert pairs == w.visible_pairs()
+    assert abs(pairs / (w.S * (w.S + 1) / 2) - 0.1095) < 5e-4       # 10.95% of dense causal pairs
+    w2 = ui.workload("llama8b_32k")
+    attn_fwd = 4 * 128 * (32768 * 32769 // 2) * 32
+    proj_fwd = 2 * 32768 * 4096 * (32 + 16) * 128 + 2 * 32768 * 32 * 128 * 4096
+    assert w2.flops_fwd_bwd() == 3.5 * attn_fwd + 3 * proj_fwd
+    assert abs(w2.flops_fwd_bwd() / 1e12 - 39.03) < 0.01
+    assert abs(ui.workload("ulysses_1m").flops_fwd_bwd() / 1e15 - 3.974) < 0.001
+    assert abs(ui.workload("share32b_5m").flops_fwd_bwd() / 1e15 - 179.554) < 0.001
