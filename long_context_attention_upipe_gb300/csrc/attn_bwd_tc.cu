@@ -13,7 +13,7 @@
 //   element-wise for tile a / b, one query row per thread (TMEM lane).
 //   TMEM per tile: a 128-column region that holds S, then dP, then dS (bf16, columns 0-63),
 //   and the dQ accumulator.  Per key tile:  S = Q K^T -> P = exp2(S c - lse2) kept in
-//   registers as bf16 -> region free -> dP = dO V^T -> dS = P (dP - D) written to TMEM ->
+//   registers in fp32 -> region free -> dP = dO V^T -> dS = P (dP - D) written to TMEM ->
 //   dQ += dS K (A operand from TMEM, K in shared memory read MN-major).
 //
 // k_attn_bwd_dkdv_tc  (one KV head x one 128-row key tile per CTA, 12 warps)

@@ -17,7 +17,7 @@
 //              B rows 0-63, B rows 64-127; one thread could not issue a stage's four loads within
 //              its MMA time) over a 6-stage ring of (A 128x64, B half 128x64) tiles; both CTAs'
 //              loads count on the even CTA's stage barrier; a stage is refilled once the MMAs
-//              that read it have completed (commit multicast to both CTAs)
+//              that read it have completed (a pair commit arrives in both CTAs)
 //   warp 1     TMEM owner in both CTAs; in the even CTA the MMA issuer (one thread): 4 MMAs
 //              (M256 N256 K16) per stage into one of two TMEM accumulators, so the epilogue of
 //              a tile overlaps the next tile
@@ -142,7 +142,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_gemm_tc(const __grid_constant__ 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
       tc::mbar_init(&full[i], 1);   // even CTA: its producer's arrival + both CTAs' bytes
-      tc::mbar_init(&empty[i], 1);  // the even CTA's MMA commit (multicast to both)
+      tc::mbar_init(&empty[i], 1);  // the even CTA's MMA commit (a pair commit arrives in both)
     }
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&acc_full[i], 1);
@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_gemm_tc(const __grid_constant__ 
   }
   tc::fence_before_sync();
   __syncthreads();
-  tc::cluster_sync();  // the peer's barriers are initialised before any multicast reaches them
+  tc::cluster_sync();  // the peer's barriers are initialised before any pair commit or load reaches them
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
@@ -348,7 +348,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_gemm_tc(const __grid_constant__ 
   }
   tc::fence_before_sync();
   __syncthreads();
-  // the peer may still multicast into this CTA's shared memory or arrive on its barriers until
+  // the peer may still load into this CTA's shared memory or arrive on its barriers until
   // its own last MMAs are done: leave together
   tc::cluster_sync();
   if (warp == 1) {
