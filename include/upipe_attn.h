@@ -53,7 +53,7 @@ typedef enum {
 } upipe_status_t;
 
 typedef struct {
-  int64_t seq_len;         /* S: 1 .. 2^31 - 1 tokens                                          */
+  int64_t seq_len;         /* S: 1 .. 2^31 - 1 tokens (TMA tile coordinates are signed 32-bit)  */
   int32_t hidden;          /* d: multiple of 64                                                */
   int32_t n_q_heads;       /* Hq                                                               */
   int32_t n_kv_heads;      /* Hkv; Hq % Hkv == 0 (g = Hq / Hkv query heads share a KV head)     */
@@ -67,7 +67,8 @@ typedef struct {
   float softmax_scale;     /* 0 selects 1/sqrt(head_dim)                                       */
 } upipe_attn_desc_t;
 
-/* Human-readable name of a status code (static string, never NULL). */
+/* Human-readable name of a status code (static string, never NULL).  No counterpart on the
+ * pages (they print no interface); a convenience of this library. */
 const char* upipe_attn_status_string(upipe_status_t status);
 
 /* Name of the CUDA runtime error (e.g. "cudaErrorInvalidValue") behind the most recent
@@ -76,11 +77,15 @@ const char* upipe_attn_last_error_string(void);
 
 /* Workspace bytes needed by upipe_attn_fwd (pass = 0) or upipe_attn_bwd (pass = 1) for this
  * descriptor.  Host-only; writes *bytes.  The size grows with heads_per_chunk (per-chunk
- * Q/O/dO/dQ buffers and the resident K/V of one KV group), not with n_q_heads. */
+ * Q/O/dO/dQ buffers and the resident K/V of one KV group), not with n_q_heads: the one reused
+ * group-sized buffer of UPipe ("Road to 5 Million Tokens" podcast summary, chapter "主要貢獻
+ * UPipe": the next group reuses the buffer the previous group allocated). */
 upipe_status_t upipe_attn_workspace_size(const upipe_attn_desc_t* desc, int pass, size_t* bytes);
 
 /* Bytes of the tile-skip table for seq_len S, with n = ceil(S/128):
- * 32-byte header + 2 * n * 16 + 4 * (ceil(n/2) + n), rounded up to a multiple of 16. */
+ * 32-byte header + 2 * n * 16 + 4 * (ceil(n/2) + n), rounded up to a multiple of 16.
+ * (MaxText long-context article, Splash attention paragraph: the table is what lets fully
+ * masked blocks be skipped.) */
 upipe_status_t upipe_attn_tile_table_size(const upipe_attn_desc_t* desc, size_t* bytes);
 
 /* Tile-skip table (Splash-style skipping of fully masked blocks, MaxText article).
@@ -100,9 +105,12 @@ upipe_status_t upipe_attn_tile_table_size(const upipe_attn_desc_t* desc, size_t*
  * The two orders are the attention kernels' dispatch orders (most work first); they do not change
  * any result.
  * seg: device int32[S] or NULL (one segment).  table: device, table_bytes from
- * upipe_attn_tile_table_size.  Only desc->seq_len and desc->causal are read. */
+ * upipe_attn_tile_table_size.  Only desc->seq_len and desc->causal are read.
+ * visited_counts_host: NULL, or host int64[2] that receives {n_partial, n_full} (the visited
+ *   tile pairs per head); then the call waits for the stream (a synchronous read of the header).
+ *   With NULL the call is asynchronous and the counts stay readable in the header. */
 upipe_status_t upipe_attn_build_tile_table(const upipe_attn_desc_t* desc, const int32_t* seg, void* table,
-                                           size_t table_bytes, void* stream);
+                                           size_t table_bytes, int64_t* visited_counts_host, void* stream);
 
 /* Forward pass of the layer.
  *   X    device bf16 [S, d]                      hidden states
@@ -142,7 +150,10 @@ upipe_status_t upipe_attn_bwd(const upipe_attn_desc_t* desc, const uint16_t* X, 
  *    are rejected with UPIPE_ERR_WORKSPACE_TOO_SMALL before any launch.
  *  - No cudaMalloc, cudaFree or other allocating call is made.
  *  - The first call on a device looks up the array's device address on that (current)
- *    device; make that first call before any stream capture.
+ *    device; make that first call before any stream capture.  The address is kept for the
+ *    life of the process: do not use this entry point across cudaDeviceReset.
+ *  - Device-detected errors land in the array's own error word: read them with
+ *    upipe_attn_no_alloc_device_status.
  *  - Every call uses the same array and leaves its contents behind; the forward pass
  *    initialises everything it reads.  Calls whose executions overlap on the GPU (different
  *    streams, or concurrent host threads) race on the array: serialise them. */
@@ -150,16 +161,18 @@ upipe_status_t upipe_attn_fwd_no_alloc(const upipe_attn_desc_t* desc, const uint
                                        const uint16_t* Wo, const int32_t* seg, uint16_t* Y, float* lse,
                                        void* stream);
 
-/* Attention core alone, Q/K/V given directly (head-major), for testing the kernels in isolation.
- *   q [Hq, S, Dh], k, v [Hkv, S, Dh] device bf16; table from upipe_attn_build_tile_table;
+/* Attention core alone, Q/K/V given directly (head-major), for testing the kernels in isolation
+ * (flash attention over whole heads: podcast summary, chapter "DeepSpeed Ulysses").
+ *   q [Hq, S, Dh], k, v [Hkv, S, Dh] device bf16; table from upipe_attn_build_tile_table (its
+ *   header's error word is set if a bounded device wait runs out, so it is not const);
  *   o [Hq, S, Dh] device bf16 (written); lse [Hq, S] device fp32 (written).
  * heads_per_chunk and hidden are ignored. */
 upipe_status_t upipe_attn_core_fwd(const upipe_attn_desc_t* desc, const uint16_t* q, const uint16_t* k,
-                                   const uint16_t* v, const int32_t* seg, const void* table, uint16_t* o,
+                                   const uint16_t* v, const int32_t* seg, void* table, uint16_t* o,
                                    float* lse, void* stream);
 
 /* The three kernels of the attention backward, one launch each, in the order the layer runs
- * them.  Arguments as in upipe_attn_core_fwd; dO [Hq, S, Dh] device bf16; lse [Hq, S] from the
+ * them (activation recompute: podcast summary, chapter "Activation checkpointing").  Arguments as in upipe_attn_core_fwd; dO [Hq, S, Dh] device bf16; lse [Hq, S] from the
  * forward pass.
  *   recompute: o [Hq, S, Dh] bf16 and D, device fp32 [2][Hq][Sp] with Sp = ceil(S/128)*128:
  *              D[0][h][i] = rowsum(dO * O) of query row i, D[1][h][i] = lse * log2(e), zeros
@@ -170,17 +183,18 @@ upipe_status_t upipe_attn_core_fwd(const upipe_attn_desc_t* desc, const uint16_t
  *              dv_j = sum P_ij dO_i,  dk_j = scale * sum P_ij (dP_ij - D_i) q_i. */
 upipe_status_t upipe_attn_core_recompute(const upipe_attn_desc_t* desc, const uint16_t* q, const uint16_t* k,
                                          const uint16_t* v, const uint16_t* dO, const float* lse, const int32_t* seg,
-                                         const void* table, uint16_t* o, float* D, void* stream);
+                                         void* table, uint16_t* o, float* D, void* stream);
 upipe_status_t upipe_attn_core_bwd_dq(const upipe_attn_desc_t* desc, const uint16_t* q, const uint16_t* k,
                                       const uint16_t* v, const uint16_t* dO, const float* lse, const float* D,
-                                      const int32_t* seg, const void* table, uint16_t* dq, void* stream);
+                                      const int32_t* seg, void* table, uint16_t* dq, void* stream);
 upipe_status_t upipe_attn_core_bwd_dkdv(const upipe_attn_desc_t* desc, const uint16_t* q, const uint16_t* k,
                                         const uint16_t* v, const uint16_t* dO, const float* lse, const float* D,
-                                        const int32_t* seg, const void* table, uint16_t* dk, uint16_t* dv,
+                                        const int32_t* seg, void* table, uint16_t* dk, uint16_t* dv,
                                         void* stream);
 
 /* Projection GEMM alone, for testing: C[M, N] (fp32, row-major, ldc) = A[M, K] * B[N, K]^T with
- * A, B device bf16 row-major (lda, ldb in elements). */
+ * A, B device bf16 row-major (lda, ldb in elements).  The per-chunk Q/K/V and O projections of
+ * the layer run on this kernel (podcast summary, Q&A chapter: UPipe concerns the layer's Q/K/V). */
 upipe_status_t upipe_attn_gemm_nt(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda,
                                   const uint16_t* B, int64_t ldb, float* C, int64_t ldc, void* stream);
 
@@ -219,8 +233,19 @@ upipe_status_t upipe_attn_accumulate(int64_t n, const uint16_t* src, float* acc,
 
 /* Reads the device error word of a workspace (after fwd/bwd) or of a table (after
  * build_tile_table) into *code (a upipe_status_t value; UPIPE_OK when none).  Synchronises
- * `stream`.  `buf` is the workspace or the table. */
+ * `stream`.  `buf` is the workspace or the table.  No counterpart on the pages. */
 upipe_status_t upipe_attn_device_status(const void* buf, int32_t* code, void* stream);
+
+/* The same read with the argument order of the library's original interface sketch: `ws` is a
+ * workspace (or a table), *code receives its device error word after `stream` has drained. */
+upipe_status_t upipe_attn_last_device_error(const void* ws, void* stream, int32_t* code);
+
+/* Device error word of the array upipe_attn_fwd_no_alloc uses as its workspace, on the current
+ * device, after `stream` has drained: segment ids that are not non-decreasing
+ * (UPIPE_ERR_SEGMENTS_NOT_CONTIGUOUS) or a bounded device wait that ran out.  Allocates nothing.
+ * The word describes the most recent upipe_attn_fwd_no_alloc call on this device (each call
+ * clears it first).  Before the first such call on a device it reports UPIPE_OK. */
+upipe_status_t upipe_attn_no_alloc_device_status(int32_t* code, void* stream);
 
 /* Number of GPU kernels this library has launched in the process so far (every entry point
  * counts its own launches; a diagnostic with no counterpart in the method).  The difference of

@@ -23,7 +23,8 @@ EXPORTS = ["upipe_attn_status_string", "upipe_attn_last_error_string", "upipe_at
            "upipe_attn_build_tile_table", "upipe_attn_fwd", "upipe_attn_bwd", "upipe_attn_core_fwd",
            "upipe_attn_core_recompute", "upipe_attn_core_bwd_dq", "upipe_attn_core_bwd_dkdv", "upipe_attn_gemm_nt",
            "upipe_attn_device_status", "upipe_attn_fwd_no_alloc", "upipe_attn_launch_count", "upipe_attn_lse_merge",
-           "upipe_attn_ring_bwd_prep", "upipe_attn_accumulate"]
+           "upipe_attn_ring_bwd_prep", "upipe_attn_accumulate", "upipe_attn_last_device_error",
+           "upipe_attn_no_alloc_device_status"]
 
 
 class Desc(ctypes.Structure):
@@ -60,7 +61,7 @@ def lib():
             "upipe_attn_last_error_string": ([], ctypes.c_char_p),
             "upipe_attn_workspace_size": ([D, ctypes.c_int, ctypes.POINTER(SZ)], ctypes.c_int),
             "upipe_attn_tile_table_size": ([D, ctypes.POINTER(SZ)], ctypes.c_int),
-            "upipe_attn_build_tile_table": ([D, P, P, SZ, P], ctypes.c_int),
+            "upipe_attn_build_tile_table": ([D, P, P, SZ, ctypes.POINTER(I64), P], ctypes.c_int),
             "upipe_attn_fwd": ([D, P, P, P, P, P, P, P, SZ, P], ctypes.c_int),
             "upipe_attn_bwd": ([D, P, P, P, P, P, P, P, P, P, P, SZ, P], ctypes.c_int),
             "upipe_attn_core_fwd": ([D, P, P, P, P, P, P, P, P], ctypes.c_int),
@@ -74,6 +75,8 @@ def lib():
             "upipe_attn_lse_merge": ([I64, ctypes.c_int32, P, P, P, P, P, P], ctypes.c_int),
             "upipe_attn_ring_bwd_prep": ([ctypes.c_int32, I64, ctypes.c_int32, P, P, P, P, P], ctypes.c_int),
             "upipe_attn_accumulate": ([I64, P, P, P, P], ctypes.c_int),
+            "upipe_attn_last_device_error": ([P, P, ctypes.POINTER(ctypes.c_int32)], ctypes.c_int),
+            "upipe_attn_no_alloc_device_status": ([ctypes.POINTER(ctypes.c_int32), P], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -118,14 +121,31 @@ def tile_table_bytes(desc: Desc) -> int:
     return n.value
 
 
-def build_tile_table(desc: Desc, seg, table, stream=None):
+def build_tile_table(desc: Desc, seg, table, stream=None, counts=False):
+    """Build the skip table into `table` (device uint8).  counts=True also returns the visited
+    tile pairs per head (n_partial, n_full), read back by the library (synchronises the stream)."""
+    out = (ctypes.c_int64 * 2)() if counts else None
     _check(lib().upipe_attn_build_tile_table(ctypes.byref(desc), _ptr(seg), _ptr(table), table.numel() * table.element_size(),
-                                             _stream(stream)), "build_tile_table")
+                                             out, _stream(stream)), "build_tile_table")
+    return (int(out[0]), int(out[1])) if counts else None
 
 
 def device_status(buf, stream=None) -> int:
     code = ctypes.c_int32(0)
     _check(lib().upipe_attn_device_status(_ptr(buf), ctypes.byref(code), _stream(stream)), "device_status")
+    return code.value
+
+
+def last_device_error(ws, stream=None) -> int:
+    code = ctypes.c_int32(0)
+    _check(lib().upipe_attn_last_device_error(_ptr(ws), _stream(stream), ctypes.byref(code)), "last_device_error")
+    return code.value
+
+
+def no_alloc_device_status(stream=None) -> int:
+    """Error word of the allocation-free forward's own workspace array (current device)."""
+    code = ctypes.c_int32(0)
+    _check(lib().upipe_attn_no_alloc_device_status(ctypes.byref(code), _stream(stream)), "no_alloc_device_status")
     return code.value
 
 

@@ -397,15 +397,28 @@ upipe_status_t upipe_attn_tile_table_size(const upipe_attn_desc_t* desc, size_t*
   return UPIPE_OK;
 }
 
+// Splash-style table of the tiles that are not fully masked (MaxText long-context article, Splash
+// attention paragraph); optionally hands the visited-tile counts back to the host.
 upipe_status_t upipe_attn_build_tile_table(const upipe_attn_desc_t* desc, const int32_t* seg, void* table,
-                                           size_t table_bytes, void* stream) {
+                                           size_t table_bytes, int64_t* visited_counts_host, void* stream) {
   if (!desc || !table || desc->seq_len < 1 || desc->seq_len > INT32_MAX) return UPIPE_ERR_INVALID_ARG;
   if (desc->causal != 0 && desc->causal != 1) return UPIPE_ERR_INVALID_ARG;
   if (!aligned16(table) || (seg && !aligned16(seg))) return UPIPE_ERR_ALIGNMENT;
   if (table_bytes < tile_table_bytes(desc->seq_len)) return UPIPE_ERR_WORKSPACE_TOO_SMALL;
-  return cuda_status(launch_tile_table(desc->seq_len, desc->causal, seg, table, (cudaStream_t)stream));
+  cudaStream_t st = (cudaStream_t)stream;
+  UPIPE_CUDA(launch_tile_table(desc->seq_len, desc->causal, seg, table, st));
+  if (visited_counts_host) {
+    long long counts[2];
+    UPIPE_CUDA(cudaMemcpyAsync(counts, table, sizeof(counts), cudaMemcpyDeviceToHost, st));
+    UPIPE_CUDA(cudaStreamSynchronize(st));
+    visited_counts_host[0] = counts[0];
+    visited_counts_host[1] = counts[1];
+  }
+  return UPIPE_OK;
 }
 
+// The layer's forward, one chunk of query heads after another in one reused workspace ("Road to
+// 5 Million Tokens" podcast summary, chapters "主要貢獻 UPipe" and "分批算 heads").
 upipe_status_t upipe_attn_fwd(const upipe_attn_desc_t* desc, const uint16_t* X, const uint16_t* Wqkv, const uint16_t* Wo,
                               const int32_t* seg, uint16_t* Y, float* lse, void* ws, size_t ws_bytes, void* stream) {
   upipe_status_t s = check_desc(desc);
@@ -420,6 +433,8 @@ upipe_status_t upipe_attn_fwd(const upipe_attn_desc_t* desc, const uint16_t* X, 
                  reinterpret_cast<const bf16*>(Wo), seg, reinterpret_cast<bf16*>(Y), lse, ws, (cudaStream_t)stream);
 }
 
+// The layer's backward, chunk by chunk, recomputing each chunk's activations from X and lse
+// (same summary, chapter "Activation checkpointing").
 upipe_status_t upipe_attn_bwd(const upipe_attn_desc_t* desc, const uint16_t* X, const uint16_t* Wqkv, const uint16_t* Wo,
                               const int32_t* seg, const uint16_t* dY, const float* lse, uint16_t* dX, float* dWqkv,
                               float* dWo, void* ws, size_t ws_bytes, void* stream) {
@@ -445,7 +460,7 @@ static upipe_status_t check_core(const upipe_attn_desc_t* desc) {
 }
 
 static AttnArgs core_args(const upipe_attn_desc_t* desc, const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                          const int32_t* seg, const void* table) {
+                          const int32_t* seg, void* table) {
   AttnArgs a{};
   a.q = reinterpret_cast<const bf16*>(q);
   a.k = reinterpret_cast<const bf16*>(k);
@@ -461,12 +476,13 @@ static AttnArgs core_args(const upipe_attn_desc_t* desc, const uint16_t* q, cons
   a.g = desc->n_q_heads / desc->n_kv_heads;
   a.causal = desc->causal;
   a.scale = desc->softmax_scale > 0.f ? desc->softmax_scale : 1.0f / std::sqrt((float)desc->head_dim);
-  a.err = reinterpret_cast<int*>(reinterpret_cast<char*>(const_cast<void*>(table)) + offsetof(TableHeader, error));
+  a.err = &reinterpret_cast<TableHeader*>(table)->error;
   return a;
 }
 
+// Flash-style attention forward over whole heads (podcast summary, chapter "DeepSpeed Ulysses").
 upipe_status_t upipe_attn_core_fwd(const upipe_attn_desc_t* desc, const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                                   const int32_t* seg, const void* table, uint16_t* o, float* lse, void* stream) {
+                                   const int32_t* seg, void* table, uint16_t* o, float* lse, void* stream) {
   upipe_status_t s = check_core(desc);
   if (s != UPIPE_OK) return s;
   if (!q || !k || !v || !table || !o || !lse) return UPIPE_ERR_INVALID_ARG;
@@ -478,9 +494,10 @@ upipe_status_t upipe_attn_core_fwd(const upipe_attn_desc_t* desc, const uint16_t
   return cuda_status(launch_attn_fwd(a, desc->head_dim, (cudaStream_t)stream));
 }
 
+// O and D recomputed from the saved lse (podcast summary, chapter "Activation checkpointing").
 upipe_status_t upipe_attn_core_recompute(const upipe_attn_desc_t* desc, const uint16_t* q, const uint16_t* k,
                                          const uint16_t* v, const uint16_t* dO, const float* lse, const int32_t* seg,
-                                         const void* table, uint16_t* o, float* D, void* stream) {
+                                         void* table, uint16_t* o, float* D, void* stream) {
   upipe_status_t s = check_core(desc);
   if (s != UPIPE_OK) return s;
   if (!q || !k || !v || !dO || !lse || !table || !o || !D) return UPIPE_ERR_INVALID_ARG;
@@ -497,7 +514,7 @@ upipe_status_t upipe_attn_core_recompute(const upipe_attn_desc_t* desc, const ui
 
 static upipe_status_t core_bwd_common(const upipe_attn_desc_t* desc, const uint16_t* q, const uint16_t* k,
                                       const uint16_t* v, const uint16_t* dO, const float* lse, const float* D,
-                                      const int32_t* seg, const void* table, AttnBwdArgs* b) {
+                                      const int32_t* seg, void* table, AttnBwdArgs* b) {
   upipe_status_t s = check_core(desc);
   if (s != UPIPE_OK) return s;
   if (!q || !k || !v || !dO || !lse || !D || !table) return UPIPE_ERR_INVALID_ARG;
@@ -513,9 +530,10 @@ static upipe_status_t core_bwd_common(const upipe_attn_desc_t* desc, const uint1
   return UPIPE_OK;
 }
 
+// dQ of the attention backward (chain rule of the same softmax; recompute as above).
 upipe_status_t upipe_attn_core_bwd_dq(const upipe_attn_desc_t* desc, const uint16_t* q, const uint16_t* k,
                                       const uint16_t* v, const uint16_t* dO, const float* lse, const float* D,
-                                      const int32_t* seg, const void* table, uint16_t* dq, void* stream) {
+                                      const int32_t* seg, void* table, uint16_t* dq, void* stream) {
   AttnBwdArgs b;
   upipe_status_t s = core_bwd_common(desc, q, k, v, dO, lse, D, seg, table, &b);
   if (s != UPIPE_OK) return s;
@@ -525,9 +543,10 @@ upipe_status_t upipe_attn_core_bwd_dq(const upipe_attn_desc_t* desc, const uint1
   return cuda_status(launch_attn_bwd_dq(b, desc->head_dim, (cudaStream_t)stream));
 }
 
+// dK, dV with the GQA heads of each KV head summed (MaxText article, Splash paragraph: GQA).
 upipe_status_t upipe_attn_core_bwd_dkdv(const upipe_attn_desc_t* desc, const uint16_t* q, const uint16_t* k,
                                         const uint16_t* v, const uint16_t* dO, const float* lse, const float* D,
-                                        const int32_t* seg, const void* table, uint16_t* dk, uint16_t* dv,
+                                        const int32_t* seg, void* table, uint16_t* dk, uint16_t* dv,
                                         void* stream) {
   AttnBwdArgs b;
   upipe_status_t s = core_bwd_common(desc, q, k, v, dO, lse, D, seg, table, &b);
@@ -581,6 +600,7 @@ upipe_status_t upipe_attn_accumulate(int64_t n, const uint16_t* src, float* acc,
 
 uint64_t upipe_attn_launch_count(void) { return upipe::g_launch_count.load(std::memory_order_relaxed); }
 
+// Error word of a workspace or table header (bounded device waits, segment order check).
 upipe_status_t upipe_attn_device_status(const void* buf, int32_t* code, void* stream) {
   if (!buf || !code) return UPIPE_ERR_INVALID_ARG;
   int32_t v = 0;
@@ -591,6 +611,10 @@ upipe_status_t upipe_attn_device_status(const void* buf, int32_t* code, void* st
   if (e != cudaSuccess) return cuda_status(e);
   *code = v;
   return UPIPE_OK;
+}
+
+upipe_status_t upipe_attn_last_device_error(const void* ws, void* stream, int32_t* code) {
+  return upipe_attn_device_status(ws, code, stream);
 }
 
 }  // extern "C"

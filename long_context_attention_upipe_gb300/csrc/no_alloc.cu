@@ -24,6 +24,24 @@ static __device__ __align__(256) unsigned char g_static_workspace[kStaticWorkspa
 std::mutex g_mutex;
 void* g_device_ptr[kMaxDevices] = {};
 
+// Device address of the array on the current device, resolved once per device (no allocation).
+upipe_status_t static_workspace(void** ws) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return upipe::cuda_status(e);
+  if (dev < 0 || dev >= kMaxDevices) return UPIPE_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (!g_device_ptr[dev]) {
+    // first call on this device: the device is current, so the symbol resolves to its copy
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_workspace);
+    if (e != cudaSuccess) return upipe::cuda_status(e);
+    g_device_ptr[dev] = p;
+  }
+  *ws = g_device_ptr[dev];
+  return UPIPE_OK;
+}
+
 }  // namespace
 
 extern "C" upipe_status_t upipe_attn_fwd_no_alloc(const upipe_attn_desc_t* desc, const uint16_t* X,
@@ -33,23 +51,20 @@ extern "C" upipe_status_t upipe_attn_fwd_no_alloc(const upipe_attn_desc_t* desc,
   upipe_status_t s = upipe_attn_workspace_size(desc, 0, &need);
   if (s != UPIPE_OK) return s;
   if (need > kStaticWorkspaceBytes) return UPIPE_ERR_WORKSPACE_TOO_SMALL;  // descriptor too large for the array
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return upipe::cuda_status(e);
-  if (dev < 0 || dev >= kMaxDevices) return UPIPE_ERR_UNSUPPORTED;
   void* ws = nullptr;
-  {
-    // first call on this device: resolve the array's device address (the device is current)
-    std::lock_guard<std::mutex> lock(g_mutex);
-    if (!g_device_ptr[dev]) {
-      void* p = nullptr;
-      e = cudaGetSymbolAddress(&p, g_static_workspace);
-      if (e != cudaSuccess) return upipe::cuda_status(e);
-      g_device_ptr[dev] = p;
-    }
-    ws = g_device_ptr[dev];
-  }
+  s = static_workspace(&ws);
+  if (s != UPIPE_OK) return s;
   // every buffer that must start from a known state (the table header with its error word, the
   // first chunk's output accumulator) is initialised by the forward pass itself
   return upipe_attn_fwd(desc, X, Wqkv, Wo, seg, Y, lse, ws, kStaticWorkspaceBytes, stream);
+}
+
+// The array's error word (the table header at its base), read like any workspace's.  Before the
+// first forward on a device the array is still zero-initialised, so the word reads UPIPE_OK.
+extern "C" upipe_status_t upipe_attn_no_alloc_device_status(int32_t* code, void* stream) {
+  if (!code) return UPIPE_ERR_INVALID_ARG;
+  void* ws = nullptr;
+  upipe_status_t s = static_workspace(&ws);
+  if (s != UPIPE_OK) return s;
+  return upipe_attn_device_status(ws, code, stream);
 }

@@ -73,8 +73,10 @@ def test_fwd_host_checks_run_before_any_launch():
     bad = up.make_desc(512, 256, 4, 2, 96, 2)
     assert L.upipe_attn_fwd(ctypes.byref(bad), fake, fake, fake, None, fake, fake, fake, 1 << 40, None) == 2
     t = up.make_desc(512, 256, 4, 2, 64, 2)
-    assert L.upipe_attn_build_tile_table(ctypes.byref(t), None, fake, 16, None) == 4
-    assert L.upipe_attn_build_tile_table(ctypes.byref(t), odd, fake, 1 << 20, None) == 3
+    assert L.upipe_attn_build_tile_table(ctypes.byref(t), None, fake, 16, None, None) == 4
+    assert L.upipe_attn_build_tile_table(ctypes.byref(t), odd, fake, 1 << 20, None, None) == 3
+    assert L.upipe_attn_last_device_error(None, None, ctypes.byref(ctypes.c_int32())) == 1   # NULL workspace
+    assert L.upipe_attn_no_alloc_device_status(None, None) == 1                            # NULL code
     assert up.launch_count() == launches  # rejected calls launch nothing
 
 

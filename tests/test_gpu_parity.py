@@ -26,12 +26,13 @@ def gpu_table(S, seg_np, causal):
     desc = up.make_desc(S, 64, 1, 1, 64, 1, causal)
     table = torch.empty(up.tile_table_bytes(desc), dtype=torch.uint8, device="cuda")
     seg = torch.from_numpy(seg_np).cuda() if seg_np is not None else None
-    up.build_tile_table(desc, seg, table)
+    host_counts = up.build_tile_table(desc, seg, table, counts=True)   # read back by the library
     torch.cuda.synchronize()
     t = table.cpu().numpy()
     nt = -(-S // 128)
     head = t[:32]
     counts = head[:16].view(np.int64)
+    assert list(host_counts) == counts.tolist()
     err = int(head[16:20].view(np.int32)[0])
     q_rows = t[32:32 + 16 * nt].view(np.int32).reshape(nt, 4)
     kv_rows = t[32 + 16 * nt:32 + 32 * nt].view(np.int32).reshape(nt, 4)
@@ -125,6 +126,7 @@ def test_tile_table_rejects_unsorted_segments():
     *_, err, table = gpu_table(256, seg, True)
     assert err == 5
     assert up.device_status(table) == 5
+    assert up.last_device_error(table) == 5
 
 
 # ----------------------------------------------------------------------------------------------

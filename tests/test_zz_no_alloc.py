@@ -62,6 +62,24 @@ def test_no_alloc_forward_matches_regular_forward_twice():
         assert max_abs(got_lse, want_lse) <= 1e-3
 
 
+def test_no_alloc_forward_reports_device_errors():
+    # segment ids that decrease are only visible on the device; the error word of the library's
+    # own array must report them, and the next good call must clear it again
+    S, d, Hq, Hkv, Dh = 256, 128, 2, 1, 64
+    X, W, Wo, _ = layer_inputs(S, d, Hq, Hkv, Dh, dy=False)
+    Xt, Wt, Wot = bf16_tensor(X), bf16_tensor(W), bf16_tensor(Wo)
+    desc = up.make_desc(S, d, Hq, Hkv, Dh, 1, True)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    Y = torch.empty_like(Xt)
+    lse = torch.empty(Hq, S, dtype=torch.float32, device="cuda")
+    for ids, want in (([0] * 100 + [2] * 100 + [1] * 56, 5), ([0] * 100 + [1] * 156, 0)):
+        seg = torch.tensor(ids, dtype=torch.int32, device="cuda")
+        rc = up.lib().upipe_attn_fwd_no_alloc(ctypes.byref(desc), _ptr(Xt), _ptr(Wt), _ptr(Wot), _ptr(seg), _ptr(Y),
+                                              _ptr(lse), stream)
+        assert rc == 0
+        assert up.no_alloc_device_status() == want
+
+
 def test_no_alloc_forward_rejects_too_large_descriptor():
     # the 32k-token, 8-head chunk needs a forward workspace far above the 32 MiB array
     desc = up.make_desc(32768, 4096, 32, 8, 128, 8, True)
