@@ -3,8 +3,10 @@
 One step = upipe_attn_fwd + upipe_attn_bwd of the whole layer (tile table, per-chunk QKV
 projection, attention forward, output-projection accumulation; recompute, attention backward,
 input and weight gradients) on one batch of synthetic seeded inputs already resident in HBM.
-The default workload is the Llama-3.1-8B-shaped attention layer at 32,768 tokens (hidden 4096,
-32 query / 8 KV heads, head_dim 128, causal, one segment) with 8 query heads per chunk.
+The default workload is the single-GPU share of an 8-way Ulysses split at 1,048,576 tokens
+(4 query heads, 1 KV head, head_dim 128, hidden 4096, causal) with 4 query heads per chunk,
+swept over heads_per_chunk 1, 2 and 4; `--workload llama8b_32k` selects the Llama-3.1-8B-shaped
+layer at 32,768 tokens (32 / 8 heads, 8 per chunk).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -35,8 +37,9 @@ def parse():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="llama8b_32k")
-    ap.add_argument("--hpc", type=int, default=8)
+    ap.add_argument("--workload", default="ulysses_1m")
+    ap.add_argument("--hpc", type=int, default=None, help="query heads per chunk (default: the workload's largest "
+                    "swept value, 4 at 1M tokens, 8 at 32K)")
     ap.add_argument("--accum-mode", type=int, default=0)
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="launch the step's kernels one by one instead of replaying "
@@ -177,6 +180,8 @@ def run_reference(args):
     if rank != 0:
         return
     w = ui.workload(args.workload)
+    if args.hpc is None:
+        args.hpc = max(w.hpc_sweep)
     for _ in range(args.warmup):
         oracle_sample(w, args.sample_tokens)
     times = []
@@ -226,6 +231,84 @@ def attn_kernel_flops(w, nh, kernel):
     return per_pair * w.visible_pairs() * nh
 
 
+GEMM_KINDS = {"qkv_proj", "o_proj", "do_proj", "dwo", "dx_proj", "dwqkv"}
+ATTN_PER_PAIR = {"attn_fwd": 4, "recompute": 4, "bwd_dq": 6, "bwd_dkdv": 8}   # MMA FLOPs per visible pair / Dh
+EPI_NAMES = {0: "store bf16", 1: "store fp32", 2: "fp32 C += A B^T", 3: "bf16 C += A B^T"}
+
+
+def gemm_bytes(r):
+    """Algorithmic HBM bytes of one GEMM launch: A and B read once, C written (and read too when
+    the epilogue accumulates); split-K partials are scratch, not counted."""
+    m, n, k, epi = r["m"], r["n"], r["k"], r["epilogue"]
+    c = {0: 2 * m * n, 1: 4 * m * n, 2: 8 * m * n, 3: 4 * m * n}[epi]
+    return 2 * m * k + 2 * n * k + c
+
+
+def summarize_kernels(recs, w, peaks, step_ms):
+    """Per kernel class of one step: launches, device ms, executed FLOPs -> TFLOP/s, algorithmic
+    HBM bytes -> GB/s, and the roofline that bounds it (tensor for the contractions, hbm for the
+    conversion / zeroing passes and for GEMMs whose bytes take longer than their FLOPs)."""
+    groups = {}
+    for r in recs:
+        key = r["kind"] if r["kind"] not in GEMM_KINDS else f'{r["kind"]} ({EPI_NAMES[r["epilogue"]]})'
+        g = groups.setdefault(key, {"kernel": key, "launches": 0, "ms": 0.0, "flops": 0.0, "bytes": 0.0})
+        g["launches"] += 1
+        g["ms"] += r["ms"]
+        if r["kind"] in GEMM_KINDS:
+            g["flops"] += 2.0 * r["m"] * r["n"] * r["k"]
+            g["bytes"] += gemm_bytes(r)
+            g["shape"] = [r["m"], r["n"], r["k"]]
+        elif r["kind"] in ATTN_PER_PAIR:
+            g["flops"] += ATTN_PER_PAIR[r["kind"]] * w.Dh * w.visible_pairs() * r["n"]
+        elif r["kind"] == "convert":
+            g["bytes"] += 6.0 * r["m"]
+        elif r["kind"] == "zero":
+            g["bytes"] += 4.0 * r["m"]
+        elif r["kind"] == "tile_table":
+            g["bytes"] += 4.0 * r["m"]
+    sustained = step_ms > 500.0
+    peak_t = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
+    peak_kind = f"measured bf16 {'sustained (inside a step of ' + format(step_ms / 1e3, '.1f') + ' s)' if sustained else 'burst'}"
+    out = []
+    for g in groups.values():
+        sec = g["ms"] * 1e-3
+        t_flops = g["flops"] / (peak_t * 1e12)
+        t_bytes = g["bytes"] / (peaks["hbm_gbs"] * 1e9)
+        bound = "tensor" if g["flops"] and t_flops >= t_bytes else "hbm"
+        e = {"kernel": g["kernel"], "launches": g["launches"], "ms": round(g["ms"], 4),
+             "share": round(g["ms"] / step_ms, 4), "bound": bound}
+        if "shape" in g:
+            e["mnk_last"] = g["shape"]
+        if g["flops"]:
+            e["tflops"] = g["flops"] / sec / 1e12 if sec > 0 else None
+        if g["bytes"]:
+            e["gbs"] = g["bytes"] / sec / 1e9 if sec > 0 else None
+            e["bytes_per_launch"] = g["bytes"] / g["launches"]
+        if bound == "tensor":
+            e["peak"], e["peak_kind"] = peak_t, peak_kind
+            e["frac"] = e["tflops"] / peak_t
+        else:
+            e["peak"], e["peak_kind"] = peaks["hbm_gbs"], "measured HBM copy bandwidth"
+            e["frac"] = e["gbs"] / peaks["hbm_gbs"] if e.get("gbs") else None
+        out.append(e)
+    out.sort(key=lambda e: -e["ms"])
+    return out
+
+
+def instrumented_step(up, step, w, peaks, step_ms):
+    """One eager step with the library's per-launch event timing on; per-kernel summary."""
+    import torch
+    torch.cuda.synchronize()
+    up.timing_records()          # drop anything logged before
+    up.timing_enable(True)
+    try:
+        step()
+        torch.cuda.synchronize()
+    finally:
+        up.timing_enable(False)
+    return summarize_kernels(up.timing_records(), w, peaks, step_ms)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -249,6 +332,8 @@ def main():
     import upipe_inputs as ui
 
     w = ui.workload(args.workload)
+    if args.hpc is None:
+        args.hpc = max(w.hpc_sweep)
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream()
     S, d, Hq, Hkv, Dh = w.S, w.d, w.Hq, w.Hkv, w.Dh
@@ -394,7 +479,6 @@ def main():
 
     # ---------------- main timed run
     torch.cuda.reset_peak_memory_stats(dev)
-    base_alloc = torch.cuda.memory_allocated(dev)
     desc, layer, step, outs, step_on = make_layer(args.hpc)
     for _ in range(max(3, args.warmup)):
         step()
@@ -422,30 +506,24 @@ def main():
     peak_gb = torch.cuda.max_memory_allocated(dev) / 1e9
     ms_all = max_over_ranks(ms, dev)
     value = job_value(flops, world, ms_all)
+    # one more step, launched kernel by kernel with the library's per-launch event timing on: the
+    # same launches as a timed step, each bracketed by CUDA events on the step's stream
+    step_kernels = instrumented_step(up, step, w, peaks, ms)
 
     result = {}
     if rank == 0:
-        # ---------------- per-kernel timing of the attention kernels (same launch configuration)
-        hpc = args.hpc
-        n_chunks = Hq // hpc
-        kernels = chunk_kernels(hpc)
-        ktimes = {}
-        for name in ("fwd", "recompute", "dq", "dkdv"):
-            f = kernels[name]
-            for _ in range(2):
-                f()
-            ktimes[name] = time_steps(f, 5)
-        shares = {n: ktimes[n] * n_chunks / ms for n in ktimes}
-        dom = max(ktimes, key=lambda n: ktimes[n] * n_chunks)
-        achieved = attn_kernel_flops(w, hpc, dom) / (ktimes[dom] * 1e-3) / 1e12
-        peak = peaks["bf16_tflops"]
-        traffic = measured_traffic(dom, args.workload, hpc)
-        roofline = {"bound": "tensor", "kernel": f"attention {dom}", "achieved": achieved, "peak": peak,
-                    "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
-                    "peak_kind": f"{peak_kind} bf16 burst (kernel timed alone)"}
-        kernel_ms = {n: round(t, 4) for n, t in ktimes.items()}
+        # ---------------- the dominant kernel of the step against its roofline
+        dom = max((k for k in step_kernels if k["bound"] == "tensor"), key=lambda k: k["ms"])
+        traffic = measured_traffic(dom["kernel"], args.workload, args.hpc)
+        roofline = {"bound": "tensor", "kernel": dom["kernel"], "achieved": dom["tflops"], "peak": dom["peak"],
+                    "unit": "TFLOP/s", "frac": dom["tflops"] / dom["peak"],
+                    "traffic": None if traffic is None else traffic,
+                    "peak_kind": dom["peak_kind"],
+                    "how": "executed MMA FLOPs of its launches in one step / their CUDA-event durations inside "
+                           "that step"}
 
-        # ---------------- hpc sweep: speed and peak memory vs chunk size
+        # ---------------- hpc sweep: speed and peak memory vs chunk size (plus the HBM-bound kernels
+        # of the chunked schedule: the fp32 accumulating projections and the fp32 -> bf16 pass)
         sweep = []
         if not args.no_sweep:
             del layer, graph, timed, step, step_on
@@ -455,25 +533,30 @@ def main():
                 torch.cuda.reset_peak_memory_stats(dev)
                 before = torch.cuda.memory_allocated(dev)
                 dsc, lay, stp, _, stp_on = make_layer(h)
+                eager = stp
                 gr = None if args.no_graph else graph_of(stp_on)[0]
                 if gr is not None:
                     stp = gr.replay
                 stp()
-                t = time_steps(stp, 3)
+                t = time_steps(stp, 3 if ms < 2000 else 2)
                 pk = torch.cuda.max_memory_allocated(dev) / 1e9
+                kern = instrumented_step(up, eager, w, peaks, t)
                 sweep.append({"heads_per_chunk": h, "ms_per_step": round(t, 3),
                               "tflops": round(flops / (t * 1e-3) / 1e12, 2), "peak_hbm_gb": round(pk, 3),
                               "workspace_gb": round((up.workspace_bytes(dsc, 0) + up.workspace_bytes(dsc, 1)) / 1e9, 3),
-                              "inputs_outputs_gb": round(before / 1e9, 3)})
-                del lay, stp, gr, stp_on  # the graph and the step closures hold the layer's workspace
+                              "inputs_outputs_gb": round(before / 1e9, 3),
+                              "hbm_kernels": [k for k in kern if k["bound"] == "hbm"]})
+                del lay, stp, gr, stp_on, eager  # the graph and the step closures hold the layer's workspace
+            torch.cuda.empty_cache()
             desc, layer, step, outs, step_on = make_layer(args.hpc)
 
         # ---------------- end to end through the C-ABI with host buffers
-        # Every step uploads its X, Wqkv, Wo and dY from pinned host memory and reads dX, dWqkv
+        # Every step uploads its X, Wqkv, Wo and dY from pinned host memory and reads Y, dX, dWqkv
         # and dWo back, all inside the timed region.  The copies run on two copy streams beside
         # the compute: dY and the next step's X / Wqkv / Wo (double-buffered) upload while the
-        # forward runs, and the results download while the next step's forward runs.  Step 0
-        # uploads its own inputs before its forward; the last step prefetches nothing.
+        # forward runs, Y downloads while the backward runs, and dX / dWqkv / dWo download while
+        # the next step's forward runs.  Step 0 uploads its own inputs before its forward; the last
+        # step prefetches nothing.
         e2e = None
         if not args.no_e2e:
             Y, lse, dX, dW, dWo = outs
@@ -484,11 +567,12 @@ def main():
             hX, hW, hWo, hdY = pin(X), pin(W), pin(Wo), pin(dY)
             for h, t in ((hX, X), (hW, W), (hWo, Wo), (hdY, dY)):
                 h.copy_(t)
-            hdX, hdW, hdWo = pin(dX), pin(dW), pin(dWo)
+            hY, hdX, hdW, hdWo = pin(Y), pin(dX), pin(dW), pin(dWo)
             ins = [(X, W, Wo), (torch.empty_like(X), torch.empty_like(W), torch.empty_like(Wo))]
             cin, cout = torch.cuda.Stream(), torch.cuda.Stream()
             in_ready = [torch.cuda.Event(), torch.cuda.Event()]
-            dy_ready, bwd_done, out_done = torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()
+            dy_ready, fwd_done, bwd_done = torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()
+            y_done, out_done = torch.cuda.Event(), torch.cuda.Event()
 
             def upload(b):
                 for dst, src in zip(ins[b], (hX, hW, hWo)):
@@ -503,6 +587,7 @@ def main():
                 e0.record(stream)
                 bwd_done.record(stream)
                 out_done.record(stream)
+                y_done.record(stream)
                 cin.wait_stream(stream)
                 cout.wait_stream(stream)
                 with torch.cuda.stream(cin):
@@ -511,13 +596,19 @@ def main():
                     b = k & 1
                     Xb, Wb, Wob = ins[b]
                     stream.wait_event(in_ready[b])
+                    stream.wait_event(y_done)             # the previous step's Y has been read back
                     up.fwd(desc, Xb, Wb, Wob, seg_t, Y, lse, layer.ws_fwd, stream)
+                    fwd_done.record(stream)
                     with torch.cuda.stream(cin):
                         cin.wait_event(bwd_done)          # the previous backward read dY and ins[1 - b]
                         dY.copy_(hdY, non_blocking=True)
                         dy_ready.record(cin)
                         if k + 1 < n:
                             upload(1 - b)
+                    with torch.cuda.stream(cout):
+                        cout.wait_event(fwd_done)
+                        hY.copy_(Y, non_blocking=True)
+                        y_done.record(cout)
                     stream.wait_event(dy_ready)
                     stream.wait_event(out_done)           # the previous results have been read back
                     up.bwd(desc, Xb, Wb, Wob, seg_t, dY, lse, dX, dW, dWo, layer.ws_bwd, stream)
@@ -533,13 +624,15 @@ def main():
                 barrier()
                 return e0.elapsed_time(e1) / n
 
-            e2e_run(2)
-            t = e2e_run(max(3, args.steps // 2))
+            e2e_run(1 if ms > 2000 else 2)
+            n_e2e = max(2, args.steps // 4) if ms > 2000 else max(3, args.steps // 2)
+            t = e2e_run(n_e2e)
             h2d = sum(x.numel() * x.element_size() for x in (hX, hW, hWo, hdY))
-            d2h = sum(x.numel() * x.element_size() for x in (hdX, hdW, hdWo))
+            d2h = sum(x.numel() * x.element_size() for x in (hY, hdX, hdW, hdWo))
             e2e = {"value": flops / (t * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                   "d2h_bytes_per_step": d2h, "ms_per_step": t,
-                   "overlap": "dY and the next step's inputs upload during the forward; results download during the next forward"}
+                   "d2h_bytes_per_step": d2h, "ms_per_step": t, "steps": n_e2e,
+                   "overlap": "dY and the next step's inputs upload during the forward; Y downloads during the "
+                              "backward; dX, dWqkv, dWo download during the next forward"}
             del ins
 
         # ---------------- CPU baseline: the oracle on a bounded sample
@@ -550,6 +643,9 @@ def main():
                    "sample": f"oracle fp64 forward+backward on the first {Ssamp} tokens of {w.name}; "
                              f"{dt:.2f} s for {fl / 1e12:.4f} TFLOP"}
 
+        sustained = ms > 500.0
+        peak_step = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
+        x_mb = S * d * 2 / 1e6
         result = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": max(3, args.warmup), "ms_per_step": ms_all, "higher_is_better": True, "scaling": "weak",
@@ -557,14 +653,16 @@ def main():
             "config": {"workload": w.name, "seq_len": S, "hidden": d, "n_q_heads": Hq, "n_kv_heads": Hkv,
                        "head_dim": Dh, "heads_per_chunk": args.hpc, "causal": bool(w.causal),
                        "accum_mode": args.accum_mode,
-                       "l2": "inputs larger than L2 (X and dY are 268 MB each); no flush",
+                       "l2": f"inputs larger than L2 (X and dY are {x_mb:.0f} MB each); no flush",
                        "flops_per_step": flops, "parallelism": f"replicas{world}"},
             "tokens_per_s": S * world / (ms_all * 1e-3),
-            "pct_bf16_peak": 100.0 * (value / world) / peaks["bf16_tflops_sustained"],
+            "pct_bf16_peak": 100.0 * (value / world) / peak_step,
+            "pct_bf16_peak_of": (f"{peak_kind} bf16 {'sustained' if sustained else 'burst'} peak "
+                                 f"{peak_step} TFLOP/s ({'steps of ' + format(ms / 1e3, '.1f') + ' s run under the power cap' if sustained else 'sub-second steps'})"),
+            "pct_bf16_peak_burst": 100.0 * (value / world) / peaks["bf16_tflops"],
             "peak_hbm_gb": round(peak_gb, 3),
             "roofline": roofline,
-            "kernel_ms": kernel_ms,
-            "kernel_share": {n: round(s, 3) for n, s in shares.items()},
+            "step_kernels": step_kernels,
             "hpc_sweep": sweep,
             "e2e": e2e,
             "cpu_baseline": cpu,

@@ -247,6 +247,34 @@ upipe_status_t upipe_attn_last_device_error(const void* ws, void* stream, int32_
  * clears it first).  Before the first such call on a device it reports UPIPE_OK. */
 upipe_status_t upipe_attn_no_alloc_device_status(int32_t* code, void* stream);
 
+/* Per-launch timing of the layer's kernels, a diagnostic with no counterpart on the pages (the
+ * pages point to a profiler to find where memory and time go: podcast summary, chapter
+ * "PyTorch profiler").  While enabled, every kernel launch of upipe_attn_fwd / upipe_attn_bwd is
+ * bracketed by two CUDA events on the call's stream and logged with its kind and shape; do not
+ * enable it while a stream is being captured into a CUDA graph.  Process-wide; off by default.
+ *   kind      UPIPE_K_* below
+ *   epilogue  GEMMs: 0 store bf16, 1 store fp32, 2 fp32 C += A B^T, 3 bf16 C += A B^T
+ *   m, n, k   GEMMs: C[m, n] = A[m, k] B[n, k]^T; attention kernels: m = S, n = query heads,
+ *             k = head_dim; conversions / zeroing: m = elements; tile table: m = S
+ *   split_k   GEMM K splits (> 1: the record includes the split reduction)
+ *   chunk     head chunk index (-1 for the tile table)
+ *   ms        device time between the two events
+ * upipe_attn_timing_collect waits for the logged launches, copies up to `cap` records (in
+ * launch order) into `out`, writes the total count to *n and clears the log. */
+enum {
+  UPIPE_K_TILE_TABLE = 0, UPIPE_K_QKV_PROJ = 1, UPIPE_K_ATTN_FWD = 2, UPIPE_K_O_PROJ = 3, UPIPE_K_CONVERT = 4,
+  UPIPE_K_DO_PROJ = 5, UPIPE_K_RECOMPUTE = 6, UPIPE_K_DWO = 7, UPIPE_K_BWD_DQ = 8, UPIPE_K_BWD_DKDV = 9,
+  UPIPE_K_DX_PROJ = 10, UPIPE_K_DWQKV = 11, UPIPE_K_ZERO = 12
+};
+typedef struct {
+  int32_t kind, epilogue, split_k, chunk;
+  int64_t m, n, k;
+  float ms;
+  int32_t reserved;
+} upipe_attn_timing_t;
+upipe_status_t upipe_attn_timing_enable(int32_t on);
+upipe_status_t upipe_attn_timing_collect(upipe_attn_timing_t* out, int32_t cap, int32_t* n);
+
 /* Number of GPU kernels this library has launched in the process so far (every entry point
  * counts its own launches; a diagnostic with no counterpart in the method).  The difference of
  * two reads brackets the launches of the calls between them on any thread. */

@@ -24,7 +24,11 @@ EXPORTS = ["upipe_attn_status_string", "upipe_attn_last_error_string", "upipe_at
            "upipe_attn_core_recompute", "upipe_attn_core_bwd_dq", "upipe_attn_core_bwd_dkdv", "upipe_attn_gemm_nt",
            "upipe_attn_device_status", "upipe_attn_fwd_no_alloc", "upipe_attn_launch_count", "upipe_attn_lse_merge",
            "upipe_attn_ring_bwd_prep", "upipe_attn_accumulate", "upipe_attn_last_device_error",
-           "upipe_attn_no_alloc_device_status"]
+           "upipe_attn_no_alloc_device_status", "upipe_attn_timing_enable", "upipe_attn_timing_collect"]
+
+# kinds of the per-launch timing records (upipe_attn_timing_collect)
+KERNEL_KINDS = {0: "tile_table", 1: "qkv_proj", 2: "attn_fwd", 3: "o_proj", 4: "convert", 5: "do_proj",
+                6: "recompute", 7: "dwo", 8: "bwd_dq", 9: "bwd_dkdv", 10: "dx_proj", 11: "dwqkv", 12: "zero"}
 
 
 class Desc(ctypes.Structure):
@@ -36,6 +40,12 @@ class Desc(ctypes.Structure):
 def make_desc(S, d, Hq, Hkv, Dh, hpc=None, causal=True, accum_mode=0, scale=0.0) -> Desc:
     return Desc(int(S), int(d), int(Hq), int(Hkv), int(Dh), int(hpc if hpc is not None else Hq), int(bool(causal)),
                 int(accum_mode), float(scale))
+
+
+class TimingRec(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("epilogue", ctypes.c_int32), ("split_k", ctypes.c_int32),
+                ("chunk", ctypes.c_int32), ("m", ctypes.c_int64), ("n", ctypes.c_int64), ("k", ctypes.c_int64),
+                ("ms", ctypes.c_float), ("reserved", ctypes.c_int32)]
 
 
 class UpipeError(RuntimeError):
@@ -77,6 +87,9 @@ def lib():
             "upipe_attn_accumulate": ([I64, P, P, P, P], ctypes.c_int),
             "upipe_attn_last_device_error": ([P, P, ctypes.POINTER(ctypes.c_int32)], ctypes.c_int),
             "upipe_attn_no_alloc_device_status": ([ctypes.POINTER(ctypes.c_int32), P], ctypes.c_int),
+            "upipe_attn_timing_enable": ([ctypes.c_int32], ctypes.c_int),
+            "upipe_attn_timing_collect": ([ctypes.POINTER(TimingRec), ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)],
+                                          ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -147,6 +160,20 @@ def no_alloc_device_status(stream=None) -> int:
     code = ctypes.c_int32(0)
     _check(lib().upipe_attn_no_alloc_device_status(ctypes.byref(code), _stream(stream)), "no_alloc_device_status")
     return code.value
+
+
+def timing_enable(on: bool = True):
+    """Log every kernel launch of upipe_attn_fwd / _bwd with CUDA events (not during graph capture)."""
+    _check(lib().upipe_attn_timing_enable(int(bool(on))), "timing_enable")
+
+
+def timing_records(cap: int = 1 << 16):
+    """Collect the logged launches (waits for them), clearing the log; returns a list of dicts."""
+    buf = (TimingRec * cap)()
+    n = ctypes.c_int32(0)
+    _check(lib().upipe_attn_timing_collect(buf, cap, ctypes.byref(n)), "timing_collect")
+    return [{"kind": KERNEL_KINDS.get(r.kind, r.kind), "epilogue": r.epilogue, "split_k": r.split_k,
+             "chunk": r.chunk, "m": r.m, "n": r.n, "k": r.k, "ms": r.ms} for r in buf[:min(n.value, cap)]]
 
 
 def launch_count() -> int:

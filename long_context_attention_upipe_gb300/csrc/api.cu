@@ -23,6 +23,8 @@
 #include <atomic>
 #include <cmath>
 #include <cstring>
+#include <mutex>
+#include <vector>
 
 #include "common.cuh"
 #include "internal.h"
@@ -40,6 +42,44 @@ upipe_status_t cuda_status(cudaError_t e) {
   g_last_cuda_error = cudaGetErrorName(e);
   return UPIPE_ERR_CUDA;
 }
+
+// ------------------------------------------------------------------------ per-launch timing
+// When enabled (upipe_attn_timing_enable), every kernel launch of the fwd/bwd schedule is
+// bracketed by two CUDA events on its stream and logged with its kind and shape; the caller
+// collects the durations after the work has run.  Off by default, and then free.
+namespace {
+struct TimingRec {
+  int32_t kind, epi, split_k, chunk;
+  int64_t m, n, k;
+  cudaEvent_t e0, e1;
+};
+std::atomic<int> g_timing_on{0};
+std::mutex g_timing_mutex;
+std::vector<TimingRec> g_timing;
+
+class Timed {
+ public:
+  Timed(int kind, int epi, int64_t m, int64_t n, int64_t k, int split_k, int chunk, cudaStream_t st) : st_(st) {
+    if (!g_timing_on.load(std::memory_order_relaxed)) return;
+    rec_ = TimingRec{kind, epi, split_k, chunk, m, n, k, nullptr, nullptr};
+    if (cudaEventCreate(&rec_.e0) != cudaSuccess || cudaEventCreate(&rec_.e1) != cudaSuccess ||
+        cudaEventRecord(rec_.e0, st_) != cudaSuccess)
+      return;
+    on_ = true;
+  }
+  ~Timed() {
+    if (!on_) return;
+    if (cudaEventRecord(rec_.e1, st_) != cudaSuccess) return;
+    std::lock_guard<std::mutex> lock(g_timing_mutex);
+    g_timing.push_back(rec_);
+  }
+
+ private:
+  cudaStream_t st_;
+  TimingRec rec_{};
+  bool on_ = false;
+};
+}  // namespace
 
 namespace {
 
@@ -214,8 +254,10 @@ int accum_epi(const Plan& p, int c) {
   return c == 0 ? EPI_STORE_F32 : EPI_ACC_F32;
 }
 
+bool finishes_accum(const Plan& p, int c) { return p.n_chunks > 1 && p.accum == 0 && c == p.n_chunks - 1; }
+
 cudaError_t accum_finish(const Plan& p, int c, const float* acc, bf16* out, cudaStream_t st) {
-  if (p.n_chunks == 1 || p.accum == 1 || c != p.n_chunks - 1) return cudaSuccess;
+  if (!finishes_accum(p, c)) return cudaSuccess;
   return launch_f32_to_bf16(acc, out, p.S * p.d, 1.f, st);
 }
 
@@ -247,15 +289,27 @@ AttnArgs attn_args(const Plan& p, int c, void* ws, const int32_t* seg, float* ls
   return a;
 }
 
+// width (columns) of the chunk's Q (and, at a group start, K and V) projection
+int64_t qkv_width(const Plan& p, bool with_kv) { return (int64_t)(p.hpc + (with_kv ? 2 * p.kvc : 0)) * p.Dh; }
+
 upipe_status_t run_fwd(const Plan& p, const bf16* X, const bf16* Wqkv, const bf16* Wo, const int32_t* seg, bf16* Y,
                        float* lse, void* ws, cudaStream_t st) {
-  UPIPE_CUDA(launch_tile_table(p.S, p.causal, seg, at<char>(ws, p.table), st));
+  {
+    Timed t(UPIPE_K_TILE_TABLE, 0, p.S, 0, 0, 1, -1, st);
+    UPIPE_CUDA(launch_tile_table(p.S, p.causal, seg, at<char>(ws, p.table), st));
+  }
   const int sh = log2i(p.Dh);
   for (int c = 0; c < p.n_chunks; ++c) {
     const bool new_group = p.hpc >= p.g || (c * p.hpc) % p.g == 0;
-    UPIPE_CUDA(project_qkv(p, c, new_group, X, Wqkv, ws, st));
+    {
+      Timed t(UPIPE_K_QKV_PROJ, EPI_STORE_BF16, p.S, qkv_width(p, new_group), p.d, 1, c, st);
+      UPIPE_CUDA(project_qkv(p, c, new_group, X, Wqkv, ws, st));
+    }
     AttnArgs a = attn_args(p, c, ws, seg, lse);
-    UPIPE_CUDA(launch_attn_fwd(a, p.Dh, st));
+    {
+      Timed t(UPIPE_K_ATTN_FWD, 0, p.S, p.hpc, p.Dh, 1, c, st);
+      UPIPE_CUDA(launch_attn_fwd(a, p.Dh, st));
+    }
     // Y (+)= O_c * Wo_c^T
     TcGemmArgs g{};
     g.M = p.S; g.N = p.d; g.K = (int64_t)p.hpc * p.Dh;
@@ -263,15 +317,24 @@ upipe_status_t run_fwd(const Plan& p, const bf16* X, const bf16* Wqkv, const bf1
     g.b = op2d(Wo + (int64_t)c * p.hpc * p.Dh, (uint64_t)p.hpc * p.Dh, p.d, (uint64_t)p.Hq * p.Dh, 1);  // Wo_c
     g.epi = accum_epi(p, c);
     set_accum_out(g.c, p, g.epi, Y, p.yacc ? at<float>(ws, p.yacc) : nullptr);
-    UPIPE_CUDA(launch_gemm_tc(g, 1, nullptr, st));
-    UPIPE_CUDA(accum_finish(p, c, p.yacc ? at<float>(ws, p.yacc) : nullptr, Y, st));
+    {
+      Timed t(UPIPE_K_O_PROJ, g.epi, g.M, g.N, g.K, 1, c, st);
+      UPIPE_CUDA(launch_gemm_tc(g, 1, nullptr, st));
+    }
+    if (finishes_accum(p, c)) {
+      Timed t(UPIPE_K_CONVERT, 0, p.S * p.d, 1, 1, 1, c, st);
+      UPIPE_CUDA(accum_finish(p, c, p.yacc ? at<float>(ws, p.yacc) : nullptr, Y, st));
+    }
   }
   return UPIPE_OK;
 }
 
 upipe_status_t run_bwd(const Plan& p, const bf16* X, const bf16* Wqkv, const bf16* Wo, const int32_t* seg,
                        const bf16* dY, const float* lse, bf16* dX, float* dWqkv, float* dWo, void* ws, cudaStream_t st) {
-  UPIPE_CUDA(launch_tile_table(p.S, p.causal, seg, at<char>(ws, p.table), st));
+  {
+    Timed t(UPIPE_K_TILE_TABLE, 0, p.S, 0, 0, 1, -1, st);
+    UPIPE_CUDA(launch_tile_table(p.S, p.causal, seg, at<char>(ws, p.table), st));
+  }
   const int sh = log2i(p.Dh);
   const int64_t HD = (int64_t)p.Hq * p.Dh;
   float* split = p.split ? at<float>(ws, p.split) : nullptr;
@@ -279,8 +342,12 @@ upipe_status_t run_bwd(const Plan& p, const bf16* X, const bf16* Wqkv, const bf1
     const bool new_group = p.hpc >= p.g || (c * p.hpc) % p.g == 0;
     const bool end_group = p.hpc >= p.g || ((c + 1) * p.hpc) % p.g == 0;
     const int kv0 = (c * p.hpc) / p.g;
-    UPIPE_CUDA(project_qkv(p, c, new_group, X, Wqkv, ws, st));
+    {
+      Timed t(UPIPE_K_QKV_PROJ, EPI_STORE_BF16, p.S, qkv_width(p, new_group), p.d, 1, c, st);
+      UPIPE_CUDA(project_qkv(p, c, new_group, X, Wqkv, ws, st));
+    }
     if (new_group && p.hpc < p.g) {
+      Timed t(UPIPE_K_ZERO, 0, 2 * p.S * p.Dh, 1, 1, 1, c, st);
       UPIPE_CUDA(launch_zero(at<char>(ws, p.dkacc), (int64_t)p.S * p.Dh * 4, st));
       UPIPE_CUDA(launch_zero(at<char>(ws, p.dvacc), (int64_t)p.S * p.Dh * 4, st));
     }
@@ -292,12 +359,16 @@ upipe_status_t run_bwd(const Plan& p, const bf16* X, const bf16* Wqkv, const bf1
       for (int hl = 0; hl < p.hpc; ++hl) g.c.blk[hl] = at<bf16>(ws, p.dO) + (int64_t)hl * p.S * p.Dh;
       g.c.ld = p.Dh; g.c.blk_shift = sh; g.c.blk_dim = 1;
       g.epi = EPI_STORE_BF16;
+      Timed t(UPIPE_K_DO_PROJ, g.epi, g.M, g.N, g.K, 1, c, st);
       UPIPE_CUDA(launch_gemm_tc(g, 1, nullptr, st));
     }
     AttnArgs a = attn_args(p, c, ws, seg, const_cast<float*>(lse));
     a.dO = at<bf16>(ws, p.dO);
     a.D = at<float>(ws, p.D);
-    UPIPE_CUDA(launch_attn_recompute(a, p.Dh, st));
+    {
+      Timed t(UPIPE_K_RECOMPUTE, 0, p.S, p.hpc, p.Dh, 1, c, st);
+      UPIPE_CUDA(launch_attn_recompute(a, p.Dh, st));
+    }
     {  // dWo_c = dY^T * O_c   (split-K over S)
       TcGemmArgs g{};
       g.M = p.d; g.N = (int64_t)p.hpc * p.Dh; g.K = p.S;
@@ -305,6 +376,7 @@ upipe_status_t run_bwd(const Plan& p, const bf16* X, const bf16* Wqkv, const bf1
       g.b = op3d(at<bf16>(ws, p.o), p.Dh, p.S, p.hpc, 0, sh, 0);    // O_c: N blocked by head
       g.c.blk[0] = dWo + (int64_t)c * p.hpc * p.Dh; g.c.ld = HD; g.c.blk_shift = -1;
       g.epi = EPI_STORE_F32;
+      Timed t(UPIPE_K_DWO, g.epi, g.M, g.N, g.K, p.split_wo, c, st);
       UPIPE_CUDA(launch_gemm_tc(g, p.split_wo, split, st));
     }
     AttnBwdArgs b{};
@@ -316,9 +388,16 @@ upipe_status_t run_bwd(const Plan& p, const bf16* X, const bf16* Wqkv, const bf1
     b.dk_acc = p.dkacc ? at<float>(ws, p.dkacc) : nullptr;
     b.dv_acc = p.dvacc ? at<float>(ws, p.dvacc) : nullptr;
     b.nkv = p.kvc;
-    UPIPE_CUDA(launch_attn_bwd_dq(b, p.Dh, st));
-    UPIPE_CUDA(launch_attn_bwd_dkdv(b, p.Dh, st));
+    {
+      Timed t(UPIPE_K_BWD_DQ, 0, p.S, p.hpc, p.Dh, 1, c, st);
+      UPIPE_CUDA(launch_attn_bwd_dq(b, p.Dh, st));
+    }
+    {
+      Timed t(UPIPE_K_BWD_DKDV, 0, p.S, p.hpc, p.Dh, 1, c, st);
+      UPIPE_CUDA(launch_attn_bwd_dkdv(b, p.Dh, st));
+    }
     if (end_group && p.hpc < p.g) {
+      Timed t(UPIPE_K_CONVERT, 0, 2 * p.S * p.Dh, 1, 1, 1, c, st);
       UPIPE_CUDA(launch_f32_to_bf16(at<float>(ws, p.dkacc), at<bf16>(ws, p.dk), p.S * p.Dh, 1.f, st));
       UPIPE_CUDA(launch_f32_to_bf16(at<float>(ws, p.dvacc), at<bf16>(ws, p.dv), p.S * p.Dh, 1.f, st));
     }
@@ -342,8 +421,14 @@ upipe_status_t run_bwd(const Plan& p, const bf16* X, const bf16* Wqkv, const bf1
       for (int i = 0; i < nb; ++i) g.b.row_base[i] = blk_row[i];
       g.epi = accum_epi(p, c);
       set_accum_out(g.c, p, g.epi, dX, p.dxacc ? at<float>(ws, p.dxacc) : nullptr);
-      UPIPE_CUDA(launch_gemm_tc(g, 1, nullptr, st));
-      UPIPE_CUDA(accum_finish(p, c, p.dxacc ? at<float>(ws, p.dxacc) : nullptr, dX, st));
+      {
+        Timed t(UPIPE_K_DX_PROJ, g.epi, g.M, g.N, g.K, 1, c, st);
+        UPIPE_CUDA(launch_gemm_tc(g, 1, nullptr, st));
+      }
+      if (finishes_accum(p, c)) {
+        Timed t(UPIPE_K_CONVERT, 0, p.S * p.d, 1, 1, 1, c, st);
+        UPIPE_CUDA(accum_finish(p, c, p.dxacc ? at<float>(ws, p.dxacc) : nullptr, dX, st));
+      }
     }
     {  // dWqkv rows of these blocks = dQKV_block^T * X   (split-K over S)
       TcGemmArgs g{};
@@ -354,6 +439,7 @@ upipe_status_t run_bwd(const Plan& p, const bf16* X, const bf16* Wqkv, const bf1
       g.c.ld = p.d; g.c.blk_shift = sh; g.c.blk_dim = 0;
       g.epi = EPI_STORE_F32;
       const int split_k = nb == p.hpc ? p.split_wqkv_q : p.split_wqkv_full;
+      Timed t(UPIPE_K_DWQKV, g.epi, g.M, g.N, g.K, split_k, c, st);
       UPIPE_CUDA(launch_gemm_tc(g, split_k, split, st));
     }
   }
@@ -611,6 +697,39 @@ upipe_status_t upipe_attn_device_status(const void* buf, int32_t* code, void* st
   if (e != cudaSuccess) return cuda_status(e);
   *code = v;
   return UPIPE_OK;
+}
+
+upipe_status_t upipe_attn_timing_enable(int32_t on) {
+  if (on != 0 && on != 1) return UPIPE_ERR_INVALID_ARG;
+  g_timing_on.store(on, std::memory_order_relaxed);
+  return UPIPE_OK;
+}
+
+upipe_status_t upipe_attn_timing_collect(upipe_attn_timing_t* out, int32_t cap, int32_t* n) {
+  if (!n || cap < 0 || (cap > 0 && !out)) return UPIPE_ERR_INVALID_ARG;
+  std::vector<TimingRec> recs;
+  {
+    std::lock_guard<std::mutex> lock(g_timing_mutex);
+    recs.swap(g_timing);
+  }
+  upipe_status_t status = UPIPE_OK;
+  int32_t k = 0;
+  for (const TimingRec& r : recs) {
+    float ms = -1.f;
+    cudaError_t e = cudaEventSynchronize(r.e1);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, r.e0, r.e1);
+    if (e != cudaSuccess && status == UPIPE_OK) status = cuda_status(e);
+    if (k < cap) {
+      upipe_attn_timing_t& o = out[k];
+      o.kind = r.kind; o.epilogue = r.epi; o.split_k = r.split_k; o.chunk = r.chunk;
+      o.m = r.m; o.n = r.n; o.k = r.k; o.ms = ms;
+    }
+    ++k;
+    cudaEventDestroy(r.e0);
+    cudaEventDestroy(r.e1);
+  }
+  *n = k;
+  return status;
 }
 
 upipe_status_t upipe_attn_last_device_error(const void* ws, void* stream, int32_t* code) {

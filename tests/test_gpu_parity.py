@@ -297,3 +297,39 @@ def test_layer_step_replays_bit_exact_from_a_cuda_graph():
     torch.cuda.synchronize()
     for got, want in zip((Y, lse, dX, dW, dWo), eager):
         assert torch.equal(got, want)
+
+
+def test_per_launch_timing_logs_the_schedule():
+    """With timing on, every kernel launch of a forward and a backward is logged once with its
+    kind and shape, the results are unchanged, and turning it off logs nothing more."""
+    S, d, Hq, Hkv, Dh, hpc = 512, 256, 4, 2, 64, 1      # 4 chunks, 2 per KV group (hpc < g)
+    X, W, Wo, dY = layer_inputs(S, d, Hq, Hkv, Dh)
+    Xt, Wt, Wot, dYt = (bf16_tensor(x) for x in (X, W, Wo, dY))
+    layer = up.Layer(up.make_desc(S, d, Hq, Hkv, Dh, hpc, True))
+    Y0, lse0 = layer.forward(Xt, Wt, Wot)
+    torch.cuda.synchronize()
+    up.timing_records()
+    up.timing_enable(True)
+    try:
+        Y, lse = layer.forward(Xt, Wt, Wot)
+        dX, dW, dWo = layer.backward(Xt, Wt, Wot, None, dYt, lse)
+        torch.cuda.synchronize()
+    finally:
+        up.timing_enable(False)
+    recs = up.timing_records()
+    kinds = [r["kind"] for r in recs]
+    n_chunks = Hq // hpc
+    assert kinds.count("tile_table") == 2
+    assert kinds.count("attn_fwd") == n_chunks and kinds.count("recompute") == n_chunks
+    assert kinds.count("bwd_dq") == n_chunks and kinds.count("bwd_dkdv") == n_chunks
+    assert kinds.count("qkv_proj") == 2 * n_chunks and kinds.count("o_proj") == n_chunks
+    assert kinds.count("dx_proj") == n_chunks and kinds.count("dwqkv") == n_chunks
+    assert kinds.count("convert") == 2 + Hkv      # Y and dX sums once each, dK/dV at each group end
+    assert kinds.count("zero") == Hkv
+    assert all(r["ms"] >= 0 for r in recs)
+    epis = [r["epilogue"] for r in recs if r["kind"] == "o_proj"]
+    assert epis == [1] + [2] * (n_chunks - 1)     # first chunk stores the fp32 sum, later chunks add
+    assert torch.equal(Y, Y0) and torch.equal(lse, lse0)
+    layer.forward(Xt, Wt, Wot)
+    torch.cuda.synchronize()
+    assert up.timing_records() == []

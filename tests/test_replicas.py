@@ -52,3 +52,31 @@ def test_reference_arm_other_ranks_exit_without_work():
                         "--steps", "1", "--warmup", "0"], env=env, capture_output=True, text=True, timeout=300)
     assert r.returncode == 0
     assert r.stdout.strip() == ""
+
+
+def test_kernel_summary_accounting():
+    """The bench's per-kernel figures: GEMM FLOPs 2mnk and algorithmic bytes (A, B read once; C
+    written, and read as well when accumulated), conversion 6 bytes per element, attention FLOPs
+    from the visible pairs; the bound is the roofline whose time is longer."""
+    import upipe_inputs as ui
+    w = ui.workload("ulysses_1m")
+    peaks = {"hbm_gbs": 6000.0, "bf16_tflops": 2000.0, "bf16_tflops_sustained": 1500.0}
+    S, d, Dh = w.S, w.d, w.Dh
+    recs = [
+        {"kind": "o_proj", "epilogue": 2, "split_k": 1, "chunk": 1, "m": S, "n": d, "k": Dh, "ms": 10.0},
+        {"kind": "qkv_proj", "epilogue": 0, "split_k": 1, "chunk": 0, "m": S, "n": 3 * Dh, "k": d, "ms": 2.0},
+        {"kind": "convert", "epilogue": 0, "split_k": 1, "chunk": 3, "m": S * d, "n": 1, "k": 1, "ms": 4.0},
+        {"kind": "bwd_dkdv", "epilogue": 0, "split_k": 1, "chunk": 0, "m": S, "n": 1, "k": Dh, "ms": 500.0},
+    ]
+    out = {e["kernel"]: e for e in bench.summarize_kernels(recs, w, peaks, 4000.0)}
+    acc = out["o_proj (fp32 C += A B^T)"]
+    assert acc["bound"] == "hbm"                        # K = 128: the fp32 read-modify-write dominates
+    assert acc["bytes_per_launch"] == 2 * S * Dh + 2 * d * Dh + 8 * S * d
+    assert abs(acc["gbs"] - acc["bytes_per_launch"] / 1e-2 / 1e9) < 1e-6
+    qkv = out["qkv_proj (store bf16)"]
+    assert qkv["bound"] == "tensor" and abs(qkv["tflops"] - 2.0 * S * 3 * Dh * d / 2e-3 / 1e12) < 1e-9
+    assert qkv["peak"] == 1500.0                        # a step of 4 s runs under the power cap: sustained
+    assert out["convert"]["bytes_per_launch"] == 6 * S * d and out["convert"]["bound"] == "hbm"
+    dkdv = out["bwd_dkdv"]
+    assert abs(dkdv["tflops"] - 8 * Dh * S * (S + 1) // 2 / 0.5 / 1e12) < 1e-6
+    assert list(out)[0] == "bwd_dkdv"                   # sorted by time
