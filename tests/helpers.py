@@ -9,6 +9,12 @@ import upipe_inputs as ui
 OUT_MAX_ABS = 1e-2
 OUT_REL_FRO = 5e-3
 GRAD_REL_FRO = 1e-2
+# Full-size layers (hidden 4096): the output passes four bf16-stored stages, and an exact
+# implementation of those roundings is already 0.0156 from the fp64 oracle (max-abs beyond Y's
+# rounding) with a log-sum-exp 7.1e-3 off relative to max(1, |lse|); tests/test_error_budget.py
+# derives both and pins these bars to them.
+FULL_OUT_MAX_ABS = 2e-2
+FULL_LSE_REL = 1e-2
 
 
 def rel_fro(got, want):
