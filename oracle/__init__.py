@@ -217,13 +217,21 @@ def layer_forward_rows(X_rows, X_keys, key_index, rows, Wqkv, Wo, seg, Hq, Hkv, 
     positions `key_index` (sorted), which must include every key any of the rows can see.
     Returns Y [R, d] and LSE [Hq, R].
     """
+    Wq, Wk, Wv = split_wqkv(_widen(Wqkv), Hq, Hkv, Dh)
+    K, V = project_kv(X_keys, Wk, Wv, Hkv, Dh)
+    return layer_forward_rows_kv(X_rows, rows, K, V, key_index, Wqkv, Wo, seg, Hq, Hkv, Dh, causal, scale)
+
+
+def layer_forward_rows_kv(X_rows, rows, K, V, key_index, Wqkv, Wo, seg, Hq, Hkv, Dh, causal=True, scale=None):
+    """As layer_forward_rows, with the keys' K, V [Hkv, n, Dh] (float64, from project_kv) given
+    instead of their hidden states, so that a caller can project a multi-million-key sequence
+    block by block once and reuse it."""
     X_rows, Wqkv, Wo = _widen(X_rows), _widen(Wqkv), _widen(Wo)
     scale = default_scale(Dh) if scale is None else scale
     rows = np.asarray(rows, dtype=np.int64)
     key_index = np.asarray(key_index, dtype=np.int64)
-    Wq, Wk, Wv = split_wqkv(Wqkv, Hq, Hkv, Dh)
+    Wq, _, _ = split_wqkv(Wqkv, Hq, Hkv, Dh)
     Q = heads(X_rows @ Wq.T, Hq, Dh)
-    K, V = project_kv(X_keys, Wk, Wv, Hkv, Dh)
     g = Hq // Hkv
     O = np.zeros((Hq, rows.size, Dh))
     LSE = np.full((Hq, rows.size), NEG_INF)

@@ -41,7 +41,7 @@ def test_device_generator_matches_host_bit_for_bit():
         np.testing.assert_array_equal(got, ui.normal_bf16(n, tid, std, first=first))
 
 
-def run_layer(w, hpc, prefix, accum=0):
+def run_layer(w, hpc, prefix, accum=0, keep_x=False):
     S, d, Hq, Hkv, Dh = w.S, w.d, w.Hq, w.Hkv, w.Dh
     X = dev_fill((S, d), ui.TID_X, 1.0)
     W = dev_fill(((Hq + 2 * Hkv) * Dh, d), ui.TID_WQKV, ui.W_STD)
@@ -55,7 +55,48 @@ def run_layer(w, hpc, prefix, accum=0):
     dX, dW, dWo = layer.backward(X, W, Wo, seg_t, dY, lse)
     torch.cuda.synchronize()
     assert up.device_status(layer.ws_fwd) == 0 and up.device_status(layer.ws_bwd) == 0
+    if keep_x:
+        return seg, Y, lse, dX, dW, dWo, X
     return seg, Y, lse, dX, dW, dWo
+
+
+_KV_CACHE = {}
+
+
+def oracle_kv(w, X, block=1 << 18):
+    """float64 K, V [Hkv, S, Dh] of every key, projected by the oracle block by block from the
+    hidden states X [S, d].  X was written on the device by the shared seeded generator; its first
+    and last blocks are compared with the host generator bit for bit here, so what the oracle
+    projects are the generator's values.  Cached per workload (the same inputs serve every
+    heads_per_chunk)."""
+    if w.name in _KV_CACHE:
+        return _KV_CACHE[w.name]
+    S, d = X.shape
+    Wh = ui.normal_bf16((w.Hq + 2 * w.Hkv) * w.Dh * d, ui.TID_WQKV, ui.W_STD).reshape(-1, d)
+    _, Wk, Wv = orc.split_wqkv(orc.bf16_bits_to_f64(Wh), w.Hq, w.Hkv, w.Dh)
+    K = np.empty((w.Hkv, S, w.Dh))
+    V = np.empty((w.Hkv, S, w.Dh))
+    for a in range(0, S, block):
+        xb = X[a: a + block].cpu().view(torch.int16).numpy().view(np.uint16)
+        if a == 0 or a + block >= S:
+            np.testing.assert_array_equal(xb, ui.normal_bf16(xb.size, ui.TID_X, first=a * d).reshape(xb.shape))
+        K[:, a: a + xb.shape[0]], V[:, a: a + xb.shape[0]] = orc.project_kv(xb, Wk, Wv, w.Hkv, w.Dh)
+    _KV_CACHE.clear()
+    _KV_CACHE[w.name] = (K, V)
+    return K, V
+
+
+def check_rows_against_oracle(w, rows, Y, lse, K, V):
+    """Y and lse on the sampled rows against the oracle over every key (one causal segment)."""
+    _, W, Wo, _ = host_inputs(w, np.arange(1), 1)
+    Xr = ui.normal_bf16_rows(rows, w.d, ui.TID_X)
+    Y_ref, L_ref = orc.layer_forward_rows_kv(Xr, rows, K, V, np.arange(w.S), W, Wo, None, w.Hq, w.Hkv, w.Dh,
+                                             w.causal)
+    y = to_f64(Y[torch.from_numpy(rows).cuda()])
+    assert max_abs_bf16_out(y, Y_ref) <= FULL_OUT_MAX_ABS, max_abs_bf16_out(y, Y_ref)
+    assert rel_fro(y, Y_ref) <= OUT_REL_FRO, rel_fro(y, Y_ref)
+    lse_err = np.abs(to_f64(lse)[:, rows] - L_ref) / np.maximum(1.0, np.abs(L_ref))
+    assert lse_err.max() <= FULL_LSE_REL, lse_err.max()
 
 
 def all_finite(t, rows=1 << 18):
@@ -76,7 +117,8 @@ def host_inputs(w, rows_needed, prefix):
     return Xr, W, Wo, dYp
 
 
-@pytest.mark.parametrize("key,hpc,prefix", [("llama8b_32k", 8, 1024), ("packed_131k", 8, 2048)])
+@pytest.mark.parametrize("key,hpc,prefix", [("llama8b_32k", 8, 1024), ("llama8b_32k", 4, 1024),
+                                            ("llama8b_32k", 32, 1024), ("packed_131k", 8, 2048)])
 def test_full_size_layer(key, hpc, prefix):
     w = ui.workload(key)
     S = w.S
@@ -147,38 +189,36 @@ def test_full_size_tail_window_backward():
     assert rel_fro(to_f64(dWo), dWo_ref) <= GRAD_REL_FRO, rel_fro(to_f64(dWo), dWo_ref)
 
 
-def test_full_size_1m_share():
-    """The 1M-token share (4 query heads, 1 KV head, one chunk as benchmarked).  The oracle checks
-    sampled rows across the whole sequence (first, tile-boundary, middle, random and last rows;
-    K and V of all 2^20 keys projected in float64 block by block); causality makes the first T
-    rows of the 1M-token layer equal to a T-token layer on the same inputs (checked against a
-    separate 4096-token run of the library); all outputs are finite; and with dY zero past the
-    first P rows every gradient equals the oracle's on the first P tokens and dX rows >= P are
-    exactly zero."""
+@pytest.mark.parametrize("hpc", [4, 2, 1])
+def test_full_size_1m_share(hpc):
+    """The 1M-token share (4 query heads, 1 KV head) at every heads_per_chunk the benchmark sweeps:
+    4 (one chunk), 2 and 1 (chunks that hold part of the KV group, so dK / dV accumulate in fp32
+    across chunks and Y / dX in the fp32 workspace sums).  The oracle checks 64 sampled rows across
+    the whole sequence (first, tile-boundary, middle, last and random rows; K and V of all 2^20 keys
+    projected in float64 block by block); causality makes the first T rows of the 1M-token layer
+    equal to a T-token layer on the same inputs (checked against a separate 4096-token run of the
+    library); all outputs are finite; and with dY zero past the first P rows every gradient equals
+    the oracle's on the first P tokens and dX rows >= P are exactly zero."""
     w = ui.workload("ulysses_1m")
     S = w.S
-    hpc, prefix, T = 4, 1024, 4096
-    seg, Y, lse, dX, dW, dWo = run_layer(w, hpc, prefix)
+    prefix, T = 1024, 4096
+    torch.cuda.empty_cache()
+    seg, Y, lse, dX, dW, dWo, X = run_layer(w, hpc, prefix, keep_x=True)
     for t in (Y, lse, dX, dW, dWo):
         assert bool(torch.isfinite(t.float()).all())
     for a in range(prefix, S, 1 << 18):     # in slices: a whole-tensor count would need ~8 GB
         assert not bool((dX[a: a + (1 << 18)] != 0).any())
-    # oracle on sampled rows of the whole sequence
+    # oracle on 64 sampled rows of the whole sequence
+    fixed = [0, 1, 127, 128, 129, 1000, 2047, 2048, T - 129, T - 1, S // 2 - 1, S // 2, S // 2 + 1,
+             S - 257, S - 256, S - 129, S - 128, S - 127, S - 2, S - 1]
     rng = np.random.default_rng(1234)
-    rows = np.unique(np.concatenate([
-        [0, 1, 127, 128, 129, 1000, 2047, 2048, T - 129, T - 1, S // 2 - 1, S // 2, S // 2 + 1],
-        [S - 257, S - 256, S - 129, S - 128, S - 127, S - 2, S - 1],
-        rng.integers(0, S, size=12)]))
-    key_index = np.arange(0, S)
-    Xk = ui.normal_bf16(S * w.d, ui.TID_X).reshape(S, w.d)
-    _, W, Wo, dYp = host_inputs(w, np.arange(1), prefix)
-    Y_ref, L_ref = orc.layer_forward_rows(Xk[rows], Xk, key_index, rows, W, Wo, None, w.Hq, w.Hkv, w.Dh, w.causal)
-    del Xk
-    y = to_f64(Y[torch.from_numpy(rows).cuda()])
-    assert max_abs_bf16_out(y, Y_ref) <= FULL_OUT_MAX_ABS, max_abs_bf16_out(y, Y_ref)
-    assert rel_fro(y, Y_ref) <= OUT_REL_FRO, rel_fro(y, Y_ref)
-    lse_err = np.abs(to_f64(lse)[:, rows] - L_ref) / np.maximum(1.0, np.abs(L_ref))
-    assert lse_err.max() <= FULL_LSE_REL, lse_err.max()
+    rows = set(fixed)
+    while len(rows) < 64:
+        rows.add(int(rng.integers(0, S)))
+    rows = np.array(sorted(rows))
+    K, V = oracle_kv(w, X)
+    del X
+    check_rows_against_oracle(w, rows, Y, lse, K, V)
     # causality: the first T rows equal a T-token layer's (same tiles, same order of work)
     small = up.Layer(up.make_desc(T, w.d, w.Hq, w.Hkv, w.Dh, hpc, w.causal))
     Wd = dev_fill(((w.Hq + 2 * w.Hkv) * w.Dh, w.d), ui.TID_WQKV, ui.W_STD)
@@ -188,6 +228,7 @@ def test_full_size_1m_share():
     assert max_abs(to_f64(Y[:T]), to_f64(Ys)) <= 1e-6 * max(1.0, float(Ys.float().abs().max()))
     assert max_abs(to_f64(lse[:, :T]), to_f64(lses)) <= 1e-6 * max(1.0, float(lses.abs().max()))
     # backward on the prefix
+    _, W, Wo, dYp = host_inputs(w, np.arange(1), prefix)
     Xp = ui.normal_bf16_rows(np.arange(prefix), w.d, ui.TID_X)
     dX_ref, dW_ref, dWo_ref = orc.layer_backward(Xp, W, Wo, None, dYp, w.Hq, w.Hkv, w.Dh, w.causal)
     assert rel_fro(to_f64(dX[:prefix]), dX_ref) <= GRAD_REL_FRO, rel_fro(to_f64(dX[:prefix]), dX_ref)
@@ -195,31 +236,30 @@ def test_full_size_1m_share():
     assert rel_fro(to_f64(dWo), dWo_ref) <= GRAD_REL_FRO, rel_fro(to_f64(dWo), dWo_ref)
 
 
-def test_full_size_5m_share():
-    """The 5M-token 32B-shaped share (8 query heads, 1 KV head, hidden 5120), two heads per chunk
-    with bf16 partial sums (fp32 sums would not fit beside the caller's 205 GB of X, Y, dY and dX).
-    Checked as the 1M share is, except that the oracle rows lie in the first 4096 tokens: a row near
-    the end would need the float64 projection of all five million keys.  Those rows against the
-    oracle; the first T rows against a separate T-token run with the same chunking (causality);
-    finite outputs; dX exactly zero past the first P rows, where dY is zero; every gradient against
-    the oracle on the first P tokens."""
+@pytest.mark.parametrize("hpc", [2, 1])
+def test_full_size_5m_share(hpc):
+    """The 5M-token 32B-shaped share (8 query heads, 1 KV head, hidden 5120) with one and with two
+    heads per chunk and bf16 partial sums (fp32 sums would not fit beside the caller's 205 GB of X,
+    Y, dY and dX).  The oracle checks rows at the start, in the middle, near the end and in the
+    ragged last tile (S mod 128 = 64: rows S-64 .. S-1), each against every key it sees (K and V of
+    all five million keys projected in float64 block by block); the first T rows against a separate
+    T-token run with the same chunking (causality); finite outputs; dX exactly zero past the first
+    P rows, where dY is zero; every gradient against the oracle on the first P tokens."""
     w = ui.workload("share32b_5m")
-    hpc, prefix, T = 2, 1024, 4096
+    S = w.S
+    prefix, T = 1024, 4096
     torch.cuda.empty_cache()  # the earlier full-size tests' cached blocks: this one needs ~239 GB
-    seg, Y, lse, dX, dW, dWo = run_layer(w, hpc, prefix, accum=1)
+    seg, Y, lse, dX, dW, dWo, X = run_layer(w, hpc, prefix, accum=1, keep_x=True)
     assert all_finite(Y) and all_finite(dX)
     for t in (lse, dW, dWo):
         assert bool(torch.isfinite(t.float()).all())
     assert all_zero_from(dX, prefix)
-    rows = np.array([0, 1, 127, 128, 129, 1000, 2047, 2048, T - 129, T - 1])
-    key_index = np.arange(0, T)
-    Xk, W, Wo, dYp = host_inputs(w, key_index, prefix)
-    Y_ref, L_ref = orc.layer_forward_rows(Xk[rows], Xk, key_index, rows, W, Wo, None, w.Hq, w.Hkv, w.Dh, w.causal)
-    y = to_f64(Y[torch.from_numpy(rows).cuda()])
-    assert max_abs_bf16_out(y, Y_ref) <= FULL_OUT_MAX_ABS, max_abs_bf16_out(y, Y_ref)
-    assert rel_fro(y, Y_ref) <= OUT_REL_FRO, rel_fro(y, Y_ref)
-    lse_err = np.abs(to_f64(lse)[:, rows] - L_ref) / np.maximum(1.0, np.abs(L_ref))
-    assert lse_err.max() <= FULL_LSE_REL, lse_err.max()
+    assert S % 128 == 64
+    rows = np.array([0, 1, 127, 128, 129, 1000, 2047, 2048, T - 129, T - 1, S // 2, 1 << 22,
+                     S - 193, S - 129, S - 65, S - 64, S - 63, S - 33, S - 2, S - 1])
+    K, V = oracle_kv(w, X)
+    del X
+    check_rows_against_oracle(w, rows, Y, lse, K, V)
     small = up.Layer(up.make_desc(T, w.d, w.Hq, w.Hkv, w.Dh, hpc, w.causal, 1))
     Wd = dev_fill(((w.Hq + 2 * w.Hkv) * w.Dh, w.d), ui.TID_WQKV, ui.W_STD)
     Wod = dev_fill((w.d, w.Hq * w.Dh), ui.TID_WO, ui.W_STD)
@@ -227,6 +267,7 @@ def test_full_size_5m_share():
     torch.cuda.synchronize()
     assert max_abs(to_f64(Y[:T]), to_f64(Ys)) <= 1e-6 * max(1.0, float(Ys.float().abs().max()))
     assert max_abs(to_f64(lse[:, :T]), to_f64(lses)) <= 1e-6 * max(1.0, float(lses.abs().max()))
+    _, W, Wo, dYp = host_inputs(w, np.arange(1), prefix)
     Xp = ui.normal_bf16_rows(np.arange(prefix), w.d, ui.TID_X)
     dX_ref, dW_ref, dWo_ref = orc.layer_backward(Xp, W, Wo, None, dYp, w.Hq, w.Hkv, w.Dh, w.causal)
     assert rel_fro(to_f64(dX[:prefix]), dX_ref) <= GRAD_REL_FRO, rel_fro(to_f64(dX[:prefix]), dX_ref)
