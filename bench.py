@@ -45,6 +45,7 @@ def parse():
     ap.add_argument("--no-graph", action="store_true", help="launch the step's kernels one by one instead of replaying "
                     "a CUDA graph of them")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-offload", action="store_true", help="skip the leg with X and dY in pinned host memory")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--sample-tokens", type=int, default=1024, help="oracle sample length (CPU legs)")
     ap.add_argument("--kernel", default=None, choices=["fwd", "recompute", "dq", "dkdv", "lse_merge", "ring", "ring_bwd"],
@@ -477,6 +478,80 @@ def main():
         print(json.dumps({"kernel": args.kernel, "workload": w.name, "heads": args.hpc, "ms": ms_k, "tflops": tf}))
         return
 
+    # ---------------- hpc sweep first, on a clean device: speed and peak memory vs chunk size (plus
+    # the HBM-bound kernels of the chunked schedule: the fp32 accumulating projections and the
+    # fp32 -> bf16 pass)
+    import gc
+    sweep = []
+    if not args.no_sweep:   # every rank runs it (its timing takes the job's barriers); rank 0 reports
+        for h in w.hpc_sweep:
+            gc.collect()
+            torch.cuda.synchronize()
+            torch.cuda.empty_cache()
+            before = torch.cuda.memory_allocated(dev)      # the inputs X, Wqkv, Wo, dY (and segments)
+            torch.cuda.reset_peak_memory_stats(dev)
+            dsc, lay, stp, _, stp_on = make_layer(h)
+            eager = stp
+            gr = None if args.no_graph else graph_of(stp_on)[0]
+            if gr is not None:
+                stp = gr.replay
+            stp()
+            t = time_steps(stp, 3 if w.S < (1 << 19) else 2)
+            pk = torch.cuda.max_memory_allocated(dev)
+            kern = instrumented_step(up, eager, w, peaks, t)
+            sweep.append({"heads_per_chunk": h, "ms_per_step": round(t, 3),
+                          "tflops": round(flops / (t * 1e-3) / 1e12, 2),
+                          "peak_hbm_gb": round(pk / 1e9, 3),
+                          "layer_peak_gb": round((pk - before) / 1e9, 3),
+                          "workspace_gb": round((up.workspace_bytes(dsc, 0) + up.workspace_bytes(dsc, 1)) / 1e9, 3),
+                          "inputs_gb": round(before / 1e9, 3),
+                          "hbm_kernels": [k for k in kern if k["bound"] == "hbm"]})
+            del dsc, lay, stp, gr, stp_on, eager, _  # the graph and the step closures hold the layer's workspace
+        gc.collect()
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+
+    # ---------------- CPU offload of the layer's inputs: X and dY in pinned host memory, streamed in
+    # 65,536-row blocks; throughput and device peak against the resident layer at the same chunking
+    offload = None
+    if not args.no_offload:
+        gc.collect()
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        hX = torch.empty(X.shape, dtype=X.dtype, pin_memory=True)
+        hdY = torch.empty(dY.shape, dtype=dY.dtype, pin_memory=True)
+        hX.copy_(X)
+        hdY.copy_(dY)
+        before = torch.cuda.memory_allocated(dev)
+        torch.cuda.reset_peak_memory_stats(dev)
+        odesc = up.make_desc(S, d, Hq, Hkv, Dh, args.hpc, w.causal, args.accum_mode)
+        ows = torch.empty(max(up.workspace_bytes_offload(odesc, 0), up.workspace_bytes_offload(odesc, 1)),
+                          dtype=torch.uint8, device=dev)
+        oY, odX = torch.empty_like(X), torch.empty_like(X)
+        olse = torch.empty(Hq, S, dtype=torch.float32, device=dev)
+        odW = torch.empty(W.shape, dtype=torch.float32, device=dev)
+        odWo = torch.empty(Wo.shape, dtype=torch.float32, device=dev)
+
+        def ostep():
+            up.fwd_offload(odesc, hX, W, Wo, seg_t, oY, olse, ows, 0, stream)
+            up.bwd_offload(odesc, hX, W, Wo, seg_t, hdY, olse, odX, odW, odWo, ows, 0, stream)
+
+        ostep()
+        t_off = max_over_ranks(time_steps(ostep, 2 if w.S >= (1 << 19) else 3), dev)
+        pk = torch.cuda.max_memory_allocated(dev)
+        inputs = sum(x.numel() * x.element_size() for x in (X, dY))
+        held = pk - before + (before - inputs)          # everything on the device but X and dY
+        n_chunks = Hq // args.hpc
+        offload = {"heads_per_chunk": args.hpc, "stage_rows": 65536, "ms_per_step": t_off,
+                   "tflops": job_value(flops, world, t_off), "device_peak_gb": round(held / 1e9, 3),
+                   "h2d_bytes_per_step": n_chunks * inputs // 2 + 2 * n_chunks * inputs,
+                   "what": "X and dY in pinned host memory, staged in row blocks by the library (upipe_attn_fwd_offload "
+                           "/ upipe_attn_bwd_offload); device peak excludes X and dY"}
+        del ows, oY, odX, olse, odW, odWo, hX, hdY
+        gc.collect()
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+
     # ---------------- main timed run
     torch.cuda.reset_peak_memory_stats(dev)
     desc, layer, step, outs, step_on = make_layer(args.hpc)
@@ -510,6 +585,91 @@ def main():
     # same launches as a timed step, each bracketed by CUDA events on the step's stream
     step_kernels = instrumented_step(up, step, w, peaks, ms)
 
+    # ---------------- end to end through the C-ABI with host buffers
+    # Every step uploads its X, Wqkv, Wo and dY from pinned host memory and reads Y, dX, dWqkv
+    # and dWo back, all inside the timed region.  The copies run on two copy streams beside
+    # the compute: dY and the next step's X / Wqkv / Wo (double-buffered) upload while the
+    # forward runs, Y downloads while the backward runs, and dX / dWqkv / dWo download while
+    # the next step's forward runs.  Step 0 uploads its own inputs before its forward; the last
+    # step prefetches nothing.
+    e2e = None
+    if not args.no_e2e:
+        Y, lse, dX, dW, dWo = outs
+
+        def pin(t):
+            return torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+
+        hX, hW, hWo, hdY = pin(X), pin(W), pin(Wo), pin(dY)
+        for h, t in ((hX, X), (hW, W), (hWo, Wo), (hdY, dY)):
+            h.copy_(t)
+        hY, hdX, hdW, hdWo = pin(Y), pin(dX), pin(dW), pin(dWo)
+        ins = [(X, W, Wo), (torch.empty_like(X), torch.empty_like(W), torch.empty_like(Wo))]
+        cin, cout = torch.cuda.Stream(), torch.cuda.Stream()
+        in_ready = [torch.cuda.Event(), torch.cuda.Event()]
+        dy_ready, fwd_done, bwd_done = torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()
+        y_done, out_done = torch.cuda.Event(), torch.cuda.Event()
+
+        def upload(b):
+            for dst, src in zip(ins[b], (hX, hW, hWo)):
+                dst.copy_(src, non_blocking=True)
+            in_ready[b].record(cin)
+
+        def e2e_run(n):
+            """n steps; returns ms per step (CUDA events on the compute stream, which waits
+            for the last download before the end event)."""
+            barrier()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            bwd_done.record(stream)
+            out_done.record(stream)
+            y_done.record(stream)
+            cin.wait_stream(stream)
+            cout.wait_stream(stream)
+            with torch.cuda.stream(cin):
+                upload(0)
+            for k in range(n):
+                b = k & 1
+                Xb, Wb, Wob = ins[b]
+                stream.wait_event(in_ready[b])
+                stream.wait_event(y_done)             # the previous step's Y has been read back
+                up.fwd(desc, Xb, Wb, Wob, seg_t, Y, lse, layer.ws_fwd, stream)
+                fwd_done.record(stream)
+                with torch.cuda.stream(cin):
+                    cin.wait_event(bwd_done)          # the previous backward read dY and ins[1 - b]
+                    dY.copy_(hdY, non_blocking=True)
+                    dy_ready.record(cin)
+                    if k + 1 < n:
+                        upload(1 - b)
+                with torch.cuda.stream(cout):
+                    cout.wait_event(fwd_done)
+                    hY.copy_(Y, non_blocking=True)
+                    y_done.record(cout)
+                stream.wait_event(dy_ready)
+                stream.wait_event(out_done)           # the previous results have been read back
+                up.bwd(desc, Xb, Wb, Wob, seg_t, dY, lse, dX, dW, dWo, layer.ws_bwd, stream)
+                bwd_done.record(stream)
+                with torch.cuda.stream(cout):
+                    cout.wait_event(bwd_done)
+                    hdX.copy_(dX, non_blocking=True)
+                    hdW.copy_(dW, non_blocking=True)
+                    hdWo.copy_(dWo, non_blocking=True)
+                    out_done.record(cout)
+            stream.wait_event(out_done)
+            e1.record(stream)
+            barrier()
+            return e0.elapsed_time(e1) / n
+
+        e2e_run(1 if ms > 2000 else 2)
+        n_e2e = max(2, args.steps // 4) if ms > 2000 else max(3, args.steps // 2)
+        t = max_over_ranks(e2e_run(n_e2e), dev)
+        h2d = sum(x.numel() * x.element_size() for x in (hX, hW, hWo, hdY))
+        d2h = sum(x.numel() * x.element_size() for x in (hY, hdX, hdW, hdWo))
+        e2e = {"value": job_value(flops, world, t), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": t, "steps": n_e2e,
+               "overlap": "dY and the next step's inputs upload during the forward; Y downloads during the "
+                          "backward; dX, dWqkv, dWo download during the next forward"}
+        del ins
+
     result = {}
     if rank == 0:
         # ---------------- the dominant kernel of the step against its roofline
@@ -522,119 +682,6 @@ def main():
                     "how": "executed MMA FLOPs of its launches in one step / their CUDA-event durations inside "
                            "that step"}
 
-        # ---------------- hpc sweep: speed and peak memory vs chunk size (plus the HBM-bound kernels
-        # of the chunked schedule: the fp32 accumulating projections and the fp32 -> bf16 pass)
-        sweep = []
-        if not args.no_sweep:
-            del layer, graph, timed, step, step_on
-            for h in w.hpc_sweep:
-                torch.cuda.synchronize()
-                torch.cuda.empty_cache()
-                torch.cuda.reset_peak_memory_stats(dev)
-                before = torch.cuda.memory_allocated(dev)
-                dsc, lay, stp, _, stp_on = make_layer(h)
-                eager = stp
-                gr = None if args.no_graph else graph_of(stp_on)[0]
-                if gr is not None:
-                    stp = gr.replay
-                stp()
-                t = time_steps(stp, 3 if ms < 2000 else 2)
-                pk = torch.cuda.max_memory_allocated(dev) / 1e9
-                kern = instrumented_step(up, eager, w, peaks, t)
-                sweep.append({"heads_per_chunk": h, "ms_per_step": round(t, 3),
-                              "tflops": round(flops / (t * 1e-3) / 1e12, 2), "peak_hbm_gb": round(pk, 3),
-                              "workspace_gb": round((up.workspace_bytes(dsc, 0) + up.workspace_bytes(dsc, 1)) / 1e9, 3),
-                              "inputs_outputs_gb": round(before / 1e9, 3),
-                              "hbm_kernels": [k for k in kern if k["bound"] == "hbm"]})
-                del lay, stp, gr, stp_on, eager  # the graph and the step closures hold the layer's workspace
-            torch.cuda.empty_cache()
-            desc, layer, step, outs, step_on = make_layer(args.hpc)
-
-        # ---------------- end to end through the C-ABI with host buffers
-        # Every step uploads its X, Wqkv, Wo and dY from pinned host memory and reads Y, dX, dWqkv
-        # and dWo back, all inside the timed region.  The copies run on two copy streams beside
-        # the compute: dY and the next step's X / Wqkv / Wo (double-buffered) upload while the
-        # forward runs, Y downloads while the backward runs, and dX / dWqkv / dWo download while
-        # the next step's forward runs.  Step 0 uploads its own inputs before its forward; the last
-        # step prefetches nothing.
-        e2e = None
-        if not args.no_e2e:
-            Y, lse, dX, dW, dWo = outs
-
-            def pin(t):
-                return torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-
-            hX, hW, hWo, hdY = pin(X), pin(W), pin(Wo), pin(dY)
-            for h, t in ((hX, X), (hW, W), (hWo, Wo), (hdY, dY)):
-                h.copy_(t)
-            hY, hdX, hdW, hdWo = pin(Y), pin(dX), pin(dW), pin(dWo)
-            ins = [(X, W, Wo), (torch.empty_like(X), torch.empty_like(W), torch.empty_like(Wo))]
-            cin, cout = torch.cuda.Stream(), torch.cuda.Stream()
-            in_ready = [torch.cuda.Event(), torch.cuda.Event()]
-            dy_ready, fwd_done, bwd_done = torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()
-            y_done, out_done = torch.cuda.Event(), torch.cuda.Event()
-
-            def upload(b):
-                for dst, src in zip(ins[b], (hX, hW, hWo)):
-                    dst.copy_(src, non_blocking=True)
-                in_ready[b].record(cin)
-
-            def e2e_run(n):
-                """n steps; returns ms per step (CUDA events on the compute stream, which waits
-                for the last download before the end event)."""
-                barrier()
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                bwd_done.record(stream)
-                out_done.record(stream)
-                y_done.record(stream)
-                cin.wait_stream(stream)
-                cout.wait_stream(stream)
-                with torch.cuda.stream(cin):
-                    upload(0)
-                for k in range(n):
-                    b = k & 1
-                    Xb, Wb, Wob = ins[b]
-                    stream.wait_event(in_ready[b])
-                    stream.wait_event(y_done)             # the previous step's Y has been read back
-                    up.fwd(desc, Xb, Wb, Wob, seg_t, Y, lse, layer.ws_fwd, stream)
-                    fwd_done.record(stream)
-                    with torch.cuda.stream(cin):
-                        cin.wait_event(bwd_done)          # the previous backward read dY and ins[1 - b]
-                        dY.copy_(hdY, non_blocking=True)
-                        dy_ready.record(cin)
-                        if k + 1 < n:
-                            upload(1 - b)
-                    with torch.cuda.stream(cout):
-                        cout.wait_event(fwd_done)
-                        hY.copy_(Y, non_blocking=True)
-                        y_done.record(cout)
-                    stream.wait_event(dy_ready)
-                    stream.wait_event(out_done)           # the previous results have been read back
-                    up.bwd(desc, Xb, Wb, Wob, seg_t, dY, lse, dX, dW, dWo, layer.ws_bwd, stream)
-                    bwd_done.record(stream)
-                    with torch.cuda.stream(cout):
-                        cout.wait_event(bwd_done)
-                        hdX.copy_(dX, non_blocking=True)
-                        hdW.copy_(dW, non_blocking=True)
-                        hdWo.copy_(dWo, non_blocking=True)
-                        out_done.record(cout)
-                stream.wait_event(out_done)
-                e1.record(stream)
-                barrier()
-                return e0.elapsed_time(e1) / n
-
-            e2e_run(1 if ms > 2000 else 2)
-            n_e2e = max(2, args.steps // 4) if ms > 2000 else max(3, args.steps // 2)
-            t = e2e_run(n_e2e)
-            h2d = sum(x.numel() * x.element_size() for x in (hX, hW, hWo, hdY))
-            d2h = sum(x.numel() * x.element_size() for x in (hY, hdX, hdW, hdWo))
-            e2e = {"value": flops / (t * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                   "d2h_bytes_per_step": d2h, "ms_per_step": t, "steps": n_e2e,
-                   "overlap": "dY and the next step's inputs upload during the forward; Y downloads during the "
-                              "backward; dX, dWqkv, dWo download during the next forward"}
-            del ins
-
         # ---------------- CPU baseline: the oracle on a bounded sample
         cpu = None
         if not args.no_cpu and world == 1:
@@ -643,6 +690,11 @@ def main():
                    "sample": f"oracle fp64 forward+backward on the first {Ssamp} tokens of {w.name}; "
                              f"{dt:.2f} s for {fl / 1e12:.4f} TFLOP"}
 
+        if offload is not None:
+            offload["time_vs_resident"] = offload["ms_per_step"] / ms_all
+            res = next((e for e in sweep if e["heads_per_chunk"] == args.hpc), None)
+            if res is not None:
+                offload["resident_device_peak_gb"] = res["peak_hbm_gb"]
         sustained = ms > 500.0
         peak_step = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
         x_mb = S * d * 2 / 1e6
@@ -664,6 +716,7 @@ def main():
             "roofline": roofline,
             "step_kernels": step_kernels,
             "hpc_sweep": sweep,
+            "offload": offload,
             "e2e": e2e,
             "cpu_baseline": cpu,
             "gpu_launches": launches,

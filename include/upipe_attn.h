@@ -141,6 +141,33 @@ upipe_status_t upipe_attn_bwd(const upipe_attn_desc_t* desc, const uint16_t* X, 
                               uint16_t* dX, float* dWqkv, float* dWo, void* ws, size_t ws_bytes,
                               void* stream);
 
+/* CPU offload of the layer's inputs ("Road to 5 Million Tokens" podcast summary, chapter on moving
+ * part of the inputs to the CPU; neuro-slop.ru transcript, implementation plan step 2: block
+ * inputs offloaded to the CPU).  Same layer, same results as upipe_attn_fwd / upipe_attn_bwd, but
+ * X (and, in the backward, dY) stay in page-locked host memory and never occupy device memory as a
+ * whole: the library brings them in `stage_rows` rows at a time (0 selects 65536; otherwise a
+ * multiple of 128) into two staging buffers per tensor inside the workspace, one
+ * cudaMemcpyAsync per block on a copy stream of its own, issued one block ahead so that copies
+ * overlap the projections.  Per chunk the forward streams X once (the Q/K/V projection); the
+ * backward streams X and dY twice (the Q/K/V and dO projections before the attention kernels,
+ * the weight gradients dWo and dWqkv after them, summed block by block in a fixed order).
+ *   X_host, dY_host  page-locked host bf16 [S, d] (cudaHostAlloc or cudaHostRegister); anything
+ *                    else is rejected with UPIPE_ERR_INVALID_ARG before any launch
+ *   ws               device workspace of upipe_attn_workspace_size_offload(desc, pass, stage_rows)
+ *                    bytes (the regular workspace plus 2 or 4 staging buffers of stage_rows x d)
+ * Y, lse and dX are bit-identical to the regular calls'; dWqkv and dWo equal theirs to rounding
+ * (their sums over S are split at other places).  The host buffers must not change until the
+ * call's work on `stream` has completed. */
+upipe_status_t upipe_attn_workspace_size_offload(const upipe_attn_desc_t* desc, int pass, int64_t stage_rows,
+                                                 size_t* bytes);
+upipe_status_t upipe_attn_fwd_offload(const upipe_attn_desc_t* desc, const uint16_t* X_host, const uint16_t* Wqkv,
+                                      const uint16_t* Wo, const int32_t* seg, uint16_t* Y, float* lse, void* ws,
+                                      size_t ws_bytes, int64_t stage_rows, void* stream);
+upipe_status_t upipe_attn_bwd_offload(const upipe_attn_desc_t* desc, const uint16_t* X_host, const uint16_t* Wqkv,
+                                      const uint16_t* Wo, const int32_t* seg, const uint16_t* dY_host, const float* lse,
+                                      uint16_t* dX, float* dWqkv, float* dWo, void* ws, size_t ws_bytes,
+                                      int64_t stage_rows, void* stream);
+
 /* Forward pass for callers that cannot allocate device memory (for example code recorded into
  * someone else's CUDA graph, or a plugin that only receives input and output pointers).  The
  * pages describe nothing like it; it is a convenience of this library.  Same arguments and
@@ -274,6 +301,19 @@ typedef struct {
 } upipe_attn_timing_t;
 upipe_status_t upipe_attn_timing_enable(int32_t on);
 upipe_status_t upipe_attn_timing_collect(upipe_attn_timing_t* out, int32_t cap, int32_t* n);
+
+/* Limit of every bounded device-side wait of the library's kernels, in nanoseconds (0 restores the
+ * default of 4 s; at most 60 s).  Each kernel receives the value in effect when it is launched.
+ * When a wait runs out, the kernel raises UPIPE_ERR_DEVICE_TIMEOUT in the error word of its
+ * workspace or table and returns instead of hanging.  A diagnostic with no counterpart on the
+ * pages: shorter limits are for testing the timeout path with upipe_attn_wait_probe. */
+upipe_status_t upipe_attn_set_wait_limit_ns(uint64_t ns);
+
+/* Runs the library's bounded wait on a barrier that nothing completes (arrive = 0) or on one it
+ * completes itself first (arrive = 1), under the current wait limit.  `buf` is a device buffer
+ * of at least 32 bytes laid out as a table header; its error word is cleared, then set to
+ * UPIPE_ERR_DEVICE_TIMEOUT if the wait runs out (read it with upipe_attn_device_status). */
+upipe_status_t upipe_attn_wait_probe(void* buf, size_t bytes, int32_t arrive, void* stream);
 
 /* Number of GPU kernels this library has launched in the process so far (every entry point
  * counts its own launches; a diagnostic with no counterpart in the method).  The difference of

@@ -24,7 +24,9 @@ EXPORTS = ["upipe_attn_status_string", "upipe_attn_last_error_string", "upipe_at
            "upipe_attn_core_recompute", "upipe_attn_core_bwd_dq", "upipe_attn_core_bwd_dkdv", "upipe_attn_gemm_nt",
            "upipe_attn_device_status", "upipe_attn_fwd_no_alloc", "upipe_attn_launch_count", "upipe_attn_lse_merge",
            "upipe_attn_ring_bwd_prep", "upipe_attn_accumulate", "upipe_attn_last_device_error",
-           "upipe_attn_no_alloc_device_status", "upipe_attn_timing_enable", "upipe_attn_timing_collect"]
+           "upipe_attn_no_alloc_device_status", "upipe_attn_timing_enable", "upipe_attn_timing_collect",
+           "upipe_attn_workspace_size_offload", "upipe_attn_fwd_offload", "upipe_attn_bwd_offload",
+           "upipe_attn_set_wait_limit_ns", "upipe_attn_wait_probe"]
 
 # kinds of the per-launch timing records (upipe_attn_timing_collect)
 KERNEL_KINDS = {0: "tile_table", 1: "qkv_proj", 2: "attn_fwd", 3: "o_proj", 4: "convert", 5: "do_proj",
@@ -88,6 +90,11 @@ def lib():
             "upipe_attn_last_device_error": ([P, P, ctypes.POINTER(ctypes.c_int32)], ctypes.c_int),
             "upipe_attn_no_alloc_device_status": ([ctypes.POINTER(ctypes.c_int32), P], ctypes.c_int),
             "upipe_attn_timing_enable": ([ctypes.c_int32], ctypes.c_int),
+            "upipe_attn_set_wait_limit_ns": ([ctypes.c_uint64], ctypes.c_int),
+            "upipe_attn_wait_probe": ([P, SZ, ctypes.c_int32, P], ctypes.c_int),
+            "upipe_attn_workspace_size_offload": ([D, ctypes.c_int, I64, ctypes.POINTER(SZ)], ctypes.c_int),
+            "upipe_attn_fwd_offload": ([D, P, P, P, P, P, P, P, SZ, I64, P], ctypes.c_int),
+            "upipe_attn_bwd_offload": ([D, P, P, P, P, P, P, P, P, P, P, SZ, I64, P], ctypes.c_int),
             "upipe_attn_timing_collect": ([ctypes.POINTER(TimingRec), ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)],
                                           ctypes.c_int),
         }
@@ -176,6 +183,17 @@ def timing_records(cap: int = 1 << 16):
              "chunk": r.chunk, "m": r.m, "n": r.n, "k": r.k, "ms": r.ms} for r in buf[:min(n.value, cap)]]
 
 
+def set_wait_limit_ns(ns: int):
+    """Limit of the kernels' bounded device waits (0: the default 4 s)."""
+    _check(lib().upipe_attn_set_wait_limit_ns(int(ns)), "set_wait_limit_ns")
+
+
+def wait_probe(buf, arrive: bool, stream=None):
+    """One bounded wait on a barrier nothing completes (arrive=False) or one already completed."""
+    _check(lib().upipe_attn_wait_probe(_ptr(buf), buf.numel() * buf.element_size(), int(bool(arrive)),
+                                       _stream(stream)), "wait_probe")
+
+
 def launch_count() -> int:
     """Kernels the library has launched in this process so far."""
     return int(lib().upipe_attn_launch_count())
@@ -190,6 +208,33 @@ def bwd(desc: Desc, X, Wqkv, Wo, seg, dY, lse, dX, dWqkv, dWo, ws, stream=None):
     _check(lib().upipe_attn_bwd(ctypes.byref(desc), _bf16(X), _bf16(Wqkv), _bf16(Wo), _ptr(seg), _bf16(dY), _ptr(lse),
                                 _bf16(dX), _ptr(dWqkv), _ptr(dWo), _ptr(ws), ws.numel() * ws.element_size(),
                                 _stream(stream)), "bwd")
+
+
+def workspace_bytes_offload(desc: Desc, pass_: int, stage_rows: int = 0) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().upipe_attn_workspace_size_offload(ctypes.byref(desc), pass_, stage_rows, ctypes.byref(n)),
+           "workspace_size_offload")
+    return n.value
+
+
+def _host_bf16(t):
+    assert t.dtype == torch.bfloat16 and t.is_contiguous() and t.device.type == "cpu" and t.is_pinned(), \
+        "pinned host bf16 contiguous tensor expected"
+    return _ptr(t)
+
+
+def fwd_offload(desc: Desc, X_host, Wqkv, Wo, seg, Y, lse, ws, stage_rows=0, stream=None):
+    """Forward with X in pinned host memory, brought in stage_rows rows at a time."""
+    _check(lib().upipe_attn_fwd_offload(ctypes.byref(desc), _host_bf16(X_host), _bf16(Wqkv), _bf16(Wo), _ptr(seg),
+                                        _bf16(Y), _ptr(lse), _ptr(ws), ws.numel() * ws.element_size(), stage_rows,
+                                        _stream(stream)), "fwd_offload")
+
+
+def bwd_offload(desc: Desc, X_host, Wqkv, Wo, seg, dY_host, lse, dX, dWqkv, dWo, ws, stage_rows=0, stream=None):
+    """Backward with X and dY in pinned host memory, brought in stage_rows rows at a time."""
+    _check(lib().upipe_attn_bwd_offload(ctypes.byref(desc), _host_bf16(X_host), _bf16(Wqkv), _bf16(Wo), _ptr(seg),
+                                        _host_bf16(dY_host), _ptr(lse), _bf16(dX), _ptr(dWqkv), _ptr(dWo), _ptr(ws),
+                                        ws.numel() * ws.element_size(), stage_rows, _stream(stream)), "bwd_offload")
 
 
 def core_fwd(desc: Desc, q, k, v, seg, table, o, lse, stream=None):

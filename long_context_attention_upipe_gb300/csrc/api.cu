@@ -31,11 +31,18 @@
 
 namespace upipe {
 
+// Default limit of a bounded device wait (4 s), and the largest a caller may set (60 s).
+constexpr uint64_t tc_wait_default_ns = 4000000000ull;
+constexpr uint64_t kMaxWaitLimitNs = 60000000000ull;
+
 // Name of the CUDA error behind the last UPIPE_ERR_CUDA returned on this host thread.
 thread_local const char* g_last_cuda_error = "cudaSuccess";
 
 std::atomic<uint64_t> g_launch_count{0};
 void note_launch() { g_launch_count.fetch_add(1, std::memory_order_relaxed); }
+
+std::atomic<uint64_t> g_wait_limit_ns{tc_wait_default_ns};
+uint64_t wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
 
 upipe_status_t cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return UPIPE_OK;
@@ -93,7 +100,14 @@ struct Plan {
   // workspace offsets
   size_t table, k, v, q, o, yacc, dO, D, dq, dk, dv, dkacc, dvacc, dxacc, split, total;
   int split_wo, split_wqkv_q, split_wqkv_full;
+  // host-resident X / dY: rows per staged block, the two staging buffers of each, and the K
+  // splits of the weight-gradient GEMMs over one block
+  int64_t R;
+  size_t xs[2], dys[2];
+  int split_wo_blk, split_wqkv_q_blk, split_wqkv_full_blk;
 };
+
+constexpr int64_t kDefaultStageRows = 65536;
 
 int num_sms() {
   static int sms = 0;
@@ -122,7 +136,8 @@ upipe_status_t check_desc(const upipe_attn_desc_t* d) {
   return UPIPE_OK;
 }
 
-Plan make_plan(const upipe_attn_desc_t* desc, int pass) {
+// stage_rows > 0: X (and dY) stay in host memory and are staged in blocks of that many rows.
+Plan make_plan(const upipe_attn_desc_t* desc, int pass, int64_t stage_rows = 0) {
   Plan p;
   p.S = desc->seq_len;
   p.d = desc->hidden;
@@ -146,6 +161,19 @@ Plan make_plan(const upipe_attn_desc_t* desc, int pass) {
   p.o = take(p.hpc * head);
   p.yacc = p.dO = p.D = p.dq = p.dk = p.dv = p.dkacc = p.dvacc = p.dxacc = p.split = 0;
   p.split_wo = p.split_wqkv_q = p.split_wqkv_full = 1;
+  p.R = 0;
+  p.xs[0] = p.xs[1] = p.dys[0] = p.dys[1] = 0;
+  p.split_wo_blk = p.split_wqkv_q_blk = p.split_wqkv_full_blk = 1;
+  if (stage_rows > 0) {
+    p.R = std::min<int64_t>(stage_rows, p.S);
+    const size_t blk = (size_t)p.R * p.d * sizeof(bf16);
+    p.xs[0] = take(blk);
+    p.xs[1] = take(blk);
+    if (pass == 1) {
+      p.dys[0] = take(blk);
+      p.dys[1] = take(blk);
+    }
+  }
   const bool multi = p.n_chunks > 1;
   if (pass == 0) {
     if (multi && p.accum == 0) p.yacc = take((size_t)p.S * p.d * sizeof(float));
@@ -168,6 +196,14 @@ Plan make_plan(const upipe_attn_desc_t* desc, int pass) {
     size_t sb = gemm_split_scratch_bytes(p.d, (int64_t)p.hpc * p.Dh, p.split_wo);
     sb = std::max(sb, gemm_split_scratch_bytes((int64_t)p.hpc * p.Dh, p.d, p.split_wqkv_q));
     sb = std::max(sb, gemm_split_scratch_bytes(full_rows, p.d, p.split_wqkv_full));
+    if (p.R) {  // the weight gradients are summed block by block: K = one block's rows
+      p.split_wo_blk = gemm_pick_split(p.d, (int64_t)p.hpc * p.Dh, p.R, sms);
+      p.split_wqkv_q_blk = gemm_pick_split((int64_t)p.hpc * p.Dh, p.d, p.R, sms);
+      p.split_wqkv_full_blk = gemm_pick_split(full_rows, p.d, p.R, sms);
+      sb = std::max(sb, gemm_split_scratch_bytes(p.d, (int64_t)p.hpc * p.Dh, p.split_wo_blk));
+      sb = std::max(sb, gemm_split_scratch_bytes((int64_t)p.hpc * p.Dh, p.d, p.split_wqkv_q_blk));
+      sb = std::max(sb, gemm_split_scratch_bytes(full_rows, p.d, p.split_wqkv_full_blk));
+    }
     if (sb) p.split = take(sb);
   }
   p.total = off;
@@ -213,33 +249,56 @@ TcOperand op3d(const void* base, uint64_t inner, uint64_t outer, uint64_t planes
   return o;
 }
 
-// Q (and, at the start of a KV group, K and V) of chunk c:  [Q|K|V]_c = X * Wqkv_c^T
+// Rows [r0, r0 + rows) of a head-major [planes][S][Dh] workspace tensor as a 3-D operand.
+TcOperand op3d_rows(const Plan& p, const bf16* base, uint64_t planes, int64_t r0, int64_t rows, int k_major,
+                    int blk_shift, int blk_dim) {
+  TcOperand o = op3d(base + r0 * p.Dh, p.Dh, (uint64_t)rows, planes, k_major, blk_shift, blk_dim);
+  o.plane_stride = (uint64_t)p.S * p.Dh;
+  return o;
+}
+
+// Q (and, at the start of a KV group, K and V) of chunk c:  [Q|K|V]_c = X * Wqkv_c^T for the
+// sequence rows [r0, r0 + rows); Xr points at row r0's hidden state (rows of d elements).
 // B = the chunk's rows of Wqkv (a 2-D map with one starting row per head), output head-major.
-cudaError_t project_qkv(const Plan& p, int c, bool with_kv, const bf16* X, const bf16* Wqkv, void* ws, cudaStream_t st) {
+cudaError_t project_qkv(const Plan& p, int c, bool with_kv, const bf16* Xr, int64_t r0, int64_t rows,
+                        const bf16* Wqkv, void* ws, cudaStream_t st) {
   TcGemmArgs g{};
   const int sh = log2i(p.Dh);
   const uint64_t wrows = (uint64_t)(p.Hq + 2 * p.Hkv) * p.Dh;
-  g.a = op2d(X, p.d, p.S, p.d, 1);
+  g.a = op2d(Xr, p.d, (uint64_t)rows, p.d, 1);
   g.b = op2d(Wqkv, p.d, wrows, p.d, 1);
   g.b.blk_shift = sh; g.b.blk_dim = 0;
   g.c.ld = p.Dh; g.c.blk_shift = sh; g.c.blk_dim = 1;
   int nb = 0;
   for (int hl = 0; hl < p.hpc; ++hl, ++nb) {
     g.b.row_base[nb] = (int32_t)wrow_q(p, c * p.hpc + hl);
-    g.c.blk[nb] = at<bf16>(ws, p.q) + (int64_t)hl * p.S * p.Dh;
+    g.c.blk[nb] = at<bf16>(ws, p.q) + (int64_t)hl * p.S * p.Dh + r0 * p.Dh;
   }
   if (with_kv) {
     const int kv0 = (c * p.hpc) / p.g;
     for (int j = 0; j < p.kvc; ++j, ++nb) {
       g.b.row_base[nb] = (int32_t)wrow_k(p, kv0 + j);
-      g.c.blk[nb] = at<bf16>(ws, p.k) + (int64_t)j * p.S * p.Dh;
+      g.c.blk[nb] = at<bf16>(ws, p.k) + (int64_t)j * p.S * p.Dh + r0 * p.Dh;
     }
     for (int j = 0; j < p.kvc; ++j, ++nb) {
       g.b.row_base[nb] = (int32_t)wrow_v(p, kv0 + j);
-      g.c.blk[nb] = at<bf16>(ws, p.v) + (int64_t)j * p.S * p.Dh;
+      g.c.blk[nb] = at<bf16>(ws, p.v) + (int64_t)j * p.S * p.Dh + r0 * p.Dh;
     }
   }
-  g.M = p.S; g.N = (int64_t)nb * p.Dh; g.K = p.d;
+  g.M = rows; g.N = (int64_t)nb * p.Dh; g.K = p.d;
+  g.epi = EPI_STORE_BF16;
+  return launch_gemm_tc(g, 1, nullptr, st);
+}
+
+// dO_c rows [r0, r0 + rows) = dY rows * Wo_c   (Wo_c: columns of Wo, read as [K = d][N = hpc Dh])
+cudaError_t project_do(const Plan& p, int c, const bf16* dYr, int64_t r0, int64_t rows, const bf16* Wo, void* ws,
+                       cudaStream_t st) {
+  TcGemmArgs g{};
+  g.M = rows; g.N = (int64_t)p.hpc * p.Dh; g.K = p.d;
+  g.a = op2d(dYr, p.d, (uint64_t)rows, p.d, 1);
+  g.b = op2d(Wo + (int64_t)c * p.hpc * p.Dh, (uint64_t)p.hpc * p.Dh, p.d, (uint64_t)p.Hq * p.Dh, 0);
+  for (int hl = 0; hl < p.hpc; ++hl) g.c.blk[hl] = at<bf16>(ws, p.dO) + (int64_t)hl * p.S * p.Dh + r0 * p.Dh;
+  g.c.ld = p.Dh; g.c.blk_shift = log2i(p.Dh); g.c.blk_dim = 1;
   g.epi = EPI_STORE_BF16;
   return launch_gemm_tc(g, 1, nullptr, st);
 }
@@ -303,7 +362,7 @@ upipe_status_t run_fwd(const Plan& p, const bf16* X, const bf16* Wqkv, const bf1
     const bool new_group = p.hpc >= p.g || (c * p.hpc) % p.g == 0;
     {
       Timed t(UPIPE_K_QKV_PROJ, EPI_STORE_BF16, p.S, qkv_width(p, new_group), p.d, 1, c, st);
-      UPIPE_CUDA(project_qkv(p, c, new_group, X, Wqkv, ws, st));
+      UPIPE_CUDA(project_qkv(p, c, new_group, X, 0, p.S, Wqkv, ws, st));
     }
     AttnArgs a = attn_args(p, c, ws, seg, lse);
     {
@@ -344,23 +403,16 @@ upipe_status_t run_bwd(const Plan& p, const bf16* X, const bf16* Wqkv, const bf1
     const int kv0 = (c * p.hpc) / p.g;
     {
       Timed t(UPIPE_K_QKV_PROJ, EPI_STORE_BF16, p.S, qkv_width(p, new_group), p.d, 1, c, st);
-      UPIPE_CUDA(project_qkv(p, c, new_group, X, Wqkv, ws, st));
+      UPIPE_CUDA(project_qkv(p, c, new_group, X, 0, p.S, Wqkv, ws, st));
     }
     if (new_group && p.hpc < p.g) {
       Timed t(UPIPE_K_ZERO, 0, 2 * p.S * p.Dh, 1, 1, 1, c, st);
       UPIPE_CUDA(launch_zero(at<char>(ws, p.dkacc), (int64_t)p.S * p.Dh * 4, st));
       UPIPE_CUDA(launch_zero(at<char>(ws, p.dvacc), (int64_t)p.S * p.Dh * 4, st));
     }
-    {  // dO_c = dY * Wo_c   (Wo_c: columns of Wo, read as [K = d][N = hpc Dh])
-      TcGemmArgs g{};
-      g.M = p.S; g.N = (int64_t)p.hpc * p.Dh; g.K = p.d;
-      g.a = op2d(dY, p.d, p.S, p.d, 1);
-      g.b = op2d(Wo + (int64_t)c * p.hpc * p.Dh, (uint64_t)p.hpc * p.Dh, p.d, HD, 0);
-      for (int hl = 0; hl < p.hpc; ++hl) g.c.blk[hl] = at<bf16>(ws, p.dO) + (int64_t)hl * p.S * p.Dh;
-      g.c.ld = p.Dh; g.c.blk_shift = sh; g.c.blk_dim = 1;
-      g.epi = EPI_STORE_BF16;
-      Timed t(UPIPE_K_DO_PROJ, g.epi, g.M, g.N, g.K, 1, c, st);
-      UPIPE_CUDA(launch_gemm_tc(g, 1, nullptr, st));
+    {  // dO_c = dY * Wo_c
+      Timed t(UPIPE_K_DO_PROJ, EPI_STORE_BF16, p.S, (int64_t)p.hpc * p.Dh, p.d, 1, c, st);
+      UPIPE_CUDA(project_do(p, c, dY, 0, p.S, Wo, ws, st));
     }
     AttnArgs a = attn_args(p, c, ws, seg, const_cast<float*>(lse));
     a.dO = at<bf16>(ws, p.dO);
@@ -443,6 +495,262 @@ upipe_status_t run_bwd(const Plan& p, const bf16* X, const bf16* Wqkv, const bf1
       UPIPE_CUDA(launch_gemm_tc(g, split_k, split, st));
     }
   }
+  return UPIPE_OK;
+}
+
+// ------------------------------------------------------------------------ host-resident X / dY
+// CPU offload of the layer's inputs ("Road to 5 Million Tokens" podcast summary, chapter on
+// offloading part of the inputs to the CPU; neuro-slop.ru transcript, implementation plan step
+// 2): X and dY stay in pinned host memory and are brought in block by block, R rows at a time,
+// into two device staging buffers each.  Every block is one cudaMemcpyAsync on a copy stream,
+// issued one block ahead, so the copy of block b + 1 runs while the projections of block b do.
+// Events order the reuse of a staging buffer after the kernels that read it.
+class Stager {
+ public:
+  Stager(const Plan& p, void* ws, cudaStream_t st, const bf16* hx, const bf16* hdy)
+      : p_(p), ws_(ws), st_(st), hx_(hx), hdy_(hdy) {}
+  ~Stager() {
+    for (cudaEvent_t e : {entry_, ready_[0], ready_[1], free_[0], free_[1]})
+      if (e) cudaEventDestroy(e);
+    if (cs_) cudaStreamDestroy(cs_);
+  }
+  cudaError_t begin() {
+    cudaError_t e = cudaStreamCreateWithFlags(&cs_, cudaStreamNonBlocking);
+    for (cudaEvent_t* ev : {&entry_, &ready_[0], &ready_[1], &free_[0], &free_[1]})
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+    // the copies start after the work queued before this call (which may still read the buffers)
+    if (e == cudaSuccess) e = cudaEventRecord(entry_, st_);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(cs_, entry_, 0);
+    for (int k = 0; k < 2 && e == cudaSuccess; ++k) e = cudaEventRecord(free_[k], st_);
+    return e;
+  }
+  int64_t blocks() const { return ceil_div(p_.S, p_.R); }
+  int64_t row0(int64_t b) const { return b * p_.R; }
+  int64_t rows(int64_t b) const { return std::min(p_.R, p_.S - b * p_.R); }
+  const bf16* x(int64_t b) const { return at<bf16>(ws_, p_.xs[b & 1]); }
+  const bf16* dy(int64_t b) const { return at<bf16>(ws_, p_.dys[b & 1]); }
+  // copy block b of each host tensor into staging buffer b % 2 once its last readers are done
+  cudaError_t prefetch(int64_t b) {
+    const int k = (int)(b & 1);
+    const size_t bytes = (size_t)rows(b) * p_.d * sizeof(bf16);
+    const size_t off = (size_t)row0(b) * p_.d;
+    cudaError_t e = cudaStreamWaitEvent(cs_, free_[k], 0);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(at<bf16>(ws_, p_.xs[k]), hx_ + off, bytes, cudaMemcpyHostToDevice, cs_);
+    if (e == cudaSuccess && hdy_)
+      e = cudaMemcpyAsync(at<bf16>(ws_, p_.dys[k]), hdy_ + off, bytes, cudaMemcpyHostToDevice, cs_);
+    if (e == cudaSuccess) e = cudaEventRecord(ready_[k], cs_);
+    return e;
+  }
+  cudaError_t acquire(int64_t b) { return cudaStreamWaitEvent(st_, ready_[b & 1], 0); }
+  cudaError_t release(int64_t b) { return cudaEventRecord(free_[b & 1], st_); }
+
+ private:
+  const Plan& p_;
+  void* ws_;
+  cudaStream_t st_;
+  const bf16* hx_;
+  const bf16* hdy_;
+  cudaStream_t cs_ = nullptr;
+  cudaEvent_t entry_ = nullptr, ready_[2] = {nullptr, nullptr}, free_[2] = {nullptr, nullptr};
+};
+
+// f(b, r0, rows) for every staged block, each with its block resident in the staging buffers.
+template <typename F>
+upipe_status_t over_blocks(Stager& sg, F&& f) {
+  const int64_t nb = sg.blocks();
+  UPIPE_CUDA(sg.prefetch(0));
+  for (int64_t b = 0; b < nb; ++b) {
+    if (b + 1 < nb) UPIPE_CUDA(sg.prefetch(b + 1));
+    UPIPE_CUDA(sg.acquire(b));
+    const upipe_status_t s = f(b, sg.row0(b), sg.rows(b));
+    if (s != UPIPE_OK) return s;
+    UPIPE_CUDA(sg.release(b));
+  }
+  return UPIPE_OK;
+}
+
+// A weight gradient summed over the staged blocks: block 0 stores, later blocks add (split-K
+// partials of a block are reduced in a fixed order, onto the running sum).
+cudaError_t block_weight_grad(TcGemmArgs g, int64_t b, int split, float* scratch, cudaStream_t st) {
+  if (split > 1) {
+    g.epi = EPI_STORE_F32;
+    g.split_accumulate = b > 0;
+  } else {
+    g.epi = b > 0 ? EPI_ACC_F32 : EPI_STORE_F32;
+  }
+  return launch_gemm_tc(g, split, scratch, st);
+}
+
+upipe_status_t run_fwd_offload(const Plan& p, const bf16* hX, const bf16* Wqkv, const bf16* Wo, const int32_t* seg,
+                               bf16* Y, float* lse, void* ws, cudaStream_t st) {
+  Stager sg(p, ws, st, hX, nullptr);
+  UPIPE_CUDA(sg.begin());
+  {
+    Timed t(UPIPE_K_TILE_TABLE, 0, p.S, 0, 0, 1, -1, st);
+    UPIPE_CUDA(launch_tile_table(p.S, p.causal, seg, at<char>(ws, p.table), st));
+  }
+  const int sh = log2i(p.Dh);
+  for (int c = 0; c < p.n_chunks; ++c) {
+    const bool new_group = p.hpc >= p.g || (c * p.hpc) % p.g == 0;
+    upipe_status_t s = over_blocks(sg, [&](int64_t b, int64_t r0, int64_t rows) -> upipe_status_t {
+      Timed t(UPIPE_K_QKV_PROJ, EPI_STORE_BF16, rows, qkv_width(p, new_group), p.d, 1, c, st);
+      UPIPE_CUDA(project_qkv(p, c, new_group, sg.x(b), r0, rows, Wqkv, ws, st));
+      return UPIPE_OK;
+    });
+    if (s != UPIPE_OK) return s;
+    AttnArgs a = attn_args(p, c, ws, seg, lse);
+    {
+      Timed t(UPIPE_K_ATTN_FWD, 0, p.S, p.hpc, p.Dh, 1, c, st);
+      UPIPE_CUDA(launch_attn_fwd(a, p.Dh, st));
+    }
+    TcGemmArgs g{};
+    g.M = p.S; g.N = p.d; g.K = (int64_t)p.hpc * p.Dh;
+    g.a = op3d(at<bf16>(ws, p.o), p.Dh, p.S, p.hpc, 1, sh, 1);
+    g.b = op2d(Wo + (int64_t)c * p.hpc * p.Dh, (uint64_t)p.hpc * p.Dh, p.d, (uint64_t)p.Hq * p.Dh, 1);
+    g.epi = accum_epi(p, c);
+    set_accum_out(g.c, p, g.epi, Y, p.yacc ? at<float>(ws, p.yacc) : nullptr);
+    {
+      Timed t(UPIPE_K_O_PROJ, g.epi, g.M, g.N, g.K, 1, c, st);
+      UPIPE_CUDA(launch_gemm_tc(g, 1, nullptr, st));
+    }
+    if (finishes_accum(p, c)) {
+      Timed t(UPIPE_K_CONVERT, 0, p.S * p.d, 1, 1, 1, c, st);
+      UPIPE_CUDA(accum_finish(p, c, p.yacc ? at<float>(ws, p.yacc) : nullptr, Y, st));
+    }
+  }
+  return UPIPE_OK;
+}
+
+// Backward with X and dY in host memory.  Per chunk, two passes over the staged blocks: before
+// the attention kernels the chunk's Q (K, V) and dO projections; after them the weight
+// gradients dWo_c = dY^T O_c and dWqkv_c = dQKV_c^T X, summed block by block.  dX needs neither
+// X nor dY and runs over the whole sequence as in upipe_attn_bwd.
+upipe_status_t run_bwd_offload(const Plan& p, const bf16* hX, const bf16* Wqkv, const bf16* Wo, const int32_t* seg,
+                               const bf16* hdY, const float* lse, bf16* dX, float* dWqkv, float* dWo, void* ws,
+                               cudaStream_t st) {
+  Stager sg(p, ws, st, hX, hdY);
+  UPIPE_CUDA(sg.begin());
+  {
+    Timed t(UPIPE_K_TILE_TABLE, 0, p.S, 0, 0, 1, -1, st);
+    UPIPE_CUDA(launch_tile_table(p.S, p.causal, seg, at<char>(ws, p.table), st));
+  }
+  const int sh = log2i(p.Dh);
+  const int64_t HD = (int64_t)p.Hq * p.Dh;
+  float* split = p.split ? at<float>(ws, p.split) : nullptr;
+  for (int c = 0; c < p.n_chunks; ++c) {
+    const bool new_group = p.hpc >= p.g || (c * p.hpc) % p.g == 0;
+    const bool end_group = p.hpc >= p.g || ((c + 1) * p.hpc) % p.g == 0;
+    const int kv0 = (c * p.hpc) / p.g;
+    if (new_group && p.hpc < p.g) {
+      Timed t(UPIPE_K_ZERO, 0, 2 * p.S * p.Dh, 1, 1, 1, c, st);
+      UPIPE_CUDA(launch_zero(at<char>(ws, p.dkacc), (int64_t)p.S * p.Dh * 4, st));
+      UPIPE_CUDA(launch_zero(at<char>(ws, p.dvacc), (int64_t)p.S * p.Dh * 4, st));
+    }
+    upipe_status_t s = over_blocks(sg, [&](int64_t b, int64_t r0, int64_t rows) -> upipe_status_t {
+      {
+        Timed t(UPIPE_K_QKV_PROJ, EPI_STORE_BF16, rows, qkv_width(p, new_group), p.d, 1, c, st);
+        UPIPE_CUDA(project_qkv(p, c, new_group, sg.x(b), r0, rows, Wqkv, ws, st));
+      }
+      Timed t(UPIPE_K_DO_PROJ, EPI_STORE_BF16, rows, (int64_t)p.hpc * p.Dh, p.d, 1, c, st);
+      UPIPE_CUDA(project_do(p, c, sg.dy(b), r0, rows, Wo, ws, st));
+      return UPIPE_OK;
+    });
+    if (s != UPIPE_OK) return s;
+    AttnArgs a = attn_args(p, c, ws, seg, const_cast<float*>(lse));
+    a.dO = at<bf16>(ws, p.dO);
+    a.D = at<float>(ws, p.D);
+    {
+      Timed t(UPIPE_K_RECOMPUTE, 0, p.S, p.hpc, p.Dh, 1, c, st);
+      UPIPE_CUDA(launch_attn_recompute(a, p.Dh, st));
+    }
+    AttnBwdArgs bw{};
+    bw.f = a;
+    bw.dq = at<bf16>(ws, p.dq);
+    bw.dk = at<bf16>(ws, p.dk);
+    bw.dv = at<bf16>(ws, p.dv);
+    bw.acc_kv = p.hpc < p.g;
+    bw.dk_acc = p.dkacc ? at<float>(ws, p.dkacc) : nullptr;
+    bw.dv_acc = p.dvacc ? at<float>(ws, p.dvacc) : nullptr;
+    bw.nkv = p.kvc;
+    {
+      Timed t(UPIPE_K_BWD_DQ, 0, p.S, p.hpc, p.Dh, 1, c, st);
+      UPIPE_CUDA(launch_attn_bwd_dq(bw, p.Dh, st));
+    }
+    {
+      Timed t(UPIPE_K_BWD_DKDV, 0, p.S, p.hpc, p.Dh, 1, c, st);
+      UPIPE_CUDA(launch_attn_bwd_dkdv(bw, p.Dh, st));
+    }
+    if (end_group && p.hpc < p.g) {
+      Timed t(UPIPE_K_CONVERT, 0, 2 * p.S * p.Dh, 1, 1, 1, c, st);
+      UPIPE_CUDA(launch_f32_to_bf16(at<float>(ws, p.dkacc), at<bf16>(ws, p.dk), p.S * p.Dh, 1.f, st));
+      UPIPE_CUDA(launch_f32_to_bf16(at<float>(ws, p.dvacc), at<bf16>(ws, p.dv), p.S * p.Dh, 1.f, st));
+    }
+    int32_t blk_row[kMaxBlocks];
+    int nb = 0;
+    for (int hl = 0; hl < p.hpc; ++hl, ++nb) blk_row[nb] = (int32_t)wrow_q(p, c * p.hpc + hl);
+    if (end_group) {
+      for (int j = 0; j < p.kvc; ++j, ++nb) blk_row[nb] = (int32_t)wrow_k(p, kv0 + j);
+      for (int j = 0; j < p.kvc; ++j, ++nb) blk_row[nb] = (int32_t)wrow_v(p, kv0 + j);
+    }
+    const uint64_t planes = (uint64_t)(p.hpc + 2 * p.kvc);
+    const uint64_t wrows = (uint64_t)(p.Hq + 2 * p.Hkv) * p.Dh;
+    {  // dX (+)= dQKV_c * Wqkv_c over the whole sequence
+      TcGemmArgs g{};
+      g.M = p.S; g.N = p.d; g.K = (int64_t)nb * p.Dh;
+      g.a = op3d(at<bf16>(ws, p.dq), p.Dh, p.S, planes, 1, sh, 1);
+      g.b = op2d(Wqkv, p.d, wrows, p.d, 0);
+      g.b.blk_shift = sh; g.b.blk_dim = 1;
+      for (int i = 0; i < nb; ++i) g.b.row_base[i] = blk_row[i];
+      g.epi = accum_epi(p, c);
+      set_accum_out(g.c, p, g.epi, dX, p.dxacc ? at<float>(ws, p.dxacc) : nullptr);
+      {
+        Timed t(UPIPE_K_DX_PROJ, g.epi, g.M, g.N, g.K, 1, c, st);
+        UPIPE_CUDA(launch_gemm_tc(g, 1, nullptr, st));
+      }
+      if (finishes_accum(p, c)) {
+        Timed t(UPIPE_K_CONVERT, 0, p.S * p.d, 1, 1, 1, c, st);
+        UPIPE_CUDA(accum_finish(p, c, p.dxacc ? at<float>(ws, p.dxacc) : nullptr, dX, st));
+      }
+    }
+    const int split_qkv = nb == p.hpc ? p.split_wqkv_q_blk : p.split_wqkv_full_blk;
+    s = over_blocks(sg, [&](int64_t b, int64_t r0, int64_t rows) -> upipe_status_t {
+      {  // dWo_c (+)= dY_b^T * O_c rows of the block
+        TcGemmArgs g{};
+        g.M = p.d; g.N = (int64_t)p.hpc * p.Dh; g.K = rows;
+        g.a = op2d(sg.dy(b), p.d, (uint64_t)rows, p.d, 0);
+        g.b = op3d_rows(p, at<bf16>(ws, p.o), p.hpc, r0, rows, 0, sh, 0);
+        g.c.blk[0] = dWo + (int64_t)c * p.hpc * p.Dh; g.c.ld = HD; g.c.blk_shift = -1;
+        Timed t(UPIPE_K_DWO, b > 0 ? EPI_ACC_F32 : EPI_STORE_F32, g.M, g.N, g.K, p.split_wo_blk, c, st);
+        UPIPE_CUDA(block_weight_grad(g, b, p.split_wo_blk, split, st));
+      }
+      // dWqkv rows of the final blocks (+)= dQKV_b^T * X_b
+      TcGemmArgs g{};
+      g.M = (int64_t)nb * p.Dh; g.N = p.d; g.K = rows;
+      g.a = op3d_rows(p, at<bf16>(ws, p.dq), planes, r0, rows, 0, sh, 0);
+      g.b = op2d(sg.x(b), p.d, (uint64_t)rows, p.d, 0);
+      for (int i = 0; i < nb; ++i) g.c.blk[i] = dWqkv + (int64_t)blk_row[i] * p.d;
+      g.c.ld = p.d; g.c.blk_shift = sh; g.c.blk_dim = 0;
+      Timed t(UPIPE_K_DWQKV, b > 0 ? EPI_ACC_F32 : EPI_STORE_F32, g.M, g.N, g.K, split_qkv, c, st);
+      UPIPE_CUDA(block_weight_grad(g, b, split_qkv, split, st));
+      return UPIPE_OK;
+    });
+    if (s != UPIPE_OK) return s;
+  }
+  return UPIPE_OK;
+}
+
+// Host tensors of the offloaded entry points must be page-locked (pinned or registered).
+bool pinned_host(const void* ptr) {
+  cudaPointerAttributes attr{};
+  if (cudaPointerGetAttributes(&attr, ptr) != cudaSuccess) {
+    cudaGetLastError();  // the failed query's error is not sticky: clear it
+    return false;
+  }
+  return attr.type == cudaMemoryTypeHost;
+}
+
+upipe_status_t check_stage_rows(int64_t stage_rows) {
+  if (stage_rows < 0 || (stage_rows > 0 && stage_rows % kTile != 0)) return UPIPE_ERR_INVALID_ARG;
   return UPIPE_OK;
 }
 
@@ -699,6 +1007,56 @@ upipe_status_t upipe_attn_device_status(const void* buf, int32_t* code, void* st
   return UPIPE_OK;
 }
 
+upipe_status_t upipe_attn_workspace_size_offload(const upipe_attn_desc_t* desc, int pass, int64_t stage_rows,
+                                                 size_t* bytes) {
+  upipe_status_t s = check_desc(desc);
+  if (s != UPIPE_OK) return s;
+  if (!bytes || (pass != 0 && pass != 1)) return UPIPE_ERR_INVALID_ARG;
+  if ((s = check_stage_rows(stage_rows)) != UPIPE_OK) return s;
+  *bytes = make_plan(desc, pass, stage_rows ? stage_rows : kDefaultStageRows).total;
+  return UPIPE_OK;
+}
+
+// The layer's forward with X in host memory (CPU offload of the inputs: podcast summary, chapter
+// on offloading inputs to the CPU; transcript, implementation plan step 2).
+upipe_status_t upipe_attn_fwd_offload(const upipe_attn_desc_t* desc, const uint16_t* X_host, const uint16_t* Wqkv,
+                                      const uint16_t* Wo, const int32_t* seg, uint16_t* Y, float* lse, void* ws,
+                                      size_t ws_bytes, int64_t stage_rows, void* stream) {
+  upipe_status_t s = check_desc(desc);
+  if (s != UPIPE_OK) return s;
+  if ((s = check_stage_rows(stage_rows)) != UPIPE_OK) return s;
+  if (!X_host || !Wqkv || !Wo || !Y || !lse || !ws) return UPIPE_ERR_INVALID_ARG;
+  if (!aligned16(X_host) || !aligned16(Wqkv) || !aligned16(Wo) || !aligned16(Y) || !aligned16(lse) || !aligned16(ws) ||
+      (seg && !aligned16(seg)))
+    return UPIPE_ERR_ALIGNMENT;
+  const Plan p = make_plan(desc, 0, stage_rows ? stage_rows : kDefaultStageRows);
+  if (ws_bytes < p.total) return UPIPE_ERR_WORKSPACE_TOO_SMALL;
+  if (!pinned_host(X_host)) return UPIPE_ERR_INVALID_ARG;
+  return run_fwd_offload(p, reinterpret_cast<const bf16*>(X_host), reinterpret_cast<const bf16*>(Wqkv),
+                         reinterpret_cast<const bf16*>(Wo), seg, reinterpret_cast<bf16*>(Y), lse, ws,
+                         (cudaStream_t)stream);
+}
+
+// The layer's backward with X and dY in host memory (same passages).
+upipe_status_t upipe_attn_bwd_offload(const upipe_attn_desc_t* desc, const uint16_t* X_host, const uint16_t* Wqkv,
+                                      const uint16_t* Wo, const int32_t* seg, const uint16_t* dY_host, const float* lse,
+                                      uint16_t* dX, float* dWqkv, float* dWo, void* ws, size_t ws_bytes,
+                                      int64_t stage_rows, void* stream) {
+  upipe_status_t s = check_desc(desc);
+  if (s != UPIPE_OK) return s;
+  if ((s = check_stage_rows(stage_rows)) != UPIPE_OK) return s;
+  if (!X_host || !Wqkv || !Wo || !dY_host || !lse || !dX || !dWqkv || !dWo || !ws) return UPIPE_ERR_INVALID_ARG;
+  if (!aligned16(X_host) || !aligned16(Wqkv) || !aligned16(Wo) || !aligned16(dY_host) || !aligned16(lse) ||
+      !aligned16(dX) || !aligned16(dWqkv) || !aligned16(dWo) || !aligned16(ws) || (seg && !aligned16(seg)))
+    return UPIPE_ERR_ALIGNMENT;
+  const Plan p = make_plan(desc, 1, stage_rows ? stage_rows : kDefaultStageRows);
+  if (ws_bytes < p.total) return UPIPE_ERR_WORKSPACE_TOO_SMALL;
+  if (!pinned_host(X_host) || !pinned_host(dY_host)) return UPIPE_ERR_INVALID_ARG;
+  return run_bwd_offload(p, reinterpret_cast<const bf16*>(X_host), reinterpret_cast<const bf16*>(Wqkv),
+                         reinterpret_cast<const bf16*>(Wo), seg, reinterpret_cast<const bf16*>(dY_host), lse,
+                         reinterpret_cast<bf16*>(dX), dWqkv, dWo, ws, (cudaStream_t)stream);
+}
+
 upipe_status_t upipe_attn_timing_enable(int32_t on) {
   if (on != 0 && on != 1) return UPIPE_ERR_INVALID_ARG;
   g_timing_on.store(on, std::memory_order_relaxed);
@@ -730,6 +1088,18 @@ upipe_status_t upipe_attn_timing_collect(upipe_attn_timing_t* out, int32_t cap, 
   }
   *n = k;
   return status;
+}
+
+upipe_status_t upipe_attn_set_wait_limit_ns(uint64_t ns) {
+  if (ns > kMaxWaitLimitNs) return UPIPE_ERR_INVALID_ARG;
+  g_wait_limit_ns.store(ns ? ns : tc_wait_default_ns, std::memory_order_relaxed);
+  return UPIPE_OK;
+}
+
+upipe_status_t upipe_attn_wait_probe(void* buf, size_t bytes, int32_t arrive, void* stream) {
+  if (!buf || bytes < sizeof(TableHeader) || (arrive != 0 && arrive != 1)) return UPIPE_ERR_INVALID_ARG;
+  if (!aligned16(buf)) return UPIPE_ERR_ALIGNMENT;
+  return cuda_status(launch_wait_probe(buf, arrive, (cudaStream_t)stream));
 }
 
 upipe_status_t upipe_attn_last_device_error(const void* ws, void* stream, int32_t* code) {

@@ -210,11 +210,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dq_tc(const __grid_con
         }
         for (int j = j0, n = 0; j < j1; ++j, ++n) {
           // K_j into K slot n % 2 once K_{j-2} is released; V_j into the V slot once dP of V_{j-1} is done
-          if (n >= 2 && !tc::mbar_wait(&k_empty[n & 1], ((n >> 1) - 1) & 1, abort_flag, a.err)) break;
+          if (n >= 2 && !tc::mbar_wait(&k_empty[n & 1], ((n >> 1) - 1) & 1, abort_flag, a.err, a.wait_ns)) break;
           tc::mbar_arrive_expect_tx(&k_full[n & 1], L::TB);
           for (int at = 0; at < DH / 64; ++at)
             tc::tma_load_3d(smem + L::KR + (n & 1) * L::TB + at * kBoxBytes, &tk, &k_full[n & 1], at * 64, j * kTile, kvh);
-          if (n >= 1 && !tc::mbar_wait(v_empty, (n - 1) & 1, abort_flag, a.err)) break;
+          if (n >= 1 && !tc::mbar_wait(v_empty, (n - 1) & 1, abort_flag, a.err, a.wait_ns)) break;
           tc::mbar_arrive_expect_tx(v_full, L::TB);
           for (int at = 0; at < DH / 64; ++at)
             tc::tma_load_3d(smem + L::VR + at * kBoxBytes, &tv, v_full, at * 64, j * kTile, kvh);
@@ -226,12 +226,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dq_tc(const __grid_con
         const uint64_t dQ = kdesc(smem_u32(smem + L::Q)), dDO = kdesc(smem_u32(smem + L::DO));
         const uint64_t dK = kdesc(smem_u32(smem + L::KR)), dKmn = mndesc(smem_u32(smem + L::KR));
         const uint64_t dV = kdesc(smem_u32(smem + L::VR));
-        bool ok = tc::mbar_wait(q_full, 0, abort_flag, a.err);
+        bool ok = tc::mbar_wait(q_full, 0, abort_flag, a.err, a.wait_ns);
         const int4 rng[2] = {rng0, rng1};
         int cnt[2] = {0, 0};
         bool first[2] = {true, true};
         if (ok) {
-          ok = tc::mbar_wait(&k_full[0], 0, abort_flag, a.err);
+          ok = tc::mbar_wait(&k_full[0], 0, abort_flag, a.err, a.wait_ns);
           tc::fence_after_sync();
           for (int t = 0; t < 2 && ok; ++t)
             if (in_range(rng[t], j0)) {
@@ -241,12 +241,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dq_tc(const __grid_con
         }
         for (int j = j0, n = 0; ok && j < j1; ++j, ++n) {
           const uint64_t kb = tc::sdesc_add(dKmn, (n & 1) * L::TB);
-          ok = tc::mbar_wait(v_full, n & 1, abort_flag, a.err);  // V_j
+          ok = tc::mbar_wait(v_full, n & 1, abort_flag, a.err, a.wait_ns);  // V_j
           if (!ok) break;
           tc::fence_after_sync();
           for (int t = 0; t < 2 && ok; ++t)
             if (in_range(rng[t], j)) {
-              ok = tc::mbar_wait(&s_free[t], cnt[t] & 1, abort_flag, a.err);
+              ok = tc::mbar_wait(&s_free[t], cnt[t] & 1, abort_flag, a.err, a.wait_ns);
               if (!ok) break;
               tc::fence_after_sync();
               mma_nt<DH>(tmem + L::r_col(t), tc::sdesc_add(dDO, t * L::TB), dV);  // dP = dO V^T
@@ -255,12 +255,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dq_tc(const __grid_con
           if (!ok) break;
           tc::mma_commit(v_empty);
           if (j + 1 < j1) {
-            ok = tc::mbar_wait(&k_full[(n + 1) & 1], ((n + 1) >> 1) & 1, abort_flag, a.err);  // K_j+1
+            ok = tc::mbar_wait(&k_full[(n + 1) & 1], ((n + 1) >> 1) & 1, abort_flag, a.err, a.wait_ns);  // K_j+1
             tc::fence_after_sync();
           }
           for (int t = 0; t < 2 && ok; ++t) {
             if (in_range(rng[t], j)) {
-              ok = tc::mbar_wait(&ds_full[t], cnt[t] & 1, abort_flag, a.err);
+              ok = tc::mbar_wait(&ds_full[t], cnt[t] & 1, abort_flag, a.err, a.wait_ns);
               if (!ok) break;
               ++cnt[t];
               tc::fence_after_sync();
@@ -301,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dq_tc(const __grid_con
       int cnt = 0;
       for (int j = rg.x; j < rg.w; ++j, ++cnt) {
         const bool partial = j < rg.y || j >= rg.z || (ragged && j == nt - 1);
-        ok = tc::mbar_wait(&s_full[t], cnt & 1, abort_flag, a.err);
+        ok = tc::mbar_wait(&s_full[t], cnt & 1, abort_flag, a.err, a.wait_ns);
         if (!ok) break;
         tc::fence_after_sync();
         // P = exp2(s c - lse2) in fp32, in place of the scores (P only feeds dS here, so it is
@@ -338,14 +338,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dq_tc(const __grid_con
         }
         tc::fence_before_sync();
         tc::mbar_arrive(&s_free[t]);
-        ok = tc::mbar_wait(&dp_full[t], cnt & 1, abort_flag, a.err);
+        ok = tc::mbar_wait(&dp_full[t], cnt & 1, abort_flag, a.err, a.wait_ns);
         if (!ok) break;
         tc::fence_after_sync();
         ds_pass_f32(r_addr, sa, sb, [&](int) { return make_float2(-Dr, -Dr); });
         tc::fence_before_sync();
         tc::mbar_arrive(&ds_full[t]);
       }
-      if (ok) ok = tc::mbar_wait(&dq_full[t], 0, abort_flag, a.err);
+      if (ok) ok = tc::mbar_wait(&dq_full[t], 0, abort_flag, a.err, a.wait_ns);
       tc::fence_after_sync();
       bf16* dqrow = b.dq + ((int64_t)h * S + (row_ok ? row : 0)) * DH;
 #pragma unroll
@@ -485,11 +485,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
           const int hh = h_first + n / nq;
           const int qi = tr.x + n % nq;
           const int sq = n % NQ, so = n % NO;
-          if (n >= NQ && !tc::mbar_wait(&q_empty[sq], ((n / NQ) - 1) & 1, abort_flag, a.err)) break;
+          if (n >= NQ && !tc::mbar_wait(&q_empty[sq], ((n / NQ) - 1) & 1, abort_flag, a.err, a.wait_ns)) break;
           tc::mbar_arrive_expect_tx(&q_full[sq], L::TB);
           for (int at = 0; at < DH / 64; ++at)
             tc::tma_load_3d(smem + L::QR + sq * L::TB + at * kBoxBytes, &tq, &q_full[sq], at * 64, qi * kTile, hh);
-          if (n >= NO && !tc::mbar_wait(&o_empty[so], ((n / NO) - 1) & 1, abort_flag, a.err)) break;
+          if (n >= NO && !tc::mbar_wait(&o_empty[so], ((n / NO) - 1) & 1, abort_flag, a.err, a.wait_ns)) break;
           tc::mbar_arrive_expect_tx(&o_full[so], L::TB);
           for (int at = 0; at < DH / 64; ++at)
             tc::tma_load_3d(smem + L::OR + so * L::TB + at * kBoxBytes, &tdo, &o_full[so], at * 64, qi * kTile, hh);
@@ -509,9 +509,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
         const uint64_t dO = tc::sdesc_add(kdesc(smem_u32(smem + L::OR)), (g % NO) * L::TB);  // item n uses dO slot n % 2 == g
         const uint64_t dOmn = tc::sdesc_add(mndesc(smem_u32(smem + L::OR)), (g % NO) * L::TB);
         const uint32_t r_tm = tmem + L::r_col(g);
-        bool ok = tc::mbar_wait(kv_full, 0, abort_flag, a.err);
+        bool ok = tc::mbar_wait(kv_full, 0, abort_flag, a.err, a.wait_ns);
         auto issue_st = [&](int n) {  // S^T of item n into this group's region
-          if (ok) ok = tc::mbar_wait(&q_full[n % NQ], (n / NQ) & 1, abort_flag, a.err);
+          if (ok) ok = tc::mbar_wait(&q_full[n % NQ], (n / NQ) & 1, abort_flag, a.err, a.wait_ns);
           if (!ok) return;
           tc::fence_after_sync();
           mma_nt<DH>(r_tm, dK, tc::sdesc_add(dQ, (n % NQ) * L::TB));
@@ -522,9 +522,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
           const uint32_t ph = (n >> 1) & 1;
           // the waits that are normally already satisfied come first, so that the issue of dV
           // follows the element-wise group's P^T arrival as closely as possible
-          ok = tc::mbar_wait(&o_full[g], (n / NO) & 1, abort_flag, a.err);
-          if (ok && n > 0) ok = tc::mbar_wait(dv_tok, (n - 1) & 1, abort_flag, a.err);  // dV(n-1) issued
-          if (ok) ok = tc::mbar_wait(&p_full[g], ph, abort_flag, a.err);
+          ok = tc::mbar_wait(&o_full[g], (n / NO) & 1, abort_flag, a.err, a.wait_ns);
+          if (ok && n > 0) ok = tc::mbar_wait(dv_tok, (n - 1) & 1, abort_flag, a.err, a.wait_ns);  // dV(n-1) issued
+          if (ok) ok = tc::mbar_wait(&p_full[g], ph, abort_flag, a.err, a.wait_ns);
           if (!ok) break;
           tc::fence_after_sync();
           mma_acc<DH>(tmem + L::DV_COL, r_tm, dOmn, n > 0);  // dV += P^T dO
@@ -533,8 +533,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
           mma_nt<DH>(r_tm, dV, dO);  // dP^T = V dO^T
           tc::mma_commit(&dp_full[g]);
           tc::mma_commit(&o_empty[g]);
-          if (n > 0) ok = tc::mbar_wait(dk_tok, (n - 1) & 1, abort_flag, a.err);  // dK(n-1) issued
-          if (ok) ok = tc::mbar_wait(&ds_full[g], ph, abort_flag, a.err);
+          if (n > 0) ok = tc::mbar_wait(dk_tok, (n - 1) & 1, abort_flag, a.err, a.wait_ns);  // dK(n-1) issued
+          if (ok) ok = tc::mbar_wait(&ds_full[g], ph, abort_flag, a.err, a.wait_ns);
           if (!ok) break;
           tc::fence_after_sync();
           mma_acc<DH>(tmem + L::DK_COL, r_tm, tc::sdesc_add(dQmn, (n % NQ) * L::TB), n > 0);  // dK += dS^T Q
@@ -602,7 +602,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
       tc::named_bar_sync(1 + grp, 128);
       if (n + 2 < n_items) vec_next = load_vec(n + 2);
       take_turn();
-      ok = tc::mbar_wait(&s_full[grp], cyc, abort_flag, a.err);
+      ok = tc::mbar_wait(&s_full[grp], cyc, abort_flag, a.err, a.wait_ns);
       if (!ok) break;
       tc::fence_after_sync();
       // P^T = exp2(s c - lse2) kept in fp32 in place of the scores (for dS^T); its bf16 copy goes
@@ -650,7 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
       tc::mbar_arrive(&p_full[grp]);
       give_turn();
       take_turn();
-      ok = tc::mbar_wait(&dp_full[grp], cyc, abort_flag, a.err);
+      ok = tc::mbar_wait(&dp_full[grp], cyc, abort_flag, a.err, a.wait_ns);
       if (!ok) break;
       tc::fence_after_sync();
       ds_pass_f32(r_addr, sa, sb, [&](int k) { return *reinterpret_cast<const float2*>(nvec + 128 + k); });
@@ -661,7 +661,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
     // after an abort, hand over the turns still owed so the other group never blocks on them
     for (int k = turn; k < n_give; ++k) tc::named_bar_arrive(kPing + 1 - grp, 256);
     // epilogue: group 0 writes dK rows (scaled), group 1 writes dV rows
-    if (ok && n_items > 0) ok = tc::mbar_wait(acc_full, 0, abort_flag, a.err);
+    if (ok && n_items > 0) ok = tc::mbar_wait(acc_full, 0, abort_flag, a.err, a.wait_ns);
     tc::fence_after_sync();
     const uint32_t acc_addr = lane_addr + (grp == 0 ? L::DK_COL : L::DV_COL);
     const float mul = grp == 0 ? a.scale : 1.f;
@@ -723,7 +723,9 @@ cudaError_t launch(KFN kfn, size_t bytes, dim3 grid, const CUtensorMap& tq, cons
   const size_t smem = bytes > 120 * 1024 ? bytes : 120 * 1024;
   cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kfn<<<grid, kThreads, smem, st>>>(tq, tdo, tk, tv, b);
+  AttnBwdArgs args = b;
+  args.f.wait_ns = wait_limit_ns();
+  kfn<<<grid, kThreads, smem, st>>>(tq, tdo, tk, tv, args);
   note_launch();
   return cudaGetLastError();
 }

@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const int n_items = 2 * (j1 - j0);
       for (int it = 0; it < n_items; ++it) {
         const int sl = it % NS;
-        if (it >= NS && !tc::mbar_wait(&slot_empty[sl], ((it / NS) - 1) & 1, abort_flag, a.err)) break;
+        if (it >= NS && !tc::mbar_wait(&slot_empty[sl], ((it / NS) - 1) & 1, abort_flag, a.err, a.wait_ns)) break;
         tc::mbar_arrive_expect_tx(&slot_full[sl], L::TB);
         const CUtensorMap* map = (it & 1) ? &tv : &tk;
         const int row = (j0 + (it >> 1)) * kTile;
@@ -154,11 +154,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const uint64_t dV = tc::sdesc_sw128(sR, kBoxBytes, 1024);    // ring slot 0 read as V (MN-major)
       const uint32_t s_tm = tmem + L::s_col(t), o_tm = tmem + L::o_col(t);
       const int4 rg = t ? rng1 : rng0;
-      bool ok = tc::mbar_wait(q_full, 0, abort_flag, a.err);
+      bool ok = tc::mbar_wait(q_full, 0, abort_flag, a.err, a.wait_ns);
       struct Pos { int slot; uint32_t phase; };
       auto next = [](Pos p) { return p.slot + 1 == NS ? Pos{0, p.phase ^ 1u} : Pos{p.slot + 1, p.phase}; };
       auto wait_item = [&](Pos p) {
-        if (ok) ok = tc::mbar_wait(&slot_full[p.slot], p.phase, abort_flag, a.err);
+        if (ok) ok = tc::mbar_wait(&slot_full[p.slot], p.phase, abort_flag, a.err, a.wait_ns);
         tc::fence_after_sync();
       };
       auto issue_s = [&](int slot) {
@@ -190,7 +190,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (j + 1 < j1) wait_item(knext);      // K_j+1
         if (!ok) break;
         if (in_range(rg, j)) {
-          ok = tc::mbar_wait(&p_full[t], cnt_p & 1, abort_flag, a.err);
+          ok = tc::mbar_wait(&p_full[t], cnt_p & 1, abort_flag, a.err, a.wait_ns);
           if (!ok) break;
           ++cnt_p;
           tc::fence_after_sync();
@@ -245,7 +245,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const bool partial = j < rg.y || j >= rg.z || (ragged && j == nt - 1);
         const bool pp = j >= pp_lo && j < pp_hi;
         if (pp) tc::named_bar_sync(kPing + t, 256);
-        ok = tc::mbar_wait(&s_full[t], cnt & 1, abort_flag, a.err);
+        ok = tc::mbar_wait(&s_full[t], cnt & 1, abort_flag, a.err, a.wait_ns);
         if (!ok) break;
         tc::fence_after_sync();
         uint32_t sv[128];
@@ -321,7 +321,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       // after an abort, hand over the turns still owed so the other group never blocks on them
       for (int k = turn; k < n_give; ++k) tc::named_bar_arrive(kPing + 1 - t, 256);
-      if (ok) ok = tc::mbar_wait(&o_full[t], 0, abort_flag, a.err);
+      if (ok) ok = tc::mbar_wait(&o_full[t], 0, abort_flag, a.err, a.wait_ns);
       tc::fence_after_sync();
       // epilogue: O / l -> bf16 row; lse or D
       const float inv = (MODE == 0) ? (l > 0.f ? 1.f / l : 0.f) : 1.f;
@@ -386,7 +386,9 @@ cudaError_t run(const AttnArgs& a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   const int nt = (int)ceil_div(a.S, kTile);
   dim3 grid((unsigned)a.nh, (unsigned)ceil_div(nt, 2));
-  kfn<<<grid, kFwdThreads, smem, st>>>(tq, tk, tv, a);
+  AttnArgs args = a;
+  args.wait_ns = wait_limit_ns();
+  kfn<<<grid, kFwdThreads, smem, st>>>(tq, tk, tv, args);
   note_launch();
   return cudaGetLastError();
 }

@@ -62,6 +62,7 @@ struct TcGemmParams {
   int tiles_m, tiles_n;
   float* split_out;
   int tma_out;  // 0: per-thread stores; 1: TMA store (2-D map); 2: TMA reduce-add (2-D); 3: TMA store of split partials (3-D)
+  uint64_t wait_ns;  // limit of each bounded wait
 };
 
 enum : int { TMA_OUT_NONE = 0, TMA_OUT_STORE = 1, TMA_OUT_ADD = 2, TMA_OUT_SPLIT = 3 };
@@ -190,7 +191,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_gemm_tc(const __grid_constant__ 
         const int nk = k_tiles(ks);
         for (int kt = 0; kt < nk; ++kt, ++it) {
           const int s = it % STAGES;
-          if (it >= STAGES && !(ok = tc::mbar_wait(&empty[s], ((it / STAGES) - 1) & 1, abort_flag, nullptr))) break;
+          if (it >= STAGES && !(ok = tc::mbar_wait(&empty[s], ((it / STAGES) - 1) & 1, abort_flag, nullptr, p.wait_ns))) break;
           if (q == 0 && crank == 0) tc::mbar_arrive_expect_tx(&full[s], 2 * STAGE);  // both CTAs' A and B halves
           const uint32_t bar = full0 + s * 8;
           uint8_t* sa = smem + s * STAGE;
@@ -217,12 +218,12 @@ __global__ void __launch_bounds__(THREADS, 1) k_gemm_tc(const __grid_constant__ 
         decode(t, tm, tn, ks);
         const int nk = k_tiles(ks);
         const int buf = tcount & 1;
-        if (tcount >= 2 && !(ok = tc::mbar_wait(&acc_empty[buf], ((tcount >> 1) - 1) & 1, abort_flag, nullptr))) break;
+        if (tcount >= 2 && !(ok = tc::mbar_wait(&acc_empty[buf], ((tcount >> 1) - 1) & 1, abort_flag, nullptr, p.wait_ns))) break;
         tc::fence_after_sync();
         const uint32_t d = tmem + buf * BN;
         for (int kt = 0; kt < nk; ++kt, ++it) {
           const int s = it % STAGES;
-          if (!(ok = tc::mbar_wait(&full[s], (it / STAGES) & 1, abort_flag, nullptr))) break;
+          if (!(ok = tc::mbar_wait(&full[s], (it / STAGES) & 1, abort_flag, nullptr, p.wait_ns))) break;
           tc::fence_after_sync();
           const uint64_t ad = tc::opaque(tc::sdesc_add(a0, s * STAGE)), bd = tc::opaque(tc::sdesc_add(b0, s * STAGE));
 #pragma unroll
@@ -245,7 +246,7 @@ __global__ void __launch_bounds__(THREADS, 1) k_gemm_tc(const __grid_constant__ 
       decode(t, tm, tn, ks);
       const int nk = k_tiles(ks);
       const int buf = tcount & 1;
-      if (ok) ok = tc::mbar_wait(&acc_full[buf], (tcount >> 1) & 1, abort_flag, nullptr);
+      if (ok) ok = tc::mbar_wait(&acc_full[buf], (tcount >> 1) & 1, abort_flag, nullptr, p.wait_ns);
       tc::fence_after_sync();
       const int64_t m = (int64_t)tm * BM + row_in_tile;
       const bool m_ok = m < p.M;
@@ -357,8 +358,9 @@ __global__ void __launch_bounds__(THREADS, 1) k_gemm_tc(const __grid_constant__ 
   }
 }
 
-// Fixed-order reduction of split-K partials into the (blocked) fp32 output.
-__global__ void k_split_reduce(const float* __restrict__ part, int splits, int64_t M, int64_t N, GemmOutput out) {
+// Fixed-order reduction of split-K partials into the (blocked) fp32 output (or onto it).
+__global__ void k_split_reduce(const float* __restrict__ part, int splits, int64_t M, int64_t N, GemmOutput out,
+                               int accumulate) {
   const int64_t total = M * N / 4;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
@@ -369,12 +371,17 @@ __global__ void k_split_reduce(const float* __restrict__ part, int splits, int64
       const float4 v = reinterpret_cast<const float4*>(part + (int64_t)z * M * N)[i];
       s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
     }
-    *reinterpret_cast<float4*>(out_ptr<float>(out, m, n)) = s;
+    float4* dst = reinterpret_cast<float4*>(out_ptr<float>(out, m, n));
+    if (accumulate) {
+      const float4 o = *dst;
+      s.x += o.x; s.y += o.y; s.z += o.z; s.w += o.w;
+    }
+    *dst = s;
   }
 }
 
 bool make_map(CUtensorMap* map, const TcOperand& o) {
-  if (o.rank == 3) return make_tmap_3d_bf16(map, o.base, o.inner, o.outer, o.planes, 64, 64);
+  if (o.rank == 3) return make_tmap_3d_bf16(map, o.base, o.inner, o.outer, o.planes, 64, 64, o.plane_stride);
   return make_tmap_2d_bf16(map, o.base, o.inner, o.outer, o.row_stride, 64, 64);
 }
 
@@ -405,10 +412,10 @@ int gemm_pick_split(int64_t M, int64_t N, int64_t K, int num_sms) {
 }
 
 cudaError_t launch_split_reduce(const float* part, int splits, int64_t M, int64_t N, const GemmOutput& out,
-                                cudaStream_t st) {
+                                int accumulate, cudaStream_t st) {
   const int64_t total4 = M * N / 4;
   const unsigned blocks = (unsigned)std::max<int64_t>(1, std::min<int64_t>(ceil_div(total4, 256), 152 * 8));
-  k_split_reduce<<<blocks, 256, 0, st>>>(part, splits, M, N, out);
+  k_split_reduce<<<blocks, 256, 0, st>>>(part, splits, M, N, out, accumulate);
   note_launch();
   return cudaGetLastError();
 }
@@ -431,6 +438,7 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, int split_k, float* split_scratc
   p.tiles_m = (int)ceil_div(g.M, BM);
   p.tiles_n = (int)ceil_div(g.N, BN);
   p.split_out = split_k > 1 ? split_scratch : nullptr;
+  p.wait_ns = wait_limit_ns();
   // fp32 outputs through TMA where the layout allows it (16-byte aligned base and rows)
   CUtensorMap tout;
   std::memset(&tout, 0, sizeof(tout));
@@ -473,7 +481,7 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, int split_k, float* split_scratc
   note_launch();
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess || split_k <= 1) return e;
-  return launch_split_reduce(split_scratch, split_k, g.M, g.N, g.c, st);
+  return launch_split_reduce(split_scratch, split_k, g.M, g.N, g.c, g.split_accumulate, st);
 }
 
 }  // namespace upipe

@@ -12,6 +12,13 @@ namespace upipe {
 // upipe_attn_launch_count).
 void note_launch();
 
+// Limit of every bounded device-side wait, in nanoseconds, passed to each kernel at launch
+// (upipe_attn_set_wait_limit_ns; 4 s by default).
+uint64_t wait_limit_ns();
+// A kernel whose one bounded wait nothing satisfies (arrive = 0), or one that is satisfied at
+// once (arrive = 1): the timeout path of the wait helper, reported in a table header's error word.
+cudaError_t launch_wait_probe(void* header, int arrive, cudaStream_t st);
+
 // ---------------------------------------------------------------- tile-skip table
 size_t tile_table_bytes(int64_t S);
 cudaError_t launch_tile_table(int64_t S, int causal, const int32_t* seg, void* table, cudaStream_t st);
@@ -62,6 +69,7 @@ struct TcOperand {
   const void* base;
   int rank;
   uint64_t inner, outer, planes, row_stride;
+  uint64_t plane_stride;  // rank 3: elements between planes (0: dense, outer * inner)
   int k_major;
   int blk_shift;
   int blk_dim;
@@ -73,14 +81,15 @@ struct TcGemmArgs {
   TcOperand a, b;
   GemmOutput c;
   int epi;
+  int split_accumulate;  // split_k > 1: the reduction adds the splits' sum to the fp32 output
 };
 
 // C = A * B^T with the given epilogue on the tcgen05 path.  split_k > 1 requires
 // epi == EPI_STORE_F32 and a scratch of split_k * M * N floats; the splits are reduced in a
-// fixed order (deterministic).
+// fixed order (deterministic), into C (or onto it with split_accumulate).
 cudaError_t launch_gemm_tc(const TcGemmArgs& args, int split_k, float* split_scratch, cudaStream_t st);
 cudaError_t launch_split_reduce(const float* part, int splits, int64_t M, int64_t N, const GemmOutput& out,
-                                cudaStream_t st);
+                                int accumulate, cudaStream_t st);
 
 // ---------------------------------------------------------------- attention core
 struct AttnArgs {
@@ -104,6 +113,7 @@ struct AttnArgs {
   int causal;
   float scale;      // softmax scale
   int* err;         // device error word (table header), set by bounded waits that time out
+  uint64_t wait_ns; // limit of each bounded wait (set at launch)
 };
 
 cudaError_t launch_attn_fwd(const AttnArgs& a, int head_dim, cudaStream_t st);

@@ -12,7 +12,8 @@
 namespace upipe {
 namespace tc {
 
-// A bounded wait gives up after this many nanoseconds of %globaltimer and reports a timeout.
+// A bounded wait gives up after this many nanoseconds of %globaltimer and reports a timeout
+// (the default; every launch passes the limit in effect as a kernel argument).
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
 
 __device__ __forceinline__ uint64_t globaltimer() {
@@ -43,15 +44,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete.  Returns false if the CTA's abort flag
-// is raised or the wait exceeds kWaitLimitNs (then the abort flag and the error word are set).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err) {
+// is raised or the wait exceeds limit_ns (then the abort flag and the error word are set).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int* err,
+                                          uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63) == 0) {
       if (*abort_flag) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
+      if (globaltimer() - t0 > limit_ns) {
         *abort_flag = 1;
         if (err) atomicCAS(err, 0, (int)UPIPE_ERR_DEVICE_TIMEOUT);
         return false;
@@ -286,7 +288,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 // Host: tensor maps (driver entry point resolved through the runtime, no -lcuda).
 bool make_tmap_3d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t planes,
-                       uint32_t box_inner, uint32_t box_rows);
+                       uint32_t box_inner, uint32_t box_rows, uint64_t plane_stride_elems = 0);
 bool make_tmap_2d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t row_stride_elems,
                        uint32_t box_inner, uint32_t box_rows);
 // fp32 output map of rank 2 ({inner, rows}) or 3 ({inner, rows, planes}); 32 x 32 boxes, 128-byte swizzle

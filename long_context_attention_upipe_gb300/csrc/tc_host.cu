@@ -22,12 +22,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 }  // namespace
 
+// plane_stride_elems 0: dense planes of rows x inner; else the elements between planes (a window
+// of `rows` rows out of longer planes)
 bool make_tmap_3d_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t planes,
-                       uint32_t box_inner, uint32_t box_rows) {
+                       uint32_t box_inner, uint32_t box_rows, uint64_t plane_stride_elems) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {inner, rows, planes};
-  cuuint64_t strides[2] = {inner * 2, inner * rows * 2};
+  cuuint64_t strides[2] = {inner * 2, (plane_stride_elems ? plane_stride_elems : inner * rows) * 2};
   cuuint32_t box[3] = {box_inner, box_rows, 1};
   cuuint32_t es[3] = {1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,

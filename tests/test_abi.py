@@ -80,6 +80,41 @@ def test_fwd_host_checks_run_before_any_launch():
     assert up.launch_count() == launches  # rejected calls launch nothing
 
 
+def test_offload_entry_points_check_arguments_before_any_launch():
+    d = up.make_desc(512, 256, 4, 2, 64, 2)
+    L = up.lib()
+    launches = up.launch_count()
+    fake = ctypes.c_void_p(0x10000)       # never dereferenced: the checks fail first
+    n = ctypes.c_size_t(0)
+    assert L.upipe_attn_workspace_size_offload(ctypes.byref(d), 0, 100, ctypes.byref(n)) == 1   # not a multiple of 128
+    assert L.upipe_attn_workspace_size_offload(ctypes.byref(d), 1, -128, ctypes.byref(n)) == 1
+    assert L.upipe_attn_fwd_offload(ctypes.byref(d), fake, fake, fake, None, fake, fake, fake, 1 << 40, 96, None) == 1
+    assert L.upipe_attn_fwd_offload(ctypes.byref(d), fake, fake, fake, None, fake, fake, fake, 16, 0, None) == 4
+    assert L.upipe_attn_bwd_offload(ctypes.byref(d), fake, fake, fake, None, None, fake, fake, fake, fake, fake, 1 << 40,
+                                    0, None) == 1                                               # NULL dY
+    assert up.launch_count() == launches
+
+
+def test_wait_limit_and_probe_check_arguments():
+    L = up.lib()
+    assert L.upipe_attn_set_wait_limit_ns(61 * 10 ** 9) == 1      # above the 60 s cap
+    assert L.upipe_attn_set_wait_limit_ns(0) == 0                  # the default
+    fake = ctypes.c_void_p(0x10000)
+    assert L.upipe_attn_wait_probe(None, 64, 0, None) == 1
+    assert L.upipe_attn_wait_probe(fake, 16, 0, None) == 1         # smaller than a table header
+    assert L.upipe_attn_wait_probe(ctypes.c_void_p(0x10008), 64, 0, None) == 3
+
+
+def test_offload_workspace_adds_the_staging_buffers():
+    d = up.make_desc(1 << 20, 4096, 4, 1, 128, 4)
+    for pass_, tensors in ((0, 2), (1, 4)):           # X twice; X and dY twice each
+        base = up.workspace_bytes(d, pass_)
+        off = up.workspace_bytes_offload(d, pass_, 65536)
+        assert off - base >= tensors * 65536 * 4096 * 2
+        assert off - base < tensors * 65536 * 4096 * 2 + (64 << 20)   # plus block split-K partials, alignment
+    assert up.workspace_bytes_offload(d, 1, 0) == up.workspace_bytes_offload(d, 1, 65536)   # the default
+
+
 def test_ring_entry_points_check_arguments_before_any_launch():
     L = up.lib()
     launches = up.launch_count()

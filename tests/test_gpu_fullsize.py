@@ -273,3 +273,65 @@ def test_full_size_5m_share(hpc):
     assert rel_fro(to_f64(dX[:prefix]), dX_ref) <= GRAD_REL_FRO, rel_fro(to_f64(dX[:prefix]), dX_ref)
     assert rel_fro(to_f64(dW), dW_ref) <= GRAD_REL_FRO, rel_fro(to_f64(dW), dW_ref)
     assert rel_fro(to_f64(dWo), dWo_ref) <= GRAD_REL_FRO, rel_fro(to_f64(dWo), dWo_ref)
+
+
+def test_full_size_5m_share_offload_fp32_sums():
+    """The 5M-token share with fp32 partial sums (accum_mode 0), which does not fit on the GPU
+    beside a device-resident X and dY: X and dY stay in pinned host memory and are streamed in
+    65,536-row blocks (CPU offload of the layer's inputs).  Checked as the bf16-sum run is (rows
+    against the oracle over all keys, including the ragged last tile; finite outputs; dX exactly
+    zero past the first P rows; gradients against the oracle on the first P tokens), and the
+    device peak must stay below what the same layer needs with X and dY on the device."""
+    w = ui.workload("share32b_5m")
+    S, d, Hq, Hkv, Dh = w.S, w.d, w.Hq, w.Hkv, w.Dh
+    hpc, prefix, block = 2, 1024, 1 << 20
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    # pinned host X (seeded generator, filled on the device a block at a time) and dY (prefix only)
+    hX = torch.empty((S, d), dtype=torch.bfloat16, pin_memory=True)
+    tmp = torch.empty((block, d), dtype=torch.bfloat16, device="cuda")
+    for a in range(0, S, block):
+        n = min(block, S - a)
+        ui.fill_device_bf16(tmp.data_ptr(), n * d, ui.TID_X, 1.0, first=a * d)
+        hX[a: a + n].copy_(tmp[:n])
+    hdY = torch.zeros((S, d), dtype=torch.bfloat16, pin_memory=True)
+    ui.fill_device_bf16(tmp.data_ptr(), prefix * d, ui.TID_DY, 1.0)
+    hdY[:prefix].copy_(tmp[:prefix])
+    del tmp
+    W = dev_fill(((Hq + 2 * Hkv) * Dh, d), ui.TID_WQKV, ui.W_STD)
+    Wo = dev_fill((d, Hq * Dh), ui.TID_WO, ui.W_STD)
+    desc = up.make_desc(S, d, Hq, Hkv, Dh, hpc, w.causal, 0)
+    ws_bytes = max(up.workspace_bytes_offload(desc, 0), up.workspace_bytes_offload(desc, 1))
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    torch.cuda.reset_peak_memory_stats()
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    Y = torch.empty((S, d), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((Hq, S), dtype=torch.float32, device="cuda")
+    up.fwd_offload(desc, hX, W, Wo, None, Y, lse, ws)
+    torch.cuda.synchronize()
+    assert up.device_status(ws) == 0
+    dX = torch.empty((S, d), dtype=torch.bfloat16, device="cuda")
+    dW = torch.empty(W.shape, dtype=torch.float32, device="cuda")
+    dWo = torch.empty(Wo.shape, dtype=torch.float32, device="cuda")
+    up.bwd_offload(desc, hX, W, Wo, None, hdY, lse, dX, dW, dWo, ws)
+    torch.cuda.synchronize()
+    assert up.device_status(ws) == 0
+    peak = torch.cuda.max_memory_allocated()
+    on_device = 2 * S * d * 2 + max(up.workspace_bytes(desc, 0), up.workspace_bytes(desc, 1))
+    assert peak < on_device + 2 * S * d * 2, (peak, on_device)   # X and dY never held on the device
+    assert peak <= ws_bytes + 2 * S * d * 2 + Hq * S * 4 + W.numel() * 6 + Wo.numel() * 6 + (1 << 30), peak
+    assert all_finite(Y) and all_finite(dX)
+    for t in (lse, dW, dWo):
+        assert bool(torch.isfinite(t.float()).all())
+    assert all_zero_from(dX, prefix)
+    rows = np.array([0, 1, 127, 128, 129, 1000, 2047, 2048, 4095, S // 2, 1 << 22, S - 129, S - 65, S - 64,
+                     S - 33, S - 1])
+    K, V = oracle_kv(w, hX)
+    check_rows_against_oracle(w, rows, Y, lse, K, V)
+    _, Wh, Woh, dYp = host_inputs(w, np.arange(1), prefix)
+    Xp = ui.normal_bf16_rows(np.arange(prefix), d, ui.TID_X)
+    dX_ref, dW_ref, dWo_ref = orc.layer_backward(Xp, Wh, Woh, None, dYp, Hq, Hkv, Dh, w.causal)
+    assert rel_fro(to_f64(dX[:prefix]), dX_ref) <= GRAD_REL_FRO, rel_fro(to_f64(dX[:prefix]), dX_ref)
+    assert rel_fro(to_f64(dW), dW_ref) <= GRAD_REL_FRO, rel_fro(to_f64(dW), dW_ref)
+    assert rel_fro(to_f64(dWo), dWo_ref) <= GRAD_REL_FRO, rel_fro(to_f64(dWo), dWo_ref)

@@ -333,3 +333,37 @@ def test_per_launch_timing_logs_the_schedule():
     layer.forward(Xt, Wt, Wot)
     torch.cuda.synchronize()
     assert up.timing_records() == []
+
+
+def test_bounded_wait_runs_out_and_the_gpu_stays_usable():
+    """The bounded device wait every warp-specialised kernel uses gives up after the limit, raises
+    UPIPE_ERR_DEVICE_TIMEOUT in the error word and returns: a probe kernel waits on a barrier that
+    nothing completes (and, as a control, on one it completed itself).  A layer call right after
+    it, with the default limit restored, still matches the oracle."""
+    buf = torch.zeros(64, dtype=torch.uint8, device="cuda")
+    try:
+        up.set_wait_limit_ns(2_000_000)          # 2 ms
+        up.wait_probe(buf, arrive=True)
+        assert up.device_status(buf) == 0
+        t0 = torch.cuda.Event(enable_timing=True); t1 = torch.cuda.Event(enable_timing=True)
+        t0.record()
+        up.wait_probe(buf, arrive=False)
+        t1.record()
+        assert up.device_status(buf) == 7        # UPIPE_ERR_DEVICE_TIMEOUT
+        assert 2.0 <= t0.elapsed_time(t1) < 1000.0
+    finally:
+        up.set_wait_limit_ns(0)
+    S, d, Hq, Hkv, Dh, segs, causal, hpc, accum = LAYER_CASES[0]
+    X, W, Wo, dY = layer_inputs(S, d, Hq, Hkv, Dh)
+    seg = ui.segments_from_lengths(segs)
+    layer = up.Layer(up.make_desc(S, d, Hq, Hkv, Dh, hpc, causal, accum))
+    Xt, Wt, Wot, dYt = (bf16_tensor(x) for x in (X, W, Wo, dY))
+    seg_t = torch.from_numpy(seg).cuda()
+    Y, lse = layer.forward(Xt, Wt, Wot, seg_t)
+    dX, dW, dWo = layer.backward(Xt, Wt, Wot, seg_t, dYt, lse)
+    torch.cuda.synchronize()
+    assert up.device_status(layer.ws_fwd) == 0 and up.device_status(layer.ws_bwd) == 0
+    Y_ref, _ = orc.layer_forward(X, W, Wo, seg, Hq, Hkv, Dh, causal)
+    dX_ref, _, _ = orc.layer_backward(X, W, Wo, seg, dY, Hq, Hkv, Dh, causal)
+    assert max_abs_bf16_out(to_f64(Y), Y_ref) <= OUT_MAX_ABS and rel_fro(to_f64(Y), Y_ref) <= OUT_REL_FRO
+    assert rel_fro(to_f64(dX), dX_ref) <= GRAD_REL_FRO
