@@ -372,6 +372,65 @@ def attention_backward_block(Q, K, V, dO, L, D, causal: bool, scale: float):
 
 
 # ----------------------------------------------------------------------------------------------
+# the feed-forward step beside the layer, cut into sequence tiles (Arctic sequence tiling)
+# ----------------------------------------------------------------------------------------------
+# The pages compute the loss and the MLP in pieces along the sequence so that no buffer has a
+# multi-million-token axis ("Road to 5 Million Tokens" podcast summary, 概要 and 章節 on sequence
+# tiling of the element-wise operations; neuro-slop.ru transcript, Полезные советы: loss and MLP
+# can be computed in chunks).  Every row of an MLP is computed independently, so cutting the rows
+# into tiles changes nothing: the oracle is the plain, untiled definition.  The pages do not
+# write the MLP; for the Llama-3.1-shaped configurations it is the Llama feed-forward block,
+# SwiGLU:  Y = (silu(X Wg^T) * (X Wu^T)) Wd^T,  silu(x) = x / (1 + e^-x).
+
+def silu(x):
+    """x * sigmoid(x), float64."""
+    x = np.asarray(x, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return x / (1.0 + np.exp(-x))
+
+
+def silu_grad(x):
+    """d silu / dx = sigmoid(x) (1 + x (1 - sigmoid(x)))."""
+    x = np.asarray(x, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        sg = 1.0 / (1.0 + np.exp(-x))
+    return sg * (1.0 + x * (1.0 - sg))
+
+
+def mlp_forward(X, Wgu, Wd, return_all=False):
+    """SwiGLU feed-forward of every row of X [S, d]:  G = X Wg^T, U = X Wu^T (Wgu = [Wg; Wu],
+    [2F, d], gate rows first, nn.Linear layout), A = silu(G) * U, Y = A Wd^T (Wd [d, F]).
+    Inputs are bf16 bit patterns (uint16) or floats, widened exactly to float64."""
+    X, Wgu, Wd = _widen(X), _widen(Wgu), _widen(Wd)
+    F = Wgu.shape[0] // 2
+    G = X @ Wgu[:F].T
+    U = X @ Wgu[F:].T
+    A = silu(G) * U
+    Y = A @ Wd.T
+    if return_all:
+        return Y, dict(G=G, U=U, A=A)
+    return Y
+
+
+def mlp_backward(X, Wgu, Wd, dY):
+    """Gradients of sum(dY * Y) for mlp_forward (chain rule):  dA = dY Wd,  dWd = dY^T A,
+    dG = dA * U * silu'(G),  dU = dA * silu(G),  dX = dG Wg + dU Wu,  dWgu = [dG^T X; dU^T X].
+    Returns dX [S, d], dWgu [2F, d], dWd [d, F] (float64)."""
+    X, Wgu, Wd, dY = _widen(X), _widen(Wgu), _widen(Wd), _widen(dY)
+    F = Wgu.shape[0] // 2
+    G = X @ Wgu[:F].T
+    U = X @ Wgu[F:].T
+    A = silu(G) * U
+    dA = dY @ Wd
+    dWd = dY.T @ A
+    dG = dA * U * silu_grad(G)
+    dU = dA * silu(G)
+    dX = dG @ Wgu[:F] + dU @ Wgu[F:]
+    dWgu = np.concatenate([dG.T @ X, dU.T @ X], axis=0)
+    return dX, dWgu, dWd
+
+
+# ----------------------------------------------------------------------------------------------
 # tile-skip table (Splash-style block skipping, MaxText article)
 # ----------------------------------------------------------------------------------------------
 

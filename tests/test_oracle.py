@@ -443,3 +443,78 @@ def test_bf16_widening_is_exact():
     np.testing.assert_array_equal(orc.bf16_bits_to_f64(vals), want)
     t = torch.tensor(vals.view(np.int16)).view(torch.bfloat16).double().numpy()
     np.testing.assert_array_equal(orc.bf16_bits_to_f64(vals), t)
+
+
+# ------------------------------------------------------------------------------------------
+# 8. the sequence-tiled feed-forward step (SwiGLU MLP)
+# ------------------------------------------------------------------------------------------
+
+def _mlp_inputs(S=24, d=16, F=40, seed=3):
+    rng = np.random.default_rng(seed)
+    X = rng.standard_normal((S, d))
+    Wgu = rng.standard_normal((2 * F, d)) * 0.3
+    Wd = rng.standard_normal((d, F)) * 0.3
+    dY = rng.standard_normal((S, d))
+    return X, Wgu, Wd, dY
+
+
+def test_silu_special_values():
+    assert orc.silu(0.0) == 0.0
+    assert orc.silu_grad(0.0) == 0.5
+    np.testing.assert_allclose(orc.silu(np.array([30.0, -30.0])), [30.0, -30.0 * math.exp(-30.0)], rtol=1e-12)
+    assert orc.silu(-1e4) == 0.0                       # no overflow warning turns into a NaN
+    # derivative against a central difference
+    x = np.linspace(-6, 6, 97)
+    h = 1e-6
+    np.testing.assert_allclose(orc.silu_grad(x), (orc.silu(x + h) - orc.silu(x - h)) / (2 * h), atol=1e-8)
+
+
+def test_mlp_matches_torch_autograd():
+    X, Wgu, Wd, dY = _mlp_inputs()
+    F = Wgu.shape[0] // 2
+    tX, tW, tD = (torch.tensor(a, requires_grad=True) for a in (X, Wgu, Wd))
+    Y = (torch.nn.functional.silu(tX @ tW[:F].T) * (tX @ tW[F:].T)) @ tD.T
+    Y.backward(torch.tensor(dY))
+    np.testing.assert_allclose(orc.mlp_forward(X, Wgu, Wd), Y.detach().numpy(), rtol=1e-12, atol=1e-12)
+    dX, dW, dD = orc.mlp_backward(X, Wgu, Wd, dY)
+    for got, want in ((dX, tX.grad), (dW, tW.grad), (dD, tD.grad)):
+        np.testing.assert_allclose(got, want.numpy(), rtol=1e-11, atol=1e-11)
+
+
+def test_mlp_gradients_finite_differences():
+    X, Wgu, Wd, dY = _mlp_inputs(S=6, d=5, F=7, seed=11)
+    dX, dW, dD = orc.mlp_backward(X, Wgu, Wd, dY)
+    loss = lambda X_, W_, D_: float((orc.mlp_forward(X_, W_, D_) * dY).sum())
+    h = 1e-6
+    for arr, grad, which in ((X, dX, 0), (Wgu, dW, 1), (Wd, dD, 2)):
+        num = np.zeros_like(arr)
+        for idx in np.ndindex(arr.shape):
+            a1, a2 = arr.copy(), arr.copy()
+            a1[idx] += h
+            a2[idx] -= h
+            args1, args2 = [X, Wgu, Wd], [X, Wgu, Wd]
+            args1[which], args2[which] = a1, a2
+            num[idx] = (loss(*args1) - loss(*args2)) / (2 * h)
+        np.testing.assert_allclose(grad, num, rtol=1e-6, atol=1e-7)
+
+
+def test_mlp_closed_forms_and_row_independence():
+    X, Wgu, Wd, dY = _mlp_inputs()
+    F = Wgu.shape[0] // 2
+    # up projection zero: the output and every gradient but dWu vanish
+    W0 = Wgu.copy()
+    W0[F:] = 0.0
+    assert not np.any(orc.mlp_forward(X, W0, Wd))
+    dX, dW, dD = orc.mlp_backward(X, W0, Wd, dY)
+    assert not np.any(dX) and not np.any(dW[:F]) and not np.any(dD)
+    assert np.any(dW[F:])
+    # one row, one hidden unit, by hand
+    x, wg, wu, wd = 0.7, -1.3, 0.4, 2.0
+    want = (wg * x / (1 + math.exp(-wg * x))) * (wu * x) * wd
+    got = orc.mlp_forward(np.array([[x]]), np.array([[wg], [wu]]), np.array([[wd]]))
+    assert abs(got[0, 0] - want) < 1e-15
+    # rows are independent: perturbing other rows leaves a row's output unchanged (the tiling premise)
+    Y = orc.mlp_forward(X, Wgu, Wd)
+    X2 = X.copy()
+    X2[5:] += 1.0
+    np.testing.assert_array_equal(orc.mlp_forward(X2, Wgu, Wd)[:5], Y[:5])
