@@ -46,6 +46,7 @@ def parse():
                     "a CUDA graph of them")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-offload", action="store_true", help="skip the leg with X and dY in pinned host memory")
+    ap.add_argument("--no-mlp", action="store_true", help="skip the sequence-tiled MLP leg")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--sample-tokens", type=int, default=1024, help="oracle sample length (CPU legs)")
     ap.add_argument("--kernel", default=None, choices=["fwd", "recompute", "dq", "dkdv", "lse_merge", "ring", "ring_bwd"],
@@ -296,6 +297,101 @@ def summarize_kernels(recs, w, peaks, step_ms):
     return out
 
 
+MLP_S, MLP_D, MLP_F, MLP_TILE = 131072, 4096, 14336, 8192
+MLP_KINDS = {"mlp_gate_up", "mlp_down", "mlp_dact", "mlp_dwd", "mlp_dx", "mlp_dwgu"}
+
+
+def mlp_flops(S, d, F):
+    """Algorithmic FLOPs of the SwiGLU MLP, forward + backward: 6 S d F forward (gate/up and down
+    projections), 12 S d F backward (dA, dWd, dX, dWgu); the backward's recompute of the gate/up
+    projection (4 S d F) is executed but not counted."""
+    return 18.0 * S * d * F
+
+
+def mlp_leg(up, torch, dev, peaks, time_steps):
+    """The sequence-tiled feed-forward step beside the layer: the Llama-3.1-8B MLP (hidden 4096,
+    ffn 14336) over 131,072 tokens, the per-GPU sequence shard of the 1M-token sequence under an
+    8-way Ulysses layout, in tiles of 8192 rows against one untiled pass: time, device peak and
+    the kernels of one instrumented tiled step."""
+    import gc
+    import upipe_inputs as ui
+    S, d, F = MLP_S, MLP_D, MLP_F
+    out = {"workload": f"llama3.1-8b-mlp_S{S}_d{d}_ffn{F}_swiglu", "flops_per_step": mlp_flops(S, d, F)}
+
+    def fill(shape, tid, std):
+        t = torch.empty(shape, dtype=torch.bfloat16, device=dev)
+        ui.fill_device_bf16(t.data_ptr(), t.numel(), tid, std)
+        return t
+
+    X, Wgu, Wd, dY = fill((S, d), ui.TID_X, 1.0), fill((2 * F, d), 6, ui.W_STD), fill((d, F), 7, ui.W_STD), \
+        fill((S, d), ui.TID_DY, 1.0)
+    runs = []
+    for T in (MLP_TILE, 0):
+        gc.collect()
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        before = torch.cuda.memory_allocated(dev)
+        torch.cuda.reset_peak_memory_stats(dev)
+        desc = up.make_mlp_desc(S, d, F, T)
+        ws = torch.empty(max(up.mlp_workspace_bytes(desc, 0), up.mlp_workspace_bytes(desc, 1)), dtype=torch.uint8,
+                         device=dev)
+        Y, dX = torch.empty_like(X), torch.empty_like(X)
+        dW = torch.empty(Wgu.shape, dtype=torch.float32, device=dev)
+        dD = torch.empty(Wd.shape, dtype=torch.float32, device=dev)
+
+        def step():
+            up.mlp_fwd(desc, X, Wgu, Wd, Y, ws)
+            up.mlp_bwd(desc, X, Wgu, Wd, dY, dX, dW, dD, ws)
+
+        step()
+        ms = time_steps(step, 3)
+        pk = torch.cuda.max_memory_allocated(dev)
+        r = {"tile_rows": T if T else S, "ms_per_step": ms, "tflops": out["flops_per_step"] / (ms * 1e-3) / 1e12,
+             "workspace_gb": round(ws.numel() / 1e9, 3), "layer_peak_gb": round((pk - before) / 1e9, 3)}
+        if T:
+            torch.cuda.synchronize()
+            up.timing_records()
+            up.timing_enable(True)
+            try:
+                step()
+                torch.cuda.synchronize()
+            finally:
+                up.timing_enable(False)
+            recs = up.timing_records()
+            kern = {}
+            for rec in recs:
+                k = kern.setdefault(rec["kind"], {"launches": 0, "ms": 0.0, "flops": 0.0, "bytes": 0.0})
+                k["launches"] += 1
+                k["ms"] += rec["ms"]
+                if rec["kind"] in MLP_KINDS:
+                    k["flops"] += 2.0 * rec["m"] * rec["n"] * rec["k"]
+                elif rec["kind"] == "mlp_act":
+                    k["bytes"] += 6.0 * rec["m"]
+                elif rec["kind"] == "mlp_act_bwd":
+                    k["bytes"] += 12.0 * rec["m"]
+            for name, k in kern.items():
+                sec = k["ms"] * 1e-3
+                if k["flops"]:
+                    k["tflops"] = k["flops"] / sec / 1e12
+                    k["frac"] = k["tflops"] / peaks["bf16_tflops"]
+                if k["bytes"]:
+                    k["gbs"] = k["bytes"] / sec / 1e9
+                    k["frac"] = k["gbs"] / peaks["hbm_gbs"]
+                    k["bound"] = "hbm"
+                else:
+                    k["bound"] = "tensor"
+                del k["flops"], k["bytes"]
+            r["kernels"] = kern
+        runs.append(r)
+        del ws, Y, dX, dW, dD, step
+    out["runs"] = runs
+    out["peak_ratio_untiled_over_tiled"] = runs[1]["layer_peak_gb"] / max(runs[0]["layer_peak_gb"], 1e-9)
+    del X, Wgu, Wd, dY
+    gc.collect()
+    torch.cuda.empty_cache()
+    return out
+
+
 def instrumented_step(up, step, w, peaks, step_ms):
     """One eager step with the library's per-launch event timing on; per-kernel summary."""
     import torch
@@ -396,6 +492,17 @@ def main():
         if world > 1:
             torch.distributed.barrier()
         torch.cuda.synchronize()
+
+    def time_local(step, n):
+        """This rank's device time per call (no process-group barrier)."""
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(n):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
 
     def time_steps(step, n):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -532,25 +639,44 @@ def main():
         odW = torch.empty(W.shape, dtype=torch.float32, device=dev)
         odWo = torch.empty(Wo.shape, dtype=torch.float32, device=dev)
 
-        def ostep():
-            up.fwd_offload(odesc, hX, W, Wo, seg_t, oY, olse, ows, 0, stream)
-            up.bwd_offload(odesc, hX, W, Wo, seg_t, hdY, olse, odX, odW, odWo, ows, 0, stream)
-
-        ostep()
-        t_off = max_over_ranks(time_steps(ostep, 2 if w.S >= (1 << 19) else 3), dev)
-        pk = torch.cuda.max_memory_allocated(dev)
-        inputs = sum(x.numel() * x.element_size() for x in (X, dY))
-        held = pk - before + (before - inputs)          # everything on the device but X and dY
         n_chunks = Hq // args.hpc
-        offload = {"heads_per_chunk": args.hpc, "stage_rows": 65536, "ms_per_step": t_off,
-                   "tflops": job_value(flops, world, t_off), "device_peak_gb": round(held / 1e9, 3),
-                   "h2d_bytes_per_step": n_chunks * inputs // 2 + 2 * n_chunks * inputs,
-                   "what": "X and dY in pinned host memory, staged in row blocks by the library (upipe_attn_fwd_offload "
-                           "/ upipe_attn_bwd_offload); device peak excludes X and dY"}
+        xb = X.numel() * X.element_size()
+        # host -> device copy bandwidth of this machine (pinned memory, one large copy)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        dst = torch.empty_like(X)
+        dst.copy_(hX, non_blocking=True)
+        e0.record(stream)
+        dst.copy_(hX, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        h2d_gbs = xb / (e0.elapsed_time(e1) * 1e-3) / 1e9
+        del dst
+        offload = {"heads_per_chunk": args.hpc, "stage_rows": 65536, "h2d_gbs_measured": round(h2d_gbs, 1),
+                   "what": "upipe_attn_fwd_offload / upipe_attn_bwd_offload: host tensors staged in row blocks by the "
+                           "library; device peak excludes X (and dY when it is on the host)", "runs": []}
+        for name, xa, dya, h2d in (("X on host, dY on device", hX, dY, 3 * n_chunks * xb),
+                                   ("X and dY on host", hX, hdY, 5 * n_chunks * xb)):
+            torch.cuda.synchronize()
+            torch.cuda.reset_peak_memory_stats(dev)
+
+            def ostep():
+                up.fwd_offload(odesc, xa, W, Wo, seg_t, oY, olse, ows, 0, stream)
+                up.bwd_offload(odesc, xa, W, Wo, seg_t, dya, olse, odX, odW, odWo, ows, 0, stream)
+
+            ostep()
+            t_off = max_over_ranks(time_steps(ostep, 2 if w.S >= (1 << 19) else 3), dev)
+            pk = torch.cuda.max_memory_allocated(dev)
+            off_dev = xb if dya is dY else 2 * xb      # the device copies of X (and dY) an offloading caller lacks
+            offload["runs"].append({"placement": name, "ms_per_step": t_off, "tflops": job_value(flops, world, t_off),
+                                    "device_peak_gb": round((pk - off_dev) / 1e9, 3), "h2d_bytes_per_step": h2d})
         del ows, oY, odX, olse, odW, odWo, hX, hdY
         gc.collect()
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
+
+    mlp = None
+    if not args.no_mlp and rank == 0:
+        mlp = mlp_leg(up, torch, dev, peaks, time_local)
 
     # ---------------- main timed run
     torch.cuda.reset_peak_memory_stats(dev)
@@ -691,7 +817,8 @@ def main():
                              f"{dt:.2f} s for {fl / 1e12:.4f} TFLOP"}
 
         if offload is not None:
-            offload["time_vs_resident"] = offload["ms_per_step"] / ms_all
+            for r in offload["runs"]:
+                r["time_vs_resident"] = r["ms_per_step"] / ms_all
             res = next((e for e in sweep if e["heads_per_chunk"] == args.hpc), None)
             if res is not None:
                 offload["resident_device_peak_gb"] = res["peak_hbm_gb"]
@@ -717,6 +844,7 @@ def main():
             "step_kernels": step_kernels,
             "hpc_sweep": sweep,
             "offload": offload,
+            "mlp_tiled": mlp,
             "e2e": e2e,
             "cpu_baseline": cpu,
             "gpu_launches": launches,

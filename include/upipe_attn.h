@@ -151,8 +151,11 @@ upipe_status_t upipe_attn_bwd(const upipe_attn_desc_t* desc, const uint16_t* X, 
  * overlap the projections.  Per chunk the forward streams X once (the Q/K/V projection); the
  * backward streams X and dY twice (the Q/K/V and dO projections before the attention kernels,
  * the weight gradients dWo and dWqkv after them, summed block by block in a fixed order).
- *   X_host, dY_host  page-locked host bf16 [S, d] (cudaHostAlloc or cudaHostRegister); anything
- *                    else is rejected with UPIPE_ERR_INVALID_ARG before any launch
+ *   X_host, dY_host  bf16 [S, d], each either page-locked host memory (cudaHostAlloc or
+ *                    cudaHostRegister), which is staged, or device memory, which is read in place
+ *                    (a training stack offloads the block input X; its dY is produced on the device
+ *                    during the backward); pageable host memory is rejected with
+ *                    UPIPE_ERR_INVALID_ARG before any launch
  *   ws               device workspace of upipe_attn_workspace_size_offload(desc, pass, stage_rows)
  *                    bytes (the regular workspace plus 2 or 4 staging buffers of stage_rows x d)
  * Y, lse and dX are bit-identical to the regular calls'; dWqkv and dWo equal theirs to rounding
@@ -167,6 +170,36 @@ upipe_status_t upipe_attn_bwd_offload(const upipe_attn_desc_t* desc, const uint1
                                       const uint16_t* Wo, const int32_t* seg, const uint16_t* dY_host, const float* lse,
                                       uint16_t* dX, float* dWqkv, float* dWo, void* ws, size_t ws_bytes,
                                       int64_t stage_rows, void* stream);
+
+/* The feed-forward step beside the attention layer, computed in tiles of rows along the sequence
+ * so that no intermediate spans the whole sequence (sequence tiling of the element-wise steps:
+ * "Road to 5 Million Tokens" podcast summary, 概要 and the chapter on tiling; neuro-slop.ru
+ * transcript, Полезные советы: the loss and the MLP can be computed in pieces).  The pages do not
+ * write the MLP; for the Llama-3.1-shaped layers it is the Llama feed-forward block (SwiGLU):
+ *   Y = (silu(X Wg^T) * (X Wu^T)) Wd^T,  silu(x) = x / (1 + e^-x).
+ * Per tile of T rows: H = X_t [Wg; Wu]^T (tensor cores, bf16 [T][2F]), A = silu(G) * U (bf16
+ * [T][F]), Y_t = A Wd^T.  The backward recomputes H per tile, then dA = dY_t Wd, [dG | dU] and A,
+ * dX_t = [dG | dU] [Wg; Wu], and adds the tile's dWd = dY_t^T A and dWgu = [dG | dU]^T X_t to the
+ * weight gradients (summed over tiles in a fixed order).  The workspace holds one tile's H, A,
+ * dA and dH: 2T(2F + F) bytes forward, 2T(6F) backward (plus split-K partials), so memory
+ * grows with tile_rows, not with S.
+ *   seq_len    S (1 .. 2^31 - 1)
+ *   hidden     d, multiple of 64;  ffn  F, multiple of 64
+ *   tile_rows  rows per tile, a multiple of 128, or 0 for one tile of all S rows (untiled)
+ *   X, Y, dY, dX  device bf16 [S, d];  Wgu device bf16 [2F, d] (gate rows, then up rows);
+ *   Wd device bf16 [d, F];  dWgu, dWd device fp32, same shapes (written, not accumulated). */
+typedef struct {
+  int64_t seq_len;
+  int32_t hidden;
+  int32_t ffn;
+  int64_t tile_rows;
+} upipe_mlp_desc_t;
+upipe_status_t upipe_mlp_workspace_size(const upipe_mlp_desc_t* desc, int pass, size_t* bytes);
+upipe_status_t upipe_mlp_fwd(const upipe_mlp_desc_t* desc, const uint16_t* X, const uint16_t* Wgu, const uint16_t* Wd,
+                             uint16_t* Y, void* ws, size_t ws_bytes, void* stream);
+upipe_status_t upipe_mlp_bwd(const upipe_mlp_desc_t* desc, const uint16_t* X, const uint16_t* Wgu, const uint16_t* Wd,
+                             const uint16_t* dY, uint16_t* dX, float* dWgu, float* dWd, void* ws, size_t ws_bytes,
+                             void* stream);
 
 /* Forward pass for callers that cannot allocate device memory (for example code recorded into
  * someone else's CUDA graph, or a plugin that only receives input and output pointers).  The
@@ -291,7 +324,10 @@ upipe_status_t upipe_attn_no_alloc_device_status(int32_t* code, void* stream);
 enum {
   UPIPE_K_TILE_TABLE = 0, UPIPE_K_QKV_PROJ = 1, UPIPE_K_ATTN_FWD = 2, UPIPE_K_O_PROJ = 3, UPIPE_K_CONVERT = 4,
   UPIPE_K_DO_PROJ = 5, UPIPE_K_RECOMPUTE = 6, UPIPE_K_DWO = 7, UPIPE_K_BWD_DQ = 8, UPIPE_K_BWD_DKDV = 9,
-  UPIPE_K_DX_PROJ = 10, UPIPE_K_DWQKV = 11, UPIPE_K_ZERO = 12
+  UPIPE_K_DX_PROJ = 10, UPIPE_K_DWQKV = 11, UPIPE_K_ZERO = 12,
+  /* the sequence-tiled MLP (upipe_mlp_fwd / upipe_mlp_bwd) */
+  UPIPE_K_MLP_GATE_UP = 13, UPIPE_K_MLP_ACT = 14, UPIPE_K_MLP_DOWN = 15, UPIPE_K_MLP_DACT = 16,
+  UPIPE_K_MLP_ACT_BWD = 17, UPIPE_K_MLP_DWD = 18, UPIPE_K_MLP_DX = 19, UPIPE_K_MLP_DWGU = 20
 };
 typedef struct {
   int32_t kind, epilogue, split_k, chunk;

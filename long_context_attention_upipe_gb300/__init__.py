@@ -26,17 +26,30 @@ EXPORTS = ["upipe_attn_status_string", "upipe_attn_last_error_string", "upipe_at
            "upipe_attn_ring_bwd_prep", "upipe_attn_accumulate", "upipe_attn_last_device_error",
            "upipe_attn_no_alloc_device_status", "upipe_attn_timing_enable", "upipe_attn_timing_collect",
            "upipe_attn_workspace_size_offload", "upipe_attn_fwd_offload", "upipe_attn_bwd_offload",
-           "upipe_attn_set_wait_limit_ns", "upipe_attn_wait_probe"]
+           "upipe_attn_set_wait_limit_ns", "upipe_attn_wait_probe", "upipe_mlp_workspace_size", "upipe_mlp_fwd",
+           "upipe_mlp_bwd"]
 
 # kinds of the per-launch timing records (upipe_attn_timing_collect)
 KERNEL_KINDS = {0: "tile_table", 1: "qkv_proj", 2: "attn_fwd", 3: "o_proj", 4: "convert", 5: "do_proj",
-                6: "recompute", 7: "dwo", 8: "bwd_dq", 9: "bwd_dkdv", 10: "dx_proj", 11: "dwqkv", 12: "zero"}
+                6: "recompute", 7: "dwo", 8: "bwd_dq", 9: "bwd_dkdv", 10: "dx_proj", 11: "dwqkv", 12: "zero",
+                13: "mlp_gate_up", 14: "mlp_act", 15: "mlp_down", 16: "mlp_dact", 17: "mlp_act_bwd", 18: "mlp_dwd",
+                19: "mlp_dx", 20: "mlp_dwgu"}
 
 
 class Desc(ctypes.Structure):
     _fields_ = [("seq_len", ctypes.c_int64), ("hidden", ctypes.c_int32), ("n_q_heads", ctypes.c_int32),
                 ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("heads_per_chunk", ctypes.c_int32),
                 ("causal", ctypes.c_int32), ("accum_mode", ctypes.c_int32), ("softmax_scale", ctypes.c_float)]
+
+
+class MlpDesc(ctypes.Structure):
+    _fields_ = [("seq_len", ctypes.c_int64), ("hidden", ctypes.c_int32), ("ffn", ctypes.c_int32),
+                ("tile_rows", ctypes.c_int64)]
+
+
+def make_mlp_desc(S, d, F, tile_rows=0) -> MlpDesc:
+    """Sequence-tiled SwiGLU MLP: tile_rows rows per tile (multiple of 128), 0 = one tile (untiled)."""
+    return MlpDesc(int(S), int(d), int(F), int(tile_rows))
 
 
 def make_desc(S, d, Hq, Hkv, Dh, hpc=None, causal=True, accum_mode=0, scale=0.0) -> Desc:
@@ -91,6 +104,9 @@ def lib():
             "upipe_attn_no_alloc_device_status": ([ctypes.POINTER(ctypes.c_int32), P], ctypes.c_int),
             "upipe_attn_timing_enable": ([ctypes.c_int32], ctypes.c_int),
             "upipe_attn_set_wait_limit_ns": ([ctypes.c_uint64], ctypes.c_int),
+            "upipe_mlp_workspace_size": ([ctypes.POINTER(MlpDesc), ctypes.c_int, ctypes.POINTER(SZ)], ctypes.c_int),
+            "upipe_mlp_fwd": ([ctypes.POINTER(MlpDesc), P, P, P, P, P, SZ, P], ctypes.c_int),
+            "upipe_mlp_bwd": ([ctypes.POINTER(MlpDesc), P, P, P, P, P, P, P, P, SZ, P], ctypes.c_int),
             "upipe_attn_wait_probe": ([P, SZ, ctypes.c_int32, P], ctypes.c_int),
             "upipe_attn_workspace_size_offload": ([D, ctypes.c_int, I64, ctypes.POINTER(SZ)], ctypes.c_int),
             "upipe_attn_fwd_offload": ([D, P, P, P, P, P, P, P, SZ, I64, P], ctypes.c_int),
@@ -218,23 +234,40 @@ def workspace_bytes_offload(desc: Desc, pass_: int, stage_rows: int = 0) -> int:
 
 
 def _host_bf16(t):
-    assert t.dtype == torch.bfloat16 and t.is_contiguous() and t.device.type == "cpu" and t.is_pinned(), \
-        "pinned host bf16 contiguous tensor expected"
+    """A bf16 tensor the offloaded calls stage from pinned host memory, or read in place on the device."""
+    assert t.dtype == torch.bfloat16 and t.is_contiguous() and (t.is_cuda or t.is_pinned()), \
+        "pinned host or device bf16 contiguous tensor expected"
     return _ptr(t)
 
 
 def fwd_offload(desc: Desc, X_host, Wqkv, Wo, seg, Y, lse, ws, stage_rows=0, stream=None):
-    """Forward with X in pinned host memory, brought in stage_rows rows at a time."""
+    """Forward with X in pinned host memory (or on the device), staged stage_rows rows at a time."""
     _check(lib().upipe_attn_fwd_offload(ctypes.byref(desc), _host_bf16(X_host), _bf16(Wqkv), _bf16(Wo), _ptr(seg),
                                         _bf16(Y), _ptr(lse), _ptr(ws), ws.numel() * ws.element_size(), stage_rows,
                                         _stream(stream)), "fwd_offload")
 
 
 def bwd_offload(desc: Desc, X_host, Wqkv, Wo, seg, dY_host, lse, dX, dWqkv, dWo, ws, stage_rows=0, stream=None):
-    """Backward with X and dY in pinned host memory, brought in stage_rows rows at a time."""
+    """Backward with X and / or dY in pinned host memory (each may also be on the device)."""
     _check(lib().upipe_attn_bwd_offload(ctypes.byref(desc), _host_bf16(X_host), _bf16(Wqkv), _bf16(Wo), _ptr(seg),
                                         _host_bf16(dY_host), _ptr(lse), _bf16(dX), _ptr(dWqkv), _ptr(dWo), _ptr(ws),
                                         ws.numel() * ws.element_size(), stage_rows, _stream(stream)), "bwd_offload")
+
+
+def mlp_workspace_bytes(desc: MlpDesc, pass_: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().upipe_mlp_workspace_size(ctypes.byref(desc), pass_, ctypes.byref(n)), "mlp_workspace_size")
+    return n.value
+
+
+def mlp_fwd(desc: MlpDesc, X, Wgu, Wd, Y, ws, stream=None):
+    _check(lib().upipe_mlp_fwd(ctypes.byref(desc), _bf16(X), _bf16(Wgu), _bf16(Wd), _bf16(Y), _ptr(ws),
+                               ws.numel() * ws.element_size(), _stream(stream)), "mlp_fwd")
+
+
+def mlp_bwd(desc: MlpDesc, X, Wgu, Wd, dY, dX, dWgu, dWd, ws, stream=None):
+    _check(lib().upipe_mlp_bwd(ctypes.byref(desc), _bf16(X), _bf16(Wgu), _bf16(Wd), _bf16(dY), _bf16(dX), _ptr(dWgu),
+                               _ptr(dWd), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)), "mlp_bwd")
 
 
 def core_fwd(desc: Desc, q, k, v, seg, table, o, lse, stream=None):

@@ -16,7 +16,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libupipe_attn.so")
 INCLUDE = os.path.join(ROOT, "include")
 
-SOURCES = ["api.cu", "tile_table.cu", "gemm_tc.cu", "attn_fwd_tc.cu", "attn_bwd_tc.cu", "tc_host.cu", "small.cu", "no_alloc.cu", "ring.cu", "wait_probe.cu"]
+SOURCES = ["api.cu", "tile_table.cu", "gemm_tc.cu", "attn_fwd_tc.cu", "attn_bwd_tc.cu", "tc_host.cu", "small.cu", "no_alloc.cu", "ring.cu", "wait_probe.cu", "mlp.cu"]
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
               "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]
 

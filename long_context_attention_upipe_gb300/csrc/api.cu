@@ -507,8 +507,10 @@ upipe_status_t run_bwd(const Plan& p, const bf16* X, const bf16* Wqkv, const bf1
 // Events order the reuse of a staging buffer after the kernels that read it.
 class Stager {
  public:
-  Stager(const Plan& p, void* ws, cudaStream_t st, const bf16* hx, const bf16* hdy)
-      : p_(p), ws_(ws), st_(st), hx_(hx), hdy_(hdy) {}
+  // hx / hdy: the tensors; those with *_host set are staged, the others are device memory read in
+  // place (a device-resident dY, for instance, as a training stack produces it in the backward)
+  Stager(const Plan& p, void* ws, cudaStream_t st, const bf16* hx, bool x_host, const bf16* hdy, bool dy_host)
+      : p_(p), ws_(ws), st_(st), hx_(hx), hdy_(hdy), x_host_(x_host), dy_host_(dy_host) {}
   ~Stager() {
     for (cudaEvent_t e : {entry_, ready_[0], ready_[1], free_[0], free_[1]})
       if (e) cudaEventDestroy(e);
@@ -527,16 +529,17 @@ class Stager {
   int64_t blocks() const { return ceil_div(p_.S, p_.R); }
   int64_t row0(int64_t b) const { return b * p_.R; }
   int64_t rows(int64_t b) const { return std::min(p_.R, p_.S - b * p_.R); }
-  const bf16* x(int64_t b) const { return at<bf16>(ws_, p_.xs[b & 1]); }
-  const bf16* dy(int64_t b) const { return at<bf16>(ws_, p_.dys[b & 1]); }
+  const bf16* x(int64_t b) const { return x_host_ ? at<bf16>(ws_, p_.xs[b & 1]) : hx_ + row0(b) * p_.d; }
+  const bf16* dy(int64_t b) const { return dy_host_ ? at<bf16>(ws_, p_.dys[b & 1]) : hdy_ + row0(b) * p_.d; }
   // copy block b of each host tensor into staging buffer b % 2 once its last readers are done
   cudaError_t prefetch(int64_t b) {
     const int k = (int)(b & 1);
     const size_t bytes = (size_t)rows(b) * p_.d * sizeof(bf16);
     const size_t off = (size_t)row0(b) * p_.d;
     cudaError_t e = cudaStreamWaitEvent(cs_, free_[k], 0);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(at<bf16>(ws_, p_.xs[k]), hx_ + off, bytes, cudaMemcpyHostToDevice, cs_);
-    if (e == cudaSuccess && hdy_)
+    if (e == cudaSuccess && x_host_)
+      e = cudaMemcpyAsync(at<bf16>(ws_, p_.xs[k]), hx_ + off, bytes, cudaMemcpyHostToDevice, cs_);
+    if (e == cudaSuccess && hdy_ && dy_host_)
       e = cudaMemcpyAsync(at<bf16>(ws_, p_.dys[k]), hdy_ + off, bytes, cudaMemcpyHostToDevice, cs_);
     if (e == cudaSuccess) e = cudaEventRecord(ready_[k], cs_);
     return e;
@@ -550,6 +553,7 @@ class Stager {
   cudaStream_t st_;
   const bf16* hx_;
   const bf16* hdy_;
+  bool x_host_, dy_host_;
   cudaStream_t cs_ = nullptr;
   cudaEvent_t entry_ = nullptr, ready_[2] = {nullptr, nullptr}, free_[2] = {nullptr, nullptr};
 };
@@ -581,9 +585,9 @@ cudaError_t block_weight_grad(TcGemmArgs g, int64_t b, int split, float* scratch
   return launch_gemm_tc(g, split, scratch, st);
 }
 
-upipe_status_t run_fwd_offload(const Plan& p, const bf16* hX, const bf16* Wqkv, const bf16* Wo, const int32_t* seg,
-                               bf16* Y, float* lse, void* ws, cudaStream_t st) {
-  Stager sg(p, ws, st, hX, nullptr);
+upipe_status_t run_fwd_offload(const Plan& p, const bf16* hX, bool x_host, const bf16* Wqkv, const bf16* Wo,
+                               const int32_t* seg, bf16* Y, float* lse, void* ws, cudaStream_t st) {
+  Stager sg(p, ws, st, hX, x_host, nullptr, false);
   UPIPE_CUDA(sg.begin());
   {
     Timed t(UPIPE_K_TILE_TABLE, 0, p.S, 0, 0, 1, -1, st);
@@ -625,10 +629,10 @@ upipe_status_t run_fwd_offload(const Plan& p, const bf16* hX, const bf16* Wqkv, 
 // the attention kernels the chunk's Q (K, V) and dO projections; after them the weight
 // gradients dWo_c = dY^T O_c and dWqkv_c = dQKV_c^T X, summed block by block.  dX needs neither
 // X nor dY and runs over the whole sequence as in upipe_attn_bwd.
-upipe_status_t run_bwd_offload(const Plan& p, const bf16* hX, const bf16* Wqkv, const bf16* Wo, const int32_t* seg,
-                               const bf16* hdY, const float* lse, bf16* dX, float* dWqkv, float* dWo, void* ws,
-                               cudaStream_t st) {
-  Stager sg(p, ws, st, hX, hdY);
+upipe_status_t run_bwd_offload(const Plan& p, const bf16* hX, bool x_host, const bf16* Wqkv, const bf16* Wo,
+                               const int32_t* seg, const bf16* hdY, bool dy_host, const float* lse, bf16* dX,
+                               float* dWqkv, float* dWo, void* ws, cudaStream_t st) {
+  Stager sg(p, ws, st, hX, x_host, hdY, dy_host);
   UPIPE_CUDA(sg.begin());
   {
     Timed t(UPIPE_K_TILE_TABLE, 0, p.S, 0, 0, 1, -1, st);
@@ -739,14 +743,148 @@ upipe_status_t run_bwd_offload(const Plan& p, const bf16* hX, const bf16* Wqkv, 
   return UPIPE_OK;
 }
 
-// Host tensors of the offloaded entry points must be page-locked (pinned or registered).
-bool pinned_host(const void* ptr) {
+// ------------------------------------------------------------------------ sequence-tiled MLP
+// SwiGLU feed-forward computed a tile of rows at a time (the element-wise steps beside the layer,
+// tiled along the sequence: podcast summary, chapter on sequence tiling).  Workspace: one tile's
+// H = [G | U] bf16 [T][2F] and A bf16 [T][F] (forward), plus dA [T][F] and dH [T][2F] (backward)
+// and the weight gradients' split-K partials.
+struct MlpPlan {
+  int64_t S, T;
+  int d, F;
+  size_t H, A, dA, dH, split, total;
+  int split_dwd, split_dwgu;
+};
+
+upipe_status_t check_mlp(const upipe_mlp_desc_t* m) {
+  if (!m || m->seq_len < 1 || m->seq_len > INT32_MAX || m->hidden <= 0 || m->ffn <= 0) return UPIPE_ERR_INVALID_ARG;
+  if (m->tile_rows < 0 || m->tile_rows % kTile != 0) return UPIPE_ERR_INVALID_ARG;
+  if (m->hidden % 64 != 0 || m->ffn % 64 != 0) return UPIPE_ERR_UNSUPPORTED;
+  return UPIPE_OK;
+}
+
+MlpPlan make_mlp_plan(const upipe_mlp_desc_t* m, int pass) {
+  MlpPlan p{};
+  p.S = m->seq_len;
+  p.d = m->hidden;
+  p.F = m->ffn;
+  p.T = m->tile_rows == 0 ? p.S : std::min<int64_t>(m->tile_rows, p.S);
+  size_t off = 0;
+  auto take = [&](size_t bytes) { size_t o = off; off = align_up(off + bytes); return o; };
+  p.H = take((size_t)p.T * 2 * p.F * sizeof(bf16));
+  p.A = take((size_t)p.T * p.F * sizeof(bf16));
+  p.dA = p.dH = p.split = 0;
+  p.split_dwd = p.split_dwgu = 1;
+  if (pass == 1) {
+    p.dA = take((size_t)p.T * p.F * sizeof(bf16));
+    p.dH = take((size_t)p.T * 2 * p.F * sizeof(bf16));
+    const int sms = num_sms();
+    p.split_dwd = gemm_pick_split(p.d, p.F, p.T, sms);
+    p.split_dwgu = gemm_pick_split(2 * (int64_t)p.F, p.d, p.T, sms);
+    const size_t sb = std::max(gemm_split_scratch_bytes(p.d, p.F, p.split_dwd),
+                               gemm_split_scratch_bytes(2 * (int64_t)p.F, p.d, p.split_dwgu));
+    if (sb) p.split = take(sb);
+  }
+  p.total = off;
+  return p;
+}
+
+// C[rows, N] (bf16, ld) = A[rows, K] B[N, K]^T with A, B plain row-major 2-D operands
+TcGemmArgs gemm2d(int64_t M, int64_t N, int64_t K, TcOperand a, TcOperand b, void* out, int64_t ld, int epi) {
+  TcGemmArgs g{};
+  g.M = M; g.N = N; g.K = K;
+  g.a = a; g.b = b;
+  g.c.blk[0] = out; g.c.ld = ld; g.c.blk_shift = -1; g.c.blk_dim = 0;
+  g.epi = epi;
+  return g;
+}
+
+upipe_status_t run_mlp_fwd(const MlpPlan& p, const bf16* X, const bf16* Wgu, const bf16* Wd, bf16* Y, void* ws,
+                           cudaStream_t st) {
+  const int64_t F2 = 2 * (int64_t)p.F;
+  bf16* H = at<bf16>(ws, p.H);
+  bf16* A = at<bf16>(ws, p.A);
+  for (int64_t r0 = 0, t = 0; r0 < p.S; r0 += p.T, ++t) {
+    const int64_t rows = std::min(p.T, p.S - r0);
+    {  // H = X_t [Wg; Wu]^T
+      TcGemmArgs g = gemm2d(rows, F2, p.d, op2d(X + r0 * p.d, p.d, rows, p.d, 1), op2d(Wgu, p.d, F2, p.d, 1), H, F2,
+                            EPI_STORE_BF16);
+      Timed tm(UPIPE_K_MLP_GATE_UP, g.epi, g.M, g.N, g.K, 1, (int)t, st);
+      UPIPE_CUDA(launch_gemm_tc(g, 1, nullptr, st));
+    }
+    {
+      Timed tm(UPIPE_K_MLP_ACT, 0, rows * p.F, 1, 1, 1, (int)t, st);
+      UPIPE_CUDA(launch_swiglu_fwd(H, A, rows, p.F, st));
+    }
+    {  // Y_t = A Wd^T
+      TcGemmArgs g = gemm2d(rows, p.d, p.F, op2d(A, p.F, rows, p.F, 1), op2d(Wd, p.F, p.d, p.F, 1), Y + r0 * p.d, p.d,
+                            EPI_STORE_BF16);
+      Timed tm(UPIPE_K_MLP_DOWN, g.epi, g.M, g.N, g.K, 1, (int)t, st);
+      UPIPE_CUDA(launch_gemm_tc(g, 1, nullptr, st));
+    }
+  }
+  return UPIPE_OK;
+}
+
+upipe_status_t run_mlp_bwd(const MlpPlan& p, const bf16* X, const bf16* Wgu, const bf16* Wd, const bf16* dY, bf16* dX,
+                           float* dWgu, float* dWd, void* ws, cudaStream_t st) {
+  const int64_t F2 = 2 * (int64_t)p.F;
+  bf16* H = at<bf16>(ws, p.H);
+  bf16* A = at<bf16>(ws, p.A);
+  bf16* dA = at<bf16>(ws, p.dA);
+  bf16* dH = at<bf16>(ws, p.dH);
+  float* split = p.split ? at<float>(ws, p.split) : nullptr;
+  for (int64_t r0 = 0, t = 0; r0 < p.S; r0 += p.T, ++t) {
+    const int64_t rows = std::min(p.T, p.S - r0);
+    {  // recompute H = X_t [Wg; Wu]^T
+      TcGemmArgs g = gemm2d(rows, F2, p.d, op2d(X + r0 * p.d, p.d, rows, p.d, 1), op2d(Wgu, p.d, F2, p.d, 1), H, F2,
+                            EPI_STORE_BF16);
+      Timed tm(UPIPE_K_MLP_GATE_UP, g.epi, g.M, g.N, g.K, 1, (int)t, st);
+      UPIPE_CUDA(launch_gemm_tc(g, 1, nullptr, st));
+    }
+    {  // dA = dY_t Wd   (Wd read as [K = d][N = F])
+      TcGemmArgs g = gemm2d(rows, p.F, p.d, op2d(dY + r0 * p.d, p.d, rows, p.d, 1), op2d(Wd, p.F, p.d, p.F, 0), dA,
+                            p.F, EPI_STORE_BF16);
+      Timed tm(UPIPE_K_MLP_DACT, g.epi, g.M, g.N, g.K, 1, (int)t, st);
+      UPIPE_CUDA(launch_gemm_tc(g, 1, nullptr, st));
+    }
+    {
+      Timed tm(UPIPE_K_MLP_ACT_BWD, 0, rows * p.F, 1, 1, 1, (int)t, st);
+      UPIPE_CUDA(launch_swiglu_bwd(H, dA, A, dH, rows, p.F, st));
+    }
+    {  // dWd (+)= dY_t^T A
+      TcGemmArgs g = gemm2d(p.d, p.F, rows, op2d(dY + r0 * p.d, p.d, rows, p.d, 0), op2d(A, p.F, rows, p.F, 0), dWd,
+                            p.F, EPI_STORE_F32);
+      Timed tm(UPIPE_K_MLP_DWD, t > 0 ? EPI_ACC_F32 : EPI_STORE_F32, g.M, g.N, g.K, p.split_dwd, (int)t, st);
+      UPIPE_CUDA(block_weight_grad(g, t, p.split_dwd, split, st));
+    }
+    {  // dX_t = [dG | dU] [Wg; Wu]   (Wgu read as [K = 2F][N = d])
+      TcGemmArgs g = gemm2d(rows, p.d, F2, op2d(dH, F2, rows, F2, 1), op2d(Wgu, p.d, F2, p.d, 0), dX + r0 * p.d, p.d,
+                            EPI_STORE_BF16);
+      Timed tm(UPIPE_K_MLP_DX, g.epi, g.M, g.N, g.K, 1, (int)t, st);
+      UPIPE_CUDA(launch_gemm_tc(g, 1, nullptr, st));
+    }
+    {  // dWgu (+)= [dG | dU]^T X_t
+      TcGemmArgs g = gemm2d(F2, p.d, rows, op2d(dH, F2, rows, F2, 0), op2d(X + r0 * p.d, p.d, rows, p.d, 0), dWgu,
+                            p.d, EPI_STORE_F32);
+      Timed tm(UPIPE_K_MLP_DWGU, t > 0 ? EPI_ACC_F32 : EPI_STORE_F32, g.M, g.N, g.K, p.split_dwgu, (int)t, st);
+      UPIPE_CUDA(block_weight_grad(g, t, p.split_dwgu, split, st));
+    }
+  }
+  return UPIPE_OK;
+}
+
+// Where a tensor of the offloaded entry points lives: page-locked host memory (staged), device
+// memory (read in place), or neither (pageable host memory: rejected).
+enum class Where { Host, Device, Invalid };
+Where where_is(const void* ptr) {
   cudaPointerAttributes attr{};
   if (cudaPointerGetAttributes(&attr, ptr) != cudaSuccess) {
     cudaGetLastError();  // the failed query's error is not sticky: clear it
-    return false;
+    return Where::Invalid;
   }
-  return attr.type == cudaMemoryTypeHost;
+  if (attr.type == cudaMemoryTypeHost) return Where::Host;
+  if (attr.type == cudaMemoryTypeDevice || attr.type == cudaMemoryTypeManaged) return Where::Device;
+  return Where::Invalid;
 }
 
 upipe_status_t check_stage_rows(int64_t stage_rows) {
@@ -1031,8 +1169,9 @@ upipe_status_t upipe_attn_fwd_offload(const upipe_attn_desc_t* desc, const uint1
     return UPIPE_ERR_ALIGNMENT;
   const Plan p = make_plan(desc, 0, stage_rows ? stage_rows : kDefaultStageRows);
   if (ws_bytes < p.total) return UPIPE_ERR_WORKSPACE_TOO_SMALL;
-  if (!pinned_host(X_host)) return UPIPE_ERR_INVALID_ARG;
-  return run_fwd_offload(p, reinterpret_cast<const bf16*>(X_host), reinterpret_cast<const bf16*>(Wqkv),
+  const Where wx = where_is(X_host);
+  if (wx == Where::Invalid) return UPIPE_ERR_INVALID_ARG;
+  return run_fwd_offload(p, reinterpret_cast<const bf16*>(X_host), wx == Where::Host, reinterpret_cast<const bf16*>(Wqkv),
                          reinterpret_cast<const bf16*>(Wo), seg, reinterpret_cast<bf16*>(Y), lse, ws,
                          (cudaStream_t)stream);
 }
@@ -1051,10 +1190,49 @@ upipe_status_t upipe_attn_bwd_offload(const upipe_attn_desc_t* desc, const uint1
     return UPIPE_ERR_ALIGNMENT;
   const Plan p = make_plan(desc, 1, stage_rows ? stage_rows : kDefaultStageRows);
   if (ws_bytes < p.total) return UPIPE_ERR_WORKSPACE_TOO_SMALL;
-  if (!pinned_host(X_host) || !pinned_host(dY_host)) return UPIPE_ERR_INVALID_ARG;
-  return run_bwd_offload(p, reinterpret_cast<const bf16*>(X_host), reinterpret_cast<const bf16*>(Wqkv),
-                         reinterpret_cast<const bf16*>(Wo), seg, reinterpret_cast<const bf16*>(dY_host), lse,
-                         reinterpret_cast<bf16*>(dX), dWqkv, dWo, ws, (cudaStream_t)stream);
+  const Where wx = where_is(X_host), wdy = where_is(dY_host);
+  if (wx == Where::Invalid || wdy == Where::Invalid) return UPIPE_ERR_INVALID_ARG;
+  return run_bwd_offload(p, reinterpret_cast<const bf16*>(X_host), wx == Where::Host, reinterpret_cast<const bf16*>(Wqkv),
+                         reinterpret_cast<const bf16*>(Wo), seg, reinterpret_cast<const bf16*>(dY_host),
+                         wdy == Where::Host, lse, reinterpret_cast<bf16*>(dX), dWqkv, dWo, ws, (cudaStream_t)stream);
+}
+
+upipe_status_t upipe_mlp_workspace_size(const upipe_mlp_desc_t* desc, int pass, size_t* bytes) {
+  upipe_status_t s = check_mlp(desc);
+  if (s != UPIPE_OK) return s;
+  if (!bytes || (pass != 0 && pass != 1)) return UPIPE_ERR_INVALID_ARG;
+  *bytes = make_mlp_plan(desc, pass).total;
+  return UPIPE_OK;
+}
+
+// The feed-forward step in sequence tiles (podcast summary, chapter on sequence tiling; transcript,
+// Полезные советы: the MLP computed in pieces).
+upipe_status_t upipe_mlp_fwd(const upipe_mlp_desc_t* desc, const uint16_t* X, const uint16_t* Wgu, const uint16_t* Wd,
+                             uint16_t* Y, void* ws, size_t ws_bytes, void* stream) {
+  upipe_status_t s = check_mlp(desc);
+  if (s != UPIPE_OK) return s;
+  if (!X || !Wgu || !Wd || !Y || !ws) return UPIPE_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(Wgu) || !aligned16(Wd) || !aligned16(Y) || !aligned16(ws)) return UPIPE_ERR_ALIGNMENT;
+  const MlpPlan p = make_mlp_plan(desc, 0);
+  if (ws_bytes < p.total) return UPIPE_ERR_WORKSPACE_TOO_SMALL;
+  return run_mlp_fwd(p, reinterpret_cast<const bf16*>(X), reinterpret_cast<const bf16*>(Wgu),
+                     reinterpret_cast<const bf16*>(Wd), reinterpret_cast<bf16*>(Y), ws, (cudaStream_t)stream);
+}
+
+upipe_status_t upipe_mlp_bwd(const upipe_mlp_desc_t* desc, const uint16_t* X, const uint16_t* Wgu, const uint16_t* Wd,
+                             const uint16_t* dY, uint16_t* dX, float* dWgu, float* dWd, void* ws, size_t ws_bytes,
+                             void* stream) {
+  upipe_status_t s = check_mlp(desc);
+  if (s != UPIPE_OK) return s;
+  if (!X || !Wgu || !Wd || !dY || !dX || !dWgu || !dWd || !ws) return UPIPE_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(Wgu) || !aligned16(Wd) || !aligned16(dY) || !aligned16(dX) || !aligned16(dWgu) ||
+      !aligned16(dWd) || !aligned16(ws))
+    return UPIPE_ERR_ALIGNMENT;
+  const MlpPlan p = make_mlp_plan(desc, 1);
+  if (ws_bytes < p.total) return UPIPE_ERR_WORKSPACE_TOO_SMALL;
+  return run_mlp_bwd(p, reinterpret_cast<const bf16*>(X), reinterpret_cast<const bf16*>(Wgu),
+                     reinterpret_cast<const bf16*>(Wd), reinterpret_cast<const bf16*>(dY), reinterpret_cast<bf16*>(dX),
+                     dWgu, dWd, ws, (cudaStream_t)stream);
 }
 
 upipe_status_t upipe_attn_timing_enable(int32_t on) {

@@ -141,5 +141,9 @@ cudaError_t launch_lse_merge(int64_t rows, int head_dim, const bf16* ob, const f
 cudaError_t launch_ring_bwd_prep(int nh, int64_t S, int head_dim, const bf16* o, const bf16* dout, const float* lse,
                                  float* D, cudaStream_t st);
 cudaError_t launch_accumulate(int64_t n, const bf16* src, float* acc, bf16* out, cudaStream_t st);
+// SwiGLU halves of the sequence-tiled MLP: H = [G | U] bf16 [rows][2F]
+cudaError_t launch_swiglu_fwd(const bf16* H, bf16* A, int64_t rows, int64_t F, cudaStream_t st);
+cudaError_t launch_swiglu_bwd(const bf16* H, const bf16* dA, bf16* A, bf16* dH, int64_t rows, int64_t F,
+                              cudaStream_t st);
 
 }  // namespace upipe

@@ -14,7 +14,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 def declared_functions():
     src = open(os.path.join(ROOT, "include", "upipe_attn.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(upipe_attn_\w+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(upipe_(?:attn|mlp)_\w+)\s*\(", src)))
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -103,6 +103,27 @@ def test_wait_limit_and_probe_check_arguments():
     assert L.upipe_attn_wait_probe(None, 64, 0, None) == 1
     assert L.upipe_attn_wait_probe(fake, 16, 0, None) == 1         # smaller than a table header
     assert L.upipe_attn_wait_probe(ctypes.c_void_p(0x10008), 64, 0, None) == 3
+
+
+def test_mlp_host_checks_and_workspace_grow_with_the_tile():
+    L = up.lib()
+    fake = ctypes.c_void_p(0x10000)
+    n = ctypes.c_size_t(0)
+    for bad in (up.make_mlp_desc(0, 256, 512), up.make_mlp_desc(512, 256, 512, 100), up.make_mlp_desc(512, 256, 512, -128)):
+        assert L.upipe_mlp_workspace_size(ctypes.byref(bad), 0, ctypes.byref(n)) == 1
+    assert L.upipe_mlp_workspace_size(ctypes.byref(up.make_mlp_desc(512, 100, 512)), 0, ctypes.byref(n)) == 2
+    d = up.make_mlp_desc(1 << 20, 4096, 14336, 8192)
+    launches = up.launch_count()
+    assert L.upipe_mlp_fwd(ctypes.byref(d), fake, fake, fake, fake, fake, 16, None) == 4
+    assert L.upipe_mlp_bwd(ctypes.byref(d), fake, fake, fake, None, fake, fake, fake, fake, 1 << 40, None) == 1
+    assert up.launch_count() == launches
+    # the workspace holds one tile: it grows with tile_rows, not with S
+    F, T = 14336, 8192
+    assert up.mlp_workspace_bytes(d, 0) >= T * 3 * F * 2
+    assert up.mlp_workspace_bytes(d, 0) < T * 3 * F * 2 + 4096
+    assert up.mlp_workspace_bytes(up.make_mlp_desc(1 << 21, 4096, F, T), 1) == up.mlp_workspace_bytes(d, 1)
+    untiled = up.mlp_workspace_bytes(up.make_mlp_desc(1 << 20, 4096, F, 0), 1)
+    assert untiled > 100 * up.mlp_workspace_bytes(d, 1) // 2
 
 
 def test_offload_workspace_adds_the_staging_buffers():

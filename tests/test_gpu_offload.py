@@ -76,6 +76,30 @@ def test_offload_matches_regular_and_oracle(case):
     assert rel_fro(to_f64(dW), dWq) <= GRAD_REL_FRO and rel_fro(to_f64(dWo), dWoo) <= GRAD_REL_FRO
 
 
+@pytest.mark.parametrize("x_host,dy_host", [(True, False), (False, True)])
+def test_offload_with_one_tensor_on_the_device(x_host, dy_host):
+    """A training stack offloads the block input X while dY, produced during the backward, stays
+    on the device: each tensor is staged only if it is in host memory."""
+    S, d, Hq, Hkv, Dh, hpc, stage_rows = 1000, 256, 8, 2, 128, 2, 256
+    X, W, Wo, dY = layer_inputs(S, d, Hq, Hkv, Dh)
+    Xt, Wt, Wot, dYt = (bf16_tensor(x) for x in (X, W, Wo, dY))
+    desc = up.make_desc(S, d, Hq, Hkv, Dh, hpc, True)
+    layer = up.Layer(desc)
+    Y_ref, lse_ref = layer.forward(Xt, Wt, Wot)
+    dX_ref, dW_ref, dWo_ref = layer.backward(Xt, Wt, Wot, None, dYt, lse_ref)
+    Xa = pinned(Xt.cpu()) if x_host else Xt
+    dYa = pinned(dYt.cpu()) if dy_host else dYt
+    ws = torch.empty(up.workspace_bytes_offload(desc, 1, stage_rows), dtype=torch.uint8, device="cuda")
+    Y = torch.empty_like(Xt); lse = torch.empty_like(lse_ref)
+    up.fwd_offload(desc, Xa, Wt, Wot, None, Y, lse, ws, stage_rows)
+    dX = torch.empty_like(Xt); dW = torch.empty_like(dW_ref); dWo = torch.empty_like(dWo_ref)
+    up.bwd_offload(desc, Xa, Wt, Wot, None, dYa, lse, dX, dW, dWo, ws, stage_rows)
+    torch.cuda.synchronize()
+    assert up.device_status(ws) == 0
+    assert torch.equal(Y, Y_ref) and torch.equal(lse, lse_ref) and torch.equal(dX, dX_ref)
+    assert rel_fro(to_f64(dW), to_f64(dW_ref)) <= 1e-5 and rel_fro(to_f64(dWo), to_f64(dWo_ref)) <= 1e-5
+
+
 def test_offload_rejects_pageable_host_memory():
     S, d, Hq, Hkv, Dh = 256, 128, 2, 1, 64
     X, W, Wo, _ = layer_inputs(S, d, Hq, Hkv, Dh, dy=False)
