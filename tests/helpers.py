@@ -15,6 +15,11 @@ GRAD_REL_FRO = 1e-2
 # derives both and pins these bars to them.
 FULL_OUT_MAX_ABS = 2e-2
 FULL_LSE_REL = 1e-2
+# The SwiGLU MLP at hidden 4096 / ffn 14336 stores its gate/up output and A in bf16; an exact
+# implementation of those roundings is 0.029 from the fp64 oracle beyond Y's rounding on the rows
+# the full-shape test checks (Y's standard deviation is 2.4), so its bar is 4e-2
+# (tests/test_error_budget.py).
+FULL_MLP_OUT_MAX_ABS = 4e-2
 
 
 def rel_fro(got, want):

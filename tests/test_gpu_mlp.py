@@ -11,7 +11,7 @@ import torch
 import long_context_attention_upipe_gb300 as up
 import oracle as orc
 import upipe_inputs as ui
-from helpers import FULL_OUT_MAX_ABS, GRAD_REL_FRO, OUT_MAX_ABS, OUT_REL_FRO, bf16_tensor, max_abs_bf16_out, rel_fro, to_f64
+from helpers import FULL_MLP_OUT_MAX_ABS, GRAD_REL_FRO, OUT_MAX_ABS, OUT_REL_FRO, bf16_tensor, max_abs_bf16_out, rel_fro, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -102,7 +102,9 @@ def test_mlp_full_shape_tiled_against_oracle_and_memory():
     Y_ref = orc.mlp_forward(ui.normal_bf16_rows(rows, d, ui.TID_X), Wgu, Wd)
     y = to_f64(Y[torch.from_numpy(rows).cuda()])
     assert rel_fro(y, Y_ref) <= OUT_REL_FRO, rel_fro(y, Y_ref)
-    assert max_abs_bf16_out(y, Y_ref) <= FULL_OUT_MAX_ABS, max_abs_bf16_out(y, Y_ref)
+    # the bf16-stored gate/up output and A of an exact implementation already give 0.029 here
+    # (tests/test_error_budget.py)
+    assert max_abs_bf16_out(y, Y_ref) <= FULL_MLP_OUT_MAX_ABS, max_abs_bf16_out(y, Y_ref)
     Xp = ui.normal_bf16_rows(np.arange(P), d, ui.TID_X)
     dYp = ui.normal_bf16(P * d, ui.TID_DY).reshape(P, d)
     dX_ref, dW_ref, dD_ref = orc.mlp_backward(Xp, Wgu, Wd, dYp)
