@@ -270,6 +270,8 @@ def summarize_kernels(recs, w, peaks, step_ms):
             g["bytes"] += 4.0 * r["m"]
         elif r["kind"] == "tile_table":
             g["bytes"] += 4.0 * r["m"]
+        elif r["kind"] == "h2d":
+            g["bytes"] += float(r["m"])
     sustained = step_ms > 500.0
     peak_t = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
     peak_kind = f"measured bf16 {'sustained (inside a step of ' + format(step_ms / 1e3, '.1f') + ' s)' if sustained else 'burst'}"
@@ -278,7 +280,7 @@ def summarize_kernels(recs, w, peaks, step_ms):
         sec = g["ms"] * 1e-3
         t_flops = g["flops"] / (peak_t * 1e12)
         t_bytes = g["bytes"] / (peaks["hbm_gbs"] * 1e9)
-        bound = "tensor" if g["flops"] and t_flops >= t_bytes else "hbm"
+        bound = "tensor" if g["flops"] and t_flops >= t_bytes else ("h2d" if g["kernel"] == "h2d" else "hbm")
         e = {"kernel": g["kernel"], "launches": g["launches"], "ms": round(g["ms"], 4),
              "share": round(g["ms"] / step_ms, 4), "bound": bound}
         if "shape" in g:
@@ -291,6 +293,8 @@ def summarize_kernels(recs, w, peaks, step_ms):
         if bound == "tensor":
             e["peak"], e["peak_kind"] = peak_t, peak_kind
             e["frac"] = e["tflops"] / peak_t
+        elif bound == "h2d":   # copies on the staging stream, overlapped with the kernels
+            e["share"] = None
         else:
             e["peak"], e["peak_kind"] = peaks["hbm_gbs"], "measured HBM copy bandwidth"
             e["frac"] = e["gbs"] / peaks["hbm_gbs"] if e.get("gbs") else None

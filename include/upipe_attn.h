@@ -319,6 +319,7 @@ upipe_status_t upipe_attn_no_alloc_device_status(int32_t* code, void* stream);
  *   split_k   GEMM K splits (> 1: the record includes the split reduction)
  *   chunk     head chunk index (-1 for the tile table)
  *   ms        device time between the two events
+ *   start_ms  when the first event fired, relative to the first record of the collect
  * upipe_attn_timing_collect waits for the logged launches, copies up to `cap` records (in
  * launch order) into `out`, writes the total count to *n and clears the log. */
 enum {
@@ -327,13 +328,16 @@ enum {
   UPIPE_K_DX_PROJ = 10, UPIPE_K_DWQKV = 11, UPIPE_K_ZERO = 12,
   /* the sequence-tiled MLP (upipe_mlp_fwd / upipe_mlp_bwd) */
   UPIPE_K_MLP_GATE_UP = 13, UPIPE_K_MLP_ACT = 14, UPIPE_K_MLP_DOWN = 15, UPIPE_K_MLP_DACT = 16,
-  UPIPE_K_MLP_ACT_BWD = 17, UPIPE_K_MLP_DWD = 18, UPIPE_K_MLP_DX = 19, UPIPE_K_MLP_DWGU = 20
+  UPIPE_K_MLP_ACT_BWD = 17, UPIPE_K_MLP_DWD = 18, UPIPE_K_MLP_DX = 19, UPIPE_K_MLP_DWGU = 20,
+  /* a host-to-device staging copy of the offloaded calls (on their copy stream; m = bytes,
+     chunk = row block) */
+  UPIPE_K_H2D = 21
 };
 typedef struct {
   int32_t kind, epilogue, split_k, chunk;
   int64_t m, n, k;
   float ms;
-  int32_t reserved;
+  float start_ms; /* start relative to the first record of the same collect call */
 } upipe_attn_timing_t;
 upipe_status_t upipe_attn_timing_enable(int32_t on);
 upipe_status_t upipe_attn_timing_collect(upipe_attn_timing_t* out, int32_t cap, int32_t* n);

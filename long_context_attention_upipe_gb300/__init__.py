@@ -33,7 +33,7 @@ EXPORTS = ["upipe_attn_status_string", "upipe_attn_last_error_string", "upipe_at
 KERNEL_KINDS = {0: "tile_table", 1: "qkv_proj", 2: "attn_fwd", 3: "o_proj", 4: "convert", 5: "do_proj",
                 6: "recompute", 7: "dwo", 8: "bwd_dq", 9: "bwd_dkdv", 10: "dx_proj", 11: "dwqkv", 12: "zero",
                 13: "mlp_gate_up", 14: "mlp_act", 15: "mlp_down", 16: "mlp_dact", 17: "mlp_act_bwd", 18: "mlp_dwd",
-                19: "mlp_dx", 20: "mlp_dwgu"}
+                19: "mlp_dx", 20: "mlp_dwgu", 21: "h2d"}
 
 
 class Desc(ctypes.Structure):
@@ -60,7 +60,7 @@ def make_desc(S, d, Hq, Hkv, Dh, hpc=None, causal=True, accum_mode=0, scale=0.0)
 class TimingRec(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int32), ("epilogue", ctypes.c_int32), ("split_k", ctypes.c_int32),
                 ("chunk", ctypes.c_int32), ("m", ctypes.c_int64), ("n", ctypes.c_int64), ("k", ctypes.c_int64),
-                ("ms", ctypes.c_float), ("reserved", ctypes.c_int32)]
+                ("ms", ctypes.c_float), ("start_ms", ctypes.c_float)]
 
 
 class UpipeError(RuntimeError):
@@ -196,7 +196,8 @@ def timing_records(cap: int = 1 << 16):
     n = ctypes.c_int32(0)
     _check(lib().upipe_attn_timing_collect(buf, cap, ctypes.byref(n)), "timing_collect")
     return [{"kind": KERNEL_KINDS.get(r.kind, r.kind), "epilogue": r.epilogue, "split_k": r.split_k,
-             "chunk": r.chunk, "m": r.m, "n": r.n, "k": r.k, "ms": r.ms} for r in buf[:min(n.value, cap)]]
+             "chunk": r.chunk, "m": r.m, "n": r.n, "k": r.k, "ms": r.ms, "start_ms": r.start_ms}
+            for r in buf[:min(n.value, cap)]]
 
 
 def set_wait_limit_ns(ns: int):

@@ -537,6 +537,7 @@ class Stager {
     const size_t bytes = (size_t)rows(b) * p_.d * sizeof(bf16);
     const size_t off = (size_t)row0(b) * p_.d;
     cudaError_t e = cudaStreamWaitEvent(cs_, free_[k], 0);
+    Timed t(UPIPE_K_H2D, 0, (int64_t)bytes * ((x_host_ ? 1 : 0) + (hdy_ && dy_host_ ? 1 : 0)), 1, 1, 1, (int)b, cs_);
     if (e == cudaSuccess && x_host_)
       e = cudaMemcpyAsync(at<bf16>(ws_, p_.xs[k]), hx_ + off, bytes, cudaMemcpyHostToDevice, cs_);
     if (e == cudaSuccess && hdy_ && dy_host_)
@@ -1251,16 +1252,19 @@ upipe_status_t upipe_attn_timing_collect(upipe_attn_timing_t* out, int32_t cap, 
   upipe_status_t status = UPIPE_OK;
   int32_t k = 0;
   for (const TimingRec& r : recs) {
-    float ms = -1.f;
+    float ms = -1.f, start = -1.f;
     cudaError_t e = cudaEventSynchronize(r.e1);
     if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, r.e0, r.e1);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&start, recs.front().e0, r.e0);
     if (e != cudaSuccess && status == UPIPE_OK) status = cuda_status(e);
     if (k < cap) {
       upipe_attn_timing_t& o = out[k];
       o.kind = r.kind; o.epilogue = r.epi; o.split_k = r.split_k; o.chunk = r.chunk;
-      o.m = r.m; o.n = r.n; o.k = r.k; o.ms = ms;
+      o.m = r.m; o.n = r.n; o.k = r.k; o.ms = ms; o.start_ms = start;
     }
     ++k;
+  }
+  for (const TimingRec& r : recs) {
     cudaEventDestroy(r.e0);
     cudaEventDestroy(r.e1);
   }
