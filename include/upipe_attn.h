@@ -147,7 +147,7 @@ upipe_status_t upipe_attn_bwd(const upipe_attn_desc_t* desc, const uint16_t* X, 
  * X (and, in the backward, dY) stay in page-locked host memory and never occupy device memory as a
  * whole: the library brings them in `stage_rows` rows at a time (0 selects 65536; otherwise a
  * multiple of 128) into two staging buffers per tensor inside the workspace, one
- * cudaMemcpyAsync per block on a copy stream of its own, issued one block ahead so that copies
+ * cudaMemcpyAsync per block on a copy stream the library keeps per device, issued one block ahead so that copies
  * overlap the projections.  Per chunk the forward streams X once (the Q/K/V projection); the
  * backward streams X and dY twice (the Q/K/V and dO projections before the attention kernels,
  * the weight gradients dWo and dWqkv after them, summed block by block in a fixed order).

@@ -502,9 +502,28 @@ upipe_status_t run_bwd(const Plan& p, const bf16* X, const bf16* Wqkv, const bf1
 // CPU offload of the layer's inputs ("Road to 5 Million Tokens" podcast summary, chapter on
 // offloading part of the inputs to the CPU; neuro-slop.ru transcript, implementation plan step
 // 2): X and dY stay in pinned host memory and are brought in block by block, R rows at a time,
-// into two device staging buffers each.  Every block is one cudaMemcpyAsync on a copy stream,
-// issued one block ahead, so the copy of block b + 1 runs while the projections of block b do.
+// into two device staging buffers each.  Every block is one cudaMemcpyAsync on the device's copy
+// stream (created once and kept), issued one block ahead, so the copy of block b + 1 runs while the
+// projections of block b do.
 // Events order the reuse of a staging buffer after the kernels that read it.
+// The staging copy stream of a device: created on first use and kept for the life of the process
+// (one per device; calls that run concurrently share it, which only orders their copies).
+cudaError_t copy_stream(cudaStream_t* out) {
+  static std::mutex mu;
+  static cudaStream_t streams[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!streams[dev]) {
+    e = cudaStreamCreateWithFlags(&streams[dev], cudaStreamNonBlocking);
+    if (e != cudaSuccess) return e;
+  }
+  *out = streams[dev];
+  return cudaSuccess;
+}
+
 class Stager {
  public:
   // hx / hdy: the tensors; those with *_host set are staged, the others are device memory read in
@@ -514,10 +533,9 @@ class Stager {
   ~Stager() {
     for (cudaEvent_t e : {entry_, ready_[0], ready_[1], free_[0], free_[1]})
       if (e) cudaEventDestroy(e);
-    if (cs_) cudaStreamDestroy(cs_);
   }
   cudaError_t begin() {
-    cudaError_t e = cudaStreamCreateWithFlags(&cs_, cudaStreamNonBlocking);
+    cudaError_t e = copy_stream(&cs_);
     for (cudaEvent_t* ev : {&entry_, &ready_[0], &ready_[1], &free_[0], &free_[1]})
       if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
     // the copies start after the work queued before this call (which may still read the buffers)
