@@ -52,7 +52,8 @@ def parse():
     ap.add_argument("--kernel", default=None, choices=["fwd", "recompute", "dq", "dkdv", "lse_merge", "ring", "ring_bwd"],
                     help="time one attention kernel alone at the workload's chunk shapes (for profilers); "
                          "lse_merge: the ring merge of one block into fp32 accumulators; ring: the chunk's causal "
-                         "attention as the blocks of a zigzag ring of --ring-p devices, run on this GPU")
+                         "attention as the steps of a zigzag ring of --ring-p devices (all devices' shards in one "
+                         "launch per step) on this GPU, timed against the direct kernel")
     ap.add_argument("--ring-p", type=int, default=4)
     ap.add_argument("--reps", type=int, default=3)
     return ap.parse_args()
@@ -548,13 +549,8 @@ def main():
         }
 
     if args.kernel in ("lse_merge", "ring", "ring_bwd"):
-        if seg_t is not None:
-            raise SystemExit("the ring share runs unpacked sequences only")
         g = Hq // Hkv
         kvc = max(1, args.hpc // g)
-        q = fill((args.hpc, S, Dh), 10, 1.0)
-        k = fill((kvc, S, Dh), 11, 1.0)
-        v = fill((kvc, S, Dh), 12, 1.0)
         if args.kernel == "lse_merge":
             o_b = fill((args.hpc, S, Dh), 13, 1.0)
             l_b = torch.zeros(args.hpc, S, dtype=torch.float32, device=dev)
@@ -569,19 +565,39 @@ def main():
             print(json.dumps({"kernel": "lse_merge", "workload": w.name, "heads": args.hpc, "ms": ms_k,
                               "bytes": nbytes, "gbs": gbs, "hbm_frac": gbs / peaks["hbm_gbs"]}))
             return
+        # the chunk's attention as a zigzag ring of P devices, all devices' shards batched in one
+        # launch per step (tables built once, outside the timing, as for the direct kernels)
+        P = args.ring_p
+        if S % (2 * P):
+            raise SystemExit(f"S = {S} is not a multiple of 2P = {2 * P}")
+        C = S // (2 * P)
+        qs = fill((P, args.hpc, 2 * C, Dh), 10, 1.0)
+        ks = fill((P, kvc, 2 * C, Dh), 11, 1.0)
+        vs = fill((P, kvc, 2 * C, Dh), 12, 1.0)
+        ring = up.Ring(up.make_ring_desc(P, C, args.hpc, kvc, Dh, w.causal), seg_t, stream=stream)
+        out = (torch.empty(qs.shape, dtype=torch.float32, device=dev),
+               torch.empty(qs.shape[:3], dtype=torch.float32, device=dev), torch.empty_like(qs))
+        direct = chunk_kernels(args.hpc)
         if args.kernel == "ring":
-            f = lambda: up.ring_attention_share(q, k, v, args.ring_p, 0.0, stream)
+            f = lambda: ring.forward(qs, ks, vs, stream, out)
+            fs = lambda: ring.forward(qs, ks, vs, stream, out, per_step=True)
+            fd = direct["fwd"]
             fl = attn_kernel_flops(w, args.hpc, "fwd")
-        else:  # dQ, dK, dV of the ring's blocks (recompute-free: the forward's O and lse are given)
-            do = fill((args.hpc, S, Dh), 13, 1.0)
-            o, lse_r = up.ring_attention_share(q, k, v, args.ring_p, 0.0, stream)
-            f = lambda: up.ring_attention_share_backward(q, k, v, o, lse_r, do, args.ring_p, 0.0, stream)
+        else:  # dQ, dK, dV of the ring's steps (recompute-free: the forward's O and lse are given)
+            dos = fill((P, args.hpc, 2 * C, Dh), 13, 1.0)
+            o, lse_r = ring.forward(qs, ks, vs, stream, out)
+            f = lambda: ring.backward(qs, ks, vs, o, lse_r, dos, stream)
+            fs = lambda: ring.backward(qs, ks, vs, o, lse_r, dos, stream, per_step=True)
+            fd = lambda: (direct["dq"](), direct["dkdv"]())
             fl = attn_kernel_flops(w, args.hpc, "dq") + attn_kernel_flops(w, args.hpc, "dkdv")
-        f()
+        for g_ in (f, fs, fd):
+            g_()
         ms_k = time_steps(f, args.reps)
-        tf = fl / (ms_k * 1e-3) / 1e12
-        print(json.dumps({"kernel": args.kernel, "ring_p": args.ring_p, "workload": w.name, "heads": args.hpc,
-                          "ms": ms_k, "tflops": tf}))
+        ms_s = time_steps(fs, args.reps)
+        ms_d = time_steps(fd, args.reps)
+        print(json.dumps({"kernel": args.kernel, "ring_p": P, "workload": w.name, "heads": args.hpc, "ms": ms_k,
+                          "tflops": fl / (ms_k * 1e-3) / 1e12, "ms_step_calls": ms_s, "direct_ms": ms_d,
+                          "ratio_to_direct": ms_k / ms_d}))
         return
     if args.kernel:
         f = chunk_kernels(args.hpc)[args.kernel]

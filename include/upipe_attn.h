@@ -291,6 +291,96 @@ upipe_status_t upipe_attn_ring_bwd_prep(int32_t n_heads, int64_t seq_len, int32_
  * contributions with it and rounds each gradient once.  Pointers 16-byte aligned. */
 upipe_status_t upipe_attn_accumulate(int64_t n, const uint16_t* src, float* acc, uint16_t* out, void* stream);
 
+/* ------------------------------------------------------------------------------------------
+ * Ring (P2P) context parallelism, one call per ring step (MaxText long-context article: table of
+ * the context-parallel strategies, row "P2P (Ring)", and the paragraph after it on the causal
+ * load balancing the ring needs).  The sequence of 2PC rows is cut into 2P chunks of C rows;
+ * ring device r holds chunks r and 2P-1-r as its shard, one plane of 2C rows per head (local
+ * row i is at position i < C ? rC + i : (2P-1-r)C + i - C), so every device does the same work.
+ * At step s device r attends its queries to the key/value shard of device (r - s) mod P: keys
+ * at an earlier or equal position (causal) and of the same segment.  Every step is one launch
+ * for all batched devices; its result is folded into fp32 accumulators (the log-sum-exp merge
+ * L = log(e^L_acc + e^L_b), O = (e^L_acc O_acc + e^L_b O_b) / e^L), so after the last step they
+ * hold attention over the whole sequence.  One GPU can run the shares of several devices
+ * (dev_count > 1, their shards as consecutive planes); the exchange of the shards between
+ * devices is not part of the library.
+ *
+ * Shapes (planes of 2C rows, row-major, head-major inside a device):
+ *   q, o, dO        [dev_count][n_q_heads][2C][head_dim]   bf16
+ *   k, v            [kv_count][n_kv_heads][2C][head_dim]   bf16
+ *   lse             [dev_count][n_q_heads][2C]             fp32
+ * kv_count == P: k and v hold every device's shard, in device order (shard m is device m's);
+ * otherwise kv_count == dev_count and they hold, in batch order, the shards that visit the
+ * batched devices at the step of the call (a device of a real ring passes its receive buffer).
+ * seg: NULL (one sequence) or device int32 [2PC] segment ids in SEQUENCE order (non-decreasing;
+ * packed sequences attend within their segment only). */
+typedef struct {
+  int32_t ring_size;    /* P >= 1 */
+  int32_t n_q_heads, n_kv_heads, head_dim; /* head_dim 64 or 128; n_q_heads a multiple of n_kv_heads */
+  int64_t chunk_len;    /* C >= 1, 2C <= 2^31 - 1 */
+  int32_t causal;       /* 1: causal (the ring's use); 0: every key of the segment */
+  float softmax_scale;  /* <= 0: 1/sqrt(head_dim) */
+  int32_t dev_first, dev_count; /* the ring devices dev_first .. dev_first + dev_count - 1 (<= P) */
+  int32_t kv_count;     /* P, or dev_count (see above) */
+} upipe_ring_desc_t;
+
+/* Bytes of the P per-step tile tables of a ring (device memory the caller owns, 16-byte
+ * aligned).  The tables depend on the descriptor and on seg only: build them once per segment
+ * layout and reuse them for every layer and both passes. */
+upipe_status_t upipe_attn_ring_tables_size(const upipe_ring_desc_t* desc, size_t* bytes);
+/* Builds the tables of every step (stream-ordered).  Segment ids that are not non-decreasing set
+ * UPIPE_ERR_SEGMENTS_NOT_CONTIGUOUS in the error word read by upipe_attn_device_status(tables);
+ * so does a bounded device wait of any ring step that runs out. */
+upipe_status_t upipe_attn_ring_build_tables(const upipe_ring_desc_t* desc, const int32_t* seg, void* tables,
+                                            size_t bytes, void* stream);
+
+/* Forward of ring step `step` (0 .. P-1, called in order on the same accumulators): one
+ * attention launch over all batched devices.
+ *   o_acc  device fp32 [dev_count][n_q_heads][2C][head_dim]: running output (step 0 writes it,
+ *          later steps fold into it; the last step leaves it untouched)
+ *   lse    device fp32 [dev_count][n_q_heads][2C]: running log-sum-exp (natural log), final
+ *          after the last step
+ *   o      NULL, or device bf16 like q: each step writes the merged output of the rows it
+ *          changes, so after the last step o holds the result
+ * Query tiles that see no key of the visiting shard are not touched. */
+upipe_status_t upipe_attn_ring_fwd_step(const upipe_ring_desc_t* desc, int32_t step, const uint16_t* q,
+                                        const uint16_t* k, const uint16_t* v, const int32_t* seg, void* tables,
+                                        float* o_acc, float* lse, uint16_t* o, void* stream);
+
+/* Backward of ring step `step` (0 .. P-1, in order), two launches (dQ, then dK and dV).  Every
+ * block uses the softmax over the whole key set: D from upipe_attn_ring_bwd_prep over the
+ * final o, dO and lse (n_heads = dev_count * n_q_heads, seq_len = 2C).
+ *   dq_acc          device fp32 like o_acc: dQ summed over the steps (step 0 writes it)
+ *   dk_acc, dv_acc  device fp32 [kv_count][n_kv_heads][2C][head_dim]: dK, dV of the key shards,
+ *                   indexed like k and v, summed over the steps and the query heads of each KV
+ *                   head (on a real ring they travel with their shard)
+ *   dq, dk, dv      NULL, or device bf16 like q / k / v: the running sums rounded, written for
+ *                   the rows a step changes (the last step leaves the fp32 sums untouched)
+ * Rows that no query of a step sees are not touched by that step. */
+upipe_status_t upipe_attn_ring_bwd_step(const upipe_ring_desc_t* desc, int32_t step, const uint16_t* q,
+                                        const uint16_t* k, const uint16_t* v, const uint16_t* dO, const float* D,
+                                        const int32_t* seg, void* tables, float* dq_acc, float* dk_acc,
+                                        float* dv_acc, uint16_t* dq, uint16_t* dk, uint16_t* dv, void* stream);
+
+/* All P steps of the forward (steps 0 .. P-1 in order) in one call, with the arguments of
+ * upipe_attn_ring_fwd_step.  Each step after the first may start on the SMs the previous step's
+ * last CTAs leave idle: it computes its blocks and waits for the previous step to complete only
+ * before it touches the accumulators (programmatic dependent launch).  For a GPU that holds
+ * every shard (the batched single-GPU share); a device of a real ring calls the steps one by one
+ * as its shards arrive. */
+upipe_status_t upipe_attn_ring_fwd(const upipe_ring_desc_t* desc, const uint16_t* q, const uint16_t* k,
+                                   const uint16_t* v, const int32_t* seg, void* tables, float* o_acc, float* lse,
+                                   uint16_t* o, void* stream);
+
+/* All P steps of the backward in one call: D (device fp32 [2][dev_count * n_q_heads][Sp], Sp =
+ * ceil(2C/128)*128, written) from the final o, dO and lse as upipe_attn_ring_bwd_prep writes it,
+ * then steps 0 .. P-1 chained as in upipe_attn_ring_fwd; other arguments as in
+ * upipe_attn_ring_bwd_step. */
+upipe_status_t upipe_attn_ring_bwd(const upipe_ring_desc_t* desc, const uint16_t* q, const uint16_t* k,
+                                   const uint16_t* v, const uint16_t* o, const uint16_t* dO, const float* lse,
+                                   const int32_t* seg, void* tables, float* D, float* dq_acc, float* dk_acc,
+                                   float* dv_acc, uint16_t* dq, uint16_t* dk, uint16_t* dv, void* stream);
+
 /* Reads the device error word of a workspace (after fwd/bwd) or of a table (after
  * build_tile_table) into *code (a upipe_status_t value; UPIPE_OK when none).  Synchronises
  * `stream`.  `buf` is the workspace or the table.  No counterpart on the pages. */
@@ -309,7 +399,8 @@ upipe_status_t upipe_attn_no_alloc_device_status(int32_t* code, void* stream);
 
 /* Per-launch timing of the layer's kernels, a diagnostic with no counterpart on the pages (the
  * pages point to a profiler to find where memory and time go: podcast summary, chapter
- * "PyTorch profiler").  While enabled, every kernel launch of upipe_attn_fwd / upipe_attn_bwd is
+ * "PyTorch profiler").  While enabled, every kernel launch of upipe_attn_fwd / upipe_attn_bwd
+ * (and their offloaded forms), upipe_mlp_fwd / upipe_mlp_bwd and the ring steps is
  * bracketed by two CUDA events on the call's stream and logged with its kind and shape; do not
  * enable it while a stream is being captured into a CUDA graph.  Process-wide; off by default.
  *   kind      UPIPE_K_* below
@@ -331,7 +422,9 @@ enum {
   UPIPE_K_MLP_ACT_BWD = 17, UPIPE_K_MLP_DWD = 18, UPIPE_K_MLP_DX = 19, UPIPE_K_MLP_DWGU = 20,
   /* a host-to-device staging copy of the offloaded calls (on their copy stream; m = bytes,
      chunk = row block) */
-  UPIPE_K_H2D = 21
+  UPIPE_K_H2D = 21,
+  /* ring steps (m = 2C, n = dev_count * n_q_heads, k = head_dim, chunk = step) */
+  UPIPE_K_RING_FWD = 22, UPIPE_K_RING_DQ = 23, UPIPE_K_RING_DKDV = 24
 };
 typedef struct {
   int32_t kind, epilogue, split_k, chunk;

@@ -27,13 +27,14 @@ EXPORTS = ["upipe_attn_status_string", "upipe_attn_last_error_string", "upipe_at
            "upipe_attn_no_alloc_device_status", "upipe_attn_timing_enable", "upipe_attn_timing_collect",
            "upipe_attn_workspace_size_offload", "upipe_attn_fwd_offload", "upipe_attn_bwd_offload",
            "upipe_attn_set_wait_limit_ns", "upipe_attn_wait_probe", "upipe_mlp_workspace_size", "upipe_mlp_fwd",
-           "upipe_mlp_bwd"]
+           "upipe_mlp_bwd", "upipe_attn_ring_tables_size", "upipe_attn_ring_build_tables", "upipe_attn_ring_fwd_step",
+           "upipe_attn_ring_bwd_step", "upipe_attn_ring_fwd", "upipe_attn_ring_bwd"]
 
 # kinds of the per-launch timing records (upipe_attn_timing_collect)
 KERNEL_KINDS = {0: "tile_table", 1: "qkv_proj", 2: "attn_fwd", 3: "o_proj", 4: "convert", 5: "do_proj",
                 6: "recompute", 7: "dwo", 8: "bwd_dq", 9: "bwd_dkdv", 10: "dx_proj", 11: "dwqkv", 12: "zero",
                 13: "mlp_gate_up", 14: "mlp_act", 15: "mlp_down", 16: "mlp_dact", 17: "mlp_act_bwd", 18: "mlp_dwd",
-                19: "mlp_dx", 20: "mlp_dwgu", 21: "h2d"}
+                19: "mlp_dx", 20: "mlp_dwgu", 21: "h2d", 22: "ring_fwd", 23: "ring_dq", 24: "ring_dkdv"}
 
 
 class Desc(ctypes.Structure):
@@ -55,6 +56,22 @@ def make_mlp_desc(S, d, F, tile_rows=0) -> MlpDesc:
 def make_desc(S, d, Hq, Hkv, Dh, hpc=None, causal=True, accum_mode=0, scale=0.0) -> Desc:
     return Desc(int(S), int(d), int(Hq), int(Hkv), int(Dh), int(hpc if hpc is not None else Hq), int(bool(causal)),
                 int(accum_mode), float(scale))
+
+
+class RingDesc(ctypes.Structure):
+    _fields_ = [("ring_size", ctypes.c_int32), ("n_q_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("chunk_len", ctypes.c_int64), ("causal", ctypes.c_int32),
+                ("softmax_scale", ctypes.c_float), ("dev_first", ctypes.c_int32), ("dev_count", ctypes.c_int32),
+                ("kv_count", ctypes.c_int32)]
+
+
+def make_ring_desc(P, C, Hq, Hkv, Dh, causal=True, scale=0.0, dev_first=0, dev_count=None, kv_count=None) -> RingDesc:
+    """Zigzag ring of P devices over 2PC rows (chunks of C).  By default one call runs the shares of
+    all P devices with every key/value shard held in device order (kv_count = P)."""
+    dev_count = P if dev_count is None else dev_count
+    kv_count = P if kv_count is None else kv_count
+    return RingDesc(int(P), int(Hq), int(Hkv), int(Dh), int(C), int(bool(causal)), float(scale), int(dev_first),
+                    int(dev_count), int(kv_count))
 
 
 class TimingRec(ctypes.Structure):
@@ -113,6 +130,15 @@ def lib():
             "upipe_attn_bwd_offload": ([D, P, P, P, P, P, P, P, P, P, P, SZ, I64, P], ctypes.c_int),
             "upipe_attn_timing_collect": ([ctypes.POINTER(TimingRec), ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)],
                                           ctypes.c_int),
+            "upipe_attn_ring_tables_size": ([ctypes.POINTER(RingDesc), ctypes.POINTER(SZ)], ctypes.c_int),
+            "upipe_attn_ring_build_tables": ([ctypes.POINTER(RingDesc), P, P, SZ, P], ctypes.c_int),
+            "upipe_attn_ring_fwd_step": ([ctypes.POINTER(RingDesc), ctypes.c_int32, P, P, P, P, P, P, P, P, P],
+                                         ctypes.c_int),
+            "upipe_attn_ring_bwd_step": ([ctypes.POINTER(RingDesc), ctypes.c_int32, P, P, P, P, P, P, P, P, P, P, P,
+                                          P, P, P], ctypes.c_int),
+            "upipe_attn_ring_fwd": ([ctypes.POINTER(RingDesc), P, P, P, P, P, P, P, P, P], ctypes.c_int),
+            "upipe_attn_ring_bwd": ([ctypes.POINTER(RingDesc), P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P],
+                                    ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -320,7 +346,7 @@ def lse_merge(O_b, lse_b, O_acc, lse_acc, O_out=None, stream=None):
 
 
 # ------------------------------------------------------------------------------------------------
-# Ring (P2P) context parallelism, single-GPU share: the host schedule and a one-GPU run of it
+# Ring (P2P) context parallelism, single-GPU share: one C-ABI call per ring step
 # ------------------------------------------------------------------------------------------------
 
 def zigzag_chunks(P: int):
@@ -353,63 +379,77 @@ def ring_block_schedule(P: int):
     return sched
 
 
-def _check_ring_inputs(q, k, v, P):
-    if P < 1:
-        raise ValueError("P must be at least 1")
-    if q.dim() != 3 or k.dim() != 3 or v.shape != k.shape:
-        raise ValueError("q must be [Hq, S, Dh] and k, v [Hkv, S, Dh]")
-    if q.dtype != torch.bfloat16 or k.dtype != torch.bfloat16 or v.dtype != torch.bfloat16:
-        raise ValueError("q, k, v must be bf16")
-    Hq, S, Dh = q.shape
-    Hkv = k.shape[0]
-    if k.shape[1] != S or k.shape[2] != Dh or Hq % Hkv:
-        raise ValueError("k, v must cover the same positions and head_dim as q, with Hq a multiple of Hkv")
-    if Dh not in (64, 128):
-        raise ValueError("head_dim must be 64 or 128")
-    if S % (2 * P):
-        raise ValueError("S must be a multiple of 2P")
+def zigzag_positions(P: int, C: int, r: int) -> torch.Tensor:
+    """Sequence positions of the 2C local rows of ring device r (its chunks r and 2P - 1 - r)."""
+    a, b = zigzag_chunks(P)[r]
+    return torch.cat([torch.arange(a * C, (a + 1) * C), torch.arange(b * C, (b + 1) * C)])
 
 
-def ring_attention_share(q, k, v, P: int, softmax_scale: float = 0.0, stream=None):
-    """Causal attention of q [Hq, S, Dh] over k, v [Hkv, S, Dh] computed block by block as the P
-    devices of a zigzag ring would, each block with upipe_attn_core_fwd on contiguous chunk copies
-    and folded into per-chunk fp32 accumulators with upipe_attn_lse_merge, in ring-step order.
-    One GPU runs every device's blocks in turn (there is no exchange to make).  Returns O bf16
-    [Hq, S, Dh] and lse fp32 [Hq, S].  softmax_scale 0 means 1/sqrt(Dh)."""
-    _check_ring_inputs(q, k, v, P)
-    Hq, S, Dh = q.shape
-    Hkv = k.shape[0]
-    n = 2 * P
-    C = S // n
-    descs = {kind: make_desc(C, 64, Hq, Hkv, Dh, Hq, kind == "causal", 0, softmax_scale) for kind in ("causal", "full")}
-    tables = {}
-    for kind, dsc in descs.items():
-        t = torch.empty(tile_table_bytes(dsc), dtype=torch.uint8, device=q.device)
-        build_tile_table(dsc, None, t, stream)
-        tables[kind] = t
-    # each chunk once as a dense [heads, C, Dh] block: a device holds its own query chunks, and the
-    # ring delivers the key/value chunks of the others in this form
-    qs, ks, vs = ([x[:, c * C:(c + 1) * C].contiguous() for c in range(n)] for x in (q, k, v))
-    o_acc = {c: torch.zeros(Hq, C, Dh, dtype=torch.float32, device=q.device) for c in range(n)}
-    l_acc = {c: torch.full((Hq, C), float("-inf"), dtype=torch.float32, device=q.device) for c in range(n)}
-    o_b = torch.empty(Hq, C, Dh, dtype=torch.bfloat16, device=q.device)
-    l_b = torch.empty(Hq, C, dtype=torch.float32, device=q.device)
-    o_out = {c: torch.empty(Hq, C, Dh, dtype=torch.bfloat16, device=q.device) for c in range(n)}
-    order = [blk for steps in ring_block_schedule(P) for blocks in steps for blk in blocks]
-    last = {qc: i for i, (qc, _, _) in enumerate(order)}   # the merge that also writes the bf16 output
-    for i, (qc, kc, kind) in enumerate(order):
-        core_fwd(descs[kind], qs[qc], ks[kc], vs[kc], None, tables[kind], o_b, l_b, stream)
-        lse_merge(o_b, l_b, o_acc[qc], l_acc[qc], o_out[qc] if last[qc] == i else None, stream)
-    O = torch.empty_like(q)
-    lse = torch.empty(Hq, S, dtype=torch.float32, device=q.device)
-    for c in range(n):  # placement only
-        O[:, c * C:(c + 1) * C] = o_out[c]
-        lse[:, c * C:(c + 1) * C] = l_acc[c]
-    return O, lse
+def to_zigzag(x, P: int):
+    """[H, S, ...] in sequence order -> [P, H, 2S/(2P), ...] device shards (the data loader's
+    one-time reordering for causal load balancing; not part of the ring steps)."""
+    C = x.shape[1] // (2 * P)
+    idx = torch.stack([zigzag_positions(P, C, r) for r in range(P)]).to(x.device)
+    return torch.stack([x.index_select(1, idx[r]) for r in range(P)])
+
+
+def from_zigzag(xs, P: int):
+    """Inverse of to_zigzag: [P, H, 2C, ...] shards -> [H, 2PC, ...] in sequence order."""
+    C = xs.shape[2] // 2
+    out = torch.empty((xs.shape[1], 2 * P * C) + tuple(xs.shape[3:]), dtype=xs.dtype, device=xs.device)
+    for r in range(P):
+        out[:, zigzag_positions(P, C, r).to(xs.device)] = xs[r]
+    return out
+
+
+def ring_tables_bytes(desc: RingDesc) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().upipe_attn_ring_tables_size(ctypes.byref(desc), ctypes.byref(n)), "ring_tables_size")
+    return n.value
+
+
+def ring_build_tables(desc: RingDesc, seg, tables, stream=None):
+    """The P per-step tile tables (seg: None or int32 [2PC] in sequence order)."""
+    _check(lib().upipe_attn_ring_build_tables(ctypes.byref(desc), _ptr(seg), _ptr(tables), tables.numel(),
+                                              _stream(stream)), "ring_build_tables")
+
+
+def ring_fwd_step(desc: RingDesc, step: int, q, k, v, seg, tables, o_acc, lse, o=None, stream=None):
+    """One forward ring step (upipe_attn_ring_fwd_step): q [dev_count, Hq, 2C, Dh], k, v [kv_count,
+    Hkv, 2C, Dh] bf16; o_acc fp32 like q, lse fp32 [dev_count, Hq, 2C]; o bf16 like q or None."""
+    _check(lib().upipe_attn_ring_fwd_step(ctypes.byref(desc), int(step), _bf16(q), _bf16(k), _bf16(v), _ptr(seg),
+                                          _ptr(tables), _ptr(o_acc), _ptr(lse), _bf16(o) if o is not None else None,
+                                          _stream(stream)), "ring_fwd_step")
+
+
+def ring_bwd_step(desc: RingDesc, step: int, q, k, v, dO, D, seg, tables, dq_acc, dk_acc, dv_acc, dq=None, dk=None,
+                  dv=None, stream=None):
+    """One backward ring step (upipe_attn_ring_bwd_step): dQ, dK, dV of the step's blocks folded
+    into the fp32 sums (dq_acc like q, dk_acc / dv_acc like k); dq, dk, dv bf16 or None."""
+    opt = lambda t: _bf16(t) if t is not None else None
+    _check(lib().upipe_attn_ring_bwd_step(ctypes.byref(desc), int(step), _bf16(q), _bf16(k), _bf16(v), _bf16(dO),
+                                          _ptr(D), _ptr(seg), _ptr(tables), _ptr(dq_acc), _ptr(dk_acc), _ptr(dv_acc),
+                                          opt(dq), opt(dk), opt(dv), _stream(stream)), "ring_bwd_step")
+
+
+def ring_fwd(desc: RingDesc, q, k, v, seg, tables, o_acc, lse, o=None, stream=None):
+    """All P forward steps in one call (upipe_attn_ring_fwd: consecutive steps overlap)."""
+    _check(lib().upipe_attn_ring_fwd(ctypes.byref(desc), _bf16(q), _bf16(k), _bf16(v), _ptr(seg), _ptr(tables),
+                                     _ptr(o_acc), _ptr(lse), _bf16(o) if o is not None else None, _stream(stream)),
+           "ring_fwd")
+
+
+def ring_bwd(desc: RingDesc, q, k, v, o, dO, lse, seg, tables, D, dq_acc, dk_acc, dv_acc, dq=None, dk=None, dv=None,
+             stream=None):
+    """D from the final o, dO, lse, then all P backward steps (upipe_attn_ring_bwd)."""
+    opt = lambda t: _bf16(t) if t is not None else None
+    _check(lib().upipe_attn_ring_bwd(ctypes.byref(desc), _bf16(q), _bf16(k), _bf16(v), _bf16(o), _bf16(dO), _ptr(lse),
+                                     _ptr(seg), _ptr(tables), _ptr(D), _ptr(dq_acc), _ptr(dk_acc), _ptr(dv_acc),
+                                     opt(dq), opt(dk), opt(dv), _stream(stream)), "ring_bwd")
 
 
 def ring_bwd_prep(O, dO, lse, D, stream=None):
-    """D buffer [2][H][Sp] of the backward kernels from a chunk's final O, dO [H, S, Dh] and lse."""
+    """D buffer [2][H][Sp] of the backward kernels from the final O, dO [H, S, Dh] and lse [H, S]."""
     H, S, Dh = O.shape
     _check(lib().upipe_attn_ring_bwd_prep(H, S, Dh, _bf16(O), _bf16(dO), _ptr(lse), _ptr(D), _stream(stream)),
            "ring_bwd_prep")
@@ -421,55 +461,52 @@ def accumulate(src, acc, out=None, stream=None):
                                        _stream(stream)), "accumulate")
 
 
-def ring_attention_share_backward(q, k, v, O, lse, dO, P: int, softmax_scale: float = 0.0, stream=None):
-    """Gradients of causal attention (dQ [Hq, S, Dh], dK, dV [Hkv, S, Dh], bf16) computed block by
-    block as the zigzag ring's devices would: each block runs upipe_attn_core_bwd_dq and _dkdv with
-    its query chunk's final log-sum-exp and D = rowsum(dO * O) (upipe_attn_ring_bwd_prep), and the
-    blocks' contributions are summed in fp32 per chunk (upipe_attn_accumulate), rounded once.
-    O, lse: the forward's result over the whole sequence (ring_attention_share)."""
-    _check_ring_inputs(q, k, v, P)
-    if O.shape != q.shape or dO.shape != q.shape or tuple(lse.shape) != tuple(q.shape[:2]):
-        raise ValueError("O and dO must be shaped like q, lse [Hq, S]")
-    Hq, S, Dh = q.shape
-    Hkv = k.shape[0]
-    n = 2 * P
-    C = S // n
-    dev = q.device
-    descs = {kind: make_desc(C, 64, Hq, Hkv, Dh, Hq, kind == "causal", 0, softmax_scale) for kind in ("causal", "full")}
-    tables = {}
-    for kind, dsc in descs.items():
-        t = torch.empty(tile_table_bytes(dsc), dtype=torch.uint8, device=dev)
-        build_tile_table(dsc, None, t, stream)
-        tables[kind] = t
-    cut = lambda x: [x[:, c * C:(c + 1) * C].contiguous() for c in range(n)]
-    qs, ks, vs, os_, dos, ls = cut(q), cut(k), cut(v), cut(O), cut(dO), cut(lse)
-    sp = -(-C // 128) * 128
-    Ds = [torch.empty(2, Hq, sp, dtype=torch.float32, device=dev) for _ in range(n)]
-    for c in range(n):
-        ring_bwd_prep(os_[c], dos[c], ls[c], Ds[c], stream)
-    f32 = lambda H: [torch.zeros(H, C, Dh, dtype=torch.float32, device=dev) for _ in range(n)]
-    b16 = lambda H: [torch.empty(H, C, Dh, dtype=torch.bfloat16, device=dev) for _ in range(n)]
-    dq_acc, dk_acc, dv_acc = f32(Hq), f32(Hkv), f32(Hkv)
-    dq_out, dk_out, dv_out = b16(Hq), b16(Hkv), b16(Hkv)
-    dq_b = torch.empty(Hq, C, Dh, dtype=torch.bfloat16, device=dev)
-    dk_b = torch.empty(Hkv, C, Dh, dtype=torch.bfloat16, device=dev)
-    dv_b = torch.empty(Hkv, C, Dh, dtype=torch.bfloat16, device=dev)
-    order = [blk for steps in ring_block_schedule(P) for blocks in steps for blk in blocks]
-    last_q = {qc: i for i, (qc, _, _) in enumerate(order)}
-    last_k = {kc: i for i, (_, kc, _) in enumerate(order)}
-    for i, (qc, kc, kind) in enumerate(order):
-        d, t = descs[kind], tables[kind]
-        core_bwd_dq(d, qs[qc], ks[kc], vs[kc], dos[qc], ls[qc], Ds[qc], None, t, dq_b, stream)
-        accumulate(dq_b, dq_acc[qc], dq_out[qc] if last_q[qc] == i else None, stream)
-        core_bwd_dkdv(d, qs[qc], ks[kc], vs[kc], dos[qc], ls[qc], Ds[qc], None, t, dk_b, dv_b, stream)
-        accumulate(dk_b, dk_acc[kc], dk_out[kc] if last_k[kc] == i else None, stream)
-        accumulate(dv_b, dv_acc[kc], dv_out[kc] if last_k[kc] == i else None, stream)
-    dQ, dK, dV = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    for c in range(n):  # placement only
-        dQ[:, c * C:(c + 1) * C] = dq_out[c]
-        dK[:, c * C:(c + 1) * C] = dk_out[c]
-        dV[:, c * C:(c + 1) * C] = dv_out[c]
-    return dQ, dK, dV
+class Ring:
+    """The single-GPU share of a zigzag ring: the descriptor, its per-step tables (built once per
+    segment layout) and the P forward / backward step calls.  Shards: q [dev_count, Hq, 2C, Dh],
+    k, v [kv_count, Hkv, 2C, Dh] bf16 (to_zigzag gives them from sequence order)."""
+
+    def __init__(self, desc: RingDesc, seg=None, device="cuda", stream=None):
+        self.desc = desc
+        self.seg = seg
+        self.tables = torch.empty(ring_tables_bytes(desc), dtype=torch.uint8, device=device)
+        ring_build_tables(desc, seg, self.tables, stream)
+
+    def forward(self, q, k, v, stream=None, out=None, per_step=False):
+        """All P steps (one call, consecutive steps overlapping; per_step: P separate step calls);
+        returns (o bf16 like q, lse fp32 [dev_count, Hq, 2C])."""
+        d = self.desc
+        n, S = d.dev_count, 2 * d.chunk_len
+        if out is None:
+            out = (torch.empty(n, d.n_q_heads, S, d.head_dim, dtype=torch.float32, device=q.device),
+                   torch.empty(n, d.n_q_heads, S, dtype=torch.float32, device=q.device), torch.empty_like(q))
+        o_acc, lse, o = out
+        if per_step:
+            for s in range(d.ring_size):
+                ring_fwd_step(d, s, q, k, v, self.seg, self.tables, o_acc, lse, o, stream)
+        else:
+            ring_fwd(d, q, k, v, self.seg, self.tables, o_acc, lse, o, stream)
+        return o, lse
+
+    def backward(self, q, k, v, o, lse, dO, stream=None, per_step=False):
+        """D from the final o, dO, lse, then the P steps (one call, or P step calls with per_step);
+        returns dq, dk, dv (bf16)."""
+        d = self.desc
+        n, S, Dh = d.dev_count, 2 * d.chunk_len, d.head_dim
+        H = n * d.n_q_heads
+        sp = -(-S // 128) * 128
+        D = torch.empty(2, H, sp, dtype=torch.float32, device=q.device)
+        dq_acc = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+        dk_acc = torch.empty(k.shape, dtype=torch.float32, device=q.device)
+        dv_acc = torch.empty(v.shape, dtype=torch.float32, device=q.device)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        if per_step:
+            ring_bwd_prep(o.view(H, S, Dh), dO.view(H, S, Dh), lse.view(H, S), D, stream)
+            for s in range(d.ring_size):
+                ring_bwd_step(d, s, q, k, v, dO, D, self.seg, self.tables, dq_acc, dk_acc, dv_acc, dq, dk, dv, stream)
+        else:
+            ring_bwd(d, q, k, v, o, dO, lse, self.seg, self.tables, D, dq_acc, dk_acc, dv_acc, dq, dk, dv, stream)
+        return dq, dk, dv
 
 
 class Layer:

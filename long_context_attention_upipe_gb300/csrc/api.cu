@@ -1149,6 +1149,223 @@ upipe_status_t upipe_attn_accumulate(int64_t n, const uint16_t* src, float* acc,
                                        (cudaStream_t)stream));
 }
 
+// ------------------------------------------------------------------------------------------------
+// Ring (P2P) steps (MaxText article, strategy table row "P2P (Ring)" and the paragraph on causal
+// load balancing): the zigzag shards of dev_count devices against the visiting key/value shards,
+// one launch per step and pass kernel, accumulating in fp32.
+// ------------------------------------------------------------------------------------------------
+static upipe_status_t check_ring(const upipe_ring_desc_t* d) {
+  if (!d || d->ring_size < 1 || d->chunk_len < 1 || 2 * d->chunk_len > INT32_MAX || d->n_q_heads <= 0 ||
+      d->n_kv_heads <= 0 || d->n_q_heads % d->n_kv_heads != 0 || (d->causal != 0 && d->causal != 1))
+    return UPIPE_ERR_INVALID_ARG;
+  if (d->dev_first < 0 || d->dev_count < 1 || d->dev_first + d->dev_count > d->ring_size) return UPIPE_ERR_INVALID_ARG;
+  if (d->kv_count != d->ring_size && d->kv_count != d->dev_count) return UPIPE_ERR_INVALID_ARG;
+  if (d->head_dim != 64 && d->head_dim != 128) return UPIPE_ERR_UNSUPPORTED;
+  // the launches' second grid dimension runs over the query-tile pairs of all batched devices
+  // (forward, dQ) and over the key tiles of all shards (dK/dV)
+  const int64_t nt = ceil_div(2 * d->chunk_len, kTile);
+  if ((int64_t)d->dev_count * ceil_div(nt, 2) > 65535 || (int64_t)d->kv_count * nt > 65535) return UPIPE_ERR_UNSUPPORTED;
+  return UPIPE_OK;
+}
+
+// Geometry of step `step`: k/v hold every shard in device order (kv0 = 0) or the visiting ones in
+// batch order (kv0 = the owner of the first batched device's visitor).
+static RingGeom ring_geom(const upipe_ring_desc_t* d, int step) {
+  RingGeom g{};
+  g.P = d->ring_size;
+  g.r0 = d->dev_first;
+  g.step = step;
+  g.kv0 = d->kv_count == d->ring_size ? 0 : ((d->dev_first - step) % d->ring_size + d->ring_size) % d->ring_size;
+  g.C = d->chunk_len;
+  return g;
+}
+
+static size_t ring_table_bytes(const upipe_ring_desc_t* d) {
+  return tile_table_bytes(2 * d->chunk_len, d->dev_count, d->kv_count);
+}
+
+upipe_status_t upipe_attn_ring_tables_size(const upipe_ring_desc_t* desc, size_t* bytes) {
+  upipe_status_t s = check_ring(desc);
+  if (s != UPIPE_OK) return s;
+  if (!bytes) return UPIPE_ERR_INVALID_ARG;
+  *bytes = (size_t)desc->ring_size * ring_table_bytes(desc);
+  return UPIPE_OK;
+}
+
+upipe_status_t upipe_attn_ring_build_tables(const upipe_ring_desc_t* desc, const int32_t* seg, void* tables,
+                                            size_t bytes, void* stream) {
+  upipe_status_t s = check_ring(desc);
+  if (s != UPIPE_OK) return s;
+  if (!tables) return UPIPE_ERR_INVALID_ARG;
+  if (!aligned16(tables) || (seg && !aligned16(seg))) return UPIPE_ERR_ALIGNMENT;
+  const size_t per = ring_table_bytes(desc);
+  if (bytes < per * desc->ring_size) return UPIPE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t st = (cudaStream_t)stream;
+  for (int step = 0; step < desc->ring_size; ++step) {
+    Timed t(UPIPE_K_TILE_TABLE, 0, 2 * desc->chunk_len, 0, 0, 1, -1, st);
+    UPIPE_CUDA(launch_ring_table(2 * desc->chunk_len, desc->causal, seg, ring_geom(desc, step), desc->dev_count,
+                                 desc->kv_count, at<char>(tables, per * step), st));
+  }
+  return UPIPE_OK;
+}
+
+static AttnArgs ring_args(const upipe_ring_desc_t* d, int step, const uint16_t* q, const uint16_t* k,
+                          const uint16_t* v, const int32_t* seg, void* tables) {
+  const size_t per = ring_table_bytes(d);
+  void* table = at<char>(tables, per * step);
+  const int64_t S = 2 * d->chunk_len;
+  AttnArgs a{};
+  a.q = reinterpret_cast<const bf16*>(q);
+  a.k = reinterpret_cast<const bf16*>(k);
+  a.v = reinterpret_cast<const bf16*>(v);
+  a.seg = seg;
+  a.q_rows = table_q_rows(table);
+  a.kv_rows = table_kv_rows(table, S, d->dev_count);
+  a.q_order = table_q_order(table, S, d->dev_count, d->kv_count);
+  a.kv_order = table_kv_order(table, S, d->dev_count, d->kv_count);
+  a.S = S;
+  a.nh = d->dev_count * d->n_q_heads;
+  a.nkv = d->kv_count * d->n_kv_heads;
+  a.g = d->n_q_heads / d->n_kv_heads;
+  a.hq = d->n_q_heads;
+  a.hkv = d->n_kv_heads;
+  a.ndev = d->dev_count;
+  a.kv_count = d->kv_count;
+  a.causal = d->causal;
+  a.scale = d->softmax_scale > 0.f ? d->softmax_scale : 1.0f / std::sqrt((float)d->head_dim);
+  a.err = &reinterpret_cast<TableHeader*>(tables)->error;  // every step reports into the first table
+  a.ring = ring_geom(d, step);
+  a.acc_first = step == 0;
+  a.acc_last = step == d->ring_size - 1;
+  return a;
+}
+
+static upipe_status_t ring_fwd_checks(const upipe_ring_desc_t* desc, const uint16_t* q, const uint16_t* k,
+                                      const uint16_t* v, const int32_t* seg, void* tables, float* o_acc, float* lse,
+                                      uint16_t* o) {
+  upipe_status_t s = check_ring(desc);
+  if (s != UPIPE_OK) return s;
+  if (!q || !k || !v || !tables || !o_acc || !lse) return UPIPE_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(tables) || !aligned16(o_acc) || !aligned16(lse) ||
+      (o && !aligned16(o)) || (seg && !aligned16(seg)))
+    return UPIPE_ERR_ALIGNMENT;
+  return UPIPE_OK;
+}
+
+static upipe_status_t ring_fwd_launch(const upipe_ring_desc_t* desc, int step, bool chained, const uint16_t* q,
+                                      const uint16_t* k, const uint16_t* v, const int32_t* seg, void* tables,
+                                      float* o_acc, float* lse, uint16_t* o, cudaStream_t st) {
+  AttnArgs a = ring_args(desc, step, q, k, v, seg, tables);
+  a.o_acc = o_acc;
+  a.lse = lse;
+  a.o = reinterpret_cast<bf16*>(o);
+  a.pdl = chained;
+  Timed t(UPIPE_K_RING_FWD, 0, a.S, a.nh, desc->head_dim, 1, step, st);
+  return cuda_status(launch_attn_ring_fwd(a, desc->head_dim, st));
+}
+
+upipe_status_t upipe_attn_ring_fwd_step(const upipe_ring_desc_t* desc, int32_t step, const uint16_t* q,
+                                        const uint16_t* k, const uint16_t* v, const int32_t* seg, void* tables,
+                                        float* o_acc, float* lse, uint16_t* o, void* stream) {
+  upipe_status_t s = ring_fwd_checks(desc, q, k, v, seg, tables, o_acc, lse, o);
+  if (s != UPIPE_OK) return s;
+  if (step < 0 || step >= desc->ring_size) return UPIPE_ERR_INVALID_ARG;
+  return ring_fwd_launch(desc, step, false, q, k, v, seg, tables, o_acc, lse, o, (cudaStream_t)stream);
+}
+
+upipe_status_t upipe_attn_ring_fwd(const upipe_ring_desc_t* desc, const uint16_t* q, const uint16_t* k,
+                                   const uint16_t* v, const int32_t* seg, void* tables, float* o_acc, float* lse,
+                                   uint16_t* o, void* stream) {
+  upipe_status_t s = ring_fwd_checks(desc, q, k, v, seg, tables, o_acc, lse, o);
+  if (s != UPIPE_OK) return s;
+  // timing events between the launches would break the chain: chain only while timing is off
+  const bool chain = !g_timing_on.load(std::memory_order_relaxed);
+  for (int step = 0; step < desc->ring_size; ++step) {
+    s = ring_fwd_launch(desc, step, chain && step > 0, q, k, v, seg, tables, o_acc, lse, o, (cudaStream_t)stream);
+    if (s != UPIPE_OK) return s;
+  }
+  return UPIPE_OK;
+}
+
+static upipe_status_t ring_bwd_checks(const upipe_ring_desc_t* desc, const uint16_t* q, const uint16_t* k,
+                                      const uint16_t* v, const uint16_t* dO, const float* D, const int32_t* seg,
+                                      void* tables, float* dq_acc, float* dk_acc, float* dv_acc, uint16_t* dq,
+                                      uint16_t* dk, uint16_t* dv) {
+  upipe_status_t s = check_ring(desc);
+  if (s != UPIPE_OK) return s;
+  if (!q || !k || !v || !dO || !D || !tables || !dq_acc || !dk_acc || !dv_acc) return UPIPE_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(D) || !aligned16(tables) ||
+      !aligned16(dq_acc) || !aligned16(dk_acc) || !aligned16(dv_acc) || (dq && !aligned16(dq)) ||
+      (dk && !aligned16(dk)) || (dv && !aligned16(dv)) || (seg && !aligned16(seg)))
+    return UPIPE_ERR_ALIGNMENT;
+  return UPIPE_OK;
+}
+
+// dQ then dK/dV of one step.  dq_chained: the previous kernel on the stream is the previous step's
+// dK/dV launch; kv_chained: chain the dK/dV launch to this step's dQ launch, which it follows
+// directly and whose output it does not read (it still waits for it before its epilogue, so it
+// never completes first).
+static upipe_status_t ring_bwd_launch(const upipe_ring_desc_t* desc, int step, bool dq_chained, bool kv_chained,
+                                      const uint16_t* q,
+                                      const uint16_t* k, const uint16_t* v, const uint16_t* dO, const float* D,
+                                      const int32_t* seg, void* tables, float* dq_acc, float* dk_acc, float* dv_acc,
+                                      uint16_t* dq, uint16_t* dk, uint16_t* dv, cudaStream_t st) {
+  AttnBwdArgs b{};
+  b.f = ring_args(desc, step, q, k, v, seg, tables);
+  b.f.dO = reinterpret_cast<const bf16*>(dO);
+  b.f.D = const_cast<float*>(D);
+  b.nkv = b.f.nkv;
+  b.dq_acc = dq_acc;
+  b.dq = reinterpret_cast<bf16*>(dq);
+  b.acc_kv = 1;
+  b.dk_acc = dk_acc;
+  b.dv_acc = dv_acc;
+  b.dk_out = reinterpret_cast<bf16*>(dk);
+  b.dv_out = reinterpret_cast<bf16*>(dv);
+  {
+    b.f.pdl = dq_chained;
+    Timed t(UPIPE_K_RING_DQ, 0, b.f.S, b.f.nh, desc->head_dim, 1, step, st);
+    UPIPE_CUDA(launch_attn_bwd_dq(b, desc->head_dim, st));
+  }
+  b.f.pdl = kv_chained;
+  Timed t(UPIPE_K_RING_DKDV, 0, b.f.S, b.f.nh, desc->head_dim, 1, step, st);
+  return cuda_status(launch_attn_bwd_dkdv(b, desc->head_dim, st));
+}
+
+upipe_status_t upipe_attn_ring_bwd_step(const upipe_ring_desc_t* desc, int32_t step, const uint16_t* q,
+                                        const uint16_t* k, const uint16_t* v, const uint16_t* dO, const float* D,
+                                        const int32_t* seg, void* tables, float* dq_acc, float* dk_acc,
+                                        float* dv_acc, uint16_t* dq, uint16_t* dk, uint16_t* dv, void* stream) {
+  upipe_status_t s = ring_bwd_checks(desc, q, k, v, dO, D, seg, tables, dq_acc, dk_acc, dv_acc, dq, dk, dv);
+  if (s != UPIPE_OK) return s;
+  if (step < 0 || step >= desc->ring_size) return UPIPE_ERR_INVALID_ARG;
+  // timing events between the launches would break a chain: chain only while timing is off
+  const bool chain = !g_timing_on.load(std::memory_order_relaxed);
+  return ring_bwd_launch(desc, step, false, chain, q, k, v, dO, D, seg, tables, dq_acc, dk_acc, dv_acc, dq, dk, dv,
+                         (cudaStream_t)stream);
+}
+
+upipe_status_t upipe_attn_ring_bwd(const upipe_ring_desc_t* desc, const uint16_t* q, const uint16_t* k,
+                                   const uint16_t* v, const uint16_t* o, const uint16_t* dO, const float* lse,
+                                   const int32_t* seg, void* tables, float* D, float* dq_acc, float* dk_acc,
+                                   float* dv_acc, uint16_t* dq, uint16_t* dk, uint16_t* dv, void* stream) {
+  upipe_status_t s = ring_bwd_checks(desc, q, k, v, dO, D, seg, tables, dq_acc, dk_acc, dv_acc, dq, dk, dv);
+  if (s != UPIPE_OK) return s;
+  if (!o || !lse) return UPIPE_ERR_INVALID_ARG;
+  if (!aligned16(o) || !aligned16(lse)) return UPIPE_ERR_ALIGNMENT;
+  cudaStream_t st = (cudaStream_t)stream;
+  UPIPE_CUDA(launch_ring_bwd_prep(desc->dev_count * desc->n_q_heads, 2 * desc->chunk_len, desc->head_dim,
+                                  reinterpret_cast<const bf16*>(o), reinterpret_cast<const bf16*>(dO), lse, D, st));
+  const bool chain = !g_timing_on.load(std::memory_order_relaxed);
+  for (int step = 0; step < desc->ring_size; ++step) {
+    // the first dQ launch follows the prep kernel, whose D it reads: not chained
+    s = ring_bwd_launch(desc, step, chain && step > 0, chain, q, k, v, dO, D, seg, tables, dq_acc, dk_acc, dv_acc,
+                        dq, dk, dv, st);
+    if (s != UPIPE_OK) return s;
+  }
+  return UPIPE_OK;
+}
+
 uint64_t upipe_attn_launch_count(void) { return upipe::g_launch_count.load(std::memory_order_relaxed); }
 
 // Error word of a workspace or table header (bounded device waits, segment order check).

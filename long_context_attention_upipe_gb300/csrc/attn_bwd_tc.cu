@@ -28,7 +28,7 @@
 //   barriers; the two element-wise groups take turns phase by phase (named-barrier ping-pong).
 // Every wait on an mbarrier is bounded (see tc::mbar_wait); registers are split per role with
 // setmaxnreg (launch 168 x 384; control warpgroup 72, element-wise warpgroups 216).
-#include "internal.h"
+#include "geom.cuh"
 #include "tc_common.cuh"
 
 namespace upipe {
@@ -156,15 +156,30 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dq_tc(const __grid_con
   const int64_t S = a.S;
   const int nt = (int)ceil_div(S, kTile);
   const int64_t sp = (int64_t)nt * kTile;
-  const int pair = a.q_order[blockIdx.y];  // most work first (table dispatch order), across all heads
-  const int h = blockIdx.x;
-  const int kvh = h / a.g;
+  // most work first (table dispatch order), across all heads and batched devices
+  const int npairs = (int)ceil_div(nt, 2);
+  const int entry = a.q_order[blockIdx.y];
+  const int dev = entry / npairs, pair = entry - dev * npairs;
+  const int h = dev * a.hq + blockIdx.x;                                // query plane
+  const int kvh = kv_shard_of(a.ring, dev) * a.hkv + blockIdx.x / a.g;  // KV plane
   const int qt0 = 2 * pair, qt1 = 2 * pair + 1;
   const bool valid1 = qt1 < nt;
-  const int4 rng0 = a.q_rows[qt0];
-  const int4 rng1 = valid1 ? a.q_rows[qt1] : make_int4(0, 0, 0, 0);
-  const int j0 = valid1 ? min(rng0.x, rng1.x) : rng0.x;
-  const int j1 = valid1 ? max(rng0.w, rng1.w) : rng0.w;
+  const int4 rng0 = a.q_rows[dev * nt + qt0];
+  const int4 rng1 = valid1 ? a.q_rows[dev * nt + qt1] : make_int4(0, 0, 0, 0);
+  // key tiles of the CTA: the union of its query tiles' ranges (a ring step's tile may have none)
+  const bool has0 = rng0.x < rng0.w, has1 = valid1 && rng1.x < rng1.w;
+  const int j0 = has0 && has1 ? min(rng0.x, rng1.x) : (has0 ? rng0.x : (has1 ? rng1.x : 0));
+  const int j1 = has0 && has1 ? max(rng0.w, rng1.w) : (has0 ? rng0.w : (has1 ? rng1.w : 0));
+  if (b.dq_acc) {
+    grid_dep_trigger();
+    // a ring step adds nothing to query tiles that see no key of the visiting shard (plain
+    // launches always have keys: every row sees itself); the first CTA in dispatch order still
+    // waits for the previous kernel of the chain, so that this grid never completes before it
+    if (j0 >= j1) {
+      if (blockIdx.x == 0 && blockIdx.y == 0) grid_dep_wait();
+      return;
+    }
+  }
 
   if (threadIdx.x == 0) {
     tc::mbar_init(q_full, 1);
@@ -286,11 +301,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dq_tc(const __grid_con
     if (t == 0 || valid1) {
       const int64_t row = (int64_t)(t ? qt1 : qt0) * kTile + r;
       const bool row_ok = row < S;
+      const bool has_keys = rg.x < rg.w;  // false only in a ring step
       int64_t vis_lo = 0, vis_hi = -1;
-      if (row_ok) {
-        vis_lo = seg_first(a.seg, row);
-        vis_hi = a.causal ? row : seg_last(a.seg, S, row);
-      }
+      if (row_ok) make_zig(a.seg, S, a.causal, a.ring, dev).q_interval(row, vis_lo, vis_hi);
       const float Dr = a.D[(int64_t)h * sp + row];
       const float lse2 = a.D[((int64_t)a.nh + h) * sp + row];
       const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
@@ -345,15 +358,37 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dq_tc(const __grid_con
         tc::fence_before_sync();
         tc::mbar_arrive(&ds_full[t]);
       }
-      if (ok) ok = tc::mbar_wait(&dq_full[t], 0, abort_flag, a.err, a.wait_ns);
+      if (ok && has_keys) ok = tc::mbar_wait(&dq_full[t], 0, abort_flag, a.err, a.wait_ns);
       tc::fence_after_sync();
-      bf16* dqrow = b.dq + ((int64_t)h * S + (row_ok ? row : 0)) * DH;
+      if (b.dq_acc) grid_dep_wait();  // the previous ring step's sums are complete and visible
+      bf16* dqrow = b.dq ? b.dq + ((int64_t)h * S + (row_ok ? row : 0)) * DH : nullptr;
+      float* accrow = b.dq_acc ? b.dq_acc + ((int64_t)h * S + (row_ok ? row : 0)) * DH : nullptr;
 #pragma unroll
       for (int ch = 0; ch < DH / 32; ++ch) {
         uint32_t v[32];
         tc::tmem_ld32(q_addr + ch * 32, v);
         tc::tmem_ld_wait();
-        if (ok && row_ok) {
+        if (!has_keys) {  // never in plain launches; dQ = 0 then
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0u;
+        }
+        if (accrow) {  // ring step: fold into the fp32 sum (empty tiles returned or add nothing)
+          if (ok && row_ok && has_keys) {
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4) {
+              float4 o4 = make_float4(0.f, 0.f, 0.f, 0.f);
+              if (!a.acc_first) o4 = *reinterpret_cast<const float4*>(accrow + ch * 32 + q4 * 4);
+              o4.x += __uint_as_float(v[q4 * 4 + 0]) * a.scale;
+              o4.y += __uint_as_float(v[q4 * 4 + 1]) * a.scale;
+              o4.z += __uint_as_float(v[q4 * 4 + 2]) * a.scale;
+              o4.w += __uint_as_float(v[q4 * 4 + 3]) * a.scale;
+              if (!a.acc_last) *reinterpret_cast<float4*>(accrow + ch * 32 + q4 * 4) = o4;
+              if (dqrow)
+                *reinterpret_cast<uint2*>(dqrow + ch * 32 + q4 * 4) =
+                    make_uint2(tc::pack_bf16x2(o4.x, o4.y), tc::pack_bf16x2(o4.z, o4.w));
+            }
+          }
+        } else if (ok && row_ok) {
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
             uint4 pkt;
@@ -428,16 +463,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
   const int64_t S = a.S;
   const int nt = (int)ceil_div(S, kTile);
   const int64_t sp = (int64_t)nt * kTile;
-  // grid (KV heads, key tiles) with the head fastest, the key tiles in the table's dispatch order:
-  // the key tiles seen by the most query tiles (under causality the first ones of each segment)
-  // of every head are dispatched first
-  const int jt = a.kv_order[blockIdx.y];
-  const int kvh = blockIdx.x;
-  const int4 tr = a.kv_rows[jt];  // query tiles {begin, full_begin, full_end, end}
-  const int h_first = kvh * a.g;
-  const int n_heads = max(0, min(a.nh, h_first + a.g) - h_first);
+  // grid (KV heads, key tiles of all key shards) with the head fastest, the key tiles in the
+  // table's dispatch order: the key tiles seen by the most query tiles (under causality the first
+  // ones of each segment) of every head are dispatched first
+  const int entry = a.kv_order[blockIdx.y];
+  const int shard = entry / nt, jt = entry - shard * nt;
+  const int kvh = shard * a.hkv + blockIdx.x;  // KV plane
+  const int dev = dev_of_shard(a.ring, shard);  // the batched device whose queries see this shard
+  const int4 tr = a.kv_rows[entry];             // query tiles {begin, full_begin, full_end, end}
+  const int h_first = dev * a.hq + blockIdx.x * a.g;
+  const int n_heads = dev < a.ndev ? max(0, min(a.hq, (int)blockIdx.x * a.g + a.g) - (int)blockIdx.x * a.g) : 0;
   const int nq = tr.w - tr.x;
   const int n_items = n_heads * nq;
+  if (a.ring.P) {
+    grid_dep_trigger();
+    // a ring step adds nothing to key tiles that no query of the step sees (plain launches write
+    // zeros there; the first ring step has none); the first CTA in dispatch order still waits for
+    // the previous kernel of the chain
+    if (!a.acc_first && n_items == 0) {
+      if (blockIdx.x == 0 && blockIdx.y == 0) grid_dep_wait();
+      return;
+    }
+  }
 
   if (threadIdx.x == 0) {
     tc::mbar_init(kv_full, 1);
@@ -555,10 +602,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
     const bool k_ok = krow < S;
     // the queries that see this key: [vis_lo, vis_hi]
     int64_t vis_lo = 0, vis_hi = -1;
-    if (k_ok) {
-      vis_lo = a.causal ? krow : seg_first(a.seg, krow);
-      vis_hi = seg_last(a.seg, S, krow);
-    }
+    if (k_ok) make_zig(a.seg, S, a.causal, a.ring, dev).k_interval(krow, vis_lo, vis_hi);
     const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
     const uint32_t r_addr = lane_addr + L::r_col(grp);
     float* nvec = reinterpret_cast<float*>(smem + L::VEC) + grp * 256;  // this group's -lse2 | -D
@@ -663,6 +707,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
     // epilogue: group 0 writes dK rows (scaled), group 1 writes dV rows
     if (ok && n_items > 0) ok = tc::mbar_wait(acc_full, 0, abort_flag, a.err, a.wait_ns);
     tc::fence_after_sync();
+    if (a.ring.P) grid_dep_wait();  // the previous ring step's sums are complete and visible
     const uint32_t acc_addr = lane_addr + (grp == 0 ? L::DK_COL : L::DV_COL);
     const float mul = grp == 0 ? a.scale : 1.f;
     const int64_t off = ((int64_t)kvh * S + (k_ok ? krow : 0)) * DH;
@@ -677,15 +722,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
       }
       if (ok && k_ok) {
         if (b.acc_kv) {
+          // fp32 sums over a partial KV group's chunks or over the ring's steps; a ring step also
+          // leaves the running sum rounded to bf16 if asked
           float* dst = (grp == 0 ? b.dk_acc : b.dv_acc) + off + ch * 32;
+          bf16* out = grp == 0 ? b.dk_out : b.dv_out;
+          if (out) out += off + ch * 32;
 #pragma unroll
           for (int q4 = 0; q4 < 8; ++q4) {
-            float4 o4 = *reinterpret_cast<float4*>(dst + q4 * 4);
+            float4 o4 = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (!a.acc_first) o4 = *reinterpret_cast<float4*>(dst + q4 * 4);
             o4.x += __uint_as_float(v[q4 * 4 + 0]) * mul;
             o4.y += __uint_as_float(v[q4 * 4 + 1]) * mul;
             o4.z += __uint_as_float(v[q4 * 4 + 2]) * mul;
             o4.w += __uint_as_float(v[q4 * 4 + 3]) * mul;
-            *reinterpret_cast<float4*>(dst + q4 * 4) = o4;
+            if (!a.acc_last) *reinterpret_cast<float4*>(dst + q4 * 4) = o4;
+            if (out)
+              *reinterpret_cast<uint2*>(out + q4 * 4) = make_uint2(tc::pack_bf16x2(o4.x, o4.y), tc::pack_bf16x2(o4.z, o4.w));
           }
         } else {
           bf16* dst = (grp == 0 ? b.dk : b.dv) + off + ch * 32;
@@ -724,10 +776,16 @@ cudaError_t launch(KFN kfn, size_t bytes, dim3 grid, const CUtensorMap& tq, cons
   cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   AttnBwdArgs args = b;
+  fill_planes(args.f);
   args.f.wait_ns = wait_limit_ns();
-  kfn<<<grid, kThreads, smem, st>>>(tq, tdo, tk, tv, args);
+  if (args.f.pdl) {
+    e = launch_pdl(kfn, grid, dim3(kThreads), smem, st, tq, tdo, tk, tv, args);
+  } else {
+    kfn<<<grid, kThreads, smem, st>>>(tq, tdo, tk, tv, args);
+    e = cudaGetLastError();
+  }
   note_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 template <int DH>
@@ -735,8 +793,10 @@ cudaError_t run_dq(const AttnBwdArgs& b, cudaStream_t st) {
   CUtensorMap tq, tdo, tk, tv;
   if (!make_maps<DH>(b.f, &tq, &tdo, &tk, &tv)) return cudaErrorInvalidValue;
   const int nt = (int)ceil_div(b.f.S, kTile);
-  return launch(k_attn_bwd_dq_tc<DH>, DqLayout<DH>::BYTES + 1024, dim3((unsigned)b.f.nh, (unsigned)ceil_div(nt, 2)), tq,
-                tdo, tk, tv, b, st);
+  AttnArgs f = b.f;
+  fill_planes(f);
+  return launch(k_attn_bwd_dq_tc<DH>, DqLayout<DH>::BYTES + 1024,
+                dim3((unsigned)f.hq, (unsigned)(f.ndev * ceil_div(nt, 2))), tq, tdo, tk, tv, b, st);
 }
 
 template <int DH>
@@ -744,8 +804,10 @@ cudaError_t run_dkdv(const AttnBwdArgs& b, cudaStream_t st) {
   CUtensorMap tq, tdo, tk, tv;
   if (!make_maps<DH>(b.f, &tq, &tdo, &tk, &tv)) return cudaErrorInvalidValue;
   const int nt = (int)ceil_div(b.f.S, kTile);
-  return launch(k_attn_bwd_dkdv_tc<DH>, DkvLayout<DH>::BYTES, dim3((unsigned)b.nkv, (unsigned)nt), tq, tdo, tk, tv,
-                b, st);
+  AttnArgs f = b.f;
+  fill_planes(f);
+  return launch(k_attn_bwd_dkdv_tc<DH>, DkvLayout<DH>::BYTES, dim3((unsigned)f.hkv, (unsigned)(f.kv_count * nt)), tq, tdo,
+                tk, tv, b, st);
 }
 
 }  // namespace

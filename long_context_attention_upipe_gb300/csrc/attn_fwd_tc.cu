@@ -26,7 +26,11 @@
 //
 // MODE 1 (activation recompute for the backward pass): P = exp2(S*scale*log2e - lse*log2e)
 // from the saved log-sum-exp, no rescaling; the epilogue also writes D = rowsum(dO * O).
-#include "internal.h"
+// MODE 2 (one step of the zigzag ring, all batched devices in one launch): MODE 0's softmax,
+// with the epilogue folding the block's (O, lse) into the fp32 running output and lse
+// (L = log(e^L_acc + e^L_b), O = (e^L_acc O_acc + e^L_b O_b) / e^L); query tiles that see no key
+// of the visiting shard are left alone.
+#include "geom.cuh"
 #include "tc_common.cuh"
 
 namespace upipe {
@@ -75,18 +79,33 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t S = a.S;
   const int nt = (int)ceil_div(S, kTile);
-  // grid (heads, query-tile pairs) with the head fastest, the pairs in the table's dispatch order,
-  // so the CTAs are dispatched most work first across all heads (a late long CTA would leave the
-  // others idle at the end); with packed segments the work depends on the position in the segment
-  const int pair = a.q_order[blockIdx.y];
-  const int h = blockIdx.x;
-  const int kvh = h / a.g;
+  // grid (heads, query-tile pairs of all batched devices) with the head fastest, the pairs in the
+  // table's dispatch order, so the CTAs are dispatched most work first across all heads (a late
+  // long CTA would leave the others idle at the end); with packed segments the work depends on
+  // the position in the segment
+  const int npairs = (int)ceil_div(nt, 2);
+  const int entry = a.q_order[blockIdx.y];
+  const int dev = entry / npairs, pair = entry - dev * npairs;
+  const int h = dev * a.hq + blockIdx.x;                            // query plane
+  const int kvh = kv_shard_of(a.ring, dev) * a.hkv + blockIdx.x / a.g;  // KV plane
   const int qt0 = 2 * pair, qt1 = 2 * pair + 1;
   const bool valid1 = qt1 < nt;
-  const int4 rng0 = a.q_rows[qt0];
-  const int4 rng1 = valid1 ? a.q_rows[qt1] : make_int4(0, 0, 0, 0);
-  const int j0 = valid1 ? min(rng0.x, rng1.x) : rng0.x;
-  const int j1 = valid1 ? max(rng0.w, rng1.w) : rng0.w;
+  const int4 rng0 = a.q_rows[dev * nt + qt0];
+  const int4 rng1 = valid1 ? a.q_rows[dev * nt + qt1] : make_int4(0, 0, 0, 0);
+  // key tiles of the CTA: the union of its query tiles' ranges (a ring step's tile may have none)
+  const bool has0 = rng0.x < rng0.w, has1 = valid1 && rng1.x < rng1.w;
+  const int j0 = has0 && has1 ? min(rng0.x, rng1.x) : (has0 ? rng0.x : (has1 ? rng1.x : 0));
+  const int j1 = has0 && has1 ? max(rng0.w, rng1.w) : (has0 ? rng0.w : (has1 ? rng1.w : 0));
+  if (MODE == 2) {
+    grid_dep_trigger();
+    // a ring step adds nothing to query tiles that see no key of the visiting shard (plain
+    // launches always have keys: every row sees itself).  The first CTA in dispatch order waits
+    // for the previous step even then, so that this grid never completes before it.
+    if (j0 >= j1) {
+      if (blockIdx.x == 0 && blockIdx.y == 0) grid_dep_wait();
+      return;
+    }
+  }
 
   if (threadIdx.x == 0) {
     tc::mbar_init(q_full, 1);
@@ -215,12 +234,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     if (t == 0 || valid1) {
       const int64_t row = (int64_t)(t ? qt1 : qt0) * kTile + r;
       const bool row_ok = row < S;
+      const bool has_keys = rg.x < rg.w;  // false only in a ring step
       // the keys this row sees: [vis_lo, vis_hi] (empty for rows past the end)
       int64_t vis_lo = 0, vis_hi = -1;
-      if (row_ok) {
-        vis_lo = seg_first(a.seg, row);
-        vis_hi = a.causal ? row : seg_last(a.seg, S, row);
-      }
+      if (row_ok) make_zig(a.seg, S, a.causal, a.ring, dev).q_interval(row, vis_lo, vis_hi);
       const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
       const uint32_t s_addr = lane_addr + L::s_col(t), o_addr = lane_addr + L::o_col(t);
       const float c = a.scale * kLog2e;
@@ -265,7 +282,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         float mu;
         float f = 1.f;
         bool rescale_o = false;
-        if (MODE == 0) {
+        if (MODE != 1) {
           float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
           for (int k = 0; k < 128; k += 2)
@@ -297,7 +314,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         const float l4[4] = {l2[0].x, l2[0].y, l2[1].x, l2[1].y};
         tc::tmem_st_wait();
-        if (MODE == 0 && __any_sync(0xffffffffu, rescale_o)) {
+        if (MODE != 1 && __any_sync(0xffffffffu, rescale_o)) {
           // O_t is idle here: P V of the previous tile completed before this S was ready, and
           // this tile's P V waits for the arrival below
 #pragma unroll
@@ -321,10 +338,56 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       // after an abort, hand over the turns still owed so the other group never blocks on them
       for (int k = turn; k < n_give; ++k) tc::named_bar_arrive(kPing + 1 - t, 256);
-      if (ok) ok = tc::mbar_wait(&o_full[t], 0, abort_flag, a.err, a.wait_ns);
+      if (ok && has_keys) ok = tc::mbar_wait(&o_full[t], 0, abort_flag, a.err, a.wait_ns);
       tc::fence_after_sync();
       // epilogue: O / l -> bf16 row; lse or D
-      const float inv = (MODE == 0) ? (l > 0.f ? 1.f / l : 0.f) : 1.f;
+      const float inv = (MODE != 1) ? (l > 0.f ? 1.f / l : 0.f) : 1.f;
+      if constexpr (MODE == 2) {
+        grid_dep_wait();  // the previous step's accumulators are complete and visible
+        // fold the block into the running (O_acc, lse): weights of the two sides in exp2 units
+        const float lb2 = l > 0.f ? m_used + log2f(l) : -INFINITY;
+        const float la2 = (!a.acc_first && row_ok) ? a.lse[(int64_t)h * S + row] * kLog2e : -INFINITY;
+        const float mx = fmaxf(la2, lb2);
+        float wa = 0.f, wb = 0.f, lnew = -INFINITY;
+        if (mx != -INFINITY) {
+          wa = exp2f(la2 - mx);  // 0 when la2 = -inf
+          wb = exp2f(lb2 - mx);
+          const float sum = wa + wb;
+          lnew = (mx + log2f(sum)) * kLn2;
+          wa /= sum;
+          wb = wb / sum * inv;
+        }
+        const bool act = ok && row_ok && has_keys;
+        float* arow = a.o_acc + ((int64_t)h * S + (row_ok ? row : 0)) * DH;
+        bf16* orow = a.o ? a.o + ((int64_t)h * S + (row_ok ? row : 0)) * DH : nullptr;
+#pragma unroll
+        for (int ch = 0; ch < DH / 32; ++ch) {
+          uint32_t v[32];
+          tc::tmem_ld32(o_addr + ch * 32, v);
+          tc::tmem_ld_wait();
+          if (act) {
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4) {
+              float4 o4 = make_float4(0.f, 0.f, 0.f, 0.f);
+              if (wa != 0.f) {  // a side with weight 0 contributes nothing, whatever it holds
+                const float4 p4 = *reinterpret_cast<const float4*>(arow + ch * 32 + q4 * 4);
+                o4 = make_float4(wa * p4.x, wa * p4.y, wa * p4.z, wa * p4.w);
+              }
+              if (wb != 0.f) {
+                o4.x += wb * __uint_as_float(v[q4 * 4 + 0]);
+                o4.y += wb * __uint_as_float(v[q4 * 4 + 1]);
+                o4.z += wb * __uint_as_float(v[q4 * 4 + 2]);
+                o4.w += wb * __uint_as_float(v[q4 * 4 + 3]);
+              }
+              if (!a.acc_last) *reinterpret_cast<float4*>(arow + ch * 32 + q4 * 4) = o4;
+              if (orow)
+                *reinterpret_cast<uint2*>(orow + ch * 32 + q4 * 4) =
+                    make_uint2(tc::pack_bf16x2(o4.x, o4.y), tc::pack_bf16x2(o4.z, o4.w));
+            }
+          }
+        }
+        if (act) a.lse[(int64_t)h * S + row] = lnew;
+      } else {
       bf16* orow = a.o + ((int64_t)h * S + (row_ok ? row : 0)) * DH;
       const bf16* dorow = (MODE == 1) ? a.dO + ((int64_t)h * S + (row_ok ? row : 0)) * DH : nullptr;
       float dsum = 0.f;
@@ -333,6 +396,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         uint32_t v[32];
         tc::tmem_ld32(o_addr + ch * 32, v);
         tc::tmem_ld_wait();
+        if (!has_keys) {  // never in plain launches (every row sees itself); O = 0 then
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0u;
+        }
         if (ok && row_ok) {
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
@@ -362,6 +429,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         a.D[(int64_t)h * sp + row] = row_ok ? dsum : 0.f;
         a.D[((int64_t)a.nh + h) * sp + row] = row_ok ? m_used : 0.f;
       }
+      }
     }
   }
   tc::fence_before_sync();
@@ -384,13 +452,19 @@ cudaError_t run(const AttnArgs& a, cudaStream_t st) {
   auto kfn = k_attn_fwd_tc<DH, MODE>;
   cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  const int nt = (int)ceil_div(a.S, kTile);
-  dim3 grid((unsigned)a.nh, (unsigned)ceil_div(nt, 2));
   AttnArgs args = a;
+  fill_planes(args);
+  const int nt = (int)ceil_div(a.S, kTile);
+  dim3 grid((unsigned)args.hq, (unsigned)(args.ndev * ceil_div(nt, 2)));
   args.wait_ns = wait_limit_ns();
-  kfn<<<grid, kFwdThreads, smem, st>>>(tq, tk, tv, args);
+  if (args.pdl) {
+    e = launch_pdl(kfn, grid, dim3(kFwdThreads), smem, st, tq, tk, tv, args);
+  } else {
+    kfn<<<grid, kFwdThreads, smem, st>>>(tq, tk, tv, args);
+    e = cudaGetLastError();
+  }
   note_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace
@@ -400,6 +474,9 @@ cudaError_t launch_attn_fwd(const AttnArgs& a, int head_dim, cudaStream_t st) {
 }
 cudaError_t launch_attn_recompute(const AttnArgs& a, int head_dim, cudaStream_t st) {
   return head_dim == 64 ? run<64, 1>(a, st) : run<128, 1>(a, st);
+}
+cudaError_t launch_attn_ring_fwd(const AttnArgs& a, int head_dim, cudaStream_t st) {
+  return head_dim == 64 ? run<64, 2>(a, st) : run<128, 2>(a, st);
 }
 
 }  // namespace upipe

@@ -49,6 +49,13 @@ __device__ __forceinline__ int64_t seg_last(const int32_t* seg, int64_t S, int64
   return lo;
 }
 
+// Programmatic dependent launch between consecutive ring steps: a CTA lets the next step's grid
+// start on the SMs this grid leaves free (trigger), and a step waits for the previous step to
+// complete, with its writes visible, before it touches the accumulators they share (wait).  Both
+// are no-ops for a grid launched without programmatic stream serialisation.
+__device__ __forceinline__ void grid_dep_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // First error wins; the word lives in the table header.
 __device__ __forceinline__ void set_error(int* word, int code) { atomicCAS(word, 0, code); }
 

@@ -19,24 +19,44 @@ uint64_t wait_limit_ns();
 // once (arrive = 1): the timeout path of the wait helper, reported in a table header's error word.
 cudaError_t launch_wait_probe(void* header, int arrive, cudaStream_t st);
 
+// ---------------------------------------------------------------- row geometry
+// Zigzag ring (P2P context parallelism with causal load balancing: MaxText long-context article,
+// strategy table and the paragraph after it).  The sequence is cut into 2P chunks of C rows; ring
+// device r holds chunks r and 2P-1-r as one plane of 2C rows, so local row i sits at position
+// i < C ? rC + i : (2P-1-r)C + i - C.  At ring step s device r attends to the key/value shard of
+// device (r - s) mod P.  A launch may batch the query shards of `ndev` devices r0, r0+1, ... (as
+// extra planes) against `kv_count` key/value shards; shard m in memory belongs to device
+// (kv0 + m) mod P.  P == 0: plain geometry, query and key row i share position i.
+struct RingGeom {
+  int P;
+  int r0, step, kv0;
+  int64_t C;
+};
+
 // ---------------------------------------------------------------- tile-skip table
-size_t tile_table_bytes(int64_t S);
+// Layout: header, q_rows [ndev][nt] int4, kv_rows [kv_count][nt] int4, q_order [ndev * npairs]
+// int32 (entry = device * npairs + pair), kv_order [kv_count * nt] (entry = shard * nt + tile),
+// with nt = ceil(S / 128) tiles per plane and npairs = ceil(nt / 2).
+size_t tile_table_bytes(int64_t S, int ndev = 1, int kv_count = 1);
 cudaError_t launch_tile_table(int64_t S, int causal, const int32_t* seg, void* table, cudaStream_t st);
+// The table of one ring step: seg (NULL or [2PC]) is indexed by global position.
+cudaError_t launch_ring_table(int64_t S, int causal, const int32_t* seg, const RingGeom& g, int ndev, int kv_count,
+                              void* table, cudaStream_t st);
 
 inline const int4* table_q_rows(const void* table) {
   return reinterpret_cast<const int4*>(reinterpret_cast<const char*>(table) + sizeof(TableHeader));
 }
-inline const int4* table_kv_rows(const void* table, int64_t S) {
-  return table_q_rows(table) + ceil_div(S, kTile);
+inline const int4* table_kv_rows(const void* table, int64_t S, int ndev = 1) {
+  return table_q_rows(table) + ndev * ceil_div(S, kTile);
 }
 // Dispatch orders: query-tile pairs (2p, 2p + 1) and key tiles, each by non-increasing number of
 // non-empty tiles (the work of the CTA that takes it), ties by the position the kernels used before
 // (later pairs first, earlier key tiles first).
-inline const int32_t* table_q_order(const void* table, int64_t S) {
-  return reinterpret_cast<const int32_t*>(table_kv_rows(table, S) + ceil_div(S, kTile));
+inline const int32_t* table_q_order(const void* table, int64_t S, int ndev = 1, int kv_count = 1) {
+  return reinterpret_cast<const int32_t*>(table_kv_rows(table, S, ndev) + kv_count * ceil_div(S, kTile));
 }
-inline const int32_t* table_kv_order(const void* table, int64_t S) {
-  return table_q_order(table, S) + ceil_div(ceil_div(S, kTile), 2);
+inline const int32_t* table_kv_order(const void* table, int64_t S, int ndev = 1, int kv_count = 1) {
+  return table_q_order(table, S, ndev, kv_count) + ndev * ceil_div(ceil_div(S, kTile), 2);
 }
 
 // ---------------------------------------------------------------- projection GEMMs
@@ -114,9 +134,47 @@ struct AttnArgs {
   float scale;      // softmax scale
   int* err;         // device error word (table header), set by bounded waits that time out
   uint64_t wait_ns; // limit of each bounded wait (set at launch)
+  // Planes: the nh query planes are ndev devices x hq heads, the nkv KV planes kv_count shards x
+  // hkv heads.  Zero (plain launches) means ndev = kv_count = 1, hq = nh, hkv = nkv.
+  int hq, hkv, ndev, kv_count;
+  RingGeom ring;    // ring.P == 0: plain geometry
+  // Ring steps fold their result into fp32 accumulators: acc_first (step 0) writes them instead
+  // of reading them; acc_last skips storing the fp32 state once only the bf16 result is needed.
+  int acc_first, acc_last;
+  float* o_acc;     // ring forward: [nh, S, Dh] fp32 running output (lse holds the running lse);
+                    // o (if not NULL) receives the merged output rounded to bf16
+  int pdl;          // launch with programmatic stream serialisation: the previous kernel on the
+                    // stream is the previous ring step of the same call (see grid_dep_wait)
 };
 
+// Launch with programmatic stream serialisation allowed (the grid may start while the previous
+// kernel on the stream finishes; it synchronises with grid_dep_wait).
+template <typename K, typename... Args>
+cudaError_t launch_pdl(K kfn, dim3 grid, dim3 block, size_t smem, cudaStream_t st, const Args&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kfn, args...);
+}
+
+// Plain launches leave the plane fields zero: one device, one key shard, all heads of the launch.
+inline void fill_planes(AttnArgs& a) {
+  if (a.hq == 0) a.hq = a.nh;
+  if (a.hkv == 0) a.hkv = a.nkv;
+  if (a.ndev == 0) a.ndev = 1;
+  if (a.kv_count == 0) a.kv_count = 1;
+}
+
 cudaError_t launch_attn_fwd(const AttnArgs& a, int head_dim, cudaStream_t st);
+// One ring step of the forward: the block results are merged into o_acc / lse (see AttnArgs).
+cudaError_t launch_attn_ring_fwd(const AttnArgs& a, int head_dim, cudaStream_t st);
 // O and D from the saved lse (no online rescaling): activation recompute for the backward pass.
 cudaError_t launch_attn_recompute(const AttnArgs& a, int head_dim, cudaStream_t st);
 
@@ -125,10 +183,13 @@ struct AttnBwdArgs {
   bf16* dq;         // [nh, S, Dh]
   bf16* dk;         // [nkv, S, Dh]  written when acc_kv == 0
   bf16* dv;
-  float* dk_acc;    // [nkv, S, Dh]  f32 accumulators when acc_kv == 1 (partial KV group)
+  float* dk_acc;    // [nkv, S, Dh]  f32 accumulators when acc_kv == 1 (partial KV group, ring)
   float* dv_acc;
   int acc_kv;
   int nkv;
+  float* dq_acc;    // ring: [nh, S, Dh] f32 accumulator of dQ (dq, if not NULL, gets it in bf16)
+  bf16* dk_out;     // ring: the accumulated dK, dV rounded to bf16 (NULL: not written)
+  bf16* dv_out;
 };
 cudaError_t launch_attn_bwd_dq(const AttnBwdArgs& a, int head_dim, cudaStream_t st);
 cudaError_t launch_attn_bwd_dkdv(const AttnBwdArgs& a, int head_dim, cudaStream_t st);

@@ -555,6 +555,42 @@ def tile_table(S: int, seg, causal: bool, q_tiles=None, kv_tiles=None, B: int = 
 
 
 # ----------------------------------------------------------------------------------------------
+# zigzag ring steps (MaxText long-context article: strategy table, row "P2P (Ring)", and the
+# paragraph after it: the ring needs causal load balancing, which reorders the sequence)
+# ----------------------------------------------------------------------------------------------
+
+def zigzag_positions(P: int, C: int, r: int) -> np.ndarray:
+    """Sequence positions of ring device r's rows: the 2P chunks of C rows are dealt so that
+    device r holds chunk r and chunk 2P - 1 - r (one early, one late), in that order.  The pages
+    name the balancing but not the deal; this pairing is the plainest one that gives every device
+    the same causal work."""
+    return np.concatenate([np.arange(r * C, (r + 1) * C), np.arange((2 * P - 1 - r) * C, (2 * P - r) * C)])
+
+
+def ring_step_visibility(P: int, C: int, r: int, s: int, seg, causal: bool = True) -> np.ndarray:
+    """vis[i, j]: does device r's row i see row j of the key/value shard that visits it at step s
+    (the shard of device (r - s) mod P)?  The mask definition above, on the rows' positions."""
+    src = (r - s) % P
+    return visibility(seg, zigzag_positions(P, C, r), zigzag_positions(P, C, src), causal)
+
+
+def ring_step_table(P: int, C: int, r: int, s: int, seg, causal: bool = True, B: int = TILE):
+    """The skip-table rows of one ring step, by brute-force tile classification of the step's
+    visibility (small C only): q-major rows of device r's query tiles over the visiting shard's
+    key tiles, and kv-major rows of the visiting shard's key tiles over device r's query tiles."""
+    vis = ring_step_visibility(P, C, r, s, seg, causal)
+    S = 2 * C
+    n = -(-S // B)
+    cls = np.zeros((n, n), dtype=np.int8)
+    for i in range(n):
+        for j in range(n):
+            blk = vis[i * B: (i + 1) * B, j * B: (j + 1) * B]
+            c = int(blk.sum())
+            cls[i, j] = EMPTY if c == 0 else (FULL if c == blk.size else PARTIAL)
+    return ranges_from_classes(cls), ranges_from_classes(cls.T)
+
+
+# ----------------------------------------------------------------------------------------------
 # brute-force row softmax (a pin for the vectorised code above)
 # ----------------------------------------------------------------------------------------------
 

@@ -5,6 +5,7 @@ import os
 import re
 
 import pytest
+import torch
 
 import long_context_attention_upipe_gb300 as up
 
@@ -174,20 +175,66 @@ def test_zigzag_ring_schedule_is_balanced_and_complete(P):
         assert len(set(contiguous)) > 1
 
 
-def test_ring_runs_check_their_inputs_before_touching_the_gpu():
-    import torch
-    q = torch.zeros(4, 64, 128, dtype=torch.bfloat16)
-    k = torch.zeros(2, 64, 128, dtype=torch.bfloat16)
-    with pytest.raises(ValueError):
-        up.ring_attention_share(q, k, k, 3)                    # 64 not a multiple of 2P = 6
-    with pytest.raises(ValueError):
-        up.ring_attention_share(q, k[:, :32], k[:, :32], 2)    # key positions differ
-    with pytest.raises(ValueError):
-        up.ring_attention_share(q.float(), k, k, 2)            # not bf16
-    with pytest.raises(ValueError):
-        up.ring_attention_share(q[:3], k, k, 2)                # Hq not a multiple of Hkv
-    with pytest.raises(ValueError):
-        up.ring_attention_share(q, k, k, 0)
-    lse = torch.zeros(4, 64)
-    with pytest.raises(ValueError):
-        up.ring_attention_share_backward(q, k, k, q, lse[:, :32], q, 2)
+def test_ring_step_calls_check_their_arguments_before_any_launch():
+    L = up.lib()
+    launches = up.launch_count()
+    fake = ctypes.c_void_p(0x10000)       # never dereferenced: the checks fail first
+    odd = ctypes.c_void_p(0x10008)
+    n = ctypes.c_size_t()
+    ok = up.make_ring_desc(4, 256, 8, 2, 128)
+    assert L.upipe_attn_ring_tables_size(ctypes.byref(ok), ctypes.byref(n)) == 0 and n.value > 0
+    bad = [
+        (up.make_ring_desc(0, 256, 8, 2, 128), 1),                           # no devices
+        (up.make_ring_desc(4, 0, 8, 2, 128), 1),                             # empty chunk
+        (up.make_ring_desc(4, 1 << 30, 8, 2, 128), 1),                       # 2C above 2^31 - 1
+        (up.make_ring_desc(4, 256, 6, 4, 128), 1),                           # Hq not a multiple of Hkv
+        (up.make_ring_desc(4, 256, 8, 2, 96), 2),                            # head_dim
+        (up.make_ring_desc(4, 256, 8, 2, 128, dev_first=3, dev_count=2), 1),  # devices past the ring
+        (up.make_ring_desc(4, 256, 8, 2, 128, dev_count=2, kv_count=3), 1),  # shard count neither P nor dev_count
+    ]
+    for d, code in bad:
+        assert L.upipe_attn_ring_tables_size(ctypes.byref(d), ctypes.byref(n)) == code
+        assert L.upipe_attn_ring_build_tables(ctypes.byref(d), None, fake, 1 << 20, None) == code
+        assert L.upipe_attn_ring_fwd_step(ctypes.byref(d), 0, fake, fake, fake, None, fake, fake, fake, None, None) == code
+    assert L.upipe_attn_ring_build_tables(ctypes.byref(ok), None, fake, n.value - 16, None) == 4   # too small
+    assert L.upipe_attn_ring_build_tables(ctypes.byref(ok), odd, fake, n.value, None) == 3         # seg alignment
+    f = L.upipe_attn_ring_fwd_step
+    assert f(ctypes.byref(ok), 4, fake, fake, fake, None, fake, fake, fake, None, None) == 1       # step past P - 1
+    assert f(ctypes.byref(ok), -1, fake, fake, fake, None, fake, fake, fake, None, None) == 1
+    assert f(ctypes.byref(ok), 0, fake, fake, fake, None, fake, None, fake, None, None) == 1       # no accumulator
+    assert f(ctypes.byref(ok), 0, fake, fake, fake, None, fake, fake, fake, odd, None) == 3        # o alignment
+    b = L.upipe_attn_ring_bwd_step
+    assert b(ctypes.byref(ok), 0, fake, fake, fake, fake, None, None, fake, fake, fake, fake, None, None, None,
+             None) == 1                                                                         # no D
+    assert b(ctypes.byref(ok), 0, fake, fake, fake, fake, fake, None, fake, fake, odd, fake, None, None, None,
+             None) == 3                                                                         # dk_acc alignment
+    r = L.upipe_attn_ring_fwd
+    assert r(ctypes.byref(bad[0][0]), fake, fake, fake, None, fake, fake, fake, None, None) == 1
+    assert r(ctypes.byref(ok), fake, None, fake, None, fake, fake, fake, None, None) == 1            # no k
+    assert r(ctypes.byref(ok), fake, fake, fake, odd, fake, fake, fake, None, None) == 3             # seg alignment
+    rb = L.upipe_attn_ring_bwd
+    assert rb(ctypes.byref(ok), fake, fake, fake, None, fake, fake, None, fake, fake, fake, fake, fake, None, None,
+              None, None) == 1                                                                    # no o
+    assert rb(ctypes.byref(ok), fake, fake, fake, fake, fake, odd, None, fake, fake, fake, fake, fake, None, None,
+              None, None) == 3                                                                    # lse alignment
+    assert up.launch_count() == launches  # rejected calls launch nothing
+
+
+def test_ring_tables_size_grows_with_the_batch():
+    one = up.ring_tables_bytes(up.make_ring_desc(4, 4096, 8, 2, 128, dev_first=1, dev_count=1, kv_count=1))
+    all_ = up.ring_tables_bytes(up.make_ring_desc(4, 4096, 8, 2, 128))
+    nt = 8192 // 128
+    assert one == 4 * (((32 + 2 * nt * 16 + 4 * (nt // 2 + nt)) + 15) // 16 * 16)
+    assert all_ > 3 * one
+
+
+def test_zigzag_reordering_round_trips_and_balances():
+    P, C = 3, 5
+    x = torch.arange(2 * P * C, dtype=torch.float32).reshape(1, -1, 1).repeat(2, 1, 3)
+    xs = up.to_zigzag(x, P)
+    assert tuple(xs.shape) == (P, 2, 2 * C, 3)
+    for r in range(P):
+        pos = up.zigzag_positions(P, C, r)
+        assert torch.equal(xs[r, 0, :, 0], pos.float())
+        assert bool((pos[1:] > pos[:-1]).all())           # local rows in sequence order
+    assert torch.equal(up.from_zigzag(xs, P), x)

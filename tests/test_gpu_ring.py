@@ -1,6 +1,7 @@
-"""Ring (P2P) context parallelism, single-GPU share: the log-sum-exp merge kernel against the
-oracle's merge, and the zigzag ring's blocks (upipe_attn_core_fwd per block, merged in ring order)
-against causal attention over the whole sequence."""
+"""Ring (P2P) context parallelism, single-GPU share: the ring step calls (one launch per step for
+all devices' shards, fp32 accumulation in the kernels' epilogues) against the oracle's step tables
+and its attention over the whole sequence, one device per call against the batched calls, and
+the merge, backward-prep and accumulation kernels against their definitions."""
 import numpy as np
 import pytest
 import torch
@@ -48,51 +49,207 @@ def test_lse_merge_kernel_matches_oracle(rows, Dh):
     assert torch.equal(out.view(torch.int16), Oa_dev.to(torch.bfloat16).view(torch.int16))
 
 
+# ------------------------------------------------------------------------------------------------
+# ring steps through the C-ABI: one launch per step for all devices' shards
+# ------------------------------------------------------------------------------------------------
+
 RING_CASES = [
-    # P (devices), C (chunk length), Hq, Hkv, Dh
-    (2, 256, 4, 2, 128),
-    (3, 200, 2, 1, 64),
-    (4, 128, 8, 2, 128),
+    # P (devices), C (chunk length), Hq, Hkv, Dh, packed segment lengths (None: one sequence)
+    (1, 256, 2, 1, 128, None),
+    (2, 256, 4, 2, 128, None),
+    (3, 200, 2, 1, 64, None),
+    (4, 128, 8, 2, 128, None),
+    (4, 192, 4, 1, 128, [700, 1, 300, 535]),
+    (3, 100, 2, 2, 64, [150, 10, 440]),
 ]
+ids = lambda c: f"P{c[0]}_C{c[1]}_hq{c[2]}_hkv{c[3]}_dh{c[4]}" + ("_packed" if c[5] else "")
 
 
-@pytest.mark.parametrize("case", RING_CASES, ids=lambda c: f"P{c[0]}_C{c[1]}_hq{c[2]}_hkv{c[3]}_dh{c[4]}")
-def test_zigzag_ring_share_matches_causal_attention(case):
-    P, C, Hq, Hkv, Dh = case
-    S = 2 * P * C
-    q, k, v, _ = qkv_inputs(S, Hq, Hkv, Dh)
-    qt, kt, vt = (bf16_tensor(x) for x in (q, k, v))
-    n0 = up.launch_count()
-    O, lse = up.ring_attention_share(qt, kt, vt, P)
-    torch.cuda.synchronize()
-    n_blocks = P * (2 * P + 1)
-    assert up.launch_count() - n0 == 2 * 4 + 2 * n_blocks   # two tables, then one attention + one merge per block
-    Q, K, V = (ui.bf16_to_f64(x) for x in (q, k, v))
-    O_ref, L_ref = orc.attention_forward(Q, K, V, None, True, orc.default_scale(Dh))
-    o = to_f64(O)
-    assert max_abs_bf16_out(o, O_ref) <= OUT_MAX_ABS, max_abs_bf16_out(o, O_ref)
-    assert rel_fro(o, O_ref) <= OUT_REL_FRO, rel_fro(o, O_ref)
-    assert max_abs(to_f64(lse), L_ref) <= 1e-3
-
-
-@pytest.mark.parametrize("case", RING_CASES, ids=lambda c: f"P{c[0]}_C{c[1]}_hq{c[2]}_hkv{c[3]}_dh{c[4]}")
-def test_zigzag_ring_share_backward_matches_causal_gradients(case):
-    P, C, Hq, Hkv, Dh = case
+def ring_setup(case, dev_count=None):
+    P, C, Hq, Hkv, Dh, lengths = case
     S = 2 * P * C
     q, k, v, do = qkv_inputs(S, Hq, Hkv, Dh)
-    qt, kt, vt, dot = (bf16_tensor(x) for x in (q, k, v, do))
-    O, lse = up.ring_attention_share(qt, kt, vt, P)
-    n0 = up.launch_count()
-    dq, dk, dv = up.ring_attention_share_backward(qt, kt, vt, O, lse, dot, P)
+    seg = ui.segments_from_lengths(lengths) if lengths else None
+    seg_t = torch.from_numpy(seg).cuda() if seg is not None else None
+    shards = [up.to_zigzag(bf16_tensor(x), P).contiguous() for x in (q, k, v, do)]
+    return (q, k, v, do), seg, seg_t, shards
+
+
+def table_rows(tables, per, step, S, ndev, kvc):
+    raw = tables[step * per:(step + 1) * per].cpu().numpy()
+    nt = -(-S // 128)
+    npairs = (nt + 1) // 2
+    body = raw[32:].view(np.int32)
+    qr = body[:ndev * nt * 4].reshape(ndev, nt, 4)
+    kr = body[ndev * nt * 4:(ndev + kvc) * nt * 4].reshape(kvc, nt, 4)
+    off = (ndev + kvc) * nt * 4
+    qo = body[off:off + ndev * npairs]
+    ko = body[off + ndev * npairs:off + ndev * npairs + kvc * nt]
+    return qr, kr, qo, ko
+
+
+@pytest.mark.parametrize("case", RING_CASES, ids=ids)
+@pytest.mark.parametrize("causal", [True, False])
+def test_ring_tables_bit_exact(case, causal):
+    """Every step's table (query rows per device, key rows per shard) equals the oracle's brute-force
+    tile classification of that step's visibility; the dispatch orders are permutations by
+    non-increasing work."""
+    P, C, Hq, Hkv, Dh, lengths = case
+    _, seg, seg_t, _ = ring_setup(case)
+    desc = up.make_ring_desc(P, C, Hq, Hkv, Dh, causal)
+    tables = torch.empty(up.ring_tables_bytes(desc), dtype=torch.uint8, device="cuda")
+    up.ring_build_tables(desc, seg_t, tables)
     torch.cuda.synchronize()
-    n_blocks = P * (2 * P + 1)
-    # two tables, one D buffer per chunk, then per block dQ, dK/dV and three accumulations
-    assert up.launch_count() - n0 == 2 * 4 + 2 * P + 5 * n_blocks
-    Q, K, V, dO = (ui.bf16_to_f64(x) for x in (q, k, v, do))
-    dQ, dK, dV = orc.attention_backward(Q, K, V, dO, None, True, orc.default_scale(Dh))
-    assert rel_fro(to_f64(dq), dQ) <= GRAD_REL_FRO, rel_fro(to_f64(dq), dQ)
-    assert rel_fro(to_f64(dk), dK) <= GRAD_REL_FRO, rel_fro(to_f64(dk), dK)
-    assert rel_fro(to_f64(dv), dV) <= GRAD_REL_FRO, rel_fro(to_f64(dv), dV)
+    assert up.device_status(tables) == 0
+    per = tables.numel() // P
+    for s in range(P):
+        qr, kr, qo, ko = table_rows(tables, per, s, 2 * C, P, P)
+        for r in range(P):
+            want_q, want_kv = orc.ring_step_table(P, C, r, s, seg, causal)
+            np.testing.assert_array_equal(qr[r], want_q, err_msg=f"step {s} device {r}")
+            # key shard m (held in device order) serves device (m + s) mod P at step s
+            m = (r - s) % P
+            np.testing.assert_array_equal(kr[m], want_kv, err_msg=f"step {s} shard {m}")
+        nt = qr.shape[1]
+        pair_work = np.array([sum(qr[d, t, 3] - qr[d, t, 0] for t in (2 * p_, 2 * p_ + 1) if t < nt)
+                              for d in range(P) for p_ in range((nt + 1) // 2)])
+        assert sorted(qo.tolist()) == list(range(len(pair_work)))
+        assert np.all(np.diff(pair_work[qo]) <= 0)
+        kv_work = (kr[:, :, 3] - kr[:, :, 0]).reshape(-1)
+        assert sorted(ko.tolist()) == list(range(len(kv_work)))
+        assert np.all(np.diff(kv_work[ko]) <= 0)
+
+
+def oracle_attention(arrs, seg, Dh, causal=True):
+    q, k, v, do = (ui.bf16_to_f64(x) for x in arrs)
+    O, L = orc.attention_forward(q, k, v, seg, causal, orc.default_scale(Dh))
+    return q, k, v, do, O, L
+
+
+@pytest.mark.parametrize("case", RING_CASES, ids=ids)
+def test_ring_forward_steps_match_attention_over_the_sequence(case):
+    P, C, Hq, Hkv, Dh, lengths = case
+    arrs, seg, seg_t, (qs, ks, vs, _) = ring_setup(case)
+    desc = up.make_ring_desc(P, C, Hq, Hkv, Dh)
+    ring = up.Ring(desc, seg_t)
+    o_acc = torch.full(qs.shape, float("nan"), dtype=torch.float32, device="cuda")
+    lse = torch.full(qs.shape[:3], float("nan"), dtype=torch.float32, device="cuda")
+    o = torch.full_like(qs, float("nan"))
+    n0 = up.launch_count()
+    ring.forward(qs, ks, vs, out=(o_acc, lse, o))
+    torch.cuda.synchronize()
+    assert up.launch_count() - n0 == P           # one launch per ring step, all devices batched
+    assert up.device_status(ring.tables) == 0
+    # the P step calls one by one give the chained call's results bit for bit
+    o1, lse1 = ring.forward(qs, ks, vs, per_step=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o) and torch.equal(lse1, lse)
+    *_, O_ref, L_ref = oracle_attention(arrs, seg, Dh)
+    got = to_f64(up.from_zigzag(o, P))
+    assert max_abs_bf16_out(got, O_ref) <= OUT_MAX_ABS, max_abs_bf16_out(got, O_ref)
+    assert rel_fro(got, O_ref) <= OUT_REL_FRO, rel_fro(got, O_ref)
+    assert max_abs(to_f64(up.from_zigzag(lse, P)), L_ref) <= 1e-3
+    if P > 1:   # the last step leaves the fp32 state of the earlier steps; o is its rounding
+        partial = to_f64(o_acc)
+        assert np.isfinite(partial).all()
+
+
+@pytest.mark.parametrize("case", RING_CASES[1:5], ids=ids)
+def test_one_device_per_call_matches_the_batched_steps(case):
+    """A device of a real ring calls each step with its own query shard and the visiting key/value
+    shard (dev_count = kv_count = 1): the results equal the batched run's bit for bit."""
+    P, C, Hq, Hkv, Dh, lengths = case
+    _, seg, seg_t, (qs, ks, vs, dos) = ring_setup(case)
+    ring = up.Ring(up.make_ring_desc(P, C, Hq, Hkv, Dh), seg_t)
+    o_all, lse_all = ring.forward(qs, ks, vs)
+    dq_all, dk_all, dv_all = ring.backward(qs, ks, vs, o_all, lse_all, dos)
+    torch.cuda.synchronize()
+    S, sp = 2 * C, -(-2 * C // 128) * 128
+    dk_acc = torch.empty(ks.shape, dtype=torch.float32, device="cuda")   # travels with its shard
+    dv_acc = torch.empty(ks.shape, dtype=torch.float32, device="cuda")
+    dk_out, dv_out = torch.empty_like(ks), torch.empty_like(vs)
+    per_dev = []
+    for r in range(P):
+        d1 = up.make_ring_desc(P, C, Hq, Hkv, Dh, dev_first=r, dev_count=1, kv_count=1)
+        tables = torch.empty(up.ring_tables_bytes(d1), dtype=torch.uint8, device="cuda")
+        up.ring_build_tables(d1, seg_t, tables)
+        o_acc = torch.empty((1,) + tuple(qs.shape[1:]), dtype=torch.float32, device="cuda")
+        lse = torch.empty((1,) + tuple(qs.shape[1:3]), dtype=torch.float32, device="cuda")
+        o = torch.empty_like(qs[r:r + 1])
+        for s in range(P):
+            src = (r - s) % P
+            up.ring_fwd_step(d1, s, qs[r:r + 1], ks[src:src + 1], vs[src:src + 1], seg_t, tables, o_acc, lse, o)
+        per_dev.append((d1, tables, o, lse))
+        assert torch.equal(o[0], o_all[r]) and torch.equal(lse[0], lse_all[r])
+    # backward: the shard accumulators travel with their shard, device r adding at step s to the
+    # accumulator of shard (r - s) mod P; steps run in order across the ring
+    dq = torch.empty_like(qs)
+    dq_acc = torch.empty(qs.shape, dtype=torch.float32, device="cuda")
+    Ds = []
+    for r, (d1, tables, o, lse) in enumerate(per_dev):
+        D = torch.empty(2, Hq, sp, dtype=torch.float32, device="cuda")
+        up.ring_bwd_prep(o[0], dos[r], lse[0], D)
+        Ds.append(D)
+    for s in range(P):
+        for r, (d1, tables, o, lse) in enumerate(per_dev):
+            src = (r - s) % P
+            up.ring_bwd_step(d1, s, qs[r:r + 1], ks[src:src + 1], vs[src:src + 1], dos[r:r + 1], Ds[r], seg_t, tables,
+                             dq_acc[r:r + 1], dk_acc[src:src + 1], dv_acc[src:src + 1], dq[r:r + 1],
+                             dk_out[src:src + 1], dv_out[src:src + 1])
+    torch.cuda.synchronize()
+    assert torch.equal(dq, dq_all) and torch.equal(dk_out, dk_all) and torch.equal(dv_out, dv_all)
+
+
+@pytest.mark.parametrize("case", RING_CASES, ids=ids)
+def test_ring_backward_steps_match_causal_gradients(case):
+    P, C, Hq, Hkv, Dh, lengths = case
+    arrs, seg, seg_t, (qs, ks, vs, dos) = ring_setup(case)
+    ring = up.Ring(up.make_ring_desc(P, C, Hq, Hkv, Dh), seg_t)
+    o, lse = ring.forward(qs, ks, vs)
+    n0 = up.launch_count()
+    dq, dk, dv = ring.backward(qs, ks, vs, o, lse, dos)
+    torch.cuda.synchronize()
+    assert up.launch_count() - n0 == 1 + 2 * P   # the D buffer, then dQ and dK/dV per step
+    assert up.device_status(ring.tables) == 0
+    dq1, dk1, dv1 = ring.backward(qs, ks, vs, o, lse, dos, per_step=True)
+    torch.cuda.synchronize()
+    assert torch.equal(dq1, dq) and torch.equal(dk1, dk) and torch.equal(dv1, dv)
+    Q, K, V, dO, _, _ = oracle_attention(arrs, seg, Dh)
+    dQ, dK, dV = orc.attention_backward(Q, K, V, dO, seg, True, orc.default_scale(Dh))
+    for got, want in ((dq, dQ), (dk, dK), (dv, dV)):
+        g = to_f64(up.from_zigzag(got, P))
+        assert rel_fro(g, want) <= GRAD_REL_FRO, rel_fro(g, want)
+
+
+def test_ring_step_32k_against_the_direct_kernel():
+    """The 32K-token chunk of 8 heads (Llama-3.1-8B shape, 2 KV heads) as a ring of 4: O and lse
+    agree with the direct causal kernel's to the rounding of the merge, on every row."""
+    P, S, Hq, Hkv, Dh = 4, 32768, 8, 2, 128
+    C = S // (2 * P)
+    dev = torch.device("cuda")
+
+    def fill(shape, tid):
+        t = torch.empty(shape, dtype=torch.bfloat16, device=dev)
+        ui.fill_device_bf16(t.data_ptr(), t.numel(), tid, 1.0)
+        return t
+
+    q, k, v = fill((Hq, S, Dh), 10), fill((Hkv, S, Dh), 11), fill((Hkv, S, Dh), 12)
+    desc = up.make_desc(S, 64, Hq, Hkv, Dh, Hq, True)
+    table = torch.empty(up.tile_table_bytes(desc), dtype=torch.uint8, device=dev)
+    up.build_tile_table(desc, None, table)
+    o_ref = torch.empty_like(q)
+    lse_ref = torch.empty(Hq, S, dtype=torch.float32, device=dev)
+    up.core_fwd(desc, q, k, v, None, table, o_ref, lse_ref)
+    ring = up.Ring(up.make_ring_desc(P, C, Hq, Hkv, Dh))
+    qs, ks, vs = (up.to_zigzag(x, P).contiguous() for x in (q, k, v))
+    o, lse = ring.forward(qs, ks, vs)
+    torch.cuda.synchronize()
+    assert up.device_status(ring.tables) == 0
+    o = up.from_zigzag(o, P)
+    lse = up.from_zigzag(lse, P)
+    assert (lse - lse_ref).abs().max().item() <= 1e-4
+    assert (o.float() - o_ref.float()).abs().max().item() <= 2e-2
+    assert rel_fro(to_f64(o), to_f64(o_ref)) <= 2e-3
 
 
 @pytest.mark.parametrize("S,H,Dh", [(1, 1, 64), (200, 3, 64), (1000, 4, 128)])

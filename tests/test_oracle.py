@@ -371,6 +371,66 @@ def test_zigzag_ring_blocks_reproduce_the_causal_backward():
     np.testing.assert_allclose(gv, dV, rtol=1e-10, atol=1e-11)
 
 
+def _packed(S, lengths):
+    return np.repeat(np.arange(len(lengths)), lengths)[:S] if lengths else None
+
+
+@pytest.mark.parametrize("P,C,lengths", [(1, 5, None), (2, 5, None), (3, 4, None), (4, 3, None),
+                                         (3, 4, [5, 1, 9, 9]), (4, 6, [20, 3, 1, 24])])
+def test_ring_steps_partition_the_causal_mask(P, C, lengths):
+    """Over its P steps, device r sees every (query, key) pair of the causal + segment mask on its
+    rows exactly once (the steps' key shards are disjoint and cover the sequence), and without
+    segments every device sees the same number of pairs (the zigzag balance)."""
+    S = 2 * P * C
+    seg = _packed(S, lengths)
+    full = orc.visibility(seg, np.arange(S), np.arange(S), True)
+    counts = []
+    for r in range(P):
+        qpos = orc.zigzag_positions(P, C, r)
+        got = np.zeros((2 * C, S), dtype=np.int64)
+        for s in range(P):
+            kpos = orc.zigzag_positions(P, C, (r - s) % P)
+            got[:, kpos] += orc.ring_step_visibility(P, C, r, s, seg)
+        np.testing.assert_array_equal(got, full[qpos].astype(np.int64))
+        counts.append(int(got.sum()))
+    assert sorted(np.concatenate([orc.zigzag_positions(P, C, r) for r in range(P)]).tolist()) == list(range(S))
+    if lengths is None:
+        assert len(set(counts)) == 1
+
+
+@pytest.mark.parametrize("P,C,lengths", [(3, 4, None), (4, 6, [20, 3, 1, 24]), (2, 7, [2, 2, 24])])
+@pytest.mark.parametrize("causal", [True, False])
+def test_ring_step_rows_and_columns_are_intervals(P, C, lengths, causal):
+    """In every ring step each query row sees one interval of the visiting shard's rows and each
+    key row is seen by one interval of queries, with both ends non-decreasing: the shape the tile
+    table and the kernels' per-row masks rely on."""
+    seg = _packed(2 * P * C, lengths)
+    for r in range(P):
+        for s in range(P):
+            vis = orc.ring_step_visibility(P, C, r, s, seg, causal)
+            for m in (vis, vis.T):
+                lo_prev, hi_prev = -1, -1
+                for row in m:
+                    nz = np.nonzero(row)[0]
+                    if nz.size == 0:
+                        continue
+                    assert nz.size == nz[-1] - nz[0] + 1
+                    assert nz[0] >= lo_prev and nz[-1] >= hi_prev
+                    lo_prev, hi_prev = nz[0], nz[-1]
+
+
+@pytest.mark.parametrize("C,lengths", [(64, None), (200, None), (150, [100, 1, 120, 79])])
+@pytest.mark.parametrize("causal", [True, False])
+def test_ring_step_table_of_a_one_device_ring_is_the_plain_table(C, lengths, causal):
+    """A ring of one device is the plain sequence: its step table equals the skip table of
+    2C rows computed from the row intervals."""
+    seg = _packed(2 * C, lengths)
+    q_rows, kv_rows = orc.ring_step_table(1, C, 0, 0, seg, causal)
+    want_q, want_kv, _ = orc.tile_table(2 * C, seg, causal)
+    np.testing.assert_array_equal(q_rows, want_q)
+    np.testing.assert_array_equal(kv_rows, want_kv)
+
+
 # ------------------------------------------------------------------------------------------
 # 6. tile-skip table
 # ------------------------------------------------------------------------------------------
