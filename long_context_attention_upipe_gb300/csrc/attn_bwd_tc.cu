@@ -358,11 +358,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dq_tc(const __grid_con
         tc::fence_before_sync();
         tc::mbar_arrive(&ds_full[t]);
       }
-      if (ok && has_keys) ok = tc::mbar_wait(&dq_full[t], 0, abort_flag, a.err, a.wait_ns);
-      tc::fence_after_sync();
-      if (b.dq_acc) grid_dep_wait();  // the previous ring step's sums are complete and visible
       bf16* dqrow = b.dq ? b.dq + ((int64_t)h * S + (row_ok ? row : 0)) * DH : nullptr;
       float* accrow = b.dq_acc ? b.dq_acc + ((int64_t)h * S + (row_ok ? row : 0)) * DH : nullptr;
+      // ring step: this row's running sum, loaded while the last dS K completes (all loads in
+      // flight at once)
+      float4 pa[DH / 4];
+      if (accrow) {
+        grid_dep_wait();  // the previous ring step's sums are complete and visible
+#pragma unroll
+        for (int i = 0; i < DH / 4; ++i) pa[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (ok && row_ok && has_keys && !a.acc_first) {
+#pragma unroll
+          for (int i = 0; i < DH / 4; ++i) pa[i] = reinterpret_cast<const float4*>(accrow)[i];
+        }
+      }
+      if (ok && has_keys) ok = tc::mbar_wait(&dq_full[t], 0, abort_flag, a.err, a.wait_ns);
+      tc::fence_after_sync();
 #pragma unroll
       for (int ch = 0; ch < DH / 32; ++ch) {
         uint32_t v[32];
@@ -376,8 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dq_tc(const __grid_con
           if (ok && row_ok && has_keys) {
 #pragma unroll
             for (int q4 = 0; q4 < 8; ++q4) {
-              float4 o4 = make_float4(0.f, 0.f, 0.f, 0.f);
-              if (!a.acc_first) o4 = *reinterpret_cast<const float4*>(accrow + ch * 32 + q4 * 4);
+              float4 o4 = pa[ch * 8 + q4];
               o4.x += __uint_as_float(v[q4 * 4 + 0]) * a.scale;
               o4.y += __uint_as_float(v[q4 * 4 + 1]) * a.scale;
               o4.z += __uint_as_float(v[q4 * 4 + 2]) * a.scale;
@@ -705,12 +715,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
     // after an abort, hand over the turns still owed so the other group never blocks on them
     for (int k = turn; k < n_give; ++k) tc::named_bar_arrive(kPing + 1 - grp, 256);
     // epilogue: group 0 writes dK rows (scaled), group 1 writes dV rows
-    if (ok && n_items > 0) ok = tc::mbar_wait(acc_full, 0, abort_flag, a.err, a.wait_ns);
-    tc::fence_after_sync();
-    if (a.ring.P) grid_dep_wait();  // the previous ring step's sums are complete and visible
     const uint32_t acc_addr = lane_addr + (grp == 0 ? L::DK_COL : L::DV_COL);
     const float mul = grp == 0 ? a.scale : 1.f;
     const int64_t off = ((int64_t)kvh * S + (k_ok ? krow : 0)) * DH;
+    // fp32 sums: this row's running sum, loaded while the last MMAs complete (all loads in flight
+    // at once)
+    float4 pa[DH / 4];
+    if (b.acc_kv) {
+      if (a.ring.P) grid_dep_wait();  // the previous ring step's sums are complete and visible
+#pragma unroll
+      for (int i = 0; i < DH / 4; ++i) pa[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (ok && k_ok && !a.acc_first) {
+        const float4* src = reinterpret_cast<const float4*>((grp == 0 ? b.dk_acc : b.dv_acc) + off);
+#pragma unroll
+        for (int i = 0; i < DH / 4; ++i) pa[i] = src[i];
+      }
+    }
+    if (ok && n_items > 0) ok = tc::mbar_wait(acc_full, 0, abort_flag, a.err, a.wait_ns);
+    tc::fence_after_sync();
 #pragma unroll
     for (int ch = 0; ch < DH / 32; ++ch) {
       uint32_t v[32];
@@ -729,8 +751,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
           if (out) out += off + ch * 32;
 #pragma unroll
           for (int q4 = 0; q4 < 8; ++q4) {
-            float4 o4 = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (!a.acc_first) o4 = *reinterpret_cast<float4*>(dst + q4 * 4);
+            float4 o4 = pa[ch * 8 + q4];
             o4.x += __uint_as_float(v[q4 * 4 + 0]) * mul;
             o4.y += __uint_as_float(v[q4 * 4 + 1]) * mul;
             o4.z += __uint_as_float(v[q4 * 4 + 2]) * mul;

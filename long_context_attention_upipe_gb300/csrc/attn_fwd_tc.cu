@@ -338,19 +338,30 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       // after an abort, hand over the turns still owed so the other group never blocks on them
       for (int k = turn; k < n_give; ++k) tc::named_bar_arrive(kPing + 1 - t, 256);
+      // ring step: the running output of this row, loaded while the last P V completes (all
+      // loads in flight at once: one memory latency, not one per vector)
+      float4 pa[MODE == 2 ? DH / 4 : 1];
+      float la2 = -INFINITY;
+      if constexpr (MODE == 2) {
+        grid_dep_wait();  // the previous step's accumulators are complete and visible
+        if (ok && row_ok && has_keys && !a.acc_first) {
+          const float4* src = reinterpret_cast<const float4*>(a.o_acc + ((int64_t)h * S + row) * DH);
+          la2 = a.lse[(int64_t)h * S + row] * kLog2e;
+#pragma unroll
+          for (int i = 0; i < DH / 4; ++i) pa[i] = src[i];
+        }
+      }
       if (ok && has_keys) ok = tc::mbar_wait(&o_full[t], 0, abort_flag, a.err, a.wait_ns);
       tc::fence_after_sync();
       // epilogue: O / l -> bf16 row; lse or D
       const float inv = (MODE != 1) ? (l > 0.f ? 1.f / l : 0.f) : 1.f;
       if constexpr (MODE == 2) {
-        grid_dep_wait();  // the previous step's accumulators are complete and visible
         // fold the block into the running (O_acc, lse): weights of the two sides in exp2 units
         const float lb2 = l > 0.f ? m_used + log2f(l) : -INFINITY;
-        const float la2 = (!a.acc_first && row_ok) ? a.lse[(int64_t)h * S + row] * kLog2e : -INFINITY;
         const float mx = fmaxf(la2, lb2);
         float wa = 0.f, wb = 0.f, lnew = -INFINITY;
         if (mx != -INFINITY) {
-          wa = exp2f(la2 - mx);  // 0 when la2 = -inf
+          wa = exp2f(la2 - mx);  // 0 when la2 = -inf (first step)
           wb = exp2f(lb2 - mx);
           const float sum = wa + wb;
           lnew = (mx + log2f(sum)) * kLn2;
@@ -370,7 +381,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
             for (int q4 = 0; q4 < 8; ++q4) {
               float4 o4 = make_float4(0.f, 0.f, 0.f, 0.f);
               if (wa != 0.f) {  // a side with weight 0 contributes nothing, whatever it holds
-                const float4 p4 = *reinterpret_cast<const float4*>(arow + ch * 32 + q4 * 4);
+                const float4 p4 = pa[ch * 8 + q4];
                 o4 = make_float4(wa * p4.x, wa * p4.y, wa * p4.z, wa * p4.w);
               }
               if (wb != 0.f) {
