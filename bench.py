@@ -48,7 +48,9 @@ def parse():
     ap.add_argument("--no-offload", action="store_true", help="skip the leg with X and dY in pinned host memory")
     ap.add_argument("--no-mlp", action="store_true", help="skip the sequence-tiled MLP leg")
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--sample-tokens", type=int, default=1024, help="oracle sample length (CPU legs)")
+    ap.add_argument("--sample-tokens", type=int, default=16384,
+                    help="oracle sample length (CPU legs): the first tokens of the workload as one sequence, about "
+                         "10 s of fp64 work on 16 cores")
     ap.add_argument("--kernel", default=None, choices=["fwd", "recompute", "dq", "dkdv", "lse_merge", "ring", "ring_bwd"],
                     help="time one attention kernel alone at the workload's chunk shapes (for profilers); "
                          "lse_merge: the ring merge of one block into fp32 accumulators; ring: the chunk's causal "
