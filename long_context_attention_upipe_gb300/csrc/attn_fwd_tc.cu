@@ -21,8 +21,11 @@
 //              overlaps the tensor core's work on the other tile.
 // TMEM columns: S/P_a [0,128) S/P_b [128,256) O_a [256,256+Dh) O_b [256+Dh, 256+2Dh).
 // While one softmax group works, the tensor core runs the other tile's P V and next Q K^T.
-// The running max is rescaled lazily: O is corrected only when the row max grows by more than
-// 2^8 (in exp2 units), which keeps every P <= 256 and the final O / l exact in fp32.
+// The softmax offset is optimistic: the first tile with a visible key sets it to that tile's row
+// maximum and later tiles reuse it without computing their maximum; only when a tile's row sum of P
+// exceeds 2^16 (a score outgrew the offset by 16 in exp2 units) is the offset moved to the true
+// maximum, O and l rescaled and the tile's P redone.  Every P stays <= 2^16, so O and l stay far from
+// fp32 overflow, and O / l does not depend on the offset.
 //
 // MODE 1 (activation recompute for the backward pass): P = exp2(S*scale*log2e - lse*log2e)
 // from the saved log-sum-exp, no rescaling; the epilogue also writes D = rowsum(dO * O).
@@ -279,40 +282,60 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           for (int k = 0; k < 128; ++k)
             if (k < lo || k > hi) sv[k] = 0xff800000u;  // -inf
         }
-        float mu;
         float f = 1.f;
         bool rescale_o = false;
-        if (MODE != 1) {
+        // row maximum of the tile's (masked) scores, in exp2 units
+        auto row_max = [&]() {
           float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
           for (int k = 0; k < 128; k += 2)
             m4[(k >> 1) & 3] = fmax3(m4[(k >> 1) & 3], __uint_as_float(sv[k]), __uint_as_float(sv[k + 1]));
-          const float mx = fmaxf(m_used, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * c);
-          const bool need = mx > m_used + 8.f;
-          rescale_o = need && cnt > 0 && m_used != -INFINITY;
-          if (rescale_o) f = fast_exp2(m_used - mx);
-          if (need) m_used = mx;
-          mu = m_used == -INFINITY ? 0.f : m_used;
-        } else {
-          mu = m_used;
-        }
+          return fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * c;
+        };
+        // The offset only has to keep P in range: O / l is the same for any offset.  The first
+        // tile with a visible key sets it to that tile's maximum; later tiles reuse it and their
+        // P's row sum tells whether a score outgrew it (below).
+        if (MODE != 1 && m_used == -INFINITY) m_used = row_max();  // stays -inf if all masked
+        float mu = m_used == -INFINITY ? 0.f : m_used;
         // P = exp2(s * c - mu) as bf16 pairs into the first 64 columns of S (already read)
-        float2 l2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-        const float2 cc = make_float2(c, c), nmu = make_float2(-mu, -mu);
+        float lt;
+        auto exp_store = [&]() {
+          float2 l2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+          const float2 cc = make_float2(c, c), nmu = make_float2(-mu, -mu);
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          uint32_t pk[32];
+          for (int hf = 0; hf < 2; ++hf) {
+            uint32_t pk[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float2 arg = __ffma2_rn(
-                make_float2(__uint_as_float(sv[hf * 64 + 2 * i]), __uint_as_float(sv[hf * 64 + 2 * i + 1])), cc, nmu);
-            const float2 p = make_float2(fast_exp2(arg.x), fast_exp2(arg.y));
-            l2[i & 1] = __fadd2_rn(l2[i & 1], p);
-            pk[i] = tc::pack_bf16x2(p.x, p.y);
+            for (int i = 0; i < 32; ++i) {
+              const float2 arg = __ffma2_rn(
+                  make_float2(__uint_as_float(sv[hf * 64 + 2 * i]), __uint_as_float(sv[hf * 64 + 2 * i + 1])), cc, nmu);
+              const float2 p = make_float2(fast_exp2(arg.x), fast_exp2(arg.y));
+              l2[i & 1] = __fadd2_rn(l2[i & 1], p);
+              pk[i] = tc::pack_bf16x2(p.x, p.y);
+            }
+            tc::tmem_st32(s_addr + hf * 32, pk);
           }
-          tc::tmem_st32(s_addr + hf * 32, pk);
+          lt = (l2[0].x + l2[0].y) + (l2[1].x + l2[1].y);
+        };
+        exp_store();
+        if (MODE != 1) {
+          // A row sum above 2^16 (or inf) means some P exceeded 2^16: move the offset to the true
+          // maximum, rescale the running O and l, and redo the tile's P (rare: the scores have to
+          // outgrow the first visible tile's maximum by 16 in exp2 units).  P <= 2^16 keeps O and
+          // l far from fp32 overflow, and bf16 P has the same relative precision at any size.
+          const bool redo = !(lt <= 65536.f);
+          if (__any_sync(0xffffffffu, redo)) {  // warp-uniform: the TMEM stores are collective
+            if (redo) {
+              const float mx = fmaxf(m_used, row_max());
+              rescale_o = cnt > 0;
+              f = fast_exp2(m_used - mx);
+              m_used = mx;
+              mu = mx;
+            }
+            tc::tmem_st_wait();
+            exp_store();
+          }
         }
-        const float l4[4] = {l2[0].x, l2[0].y, l2[1].x, l2[1].y};
         tc::tmem_st_wait();
         if (MODE != 1 && __any_sync(0xffffffffu, rescale_o)) {
           // O_t is idle here: P V of the previous tile completed before this S was ready, and
@@ -328,7 +351,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           }
           tc::tmem_st_wait();
         }
-        l = l * f + ((l4[0] + l4[1]) + (l4[2] + l4[3]));
+        l = l * f + lt;
         tc::fence_before_sync();
         tc::mbar_arrive(&p_full[t]);
         if (pp) {
