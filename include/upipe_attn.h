@@ -337,11 +337,12 @@ upipe_status_t upipe_attn_ring_build_tables(const upipe_ring_desc_t* desc, const
 /* Forward of ring step `step` (0 .. P-1, called in order on the same accumulators): one
  * attention launch over all batched devices.
  *   o_acc  device fp32 [dev_count][n_q_heads][2C][head_dim]: running output (step 0 writes it,
- *          later steps fold into it; the last step leaves it untouched)
+ *          later steps fold into it)
  *   lse    device fp32 [dev_count][n_q_heads][2C]: running log-sum-exp (natural log), final
  *          after the last step
- *   o      NULL, or device bf16 like q: each step writes the merged output of the rows it
- *          changes, so after the last step o holds the result
+ *   o      NULL, or device bf16 like q: the result.  A 128-row tile's rows are written by the
+ *          last step that changes them (the steps' tables say which), and that step does not
+ *          store them to o_acc; with o NULL, o_acc holds the result after the last step.
  * Query tiles that see no key of the visiting shard are not touched. */
 upipe_status_t upipe_attn_ring_fwd_step(const upipe_ring_desc_t* desc, int32_t step, const uint16_t* q,
                                         const uint16_t* k, const uint16_t* v, const int32_t* seg, void* tables,
@@ -354,9 +355,13 @@ upipe_status_t upipe_attn_ring_fwd_step(const upipe_ring_desc_t* desc, int32_t s
  *   dk_acc, dv_acc  device fp32 [kv_count][n_kv_heads][2C][head_dim]: dK, dV of the key shards,
  *                   indexed like k and v, summed over the steps and the query heads of each KV
  *                   head (on a real ring they travel with their shard)
- *   dq, dk, dv      NULL, or device bf16 like q / k / v: the running sums rounded, written for
- *                   the rows a step changes (the last step leaves the fp32 sums untouched)
- * Rows that no query of a step sees are not touched by that step. */
+ *   dq, dk, dv      NULL, or device bf16 like q / k / v: the sums rounded.  dq's rows are
+ *                   written by the last step that changes their tile, which then does not store
+ *                   dq_acc; likewise dk / dv when one call batches every device with every
+ *                   shard (dev_count = kv_count = P), else every step writes the rows it changes
+ *                   and the ring's last step does not store dk_acc / dv_acc.  With a NULL bf16
+ *                   output the fp32 sums hold the result after the last step.
+ * Tiles that no query of a step sees are not touched by that step. */
 upipe_status_t upipe_attn_ring_bwd_step(const upipe_ring_desc_t* desc, int32_t step, const uint16_t* q,
                                         const uint16_t* k, const uint16_t* v, const uint16_t* dO, const float* D,
                                         const int32_t* seg, void* tables, float* dq_acc, float* dk_acc,

@@ -1237,6 +1237,9 @@ static AttnArgs ring_args(const upipe_ring_desc_t* d, int step, const uint16_t* 
   a.ring = ring_geom(d, step);
   a.acc_first = step == 0;
   a.acc_last = step == d->ring_size - 1;
+  a.ring_tables = reinterpret_cast<const char*>(tables);
+  a.ring_table_stride = per;
+  a.kv_last_touch = d->dev_count == d->ring_size && d->kv_count == d->ring_size;
   return a;
 }
 

@@ -358,8 +358,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dq_tc(const __grid_con
         tc::fence_before_sync();
         tc::mbar_arrive(&ds_full[t]);
       }
-      bf16* dqrow = b.dq ? b.dq + ((int64_t)h * S + (row_ok ? row : 0)) * DH : nullptr;
       float* accrow = b.dq_acc ? b.dq_acc + ((int64_t)h * S + (row_ok ? row : 0)) * DH : nullptr;
+      // ring step: only the last step that touches this tile writes its bf16 result, and that
+      // step skips the fp32 store
+      const bool last = accrow && b.dq && !q_tile_touched_later(a, dev, t ? qt1 : qt0, nt);
+      bf16* dqrow = (b.dq && (!accrow || last)) ? b.dq + ((int64_t)h * S + (row_ok ? row : 0)) * DH : nullptr;
       // ring step: this row's running sum, loaded while the last dS K completes (all loads in
       // flight at once)
       float4 pa[DH / 4];
@@ -392,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dq_tc(const __grid_con
               o4.y += __uint_as_float(v[q4 * 4 + 1]) * a.scale;
               o4.z += __uint_as_float(v[q4 * 4 + 2]) * a.scale;
               o4.w += __uint_as_float(v[q4 * 4 + 3]) * a.scale;
-              if (!a.acc_last) *reinterpret_cast<float4*>(accrow + ch * 32 + q4 * 4) = o4;
+              if (!last) *reinterpret_cast<float4*>(accrow + ch * 32 + q4 * 4) = o4;
               if (dqrow)
                 *reinterpret_cast<uint2*>(dqrow + ch * 32 + q4 * 4) =
                     make_uint2(tc::pack_bf16x2(o4.x, o4.y), tc::pack_bf16x2(o4.z, o4.w));
@@ -714,7 +717,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
     }
     // after an abort, hand over the turns still owed so the other group never blocks on them
     for (int k = turn; k < n_give; ++k) tc::named_bar_arrive(kPing + 1 - grp, 256);
-    // epilogue: group 0 writes dK rows (scaled), group 1 writes dV rows
+    // epilogue: group 0 writes dK rows (scaled), group 1 writes dV rows.  Ring steps: the fp32 sum
+    // is not stored by the last step that touches the key tile (with the shards the launch's own
+    // at every step; otherwise by the ring's last step) and only that step writes the bf16 result.
+    const bool last = a.ring.P && b.dk_out && b.dv_out &&
+                      (a.kv_last_touch ? !kv_tile_touched_later(a, shard, jt, nt) : a.acc_last != 0);
     const uint32_t acc_addr = lane_addr + (grp == 0 ? L::DK_COL : L::DV_COL);
     const float mul = grp == 0 ? a.scale : 1.f;
     const int64_t off = ((int64_t)kvh * S + (k_ok ? krow : 0)) * DH;
@@ -748,6 +755,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
           // leaves the running sum rounded to bf16 if asked
           float* dst = (grp == 0 ? b.dk_acc : b.dv_acc) + off + ch * 32;
           bf16* out = grp == 0 ? b.dk_out : b.dv_out;
+          if (out && !(last || !a.kv_last_touch)) out = nullptr;  // written by a later step
           if (out) out += off + ch * 32;
 #pragma unroll
           for (int q4 = 0; q4 < 8; ++q4) {
@@ -756,7 +764,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
             o4.y += __uint_as_float(v[q4 * 4 + 1]) * mul;
             o4.z += __uint_as_float(v[q4 * 4 + 2]) * mul;
             o4.w += __uint_as_float(v[q4 * 4 + 3]) * mul;
-            if (!a.acc_last) *reinterpret_cast<float4*>(dst + q4 * 4) = o4;
+            if (!last) *reinterpret_cast<float4*>(dst + q4 * 4) = o4;
             if (out)
               *reinterpret_cast<uint2*>(out + q4 * 4) = make_uint2(tc::pack_bf16x2(o4.x, o4.y), tc::pack_bf16x2(o4.z, o4.w));
           }

@@ -392,8 +392,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           wb = wb / sum * inv;
         }
         const bool act = ok && row_ok && has_keys;
+        // the last step that touches this tile writes its bf16 result and no fp32 state (without a
+        // bf16 output, the fp32 state is the result and always stored)
+        const bool last = a.o && !q_tile_touched_later(a, dev, t ? qt1 : qt0, nt);
         float* arow = a.o_acc + ((int64_t)h * S + (row_ok ? row : 0)) * DH;
-        bf16* orow = a.o ? a.o + ((int64_t)h * S + (row_ok ? row : 0)) * DH : nullptr;
+        bf16* orow = last ? a.o + ((int64_t)h * S + (row_ok ? row : 0)) * DH : nullptr;
 #pragma unroll
         for (int ch = 0; ch < DH / 32; ++ch) {
           uint32_t v[32];
@@ -413,7 +416,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                 o4.z += wb * __uint_as_float(v[q4 * 4 + 2]);
                 o4.w += wb * __uint_as_float(v[q4 * 4 + 3]);
               }
-              if (!a.acc_last) *reinterpret_cast<float4*>(arow + ch * 32 + q4 * 4) = o4;
+              if (!last) *reinterpret_cast<float4*>(arow + ch * 32 + q4 * 4) = o4;
               if (orow)
                 *reinterpret_cast<uint2*>(orow + ch * 32 + q4 * 4) =
                     make_uint2(tc::pack_bf16x2(o4.x, o4.y), tc::pack_bf16x2(o4.z, o4.w));

@@ -120,4 +120,23 @@ __device__ __forceinline__ int dev_of_shard(const RingGeom& g, int m) {
   return g.P ? ring_mod(g.kv0 + m + g.step - g.r0, g.P) : 0;
 }
 
+// Does a later step of the ring touch query tile qt of batch device d (non-empty table row)?
+__device__ __forceinline__ bool q_tile_touched_later(const AttnArgs& a, int d, int qt, int nt) {
+  for (int s2 = a.ring.step + 1; s2 < a.ring.P; ++s2) {
+    const int4 r = reinterpret_cast<const int4*>(a.ring_tables + s2 * a.ring_table_stride +
+                                                 sizeof(TableHeader))[(int64_t)d * nt + qt];
+    if (r.x < r.w) return true;
+  }
+  return false;
+}
+// ... key tile jt of key shard m (valid when the shards are the launch's own at every step)
+__device__ __forceinline__ bool kv_tile_touched_later(const AttnArgs& a, int m, int jt, int nt) {
+  for (int s2 = a.ring.step + 1; s2 < a.ring.P; ++s2) {
+    const int4 r = reinterpret_cast<const int4*>(a.ring_tables + s2 * a.ring_table_stride + sizeof(TableHeader) +
+                                                 (size_t)a.ndev * nt * sizeof(int4))[(int64_t)m * nt + jt];
+    if (r.x < r.w) return true;
+  }
+  return false;
+}
+
 }  // namespace upipe

@@ -145,6 +145,13 @@ struct AttnArgs {
                     // o (if not NULL) receives the merged output rounded to bf16
   int pdl;          // launch with programmatic stream serialisation: the previous kernel on the
                     // stream is the previous ring step of the same call (see grid_dep_wait)
+  // Ring steps: every step's table (step s at ring_tables + s * ring_table_stride), so that a tile
+  // knows whether a later step touches it again; only the step that touches a row last writes its
+  // bf16 result and that step skips the fp32 store.  kv_last_touch: the same holds for the key
+  // shards' dK / dV sums (they are the launch's own shards at every step: all devices batched).
+  const char* ring_tables;
+  size_t ring_table_stride;
+  int kv_last_touch;
 };
 
 // Launch with programmatic stream serialisation allowed (the grid may start while the previous

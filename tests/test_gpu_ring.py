@@ -149,9 +149,6 @@ def test_ring_forward_steps_match_attention_over_the_sequence(case):
     assert max_abs_bf16_out(got, O_ref) <= OUT_MAX_ABS, max_abs_bf16_out(got, O_ref)
     assert rel_fro(got, O_ref) <= OUT_REL_FRO, rel_fro(got, O_ref)
     assert max_abs(to_f64(up.from_zigzag(lse, P)), L_ref) <= 1e-3
-    if P > 1:   # the last step leaves the fp32 state of the earlier steps; o is its rounding
-        partial = to_f64(o_acc)
-        assert np.isfinite(partial).all()
 
 
 @pytest.mark.parametrize("case", RING_CASES[1:5], ids=ids)
