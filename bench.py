@@ -48,7 +48,7 @@ def parse():
     ap.add_argument("--no-offload", action="store_true", help="skip the leg with X and dY in pinned host memory")
     ap.add_argument("--no-mlp", action="store_true", help="skip the sequence-tiled MLP leg")
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--sample-tokens", type=int, default=16384,
+    ap.add_argument("--sample-tokens", type=int, default=8192,
                     help="oracle sample length (CPU legs): the first tokens of the workload as one sequence, about "
                          "10 s of fp64 work on 16 cores")
     ap.add_argument("--kernel", default=None, choices=["fwd", "recompute", "dq", "dkdv", "lse_merge", "ring", "ring_bwd"],
