@@ -276,3 +276,57 @@ def test_accumulate_sums_in_fp32_and_rounds_once(n):
     want = acc0 + ui.bf16_to_f64(src).astype(np.float32)   # one fp32 addition per element
     np.testing.assert_array_equal(acc.cpu().numpy(), want)
     assert torch.equal(out.view(torch.int16), acc.to(torch.bfloat16).view(torch.int16))
+
+
+@pytest.mark.parametrize("lengths", [None, [150, 10, 440]])
+def test_non_causal_ring_matches_full_attention(lengths):
+    """causal = 0: every key of the segment, wherever it sits in the ring (forward and backward)."""
+    case = (3, 100, 2, 1, 64, lengths)
+    P, C, Hq, Hkv, Dh, _ = case
+    arrs, seg, seg_t, (qs, ks, vs, dos) = ring_setup(case)
+    ring = up.Ring(up.make_ring_desc(P, C, Hq, Hkv, Dh, causal=False), seg_t)
+    o, lse = ring.forward(qs, ks, vs)
+    dq, dk, dv = ring.backward(qs, ks, vs, o, lse, dos)
+    torch.cuda.synchronize()
+    assert up.device_status(ring.tables) == 0
+    Q, K, V, dO, O_ref, L_ref = oracle_attention(arrs, seg, Dh, causal=False)
+    got = to_f64(up.from_zigzag(o, P))
+    assert max_abs_bf16_out(got, O_ref) <= OUT_MAX_ABS and rel_fro(got, O_ref) <= OUT_REL_FRO
+    assert max_abs(to_f64(up.from_zigzag(lse, P)), L_ref) <= 1e-3
+    dQ, dK, dV = orc.attention_backward(Q, K, V, dO, seg, False, orc.default_scale(Dh))
+    for g_, want in ((dq, dQ), (dk, dK), (dv, dV)):
+        assert rel_fro(to_f64(up.from_zigzag(g_, P)), want) <= GRAD_REL_FRO
+
+
+def test_a_partial_batch_of_devices_matches_the_full_batch():
+    """Devices 1 and 2 of a ring of 4 in one call (their query shards, every key shard in device
+    order): their outputs and dQ equal the full batch's bit for bit."""
+    case = (4, 128, 4, 2, 128, [300, 1, 723])
+    P, C, Hq, Hkv, Dh, _ = case
+    _, seg, seg_t, (qs, ks, vs, dos) = ring_setup(case)
+    full = up.Ring(up.make_ring_desc(P, C, Hq, Hkv, Dh), seg_t)
+    o_all, lse_all = full.forward(qs, ks, vs)
+    dq_all, _, _ = full.backward(qs, ks, vs, o_all, lse_all, dos)
+    part = up.Ring(up.make_ring_desc(P, C, Hq, Hkv, Dh, dev_first=1, dev_count=2), seg_t)
+    q2, do2 = qs[1:3].contiguous(), dos[1:3].contiguous()
+    o2, lse2 = part.forward(q2, ks, vs)
+    dq2, _, _ = part.backward(q2, ks, vs, o2, lse2, do2)
+    torch.cuda.synchronize()
+    assert up.device_status(part.tables) == 0
+    assert torch.equal(o2, o_all[1:3]) and torch.equal(lse2, lse_all[1:3]) and torch.equal(dq2, dq_all[1:3])
+
+
+def test_eight_device_ring_with_ragged_chunks():
+    case = (8, 72, 2, 1, 64, None)
+    P, C, Hq, Hkv, Dh, _ = case
+    arrs, seg, seg_t, (qs, ks, vs, dos) = ring_setup(case)
+    ring = up.Ring(up.make_ring_desc(P, C, Hq, Hkv, Dh), seg_t)
+    o, lse = ring.forward(qs, ks, vs)
+    dq, dk, dv = ring.backward(qs, ks, vs, o, lse, dos)
+    torch.cuda.synchronize()
+    Q, K, V, dO, O_ref, L_ref = oracle_attention(arrs, seg, Dh)
+    got = to_f64(up.from_zigzag(o, P))
+    assert max_abs_bf16_out(got, O_ref) <= OUT_MAX_ABS and rel_fro(got, O_ref) <= OUT_REL_FRO
+    dQ, dK, dV = orc.attention_backward(Q, K, V, dO, seg, True, orc.default_scale(Dh))
+    for g_, want in ((dq, dQ), (dk, dK), (dv, dV)):
+        assert rel_fro(to_f64(up.from_zigzag(g_, P)), want) <= GRAD_REL_FRO
