@@ -197,6 +197,51 @@ def test_core_fwd_bwd_match_oracle(case):
     assert rel_fro(dv, dV) <= GRAD_REL_FRO, rel_fro(dv, dV)
 
 
+def grow_keys(k, S, every=384):
+    """K with its magnitude doubled every `every` positions (an exact bf16 exponent shift), so the
+    scores of late key tiles outgrow those of the first tile by far more than 2^16 in exp2 units."""
+    e = (np.arange(S) // every).astype(np.uint16)
+    bits = k.astype(np.uint16)
+    grown = bits + (e[None, :, None] << 7).astype(np.uint16)
+    return np.where((bits & 0x7F80) != 0, grown, bits).astype(np.uint16)
+
+
+@pytest.mark.parametrize("segs", [None, [700, 1348]])
+def test_forward_offset_moves_when_scores_outgrow_it(segs):
+    """The forward's optimistic softmax offset: keys whose magnitude doubles every 384 positions
+    make later tiles' scores exceed the first visible tile's maximum by more than 2^16, so the
+    forward has to move the offset, rescale O and l and redo the tile's P; results at the bar."""
+    S, Hq, Hkv, Dh = 2048, 2, 1, 128
+    q, k, v, do = qkv_inputs(S, Hq, Hkv, Dh)
+    k = grow_keys(k, S)
+    seg = ui.segments_from_lengths(segs) if segs else None
+    seg_t = torch.from_numpy(seg).cuda() if seg is not None else None
+    desc = up.make_desc(S, 64, Hq, Hkv, Dh, Hq, True)
+    table = torch.empty(up.tile_table_bytes(desc), dtype=torch.uint8, device="cuda")
+    up.build_tile_table(desc, seg_t, table)
+    qt, kt, vt, dot = (bf16_tensor(x) for x in (q, k, v, do))
+    o = torch.empty_like(qt)
+    lse = torch.empty(Hq, S, dtype=torch.float32, device="cuda")
+    up.core_fwd(desc, qt, kt, vt, seg_t, table, o, lse)
+    dq, dk, dv = torch.empty_like(qt), torch.empty_like(kt), torch.empty_like(vt)
+    up.core_bwd(desc, qt, kt, vt, dot, lse, seg_t, table, dq, dk, dv)
+    torch.cuda.synchronize()
+    assert up.device_status(table) == 0
+    Q, K, V, dO = (ui.bf16_to_f64(x) for x in (q, k, v, do))
+    scale = orc.default_scale(Dh)
+    O_ref, L_ref = orc.attention_forward(Q, K, V, seg, True, scale)
+    if seg is None:  # the scores really do outgrow the first tile's maximum by more than 16 in exp2 units
+        s0 = (Q[:, 1500] @ K[0, :128].T).max(axis=-1) * scale * np.log2(np.e)
+        assert np.all(L_ref[:, 1500] * np.log2(np.e) - s0 > 16)
+    assert max_abs_bf16_out(to_f64(o), O_ref) <= OUT_MAX_ABS
+    assert rel_fro(to_f64(o), O_ref) <= OUT_REL_FRO
+    assert max_abs(to_f64(lse), L_ref) <= 1e-3 * max(1.0, np.abs(L_ref).max())
+    dQ, dK, dV = orc.attention_backward(Q, K, V, dO, seg, True, scale)
+    assert rel_fro(to_f64(dq), dQ) <= GRAD_REL_FRO
+    assert rel_fro(to_f64(dk), dK) <= GRAD_REL_FRO
+    assert rel_fro(to_f64(dv), dV) <= GRAD_REL_FRO
+
+
 # ----------------------------------------------------------------------------------------------
 # the whole layer, chunked
 # ----------------------------------------------------------------------------------------------

@@ -330,3 +330,26 @@ def test_eight_device_ring_with_ragged_chunks():
     dQ, dK, dV = orc.attention_backward(Q, K, V, dO, seg, True, orc.default_scale(Dh))
     for g_, want in ((dq, dQ), (dk, dK), (dv, dV)):
         assert rel_fro(to_f64(up.from_zigzag(g_, P)), want) <= GRAD_REL_FRO
+
+
+def test_ring_forward_with_scores_that_outgrow_the_offset():
+    """Keys whose magnitude doubles every 384 positions: the ring steps' forward must move its
+    softmax offset inside a block (as the direct kernel does) and still match the oracle."""
+    from test_gpu_parity import grow_keys
+    P, C, Hq, Hkv, Dh = 2, 512, 2, 1, 128
+    S = 2 * P * C
+    q, k, v, do = qkv_inputs(S, Hq, Hkv, Dh)
+    k = grow_keys(k, S)
+    qs, ks, vs, dos = (up.to_zigzag(bf16_tensor(x), P).contiguous() for x in (q, k, v, do))
+    ring = up.Ring(up.make_ring_desc(P, C, Hq, Hkv, Dh))
+    o, lse = ring.forward(qs, ks, vs)
+    dq, dk, dv = ring.backward(qs, ks, vs, o, lse, dos)
+    torch.cuda.synchronize()
+    assert up.device_status(ring.tables) == 0
+    Q, K, V, dO, O_ref, L_ref = oracle_attention((q, k, v, do), None, Dh)
+    got = to_f64(up.from_zigzag(o, P))
+    assert max_abs_bf16_out(got, O_ref) <= OUT_MAX_ABS and rel_fro(got, O_ref) <= OUT_REL_FRO
+    assert max_abs(to_f64(up.from_zigzag(lse, P)), L_ref) <= 1e-3 * max(1.0, np.abs(L_ref).max())
+    dQ, dK, dV = orc.attention_backward(Q, K, V, dO, None, True, orc.default_scale(Dh))
+    for g_, want in ((dq, dQ), (dk, dK), (dv, dV)):
+        assert rel_fro(to_f64(up.from_zigzag(g_, P)), want) <= GRAD_REL_FRO
