@@ -358,9 +358,10 @@ upipe_status_t upipe_attn_ring_fwd_step(const upipe_ring_desc_t* desc, int32_t s
  *   dq, dk, dv      NULL, or device bf16 like q / k / v: the sums rounded.  dq's rows are
  *                   written by the last step that changes their tile, which then does not store
  *                   dq_acc; likewise dk / dv when one call batches every device with every
- *                   shard (dev_count = kv_count = P), else every step writes the rows it changes
- *                   and the ring's last step does not store dk_acc / dv_acc.  With a NULL bf16
- *                   output the fp32 sums hold the result after the last step.
+ *                   shard (dev_count = kv_count = P), else every step writes the key tiles it
+ *                   changes (so dk / dv travel with their shard like dk_acc / dv_acc) and the
+ *                   ring's last step does not store dk_acc / dv_acc.  With a NULL bf16 output the
+ *                   fp32 sums hold the result after the last step.
  * Tiles that no query of a step sees are not touched by that step. */
 upipe_status_t upipe_attn_ring_bwd_step(const upipe_ring_desc_t* desc, int32_t step, const uint16_t* q,
                                         const uint16_t* k, const uint16_t* v, const uint16_t* dO, const float* D,

@@ -353,3 +353,62 @@ def test_ring_forward_with_scores_that_outgrow_the_offset():
     dQ, dK, dV = orc.attention_backward(Q, K, V, dO, None, True, orc.default_scale(Dh))
     for g_, want in ((dq, dQ), (dk, dK), (dv, dV)):
         assert rel_fro(to_f64(up.from_zigzag(g_, P)), want) <= GRAD_REL_FRO
+
+
+def test_two_devices_per_call_with_their_visiting_shards():
+    """dev_count = kv_count = 2 of a ring of 4: each step call gets the two visiting shards in
+    batch order (what two devices of a real ring would hold); forward, lse and dQ equal the full
+    batch's bit for bit, and the dK/dV sums travel with their shards."""
+    case = (4, 128, 4, 2, 128, [300, 1, 723])
+    P, C, Hq, Hkv, Dh, _ = case
+    _, seg, seg_t, (qs, ks, vs, dos) = ring_setup(case)
+    full = up.Ring(up.make_ring_desc(P, C, Hq, Hkv, Dh), seg_t)
+    o_all, lse_all = full.forward(qs, ks, vs)
+    dq_all, dk_all, dv_all = full.backward(qs, ks, vs, o_all, lse_all, dos)
+    sp = -(-2 * C // 128) * 128
+    pair = [(0, 2), (2, 2)]        # (first device, count): two calls per step cover the ring
+    outs = {}
+    descs = {}
+    for r0, n in pair:
+        d2 = up.make_ring_desc(P, C, Hq, Hkv, Dh, dev_first=r0, dev_count=n, kv_count=n)
+        t2 = torch.empty(up.ring_tables_bytes(d2), dtype=torch.uint8, device="cuda")
+        up.ring_build_tables(d2, seg_t, t2)
+        descs[r0] = (d2, t2)
+        outs[r0] = (torch.empty((n,) + tuple(qs.shape[1:]), dtype=torch.float32, device="cuda"),
+                    torch.empty((n,) + tuple(qs.shape[1:3]), dtype=torch.float32, device="cuda"),
+                    torch.empty_like(qs[r0:r0 + n]))
+    visit = lambda s, r0, n, x: torch.stack([x[(r0 + d - s) % P] for d in range(n)]).contiguous()
+    for s in range(P):
+        for r0, n in pair:
+            d2, t2 = descs[r0]
+            o_acc, lse, o = outs[r0]
+            up.ring_fwd_step(d2, s, qs[r0:r0 + n], visit(s, r0, n, ks), visit(s, r0, n, vs), seg_t, t2, o_acc, lse, o)
+    torch.cuda.synchronize()
+    for r0, n in pair:
+        assert torch.equal(outs[r0][2], o_all[r0:r0 + n]) and torch.equal(outs[r0][1], lse_all[r0:r0 + n])
+    # backward: dK/dV sums and their bf16 roundings travel with their shard (indexed by owner here,
+    # passed in batch order); a step writes only the key tiles it touches
+    dk_acc = torch.empty(ks.shape, dtype=torch.float32, device="cuda")
+    dv_acc = torch.empty(ks.shape, dtype=torch.float32, device="cuda")
+    dk, dv = torch.empty_like(ks), torch.empty_like(vs)
+    dq = torch.empty_like(qs)
+    dq_acc = torch.empty(qs.shape, dtype=torch.float32, device="cuda")
+    Ds = {}
+    for r0, n in pair:
+        D = torch.empty(2, n * Hq, sp, dtype=torch.float32, device="cuda")
+        o = outs[r0][2]
+        up.ring_bwd_prep(o.view(n * Hq, 2 * C, Dh), dos[r0:r0 + n].reshape(n * Hq, 2 * C, Dh),
+                         outs[r0][1].view(n * Hq, 2 * C), D)
+        Ds[r0] = D
+    for s in range(P):
+        for r0, n in pair:
+            d2, t2 = descs[r0]
+            own = [(r0 + d - s) % P for d in range(n)]
+            kacc, vacc = dk_acc[own].contiguous(), dv_acc[own].contiguous()   # the travelling sums
+            kout, vout = dk[own].contiguous(), dv[own].contiguous()            # and their bf16 roundings
+            up.ring_bwd_step(d2, s, qs[r0:r0 + n], visit(s, r0, n, ks), visit(s, r0, n, vs), dos[r0:r0 + n], Ds[r0],
+                             seg_t, t2, dq_acc[r0:r0 + n], kacc, vacc, dq[r0:r0 + n], kout, vout)
+            dk_acc[own], dv_acc[own] = kacc, vacc
+            dk[own], dv[own] = kout, vout
+    torch.cuda.synchronize()
+    assert torch.equal(dq, dq_all) and torch.equal(dk, dk_all) and torch.equal(dv, dv_all)
