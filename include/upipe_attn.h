@@ -323,6 +323,8 @@ typedef struct {
   int32_t dev_first, dev_count; /* the ring devices dev_first .. dev_first + dev_count - 1 (<= P) */
   int32_t kv_count;     /* P, or dev_count (see above) */
 } upipe_ring_desc_t;
+/* A descriptor whose launches would exceed the grid's second dimension (dev_count * ceil(2C/256)
+ * query-tile pairs or kv_count * ceil(2C/128) key tiles above 65535) is UPIPE_ERR_UNSUPPORTED. */
 
 /* Bytes of the P per-step tile tables of a ring (device memory the caller owns, 16-byte
  * aligned).  The tables depend on the descriptor and on seg only: build them once per segment
