@@ -63,6 +63,7 @@ struct TcGemmParams {
   float* split_out;
   int tma_out;  // 0: per-thread stores; 1: TMA store (2-D map); 2: TMA reduce-add (2-D); 3: TMA store of split partials (3-D)
   uint64_t wait_ns;  // limit of each bounded wait
+  int m_fast;   // unit order: M-tile pairs fastest (B, the larger operand, read once) or N tiles fastest
 };
 
 enum : int { TMA_OUT_NONE = 0, TMA_OUT_STORE = 1, TMA_OUT_ADD = 2, TMA_OUT_SPLIT = 3 };
@@ -162,12 +163,21 @@ __global__ void __launch_bounds__(THREADS, 1) k_gemm_tc(const __grid_constant__ 
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  // unit t -> (m tile, n tile, split); n fastest so that clusters running together share A rows in L2
+  // unit t -> (m tile, n tile, split).  The fast index sweeps its whole operand once for every
+  // step of the slow index: with N fastest B is re-read for every pair of M tiles, with M fastest
+  // A for every N tile.  The launcher sweeps the smaller operand (the one L2 can hold), so the
+  // larger one is read from DRAM about once: an MLP's gate/up weights (28672 x 4096) do not fit in
+  // L2 and are swept over its 8192-row tiles of X otherwise.
   auto decode = [&](int64_t t, int& tm, int& tn, int& ks) {
     ks = (int)(t / tiles_pn);
     const int64_t r = t % tiles_pn;
-    tm = 2 * (int)(r / p.tiles_n) + crank;
-    tn = (int)(r % p.tiles_n);
+    if (p.m_fast) {
+      tm = 2 * (int)(r % tiles_mp) + crank;
+      tn = (int)(r / tiles_mp);
+    } else {
+      tm = 2 * (int)(r / p.tiles_n) + crank;
+      tn = (int)(r % p.tiles_n);
+    }
   };
   auto k_tiles = [&](int ks) {
     const int64_t kb = (int64_t)ks * p.k_per_split;
@@ -439,6 +449,7 @@ cudaError_t launch_gemm_tc(const TcGemmArgs& g, int split_k, float* split_scratc
   p.tiles_n = (int)ceil_div(g.N, BN);
   p.split_out = split_k > 1 ? split_scratch : nullptr;
   p.wait_ns = wait_limit_ns();
+  p.m_fast = g.N > g.M;  // sweep the smaller operand A [M, K]
   // fp32 outputs through TMA where the layout allows it (16-byte aligned base and rows)
   CUtensorMap tout;
   std::memset(&tout, 0, sizeof(tout));
