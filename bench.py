@@ -845,7 +845,11 @@ def main():
             dt, fl, threads, Ssamp = oracle_sample(w, args.sample_tokens)
             cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                    "sample": f"oracle fp64 forward+backward on the first {Ssamp} tokens of {w.name}; "
-                             f"{dt:.2f} s for {fl / 1e12:.4f} TFLOP"}
+                             f"{dt:.2f} s for {fl / 1e12:.4f} TFLOP",
+                   # labelled extrapolation: the whole step at the sample's FLOP rate
+                   "extrapolated_step_s": flops / (fl / dt),
+                   "extrapolated_how": "the workload's fwd+bwd FLOPs divided by the sample's FLOP rate "
+                                       "(extrapolated, not timed)"}
 
         if offload is not None:
             for r in offload["runs"]:
