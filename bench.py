@@ -543,11 +543,20 @@ def main():
         up.build_tile_table(cdesc, seg_t, table, stream)
         up.core_fwd(cdesc, q, k, v, seg_t, table, o, lse_c, stream)
         up.core_recompute(cdesc, q, k, v, do, lse_c, seg_t, table, o, Dt, stream)
+        # dK / dV as the layer launches it: into fp32 sums (flushed in windows) for a partial KV
+        # group or once a key tile's work items exceed the window, else straight to bf16
+        if hpc < g or min(hpc, g) * -(-S // 128) > up.DKDV_WINDOW_DEFAULT:
+            dk_acc = torch.zeros(k.shape, dtype=torch.float32, device=dev)
+            dv_acc = torch.zeros(v.shape, dtype=torch.float32, device=dev)
+            dkdv = lambda: up.core_bwd_dkdv_acc(cdesc, q, k, v, do, lse_c, Dt, seg_t, table, dk_acc, dv_acc,
+                                                stream=stream)
+        else:
+            dkdv = lambda: up.core_bwd_dkdv(cdesc, q, k, v, do, lse_c, Dt, seg_t, table, dk, dv, stream)
         return {
             "fwd": lambda: up.core_fwd(cdesc, q, k, v, seg_t, table, o, lse_c, stream),
             "recompute": lambda: up.core_recompute(cdesc, q, k, v, do, lse_c, seg_t, table, o, Dt, stream),
             "dq": lambda: up.core_bwd_dq(cdesc, q, k, v, do, lse_c, Dt, seg_t, table, dq, stream),
-            "dkdv": lambda: up.core_bwd_dkdv(cdesc, q, k, v, do, lse_c, Dt, seg_t, table, dk, dv, stream),
+            "dkdv": dkdv,
         }
 
     if args.kernel in ("lse_merge", "ring", "ring_bwd"):

@@ -251,6 +251,15 @@ upipe_status_t upipe_attn_core_bwd_dkdv(const upipe_attn_desc_t* desc, const uin
                                         const uint16_t* v, const uint16_t* dO, const float* lse, const float* D,
                                         const int32_t* seg, void* table, uint16_t* dk, uint16_t* dv,
                                         void* stream);
+/* bwd_dkdv into fp32 sums, as the layer launches it for a KV group split over head chunks or for
+ * key tiles of more work items than the window of upipe_attn_set_dkdv_window:
+ *   dk_acc, dv_acc  device fp32 [Hkv, S, Dh]: this call's dK, dV are added to what they hold
+ *                   (in windows of work items: see upipe_attn_set_dkdv_window)
+ *   dk, dv          both NULL, or device bf16 [Hkv, S, Dh] that receive the sums rounded. */
+upipe_status_t upipe_attn_core_bwd_dkdv_acc(const upipe_attn_desc_t* desc, const uint16_t* q, const uint16_t* k,
+                                            const uint16_t* v, const uint16_t* dO, const float* lse,
+                                            const float* D, const int32_t* seg, void* table, float* dk_acc,
+                                            float* dv_acc, uint16_t* dk, uint16_t* dv, void* stream);
 
 /* Projection GEMM alone, for testing: C[M, N] (fp32, row-major, ldc) = A[M, K] * B[N, K]^T with
  * A, B device bf16 row-major (lda, ldb in elements).  The per-chunk Q/K/V and O projections of
@@ -362,8 +371,10 @@ upipe_status_t upipe_attn_ring_fwd_step(const upipe_ring_desc_t* desc, int32_t s
  *                   dq_acc; likewise dk / dv when one call batches every device with every
  *                   shard (dev_count = kv_count = P), else every step writes the key tiles it
  *                   changes (so dk / dv travel with their shard like dk_acc / dv_acc) and the
- *                   ring's last step does not store dk_acc / dv_acc.  With a NULL bf16 output the
- *                   fp32 sums hold the result after the last step.
+ *                   ring's last step does not store dk_acc / dv_acc (for a key tile of more
+ *                   work items than upipe_attn_set_dkdv_window's window they then hold partial
+ *                   sums).  With a NULL bf16 output the fp32 sums hold the result after the
+ *                   last step.
  * Tiles that no query of a step sees are not touched by that step. */
 upipe_status_t upipe_attn_ring_bwd_step(const upipe_ring_desc_t* desc, int32_t step, const uint16_t* q,
                                         const uint16_t* k, const uint16_t* v, const uint16_t* dO, const float* D,
@@ -442,6 +453,20 @@ typedef struct {
 } upipe_attn_timing_t;
 upipe_status_t upipe_attn_timing_enable(int32_t on);
 upipe_status_t upipe_attn_timing_collect(upipe_attn_timing_t* out, int32_t cap, int32_t* n);
+
+/* Accumulation window of the layer backward's dK / dV kernel, in work items (query head x query
+ * tile) per key tile; 0 restores the default of 4096, otherwise even, 2 .. 2^24, else
+ * UPIPE_ERR_INVALID_ARG.  The kernel sums each key tile's dK and dV over all query heads of its KV
+ * group and all query tiles that see it (MaxText article, Splash paragraph: GQA) in tensor-memory
+ * fp32 accumulators; a very long accumulation into the same accumulator drifts low, so once a key
+ * tile has more items than the window, the layer backward entry points (upipe_attn_bwd and its
+ * offload variant) keep dK / dV as fp32 sums in their workspace and the kernel adds its
+ * accumulators into them after every full window.  Takes effect for workspaces planned (and
+ * sizes queried) after the call: a workspace must be sized under the same window it runs with.
+ * Ring backward steps flush into their dk_acc / dv_acc the same way (a key tile of a step has
+ * n_q_heads / n_kv_heads x ceil(2C/128) items at most), and so does
+ * upipe_attn_core_bwd_dkdv_acc; upipe_attn_core_bwd_dkdv, which writes bf16 only, does not flush. */
+upipe_status_t upipe_attn_set_dkdv_window(int32_t items);
 
 /* Limit of every bounded device-side wait of the library's kernels, in nanoseconds (0 restores the
  * default of 4 s; at most 60 s).  Each kernel receives the value in effect when it is launched.

@@ -21,12 +21,12 @@ UPIPE_OK = 0
 
 EXPORTS = ["upipe_attn_status_string", "upipe_attn_last_error_string", "upipe_attn_workspace_size", "upipe_attn_tile_table_size",
            "upipe_attn_build_tile_table", "upipe_attn_fwd", "upipe_attn_bwd", "upipe_attn_core_fwd",
-           "upipe_attn_core_recompute", "upipe_attn_core_bwd_dq", "upipe_attn_core_bwd_dkdv", "upipe_attn_gemm_nt",
+           "upipe_attn_core_recompute", "upipe_attn_core_bwd_dq", "upipe_attn_core_bwd_dkdv", "upipe_attn_core_bwd_dkdv_acc", "upipe_attn_gemm_nt",
            "upipe_attn_device_status", "upipe_attn_fwd_no_alloc", "upipe_attn_launch_count", "upipe_attn_lse_merge",
            "upipe_attn_ring_bwd_prep", "upipe_attn_accumulate", "upipe_attn_last_device_error",
            "upipe_attn_no_alloc_device_status", "upipe_attn_timing_enable", "upipe_attn_timing_collect",
            "upipe_attn_workspace_size_offload", "upipe_attn_fwd_offload", "upipe_attn_bwd_offload",
-           "upipe_attn_set_wait_limit_ns", "upipe_attn_wait_probe", "upipe_mlp_workspace_size", "upipe_mlp_fwd",
+           "upipe_attn_set_wait_limit_ns", "upipe_attn_set_dkdv_window", "upipe_attn_wait_probe", "upipe_mlp_workspace_size", "upipe_mlp_fwd",
            "upipe_mlp_bwd", "upipe_attn_ring_tables_size", "upipe_attn_ring_build_tables", "upipe_attn_ring_fwd_step",
            "upipe_attn_ring_bwd_step", "upipe_attn_ring_fwd", "upipe_attn_ring_bwd"]
 
@@ -110,6 +110,7 @@ def lib():
             "upipe_attn_core_recompute": ([D, P, P, P, P, P, P, P, P, P, P], ctypes.c_int),
             "upipe_attn_core_bwd_dq": ([D, P, P, P, P, P, P, P, P, P, P], ctypes.c_int),
             "upipe_attn_core_bwd_dkdv": ([D, P, P, P, P, P, P, P, P, P, P, P], ctypes.c_int),
+            "upipe_attn_core_bwd_dkdv_acc": ([D, P, P, P, P, P, P, P, P, P, P, P, P, P], ctypes.c_int),
             "upipe_attn_gemm_nt": ([I64, I64, I64, P, I64, P, I64, P, I64, P], ctypes.c_int),
             "upipe_attn_device_status": ([P, ctypes.POINTER(ctypes.c_int32), P], ctypes.c_int),
             "upipe_attn_fwd_no_alloc": ([D, P, P, P, P, P, P, P], ctypes.c_int),
@@ -121,6 +122,7 @@ def lib():
             "upipe_attn_no_alloc_device_status": ([ctypes.POINTER(ctypes.c_int32), P], ctypes.c_int),
             "upipe_attn_timing_enable": ([ctypes.c_int32], ctypes.c_int),
             "upipe_attn_set_wait_limit_ns": ([ctypes.c_uint64], ctypes.c_int),
+            "upipe_attn_set_dkdv_window": ([ctypes.c_int32], ctypes.c_int),
             "upipe_mlp_workspace_size": ([ctypes.POINTER(MlpDesc), ctypes.c_int, ctypes.POINTER(SZ)], ctypes.c_int),
             "upipe_mlp_fwd": ([ctypes.POINTER(MlpDesc), P, P, P, P, P, SZ, P], ctypes.c_int),
             "upipe_mlp_bwd": ([ctypes.POINTER(MlpDesc), P, P, P, P, P, P, P, P, SZ, P], ctypes.c_int),
@@ -231,6 +233,14 @@ def set_wait_limit_ns(ns: int):
     _check(lib().upipe_attn_set_wait_limit_ns(int(ns)), "set_wait_limit_ns")
 
 
+DKDV_WINDOW_DEFAULT = 4096   # work items per dK / dV accumulation before a flush (upipe_attn_set_dkdv_window)
+
+
+def set_dkdv_window(items: int):
+    """Work items per dK/dV tensor-memory accumulation before it is added to fp32 sums (0: 4096)."""
+    _check(lib().upipe_attn_set_dkdv_window(int(items)), "set_dkdv_window")
+
+
 def wait_probe(buf, arrive: bool, stream=None):
     """One bounded wait on a barrier nothing completes (arrive=False) or one already completed."""
     _check(lib().upipe_attn_wait_probe(_ptr(buf), buf.numel() * buf.element_size(), int(bool(arrive)),
@@ -316,6 +326,16 @@ def core_bwd_dkdv(desc: Desc, q, k, v, dO, lse, D, seg, table, dk, dv, stream=No
     _check(lib().upipe_attn_core_bwd_dkdv(ctypes.byref(desc), _bf16(q), _bf16(k), _bf16(v), _bf16(dO), _ptr(lse),
                                           _ptr(D), _ptr(seg), _ptr(table), _bf16(dk), _bf16(dv), _stream(stream)),
            "core_bwd_dkdv")
+
+
+def core_bwd_dkdv_acc(desc: Desc, q, k, v, dO, lse, D, seg, table, dk_acc, dv_acc, dk=None, dv=None, stream=None):
+    """dK, dV added to the fp32 sums dk_acc, dv_acc [Hkv, S, Dh] (flushed in windows); dk, dv: their
+    bf16 rounding, or None."""
+    _check(lib().upipe_attn_core_bwd_dkdv_acc(ctypes.byref(desc), _bf16(q), _bf16(k), _bf16(v), _bf16(dO), _ptr(lse),
+                                              _ptr(D), _ptr(seg), _ptr(table), _ptr(dk_acc), _ptr(dv_acc),
+                                              None if dk is None else _bf16(dk), None if dv is None else _bf16(dv),
+                                              _stream(stream)),
+           "core_bwd_dkdv_acc")
 
 
 def core_bwd(desc: Desc, q, k, v, dO, lse, seg, table, dq, dk, dv, stream=None):

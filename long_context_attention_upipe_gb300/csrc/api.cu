@@ -44,6 +44,12 @@ void note_launch() { g_launch_count.fetch_add(1, std::memory_order_relaxed); }
 std::atomic<uint64_t> g_wait_limit_ns{tc_wait_default_ns};
 uint64_t wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
 
+// Longest run of dK / dV accumulations into the same tensor-memory tile before the dK/dV kernel
+// adds it into fp32 sums in global memory (upipe_attn_set_dkdv_window; even).
+constexpr int kDkvWindowDefault = 4096;
+std::atomic<int> g_dkdv_window{kDkvWindowDefault};
+int dkdv_window() { return g_dkdv_window.load(std::memory_order_relaxed); }
+
 upipe_status_t cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return UPIPE_OK;
   g_last_cuda_error = cudaGetErrorName(e);
@@ -105,6 +111,11 @@ struct Plan {
   int64_t R;
   size_t xs[2], dys[2];
   int split_wo_blk, split_wqkv_q_blk, split_wqkv_full_blk;
+  // dK / dV summed in fp32 workspace buffers (dkacc, dvacc: [kvc][S][Dh]) rather than written in
+  // bf16 by the dK/dV kernel: always for a KV group split over chunks, and for whole groups once a
+  // key tile's work items (the group's query heads x query tiles) exceed the accumulation window
+  bool kv_sums;
+  int window;
 };
 
 constexpr int64_t kDefaultStageRows = 65536;
@@ -183,9 +194,11 @@ Plan make_plan(const upipe_attn_desc_t* desc, int pass, int64_t stage_rows = 0) 
     p.dq = take((p.hpc + 2 * p.kvc) * head);  // [dQ heads | dK heads | dV heads], one 3-D tensor
     p.dk = p.dq + p.hpc * head;
     p.dv = p.dk + p.kvc * head;
-    if (p.hpc < p.g) {
-      p.dkacc = take((size_t)p.S * p.Dh * sizeof(float));
-      p.dvacc = take((size_t)p.S * p.Dh * sizeof(float));
+    p.window = dkdv_window();
+    p.kv_sums = p.hpc < p.g || (int64_t)p.g * ceil_div(p.S, kTile) > p.window;
+    if (p.kv_sums) {
+      p.dkacc = take((size_t)p.kvc * p.S * p.Dh * sizeof(float));
+      p.dvacc = take((size_t)p.kvc * p.S * p.Dh * sizeof(float));
     }
     if (multi && p.accum == 0) p.dxacc = take((size_t)p.S * p.d * sizeof(float));
     const int sms = num_sms();
@@ -405,10 +418,10 @@ upipe_status_t run_bwd(const Plan& p, const bf16* X, const bf16* Wqkv, const bf1
       Timed t(UPIPE_K_QKV_PROJ, EPI_STORE_BF16, p.S, qkv_width(p, new_group), p.d, 1, c, st);
       UPIPE_CUDA(project_qkv(p, c, new_group, X, 0, p.S, Wqkv, ws, st));
     }
-    if (new_group && p.hpc < p.g) {
-      Timed t(UPIPE_K_ZERO, 0, 2 * p.S * p.Dh, 1, 1, 1, c, st);
-      UPIPE_CUDA(launch_zero(at<char>(ws, p.dkacc), (int64_t)p.S * p.Dh * 4, st));
-      UPIPE_CUDA(launch_zero(at<char>(ws, p.dvacc), (int64_t)p.S * p.Dh * 4, st));
+    if (new_group && p.kv_sums) {
+      Timed t(UPIPE_K_ZERO, 0, 2 * p.kvc * p.S * p.Dh, 1, 1, 1, c, st);
+      UPIPE_CUDA(launch_zero(at<char>(ws, p.dkacc), (int64_t)p.kvc * p.S * p.Dh * 4, st));
+      UPIPE_CUDA(launch_zero(at<char>(ws, p.dvacc), (int64_t)p.kvc * p.S * p.Dh * 4, st));
     }
     {  // dO_c = dY * Wo_c
       Timed t(UPIPE_K_DO_PROJ, EPI_STORE_BF16, p.S, (int64_t)p.hpc * p.Dh, p.d, 1, c, st);
@@ -436,7 +449,8 @@ upipe_status_t run_bwd(const Plan& p, const bf16* X, const bf16* Wqkv, const bf1
     b.dq = at<bf16>(ws, p.dq);
     b.dk = at<bf16>(ws, p.dk);
     b.dv = at<bf16>(ws, p.dv);
-    b.acc_kv = p.hpc < p.g;
+    b.acc_kv = p.kv_sums;
+    b.flush_items = p.window;
     b.dk_acc = p.dkacc ? at<float>(ws, p.dkacc) : nullptr;
     b.dv_acc = p.dvacc ? at<float>(ws, p.dvacc) : nullptr;
     b.nkv = p.kvc;
@@ -448,10 +462,10 @@ upipe_status_t run_bwd(const Plan& p, const bf16* X, const bf16* Wqkv, const bf1
       Timed t(UPIPE_K_BWD_DKDV, 0, p.S, p.hpc, p.Dh, 1, c, st);
       UPIPE_CUDA(launch_attn_bwd_dkdv(b, p.Dh, st));
     }
-    if (end_group && p.hpc < p.g) {
-      Timed t(UPIPE_K_CONVERT, 0, 2 * p.S * p.Dh, 1, 1, 1, c, st);
-      UPIPE_CUDA(launch_f32_to_bf16(at<float>(ws, p.dkacc), at<bf16>(ws, p.dk), p.S * p.Dh, 1.f, st));
-      UPIPE_CUDA(launch_f32_to_bf16(at<float>(ws, p.dvacc), at<bf16>(ws, p.dv), p.S * p.Dh, 1.f, st));
+    if (end_group && p.kv_sums) {
+      Timed t(UPIPE_K_CONVERT, 0, 2 * p.kvc * p.S * p.Dh, 1, 1, 1, c, st);
+      UPIPE_CUDA(launch_f32_to_bf16(at<float>(ws, p.dkacc), at<bf16>(ws, p.dk), p.kvc * p.S * p.Dh, 1.f, st));
+      UPIPE_CUDA(launch_f32_to_bf16(at<float>(ws, p.dvacc), at<bf16>(ws, p.dv), p.kvc * p.S * p.Dh, 1.f, st));
     }
     // blocks of dQKV_c that are final now: the chunk's dQ heads, plus dK/dV at a group end.
     // They are planes [0, nb) of the [dQ | dK | dV] tensor of the workspace.
@@ -664,10 +678,10 @@ upipe_status_t run_bwd_offload(const Plan& p, const bf16* hX, bool x_host, const
     const bool new_group = p.hpc >= p.g || (c * p.hpc) % p.g == 0;
     const bool end_group = p.hpc >= p.g || ((c + 1) * p.hpc) % p.g == 0;
     const int kv0 = (c * p.hpc) / p.g;
-    if (new_group && p.hpc < p.g) {
-      Timed t(UPIPE_K_ZERO, 0, 2 * p.S * p.Dh, 1, 1, 1, c, st);
-      UPIPE_CUDA(launch_zero(at<char>(ws, p.dkacc), (int64_t)p.S * p.Dh * 4, st));
-      UPIPE_CUDA(launch_zero(at<char>(ws, p.dvacc), (int64_t)p.S * p.Dh * 4, st));
+    if (new_group && p.kv_sums) {
+      Timed t(UPIPE_K_ZERO, 0, 2 * p.kvc * p.S * p.Dh, 1, 1, 1, c, st);
+      UPIPE_CUDA(launch_zero(at<char>(ws, p.dkacc), (int64_t)p.kvc * p.S * p.Dh * 4, st));
+      UPIPE_CUDA(launch_zero(at<char>(ws, p.dvacc), (int64_t)p.kvc * p.S * p.Dh * 4, st));
     }
     upipe_status_t s = over_blocks(sg, [&](int64_t b, int64_t r0, int64_t rows) -> upipe_status_t {
       {
@@ -691,7 +705,8 @@ upipe_status_t run_bwd_offload(const Plan& p, const bf16* hX, bool x_host, const
     bw.dq = at<bf16>(ws, p.dq);
     bw.dk = at<bf16>(ws, p.dk);
     bw.dv = at<bf16>(ws, p.dv);
-    bw.acc_kv = p.hpc < p.g;
+    bw.acc_kv = p.kv_sums;
+    bw.flush_items = p.window;
     bw.dk_acc = p.dkacc ? at<float>(ws, p.dkacc) : nullptr;
     bw.dv_acc = p.dvacc ? at<float>(ws, p.dvacc) : nullptr;
     bw.nkv = p.kvc;
@@ -703,10 +718,10 @@ upipe_status_t run_bwd_offload(const Plan& p, const bf16* hX, bool x_host, const
       Timed t(UPIPE_K_BWD_DKDV, 0, p.S, p.hpc, p.Dh, 1, c, st);
       UPIPE_CUDA(launch_attn_bwd_dkdv(bw, p.Dh, st));
     }
-    if (end_group && p.hpc < p.g) {
-      Timed t(UPIPE_K_CONVERT, 0, 2 * p.S * p.Dh, 1, 1, 1, c, st);
-      UPIPE_CUDA(launch_f32_to_bf16(at<float>(ws, p.dkacc), at<bf16>(ws, p.dk), p.S * p.Dh, 1.f, st));
-      UPIPE_CUDA(launch_f32_to_bf16(at<float>(ws, p.dvacc), at<bf16>(ws, p.dv), p.S * p.Dh, 1.f, st));
+    if (end_group && p.kv_sums) {
+      Timed t(UPIPE_K_CONVERT, 0, 2 * p.kvc * p.S * p.Dh, 1, 1, 1, c, st);
+      UPIPE_CUDA(launch_f32_to_bf16(at<float>(ws, p.dkacc), at<bf16>(ws, p.dk), p.kvc * p.S * p.Dh, 1.f, st));
+      UPIPE_CUDA(launch_f32_to_bf16(at<float>(ws, p.dvacc), at<bf16>(ws, p.dv), p.kvc * p.S * p.Dh, 1.f, st));
     }
     int32_t blk_row[kMaxBlocks];
     int nb = 0;
@@ -1109,6 +1124,27 @@ upipe_status_t upipe_attn_core_bwd_dkdv(const upipe_attn_desc_t* desc, const uin
   return cuda_status(launch_attn_bwd_dkdv(b, desc->head_dim, (cudaStream_t)stream));
 }
 
+// The same into fp32 sums, flushed in windows (the layer's launch for partial KV groups and long
+// key tiles).
+upipe_status_t upipe_attn_core_bwd_dkdv_acc(const upipe_attn_desc_t* desc, const uint16_t* q, const uint16_t* k,
+                                            const uint16_t* v, const uint16_t* dO, const float* lse,
+                                            const float* D, const int32_t* seg, void* table, float* dk_acc,
+                                            float* dv_acc, uint16_t* dk, uint16_t* dv, void* stream) {
+  AttnBwdArgs b;
+  upipe_status_t s = core_bwd_common(desc, q, k, v, dO, lse, D, seg, table, &b);
+  if (s != UPIPE_OK) return s;
+  if (!dk_acc || !dv_acc || (!dk) != (!dv)) return UPIPE_ERR_INVALID_ARG;
+  if (!aligned16(dk_acc) || !aligned16(dv_acc) || (dk && (!aligned16(dk) || !aligned16(dv))))
+    return UPIPE_ERR_ALIGNMENT;
+  b.acc_kv = 1;
+  b.flush_items = dkdv_window();
+  b.dk_acc = dk_acc;
+  b.dv_acc = dv_acc;
+  b.dk_out = reinterpret_cast<bf16*>(dk);
+  b.dv_out = reinterpret_cast<bf16*>(dv);
+  return cuda_status(launch_attn_bwd_dkdv(b, desc->head_dim, (cudaStream_t)stream));
+}
+
 upipe_status_t upipe_attn_gemm_nt(int64_t M, int64_t N, int64_t K, const uint16_t* A, int64_t lda, const uint16_t* B,
                                   int64_t ldb, float* C, int64_t ldc, void* stream) {
   if (M <= 0 || N <= 0 || K <= 0 || !A || !B || !C || lda < K || ldb < K || ldc < N) return UPIPE_ERR_INVALID_ARG;
@@ -1321,6 +1357,7 @@ static upipe_status_t ring_bwd_launch(const upipe_ring_desc_t* desc, int step, b
   b.dq_acc = dq_acc;
   b.dq = reinterpret_cast<bf16*>(dq);
   b.acc_kv = 1;
+  b.flush_items = dkdv_window();
   b.dk_acc = dk_acc;
   b.dv_acc = dv_acc;
   b.dk_out = reinterpret_cast<bf16*>(dk);
@@ -1508,6 +1545,12 @@ upipe_status_t upipe_attn_timing_collect(upipe_attn_timing_t* out, int32_t cap, 
   }
   *n = k;
   return status;
+}
+
+upipe_status_t upipe_attn_set_dkdv_window(int32_t items) {
+  if (items < 0 || (items && (items < 2 || items % 2 || items > (1 << 24)))) return UPIPE_ERR_INVALID_ARG;
+  g_dkdv_window.store(items ? items : kDkvWindowDefault, std::memory_order_relaxed);
+  return UPIPE_OK;
 }
 
 upipe_status_t upipe_attn_set_wait_limit_ns(uint64_t ns) {

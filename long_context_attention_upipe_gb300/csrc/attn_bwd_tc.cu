@@ -26,6 +26,13 @@
 //   dK += dS^T Q.  Query heads sharing the KV head accumulate in TMEM (GQA reduction inside the
 //   CTA).  The two issuers keep the shared dK / dV accumulations in item order through token
 //   barriers; the two element-wise groups take turns phase by phase (named-barrier ping-pong).
+//   A long accumulation into the same TMEM tile drifts low (against an fp64 sum of the same bf16
+//   products: 0.6% after 32K work items, 4.8% after 312K), so launches that keep fp32 sums in
+//   global memory (acc_kv) with flush_items > 0 add the accumulators into them and restart them
+//   every flush_items items (a window): both issuers commit the window's last MMAs to win_full,
+//   each element-wise group reads its accumulator (group 0 dK, group 1 dV) after its last item
+//   of the window, adds it to the global sum and arrives on win_empty, which the first MMA of the
+//   next window waits for.
 // Every wait on an mbarrier is bounded (see tc::mbar_wait); registers are split per role with
 // setmaxnreg (launch 168 x 384; control warpgroup 72, element-wise warpgroups 216).
 #include "geom.cuh"
@@ -427,6 +434,37 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dq_tc(const __grid_con
 // ================================================================================================
 // dK, dV
 // ================================================================================================
+// Adds one TMEM accumulator row (this thread's lane, DH fp32 columns, times mul) to its fp32 sum
+// in global memory, 32 columns at a time.  Out of line: it runs once per window, and inlined its
+// registers would burden the element-wise loop around it.
+template <int DH>
+__device__ __noinline__ void flush_window(uint32_t acc_addr, float* row, float mul, bool store, bool add) {
+#pragma unroll 1
+  for (int ch = 0; ch < DH / 32; ++ch) {
+    uint32_t v[32];
+    tc::tmem_ld32(acc_addr + ch * 32, v);
+    float4 w4[8];
+#pragma unroll
+    for (int q4 = 0; q4 < 8; ++q4) w4[q4] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (store && add) {
+#pragma unroll
+      for (int q4 = 0; q4 < 8; ++q4) w4[q4] = reinterpret_cast<const float4*>(row + ch * 32)[q4];
+    }
+    tc::tmem_ld_wait();
+    if (store) {
+#pragma unroll
+      for (int q4 = 0; q4 < 8; ++q4) {
+        float4 o4 = w4[q4];
+        o4.x += __uint_as_float(v[q4 * 4 + 0]) * mul;
+        o4.y += __uint_as_float(v[q4 * 4 + 1]) * mul;
+        o4.z += __uint_as_float(v[q4 * 4 + 2]) * mul;
+        o4.w += __uint_as_float(v[q4 * 4 + 3]) * mul;
+        reinterpret_cast<float4*>(row + ch * 32)[q4] = o4;
+      }
+    }
+  }
+}
+
 template <int DH>
 struct DkvLayout {
   static constexpr uint32_t TB = 128 * DH * 2;
@@ -471,6 +509,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 21);
   uint64_t* dv_tok = bars + 22;   // phase n completes once dV(n) is issued
   uint64_t* dk_tok = bars + 23;   // phase n completes once dK(n) is issued
+  uint64_t* win_full = bars + 24;   // a window's last dK and dV MMAs are complete (both issuers)
+  uint64_t* win_empty = bars + 25;  // both groups have added the window's sums to global memory
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t S = a.S;
@@ -488,6 +528,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
   const int n_heads = dev < a.ndev ? max(0, min(a.hq, (int)blockIdx.x * a.g + a.g) - (int)blockIdx.x * a.g) : 0;
   const int nq = tr.w - tr.x;
   const int n_items = n_heads * nq;
+  // windows flushed into the global fp32 sums: every full window followed by more items
+  const int F = b.acc_kv ? b.flush_items : 0;
+  const int n_win = (F > 0 && n_items > 0) ? (n_items - 1) / F : 0;
   if (a.ring.P) {
     grid_dep_trigger();
     // a ring step adds nothing to key tiles that no query of the step sees (plain launches write
@@ -510,6 +553,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
     tc::mbar_init(acc_full, n_items >= 2 ? 2 : 1);  // the last MMAs of each issuer
     tc::mbar_init(dv_tok, 1);
     tc::mbar_init(dk_tok, 1);
+    tc::mbar_init(win_full, 2);
+    tc::mbar_init(win_empty, 256);
     for (int i = 0; i < NQ; ++i) {
       tc::mbar_init(&q_full[i], 1);
       tc::mbar_init(&q_empty[i], 1);
@@ -584,10 +629,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
           // follows the element-wise group's P^T arrival as closely as possible
           ok = tc::mbar_wait(&o_full[g], (n / NO) & 1, abort_flag, a.err, a.wait_ns);
           if (ok && n > 0) ok = tc::mbar_wait(dv_tok, (n - 1) & 1, abort_flag, a.err, a.wait_ns);  // dV(n-1) issued
+          // the first item of a window restarts the accumulators once the previous window's sums
+          // are out (F is even, so that item is always this issuer's when g == 0)
+          const bool win_start = F > 0 && n > 0 && n % F == 0;
+          if (ok && win_start) ok = tc::mbar_wait(win_empty, ((n / F) - 1) & 1, abort_flag, a.err, a.wait_ns);
+          const bool acc_in = F > 0 ? n % F != 0 : n > 0;
           if (ok) ok = tc::mbar_wait(&p_full[g], ph, abort_flag, a.err, a.wait_ns);
           if (!ok) break;
           tc::fence_after_sync();
-          mma_acc<DH>(tmem + L::DV_COL, r_tm, dOmn, n > 0);  // dV += P^T dO
+          mma_acc<DH>(tmem + L::DV_COL, r_tm, dOmn, acc_in);  // dV += P^T dO
           tc::fence_before_sync();
           tc::mbar_arrive(dv_tok);
           mma_nt<DH>(r_tm, dV, dO);  // dP^T = V dO^T
@@ -597,10 +647,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
           if (ok) ok = tc::mbar_wait(&ds_full[g], ph, abort_flag, a.err, a.wait_ns);
           if (!ok) break;
           tc::fence_after_sync();
-          mma_acc<DH>(tmem + L::DK_COL, r_tm, tc::sdesc_add(dQmn, (n % NQ) * L::TB), n > 0);  // dK += dS^T Q
+          mma_acc<DH>(tmem + L::DK_COL, r_tm, tc::sdesc_add(dQmn, (n % NQ) * L::TB), acc_in);  // dK += dS^T Q
           tc::fence_before_sync();
           tc::mbar_arrive(dk_tok);
           tc::mma_commit(&q_empty[n % NQ]);
+          // this issuer's last item of a flushed window (F - 2 + g within it): its MMAs complete
+          // the window's sums together with the other issuer's
+          if (F > 0 && n % F == F - 2 + g && n / F < n_win) tc::mma_commit(win_full);
           if (n + 2 >= n_items) tc::mma_commit(acc_full);  // this issuer's last item
           if (n + 2 < n_items) issue_st(n + 2);
         }
@@ -714,6 +767,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
       tc::fence_before_sync();
       tc::mbar_arrive(&ds_full[grp]);
       give_turn();
+      if (F > 0 && n % F == F - 2 + grp && n / F < n_win) {
+        // this group's last item of a flushed window: add its accumulator (group 0 dK, group 1 dV)
+        // to the global fp32 sum, 32 columns at a time (rare: once per window, so the loads are
+        // not held ahead in registers the loop needs)
+        float* wrow = (grp == 0 ? b.dk_acc : b.dv_acc) + ((int64_t)kvh * S + (k_ok ? krow : 0)) * DH;
+        if (a.ring.P) grid_dep_wait();  // the previous ring step's sums are complete and visible
+        ok = tc::mbar_wait(win_full, (n / F) & 1, abort_flag, a.err, a.wait_ns);
+        tc::fence_after_sync();
+        // the first ring step starts the sums (nothing to add to), later flushes add to them
+        flush_window<DH>(lane_addr + (grp == 0 ? L::DK_COL : L::DV_COL), wrow, grp == 0 ? a.scale : 1.f, ok && k_ok,
+                         !(a.acc_first && n / F == 0));
+        tc::fence_before_sync();
+        tc::mbar_arrive(win_empty);  // the next window's first MMAs may overwrite the accumulators
+        if (!ok) break;
+      }
     }
     // after an abort, hand over the turns still owed so the other group never blocks on them
     for (int k = turn; k < n_give; ++k) tc::named_bar_arrive(kPing + 1 - grp, 256);
@@ -732,7 +800,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
       if (a.ring.P) grid_dep_wait();  // the previous ring step's sums are complete and visible
 #pragma unroll
       for (int i = 0; i < DH / 4; ++i) pa[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (ok && k_ok && !a.acc_first) {
+      if (ok && k_ok && (!a.acc_first || n_win > 0)) {
         const float4* src = reinterpret_cast<const float4*>((grp == 0 ? b.dk_acc : b.dv_acc) + off);
 #pragma unroll
         for (int i = 0; i < DH / 4; ++i) pa[i] = src[i];

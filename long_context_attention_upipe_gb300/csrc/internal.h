@@ -194,6 +194,9 @@ struct AttnBwdArgs {
   float* dv_acc;
   int acc_kv;
   int nkv;
+  int flush_items;  // > 0 (even; acc_kv launches): every flush_items work items the
+                    // dK / dV tensor-memory accumulators are added into dk_acc / dv_acc and
+                    // restarted, so no accumulation runs longer than that (see k_attn_bwd_dkdv_tc)
   float* dq_acc;    // ring: [nh, S, Dh] f32 accumulator of dQ (dq, if not NULL, gets it in bf16)
   bf16* dk_out;     // ring: the accumulated dK, dV rounded to bf16 (NULL: not written)
   bf16* dv_out;

@@ -78,6 +78,11 @@ def test_fwd_host_checks_run_before_any_launch():
     assert L.upipe_attn_build_tile_table(ctypes.byref(t), odd, fake, 1 << 20, None, None) == 3
     assert L.upipe_attn_last_device_error(None, None, ctypes.byref(ctypes.c_int32())) == 1   # NULL workspace
     assert L.upipe_attn_no_alloc_device_status(None, None) == 1                            # NULL code
+    core = [fake] * 6 + [None, fake]                                  # q k v dO lse D, no segments, table
+    assert L.upipe_attn_core_bwd_dkdv_acc(ctypes.byref(d), *core, None, fake, None, None, None) == 1   # NULL dk_acc
+    assert L.upipe_attn_core_bwd_dkdv_acc(ctypes.byref(d), *core, fake, fake, fake, None, None) == 1   # dk without dv
+    assert L.upipe_attn_core_bwd_dkdv_acc(ctypes.byref(d), *core, odd, fake, None, None, None) == 3
+    assert L.upipe_attn_core_bwd_dkdv_acc(ctypes.byref(d), *core, fake, fake, fake, odd, None) == 3
     assert up.launch_count() == launches  # rejected calls launch nothing
 
 
@@ -100,6 +105,10 @@ def test_wait_limit_and_probe_check_arguments():
     L = up.lib()
     assert L.upipe_attn_set_wait_limit_ns(61 * 10 ** 9) == 1      # above the 60 s cap
     assert L.upipe_attn_set_wait_limit_ns(0) == 0                  # the default
+    for bad in (-2, 1, 3, 4097, (1 << 24) + 2):
+        assert L.upipe_attn_set_dkdv_window(bad) == 1               # odd, negative or too long
+    assert L.upipe_attn_set_dkdv_window(2) == 0
+    assert L.upipe_attn_set_dkdv_window(0) == 0                     # the default
     fake = ctypes.c_void_p(0x10000)
     assert L.upipe_attn_wait_probe(None, 64, 0, None) == 1
     assert L.upipe_attn_wait_probe(fake, 16, 0, None) == 1         # smaller than a table header
@@ -135,6 +144,26 @@ def test_offload_workspace_adds_the_staging_buffers():
         assert off - base >= tensors * 65536 * 4096 * 2
         assert off - base < tensors * 65536 * 4096 * 2 + (64 << 20)   # plus block split-K partials, alignment
     assert up.workspace_bytes_offload(d, 1, 0) == up.workspace_bytes_offload(d, 1, 65536)   # the default
+
+
+def test_backward_workspace_holds_fp32_kv_sums_past_the_window():
+    # 1M tokens, one KV group of 4 query heads per chunk: 4 x 8192 items per key tile > 4096, so the
+    # default window already plans the fp32 dK / dV sums; a 32K sequence (4 x 256 items) does not
+    S, Dh = 1 << 20, 128
+    sums = 2 * S * Dh * 4
+    long_ = up.make_desc(S, 4096, 4, 1, Dh, 4)
+    short = up.make_desc(32768, 4096, 4, 1, Dh, 4)
+    base_long, base_short = up.workspace_bytes(long_, 1), up.workspace_bytes(short, 1)
+    fwd = up.workspace_bytes(long_, 0)
+    try:
+        up.set_dkdv_window((1 << 24))                   # longer than any key tile's items: no sums
+        assert base_long - up.workspace_bytes(long_, 1) >= sums
+        up.set_dkdv_window(512)                         # 32K now exceeds it too
+        assert up.workspace_bytes(short, 1) - base_short >= 2 * 32768 * Dh * 4
+        assert up.workspace_bytes(long_, 0) == fwd       # the forward keeps no dK / dV
+    finally:
+        up.set_dkdv_window(0)
+    assert up.workspace_bytes(long_, 1) == base_long
 
 
 def test_ring_entry_points_check_arguments_before_any_launch():

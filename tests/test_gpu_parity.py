@@ -197,6 +197,49 @@ def test_core_fwd_bwd_match_oracle(case):
     assert rel_fro(dv, dV) <= GRAD_REL_FRO, rel_fro(dv, dV)
 
 
+@pytest.mark.parametrize("window", [2, 4, 1 << 24])
+@pytest.mark.parametrize("case", [CORE_CASES[2], CORE_CASES[4], CORE_CASES[5]],
+                         ids=lambda c: f"S{c[0]}_hq{c[1]}_hkv{c[2]}_dh{c[3]}_c{int(c[5])}")
+def test_core_dkdv_into_fp32_sums_flushed_in_windows(case, window):
+    # dK / dV added to fp32 sums that already hold values, the tensor-memory accumulators flushed
+    # every `window` work items (2: after every item pair; 2^24: never)
+    S, Hq, Hkv, Dh, segs, causal = case
+    q, k, v, do = qkv_inputs(S, Hq, Hkv, Dh)
+    seg = ui.segments_from_lengths(segs) if segs else None
+    desc = up.make_desc(S, 64, Hq, Hkv, Dh, Hq, causal)
+    table = torch.empty(up.tile_table_bytes(desc), dtype=torch.uint8, device="cuda")
+    seg_t = torch.from_numpy(seg).cuda() if seg is not None else None
+    up.build_tile_table(desc, seg_t, table)
+    qt, kt, vt, dot = (bf16_tensor(x) for x in (q, k, v, do))
+    o = torch.empty_like(qt)
+    lse = torch.empty(Hq, S, dtype=torch.float32, device="cuda")
+    up.core_fwd(desc, qt, kt, vt, seg_t, table, o, lse)
+    D = torch.empty(2, Hq, -(-S // 128) * 128, dtype=torch.float32, device="cuda")
+    up.core_recompute(desc, qt, kt, vt, dot, lse, seg_t, table, o, D)
+    rng = np.random.default_rng(7)
+    init_k = rng.standard_normal((Hkv, S, Dh))
+    init_v = rng.standard_normal((Hkv, S, Dh))
+    dk_acc = torch.from_numpy(init_k.astype(np.float32)).cuda()
+    dv_acc = torch.from_numpy(init_v.astype(np.float32)).cuda()
+    dk, dv = torch.empty_like(kt), torch.empty_like(vt)
+    try:
+        up.set_dkdv_window(window)
+        up.core_bwd_dkdv_acc(desc, qt, kt, vt, dot, lse, D, seg_t, table, dk_acc, dv_acc, dk, dv)
+        torch.cuda.synchronize()
+    finally:
+        up.set_dkdv_window(0)
+    assert up.device_status(table) == 0
+    Q, K, V, dO = (ui.bf16_to_f64(x) for x in (q, k, v, do))
+    _, dK, dV = orc.attention_backward(Q, K, V, dO, seg, causal, orc.default_scale(Dh))
+    sk, sv = dk_acc.double().cpu().numpy() - init_k, dv_acc.double().cpu().numpy() - init_v
+    assert rel_fro(sk, dK) <= GRAD_REL_FRO, rel_fro(sk, dK)
+    assert rel_fro(sv, dV) <= GRAD_REL_FRO, rel_fro(sv, dV)
+    # the bf16 outputs are the sums rounded (to the nearest bf16: within half a bf16 unit)
+    for out, acc in ((dk, dk_acc), (dv, dv_acc)):
+        a = acc.double().cpu().numpy()
+        assert np.all(np.abs(to_f64(out) - a) <= np.abs(a) * 2.0 ** -8 + 1e-30)
+
+
 def grow_keys(k, S, every=384):
     """K with its magnitude doubled every `every` positions (an exact bf16 exponent shift), so the
     scores of late key tiles outgrow those of the first tile by far more than 2^16 in exp2 units."""
@@ -282,6 +325,39 @@ def test_layer_fwd_bwd_match_oracle(case):
     assert rel_fro(to_f64(dX), dX_ref) <= GRAD_REL_FRO, rel_fro(to_f64(dX), dX_ref)
     assert rel_fro(to_f64(dW), dW_ref) <= GRAD_REL_FRO, rel_fro(to_f64(dW), dW_ref)
     assert rel_fro(to_f64(dWo), dWo_ref) <= GRAD_REL_FRO, rel_fro(to_f64(dWo), dWo_ref)
+
+
+@pytest.mark.parametrize("window,hpc", [(2, 4), (6, 4), (30, 4), (4, 1), (8, 8)])
+def test_layer_backward_with_flushed_dkdv_windows(window, hpc):
+    # windows of a few work items: every key tile adds its tensor-memory dK / dV accumulators to
+    # the fp32 sums many times (up to 32 items per key tile of a whole group here: 4 query heads x
+    # 8 query tiles; a window of 30 leaves a ragged last one); the gradients must match the oracle
+    # and the unflushed run to rounding
+    S, d, Hq, Hkv, Dh = 1000, 256, 8, 2, 128
+    segs, causal = [250, 1, 600, 149], True
+    X, W, Wo, dY = layer_inputs(S, d, Hq, Hkv, Dh)
+    seg = ui.segments_from_lengths(segs)
+    Xt, Wt, Wot, dYt = (bf16_tensor(x) for x in (X, W, Wo, dY))
+    seg_t = torch.from_numpy(seg).cuda()
+    desc = up.make_desc(S, d, Hq, Hkv, Dh, hpc, causal)
+    plain = up.Layer(desc)
+    Y, lse = plain.forward(Xt, Wt, Wot, seg_t)
+    ref = [to_f64(t) for t in plain.backward(Xt, Wt, Wot, seg_t, dYt, lse)]
+    try:
+        up.set_dkdv_window(window)
+        flushed = up.Layer(desc)
+        if hpc >= Hq // Hkv:                                  # whole groups: now with fp32 sums
+            assert flushed.ws_bwd.numel() > plain.ws_bwd.numel()
+        got = [to_f64(t) for t in flushed.backward(Xt, Wt, Wot, seg_t, dYt, lse)]
+    finally:
+        up.set_dkdv_window(0)
+    torch.cuda.synchronize()
+    assert up.device_status(flushed.ws_bwd) == 0
+    dX_ref, dW_ref, dWo_ref = orc.layer_backward(X, W, Wo, seg, dY, Hq, Hkv, Dh, causal)
+    for g, r, o in zip(got, ref, (dX_ref, dW_ref, dWo_ref)):
+        assert rel_fro(g, o) <= GRAD_REL_FRO, rel_fro(g, o)
+        assert rel_fro(g, r) <= 2e-3, rel_fro(g, r)            # the same products, summed in 2 stages
+    np.testing.assert_array_equal(got[2], ref[2])               # dWo does not involve dK / dV
 
 
 def test_layer_output_independent_of_chunking():

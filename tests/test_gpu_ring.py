@@ -455,19 +455,19 @@ def test_ring_of_eight_at_the_1m_share_against_the_direct_kernels():
     # differences of lse and O between the two forwards move the bf16 dS roundings.  Both meet the
     # gradient bar against the oracle.  Given the ring's own lse and D, the direct kernels build
     # the very same dS tiles and only the summation differs: dQ then agrees to the bf16 rounding of
-    # sums formed in another order.  dK and dV of the first keys sum 4M products each; the direct
-    # kernel accumulates all of them in tensor memory, which drifts low by a few 1e-4 over that
-    # length, while the ring restarts the accumulation every step and adds the steps' sums in fp32
-    # (against an fp64 sum of the same bf16 products the first key tile's dV is off by 0.18% in
-    # the ring and 0.61% in the direct kernel), so those two stay at the gradient bar.
+    # sums formed in another order.  dK and dV of the first keys sum 4M products each; accumulated
+    # in tensor memory in one run they drift low (against an fp64 sum the first key tile's dK is
+    # off by 0.64%, 0.53% of it systematic), so the layer's launch adds the accumulators to fp32
+    # sums every 4096 work items (then 0.26%), and the ring restarts them every step.
     for got, want in ((dq, dq_ref), (dk, dk_ref), (dv, dv_ref)):
         assert rel(up.from_zigzag(got, P), want) <= GRAD_REL_FRO, rel(up.from_zigzag(got, P), want)
     lse_r = up.from_zigzag(lse, P).contiguous()
     Dr = torch.empty(2, Hq, S, dtype=torch.float32, device=dev)
     up.ring_bwd_prep(o, do, lse_r, Dr)
     up.core_bwd_dq(desc, q, k, v, do, lse_r, Dr, None, table, dq_ref)
-    up.core_bwd_dkdv(desc, q, k, v, do, lse_r, Dr, None, table, dk_ref, dv_ref)
+    dk_acc = torch.zeros(Hkv, S, Dh, dtype=torch.float32, device=dev)
+    dv_acc = torch.zeros_like(dk_acc)
+    up.core_bwd_dkdv_acc(desc, q, k, v, do, lse_r, Dr, None, table, dk_acc, dv_acc, dk_ref, dv_ref)
     torch.cuda.synchronize()
-    assert rel(up.from_zigzag(dq, P), dq_ref) <= 2e-3, rel(up.from_zigzag(dq, P), dq_ref)
-    for got, want in ((dk, dk_ref), (dv, dv_ref)):
-        assert rel(up.from_zigzag(got, P), want) <= GRAD_REL_FRO, rel(up.from_zigzag(got, P), want)
+    for got, want in ((dq, dq_ref), (dk, dk_ref), (dv, dv_ref)):
+        assert rel(up.from_zigzag(got, P), want) <= 3e-3, rel(up.from_zigzag(got, P), want)
