@@ -29,10 +29,11 @@
 //   A long accumulation into the same TMEM tile drifts low (against an fp64 sum of the same bf16
 //   products: 0.6% after 32K work items, 4.8% after 312K), so launches that keep fp32 sums in
 //   global memory (acc_kv) with flush_items > 0 add the accumulators into them and restart them
-//   every flush_items items (a window): both issuers commit the window's last MMAs to win_full,
-//   each element-wise group reads its accumulator (group 0 dK, group 1 dV) after its last item
-//   of the window, adds it to the global sum and arrives on win_empty, which the first MMA of the
-//   next window waits for.
+//   every flush_items items (a window): each element-wise group, after its last item of the
+//   window, waits for the window's last MMAs (the Q-slot releases of its last two items), adds
+//   its accumulator (group 0 dK, group 1 dV) to the global sum and arrives on win_empty; group 0
+//   hands the next window's first P^T to the issuer (whose dV MMA restarts the accumulators) only
+//   after win_empty completes.  The issuers only restart the accumulation at window starts.
 // Every wait on an mbarrier is bounded (see tc::mbar_wait); registers are split per role with
 // setmaxnreg (launch 168 x 384; control warpgroup 72, element-wise warpgroups 216).
 #include "geom.cuh"
@@ -435,10 +436,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dq_tc(const __grid_con
 // dK, dV
 // ================================================================================================
 // Adds one TMEM accumulator row (this thread's lane, DH fp32 columns, times mul) to its fp32 sum
-// in global memory, 32 columns at a time.  Out of line: it runs once per window, and inlined its
-// registers would burden the element-wise loop around it.
+// in global memory (or stores it there when !add), 32 columns at a time.
 template <int DH>
-__device__ __noinline__ void flush_window(uint32_t acc_addr, float* row, float mul, bool store, bool add) {
+__device__ __forceinline__ void flush_window(uint32_t acc_addr, float* row, float mul, bool store, bool add) {
 #pragma unroll 1
   for (int ch = 0; ch < DH / 32; ++ch) {
     uint32_t v[32];
@@ -477,7 +477,7 @@ struct DkvLayout {
   static constexpr uint32_t DK_COL = 256, DV_COL = 384;
 };
 
-template <int DH>
+template <int DH, bool FLUSH>
 __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_constant__ CUtensorMap tq,
                                                                   const __grid_constant__ CUtensorMap tdo,
                                                                   const __grid_constant__ CUtensorMap tk,
@@ -509,8 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 21);
   uint64_t* dv_tok = bars + 22;   // phase n completes once dV(n) is issued
   uint64_t* dk_tok = bars + 23;   // phase n completes once dK(n) is issued
-  uint64_t* win_full = bars + 24;   // a window's last dK and dV MMAs are complete (both issuers)
-  uint64_t* win_empty = bars + 25;  // both groups have added the window's sums to global memory
+  uint64_t* win_empty = bars + 24;  // both groups have added the window's sums to global memory
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t S = a.S;
@@ -528,8 +527,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
   const int n_heads = dev < a.ndev ? max(0, min(a.hq, (int)blockIdx.x * a.g + a.g) - (int)blockIdx.x * a.g) : 0;
   const int nq = tr.w - tr.x;
   const int n_items = n_heads * nq;
-  // windows flushed into the global fp32 sums: every full window followed by more items
-  const int F = b.acc_kv ? b.flush_items : 0;
+  // windows flushed into the global fp32 sums: every full window followed by more items (FLUSH:
+  // the launch has key tiles with more items than the window; the other instantiation carries
+  // none of the flush's code)
+  const int F = FLUSH ? b.flush_items : 0;
   const int n_win = (F > 0 && n_items > 0) ? (n_items - 1) / F : 0;
   if (a.ring.P) {
     grid_dep_trigger();
@@ -553,7 +554,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
     tc::mbar_init(acc_full, n_items >= 2 ? 2 : 1);  // the last MMAs of each issuer
     tc::mbar_init(dv_tok, 1);
     tc::mbar_init(dk_tok, 1);
-    tc::mbar_init(win_full, 2);
     tc::mbar_init(win_empty, 256);
     for (int i = 0; i < NQ; ++i) {
       tc::mbar_init(&q_full[i], 1);
@@ -623,39 +623,37 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
           tc::mma_commit(&s_full[g]);
         };
         issue_st(g);
-        for (int n = g; ok && n < n_items; n += 2) {
-          const uint32_t ph = (n >> 1) & 1;
-          // the waits that are normally already satisfied come first, so that the issue of dV
-          // follows the element-wise group's P^T arrival as closely as possible
-          ok = tc::mbar_wait(&o_full[g], (n / NO) & 1, abort_flag, a.err, a.wait_ns);
-          if (ok && n > 0) ok = tc::mbar_wait(dv_tok, (n - 1) & 1, abort_flag, a.err, a.wait_ns);  // dV(n-1) issued
-          // the first item of a window restarts the accumulators once the previous window's sums
-          // are out (F is even, so that item is always this issuer's when g == 0)
-          const bool win_start = F > 0 && n > 0 && n % F == 0;
-          if (ok && win_start) ok = tc::mbar_wait(win_empty, ((n / F) - 1) & 1, abort_flag, a.err, a.wait_ns);
-          const bool acc_in = F > 0 ? n % F != 0 : n > 0;
-          if (ok) ok = tc::mbar_wait(&p_full[g], ph, abort_flag, a.err, a.wait_ns);
-          if (!ok) break;
-          tc::fence_after_sync();
-          mma_acc<DH>(tmem + L::DV_COL, r_tm, dOmn, acc_in);  // dV += P^T dO
-          tc::fence_before_sync();
-          tc::mbar_arrive(dv_tok);
-          mma_nt<DH>(r_tm, dV, dO);  // dP^T = V dO^T
-          tc::mma_commit(&dp_full[g]);
-          tc::mma_commit(&o_empty[g]);
-          if (n > 0) ok = tc::mbar_wait(dk_tok, (n - 1) & 1, abort_flag, a.err, a.wait_ns);  // dK(n-1) issued
-          if (ok) ok = tc::mbar_wait(&ds_full[g], ph, abort_flag, a.err, a.wait_ns);
-          if (!ok) break;
-          tc::fence_after_sync();
-          mma_acc<DH>(tmem + L::DK_COL, r_tm, tc::sdesc_add(dQmn, (n % NQ) * L::TB), acc_in);  // dK += dS^T Q
-          tc::fence_before_sync();
-          tc::mbar_arrive(dk_tok);
-          tc::mma_commit(&q_empty[n % NQ]);
-          // this issuer's last item of a flushed window (F - 2 + g within it): its MMAs complete
-          // the window's sums together with the other issuer's
-          if (F > 0 && n % F == F - 2 + g && n / F < n_win) tc::mma_commit(win_full);
-          if (n + 2 >= n_items) tc::mma_commit(acc_full);  // this issuer's last item
-          if (n + 2 < n_items) issue_st(n + 2);
+        // windows of F items (FLUSH), each restarting the accumulators: the element-wise groups
+        // hand the first P^T of a window over only once the previous window's sums are out
+        for (int w0 = 0; ok && w0 < n_items; w0 += FLUSH ? F : n_items) {
+          const int w1 = FLUSH ? min(n_items, w0 + F) : n_items;
+          for (int n = w0 + g; ok && n < w1; n += 2) {
+            const uint32_t ph = (n >> 1) & 1;
+            // the waits that are normally already satisfied come first, so that the issue of dV
+            // follows the element-wise group's P^T arrival as closely as possible
+            ok = tc::mbar_wait(&o_full[g], (n / NO) & 1, abort_flag, a.err, a.wait_ns);
+            if (ok && n > 0) ok = tc::mbar_wait(dv_tok, (n - 1) & 1, abort_flag, a.err, a.wait_ns);  // dV(n-1) issued
+            const bool acc_in = n > w0;  // the window's first item restarts the accumulators
+            if (ok) ok = tc::mbar_wait(&p_full[g], ph, abort_flag, a.err, a.wait_ns);
+            if (!ok) break;
+            tc::fence_after_sync();
+            mma_acc<DH>(tmem + L::DV_COL, r_tm, dOmn, acc_in);  // dV += P^T dO
+            tc::fence_before_sync();
+            tc::mbar_arrive(dv_tok);
+            mma_nt<DH>(r_tm, dV, dO);  // dP^T = V dO^T
+            tc::mma_commit(&dp_full[g]);
+            tc::mma_commit(&o_empty[g]);
+            if (n > 0) ok = tc::mbar_wait(dk_tok, (n - 1) & 1, abort_flag, a.err, a.wait_ns);  // dK(n-1) issued
+            if (ok) ok = tc::mbar_wait(&ds_full[g], ph, abort_flag, a.err, a.wait_ns);
+            if (!ok) break;
+            tc::fence_after_sync();
+            mma_acc<DH>(tmem + L::DK_COL, r_tm, tc::sdesc_add(dQmn, (n % NQ) * L::TB), acc_in);  // dK += dS^T Q
+            tc::fence_before_sync();
+            tc::mbar_arrive(dk_tok);
+            tc::mma_commit(&q_empty[n % NQ]);
+            if (n + 2 >= n_items) tc::mma_commit(acc_full);  // this issuer's last item
+            if (n + 2 < n_items) issue_st(n + 2);
+          }
         }
       }
       __syncwarp();
@@ -695,91 +693,107 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
       if (turn < n_give) tc::named_bar_arrive(kPing + 1 - grp, 256);
       ++turn;
     };
-    for (int n = grp; n < n_items; n += 2) {
-      const int qi = tr.x + n % nq;
-      const bool partial = qi < tr.y || qi >= tr.z || (ragged && (qi == nt - 1 || jt == nt - 1));
-      const int cyc = (n >> 1) & 1;
-      int lo = 0, hi = 127;
-      if (partial) {
-        const int64_t col0 = (int64_t)qi * kTile;
-        lo = (int)max((int64_t)-1, min(vis_lo - col0, (int64_t)128));
-        hi = (int)max((int64_t)-1, min(vis_hi - col0, (int64_t)128));
-      }
-      // stage the item's 128 (-lse2, -D) pairs in shared memory, then start the next item's loads
-      tc::named_bar_sync(1 + grp, 128);  // the previous item's readers are done
-      nvec[r] = vec_next.x;
-      nvec[128 + r] = vec_next.y;
-      tc::named_bar_sync(1 + grp, 128);
-      if (n + 2 < n_items) vec_next = load_vec(n + 2);
-      take_turn();
-      ok = tc::mbar_wait(&s_full[grp], cyc, abort_flag, a.err, a.wait_ns);
-      if (!ok) break;
-      tc::fence_after_sync();
-      // P^T = exp2(s c - lse2) kept in fp32 in place of the scores (for dS^T); its bf16 copy goes
-      // to TMEM as the A operand of dV += P^T dO
-      uint32_t sa[64], sb[64];
-      {
-        const float2 cc = make_float2(c, c);
-        // two halves of 64 columns, the second loading while the first is computed (as in dQ)
-        auto half = [&](uint32_t (&sv)[64], int hf) {
-          if (partial) {  // masked scores -> -inf (exp2 -> 0), only on partial tiles
-#pragma unroll
-            for (int i = 0; i < 64; ++i)
-              if (hf * 64 + i < lo || hf * 64 + i > hi) sv[i] = 0xff800000u;
-          }
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            const float4 l4 = *reinterpret_cast<const float4*>(nvec + hf * 64 + 2 * i);
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int kk = 2 * (i + u);
-              const float2 arg = __ffma2_rn(make_float2(__uint_as_float(sv[kk]), __uint_as_float(sv[kk + 1])), cc,
-                                            u ? make_float2(l4.z, l4.w) : make_float2(l4.x, l4.y));
-              sv[kk] = __float_as_uint(fast_exp2(arg.x));
-              sv[kk + 1] = __float_as_uint(fast_exp2(arg.y));
+    for (int n = grp; n < n_items;) {
+      // this group's items up to the end of the current window (all of them when no flush
+      // follows), so that the per-item loop carries none of the flush
+      const bool flush = F > 0 && n / F < n_win;
+      const int w_end = flush ? (n / F + 1) * F : n_items;
+      for (; n < w_end; n += 2) {
+        const int qi = tr.x + n % nq;
+        const bool partial = qi < tr.y || qi >= tr.z || (ragged && (qi == nt - 1 || jt == nt - 1));
+        const int cyc = (n >> 1) & 1;
+        int lo = 0, hi = 127;
+        if (partial) {
+          const int64_t col0 = (int64_t)qi * kTile;
+          lo = (int)max((int64_t)-1, min(vis_lo - col0, (int64_t)128));
+          hi = (int)max((int64_t)-1, min(vis_hi - col0, (int64_t)128));
+        }
+        // stage the item's 128 (-lse2, -D) pairs in shared memory, then start the next item's loads
+        tc::named_bar_sync(1 + grp, 128);  // the previous item's readers are done
+        nvec[r] = vec_next.x;
+        nvec[128 + r] = vec_next.y;
+        tc::named_bar_sync(1 + grp, 128);
+        if (n + 2 < n_items) vec_next = load_vec(n + 2);
+        take_turn();
+        ok = tc::mbar_wait(&s_full[grp], cyc, abort_flag, a.err, a.wait_ns);
+        if (!ok) break;
+        tc::fence_after_sync();
+        // P^T = exp2(s c - lse2) kept in fp32 in place of the scores (for dS^T); its bf16 copy goes
+        // to TMEM as the A operand of dV += P^T dO
+        uint32_t sa[64], sb[64];
+        {
+          const float2 cc = make_float2(c, c);
+          // two halves of 64 columns, the second loading while the first is computed (as in dQ)
+          auto half = [&](uint32_t (&sv)[64], int hf) {
+            if (partial) {  // masked scores -> -inf (exp2 -> 0), only on partial tiles
+  #pragma unroll
+              for (int i = 0; i < 64; ++i)
+                if (hf * 64 + i < lo || hf * 64 + i > hi) sv[i] = 0xff800000u;
             }
-          }
-        };
-        tmem_ld64(r_addr, sa);
-        tmem_ld_wait_for(sa);
-        tmem_ld64(r_addr + 64, sb);
-        half(sa, 0);
-        tmem_ld_wait_for(sb);
-        half(sb, 1);
+  #pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              const float4 l4 = *reinterpret_cast<const float4*>(nvec + hf * 64 + 2 * i);
+  #pragma unroll
+              for (int u = 0; u < 2; ++u) {
+                const int kk = 2 * (i + u);
+                const float2 arg = __ffma2_rn(make_float2(__uint_as_float(sv[kk]), __uint_as_float(sv[kk + 1])), cc,
+                                              u ? make_float2(l4.z, l4.w) : make_float2(l4.x, l4.y));
+                sv[kk] = __float_as_uint(fast_exp2(arg.x));
+                sv[kk + 1] = __float_as_uint(fast_exp2(arg.y));
+              }
+            }
+          };
+          tmem_ld64(r_addr, sa);
+          tmem_ld_wait_for(sa);
+          tmem_ld64(r_addr + 64, sb);
+          half(sa, 0);
+          tmem_ld_wait_for(sb);
+          half(sb, 1);
+        }
+  #pragma unroll
+        for (int q = 0; q < 4; ++q) {  // bf16 pairs of columns [32q, 32q + 32) -> TMEM columns [16q, 16q + 16)
+          const uint32_t* pp = q < 2 ? &sa[32 * q] : &sb[32 * (q - 2)];
+          uint32_t o[16];
+  #pragma unroll
+          for (int i = 0; i < 16; ++i) o[i] = tc::pack_bf16x2(__uint_as_float(pp[2 * i]), __uint_as_float(pp[2 * i + 1]));
+          tc::tmem_st16(r_addr + 16 * q, o);
+        }
+        tc::tmem_st_wait();
+        tc::fence_before_sync();
+        tc::mbar_arrive(&p_full[grp]);
+        give_turn();
+        take_turn();
+        ok = tc::mbar_wait(&dp_full[grp], cyc, abort_flag, a.err, a.wait_ns);
+        if (!ok) break;
+        tc::fence_after_sync();
+        ds_pass_f32(r_addr, sa, sb, [&](int k) { return *reinterpret_cast<const float2*>(nvec + 128 + k); });
+        tc::fence_before_sync();
+        tc::mbar_arrive(&ds_full[grp]);
+        give_turn();
       }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {  // bf16 pairs of columns [32q, 32q + 32) -> TMEM columns [16q, 16q + 16)
-        const uint32_t* pp = q < 2 ? &sa[32 * q] : &sb[32 * (q - 2)];
-        uint32_t o[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) o[i] = tc::pack_bf16x2(__uint_as_float(pp[2 * i]), __uint_as_float(pp[2 * i + 1]));
-        tc::tmem_st16(r_addr + 16 * q, o);
-      }
-      tc::tmem_st_wait();
-      tc::fence_before_sync();
-      tc::mbar_arrive(&p_full[grp]);
-      give_turn();
-      take_turn();
-      ok = tc::mbar_wait(&dp_full[grp], cyc, abort_flag, a.err, a.wait_ns);
       if (!ok) break;
-      tc::fence_after_sync();
-      ds_pass_f32(r_addr, sa, sb, [&](int k) { return *reinterpret_cast<const float2*>(nvec + 128 + k); });
-      tc::fence_before_sync();
-      tc::mbar_arrive(&ds_full[grp]);
-      give_turn();
-      if (F > 0 && n % F == F - 2 + grp && n / F < n_win) {
-        // this group's last item of a flushed window: add its accumulator (group 0 dK, group 1 dV)
-        // to the global fp32 sum, 32 columns at a time (rare: once per window, so the loads are
-        // not held ahead in registers the loop needs)
+      if (flush) {
+        // the window's last items are done: add this group's accumulator (group 0 dK, group 1 dV)
+        // to the global fp32 sum, 32 columns at a time
+        const int w = w_end / F - 1;
         float* wrow = (grp == 0 ? b.dk_acc : b.dv_acc) + ((int64_t)kvh * S + (k_ok ? krow : 0)) * DH;
         if (a.ring.P) grid_dep_wait();  // the previous ring step's sums are complete and visible
-        ok = tc::mbar_wait(win_full, (n / F) & 1, abort_flag, a.err, a.wait_ns);
+        // the window's last two items (one per issuer) are complete once their dK MMAs have
+        // released their Q slots (each issuer's commit covers its earlier MMAs; no later phase of
+        // these barriers can complete before this group hands over its next item)
+        const int m0 = w_end - 2, m1 = w_end - 1;
+        ok = tc::mbar_wait(&q_empty[m0 % NQ], (m0 / NQ) & 1, abort_flag, a.err, a.wait_ns);
+        if (ok) ok = tc::mbar_wait(&q_empty[m1 % NQ], (m1 / NQ) & 1, abort_flag, a.err, a.wait_ns);
         tc::fence_after_sync();
         // the first ring step starts the sums (nothing to add to), later flushes add to them
         flush_window<DH>(lane_addr + (grp == 0 ? L::DK_COL : L::DV_COL), wrow, grp == 0 ? a.scale : 1.f, ok && k_ok,
-                         !(a.acc_first && n / F == 0));
+                         !(a.acc_first && w == 0));
         tc::fence_before_sync();
-        tc::mbar_arrive(win_empty);  // the next window's first MMAs may overwrite the accumulators
+        tc::mbar_arrive(win_empty);
+        // group 0 hands the next window's first P^T (whose dV MMA restarts the accumulators) over
+        // only once both groups' sums are out
+        if (grp == 0 && ok) ok = tc::mbar_wait(win_empty, w & 1, abort_flag, a.err, a.wait_ns);
+        tc::fence_after_sync();
         if (!ok) break;
       }
     }
@@ -903,8 +917,12 @@ cudaError_t run_dkdv(const AttnBwdArgs& b, cudaStream_t st) {
   const int nt = (int)ceil_div(b.f.S, kTile);
   AttnArgs f = b.f;
   fill_planes(f);
-  return launch(k_attn_bwd_dkdv_tc<DH>, DkvLayout<DH>::BYTES, dim3((unsigned)f.hkv, (unsigned)(f.kv_count * nt)), tq, tdo,
-                tk, tv, b, st);
+  // a key tile has at most min(g, hq) x nt work items (the launch's query heads of its KV head x
+  // the query tiles)
+  const bool flush = b.acc_kv && b.flush_items > 0 && (int64_t)std::min(f.g, f.hq) * nt > b.flush_items;
+  const dim3 grid((unsigned)f.hkv, (unsigned)(f.kv_count * nt));
+  return flush ? launch(k_attn_bwd_dkdv_tc<DH, true>, DkvLayout<DH>::BYTES, grid, tq, tdo, tk, tv, b, st)
+               : launch(k_attn_bwd_dkdv_tc<DH, false>, DkvLayout<DH>::BYTES, grid, tq, tdo, tk, tv, b, st);
 }
 
 }  // namespace

@@ -218,6 +218,34 @@ def test_ring_backward_steps_match_causal_gradients(case):
         assert rel_fro(g, want) <= GRAD_REL_FRO, rel_fro(g, want)
 
 
+@pytest.mark.parametrize("window", [2, 4])
+@pytest.mark.parametrize("case", [RING_CASES[1], RING_CASES[2], RING_CASES[3]], ids=ids)
+def test_ring_backward_with_flushed_dkdv_windows(case, window):
+    # the ring steps' dK / dV kernels add their accumulators to the travelling fp32 sums every
+    # `window` work items (the first step stores its first window's sums instead of adding)
+    P, C, Hq, Hkv, Dh, lengths = case
+    arrs, seg, seg_t, (qs, ks, vs, dos) = ring_setup(case)
+    ring = up.Ring(up.make_ring_desc(P, C, Hq, Hkv, Dh), seg_t)
+    o, lse = ring.forward(qs, ks, vs)
+    ref = ring.backward(qs, ks, vs, o, lse, dos)
+    try:
+        up.set_dkdv_window(window)
+        got = ring.backward(qs, ks, vs, o, lse, dos)
+        got1 = ring.backward(qs, ks, vs, o, lse, dos, per_step=True)
+    finally:
+        up.set_dkdv_window(0)
+    torch.cuda.synchronize()
+    assert up.device_status(ring.tables) == 0
+    assert all(torch.equal(a, b) for a, b in zip(got, got1))
+    assert torch.equal(got[0], ref[0])                        # dQ does not change
+    Q, K, V, dO, _, _ = oracle_attention(arrs, seg, Dh)
+    _, dK, dV = orc.attention_backward(Q, K, V, dO, seg, True, orc.default_scale(Dh))
+    for g, r, want in ((got[1], ref[1], dK), (got[2], ref[2], dV)):
+        g64 = to_f64(up.from_zigzag(g, P))
+        assert rel_fro(g64, want) <= GRAD_REL_FRO, rel_fro(g64, want)
+        assert rel_fro(g64, to_f64(up.from_zigzag(r, P))) <= 2e-3
+
+
 def test_ring_step_32k_against_the_direct_kernel():
     """The 32K-token chunk of 8 heads (Llama-3.1-8B shape, 2 KV heads) as a ring of 4: O and lse
     agree with the direct causal kernel's to the rounding of the merge, on every row."""

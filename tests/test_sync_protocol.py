@@ -151,9 +151,15 @@ def test_random_ranges_never_deadlock(kind, dq_turns):
 
 
 # dK/dV: one MMA issuer per element-wise group; the shared dK / dV accumulations stay in item
-# order through token barriers; the element-wise groups take turns phase by phase.
-def run_dkdv_pp(N, NQ=3, NO=2):
+# order through token barriers; the element-wise groups take turns phase by phase.  With a window
+# F, each group adds its accumulator to the global sums after its last item of every window that
+# more items follow (once the Q-slot releases of the window's last two items show their MMAs
+# complete), and group 0 hands the next window's first P^T over only after both groups have done
+# so; the model also checks that no window's first dV MMA (which restarts the accumulators) is
+# issued before both flushes of the previous window.
+def run_dkdv_pp(N, NQ=3, NO=2, F=None, rng=None):
     ev = set()
+    n_win = (N - 1) // F if F and N > 0 else 0
     Na, Nb = (N + 1) // 2, N // 2
     n_pp = 2 * min(Na, Nb)
     give = {0: 0, 1: 0}
@@ -174,6 +180,9 @@ def run_dkdv_pp(N, NQ=3, NO=2):
             yield lambda n=n: ("O", n) in ev
             if n > 0:
                 yield lambda n=n: ("dv_tok", n - 1) in ev
+            if F and n % F == 0 and n > 0:   # restarts the accumulators
+                w = n // F - 1
+                assert ("flushed", 0, w) in ev and ("flushed", 1, w) in ev, (N, F, n)
             ev.add(("dv_tok", n))
             ev.add(("dP", n)); ev.add(("o_empty", n))
             yield lambda n=n: ("dS", n) in ev
@@ -203,8 +212,28 @@ def run_dkdv_pp(N, NQ=3, NO=2):
             yield from take()
             yield lambda n=n: ("dP", n) in ev
             ev.add(("dS", n)); giv()
+            if F and n % F == F - 2 + g and n // F < n_win:
+                w = n // F
+                m0, m1 = (w + 1) * F - 2, (w + 1) * F - 1
+                yield lambda m0=m0, m1=m1: ("q_empty", m0) in ev and ("q_empty", m1) in ev
+                # the sums read are complete: every MMA of the window has been issued
+                assert all(("dk_tok", m) in ev for m in range(w * F, (w + 1) * F)), (N, F, w)
+                ev.add(("flushed", g, w))
+                if g == 0:
+                    yield lambda w=w: ("flushed", 1, w) in ev
     actors = [producer(), issuer(0), issuer(1), ew(0), ew(1)]
     waits = [None] * len(actors); done = [False] * len(actors)
+    if rng is not None:   # random interleaving: one step of a random runnable actor at a time
+        while not all(done):
+            ready = [i for i in range(len(actors)) if not done[i] and (waits[i] is None or waits[i]())]
+            if not ready:
+                return False
+            i = rng.choice(ready)
+            try:
+                waits[i] = next(actors[i])
+            except StopIteration:
+                done[i] = True
+        return True
     while not all(done):
         progress = False
         for i, a in enumerate(actors):
@@ -221,3 +250,11 @@ def run_dkdv_pp(N, NQ=3, NO=2):
 
 def test_dkdv_two_issuers_never_deadlock():
     assert all(run_dkdv_pp(n) for n in range(0, 40))
+
+
+@pytest.mark.parametrize("F", [2, 4, 6, 10])
+def test_dkdv_flushed_windows_never_deadlock(F):
+    assert all(run_dkdv_pp(n, F=F) for n in range(0, 40))
+    rng = random.Random(F)
+    for _ in range(300):
+        assert run_dkdv_pp(rng.randrange(0, 30), F=F, rng=rng)
