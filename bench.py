@@ -58,6 +58,9 @@ def parse():
                          "launch per step) on this GPU, timed against the direct kernel")
     ap.add_argument("--ring-p", type=int, default=4)
     ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--dkdv-window", type=int, default=0,
+                    help="work items per dK/dV tensor-memory accumulation before it is added to fp32 sums "
+                         "(upipe_attn_set_dkdv_window; 0: the library default)")
     return ap.parse_args()
 
 
@@ -437,6 +440,8 @@ def main():
     import long_context_attention_upipe_gb300 as up
     import upipe_inputs as ui
 
+    up.set_dkdv_window(args.dkdv_window)
+    window = args.dkdv_window or up.DKDV_WINDOW_DEFAULT
     w = ui.workload(args.workload)
     if args.hpc is None:
         args.hpc = max(w.hpc_sweep)
@@ -545,7 +550,7 @@ def main():
         up.core_recompute(cdesc, q, k, v, do, lse_c, seg_t, table, o, Dt, stream)
         # dK / dV as the layer launches it: into fp32 sums (flushed in windows) for a partial KV
         # group or once a key tile's work items exceed the window, else straight to bf16
-        if hpc < g or min(hpc, g) * -(-S // 128) > up.DKDV_WINDOW_DEFAULT:
+        if hpc < g or min(hpc, g) * -(-S // 128) > window:
             dk_acc = torch.zeros(k.shape, dtype=torch.float32, device=dev)
             dv_acc = torch.zeros(v.shape, dtype=torch.float32, device=dev)
             dkdv = lambda: up.core_bwd_dkdv_acc(cdesc, q, k, v, do, lse_c, Dt, seg_t, table, dk_acc, dv_acc,
