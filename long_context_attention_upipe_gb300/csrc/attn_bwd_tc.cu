@@ -696,8 +696,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
     for (int n = grp; n < n_items;) {
       // this group's items up to the end of the current window (all of them when no flush
       // follows), so that the per-item loop carries none of the flush
-      const bool flush = F > 0 && n / F < n_win;
-      const int w_end = flush ? (n / F + 1) * F : n_items;
+      const int Fd = FLUSH ? F : 1;  // F as a divisor (the other instantiation never divides)
+      const bool flush = F > 0 && n / Fd < n_win;
+      const int w_end = flush ? (n / Fd + 1) * F : n_items;
       for (; n < w_end; n += 2) {
         const int qi = tr.x + n % nq;
         const bool partial = qi < tr.y || qi >= tr.z || (ragged && (qi == nt - 1 || jt == nt - 1));
@@ -726,14 +727,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
           // two halves of 64 columns, the second loading while the first is computed (as in dQ)
           auto half = [&](uint32_t (&sv)[64], int hf) {
             if (partial) {  // masked scores -> -inf (exp2 -> 0), only on partial tiles
-  #pragma unroll
+#pragma unroll
               for (int i = 0; i < 64; ++i)
                 if (hf * 64 + i < lo || hf * 64 + i > hi) sv[i] = 0xff800000u;
             }
-  #pragma unroll
+#pragma unroll
             for (int i = 0; i < 32; i += 2) {
               const float4 l4 = *reinterpret_cast<const float4*>(nvec + hf * 64 + 2 * i);
-  #pragma unroll
+#pragma unroll
               for (int u = 0; u < 2; ++u) {
                 const int kk = 2 * (i + u);
                 const float2 arg = __ffma2_rn(make_float2(__uint_as_float(sv[kk]), __uint_as_float(sv[kk + 1])), cc,
@@ -750,11 +751,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
           tmem_ld_wait_for(sb);
           half(sb, 1);
         }
-  #pragma unroll
+#pragma unroll
         for (int q = 0; q < 4; ++q) {  // bf16 pairs of columns [32q, 32q + 32) -> TMEM columns [16q, 16q + 16)
           const uint32_t* pp = q < 2 ? &sa[32 * q] : &sb[32 * (q - 2)];
           uint32_t o[16];
-  #pragma unroll
+#pragma unroll
           for (int i = 0; i < 16; ++i) o[i] = tc::pack_bf16x2(__uint_as_float(pp[2 * i]), __uint_as_float(pp[2 * i + 1]));
           tc::tmem_st16(r_addr + 16 * q, o);
         }
@@ -775,7 +776,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_bwd_dkdv_tc(const __grid_c
       if (flush) {
         // the window's last items are done: add this group's accumulator (group 0 dK, group 1 dV)
         // to the global fp32 sum, 32 columns at a time
-        const int w = w_end / F - 1;
+        const int w = w_end / Fd - 1;
         float* wrow = (grp == 0 ? b.dk_acc : b.dv_acc) + ((int64_t)kvh * S + (k_ok ? krow : 0)) * DH;
         if (a.ring.P) grid_dep_wait();  // the previous ring step's sums are complete and visible
         // the window's last two items (one per issuer) are complete once their dK MMAs have
