@@ -84,14 +84,6 @@ __device__ __forceinline__ void box_coords(const TcOpDev& o, int64_t mn, int64_t
   }
 }
 
-__device__ __forceinline__ void load_box(uint8_t* dst, const CUtensorMap* map, const TcOpDev& o, uint64_t* bar,
-                                         int64_t mn, int64_t k) {
-  int c0, c1, c2;
-  box_coords(o, mn, k, c0, c1, c2);
-  if (o.rank == 3) tc::tma_load_3d(dst, map, bar, c0, c1, c2);
-  else tc::tma_load_2d(dst, map, bar, c0, c1);
-}
-
 // A box into this CTA's shared memory, counted on the even CTA's barrier (shared::cluster address).
 __device__ __forceinline__ void load_box_pair(uint8_t* dst, const CUtensorMap* map, const TcOpDev& o,
                                               uint32_t bar_cluster, int64_t mn, int64_t k) {
